@@ -1,0 +1,238 @@
+/*
+ * kvattn -- single-query (n_q = 1) split-KV decode attention for GB300 (sm_103a).
+ *
+ * C ABI: plain pointers and sizes only.  "device" pointers are CUDA device memory of
+ * the current device, "host" pointers are ordinary (or pinned, where stated) host
+ * memory.  Streams are passed as `void*` holding a cudaStream_t (NULL = the legacy
+ * default stream).  The caller owns every buffer; the library allocates no device
+ * memory on any decode path.  Every call validates its arguments on the host before
+ * it touches CUDA and returns a kvattn_status; it never aborts and never prints.
+ * Device calls are asynchronous on the given stream(s).
+ *
+ * Sources (web pages, cited by title and section):
+ *  [RKV]  "Rolling-KV -- overflow throughput evaluations (consolidated)",
+ *         opencoti-llamafile docs/evaluations/rolling_kv.md
+ *  [KVN]  "KVARN KV Performance optimizations", beellama.cpp issue #140
+ *
+ * Attention definition (what every decode entry point computes, up to floating-point
+ * reduction order): for sequence s and query head h, G = n_head / n_head_kv,
+ * g = floor(h / G), over the valid cells c of the sequence
+ *     x_c = scale * q[s][h] . K[c][g],   O[s][h] = sum_c softmax(x)_c V[c][g],
+ *     LSE[s][h] = ln sum_c exp(x_c)      (-inf and O = 0 when no cell is valid).
+ * Split-KV: cells are cut into splits; each split yields a partial (O_p, LSE_p) and
+ * the partials are merged with weights exp(LSE_p - max LSE) ([RKV] section 3, the
+ * decode-emitted LSE channel; [KVN] item 9, partial windows keep max, numerator and
+ * denominator and are merged afterwards).
+ *
+ * Cache layouts
+ *  f16  : K, V  half  [n_cells][n_head_kv][head_dim]          (cell-major rows)
+ *  Q8_0 : K, V  int8  [n_cells][n_head_kv][head_dim] and scales
+ *         half [n_cells][n_head_kv][head_dim / 32]; value = scale * int8, one scale
+ *         per 32 consecutive head_dim elements (structure-of-arrays planes, chosen so
+ *         that every row starts on a 16-byte boundary).
+ *  q    : half  [n_seq][n_head][head_dim];  out: float [n_seq][n_head][head_dim];
+ *  lse  : float [n_seq][n_head] (natural log).
+ */
+#ifndef KVATTN_H
+#define KVATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    KVATTN_OK = 0,
+    KVATTN_ERR_INVALID_ARG = -1,   /* null pointer, bad size, misaligned buffer */
+    KVATTN_ERR_UNSUPPORTED = -2,   /* valid but not built: head_dim, group size, split */
+    KVATTN_ERR_WORKSPACE = -3,     /* workspace smaller than the *_workspace_bytes query */
+    KVATTN_ERR_CAPACITY = -4,      /* a cell beyond the cache, or a plan row too long */
+    KVATTN_ERR_CUDA = -5,          /* a CUDA call or launch failed */
+    KVATTN_ERR_TIMEOUT = -6        /* a bounded host wait ran out */
+} kvattn_status;
+
+typedef enum { KVATTN_KV_F16 = 0, KVATTN_KV_Q8_0 = 1 } kvattn_kv_type;
+
+/* Sticky device-side status bits, read with kvattn_workspace_status. */
+#define KVATTN_DEVICE_WAIT_TIMEOUT 1u   /* a bounded pipeline wait gave up; results invalid */
+#define KVATTN_DEVICE_BAD_PLAN_ENTRY 2u /* a plan entry outside [-1, n_cells) was masked */
+
+/* Human-readable name of a kvattn_status (static storage, never NULL). */
+const char* kvattn_status_string(int status);
+
+/* ABI version of this header: (major << 16) | minor. */
+int kvattn_version(void);
+
+/*
+ * kvattn_build_cell_plan -- host.  The compact indirect cell plan of [KVN] item 4
+ * ("physical record-group-safe compact plans") with the duplicate handling of item 3
+ * and the encoded-index rule of item 5.
+ *
+ *  cells    host int64 [offsets[n_seq]]: the concatenated per-sequence lists of encoded
+ *           cell indices; low 32 bits (unsigned) = physical cell, high 32 bits = a
+ *           stage-slot tag that the read plan ignores.  Order and duplicates are free.
+ *  offsets  host int64 [n_seq + 1], non-decreasing, offsets[0] = 0.
+ *  capacity_cells  physical cells in the cache (> 0).
+ *  plan     host int32 [n_seq][plan_stride] output, or NULL to only compute seq_lens.
+ *  seq_lens host int32 [n_seq] output: 128 x (number of distinct records selected).
+ *
+ * Each sequence's row is its selected physical 128-cell records in ascending order,
+ * one complete 128-entry segment per record, entry j = record*128 + j when that cell
+ * was selected and -1 (a hole) otherwise; the rest of the row is -1.
+ * Errors: INVALID_ARG (null cells/offsets/seq_lens with work to do, bad offsets,
+ * n_seq < 0, capacity < 1, plan_stride < 0); CAPACITY (a physical cell >= capacity,
+ * or a row longer than plan_stride).  On error the outputs are unspecified.
+ */
+int kvattn_build_cell_plan(const int64_t* cells, const int64_t* offsets, int n_seq,
+                           int64_t capacity_cells, int32_t* plan, int64_t plan_stride,
+                           int32_t* seq_lens);
+
+/*
+ * kvattn_build_descriptors -- device.  Per-split descriptors of a cell plan ([KVN]
+ * item 5, "descriptor setup"; item 6, "fully masked split skipping").
+ *
+ *  cell_plan  device int32 [n_seq][plan_stride];  seq_lens device int32 [n_seq].
+ *  desc       device int32 [n_seq][ceil(max_len / split)][4] output:
+ *             {n_valid, lo, hi, flags} over plan entries [p*split, min((p+1)*split, L))
+ *             with L = min(seq_lens[s], max_len, plan_stride); an entry e is valid when
+ *             0 <= e < n_cells; lo/hi = smallest/largest valid cell (-1 if none);
+ *             flags: 1 = no valid entry, 2 = linear (e - i constant over valid entries),
+ *             4 = an entry outside [-1, n_cells) was seen, 8 = split starts at/after L.
+ * Errors: INVALID_ARG (null pointers, n_seq < 0, split < 1, max_len < 0, n_cells < 1,
+ * plan_stride < 1, more than 65535 sequences); CUDA.
+ */
+int kvattn_build_descriptors(const int32_t* cell_plan, int64_t plan_stride,
+                             const int32_t* seq_lens, int n_seq, int64_t max_len, int split,
+                             int64_t n_cells, int32_t* desc, void* stream);
+
+/* Bytes of workspace kvattn_decode needs (partials, descriptors, status word). */
+size_t kvattn_decode_workspace_bytes(int n_seq, int n_head, int head_dim, int64_t max_len,
+                                     int split);
+
+/*
+ * kvattn_decode -- device.  Split-KV decode attention ([RKV] sections 1 and 3; [KVN]
+ * items 2, 4, 6 and 9): per (sequence, KV head, split) one CTA streams the split's
+ * K/V rows through shared memory once for all G query heads of that KV head, and
+ * emits a partial (O_p, LSE_p); a second kernel merges the partials.
+ *
+ *  q        device half [n_seq][n_head][head_dim].
+ *  k_cache, v_cache  device, 16-byte aligned.  f16: half rows.  Q8_0: int8 rows.
+ *  k_scales, v_scales  device half scale planes for Q8_0 (8-byte aligned for
+ *           head_dim 128, 16-byte for 256); must be NULL for f16.
+ *  kv_type  a kvattn_kv_type.
+ *  n_cells  rows per sequence when cell_plan is NULL (sequence s reads rows
+ *           [s*n_cells, s*n_cells + seq_len)), or rows of the unified cache otherwise.
+ *  cell_plan  NULL, or device int32 [n_seq][plan_stride]: sequence s reads the cells
+ *           cell_plan[s][0 .. seq_len) with -1 holes (see kvattn_build_cell_plan).
+ *           Entries outside [-1, n_cells) are masked and flagged in the workspace.
+ *  seq_lens device int32 [n_seq]; each is clamped to [0, max_len] and to n_cells (no
+ *           plan) or plan_stride (plan).
+ *  max_len  host bound on the lengths; sizes the grid and the workspace.
+ *  n_head, n_head_kv  n_head % n_head_kv == 0 and n_head / n_head_kv <= 8.
+ *  head_dim 128 or 256.   split  cells per partial, a positive multiple of 32.
+ *  scale    softmax scale applied to q . k in fp32 (1/sqrt(head_dim) is usual).
+ *  out, lse device float outputs.   ws/ws_bytes  device workspace of at least
+ *           kvattn_decode_workspace_bytes(...) bytes, 256-byte aligned, zeroed once
+ *           after allocation (its first word is the sticky status word).
+ *  stream   cudaStream_t.
+ * Errors: INVALID_ARG, UNSUPPORTED, WORKSPACE (before any launch); CUDA.
+ */
+int kvattn_decode(const void* q, const void* k_cache, const void* v_cache,
+                  const void* k_scales, const void* v_scales, int kv_type, int64_t n_cells,
+                  const int32_t* cell_plan, int64_t plan_stride, const int32_t* seq_lens,
+                  int n_seq, int64_t max_len, int n_head, int n_head_kv, int head_dim,
+                  int split, float scale, float* out, float* lse, void* ws, size_t ws_bytes,
+                  void* stream);
+
+/*
+ * kvattn_decode_partials -- device.  The split step of kvattn_decode alone: the same
+ * arguments and checks, but every split's normalised partial and its LSE are written to
+ * caller buffers instead of being merged, so that they can be merged with partials from
+ * elsewhere (another device, a host tail) by kvattn_merge.
+ *  part_o    device float [n_seq][ceil(max_len / split)][n_head][head_dim], 16-byte aligned.
+ *  part_lse  device float [n_seq][ceil(max_len / split)][n_head].
+ * Splits past a sequence's length, and splits with no valid cell, are written as
+ * O_p = 0, LSE_p = -inf.  ws: as for kvattn_decode (status word and descriptors).
+ * Errors: as kvattn_decode.
+ */
+int kvattn_decode_partials(const void* q, const void* k_cache, const void* v_cache,
+                           const void* k_scales, const void* v_scales, int kv_type,
+                           int64_t n_cells, const int32_t* cell_plan, int64_t plan_stride,
+                           const int32_t* seq_lens, int n_seq, int64_t max_len, int n_head,
+                           int n_head_kv, int head_dim, int split, float scale, float* part_o,
+                           float* part_lse, void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * kvattn_merge -- device.  LSE-weighted merge of partial attention results ([KVN]
+ * item 9; [RKV] section 3):  M = max_p LSE_p, w_p = exp(LSE_p - M),
+ * out = sum_p w_p O_p / sum_p w_p, lse = M + ln sum_p w_p.  Parts with LSE = -inf hold
+ * no cells and are skipped without reading their O; if every part is -inf the row is
+ * O = 0, LSE = -inf.
+ *  partials device float [n_parts][n_rows][head_dim];  lses device float [n_parts][n_rows].
+ *  out      device float [n_rows][head_dim];  lse device float [n_rows].
+ *  head_dim a positive multiple of 4, at most 1024.  n_parts >= 0.  All 16-byte aligned.
+ * Errors: INVALID_ARG; CUDA.
+ */
+int kvattn_merge(const float* partials, const float* lses, int n_parts, int n_rows, int head_dim,
+                 float* out, float* lse, void* stream);
+
+/*
+ * Window + host tail ([RKV] sections 1 and 5c: "POSITION_WINDOW keeps a resident window of
+ * recent cells and streams the older tail from host RAM every decode step"; the window is
+ * attended on the device and the tail streamed once, one tile ahead, and the partials are
+ * merged).  One sequence, f16 cache.
+ *
+ * A tail context owns only CUDA events (no memory).
+ */
+typedef struct kvattn_tail_ctx kvattn_tail_ctx;
+
+int kvattn_tail_ctx_create(kvattn_tail_ctx** ctx);
+int kvattn_tail_ctx_destroy(kvattn_tail_ctx* ctx);
+
+/* Bytes of workspace for kvattn_decode_window_tail: two staging slots of tile_cells rows
+ * of K and of V, the partials of the window splits and of every tail tile, status word. */
+size_t kvattn_window_tail_workspace_bytes(int n_head, int n_head_kv, int head_dim,
+                                          int64_t n_win, int64_t n_tail, int split,
+                                          int64_t tile_cells, int tail_split);
+
+/*
+ *  q          device half [n_head][head_dim].
+ *  k_win, v_win  device half [n_win][n_head_kv][head_dim] -- the resident window.
+ *  k_tail_host, v_tail_host  PINNED host half [n_tail][n_head_kv][head_dim] -- the older
+ *             tail (cudaHostAlloc / cudaHostRegister memory).
+ *  tile_cells tail cells per host-to-device tile (a positive multiple of tail_split);
+ *             tiles are copied on copy_stream into two device staging slots, one tile
+ *             ahead of the compute (double buffering), with events ordering each copy
+ *             after the decode that last read its slot.
+ *  split      cells per partial over the window; tail_split  cells per partial inside a
+ *             tile.  Both positive multiples of 32.
+ *  out, lse   device float [n_head][head_dim], [n_head].
+ *  compute_stream, copy_stream  cudaStream_t; must differ.  On return every kernel and
+ *             copy is enqueued; out/lse are ready when compute_stream reaches this point.
+ * Errors: INVALID_ARG, UNSUPPORTED, WORKSPACE (before any CUDA call); CUDA (work already
+ * enqueued stays enqueued; outputs are then unspecified).
+ */
+int kvattn_decode_window_tail(kvattn_tail_ctx* ctx, const void* q,
+                              const void* k_win, const void* v_win, int64_t n_win,
+                              const void* k_tail_host, const void* v_tail_host, int64_t n_tail,
+                              int64_t tile_cells, int n_head, int n_head_kv, int head_dim,
+                              int split, int tail_split, float scale, float* out, float* lse,
+                              void* ws, size_t ws_bytes, void* compute_stream,
+                              void* copy_stream);
+
+/* Wait (host, bounded) until everything the last kvattn_decode_window_tail on this ctx
+ * enqueued has finished.  Polls an event; returns TIMEOUT after timeout_ms, CUDA if the
+ * work failed. */
+int kvattn_tail_wait(kvattn_tail_ctx* ctx, int timeout_ms);
+
+/* Read (and optionally clear) the sticky KVATTN_DEVICE_* bits of a decode or window+tail
+ * workspace.  Synchronises `stream`. */
+int kvattn_workspace_status(void* ws, uint32_t* flags, int clear, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KVATTN_H */

@@ -1,0 +1,569 @@
+// C-ABI entry points of kvattn: host-side validation, workspace carving, launch order,
+// and the window + host-tail pipeline.  No entry point allocates device memory.
+#include <atomic>
+#include <chrono>
+#include <cmath>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+#include <thread>
+
+#include "kvattn_internal.cuh"
+
+using namespace kvattn;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+int env_int(const char* name, int dflt) {
+    const char* v = std::getenv(name);
+    if (v == nullptr || *v == 0) return dflt;
+    return std::atoi(v);
+}
+
+bool use_pdl() {
+    static const bool on = env_int("KVATTN_PDL", 1) != 0;
+    return on;
+}
+
+int sm_count() {
+    static std::once_flag once[kMaxDevices];
+    static int count[kMaxDevices];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 1;
+    std::call_once(once[dev % kMaxDevices], [&] {
+        int n = 0;
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+        count[dev % kMaxDevices] = n > 0 ? n : 1;
+    });
+    return count[dev % kMaxDevices];
+}
+
+// Resident CTAs per SM of the split-decode kernel for (kv_type, head_dim, n_stages).
+int occupancy(int kv_type, int head_dim, int n_stages) {
+    static std::mutex mu;
+    static int cache[kMaxDevices][2][2][16];
+    static bool have[kMaxDevices][2][2][16];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 1;
+    const int d = dev % kMaxDevices, t = kv_type ? 1 : 0, h = head_dim == 256 ? 1 : 0;
+    std::lock_guard<std::mutex> lock(mu);
+    if (!have[d][t][h][n_stages]) {
+        int blocks = 0;
+        if (split_decode_occupancy(kv_type, head_dim, n_stages, &blocks) != cudaSuccess) blocks = 0;
+        cache[d][t][h][n_stages] = blocks;
+        have[d][t][h][n_stages] = true;
+    }
+    return cache[d][t][h][n_stages];
+}
+
+// Pipeline depth per CTA ("launch bounds and occupancy-aware selection", KVARN item 6):
+// the deepest ring whose resident capacity still holds the whole grid in one wave; for
+// grids larger than one wave, the deepest ring that keeps three CTAs on every SM.
+int pick_stages(int kv_type, int head_dim, int64_t grid_ctas) {
+    const int forced = env_int("KVATTN_STAGES", 0);
+    const int max_st = split_decode_max_stages();
+    const int stage = split_decode_stage_bytes(kv_type, head_dim);
+    const int hdr = split_decode_header_bytes();
+    const int limit = split_decode_max_smem();
+    if (forced >= 2 && forced <= max_st && hdr + forced * stage <= limit) return forced;
+    const int64_t n_sm = sm_count();
+    for (int st = max_st; st >= 2; --st) {
+        if (hdr + st * stage > limit) continue;
+        const int b = occupancy(kv_type, head_dim, st);
+        if (b > 0 && (int64_t)b * n_sm >= grid_ctas) return st;
+    }
+    for (int st = max_st; st >= 2; --st) {
+        if (hdr + st * stage > limit) continue;
+        if (occupancy(kv_type, head_dim, st) >= 3) return st;
+    }
+    return 2;
+}
+
+int cuda_status(cudaError_t e) { return e == cudaSuccess ? KVATTN_OK : KVATTN_ERR_CUDA; }
+
+// Failure-detection test hook (host-side switch, read on every call): with
+// KVATTN_DEBUG_STALL_TX=<bytes> the first tile of every split expects that many extra
+// bytes that no copy delivers, so its pipeline wait runs out after KVATTN_DEBUG_WAIT_MS
+// milliseconds (default 20) and the kernel reports KVATTN_DEVICE_WAIT_TIMEOUT.  All real
+// copies still complete; nothing faults or hangs.
+void apply_debug_hooks(SplitDecodeParams& p) {
+    p.wait_limit_ns = kWaitLimitNs;
+    p.stall_tx = 0;
+    const int stall = env_int("KVATTN_DEBUG_STALL_TX", 0);
+    if (stall > 0) {
+        p.stall_tx = (uint32_t)stall;
+        p.wait_limit_ns = (uint64_t)env_int("KVATTN_DEBUG_WAIT_MS", 20) * 1000000ull;
+    }
+}
+
+struct DecodeShape {
+    int n_seq, n_head, n_head_kv, head_dim, split;
+    int64_t max_len;
+};
+
+// Shape checks shared by the decode entry points.
+int check_shape(const DecodeShape& s) {
+    if (s.n_seq < 0 || s.n_head < 1 || s.n_head_kv < 1 || s.max_len < 0 || s.split < 1)
+        return KVATTN_ERR_INVALID_ARG;
+    if (s.n_head % s.n_head_kv != 0) return KVATTN_ERR_INVALID_ARG;
+    if (s.n_head / s.n_head_kv > kMaxGroup) return KVATTN_ERR_UNSUPPORTED;
+    if (s.head_dim != 128 && s.head_dim != 256) return KVATTN_ERR_UNSUPPORTED;
+    if (s.split % kTileCells != 0) return KVATTN_ERR_UNSUPPORTED;
+    if (s.n_seq > 65535 || s.n_head_kv > 65535) return KVATTN_ERR_UNSUPPORTED;
+    if ((s.max_len + s.split - 1) / s.split > (int64_t)INT32_MAX) return KVATTN_ERR_UNSUPPORTED;
+    return KVATTN_OK;
+}
+
+}  // namespace
+
+struct kvattn_tail_ctx {
+    cudaEvent_t copied[2];
+    cudaEvent_t consumed[2];
+    cudaEvent_t start;
+    cudaEvent_t done;
+    int device;
+    bool pending;
+};
+
+extern "C" {
+
+const char* kvattn_status_string(int status) {
+    switch (status) {
+    case KVATTN_OK: return "KVATTN_OK";
+    case KVATTN_ERR_INVALID_ARG: return "KVATTN_ERR_INVALID_ARG";
+    case KVATTN_ERR_UNSUPPORTED: return "KVATTN_ERR_UNSUPPORTED";
+    case KVATTN_ERR_WORKSPACE: return "KVATTN_ERR_WORKSPACE";
+    case KVATTN_ERR_CAPACITY: return "KVATTN_ERR_CAPACITY";
+    case KVATTN_ERR_CUDA: return "KVATTN_ERR_CUDA";
+    case KVATTN_ERR_TIMEOUT: return "KVATTN_ERR_TIMEOUT";
+    default: return "KVATTN_ERR_UNKNOWN";
+    }
+}
+
+int kvattn_version(void) { return (1 << 16) | 0; }
+
+int kvattn_build_cell_plan(const int64_t* cells, const int64_t* offsets, int n_seq,
+                           int64_t capacity_cells, int32_t* plan, int64_t plan_stride,
+                           int32_t* seq_lens) {
+    return build_cell_plan_host(cells, offsets, n_seq, capacity_cells, plan, plan_stride, seq_lens);
+}
+
+int kvattn_build_descriptors(const int32_t* cell_plan, int64_t plan_stride, const int32_t* seq_lens,
+                             int n_seq, int64_t max_len, int split, int64_t n_cells, int32_t* desc,
+                             void* stream) {
+    if (n_seq < 0 || split < 1 || max_len < 0 || n_cells < 1 || plan_stride < 1 || n_seq > 65535)
+        return KVATTN_ERR_INVALID_ARG;
+    const int64_t n_split = (max_len + split - 1) / split;
+    if (n_seq == 0 || n_split == 0) return KVATTN_OK;
+    if (cell_plan == nullptr || seq_lens == nullptr || desc == nullptr || !aligned(desc, 16))
+        return KVATTN_ERR_INVALID_ARG;
+    return cuda_status(launch_descriptors(cell_plan, plan_stride, seq_lens, n_seq, max_len, split,
+                                          n_cells, n_split, reinterpret_cast<int4*>(desc), nullptr,
+                                          static_cast<cudaStream_t>(stream)));
+}
+
+size_t kvattn_decode_workspace_bytes(int n_seq, int n_head, int head_dim, int64_t max_len,
+                                     int split) {
+    if (n_seq < 0 || n_head < 1 || head_dim < 1 || max_len < 0 || split < 1) return 0;
+    const int64_t n_split = (max_len + split - 1) / split;
+    return decode_ws_layout(n_seq, n_head, head_dim, n_split).total;
+}
+
+}  // extern "C"
+
+namespace {
+
+// kvattn_decode and kvattn_decode_partials: split-decode into partials (the workspace's
+// or the caller's), then -- for kvattn_decode -- the merge.
+int decode_impl(const void* q, const void* k_cache, const void* v_cache, const void* k_scales,
+                const void* v_scales, int kv_type, int64_t n_cells, const int32_t* cell_plan,
+                int64_t plan_stride, const int32_t* seq_lens, int n_seq, int64_t max_len, int n_head,
+                int n_head_kv, int head_dim, int split, float scale, float* out, float* lse,
+                float* part_o_user, float* part_lse_user, void* ws, size_t ws_bytes, void* stream) {
+    const bool merge = part_o_user == nullptr;
+    const DecodeShape shape{n_seq, n_head, n_head_kv, head_dim, split, max_len};
+    int st = check_shape(shape);
+    if (st != KVATTN_OK) return st;
+    if (q == nullptr || k_cache == nullptr || v_cache == nullptr || seq_lens == nullptr || ws == nullptr)
+        return KVATTN_ERR_INVALID_ARG;
+    if (merge && (out == nullptr || lse == nullptr)) return KVATTN_ERR_INVALID_ARG;
+    if (!merge && (part_lse_user == nullptr || !aligned(part_o_user, 16) || !aligned(part_lse_user, 4)))
+        return KVATTN_ERR_INVALID_ARG;
+    if (kv_type != KVATTN_KV_F16 && kv_type != KVATTN_KV_Q8_0) return KVATTN_ERR_INVALID_ARG;
+    if (kv_type == KVATTN_KV_Q8_0 && (k_scales == nullptr || v_scales == nullptr))
+        return KVATTN_ERR_INVALID_ARG;
+    if (kv_type == KVATTN_KV_F16 && (k_scales != nullptr || v_scales != nullptr))
+        return KVATTN_ERR_INVALID_ARG;
+    if (n_cells < 1 || (cell_plan != nullptr && plan_stride < 1) || !std::isfinite(scale))
+        return KVATTN_ERR_INVALID_ARG;
+    if (!aligned(q, 4) || !aligned(k_cache, 16) || !aligned(v_cache, 16) ||
+        (merge && (!aligned(out, 16) || !aligned(lse, 4))) || !aligned(ws, kWsAlign) ||
+        (cell_plan && !aligned(cell_plan, 4)) || !aligned(seq_lens, 4))
+        return KVATTN_ERR_INVALID_ARG;
+    if (kv_type == KVATTN_KV_Q8_0) {
+        const size_t sa = head_dim == 128 ? 8 : 16;
+        if (!aligned(k_scales, sa) || !aligned(v_scales, sa)) return KVATTN_ERR_INVALID_ARG;
+    }
+    const int64_t n_split = (max_len + split - 1) / split;
+    const DecodeWsLayout lay = decode_ws_layout(n_seq, n_head, head_dim, n_split);
+    if (ws_bytes < lay.total) return KVATTN_ERR_WORKSPACE;
+    if (n_seq == 0) return KVATTN_OK;
+
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    char* wsb = static_cast<char*>(ws);
+    uint32_t* status = reinterpret_cast<uint32_t*>(wsb);
+    float* part_o = merge ? reinterpret_cast<float*>(wsb + lay.o_off) : part_o_user;
+    float* part_lse = merge ? reinterpret_cast<float*>(wsb + lay.lse_off) : part_lse_user;
+    int4* desc = nullptr;
+    const bool pdl = use_pdl();
+    if (n_split > 0) {
+        if (cell_plan != nullptr) {
+            desc = reinterpret_cast<int4*>(wsb + lay.desc_off);
+            cudaError_t e = launch_descriptors(cell_plan, plan_stride, seq_lens, n_seq, max_len,
+                                               split, n_cells, n_split, desc, status, s);
+            if (e != cudaSuccess) return KVATTN_ERR_CUDA;
+        }
+        SplitDecodeParams p = {};
+        p.q = static_cast<const __half*>(q);
+        p.k = k_cache;
+        p.v = v_cache;
+        p.k_scale = static_cast<const __half*>(k_scales);
+        p.v_scale = static_cast<const __half*>(v_scales);
+        p.plan = cell_plan;
+        p.seq_lens = seq_lens;
+        p.desc = desc;
+        p.part_o = part_o;
+        p.part_lse = part_lse;
+        p.status = status;
+        p.n_cells = n_cells;
+        p.plan_stride = plan_stride;
+        p.max_len = max_len;
+        p.n_split = n_split;
+        p.part_base = 0;
+        p.fixed_len = 0;
+        p.n_seq = n_seq;
+        p.n_head = n_head;
+        p.n_head_kv = n_head_kv;
+        p.group = n_head / n_head_kv;
+        p.split = split;
+        const dim3 grid((unsigned)n_split, (unsigned)n_head_kv, (unsigned)n_seq);
+        p.n_stages = pick_stages(kv_type, head_dim, (int64_t)n_split * n_head_kv * n_seq);
+        p.scale_log2 = (float)((double)scale * 1.4426950408889634074);
+        apply_debug_hooks(p);
+        cudaError_t e = launch_split_decode(p, kv_type, head_dim, grid, s, pdl);
+        if (e != cudaSuccess) return KVATTN_ERR_CUDA;
+    }
+    if (!merge) return KVATTN_OK;
+    MergeParams m = {};
+    m.part_o = part_o;
+    m.part_lse = part_lse;
+    m.out = out;
+    m.lse = lse;
+    m.seq_lens = seq_lens;
+    m.n_parts = n_split;
+    m.max_len = max_len;
+    m.len_cap = cell_plan != nullptr ? plan_stride : n_cells;
+    m.n_seq = n_seq;
+    m.n_rows = n_head;
+    m.head_dim = head_dim;
+    m.split = split;
+    return cuda_status(launch_merge(m, s, pdl && n_split > 0));
+}
+
+}  // namespace
+
+extern "C" {
+
+int kvattn_decode(const void* q, const void* k_cache, const void* v_cache, const void* k_scales,
+                  const void* v_scales, int kv_type, int64_t n_cells, const int32_t* cell_plan,
+                  int64_t plan_stride, const int32_t* seq_lens, int n_seq, int64_t max_len,
+                  int n_head, int n_head_kv, int head_dim, int split, float scale, float* out,
+                  float* lse, void* ws, size_t ws_bytes, void* stream) {
+    if (out == nullptr || lse == nullptr) return KVATTN_ERR_INVALID_ARG;
+    return decode_impl(q, k_cache, v_cache, k_scales, v_scales, kv_type, n_cells, cell_plan,
+                       plan_stride, seq_lens, n_seq, max_len, n_head, n_head_kv, head_dim, split,
+                       scale, out, lse, nullptr, nullptr, ws, ws_bytes, stream);
+}
+
+int kvattn_decode_partials(const void* q, const void* k_cache, const void* v_cache,
+                           const void* k_scales, const void* v_scales, int kv_type,
+                           int64_t n_cells, const int32_t* cell_plan, int64_t plan_stride,
+                           const int32_t* seq_lens, int n_seq, int64_t max_len, int n_head,
+                           int n_head_kv, int head_dim, int split, float scale, float* part_o,
+                           float* part_lse, void* ws, size_t ws_bytes, void* stream) {
+    if (part_o == nullptr || part_lse == nullptr) return KVATTN_ERR_INVALID_ARG;
+    return decode_impl(q, k_cache, v_cache, k_scales, v_scales, kv_type, n_cells, cell_plan,
+                       plan_stride, seq_lens, n_seq, max_len, n_head, n_head_kv, head_dim, split,
+                       scale, nullptr, nullptr, part_o, part_lse, ws, ws_bytes, stream);
+}
+
+int kvattn_merge(const float* partials, const float* lses, int n_parts, int n_rows, int head_dim,
+                 float* out, float* lse, void* stream) {
+    if (n_parts < 0 || n_rows < 0 || head_dim < 4 || head_dim % 4 != 0 || head_dim > 1024)
+        return KVATTN_ERR_INVALID_ARG;
+    if (n_rows == 0) return KVATTN_OK;
+    if (out == nullptr || lse == nullptr || (n_parts > 0 && (partials == nullptr || lses == nullptr)))
+        return KVATTN_ERR_INVALID_ARG;
+    if (!aligned(out, 16) || !aligned(lse, 4) || (partials && !aligned(partials, 16)) ||
+        (lses && !aligned(lses, 4)))
+        return KVATTN_ERR_INVALID_ARG;
+    MergeParams m = {};
+    m.part_o = partials;
+    m.part_lse = lses;
+    m.out = out;
+    m.lse = lse;
+    m.seq_lens = nullptr;
+    m.n_parts = n_parts;
+    m.max_len = 0;
+    m.len_cap = 0;
+    m.n_seq = 1;
+    m.n_rows = n_rows;
+    m.head_dim = head_dim;
+    m.split = 1;
+    return cuda_status(launch_merge(m, static_cast<cudaStream_t>(stream), false));
+}
+
+// ------------------------------- window + host tail -------------------------------
+
+int kvattn_tail_ctx_create(kvattn_tail_ctx** ctx) {
+    if (ctx == nullptr) return KVATTN_ERR_INVALID_ARG;
+    *ctx = nullptr;
+    kvattn_tail_ctx* c = new (std::nothrow) kvattn_tail_ctx();
+    if (c == nullptr) return KVATTN_ERR_INVALID_ARG;
+    cudaError_t e = cudaGetDevice(&c->device);
+    cudaEvent_t* evs[6] = {&c->copied[0], &c->copied[1], &c->consumed[0], &c->consumed[1], &c->start, &c->done};
+    int made = 0;
+    for (; made < 6 && e == cudaSuccess; ++made) e = cudaEventCreateWithFlags(evs[made], cudaEventDisableTiming);
+    if (e != cudaSuccess) {
+        for (int i = 0; i < made - 1; ++i) cudaEventDestroy(*evs[i]);
+        delete c;
+        return KVATTN_ERR_CUDA;
+    }
+    c->pending = false;
+    *ctx = c;
+    return KVATTN_OK;
+}
+
+int kvattn_tail_ctx_destroy(kvattn_tail_ctx* ctx) {
+    if (ctx == nullptr) return KVATTN_ERR_INVALID_ARG;
+    cudaEvent_t evs[6] = {ctx->copied[0], ctx->copied[1], ctx->consumed[0], ctx->consumed[1], ctx->start, ctx->done};
+    int rc = KVATTN_OK;
+    for (cudaEvent_t ev : evs)
+        if (cudaEventDestroy(ev) != cudaSuccess) rc = KVATTN_ERR_CUDA;
+    delete ctx;
+    return rc;
+}
+
+namespace {
+
+struct TailLayout {
+    size_t stage_off[2][2];  // [slot][k|v]
+    DecodeWsLayout parts;    // partials of all window splits and tail tiles (n_seq = 1)
+    size_t parts_base;
+    int64_t n_split_win, n_tiles, splits_per_tile, n_parts;
+    size_t total;
+};
+
+bool tail_layout(int n_head, int n_head_kv, int head_dim, int64_t n_win, int64_t n_tail, int split,
+                 int64_t tile_cells, int tail_split, TailLayout* L) {
+    if (n_head < 1 || n_head_kv < 1 || head_dim < 1 || n_win < 0 || n_tail < 0 || split < 1 ||
+        tile_cells < 1 || tail_split < 1 || tile_cells % tail_split != 0)
+        return false;
+    const size_t tile_bytes = (size_t)tile_cells * n_head_kv * head_dim * 2;
+    size_t off = kStatusBytes;
+    for (int s = 0; s < 2; ++s)
+        for (int kv = 0; kv < 2; ++kv) {
+            L->stage_off[s][kv] = off;
+            off = align_up(off + tile_bytes, kWsAlign);
+        }
+    L->n_split_win = (n_win + split - 1) / split;
+    L->n_tiles = (n_tail + tile_cells - 1) / tile_cells;
+    L->splits_per_tile = tile_cells / tail_split;
+    L->n_parts = L->n_split_win + L->n_tiles * L->splits_per_tile;
+    L->parts = decode_ws_layout(1, n_head, head_dim, L->n_parts);
+    L->parts_base = off;
+    L->total = off + L->parts.total;
+    return true;
+}
+
+int fault_tile() {
+    // KVATTN_FAULT=copy@<t>: pretend the host-to-device copy of tail tile t failed
+    // (host-side fault injection for tests; no GPU fault is involved).
+    const char* v = std::getenv("KVATTN_FAULT");
+    if (v == nullptr || std::strncmp(v, "copy@", 5) != 0) return -1;
+    return std::atoi(v + 5);
+}
+
+}  // namespace
+
+size_t kvattn_window_tail_workspace_bytes(int n_head, int n_head_kv, int head_dim, int64_t n_win,
+                                          int64_t n_tail, int split, int64_t tile_cells,
+                                          int tail_split) {
+    TailLayout L;
+    if (!tail_layout(n_head, n_head_kv, head_dim, n_win, n_tail, split, tile_cells, tail_split, &L))
+        return 0;
+    return L.total;
+}
+
+int kvattn_decode_window_tail(kvattn_tail_ctx* ctx, const void* q, const void* k_win,
+                              const void* v_win, int64_t n_win, const void* k_tail_host,
+                              const void* v_tail_host, int64_t n_tail, int64_t tile_cells,
+                              int n_head, int n_head_kv, int head_dim, int split, int tail_split,
+                              float scale, float* out, float* lse, void* ws, size_t ws_bytes,
+                              void* compute_stream, void* copy_stream) {
+    if (ctx == nullptr || q == nullptr || out == nullptr || lse == nullptr || ws == nullptr)
+        return KVATTN_ERR_INVALID_ARG;
+    const DecodeShape sw{1, n_head, n_head_kv, head_dim, split, n_win};
+    int st = check_shape(sw);
+    if (st != KVATTN_OK) return st;
+    const DecodeShape stl{1, n_head, n_head_kv, head_dim, tail_split, tile_cells};
+    st = check_shape(stl);
+    if (st != KVATTN_OK) return st;
+    if (n_win < 0 || n_tail < 0 || tile_cells < 1 || tile_cells % tail_split != 0 ||
+        !std::isfinite(scale) || compute_stream == copy_stream)
+        return KVATTN_ERR_INVALID_ARG;
+    if ((n_win > 0 && (k_win == nullptr || v_win == nullptr)) ||
+        (n_tail > 0 && (k_tail_host == nullptr || v_tail_host == nullptr)))
+        return KVATTN_ERR_INVALID_ARG;
+    if (!aligned(q, 4) || !aligned(out, 16) || !aligned(lse, 4) || !aligned(ws, kWsAlign) ||
+        (k_win && !aligned(k_win, 16)) || (v_win && !aligned(v_win, 16)))
+        return KVATTN_ERR_INVALID_ARG;
+    TailLayout L;
+    if (!tail_layout(n_head, n_head_kv, head_dim, n_win, n_tail, split, tile_cells, tail_split, &L))
+        return KVATTN_ERR_INVALID_ARG;
+    if (ws_bytes < L.total) return KVATTN_ERR_WORKSPACE;
+
+    cudaStream_t cs = static_cast<cudaStream_t>(compute_stream);
+    cudaStream_t xs = static_cast<cudaStream_t>(copy_stream);
+    char* wsb = static_cast<char*>(ws);
+    uint32_t* status = reinterpret_cast<uint32_t*>(wsb);
+    char* parts = wsb + L.parts_base;
+    const int fault = fault_tile();
+    const bool pdl = use_pdl();
+
+    SplitDecodeParams p = {};
+    p.q = static_cast<const __half*>(q);
+    p.part_o = reinterpret_cast<float*>(parts + L.parts.o_off);
+    p.part_lse = reinterpret_cast<float*>(parts + L.parts.lse_off);
+    p.status = status;
+    p.plan = nullptr;
+    p.seq_lens = nullptr;
+    p.desc = nullptr;
+    p.n_split = L.n_parts;
+    p.n_seq = 1;
+    p.n_head = n_head;
+    p.n_head_kv = n_head_kv;
+    p.group = n_head / n_head_kv;
+    p.scale_log2 = (float)((double)scale * 1.4426950408889634074);
+    apply_debug_hooks(p);
+
+    // The copy stream may not overwrite a staging slot that an earlier call's tile decode
+    // on the compute stream still reads.
+    if (cudaEventRecord(ctx->start, cs) != cudaSuccess) return KVATTN_ERR_CUDA;
+    if (cudaStreamWaitEvent(xs, ctx->start, 0) != cudaSuccess) return KVATTN_ERR_CUDA;
+
+    // window: resident cells, attended while the first tail tiles are in flight
+    if (L.n_split_win > 0) {
+        p.k = k_win;
+        p.v = v_win;
+        p.n_cells = n_win;
+        p.max_len = n_win;
+        p.fixed_len = n_win;
+        p.split = split;
+        p.part_base = 0;
+        const dim3 grid((unsigned)L.n_split_win, (unsigned)n_head_kv, 1);
+        p.n_stages = pick_stages(KVATTN_KV_F16, head_dim, (int64_t)L.n_split_win * n_head_kv);
+        if (launch_split_decode(p, KVATTN_KV_F16, head_dim, grid, cs, pdl) != cudaSuccess)
+            return KVATTN_ERR_CUDA;
+    }
+
+    // tail: tile t -> staging slot t % 2 on the copy stream, decoded on the compute stream
+    const size_t row_bytes = (size_t)n_head_kv * head_dim * 2;
+    const int tile_stages = pick_stages(KVATTN_KV_F16, head_dim, L.splits_per_tile * n_head_kv);
+    for (int64_t t = 0; t < L.n_tiles; ++t) {
+        const int slot = (int)(t & 1);
+        const int64_t c0 = t * tile_cells;
+        const int64_t len = (c0 + tile_cells <= n_tail) ? tile_cells : n_tail - c0;
+        const size_t bytes = (size_t)len * row_bytes;
+        if (t >= 2 && cudaStreamWaitEvent(xs, ctx->consumed[slot], 0) != cudaSuccess)
+            return KVATTN_ERR_CUDA;
+        if (t == fault) return KVATTN_ERR_CUDA;
+        char* dk = wsb + L.stage_off[slot][0];
+        char* dv = wsb + L.stage_off[slot][1];
+        if (cudaMemcpyAsync(dk, static_cast<const char*>(k_tail_host) + (size_t)c0 * row_bytes, bytes,
+                            cudaMemcpyHostToDevice, xs) != cudaSuccess)
+            return KVATTN_ERR_CUDA;
+        if (cudaMemcpyAsync(dv, static_cast<const char*>(v_tail_host) + (size_t)c0 * row_bytes, bytes,
+                            cudaMemcpyHostToDevice, xs) != cudaSuccess)
+            return KVATTN_ERR_CUDA;
+        if (cudaEventRecord(ctx->copied[slot], xs) != cudaSuccess) return KVATTN_ERR_CUDA;
+        if (cudaStreamWaitEvent(cs, ctx->copied[slot], 0) != cudaSuccess) return KVATTN_ERR_CUDA;
+        p.k = dk;
+        p.v = dv;
+        p.n_cells = len;
+        p.max_len = tile_cells;
+        p.fixed_len = len;
+        p.split = tail_split;
+        p.part_base = L.n_split_win + t * L.splits_per_tile;
+        p.n_stages = tile_stages;
+        const dim3 grid((unsigned)L.splits_per_tile, (unsigned)n_head_kv, 1);
+        if (launch_split_decode(p, KVATTN_KV_F16, head_dim, grid, cs, false) != cudaSuccess)
+            return KVATTN_ERR_CUDA;
+        if (cudaEventRecord(ctx->consumed[slot], cs) != cudaSuccess) return KVATTN_ERR_CUDA;
+    }
+
+    MergeParams m = {};
+    m.part_o = reinterpret_cast<const float*>(parts + L.parts.o_off);
+    m.part_lse = reinterpret_cast<const float*>(parts + L.parts.lse_off);
+    m.out = out;
+    m.lse = lse;
+    m.seq_lens = nullptr;
+    m.n_parts = L.n_parts;
+    m.n_seq = 1;
+    m.n_rows = n_head;
+    m.head_dim = head_dim;
+    m.split = 1;
+    if (launch_merge(m, cs, pdl) != cudaSuccess) return KVATTN_ERR_CUDA;
+    if (cudaEventRecord(ctx->done, cs) != cudaSuccess) return KVATTN_ERR_CUDA;
+    ctx->pending = true;
+    return KVATTN_OK;
+}
+
+int kvattn_tail_wait(kvattn_tail_ctx* ctx, int timeout_ms) {
+    if (ctx == nullptr || timeout_ms < 0) return KVATTN_ERR_INVALID_ARG;
+    if (!ctx->pending) return KVATTN_OK;
+    const auto t0 = std::chrono::steady_clock::now();
+    for (;;) {
+        const cudaError_t e = cudaEventQuery(ctx->done);
+        if (e == cudaSuccess) {
+            ctx->pending = false;
+            return KVATTN_OK;
+        }
+        if (e != cudaErrorNotReady) return KVATTN_ERR_CUDA;
+        const auto ms = std::chrono::duration_cast<std::chrono::milliseconds>(
+                            std::chrono::steady_clock::now() - t0)
+                            .count();
+        if (ms >= timeout_ms) return KVATTN_ERR_TIMEOUT;
+        std::this_thread::sleep_for(std::chrono::microseconds(50));
+    }
+}
+
+int kvattn_workspace_status(void* ws, uint32_t* flags, int clear, void* stream) {
+    if (ws == nullptr || flags == nullptr) return KVATTN_ERR_INVALID_ARG;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    uint32_t v = 0;
+    if (cudaMemcpyAsync(&v, ws, sizeof(v), cudaMemcpyDeviceToHost, s) != cudaSuccess) return KVATTN_ERR_CUDA;
+    if (cudaStreamSynchronize(s) != cudaSuccess) return KVATTN_ERR_CUDA;
+    *flags = v;
+    if (clear) {
+        if (cudaMemsetAsync(ws, 0, sizeof(uint32_t), s) != cudaSuccess) return KVATTN_ERR_CUDA;
+        if (cudaStreamSynchronize(s) != cudaSuccess) return KVATTN_ERR_CUDA;
+    }
+    return KVATTN_OK;
+}
+
+}  // extern "C"

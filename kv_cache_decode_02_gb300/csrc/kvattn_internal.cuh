@@ -1,0 +1,255 @@
+// Internal declarations and device helpers of the kvattn library (not installed).
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include "kvattn.h"
+
+namespace kvattn {
+
+// ---------------------------------------------------------------------------------------
+// Workspace layout shared by the decode entry points.
+// ---------------------------------------------------------------------------------------
+constexpr size_t kWsAlign = 256;
+constexpr size_t kStatusBytes = 256;  // first bytes: sticky uint32 status word
+
+inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+struct DecodeWsLayout {
+    size_t desc_off, lse_off, o_off, total;
+};
+
+inline DecodeWsLayout decode_ws_layout(int n_seq, int n_head, int head_dim, int64_t n_split) {
+    DecodeWsLayout L;
+    size_t off = kStatusBytes;
+    L.desc_off = off;
+    off = align_up(off + (size_t)n_seq * (size_t)n_split * 16, kWsAlign);
+    L.lse_off = off;
+    off = align_up(off + (size_t)n_seq * (size_t)n_split * (size_t)n_head * 4, kWsAlign);
+    L.o_off = off;
+    off = align_up(off + (size_t)n_seq * (size_t)n_split * (size_t)n_head * (size_t)head_dim * 4,
+                   kWsAlign);
+    L.total = off;
+    return L;
+}
+
+// ---------------------------------------------------------------------------------------
+// Kernel parameter blocks.
+// ---------------------------------------------------------------------------------------
+struct SplitDecodeParams {
+    const __half* q;          // [S][H][D]
+    const void* k;            // [cells][Hk][D] (f16 or int8)
+    const void* v;
+    const __half* k_scale;    // Q8_0: [cells][Hk][D/32]
+    const __half* v_scale;
+    const int32_t* plan;      // nullable: [S][plan_stride]
+    const int32_t* seq_lens;  // nullable: [S]; when NULL every sequence has fixed_len cells
+    const int4* desc;         // nullable: [S][n_split]
+    float* part_o;            // [S][n_split][H][D]
+    float* part_lse;          // [S][n_split][H]
+    uint32_t* status;         // sticky status word
+    int64_t n_cells;
+    int64_t plan_stride;
+    int64_t max_len;
+    int64_t n_split;          // splits per sequence (partial stride)
+    int64_t part_base;        // first partial index written (window + tail packs several calls)
+    int64_t fixed_len;
+    uint64_t wait_limit_ns;   // bound on every pipeline wait
+    uint32_t stall_tx;        // test hook: extra bytes expected on the first tile (never arrive)
+    int n_seq, n_head, n_head_kv, group, split;
+    int n_stages;
+    float scale_log2;         // scale * log2(e)
+};
+
+struct MergeParams {
+    const float* part_o;      // parts: o[(base + p) * row_stride_parts ...]
+    const float* part_lse;
+    float* out;
+    float* lse;
+    const int32_t* seq_lens;  // nullable: per-sequence part count = ceil(clamp(len)/split)
+    int64_t n_parts;          // parts per sequence (fixed count when seq_lens == NULL)
+    int64_t max_len;
+    int64_t len_cap;          // clamp for seq_lens (n_cells or plan_stride)
+    int n_seq, n_rows;        // rows per sequence (= n_head)
+    int head_dim, split;
+};
+
+// Launchers (return cudaError_t of the launch).
+cudaError_t launch_split_decode(const SplitDecodeParams& p, int kv_type, int head_dim,
+                                dim3 grid, cudaStream_t stream, bool pdl);
+cudaError_t launch_merge(const MergeParams& p, cudaStream_t stream, bool pdl);
+int split_decode_stage_bytes(int kv_type, int head_dim);
+int split_decode_header_bytes();
+int split_decode_max_stages();
+int split_decode_max_smem();
+int split_decode_threads();
+cudaError_t split_decode_occupancy(int kv_type, int head_dim, int n_stages, int* blocks);
+cudaError_t launch_descriptors(const int32_t* plan, int64_t plan_stride, const int32_t* seq_lens,
+                               int n_seq, int64_t max_len, int split, int64_t n_cells,
+                               int64_t n_split, int4* desc, uint32_t* status,
+                               cudaStream_t stream);
+
+// Host plan builder (plan.cpp).
+int build_cell_plan_host(const int64_t* cells, const int64_t* offsets, int n_seq,
+                         int64_t capacity_cells, int32_t* plan, int64_t plan_stride,
+                         int32_t* seq_lens);
+
+// Tile geometry of the split-decode kernel.
+constexpr int kConsumerWarps = 2;
+constexpr int kWarpCells = 16;
+constexpr int kTileCells = kConsumerWarps * kWarpCells;  // cells per pipeline stage
+constexpr int kMaxGroup = 8;
+
+// ---------------------------------------------------------------------------------------
+// Device helpers: mbarrier, bulk async copies, bounded waits, tensor-core fragments.
+// ---------------------------------------------------------------------------------------
+#if defined(__CUDACC__)
+
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.expect_tx.relaxed.cta.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+    asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+__device__ __forceinline__ uint64_t global_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+#endif  // __CUDACC__
+
+// Default bound on a pipeline wait (wall time).
+constexpr uint64_t kWaitLimitNs = 2000000000ull;
+
+#if defined(__CUDACC__)
+
+// Bounded wait on an mbarrier phase.  Gives up after `limit_ns` of wall time, or early
+// when another thread of the CTA has already given up (`*abort` set).  Returns false on
+// give-up.
+__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
+                                                  volatile int* abort, uint64_t limit_ns) {
+    if (mbar_test(bar, parity)) return true;
+    uint64_t t0 = global_ns();
+    for (uint32_t it = 1;; ++it) {
+        if (mbar_test(bar, parity)) return true;
+        if ((it & 255u) == 0) {
+            if (*abort) return false;
+            if (global_ns() - t0 > limit_ns) {
+                *abort = 1;
+                return false;
+            }
+        }
+    }
+}
+
+// 1-D bulk async copy global -> shared, completion counted on an mbarrier (bytes).
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes,
+                                         uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+            dst),
+        "l"(src), "r"(bytes), "r"(bar)
+        : "memory");
+}
+
+// Small LSU async copies (8 or 16 bytes) and their mbarrier completion arrive.
+__device__ __forceinline__ void cp_async_8(uint32_t dst, const void* src) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_16(uint32_t dst, const void* src) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_arrive_noinc(uint32_t bar) {
+    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
+                                        uint32_t& r3) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+                 : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x4_trans(uint32_t addr, uint32_t& r0, uint32_t& r1,
+                                              uint32_t& r2, uint32_t& r3) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+                 : "r"(addr));
+}
+
+// D(16x8 f32) += A(16x16 f16, row) * B(16x8 f16, col)
+__device__ __forceinline__ void mma_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                          uint32_t a3, uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+        "{%8,%9}, {%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ float fast_exp2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+__device__ __forceinline__ float fast_log2(float x) {
+    float y;
+    asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+__device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
+    __half2 h = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&h);
+}
+
+// Two int8 lanes of a byte permutation -> exact half2, with the magic-number method of
+// Kim et al. 2022 ("Who Says Elephants Can't Run"): byte b becomes the f16 1024 + (b ^ 0x80),
+// then subtracting 1152 leaves the signed value.  `sel` picks the two bytes into positions
+// 0 and 2 of the prmt result.
+__device__ __forceinline__ uint32_t i8pair_to_h2(uint32_t w0, uint32_t w1, uint32_t sel) {
+    uint32_t t;
+    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(t) : "r"(w0), "r"(w1), "r"(sel));
+    t = ((t ^ 0x00800080u) & 0x00FF00FFu) | 0x64006400u;
+    uint32_t r;
+    const uint32_t bias = 0x64806480u;  // (1152, 1152) in f16
+    asm("sub.f16x2 %0, %1, %2;" : "=r"(r) : "r"(t), "r"(bias));
+    return r;
+}
+
+__device__ __forceinline__ void pdl_wait() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+#endif  // __CUDACC__
+
+}  // namespace kvattn

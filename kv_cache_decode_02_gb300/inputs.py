@@ -84,6 +84,16 @@ def normal_f16(rng: np.random.Generator, shape, chunk: int = 1 << 24) -> np.ndar
     return out.reshape(shape)
 
 
+def normal_f16_torch(seed, shape, device="cuda"):
+    """N(0, 1) draws rounded to f16 from a seeded torch generator on ``device`` (used for
+    benchmark-only buffers too large to draw quickly on the host)."""
+    import torch
+    g = torch.Generator(device=device)
+    s = np.random.SeedSequence(list(seed) if isinstance(seed, (tuple, list)) else [seed])
+    g.manual_seed(int(s.generate_state(1, dtype=np.uint64)[0] >> 1))
+    return torch.randn(shape, generator=g, device=device, dtype=torch.float32).half()
+
+
 def q8_0_planes(rng: np.random.Generator, n_cells: int, n_head_kv: int, head_dim: int):
     """Q8_0 SoA planes: int8 values uniform in [-127, 127], f16 scales ~U(0.001, 0.02)."""
     assert head_dim % 32 == 0

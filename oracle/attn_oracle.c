@@ -56,6 +56,17 @@ double oracle_f16_to_f64(uint16_t h) {
     return sign ? -v : v;
 }
 
+/* All 65536 binary16 values, filled once from oracle_f16_to_f64 before any parallel work
+ * (a cache of the definition above, so that large cases run in seconds). */
+static double f16_table[65536];
+static int f16_table_ready = 0;
+
+static void f16_table_init(void) {
+    if (f16_table_ready) return;
+    for (int i = 0; i < 65536; ++i) f16_table[i] = oracle_f16_to_f64((uint16_t)i);
+    f16_table_ready = 1;
+}
+
 /* One K or V source: element (cell, kv_head, dim) -> exact fp64 value. */
 typedef struct {
     int kind;
@@ -67,11 +78,11 @@ static double kv_value(const kv_source* src, int64_t cell, int g, int d, int Hk,
     int64_t idx = (cell * Hk + g) * (int64_t)D + d;
     switch (src->kind) {
     case ORACLE_KV_F16:
-        return oracle_f16_to_f64(((const uint16_t*)src->data)[idx]);
+        return f16_table[((const uint16_t*)src->data)[idx]];
     case ORACLE_KV_Q8_0: {
         double qs = (double)((const int8_t*)src->data)[idx];
         int64_t sidx = (cell * Hk + g) * (int64_t)(D / 32) + d / 32;
-        return oracle_f16_to_f64(src->scale[sidx]) * qs;
+        return f16_table[src->scale[sidx]] * qs;
     }
     default:
         return ((const double*)src->data)[idx];
@@ -94,6 +105,7 @@ static int oracle_decode(const void* q, int q_is_f64, const kv_source* K, const 
                          double* out, double* lse, int n_threads) {
     if (S < 0 || H <= 0 || Hk <= 0 || D <= 0 || H % Hk != 0) return -1;
     int G = H / Hk;
+    f16_table_init();
     for (int s = 0; s < S; ++s) {
         if (seq_lens[s] < 0) return -1;
         if (plan) {

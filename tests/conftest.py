@@ -34,5 +34,5 @@ def kvattn():
     """The C-ABI binding, built in-tree on first use (nvcc cross-compiles without a GPU)."""
     from kv_cache_decode_02_gb300 import _build
     _build.build_library()
-    import kv_cache_decode_02_gb300 as k
+    from kv_cache_decode_02_gb300 import kvattn as k
     return k

@@ -1,0 +1,104 @@
+"""Window + pinned-host tail on small cases: ragged last tile, no window, no tail,
+repeated calls reusing the staging slots, host-side fault injection and the bounded
+host wait."""
+import numpy as np
+import pytest
+
+import oracle
+from tests.gpu_util import assert_close, dev
+
+pytestmark = pytest.mark.gpu
+
+
+def make(rng, N, n_win, H, Hk, D):
+    q = rng.standard_normal((1, H, D), dtype=np.float32).astype(np.float16)
+    k = rng.standard_normal((N, Hk, D), dtype=np.float32).astype(np.float16)
+    v = rng.standard_normal((N, Hk, D), dtype=np.float32).astype(np.float16)
+    return q, k, v
+
+
+def run(kvattn, wt, q, k, v, n_win, tile, split=128, tail_split=64, ws=None, copy_stream=None):
+    import torch
+    n_tail = k.shape[0] - n_win
+    k_tail = torch.from_numpy(k[:n_tail]).pin_memory()
+    v_tail = torch.from_numpy(v[:n_tail]).pin_memory()
+    k_win = dev(k[n_tail:]) if n_win else None
+    v_win = dev(v[n_tail:]) if n_win else None
+    if copy_stream is None:
+        copy_stream = torch.cuda.Stream()
+    out, lse = wt(dev(q[0]), k_win, v_win, k_tail if n_tail else None, v_tail if n_tail else None,
+                  split=split, tile_cells=tile, tail_split=tail_split, ws=ws, copy_stream=copy_stream)
+    kvattn.kvattn_tail_wait(wt.ctx, 30000)
+    torch.cuda.synchronize()
+    return out.view(1, *out.shape), lse.view(1, -1)
+
+
+@pytest.mark.parametrize("N,n_win,tile,H,Hk", [
+    (5000, 1000, 512, 40, 8),     # ragged last tile (4000 = 7 x 512 + 416)
+    (3000, 0, 256, 16, 4),        # everything in the tail
+    (777, 777, 256, 16, 4),       # everything resident
+    (4096, 64, 128, 24, 4),       # many small tiles, GQA-6
+])
+def test_window_tail_small(kvattn, N, n_win, tile, H, Hk):
+    rng = np.random.default_rng(N + n_win)
+    q, k, v = make(rng, N, n_win, H, Hk, 128)
+    wt = kvattn.WindowTail()
+    out, lse = run(kvattn, wt, q, k, v, n_win, tile)
+    wo, wl = oracle.decode_f16(q, k, v, [N])
+    assert_close(out, lse, wo, wl)
+    wt.close()
+
+
+def test_repeated_calls_reuse_slots(kvattn):
+    import torch
+    rng = np.random.default_rng(3)
+    N, n_win, H, Hk, D = 6000, 500, 16, 4, 128
+    wt = kvattn.WindowTail()
+    ws = wt.workspace(H, Hk, D, n_win, N - n_win, 128, 256, 64)
+    cs = torch.cuda.Stream()
+    for trial in range(3):
+        q, k, v = make(rng, N, n_win, H, Hk, D)
+        out, lse = run(kvattn, wt, q, k, v, n_win, 256, ws=ws, copy_stream=cs)
+        wo, wl = oracle.decode_f16(q, k, v, [N])
+        assert_close(out, lse, wo, wl)
+    wt.close()
+
+
+def test_fault_injection_then_recovery(kvattn, monkeypatch):
+    """A failed tile copy (injected on the host) returns an error; the next call works."""
+    rng = np.random.default_rng(4)
+    N, n_win, H, Hk, D = 4000, 500, 16, 4, 128
+    q, k, v = make(rng, N, n_win, H, Hk, D)
+    wt = kvattn.WindowTail()
+    monkeypatch.setenv("KVATTN_FAULT", "copy@3")
+    with pytest.raises(kvattn.KvattnError) as e:
+        run(kvattn, wt, q, k, v, n_win, 256)
+    assert e.value.status == kvattn.KVATTN_ERR_CUDA
+    monkeypatch.delenv("KVATTN_FAULT")
+    out, lse = run(kvattn, wt, q, k, v, n_win, 256)
+    wo, wl = oracle.decode_f16(q, k, v, [N])
+    assert_close(out, lse, wo, wl)
+    wt.close()
+
+
+def test_host_wait_times_out_then_completes(kvattn):
+    """kvattn_tail_wait gives up after its limit while the stream is still busy."""
+    import torch
+    rng = np.random.default_rng(5)
+    N, n_win, H, Hk, D = 3000, 500, 16, 4, 128
+    q, k, v = make(rng, N, n_win, H, Hk, D)
+    n_tail = N - n_win
+    k_tail = torch.from_numpy(k[:n_tail]).pin_memory()
+    v_tail = torch.from_numpy(v[:n_tail]).pin_memory()
+    wt = kvattn.WindowTail()
+    torch.cuda._sleep(400_000_000)   # a bounded busy kernel ahead of the decode on this stream
+    out, lse = wt(dev(q[0]), dev(k[n_tail:]), dev(v[n_tail:]), k_tail, v_tail, split=128,
+                  tile_cells=256, tail_split=64, copy_stream=torch.cuda.Stream())
+    with pytest.raises(kvattn.KvattnError) as e:
+        kvattn.kvattn_tail_wait(wt.ctx, 1)
+    assert e.value.status == kvattn.KVATTN_ERR_TIMEOUT
+    kvattn.kvattn_tail_wait(wt.ctx, 60000)
+    torch.cuda.synchronize()
+    wo, wl = oracle.decode_f16(q, k, v, [N])
+    assert_close(out.view(1, *out.shape), lse.view(1, -1), wo, wl)
+    wt.close()
