@@ -91,9 +91,15 @@ def test_host_wait_times_out_then_completes(kvattn):
     k_tail = torch.from_numpy(k[:n_tail]).pin_memory()
     v_tail = torch.from_numpy(v[:n_tail]).pin_memory()
     wt = kvattn.WindowTail()
+    qd, kw, vw = dev(q[0]), dev(k[n_tail:]), dev(v[n_tail:])
+    ws = wt.workspace(H, Hk, D, n_win, n_tail, 128, 256, 64)
+    out = torch.empty((H, D), dtype=torch.float32, device="cuda")
+    lse = torch.empty((H,), dtype=torch.float32, device="cuda")
+    copy_stream = torch.cuda.Stream()
+    torch.cuda.synchronize()
     torch.cuda._sleep(400_000_000)   # a bounded busy kernel ahead of the decode on this stream
-    out, lse = wt(dev(q[0]), dev(k[n_tail:]), dev(v[n_tail:]), k_tail, v_tail, split=128,
-                  tile_cells=256, tail_split=64, copy_stream=torch.cuda.Stream())
+    wt(qd, kw, vw, k_tail, v_tail, split=128, tile_cells=256, tail_split=64, out=out, lse=lse, ws=ws,
+       copy_stream=copy_stream)
     with pytest.raises(kvattn.KvattnError) as e:
         kvattn.kvattn_tail_wait(wt.ctx, 1)
     assert e.value.status == kvattn.KVATTN_ERR_TIMEOUT
