@@ -438,17 +438,17 @@ def run_ours(args):
     value = step_bytes * world / (ms * 1e-3) / 1e9
 
     # the dominant kernel alone: split-decode launches bracketed by events
-    evs = []
-    for rep in range(max(1, args.kernel_reps)):
-        for l in range(args.layers):
-            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            a.record(stream)
-            data.call_partials(K, l, stream)
-            b.record(stream)
-            evs.append((a, b))
+    # average launch duration: back-to-back launches on the stream, events at both ends
+    for l in range(args.layers):
+        data.call_partials(K, l, stream)
+    n_launch = max(1, args.kernel_reps) * args.layers
+    ka, kb = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ka.record(stream)
+    for i in range(n_launch):
+        data.call_partials(K, i % args.layers, stream)
+    kb.record(stream)
     torch.cuda.synchronize()
-    kern_ms = float(np.mean([a.elapsed_time(b) for a, b in evs[args.layers:]] or
-                            [a.elapsed_time(b) for a, b in evs]))
+    kern_ms = ka.elapsed_time(kb) / n_launch
     achieved = data.bytes_per_op / (kern_ms * 1e-3) / 1e9
     traffic = profiled_traffic("split_decode_f16_qwen3_8b_layer.md")
 
@@ -554,7 +554,7 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--layers", type=int, default=36)
     ap.add_argument("--soak", type=float, default=1.0, help="seconds of untimed load before timing")
-    ap.add_argument("--kernel-reps", type=int, default=5)
+    ap.add_argument("--kernel-reps", type=int, default=20)
     ap.add_argument("--eager", action="store_true", help="launch each call instead of a CUDA graph")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-workloads", action="store_true")

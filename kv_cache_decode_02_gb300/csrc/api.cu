@@ -85,6 +85,38 @@ int pick_stages(int kv_type, int head_dim, int64_t grid_ctas) {
 
 int cuda_status(cudaError_t e) { return e == cudaSuccess ? KVATTN_OK : KVATTN_ERR_CUDA; }
 
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn tensor_map_encoder() {
+    static std::once_flag once;
+    static EncodeTiledFn fn = nullptr;
+    std::call_once(once, [] {
+        void* ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(ptr);
+    });
+    return fn;
+}
+
+bool use_tma_env() {
+    static const bool on = env_int("KVATTN_TMA", 1) != 0;
+    return on;
+}
+
+// Tensor maps of the K and V caches for the TMA path of the split-decode kernel.
+void set_kv_maps(SplitDecodeParams& p, int kv_type, int64_t cells, int n_head_kv, int head_dim) {
+    p.use_tma = 0;
+    if (!use_tma_env()) return;
+    if (encode_kv_tensor_map(&p.tmap_k, p.k, kv_type, cells, n_head_kv, head_dim) &&
+        encode_kv_tensor_map(&p.tmap_v, p.v, kv_type, cells, n_head_kv, head_dim))
+        p.use_tma = 1;
+}
+
 // Failure-detection test hook (host-side switch, read on every call): with
 // KVATTN_DEBUG_STALL_TX=<bytes> the first tile of every split expects that many extra
 // bytes that no copy delivers, so its pipeline wait runs out after KVATTN_DEBUG_WAIT_MS
@@ -119,6 +151,23 @@ int check_shape(const DecodeShape& s) {
 }
 
 }  // namespace
+
+bool kvattn::encode_kv_tensor_map(CUtensorMap* map, const void* base, int kv_type, int64_t cells,
+                                  int n_head_kv, int head_dim) {
+    EncodeTiledFn enc = tensor_map_encoder();
+    if (enc == nullptr || base == nullptr || cells < 1 || !aligned(base, 16)) return false;
+    const bool f16 = kv_type == KVATTN_KV_F16;
+    const cuuint64_t row_bytes = (cuuint64_t)head_dim * (f16 ? 2 : 1);
+    const cuuint64_t dims[3] = {(cuuint64_t)head_dim, (cuuint64_t)n_head_kv, (cuuint64_t)cells};
+    const cuuint64_t strides[2] = {row_bytes, row_bytes * (cuuint64_t)n_head_kv};
+    const cuuint32_t box[3] = {f16 ? 64u : 128u, 1u, (cuuint32_t)kTileCells};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    const CUresult r = enc(map, f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8, 3,
+                           const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                           CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
 
 struct kvattn_tail_ctx {
     cudaEvent_t copied[2];
@@ -254,6 +303,7 @@ int decode_impl(const void* q, const void* k_cache, const void* v_cache, const v
         p.n_stages = pick_stages(kv_type, head_dim, (int64_t)n_split * n_head_kv * n_seq);
         p.scale_log2 = (float)((double)scale * 1.4426950408889634074);
         apply_debug_hooks(p);
+        set_kv_maps(p, kv_type, cell_plan != nullptr ? n_cells : n_cells * (int64_t)n_seq, n_head_kv, head_dim);
         cudaError_t e = launch_split_decode(p, kv_type, head_dim, grid, s, pdl);
         if (e != cudaSuccess) return KVATTN_ERR_CUDA;
     }
@@ -477,6 +527,7 @@ int kvattn_decode_window_tail(kvattn_tail_ctx* ctx, const void* q, const void* k
         p.part_base = 0;
         const dim3 grid((unsigned)L.n_split_win, (unsigned)n_head_kv, 1);
         p.n_stages = pick_stages(KVATTN_KV_F16, head_dim, (int64_t)L.n_split_win * n_head_kv);
+        set_kv_maps(p, KVATTN_KV_F16, n_win, n_head_kv, head_dim);
         if (launch_split_decode(p, KVATTN_KV_F16, head_dim, grid, cs, pdl) != cudaSuccess)
             return KVATTN_ERR_CUDA;
     }
@@ -484,6 +535,13 @@ int kvattn_decode_window_tail(kvattn_tail_ctx* ctx, const void* q, const void* k
     // tail: tile t -> staging slot t % 2 on the copy stream, decoded on the compute stream
     const size_t row_bytes = (size_t)n_head_kv * head_dim * 2;
     const int tile_stages = pick_stages(KVATTN_KV_F16, head_dim, L.splits_per_tile * n_head_kv);
+    SplitDecodeParams slot_params[2];
+    for (int sl = 0; sl < 2; ++sl) {
+        slot_params[sl] = p;
+        slot_params[sl].k = wsb + L.stage_off[sl][0];
+        slot_params[sl].v = wsb + L.stage_off[sl][1];
+        set_kv_maps(slot_params[sl], KVATTN_KV_F16, tile_cells, n_head_kv, head_dim);
+    }
     for (int64_t t = 0; t < L.n_tiles; ++t) {
         const int slot = (int)(t & 1);
         const int64_t c0 = t * tile_cells;
@@ -502,16 +560,15 @@ int kvattn_decode_window_tail(kvattn_tail_ctx* ctx, const void* q, const void* k
             return KVATTN_ERR_CUDA;
         if (cudaEventRecord(ctx->copied[slot], xs) != cudaSuccess) return KVATTN_ERR_CUDA;
         if (cudaStreamWaitEvent(cs, ctx->copied[slot], 0) != cudaSuccess) return KVATTN_ERR_CUDA;
-        p.k = dk;
-        p.v = dv;
-        p.n_cells = len;
-        p.max_len = tile_cells;
-        p.fixed_len = len;
-        p.split = tail_split;
-        p.part_base = L.n_split_win + t * L.splits_per_tile;
-        p.n_stages = tile_stages;
+        SplitDecodeParams& tp = slot_params[slot];
+        tp.n_cells = len;
+        tp.max_len = tile_cells;
+        tp.fixed_len = len;
+        tp.split = tail_split;
+        tp.part_base = L.n_split_win + t * L.splits_per_tile;
+        tp.n_stages = tile_stages;
         const dim3 grid((unsigned)L.splits_per_tile, (unsigned)n_head_kv, 1);
-        if (launch_split_decode(p, KVATTN_KV_F16, head_dim, grid, cs, false) != cudaSuccess)
+        if (launch_split_decode(tp, KVATTN_KV_F16, head_dim, grid, cs, false) != cudaSuccess)
             return KVATTN_ERR_CUDA;
         if (cudaEventRecord(ctx->consumed[slot], cs) != cudaSuccess) return KVATTN_ERR_CUDA;
     }

@@ -3,6 +3,7 @@
 
 #include <cstddef>
 #include <cstdint>
+#include <cuda.h>  // CUtensorMap (type only; the encoder is fetched through the runtime)
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
@@ -40,6 +41,8 @@ inline DecodeWsLayout decode_ws_layout(int n_seq, int n_head, int head_dim, int6
 // Kernel parameter blocks.
 // ---------------------------------------------------------------------------------------
 struct SplitDecodeParams {
+    CUtensorMap tmap_k;       // 3-D {row elements, KV heads, cells} views of the caches for
+    CUtensorMap tmap_v;       // the TMA path (valid when use_tma != 0)
     const __half* q;          // [S][H][D]
     const void* k;            // [cells][Hk][D] (f16 or int8)
     const void* v;
@@ -61,8 +64,15 @@ struct SplitDecodeParams {
     uint32_t stall_tx;        // test hook: extra bytes expected on the first tile (never arrive)
     int n_seq, n_head, n_head_kv, group, split;
     int n_stages;
+    int use_tma;              // tiles that are one physical run load through tmap_k/tmap_v
     float scale_log2;         // scale * log2(e)
 };
+
+// Fill a 3-D tensor map {row elements, n_head_kv, cells} over a cell-major cache with
+// 32-cell x 128-byte boxes and the 128-byte swizzle.  Returns false if the driver's
+// encoder is unavailable or rejects the geometry (the caller then loads per cell).
+bool encode_kv_tensor_map(CUtensorMap* map, const void* base, int kv_type, int64_t cells,
+                          int n_head_kv, int head_dim);
 
 struct MergeParams {
     const float* part_o;      // parts: o[(base + p) * row_stride_parts ...]

@@ -4,10 +4,13 @@
 // decode op's LSE channel).  For one output row:
 //     M = max_p LSE_p,  w_p = exp(LSE_p - M),
 //     O = sum_p w_p O_p / sum_p w_p,  LSE = M + ln sum_p w_p.
-// Parts with LSE = -inf carry no cells; they are skipped and their O is never read.
+// Parts with LSE = -inf carry no cells; they get weight 0 and their O is never read.
 //
-// One CTA of 8 warps per row; warp w takes parts w, w+8, ...; each lane owns float4
-// chunks of head_dim, so every part's O row is read with coalesced 16-byte loads.
+// One CTA of 8 warps per row.  Latency, not bandwidth, bounds this kernel (a row has a
+// few KB to a few MB of partials sitting in L2), so it avoids dependent load chains:
+// pass 1 loads every LSE of the row in parallel and reduces the maximum; pass 2 turns them
+// into weights in shared memory; pass 3 has warp w sum parts w, w+8, ... with each lane
+// owning float4 chunks of head_dim, the loads of several parts issued back to back.
 #include <cmath>
 
 #include "kvattn_internal.cuh"
@@ -17,11 +20,13 @@ namespace kvattn {
 namespace {
 
 constexpr int kMergeWarps = 8;
-constexpr int kMaxChunks = 8;  // head_dim <= 1024
+constexpr int kMergeThreads = kMergeWarps * 32;
+constexpr int kMaxChunks = 8;      // head_dim <= 1024: float4 chunks per lane
+constexpr int kWeightCache = 4096; // parts whose weights stay in shared memory
 
-__global__ void __launch_bounds__(kMergeWarps * 32) merge_kernel(const MergeParams p) {
-    __shared__ float red_m[kMergeWarps];
-    __shared__ float red_w[kMergeWarps];
+__global__ void __launch_bounds__(kMergeThreads) merge_kernel(const MergeParams p) {
+    __shared__ float red[kMergeWarps];
+    __shared__ float wts[kWeightCache];
     extern __shared__ float4 acc_smem[];  // [warps][head_dim / 4]
 
     pdl_wait();
@@ -45,54 +50,92 @@ __global__ void __launch_bounds__(kMergeWarps * 32) merge_kernel(const MergePara
     const int64_t lse_stride = p.n_rows;
     const int64_t o_stride = (int64_t)p.n_rows * p.head_dim;
 
-    // pass 1: the row maximum over the parts
+    // pass 1: maximum LSE (all loads independent)
     float m = -INFINITY;
-    for (int64_t q = warp * 32 + lane; q < n_parts; q += kMergeWarps * 32) m = fmaxf(m, lse_base[q * lse_stride]);
+    for (int64_t q = threadIdx.x; q < n_parts; q += kMergeThreads) {
+        const float l = __ldg(lse_base + q * lse_stride);
+        if (q < kWeightCache) wts[q] = l;
+        m = fmaxf(m, l);
+    }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-    if (lane == 0) red_m[warp] = m;
+    if (lane == 0) red[warp] = m;
     __syncthreads();
-    float M = red_m[0];
+    float M = red[0];
 #pragma unroll
-    for (int w = 1; w < kMergeWarps; ++w) M = fmaxf(M, red_m[w]);
+    for (int w = 1; w < kMergeWarps; ++w) M = fmaxf(M, red[w]);
+    __syncthreads();
 
-    // pass 2: weighted sums
+    // pass 2: weights exp(LSE_p - M) (0 for empty parts) and their sum
+    float wsum = 0.f;
+    if (M != -INFINITY) {
+        for (int64_t q = threadIdx.x; q < n_parts; q += kMergeThreads) {
+            const float l = q < kWeightCache ? wts[q] : __ldg(lse_base + q * lse_stride);
+            const float w = (l == -INFINITY) ? 0.f : __expf(l - M);
+            if (q < kWeightCache) wts[q] = w;
+            wsum += w;
+        }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) wsum += __shfl_xor_sync(0xffffffffu, wsum, o);
+    if (lane == 0) red[warp] = wsum;
+    __syncthreads();
+    float W = 0.f;
+#pragma unroll
+    for (int w = 0; w < kMergeWarps; ++w) W += red[w];
+
+    // pass 3: weighted sum of the O rows
     float4 acc[kMaxChunks];
 #pragma unroll
     for (int c = 0; c < kMaxChunks; ++c) acc[c] = make_float4(0.f, 0.f, 0.f, 0.f);
-    float wsum = 0.f;
-    if (M != -INFINITY) {
-        for (int64_t q = warp; q < n_parts; q += kMergeWarps) {
-            const float l = lse_base[q * lse_stride];
-            if (l == -INFINITY) continue;
-            const float w = __expf(l - M);
-            wsum += w;
-            const float4* src = reinterpret_cast<const float4*>(o_base + q * o_stride);
+    if (W > 0.f) {
+        constexpr int kUnroll = 4;
+        for (int64_t q0 = warp; q0 < n_parts; q0 += kMergeWarps * kUnroll) {
+            float w[kUnroll];
+#pragma unroll
+            for (int u = 0; u < kUnroll; ++u) {
+                const int64_t q = q0 + (int64_t)u * kMergeWarps;
+                float wq = 0.f;
+                if (q < n_parts) {
+                    if (q < kWeightCache) {
+                        wq = wts[q];
+                    } else {
+                        const float l = __ldg(lse_base + q * lse_stride);
+                        wq = (l == -INFINITY) ? 0.f : __expf(l - M);
+                    }
+                }
+                w[u] = wq;
+            }
 #pragma unroll
             for (int c = 0; c < kMaxChunks; ++c) {
                 const int ci = lane + 32 * c;
                 if (ci < chunks) {
-                    const float4 v = __ldg(src + ci);
-                    acc[c].x = fmaf(w, v.x, acc[c].x);
-                    acc[c].y = fmaf(w, v.y, acc[c].y);
-                    acc[c].z = fmaf(w, v.z, acc[c].z);
-                    acc[c].w = fmaf(w, v.w, acc[c].w);
+                    float4 v[kUnroll];
+#pragma unroll
+                    for (int u = 0; u < kUnroll; ++u) {
+                        const int64_t q = q0 + (int64_t)u * kMergeWarps;
+                        v[u] = w[u] != 0.f ? __ldg(reinterpret_cast<const float4*>(o_base + q * o_stride) + ci)
+                                           : make_float4(0.f, 0.f, 0.f, 0.f);
+                    }
+#pragma unroll
+                    for (int u = 0; u < kUnroll; ++u) {
+                        acc[c].x = fmaf(w[u], v[u].x, acc[c].x);
+                        acc[c].y = fmaf(w[u], v[u].y, acc[c].y);
+                        acc[c].z = fmaf(w[u], v[u].z, acc[c].z);
+                        acc[c].w = fmaf(w[u], v[u].w, acc[c].w);
+                    }
                 }
             }
         }
     }
-    if (lane == 0) red_w[warp] = wsum;
 #pragma unroll
     for (int c = 0; c < kMaxChunks; ++c) {
         const int ci = lane + 32 * c;
         if (ci < chunks) acc_smem[warp * chunks + ci] = acc[c];
     }
     __syncthreads();
-    float W = 0.f;
-#pragma unroll
-    for (int w = 0; w < kMergeWarps; ++w) W += red_w[w];
     float4* out = reinterpret_cast<float4*>(p.out + (int64_t)row * p.head_dim);
-    for (int ci = threadIdx.x; ci < chunks; ci += kMergeWarps * 32) {
+    for (int ci = threadIdx.x; ci < chunks; ci += kMergeThreads) {
         float4 t = make_float4(0.f, 0.f, 0.f, 0.f);
         if (W > 0.f) {
 #pragma unroll
@@ -122,7 +165,7 @@ cudaError_t launch_merge(const MergeParams& p, cudaStream_t stream, bool pdl) {
     if (rows == 0) return cudaSuccess;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(rows, 1, 1);
-    cfg.blockDim = dim3(kMergeWarps * 32, 1, 1);
+    cfg.blockDim = dim3(kMergeThreads, 1, 1);
     cfg.dynamicSmemBytes = kMergeWarps * p.head_dim * sizeof(float);
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
