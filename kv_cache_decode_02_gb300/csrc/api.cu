@@ -61,8 +61,10 @@ int occupancy(int kv_type, int head_dim, int n_stages) {
 }
 
 // Pipeline depth per CTA ("launch bounds and occupancy-aware selection", KVARN item 6):
-// the deepest ring whose resident capacity still holds the whole grid in one wave; for
-// grids larger than one wave, the deepest ring that keeps three CTAs on every SM.
+// the deepest ring (3 stages or more) whose resident capacity still holds the whole grid
+// in one wave; grids larger than one wave take 2 stages, which keeps the most CTAs per SM
+// (measured on GB300: Q8_0 at 131072 cells 111 -> 91 us, a 4-sequence plan 190 -> 141 us
+// going from the deepest ring to 2 stages).
 int pick_stages(int kv_type, int head_dim, int64_t grid_ctas) {
     const int forced = env_int("KVATTN_STAGES", 0);
     const int max_st = split_decode_max_stages();
@@ -71,14 +73,10 @@ int pick_stages(int kv_type, int head_dim, int64_t grid_ctas) {
     const int limit = split_decode_max_smem();
     if (forced >= 2 && forced <= max_st && hdr + forced * stage <= limit) return forced;
     const int64_t n_sm = sm_count();
-    for (int st = max_st; st >= 2; --st) {
+    for (int st = max_st; st >= 3; --st) {
         if (hdr + st * stage > limit) continue;
         const int b = occupancy(kv_type, head_dim, st);
         if (b > 0 && (int64_t)b * n_sm >= grid_ctas) return st;
-    }
-    for (int st = max_st; st >= 2; --st) {
-        if (hdr + st * stage > limit) continue;
-        if (occupancy(kv_type, head_dim, st) >= 3) return st;
     }
     return 2;
 }
@@ -293,6 +291,7 @@ int decode_impl(const void* q, const void* k_cache, const void* v_cache, const v
         p.max_len = max_len;
         p.n_split = n_split;
         p.part_base = 0;
+        p.part_stride = n_split;
         p.fixed_len = 0;
         p.n_seq = n_seq;
         p.n_head = n_head;
@@ -300,7 +299,7 @@ int decode_impl(const void* q, const void* k_cache, const void* v_cache, const v
         p.group = n_head / n_head_kv;
         p.split = split;
         const dim3 grid((unsigned)n_split, (unsigned)n_head_kv, (unsigned)n_seq);
-        p.n_stages = pick_stages(kv_type, head_dim, (int64_t)n_split * n_head_kv * n_seq);
+        p.n_stages = pick_stages(kv_type, head_dim, n_split * n_head_kv * n_seq);
         p.scale_log2 = (float)((double)scale * 1.4426950408889634074);
         apply_debug_hooks(p);
         set_kv_maps(p, kv_type, cell_plan != nullptr ? n_cells : n_cells * (int64_t)n_seq, n_head_kv, head_dim);
@@ -321,6 +320,7 @@ int decode_impl(const void* q, const void* k_cache, const void* v_cache, const v
     m.n_rows = n_head;
     m.head_dim = head_dim;
     m.split = split;
+    m.all_written = 1;
     return cuda_status(launch_merge(m, s, pdl && n_split > 0));
 }
 
@@ -504,6 +504,7 @@ int kvattn_decode_window_tail(kvattn_tail_ctx* ctx, const void* q, const void* k
     p.seq_lens = nullptr;
     p.desc = nullptr;
     p.n_split = L.n_parts;
+    p.part_stride = L.n_parts;
     p.n_seq = 1;
     p.n_head = n_head;
     p.n_head_kv = n_head_kv;
@@ -584,6 +585,7 @@ int kvattn_decode_window_tail(kvattn_tail_ctx* ctx, const void* q, const void* k
     m.n_rows = n_head;
     m.head_dim = head_dim;
     m.split = 1;
+    m.all_written = 1;
     if (launch_merge(m, cs, pdl) != cudaSuccess) return KVATTN_ERR_CUDA;
     if (cudaEventRecord(ctx->done, cs) != cudaSuccess) return KVATTN_ERR_CUDA;
     ctx->pending = true;

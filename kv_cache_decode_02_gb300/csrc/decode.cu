@@ -436,15 +436,16 @@ __global__ void __launch_bounds__(kThreads) split_decode_kernel(const __grid_con
     pdl_wait();
 
     // The split's range of plan entries / cells.
+    // (the length and the descriptor are independent loads: issue both before using either)
     const int64_t cap = p.plan ? p.plan_stride : p.n_cells;
     int64_t L = p.seq_lens != nullptr ? (int64_t)p.seq_lens[s] : p.fixed_len;
+    const int desc_valid = p.desc != nullptr ? p.desc[(int64_t)s * p.n_split + split_idx].x : 1;
     L = L < 0 ? 0 : L;
     L = L < p.max_len ? L : p.max_len;
     L = L < cap ? L : cap;
     const int64_t i0 = (int64_t)split_idx * p.split;
     const int64_t i1 = (i0 + p.split < L) ? i0 + p.split : L;
-    bool empty = i0 >= i1;
-    if (!empty && p.desc != nullptr) empty = p.desc[(int64_t)s * p.n_split + split_idx].x == 0;
+    const bool empty = i0 >= i1 || desc_valid == 0;
     const int n_tiles = empty ? 0 : (int)((i1 - i0 + kTileCells - 1) / kTileCells);
 
     const int gq = lane >> 2;
@@ -458,7 +459,19 @@ __global__ void __launch_bounds__(kThreads) split_decode_kernel(const __grid_con
         // ------------------------------- producer -------------------------------
         const int64_t Hk = p.n_head_kv;
         bool bad = false;
+        // plan entries of this lane's cell, prefetched four tiles ahead
+        const int32_t* prow = p.plan != nullptr ? p.plan + (int64_t)s * p.plan_stride : nullptr;
+        auto plan_entry = [&](int tt) -> int32_t {
+            const int64_t i = i0 + (int64_t)tt * kTileCells + lane;
+            return (prow != nullptr && tt < n_tiles && i < i1) ? __ldg(prow + i) : -1;
+        };
+        int32_t e0 = plan_entry(0), e1 = plan_entry(1), e2 = plan_entry(2), e3 = plan_entry(3);
         for (int t = 0; t < n_tiles; ++t) {
+            const int32_t e = e0;
+            e0 = e1;
+            e1 = e2;
+            e2 = e3;
+            e3 = plan_entry(t + 4);
             const int st = t % n_stages;
             const int use = t / n_stages;
             if (use > 0) {
@@ -473,7 +486,6 @@ __global__ void __launch_bounds__(kThreads) split_decode_kernel(const __grid_con
             int64_t cell = 0;
             if (valid) {
                 if (p.plan != nullptr) {
-                    const int32_t e = p.plan[(int64_t)s * p.plan_stride + i];
                     if (e < -1 || (int64_t)e >= p.n_cells) {
                         bad = true;
                         valid = false;
@@ -650,13 +662,17 @@ __global__ void __launch_bounds__(kThreads) split_decode_kernel(const __grid_con
         l_run += __shfl_xor_sync(0xffffffffu, l_run, 2);
     }
 
-    // ------------------------- merge the consumer warps -------------------------
+    // ------------------------- combine the consumer warps -------------------------
     __syncthreads();
     const bool aborted = *abort_flag != 0;
-    float* cm = reinterpret_cast<float*>(stages);       // [warps][8] running max (log2)
+    const bool have = !aborted && n_tiles > 0;
+    float* cm = reinterpret_cast<float*>(stages);       // [warps][8] running max (log2 units)
     float* cl = cm + kConsumerWarps * 8;                // [warps][8] running sum
-    float* co = cl + kConsumerWarps * 8;                // [warps][8][D + 4] unnormalised O
-    if (!aborted && n_tiles > 0 && warp < kConsumerWarps) {
+    float* xm = cl + kConsumerWarps * 8;                // [8] this CTA's max (log2), -inf: no cell
+    float* xl = xm + 8;                                 // [8] this CTA's sum
+    float* co = xl + 8;                                 // [warps][8][D + 4]; warp 0's rows end up
+                                                        // holding the CTA's unnormalised O
+    if (have && warp < kConsumerWarps) {
         if (tq == 0) {
             cm[warp * 8 + gq] = m_run;
             cl[warp * 8 + gq] = l_run;
@@ -673,39 +689,54 @@ __global__ void __launch_bounds__(kThreads) split_decode_kernel(const __grid_con
         }
     }
     __syncthreads();
+    const int G_rows = p.group;
+    if (threadIdx.x < 8) {
+        const int r = threadIdx.x;
+        float M = -INFINITY, den = 0.f;
+        if (have && r < G_rows) {
+#pragma unroll
+            for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, cm[w * 8 + r]);
+            if (M != -INFINITY) {
+#pragma unroll
+                for (int w = 0; w < kConsumerWarps; ++w)
+                    if (cm[w * 8 + r] != -INFINITY) den = fmaf(fast_exp2(cm[w * 8 + r] - M), cl[w * 8 + r], den);
+            }
+        }
+        xm[r] = den > 0.f ? M : -INFINITY;
+        xl[r] = den;
+    }
+    if (have) {
+        for (int idx = threadIdx.x; idx < G_rows * D; idx += kThreads) {
+            const int r = idx / D;
+            const int d = idx - r * D;
+            float M = -INFINITY;
+#pragma unroll
+            for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, cm[w * 8 + r]);
+            float o = 0.f;
+            if (M != -INFINITY) {
+#pragma unroll
+                for (int w = 0; w < kConsumerWarps; ++w)
+                    if (cm[w * 8 + r] != -INFINITY)
+                        o = fmaf(fast_exp2(cm[w * 8 + r] - M), co[(w * 8 + r) * G::kOStride + d], o);
+            }
+            co[r * G::kOStride + d] = o;  // warp 0's slot: read above by this thread only
+        }
+    }
+    __syncthreads();
+
+    constexpr float kLn2 = 0.69314718055994530942f;
+    const int H = p.n_head;
     if (aborted) {
         if (threadIdx.x == 0) atomicOr(p.status, KVATTN_DEVICE_WAIT_TIMEOUT);
     } else {
-        const int64_t part = (int64_t)s * p.n_split + p.part_base + split_idx;
-        const int H = p.n_head;
-        for (int idx = threadIdx.x; idx < p.group * D; idx += kThreads) {
+        const int64_t part = (int64_t)s * p.part_stride + p.part_base + split_idx;
+        for (int idx = threadIdx.x; idx < G_rows * D; idx += kThreads) {
             const int r = idx / D;
             const int d = idx - r * D;
-            const int h = g * p.group + r;
-            float o = 0.f, lse = -INFINITY;
-            if (n_tiles > 0) {
-                float M = -INFINITY;
-#pragma unroll
-                for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, cm[w * 8 + r]);
-                float num = 0.f, den = 0.f;
-                if (M != -INFINITY) {
-#pragma unroll
-                    for (int w = 0; w < kConsumerWarps; ++w) {
-                        const float mw = cm[w * 8 + r];
-                        if (mw != -INFINITY) {
-                            const float sc = fast_exp2(mw - M);
-                            num = fmaf(sc, co[(w * 8 + r) * G::kOStride + d], num);
-                            den = fmaf(sc, cl[w * 8 + r], den);
-                        }
-                    }
-                }
-                if (den > 0.f) {
-                    o = num / den;
-                    lse = (M + fast_log2(den)) * 0.69314718055994530942f;
-                }
-            }
-            p.part_o[(part * H + h) * D + d] = o;
-            if (d == 0) p.part_lse[part * H + h] = lse;
+            const int h = g * G_rows + r;
+            const bool ok = xm[r] != -INFINITY;
+            p.part_o[(part * H + h) * D + d] = ok ? co[r * G::kOStride + d] / xl[r] : 0.f;
+            if (d == 0) p.part_lse[part * H + h] = ok ? (xm[r] + fast_log2(xl[r])) * kLn2 : -INFINITY;
         }
     }
     pdl_launch_dependents();

@@ -23,6 +23,7 @@ struct DecodeWsLayout {
     size_t desc_off, lse_off, o_off, total;
 };
 
+// status word | descriptors | partial LSE | partial O
 inline DecodeWsLayout decode_ws_layout(int n_seq, int n_head, int head_dim, int64_t n_split) {
     DecodeWsLayout L;
     size_t off = kStatusBytes;
@@ -57,7 +58,8 @@ struct SplitDecodeParams {
     int64_t n_cells;
     int64_t plan_stride;
     int64_t max_len;
-    int64_t n_split;          // splits per sequence (partial stride)
+    int64_t n_split;          // splits per sequence (descriptor stride)
+    int64_t part_stride;      // partial slots per sequence
     int64_t part_base;        // first partial index written (window + tail packs several calls)
     int64_t fixed_len;
     uint64_t wait_limit_ns;   // bound on every pipeline wait
@@ -80,6 +82,8 @@ struct MergeParams {
     float* out;
     float* lse;
     const int32_t* seq_lens;  // nullable: per-sequence part count = ceil(clamp(len)/split)
+    int all_written;          // every part's O was written (0 for empty parts): read O and LSE
+                              // in one round instead of gating O on the LSE
     int64_t n_parts;          // parts per sequence (fixed count when seq_lens == NULL)
     int64_t max_len;
     int64_t len_cap;          // clamp for seq_lens (n_cells or plan_stride)

@@ -7,10 +7,13 @@
 // Parts with LSE = -inf carry no cells; they get weight 0 and their O is never read.
 //
 // One CTA of 8 warps per row.  Latency, not bandwidth, bounds this kernel (a row has a
-// few KB to a few MB of partials sitting in L2), so it avoids dependent load chains:
-// pass 1 loads every LSE of the row in parallel and reduces the maximum; pass 2 turns them
-// into weights in shared memory; pass 3 has warp w sum parts w, w+8, ... with each lane
-// owning float4 chunks of head_dim, the loads of several parts issued back to back.
+// few KB to a few MB of partials sitting in L2), so it avoids dependent load chains.
+//  * partials written by the decode kernels (every O written, 0 for empty parts): warp w
+//    reads parts w, w+8, ... eight at a time, LSE and O in the same round, and keeps a
+//    running (max, sum, O); the warps are then combined with the same rescaling.
+//  * caller partials (kvattn_merge: an empty part's O may be anything): pass 1 loads every
+//    LSE in parallel and reduces the maximum, pass 2 turns them into weights in shared
+//    memory, pass 3 sums the O rows of non-empty parts only, several loads in flight.
 #include <cmath>
 
 #include "kvattn_internal.cuh"
@@ -21,7 +24,7 @@ namespace {
 
 constexpr int kMergeWarps = 8;
 constexpr int kMergeThreads = kMergeWarps * 32;
-constexpr int kMaxChunks = 8;      // head_dim <= 1024: float4 chunks per lane
+constexpr int kMaxChunks = 8;      // head_dim <= 1024: float4 chunks per lane (public merge)
 constexpr int kWeightCache = 4096; // parts whose weights stay in shared memory
 
 __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const MergeParams p) {
@@ -49,6 +52,107 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const MergeParams 
     const float* o_base = p.part_o + ((int64_t)s * p.n_parts * p.n_rows + h) * p.head_dim;
     const int64_t lse_stride = p.n_rows;
     const int64_t o_stride = (int64_t)p.n_rows * p.head_dim;
+
+    if (p.all_written) {
+        // One round of loads per batch: warp w reads parts w, w+8, ... eight at a time, LSE
+        // and O together (the decode path writes O = 0 for empty parts), and folds them into
+        // a running (max, sum, O) with the same rescaling the decode kernel uses.
+        constexpr int kBatch = 8;
+        float mw = -INFINITY, sw = 0.f;
+        float4 acc[kMaxChunks];
+#pragma unroll
+        for (int c = 0; c < kMaxChunks; ++c) acc[c] = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int64_t q0 = warp; q0 < n_parts; q0 += (int64_t)kMergeWarps * kBatch) {
+            float l[kBatch];
+#pragma unroll
+            for (int u = 0; u < kBatch; ++u) {
+                const int64_t q = q0 + (int64_t)u * kMergeWarps;
+                l[u] = q < n_parts ? __ldg(lse_base + q * lse_stride) : -INFINITY;
+            }
+            float4 v[kBatch][2];
+#pragma unroll
+            for (int u = 0; u < kBatch; ++u) {
+                const int64_t q = q0 + (int64_t)u * kMergeWarps;
+#pragma unroll
+                for (int c = 0; c < 2; ++c) {
+                    const int ci = lane + 32 * c;
+                    v[u][c] = (q < n_parts && ci < chunks)
+                                  ? __ldg(reinterpret_cast<const float4*>(o_base + q * o_stride) + ci)
+                                  : make_float4(0.f, 0.f, 0.f, 0.f);
+                }
+            }
+            float bm = -INFINITY;
+#pragma unroll
+            for (int u = 0; u < kBatch; ++u) bm = fmaxf(bm, l[u]);
+            const float nm = fmaxf(mw, bm);
+            if (nm == -INFINITY) continue;
+            const float keep = __expf(mw - nm);  // 0 when nothing was accumulated yet
+            sw *= keep;
+#pragma unroll
+            for (int c = 0; c < 2; ++c) {
+                acc[c].x *= keep;
+                acc[c].y *= keep;
+                acc[c].z *= keep;
+                acc[c].w *= keep;
+            }
+#pragma unroll
+            for (int u = 0; u < kBatch; ++u) {
+                const float w = l[u] == -INFINITY ? 0.f : __expf(l[u] - nm);
+                sw += w;
+#pragma unroll
+                for (int c = 0; c < 2; ++c) {
+                    acc[c].x = fmaf(w, v[u][c].x, acc[c].x);
+                    acc[c].y = fmaf(w, v[u][c].y, acc[c].y);
+                    acc[c].z = fmaf(w, v[u][c].z, acc[c].z);
+                    acc[c].w = fmaf(w, v[u][c].w, acc[c].w);
+                }
+            }
+            mw = nm;
+        }
+        if (lane == 0) {
+            red[warp] = mw;
+            wts[warp] = sw;
+        }
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+            const int ci = lane + 32 * c;
+            if (ci < chunks) acc_smem[warp * chunks + ci] = acc[c];
+        }
+        __syncthreads();
+        float M = -INFINITY;
+#pragma unroll
+        for (int w = 0; w < kMergeWarps; ++w) M = fmaxf(M, red[w]);
+        float W = 0.f;
+        float scw[kMergeWarps];
+#pragma unroll
+        for (int w = 0; w < kMergeWarps; ++w) {
+            scw[w] = (M == -INFINITY || red[w] == -INFINITY) ? 0.f : __expf(red[w] - M);
+            W = fmaf(scw[w], wts[w], W);
+        }
+        float4* out = reinterpret_cast<float4*>(p.out + (int64_t)row * p.head_dim);
+        for (int ci = threadIdx.x; ci < chunks; ci += kMergeThreads) {
+            float4 t = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (W > 0.f) {
+#pragma unroll
+                for (int w = 0; w < kMergeWarps; ++w) {
+                    const float4 a = acc_smem[w * chunks + ci];
+                    t.x = fmaf(scw[w], a.x, t.x);
+                    t.y = fmaf(scw[w], a.y, t.y);
+                    t.z = fmaf(scw[w], a.z, t.z);
+                    t.w = fmaf(scw[w], a.w, t.w);
+                }
+                const float inv = 1.f / W;
+                t.x *= inv;
+                t.y *= inv;
+                t.z *= inv;
+                t.w *= inv;
+            }
+            out[ci] = t;
+        }
+        if (threadIdx.x == 0) p.lse[row] = (W > 0.f) ? M + __logf(W) : -INFINITY;
+        pdl_launch_dependents();
+        return;
+    }
 
     // pass 1: maximum LSE (all loads independent)
     float m = -INFINITY;
@@ -160,7 +264,9 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const MergeParams 
 
 }  // namespace
 
-cudaError_t launch_merge(const MergeParams& p, cudaStream_t stream, bool pdl) {
+cudaError_t launch_merge(const MergeParams& params, cudaStream_t stream, bool pdl) {
+    MergeParams p = params;
+    if (p.head_dim > 256) p.all_written = 0;  // the one-round path holds two float4 per lane
     const int rows = p.n_seq * p.n_rows;
     if (rows == 0) return cudaSuccess;
     cudaLaunchConfig_t cfg = {};

@@ -303,8 +303,11 @@ def test_partials_then_merge_equals_decode(kvattn):
         mo, ml = kvattn.merge(part_o[s].contiguous(), part_l[s].contiguous())
         torch.cuda.synchronize()
         assert_close(mo.view(1, H, D), ml.view(1, H), wo[s:s + 1], wl[s:s + 1])
+    # kvattn_decode combines splits in clusters before its final merge: the same values up
+    # to the order of the fp32 reductions
     do, dl = run_contiguous(kvattn, q, k, v, lens, split)
     for s in range(S):
         mo, ml = kvattn.merge(part_o[s].contiguous(), part_l[s].contiguous())
         torch.cuda.synchronize()
-        assert np.array_equal(mo.cpu().numpy(), do.cpu().numpy()[s])
+        assert np.max(np.abs(mo.cpu().numpy() - do.cpu().numpy()[s])) <= 1e-5
+        assert np.max(np.abs(ml.cpu().numpy() - dl.cpu().numpy()[s])) <= 1e-5
