@@ -179,6 +179,38 @@ int kvattn_merge(const float* partials, const float* lses, int n_parts, int n_ro
                  float* out, float* lse, void* stream);
 
 /*
+ * kvattn_decode_noalloc -- device.  kvattn_decode for callers that cannot allocate device
+ * memory.  The pages have no counterpart of this entry point; it exists for code that is
+ * not allowed to call cudaMalloc where it runs decode attention -- inside a fixed memory
+ * pool's budget, as a plugin that is handed only its inputs and outputs, or on a path that
+ * must not wait on the driver's allocator.  It allocates nothing: the caller passes the
+ * same inputs and outputs as kvattn_decode (no workspace), and the scratch lives in an
+ * array of KVATTN_NOALLOC_SCRATCH_BYTES bytes that the library keeps in device memory on
+ * every GPU that loads it, until the process exits.
+ *
+ *  Arguments, layouts and results: as kvattn_decode.
+ *  Limit: a call whose kvattn_decode_workspace_bytes(n_seq, n_head, head_dim, max_len,
+ *         split) exceeds KVATTN_NOALLOC_SCRATCH_BYTES returns KVATTN_ERR_WORKSPACE and
+ *         launches nothing; use kvattn_decode with a caller workspace for such shapes.
+ *  Set-up: the first call on a device looks up the array's device address on that device
+ *         (cudaGetSymbolAddress) and remembers it; make that first call before any stream
+ *         capture begins on the device.
+ *  Sharing: every call on a device uses the same array, which keeps the previous call's
+ *         contents (each call clears the status word it needs at zero).  Calls whose work
+ *         overlaps on the GPU -- on different streams, or from different threads without
+ *         ordering -- race on the array and give wrong results; order them on one stream.
+ *  Device-side status bits of this path are not reported.
+ * Errors: INVALID_ARG, UNSUPPORTED, WORKSPACE (before any launch); CUDA.
+ */
+#define KVATTN_NOALLOC_SCRATCH_BYTES (16u * 1024u * 1024u)
+
+int kvattn_decode_noalloc(const void* q, const void* k_cache, const void* v_cache,
+                          const void* k_scales, const void* v_scales, int kv_type, int64_t n_cells,
+                          const int32_t* cell_plan, int64_t plan_stride, const int32_t* seq_lens,
+                          int n_seq, int64_t max_len, int n_head, int n_head_kv, int head_dim,
+                          int split, float scale, float* out, float* lse, void* stream);
+
+/*
  * Window + host tail ([RKV] sections 1 and 5c: "POSITION_WINDOW keeps a resident window of
  * recent cells and streams the older tail from host RAM every decode step"; the window is
  * attended on the device and the tail streamed once, one tile ahead, and the partials are

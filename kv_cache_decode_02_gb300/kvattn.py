@@ -40,7 +40,7 @@ EXPORTED = (
     "kvattn_decode_workspace_bytes", "kvattn_decode", "kvattn_decode_partials", "kvattn_merge",
     "kvattn_tail_ctx_create",
     "kvattn_tail_ctx_destroy", "kvattn_window_tail_workspace_bytes", "kvattn_decode_window_tail",
-    "kvattn_tail_wait", "kvattn_workspace_status",
+    "kvattn_tail_wait", "kvattn_workspace_status", "kvattn_decode_noalloc",
 )
 
 _P = ctypes.c_void_p
@@ -64,6 +64,10 @@ lib.kvattn_decode.argtypes = [_P, _P, _P, _P, _P, _I, _I64, _P, _I64, _P, _I, _I
 lib.kvattn_decode.restype = _I
 lib.kvattn_decode_partials.argtypes = lib.kvattn_decode.argtypes
 lib.kvattn_decode_partials.restype = _I
+lib.kvattn_decode_noalloc.argtypes = [_P, _P, _P, _P, _P, _I, _I64, _P, _I64, _P, _I, _I64, _I, _I, _I, _I,
+                                      _F, _P, _P, _P]
+lib.kvattn_decode_noalloc.restype = _I
+KVATTN_NOALLOC_SCRATCH_BYTES = 16 * 1024 * 1024
 lib.kvattn_merge.argtypes = [_P, _P, _I, _I, _I, _P, _P, _P]
 lib.kvattn_merge.restype = _I
 lib.kvattn_tail_ctx_create.argtypes = [ctypes.POINTER(_P)]
@@ -159,6 +163,18 @@ def kvattn_decode_partials(q, k_cache, v_cache, k_scales, v_scales, kv_type, n_c
                                     scale, _ptr(part_o), _ptr(part_lse), _ptr(ws), ws_bytes,
                                     _stream(stream))
     _check(rc, "kvattn_decode_partials")
+
+
+def kvattn_decode_noalloc(q, k_cache, v_cache, k_scales, v_scales, kv_type, n_cells, cell_plan,
+                          plan_stride, seq_lens, n_seq, max_len, n_head, n_head_kv, head_dim, split, scale,
+                          out, lse, stream=None):
+    """kvattn_decode without a workspace, for callers that cannot allocate device memory:
+    the library keeps the scratch in its own fixed-size device array (see kvattn.h)."""
+    rc = lib.kvattn_decode_noalloc(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(k_scales),
+                                   _ptr(v_scales), kv_type, n_cells, _ptr(cell_plan), plan_stride,
+                                   _ptr(seq_lens), n_seq, max_len, n_head, n_head_kv, head_dim, split,
+                                   scale, _ptr(out), _ptr(lse), _stream(stream))
+    _check(rc, "kvattn_decode_noalloc")
 
 
 def kvattn_merge(partials, lses, n_parts, n_rows, head_dim, out, lse, stream=None):
