@@ -337,6 +337,19 @@ def bench_workloads(K, torch, stream, peak):
                    "host_ms_per_call": round(host_ms, 3),
                    "model_ms": round(tail_bytes / (h2d_big * 1e9) * 1e3, 3)}
     wt.close()
+    # the same window + tail, the tail read in place from pinned host memory (no staging)
+    fn = lambda: K.window_tail_direct(q, k_win, v_win, k_tail, v_tail, split=w.split, tail_split=w.tail_split,
+                                      out=out, lse=lse, ws=ws_direct, stream=stream)
+    ws_direct = torch.zeros(K.kvattn_window_tail_direct_workspace_bytes(H, Hk, D, w.n_window, n_tail, w.split,
+                                                                        w.tail_split), dtype=torch.uint8,
+                            device="cuda")
+    fn()
+    torch.cuda.synchronize()
+    ms_d = timed(fn, 5)
+    gbs_d = tail_bytes / (ms_d * 1e-3) / 1e9
+    res[w.name + "_direct"] = {"ms_per_op": round(ms_d, 3), "tail_bytes": tail_bytes, "tail_gbs": round(gbs_d, 1),
+                              "frac_of_measured_h2d": round(gbs_d / h2d_big, 3),
+                              "how": "tail rows read in place from pinned host memory by the decode kernel"}
     del flush
     return res
 

@@ -235,9 +235,14 @@ size_t kvattn_window_tail_workspace_bytes(int n_head, int n_head_kv, int head_di
  *  k_tail_host, v_tail_host  PINNED host half [n_tail][n_head_kv][head_dim] -- the older
  *             tail (cudaHostAlloc / cudaHostRegister memory).
  *  tile_cells tail cells per host-to-device tile (a positive multiple of tail_split);
- *             tiles are copied on copy_stream into two device staging slots, one tile
- *             ahead of the compute (double buffering), with events ordering each copy
- *             after the decode that last read its slot.
+ *             tiles are copied into two device staging slots, one tile ahead of the
+ *             compute (double buffering), each copy ordered after the decode that last
+ *             read its slot.  The first call with a given set of arguments records the
+ *             whole pipeline as a CUDA graph (on the context's own streams) and launches it
+ *             on compute_stream; later calls with the same arguments replay that graph, so
+ *             the host enqueues one launch instead of about three operations per tile.  A
+ *             call on a compute_stream that is itself being captured enqueues the pipeline
+ *             on compute_stream and copy_stream directly.
  *  split      cells per partial over the window; tail_split  cells per partial inside a
  *             tile.  Both positive multiples of 32.
  *  out, lse   device float [n_head][head_dim], [n_head].
@@ -253,6 +258,36 @@ int kvattn_decode_window_tail(kvattn_tail_ctx* ctx, const void* q,
                               int split, int tail_split, float scale, float* out, float* lse,
                               void* ws, size_t ws_bytes, void* compute_stream,
                               void* copy_stream);
+
+/*
+ * kvattn_decode_window_tail_direct -- device.  The same window + host tail attention
+ * ([RKV] sections 1 and 5c), but the decode kernel reads the tail's rows straight from
+ * pinned host memory with 16-byte asynchronous loads, with no staging copies and no copy
+ * stream.  Attention reads every tail byte exactly once, so reading host memory in place
+ * costs no more link traffic than copying it first ([KVN], the note that plain zero-copy
+ * lost only because a GEMM re-reads each weight tile), and it avoids the fixed per-copy
+ * cost of many 1 MiB host-to-device copies.
+ *
+ *  q, k_win, v_win, n_win, split, scale, out, lse: as kvattn_decode_window_tail.
+ *  k_tail_host, v_tail_host  pinned, device-mapped host memory (cudaHostAlloc,
+ *             torch pin_memory(), or cudaHostRegister with mapping), 16-byte aligned,
+ *             half [n_tail][n_head_kv][head_dim].
+ *  tail_split cells per partial over the tail (a positive multiple of 32).
+ *  ws         at least kvattn_window_tail_direct_workspace_bytes(...) bytes.
+ *  stream     everything runs on this stream.
+ * Errors: INVALID_ARG (including tail memory the device cannot address), UNSUPPORTED,
+ * WORKSPACE (before any launch); CUDA.
+ */
+size_t kvattn_window_tail_direct_workspace_bytes(int n_head, int n_head_kv, int head_dim,
+                                                 int64_t n_win, int64_t n_tail, int split,
+                                                 int tail_split);
+
+int kvattn_decode_window_tail_direct(const void* q, const void* k_win, const void* v_win,
+                                     int64_t n_win, const void* k_tail_host,
+                                     const void* v_tail_host, int64_t n_tail, int n_head,
+                                     int n_head_kv, int head_dim, int split, int tail_split,
+                                     float scale, float* out, float* lse, void* ws,
+                                     size_t ws_bytes, void* stream);
 
 /* Wait (host, bounded) until everything the last kvattn_decode_window_tail on this ctx
  * enqueued has finished.  Polls an event; returns TIMEOUT after timeout_ms, CUDA if the

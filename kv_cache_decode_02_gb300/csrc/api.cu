@@ -167,11 +167,31 @@ bool kvattn::encode_kv_tensor_map(CUtensorMap* map, const void* base, int kv_typ
     return r == CUDA_SUCCESS;
 }
 
+// Everything a captured window + tail graph depends on; a call with the same key replays it.
+struct TailGraphKey {
+    const void *q, *k_win, *v_win, *k_tail, *v_tail;
+    int64_t n_win, n_tail, tile_cells;
+    int n_head, n_head_kv, head_dim, split, tail_split;
+    float scale;
+    float *out, *lse;
+    void* ws;
+    size_t ws_bytes;
+    uint32_t stall_tx;
+    uint64_t wait_limit_ns;
+    int pdl, device;
+    bool operator==(const TailGraphKey& o) const { return std::memcmp(this, &o, sizeof(*this)) == 0; }
+};
+
 struct kvattn_tail_ctx {
     cudaEvent_t copied[2];
     cudaEvent_t consumed[2];
     cudaEvent_t start;
     cudaEvent_t done;
+    cudaEvent_t joined;
+    cudaStream_t cap_main;  // private streams the pipeline is recorded on
+    cudaStream_t cap_fork;
+    cudaGraphExec_t exec;
+    TailGraphKey key;
     int device;
     bool pending;
 };
@@ -385,23 +405,38 @@ int kvattn_tail_ctx_create(kvattn_tail_ctx** ctx) {
     kvattn_tail_ctx* c = new (std::nothrow) kvattn_tail_ctx();
     if (c == nullptr) return KVATTN_ERR_INVALID_ARG;
     cudaError_t e = cudaGetDevice(&c->device);
-    cudaEvent_t* evs[6] = {&c->copied[0], &c->copied[1], &c->consumed[0], &c->consumed[1], &c->start, &c->done};
-    int made = 0;
-    for (; made < 6 && e == cudaSuccess; ++made) e = cudaEventCreateWithFlags(evs[made], cudaEventDisableTiming);
+    cudaEvent_t* evs[7] = {&c->copied[0], &c->copied[1], &c->consumed[0], &c->consumed[1],
+                           &c->start,     &c->done,      &c->joined};
+    int made = 0;  // events created so far
+    for (; e == cudaSuccess && made < 7; ++made) {
+        e = cudaEventCreateWithFlags(evs[made], cudaEventDisableTiming);
+        if (e != cudaSuccess) break;
+    }
+    c->cap_main = c->cap_fork = nullptr;
+    if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&c->cap_main, cudaStreamNonBlocking);
+    if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&c->cap_fork, cudaStreamNonBlocking);
     if (e != cudaSuccess) {
-        for (int i = 0; i < made - 1; ++i) cudaEventDestroy(*evs[i]);
+        for (int i = 0; i < made; ++i) cudaEventDestroy(*evs[i]);
+        if (c->cap_main) cudaStreamDestroy(c->cap_main);
+        if (c->cap_fork) cudaStreamDestroy(c->cap_fork);
         delete c;
         return KVATTN_ERR_CUDA;
     }
     c->pending = false;
+    c->exec = nullptr;
+    std::memset(&c->key, 0, sizeof(c->key));
     *ctx = c;
     return KVATTN_OK;
 }
 
 int kvattn_tail_ctx_destroy(kvattn_tail_ctx* ctx) {
     if (ctx == nullptr) return KVATTN_ERR_INVALID_ARG;
-    cudaEvent_t evs[6] = {ctx->copied[0], ctx->copied[1], ctx->consumed[0], ctx->consumed[1], ctx->start, ctx->done};
+    cudaEvent_t evs[7] = {ctx->copied[0], ctx->copied[1], ctx->consumed[0], ctx->consumed[1],
+                          ctx->start,     ctx->done,      ctx->joined};
     int rc = KVATTN_OK;
+    if (ctx->exec != nullptr && cudaGraphExecDestroy(ctx->exec) != cudaSuccess) rc = KVATTN_ERR_CUDA;
+    if (cudaStreamDestroy(ctx->cap_main) != cudaSuccess) rc = KVATTN_ERR_CUDA;
+    if (cudaStreamDestroy(ctx->cap_fork) != cudaSuccess) rc = KVATTN_ERR_CUDA;
     for (cudaEvent_t ev : evs)
         if (cudaEventDestroy(ev) != cudaSuccess) rc = KVATTN_ERR_CUDA;
     delete ctx;
@@ -450,6 +485,142 @@ int fault_tile() {
 
 }  // namespace
 
+}  // extern "C"
+
+namespace {
+
+bool use_tail_graph() {
+    static const bool on = env_int("KVATTN_TAIL_GRAPH", 1) != 0;
+    return on;
+}
+
+// Kernel parameters of one window + tail call, fixed before any enqueue or capture.
+struct TailPlan {
+    TailLayout L;
+    SplitDecodeParams base;     // common fields
+    SplitDecodeParams window;   // the resident window
+    SplitDecodeParams slot[2];  // the two staging slots (tensor maps over tile_cells rows)
+    MergeParams merge;
+    size_t row_bytes;
+    char* wsb;
+    bool pdl;
+};
+
+void prepare_window_tail(TailPlan& t, const void* q, const void* k_win, const void* v_win, int64_t n_win,
+                         int64_t n_tail, int64_t tile_cells, int n_head, int n_head_kv, int head_dim, int split,
+                         int tail_split, float scale, float* out, float* lse, void* ws, const TailLayout& L) {
+    t.L = L;
+    t.wsb = static_cast<char*>(ws);
+    t.pdl = use_pdl();
+    t.row_bytes = (size_t)n_head_kv * head_dim * 2;
+    char* parts = t.wsb + L.parts_base;
+    SplitDecodeParams& p = t.base;
+    p = SplitDecodeParams{};
+    p.q = static_cast<const __half*>(q);
+    p.part_o = reinterpret_cast<float*>(parts + L.parts.o_off);
+    p.part_lse = reinterpret_cast<float*>(parts + L.parts.lse_off);
+    p.status = reinterpret_cast<uint32_t*>(t.wsb);
+    p.n_split = L.n_parts;
+    p.part_stride = L.n_parts;
+    p.n_seq = 1;
+    p.n_head = n_head;
+    p.n_head_kv = n_head_kv;
+    p.group = n_head / n_head_kv;
+    p.scale_log2 = (float)((double)scale * 1.4426950408889634074);
+    apply_debug_hooks(p);
+    t.window = p;
+    if (L.n_split_win > 0) {
+        SplitDecodeParams& w = t.window;
+        w.k = k_win;
+        w.v = v_win;
+        w.n_cells = n_win;
+        w.max_len = n_win;
+        w.fixed_len = n_win;
+        w.split = split;
+        w.part_base = 0;
+        w.n_stages = pick_stages(KVATTN_KV_F16, head_dim, (int64_t)L.n_split_win * n_head_kv);
+        set_kv_maps(w, KVATTN_KV_F16, n_win, n_head_kv, head_dim);
+    }
+    const int tile_stages = pick_stages(KVATTN_KV_F16, head_dim, L.splits_per_tile * n_head_kv);
+    for (int sl = 0; sl < 2; ++sl) {
+        SplitDecodeParams& tp = t.slot[sl];
+        tp = p;
+        tp.k = t.wsb + L.stage_off[sl][0];
+        tp.v = t.wsb + L.stage_off[sl][1];
+        tp.max_len = tile_cells;
+        tp.split = tail_split;
+        tp.n_stages = tile_stages;
+        set_kv_maps(tp, KVATTN_KV_F16, tile_cells, n_head_kv, head_dim);
+    }
+    MergeParams& m = t.merge;
+    m = MergeParams{};
+    m.part_o = p.part_o;
+    m.part_lse = p.part_lse;
+    m.out = out;
+    m.lse = lse;
+    m.seq_lens = nullptr;
+    m.n_parts = L.n_parts;
+    m.n_seq = 1;
+    m.n_rows = n_head;
+    m.head_dim = head_dim;
+    m.split = 1;
+    m.all_written = 1;
+    (void)n_tail;
+}
+
+// Enqueue the window decode, the double-buffered tile pipeline and the final merge.
+int enqueue_window_tail(kvattn_tail_ctx* ctx, const TailPlan& t, const void* k_tail_host, const void* v_tail_host,
+                        int64_t n_tail, int64_t tile_cells, cudaStream_t cs, cudaStream_t xs, int fault) {
+    const TailLayout& L = t.L;
+    const int head_dim = t.merge.head_dim;
+    const int n_head_kv = t.base.n_head_kv;
+    // The copy stream may not overwrite a staging slot that an earlier call's tile decode
+    // on the compute stream still reads.
+    if (cudaEventRecord(ctx->start, cs) != cudaSuccess) return KVATTN_ERR_CUDA;
+    if (cudaStreamWaitEvent(xs, ctx->start, 0) != cudaSuccess) return KVATTN_ERR_CUDA;
+    // window: resident cells, attended while the first tail tiles are in flight
+    if (L.n_split_win > 0) {
+        const dim3 grid((unsigned)L.n_split_win, (unsigned)n_head_kv, 1);
+        if (launch_split_decode(t.window, KVATTN_KV_F16, head_dim, grid, cs, t.pdl) != cudaSuccess)
+            return KVATTN_ERR_CUDA;
+    }
+    // tail: tile i -> staging slot i % 2 on the copy stream, decoded on the compute stream
+    SplitDecodeParams slot[2] = {t.slot[0], t.slot[1]};
+    for (int64_t i = 0; i < L.n_tiles; ++i) {
+        const int sl = (int)(i & 1);
+        const int64_t c0 = i * tile_cells;
+        const int64_t len = (c0 + tile_cells <= n_tail) ? tile_cells : n_tail - c0;
+        const size_t bytes = (size_t)len * t.row_bytes;
+        if (i >= 2 && cudaStreamWaitEvent(xs, ctx->consumed[sl], 0) != cudaSuccess) return KVATTN_ERR_CUDA;
+        if (i == fault) return KVATTN_ERR_CUDA;
+        if (cudaMemcpyAsync(const_cast<void*>(slot[sl].k), static_cast<const char*>(k_tail_host) + (size_t)c0 * t.row_bytes,
+                            bytes, cudaMemcpyHostToDevice, xs) != cudaSuccess)
+            return KVATTN_ERR_CUDA;
+        if (cudaMemcpyAsync(const_cast<void*>(slot[sl].v), static_cast<const char*>(v_tail_host) + (size_t)c0 * t.row_bytes,
+                            bytes, cudaMemcpyHostToDevice, xs) != cudaSuccess)
+            return KVATTN_ERR_CUDA;
+        if (cudaEventRecord(ctx->copied[sl], xs) != cudaSuccess) return KVATTN_ERR_CUDA;
+        if (cudaStreamWaitEvent(cs, ctx->copied[sl], 0) != cudaSuccess) return KVATTN_ERR_CUDA;
+        SplitDecodeParams& tp = slot[sl];
+        tp.n_cells = len;
+        tp.fixed_len = len;
+        tp.part_base = L.n_split_win + i * L.splits_per_tile;
+        const dim3 grid((unsigned)L.splits_per_tile, (unsigned)n_head_kv, 1);
+        if (launch_split_decode(tp, KVATTN_KV_F16, head_dim, grid, cs, false) != cudaSuccess)
+            return KVATTN_ERR_CUDA;
+        if (cudaEventRecord(ctx->consumed[sl], cs) != cudaSuccess) return KVATTN_ERR_CUDA;
+    }
+    // join the copy stream back into the compute stream
+    if (cudaEventRecord(ctx->joined, xs) != cudaSuccess) return KVATTN_ERR_CUDA;
+    if (cudaStreamWaitEvent(cs, ctx->joined, 0) != cudaSuccess) return KVATTN_ERR_CUDA;
+    if (launch_merge(t.merge, cs, t.pdl) != cudaSuccess) return KVATTN_ERR_CUDA;
+    return KVATTN_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
 size_t kvattn_window_tail_workspace_bytes(int n_head, int n_head_kv, int head_dim, int64_t n_win,
                                           int64_t n_tail, int split, int64_t tile_cells,
                                           int tail_split) {
@@ -489,107 +660,174 @@ int kvattn_decode_window_tail(kvattn_tail_ctx* ctx, const void* q, const void* k
 
     cudaStream_t cs = static_cast<cudaStream_t>(compute_stream);
     cudaStream_t xs = static_cast<cudaStream_t>(copy_stream);
-    char* wsb = static_cast<char*>(ws);
-    uint32_t* status = reinterpret_cast<uint32_t*>(wsb);
-    char* parts = wsb + L.parts_base;
+    TailPlan plan;
+    prepare_window_tail(plan, q, k_win, v_win, n_win, n_tail, tile_cells, n_head, n_head_kv, head_dim, split,
+                        tail_split, scale, out, lse, ws, L);
     const int fault = fault_tile();
-    const bool pdl = use_pdl();
 
+    cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(cs, &cap) != cudaSuccess) return KVATTN_ERR_CUDA;
+    const bool use_graph = use_tail_graph() && cap == cudaStreamCaptureStatusNone && fault < 0;
+    if (!use_graph) {
+        const int rc = enqueue_window_tail(ctx, plan, k_tail_host, v_tail_host, n_tail, tile_cells, cs, xs, fault);
+        if (rc != KVATTN_OK) return rc;
+    } else {
+        TailGraphKey key;
+        std::memset(&key, 0, sizeof(key));
+        key.q = q;
+        key.k_win = k_win;
+        key.v_win = v_win;
+        key.k_tail = k_tail_host;
+        key.v_tail = v_tail_host;
+        key.n_win = n_win;
+        key.n_tail = n_tail;
+        key.tile_cells = tile_cells;
+        key.n_head = n_head;
+        key.n_head_kv = n_head_kv;
+        key.head_dim = head_dim;
+        key.split = split;
+        key.tail_split = tail_split;
+        key.scale = scale;
+        key.out = out;
+        key.lse = lse;
+        key.ws = ws;
+        key.ws_bytes = ws_bytes;
+        key.stall_tx = plan.base.stall_tx;
+        key.wait_limit_ns = plan.base.wait_limit_ns;
+        key.pdl = plan.pdl ? 1 : 0;
+        cudaGetDevice(&key.device);
+        if (ctx->exec == nullptr || !(ctx->key == key)) {
+            if (ctx->exec != nullptr) {
+                cudaGraphExecDestroy(ctx->exec);
+                ctx->exec = nullptr;
+            }
+            // Record the pipeline once as a graph: ~3 operations per tile would otherwise
+            // cost more host time per call than the host-to-device copies themselves.
+            // (recorded on private streams: the caller's may be the legacy default stream)
+            if (cudaStreamBeginCapture(ctx->cap_main, cudaStreamCaptureModeThreadLocal) != cudaSuccess)
+                return KVATTN_ERR_CUDA;
+            const int rc = enqueue_window_tail(ctx, plan, k_tail_host, v_tail_host, n_tail, tile_cells, ctx->cap_main,
+                                               ctx->cap_fork, -1);
+            cudaGraph_t graph = nullptr;
+            const cudaError_t ec = cudaStreamEndCapture(ctx->cap_main, &graph);
+            if (rc != KVATTN_OK || ec != cudaSuccess || graph == nullptr) {
+                if (graph != nullptr) cudaGraphDestroy(graph);
+                return rc != KVATTN_OK ? rc : KVATTN_ERR_CUDA;
+            }
+            cudaGraphExec_t exec = nullptr;
+            const cudaError_t ei = cudaGraphInstantiate(&exec, graph, 0);
+            cudaGraphDestroy(graph);
+            if (ei != cudaSuccess) return KVATTN_ERR_CUDA;
+            ctx->exec = exec;
+            ctx->key = key;
+        }
+        if (cudaGraphLaunch(ctx->exec, cs) != cudaSuccess) return KVATTN_ERR_CUDA;
+    }
+    if (cudaEventRecord(ctx->done, cs) != cudaSuccess) return KVATTN_ERR_CUDA;
+    ctx->pending = true;
+    return KVATTN_OK;
+}
+
+size_t kvattn_window_tail_direct_workspace_bytes(int n_head, int n_head_kv, int head_dim, int64_t n_win,
+                                                 int64_t n_tail, int split, int tail_split) {
+    if (n_head < 1 || n_head_kv < 1 || head_dim < 1 || n_win < 0 || n_tail < 0 || split < 1 || tail_split < 1)
+        return 0;
+    const int64_t parts = (n_win + split - 1) / split + (n_tail + tail_split - 1) / tail_split;
+    return decode_ws_layout(1, n_head, head_dim, parts).total;
+}
+
+int kvattn_decode_window_tail_direct(const void* q, const void* k_win, const void* v_win, int64_t n_win,
+                                     const void* k_tail_host, const void* v_tail_host, int64_t n_tail, int n_head,
+                                     int n_head_kv, int head_dim, int split, int tail_split, float scale, float* out,
+                                     float* lse, void* ws, size_t ws_bytes, void* stream) {
+    if (q == nullptr || out == nullptr || lse == nullptr || ws == nullptr) return KVATTN_ERR_INVALID_ARG;
+    int st = check_shape(DecodeShape{1, n_head, n_head_kv, head_dim, split, n_win});
+    if (st != KVATTN_OK) return st;
+    st = check_shape(DecodeShape{1, n_head, n_head_kv, head_dim, tail_split, n_tail});
+    if (st != KVATTN_OK) return st;
+    if (!std::isfinite(scale)) return KVATTN_ERR_INVALID_ARG;
+    if ((n_win > 0 && (k_win == nullptr || v_win == nullptr)) ||
+        (n_tail > 0 && (k_tail_host == nullptr || v_tail_host == nullptr)))
+        return KVATTN_ERR_INVALID_ARG;
+    if (!aligned(q, 4) || !aligned(out, 16) || !aligned(lse, 4) || !aligned(ws, kWsAlign) ||
+        (k_win && !aligned(k_win, 16)) || (v_win && !aligned(v_win, 16)) ||
+        (k_tail_host && !aligned(k_tail_host, 16)) || (v_tail_host && !aligned(v_tail_host, 16)))
+        return KVATTN_ERR_INVALID_ARG;
+    const int64_t n_split_win = (n_win + split - 1) / split;
+    const int64_t n_split_tail = (n_tail + tail_split - 1) / tail_split;
+    const int64_t n_parts = n_split_win + n_split_tail;
+    const DecodeWsLayout lay = decode_ws_layout(1, n_head, head_dim, n_parts);
+    if (ws_bytes < lay.total) return KVATTN_ERR_WORKSPACE;
+    // the device's view of the pinned tail (fails for memory that is not pinned and mapped)
+    void* dk = nullptr;
+    void* dv = nullptr;
+    if (n_tail > 0) {
+        if (cudaHostGetDevicePointer(&dk, const_cast<void*>(k_tail_host), 0) != cudaSuccess ||
+            cudaHostGetDevicePointer(&dv, const_cast<void*>(v_tail_host), 0) != cudaSuccess) {
+            cudaGetLastError();  // clear the error the failed query leaves behind
+            return KVATTN_ERR_INVALID_ARG;
+        }
+    }
+    cudaStream_t cs = static_cast<cudaStream_t>(stream);
+    char* wsb = static_cast<char*>(ws);
+    const bool pdl = use_pdl();
     SplitDecodeParams p = {};
     p.q = static_cast<const __half*>(q);
-    p.part_o = reinterpret_cast<float*>(parts + L.parts.o_off);
-    p.part_lse = reinterpret_cast<float*>(parts + L.parts.lse_off);
-    p.status = status;
-    p.plan = nullptr;
-    p.seq_lens = nullptr;
-    p.desc = nullptr;
-    p.n_split = L.n_parts;
-    p.part_stride = L.n_parts;
+    p.part_o = reinterpret_cast<float*>(wsb + lay.o_off);
+    p.part_lse = reinterpret_cast<float*>(wsb + lay.lse_off);
+    p.status = reinterpret_cast<uint32_t*>(wsb);
+    p.n_split = n_parts;
+    p.part_stride = n_parts;
     p.n_seq = 1;
     p.n_head = n_head;
     p.n_head_kv = n_head_kv;
     p.group = n_head / n_head_kv;
     p.scale_log2 = (float)((double)scale * 1.4426950408889634074);
     apply_debug_hooks(p);
-
-    // The copy stream may not overwrite a staging slot that an earlier call's tile decode
-    // on the compute stream still reads.
-    if (cudaEventRecord(ctx->start, cs) != cudaSuccess) return KVATTN_ERR_CUDA;
-    if (cudaStreamWaitEvent(xs, ctx->start, 0) != cudaSuccess) return KVATTN_ERR_CUDA;
-
-    // window: resident cells, attended while the first tail tiles are in flight
-    if (L.n_split_win > 0) {
-        p.k = k_win;
-        p.v = v_win;
-        p.n_cells = n_win;
-        p.max_len = n_win;
-        p.fixed_len = n_win;
-        p.split = split;
-        p.part_base = 0;
-        const dim3 grid((unsigned)L.n_split_win, (unsigned)n_head_kv, 1);
-        p.n_stages = pick_stages(KVATTN_KV_F16, head_dim, (int64_t)L.n_split_win * n_head_kv);
-        set_kv_maps(p, KVATTN_KV_F16, n_win, n_head_kv, head_dim);
-        if (launch_split_decode(p, KVATTN_KV_F16, head_dim, grid, cs, pdl) != cudaSuccess)
+    if (n_split_win > 0) {
+        SplitDecodeParams w = p;
+        w.k = k_win;
+        w.v = v_win;
+        w.n_cells = n_win;
+        w.max_len = n_win;
+        w.fixed_len = n_win;
+        w.split = split;
+        w.part_base = 0;
+        w.n_stages = pick_stages(KVATTN_KV_F16, head_dim, n_split_win * n_head_kv);
+        set_kv_maps(w, KVATTN_KV_F16, n_win, n_head_kv, head_dim);
+        if (launch_split_decode(w, KVATTN_KV_F16, head_dim, dim3((unsigned)n_split_win, (unsigned)n_head_kv, 1),
+                                cs, pdl) != cudaSuccess)
             return KVATTN_ERR_CUDA;
     }
-
-    // tail: tile t -> staging slot t % 2 on the copy stream, decoded on the compute stream
-    const size_t row_bytes = (size_t)n_head_kv * head_dim * 2;
-    const int tile_stages = pick_stages(KVATTN_KV_F16, head_dim, L.splits_per_tile * n_head_kv);
-    SplitDecodeParams slot_params[2];
-    for (int sl = 0; sl < 2; ++sl) {
-        slot_params[sl] = p;
-        slot_params[sl].k = wsb + L.stage_off[sl][0];
-        slot_params[sl].v = wsb + L.stage_off[sl][1];
-        set_kv_maps(slot_params[sl], KVATTN_KV_F16, tile_cells, n_head_kv, head_dim);
+    if (n_split_tail > 0) {
+        // the tail's rows cross the host link once, straight into shared memory
+        SplitDecodeParams t = p;
+        t.k = dk;
+        t.v = dv;
+        t.n_cells = n_tail;
+        t.max_len = n_tail;
+        t.fixed_len = n_tail;
+        t.split = tail_split;
+        t.part_base = n_split_win;
+        t.use_tma = 0;
+        t.src_lsu = 1;
+        t.n_stages = pick_stages(KVATTN_KV_F16, head_dim, n_split_tail * n_head_kv);
+        if (launch_split_decode(t, KVATTN_KV_F16, head_dim, dim3((unsigned)n_split_tail, (unsigned)n_head_kv, 1),
+                                cs, false) != cudaSuccess)
+            return KVATTN_ERR_CUDA;
     }
-    for (int64_t t = 0; t < L.n_tiles; ++t) {
-        const int slot = (int)(t & 1);
-        const int64_t c0 = t * tile_cells;
-        const int64_t len = (c0 + tile_cells <= n_tail) ? tile_cells : n_tail - c0;
-        const size_t bytes = (size_t)len * row_bytes;
-        if (t >= 2 && cudaStreamWaitEvent(xs, ctx->consumed[slot], 0) != cudaSuccess)
-            return KVATTN_ERR_CUDA;
-        if (t == fault) return KVATTN_ERR_CUDA;
-        char* dk = wsb + L.stage_off[slot][0];
-        char* dv = wsb + L.stage_off[slot][1];
-        if (cudaMemcpyAsync(dk, static_cast<const char*>(k_tail_host) + (size_t)c0 * row_bytes, bytes,
-                            cudaMemcpyHostToDevice, xs) != cudaSuccess)
-            return KVATTN_ERR_CUDA;
-        if (cudaMemcpyAsync(dv, static_cast<const char*>(v_tail_host) + (size_t)c0 * row_bytes, bytes,
-                            cudaMemcpyHostToDevice, xs) != cudaSuccess)
-            return KVATTN_ERR_CUDA;
-        if (cudaEventRecord(ctx->copied[slot], xs) != cudaSuccess) return KVATTN_ERR_CUDA;
-        if (cudaStreamWaitEvent(cs, ctx->copied[slot], 0) != cudaSuccess) return KVATTN_ERR_CUDA;
-        SplitDecodeParams& tp = slot_params[slot];
-        tp.n_cells = len;
-        tp.max_len = tile_cells;
-        tp.fixed_len = len;
-        tp.split = tail_split;
-        tp.part_base = L.n_split_win + t * L.splits_per_tile;
-        tp.n_stages = tile_stages;
-        const dim3 grid((unsigned)L.splits_per_tile, (unsigned)n_head_kv, 1);
-        if (launch_split_decode(tp, KVATTN_KV_F16, head_dim, grid, cs, false) != cudaSuccess)
-            return KVATTN_ERR_CUDA;
-        if (cudaEventRecord(ctx->consumed[slot], cs) != cudaSuccess) return KVATTN_ERR_CUDA;
-    }
-
     MergeParams m = {};
-    m.part_o = reinterpret_cast<const float*>(parts + L.parts.o_off);
-    m.part_lse = reinterpret_cast<const float*>(parts + L.parts.lse_off);
+    m.part_o = p.part_o;
+    m.part_lse = p.part_lse;
     m.out = out;
     m.lse = lse;
-    m.seq_lens = nullptr;
-    m.n_parts = L.n_parts;
+    m.n_parts = n_parts;
     m.n_seq = 1;
     m.n_rows = n_head;
     m.head_dim = head_dim;
     m.split = 1;
     m.all_written = 1;
-    if (launch_merge(m, cs, pdl) != cudaSuccess) return KVATTN_ERR_CUDA;
-    if (cudaEventRecord(ctx->done, cs) != cudaSuccess) return KVATTN_ERR_CUDA;
-    ctx->pending = true;
-    return KVATTN_OK;
+    return cuda_status(launch_merge(m, cs, pdl && n_parts > 0));
 }
 
 int kvattn_tail_wait(kvattn_tail_ctx* ctx, int timeout_ms) {

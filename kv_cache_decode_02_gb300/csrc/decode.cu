@@ -425,7 +425,7 @@ __global__ void __launch_bounds__(kThreads) split_decode_kernel(const __grid_con
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < n_stages; ++i) {
-            mbar_init(smem_addr(&full_bar[i]), G::kArrivals);
+            mbar_init(smem_addr(&full_bar[i]), p.src_lsu ? 64 : G::kArrivals);
             mbar_init(smem_addr(&empty_bar[i]), kConsumerWarps * 32);
         }
         *abort_flag = 0;
@@ -520,8 +520,9 @@ __global__ void __launch_bounds__(kThreads) split_decode_kernel(const __grid_con
             if (lane == 0) {
                 tile_mask[st] = mask;
                 tile_swz[st] = use_tma ? 1u : 0u;
-                const uint32_t bytes = use_tma ? (uint32_t)(2 * G::kSwzSection)
-                                               : (uint32_t)__popc(mask) * 2u * (uint32_t)G::kRowBytes;
+                const uint32_t bytes = use_tma     ? (uint32_t)(2 * G::kSwzSection)
+                                       : p.src_lsu ? 0u  // cp.async completions arrive instead
+                                                   : (uint32_t)__popc(mask) * 2u * (uint32_t)G::kRowBytes;
                 mbar_expect_tx(bar, bytes + (t == 0 ? p.stall_tx : 0u));
             }
             __syncwarp();
@@ -541,12 +542,40 @@ __global__ void __launch_bounds__(kThreads) split_decode_kernel(const __grid_con
             if (!use_tma) {
                 unsigned char* krow = stage + lane * G::kPadRow;
                 unsigned char* vrow = stage + G::kPadSection + lane * G::kPadRow;
+                if (p.src_lsu) {
+                    // 16-byte asynchronous loads, a whole row per group of lanes, so every
+                    // request covers full lines (the source may sit across the host link)
+                    constexpr int kLanesPerRow = G::kRowBytes / 16 < 32 ? G::kRowBytes / 16 : 32;
+                    constexpr int kRowsPerPass = 32 / kLanesPerRow;
+                    constexpr int kChunksPerLane = G::kRowBytes / 16 / kLanesPerRow;
+                    const int sub = lane % kLanesPerRow;
+                    for (int r0 = 0; r0 < kTileCells; r0 += kRowsPerPass) {
+                        const int c = r0 + lane / kLanesPerRow;
+                        const bool cv = __shfl_sync(0xffffffffu, valid, c);
+                        const int64_t ccell = __shfl_sync(0xffffffffu, cell, c);
+                        if (cv) {
+                            const int64_t row = ccell * Hk + g;
+                            const char* ksrc = static_cast<const char*>(p.k) + row * G::kRowBytes;
+                            const char* vsrc = static_cast<const char*>(p.v) + row * G::kRowBytes;
+                            unsigned char* kd = stage + c * G::kPadRow;
+                            unsigned char* vd = stage + G::kPadSection + c * G::kPadRow;
+#pragma unroll
+                            for (int j = 0; j < kChunksPerLane; ++j) {
+                                const int off = 16 * (sub + j * kLanesPerRow);
+                                cp_async_16_cg(smem_addr(kd + off), ksrc + off);
+                                cp_async_16_cg(smem_addr(vd + off), vsrc + off);
+                            }
+                        }
+                    }
+                }
                 if (valid) {
-                    const int64_t row = cell * Hk + g;
-                    bulk_g2s(smem_addr(krow), static_cast<const char*>(p.k) + row * G::kRowBytes,
-                             G::kRowBytes, bar);
-                    bulk_g2s(smem_addr(vrow), static_cast<const char*>(p.v) + row * G::kRowBytes,
-                             G::kRowBytes, bar);
+                    if (!p.src_lsu) {
+                        const int64_t row = cell * Hk + g;
+                        bulk_g2s(smem_addr(krow), static_cast<const char*>(p.k) + row * G::kRowBytes,
+                                 G::kRowBytes, bar);
+                        bulk_g2s(smem_addr(vrow), static_cast<const char*>(p.v) + row * G::kRowBytes,
+                                 G::kRowBytes, bar);
+                    }
                 } else {
                     uint4* z = reinterpret_cast<uint4*>(vrow);
 #pragma unroll
@@ -574,8 +603,8 @@ __global__ void __launch_bounds__(kThreads) split_decode_kernel(const __grid_con
                     for (int k = 0; k < G::kSclBytes / 4; ++k) zs[k] = 0u;
                     wrote = true;
                 }
-                cp_async_arrive_noinc(bar);
             }
+            if (KVT == KVATTN_KV_Q8_0 || p.src_lsu) cp_async_arrive_noinc(bar);
             if (wrote) fence_proxy_async();  // zero-fills before later async writes to this stage
             mbar_arrive(bar);
         }

@@ -67,6 +67,8 @@ struct SplitDecodeParams {
     int n_seq, n_head, n_head_kv, group, split;
     int n_stages;
     int use_tma;              // tiles that are one physical run load through tmap_k/tmap_v
+    int src_lsu;              // K/V rows arrive by 16-byte cp.async (e.g. straight from pinned
+                              // host memory) instead of the TMA engine
     float scale_log2;         // scale * log2(e)
 };
 
@@ -199,6 +201,9 @@ __device__ __forceinline__ void cp_async_8(uint32_t dst, const void* src) {
 }
 __device__ __forceinline__ void cp_async_16(uint32_t dst, const void* src) {
     asm volatile("cp.async.ca.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_16_cg(uint32_t dst, const void* src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
 }
 __device__ __forceinline__ void cp_async_arrive_noinc(uint32_t bar) {
     asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");

@@ -41,6 +41,7 @@ EXPORTED = (
     "kvattn_tail_ctx_create",
     "kvattn_tail_ctx_destroy", "kvattn_window_tail_workspace_bytes", "kvattn_decode_window_tail",
     "kvattn_tail_wait", "kvattn_workspace_status", "kvattn_decode_noalloc",
+    "kvattn_window_tail_direct_workspace_bytes", "kvattn_decode_window_tail_direct",
 )
 
 _P = ctypes.c_void_p
@@ -79,6 +80,11 @@ lib.kvattn_window_tail_workspace_bytes.restype = _SZ
 lib.kvattn_decode_window_tail.argtypes = [_P, _P, _P, _P, _I64, _P, _P, _I64, _I64, _I, _I, _I, _I,
                                           _I, _F, _P, _P, _P, _SZ, _P, _P]
 lib.kvattn_decode_window_tail.restype = _I
+lib.kvattn_window_tail_direct_workspace_bytes.argtypes = [_I, _I, _I, _I64, _I64, _I, _I]
+lib.kvattn_window_tail_direct_workspace_bytes.restype = _SZ
+lib.kvattn_decode_window_tail_direct.argtypes = [_P, _P, _P, _I64, _P, _P, _I64, _I, _I, _I, _I, _I, _F, _P,
+                                                 _P, _P, _SZ, _P]
+lib.kvattn_decode_window_tail_direct.restype = _I
 lib.kvattn_tail_wait.argtypes = [_P, _I]
 lib.kvattn_tail_wait.restype = _I
 lib.kvattn_workspace_status.argtypes = [_P, ctypes.POINTER(ctypes.c_uint32), _I, _P]
@@ -208,6 +214,44 @@ def kvattn_decode_window_tail(ctx, q, k_win, v_win, n_win, k_tail_host, v_tail_h
                                        _ptr(out), _ptr(lse), _ptr(ws), ws_bytes,
                                        _stream(compute_stream), _stream(copy_stream))
     _check(rc, "kvattn_decode_window_tail")
+
+
+def kvattn_window_tail_direct_workspace_bytes(n_head, n_head_kv, head_dim, n_win, n_tail, split,
+                                              tail_split) -> int:
+    return lib.kvattn_window_tail_direct_workspace_bytes(n_head, n_head_kv, head_dim, n_win, n_tail, split,
+                                                         tail_split)
+
+
+def kvattn_decode_window_tail_direct(q, k_win, v_win, n_win, k_tail_host, v_tail_host, n_tail, n_head,
+                                     n_head_kv, head_dim, split, tail_split, scale, out, lse, ws, ws_bytes,
+                                     stream=None):
+    rc = lib.kvattn_decode_window_tail_direct(_ptr(q), _ptr(k_win), _ptr(v_win), n_win, _ptr(k_tail_host),
+                                              _ptr(v_tail_host), n_tail, n_head, n_head_kv, head_dim, split,
+                                              tail_split, scale, _ptr(out), _ptr(lse), _ptr(ws), ws_bytes,
+                                              _stream(stream))
+    _check(rc, "kvattn_decode_window_tail_direct")
+
+
+def window_tail_direct(q, k_win, v_win, k_tail_host, v_tail_host, *, split, tail_split, scale=None,
+                       out=None, lse=None, ws=None, stream=None):
+    """Window in HBM + tail read in place from pinned host memory.  q: half [H][D]."""
+    import torch
+    H, D = q.shape[-2], q.shape[-1]
+    Hk = k_win.shape[-2] if k_win is not None else k_tail_host.shape[-2]
+    n_win = k_win.shape[0] if k_win is not None else 0
+    n_tail = k_tail_host.shape[0] if k_tail_host is not None else 0
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    if out is None:
+        out = torch.empty((H, D), dtype=torch.float32, device=q.device)
+    if lse is None:
+        lse = torch.empty((H,), dtype=torch.float32, device=q.device)
+    if ws is None:
+        nbytes = kvattn_window_tail_direct_workspace_bytes(H, Hk, D, n_win, n_tail, split, tail_split)
+        ws = torch.zeros(max(nbytes, 256), dtype=torch.uint8, device=q.device)
+    kvattn_decode_window_tail_direct(q, k_win, v_win, n_win, k_tail_host, v_tail_host, n_tail, H, Hk, D, split,
+                                     tail_split, scale, out, lse, ws, ws.numel(), stream)
+    return out, lse
 
 
 def kvattn_tail_wait(ctx: int, timeout_ms: int) -> None:

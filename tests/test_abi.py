@@ -144,3 +144,21 @@ def test_window_tail_validation(kvattn):
     assert f(*bad) == -1
     assert kvattn.lib.kvattn_tail_ctx_destroy(None) == -1
     assert kvattn.lib.kvattn_tail_wait(None, 10) == -1
+
+
+def test_window_tail_direct_validation(kvattn):
+    f = kvattn.lib.kvattn_decode_window_tail_direct
+    n = kvattn.kvattn_window_tail_direct_workspace_bytes(40, 8, 128, 16384, 507904, 256, 128)
+    assert n > (64 + 3968) * 40 * 128 * 4
+    base = [A, B, C, 16384, A + 4096, B + 4096, 507904, 40, 8, 128, 256, 128, 0.0884, C + 8192, C + 16384,
+            A + (1 << 20), n, None]
+    bad = list(base); bad[0] = None
+    assert f(*bad) == -1
+    bad = list(base); bad[9] = 64                 # head_dim
+    assert f(*bad) == -2
+    bad = list(base); bad[11] = 48                # tail split not a multiple of 32
+    assert f(*bad) == -2
+    bad = list(base); bad[16] = n - 1             # workspace
+    assert f(*bad) == -3
+    bad = list(base); bad[4] = A + 4100           # tail not 16-byte aligned
+    assert f(*bad) == -1

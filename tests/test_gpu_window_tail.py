@@ -108,3 +108,59 @@ def test_host_wait_times_out_then_completes(kvattn):
     wo, wl = oracle.decode_f16(q, k, v, [N])
     assert_close(out.view(1, *out.shape), lse.view(1, -1), wo, wl)
     wt.close()
+
+
+def test_replayed_graph_reads_new_host_data(kvattn):
+    """Same buffers, new contents: the recorded pipeline must copy the new tail each call."""
+    import torch
+    rng = np.random.default_rng(6)
+    N, n_win, H, Hk, D = 5000, 700, 16, 4, 128
+    n_tail = N - n_win
+    k_tail = torch.empty((n_tail, Hk, D), dtype=torch.float16).pin_memory()
+    v_tail = torch.empty((n_tail, Hk, D), dtype=torch.float16).pin_memory()
+    kw = torch.empty((n_win, Hk, D), dtype=torch.float16, device="cuda")
+    vw = torch.empty((n_win, Hk, D), dtype=torch.float16, device="cuda")
+    qd = torch.empty((H, D), dtype=torch.float16, device="cuda")
+    wt = kvattn.WindowTail()
+    ws = wt.workspace(H, Hk, D, n_win, n_tail, 128, 512, 128)
+    out = torch.empty((H, D), dtype=torch.float32, device="cuda")
+    lse = torch.empty((H,), dtype=torch.float32, device="cuda")
+    cs = torch.cuda.Stream()
+    for trial in range(3):
+        q, k, v = make(rng, N, n_win, H, Hk, D)
+        torch.cuda.synchronize()
+        k_tail.copy_(torch.from_numpy(k[:n_tail]))
+        v_tail.copy_(torch.from_numpy(v[:n_tail]))
+        kw.copy_(torch.from_numpy(k[n_tail:]))
+        vw.copy_(torch.from_numpy(v[n_tail:]))
+        qd.copy_(torch.from_numpy(q[0]))
+        torch.cuda.synchronize()
+        wt(qd, kw, vw, k_tail, v_tail, split=128, tile_cells=512, tail_split=128, out=out, lse=lse, ws=ws,
+           copy_stream=cs)
+        kvattn.kvattn_tail_wait(wt.ctx, 30000)
+        torch.cuda.synchronize()
+        wo, wl = oracle.decode_f16(q, k, v, [N])
+        assert_close(out.view(1, H, D), lse.view(1, H), wo, wl)
+    wt.close()
+
+
+@pytest.mark.parametrize("N,n_win,H,Hk,tail_split", [
+    (5000, 1000, 40, 8, 128),     # ragged tail
+    (3000, 0, 16, 4, 64),         # everything in the tail
+    (777, 777, 16, 4, 128),       # everything resident
+    (4100, 64, 24, 4, 256),       # GQA-6
+])
+def test_direct_tail_reads(kvattn, N, n_win, H, Hk, tail_split):
+    """The tail read in place from pinned host memory (no staging copies)."""
+    import torch
+    rng = np.random.default_rng(N + 7 * n_win)
+    q, k, v = make(rng, N, n_win, H, Hk, 128)
+    n_tail = N - n_win
+    k_tail = torch.from_numpy(k[:n_tail]).pin_memory() if n_tail else None
+    v_tail = torch.from_numpy(v[:n_tail]).pin_memory() if n_tail else None
+    kw = dev(k[n_tail:]) if n_win else None
+    vw = dev(v[n_tail:]) if n_win else None
+    out, lse = kvattn.window_tail_direct(dev(q[0]), kw, vw, k_tail, v_tail, split=128, tail_split=tail_split)
+    torch.cuda.synchronize()
+    wo, wl = oracle.decode_f16(q, k, v, [N])
+    assert_close(out.view(1, H, 128), lse.view(1, H), wo, wl)

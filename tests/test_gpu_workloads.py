@@ -86,3 +86,18 @@ def test_window_tail_equals_resident_and_oracle(kvattn):
     assert np.max(np.abs(ro.cpu().numpy()[0] - out.cpu().numpy())) <= 2e-3
     assert np.max(np.abs(rl.cpu().numpy()[0] - lse.cpu().numpy())) <= 1e-4
     wt.close()
+
+
+def test_window_tail_direct_full(kvattn):
+    import torch
+    w = inputs.WINDOW_TAIL
+    q = inputs.make_q(w)
+    k, v = inputs.make_kv_f16(w)
+    n_tail = w.n_cells - w.n_window
+    k_tail = torch.from_numpy(k[:n_tail]).pin_memory()
+    v_tail = torch.from_numpy(v[:n_tail]).pin_memory()
+    out, lse = kvattn.window_tail_direct(dev(q[0]), dev(k[n_tail:]), dev(v[n_tail:]), k_tail, v_tail,
+                                         split=w.split, tail_split=w.tail_split)
+    torch.cuda.synchronize()
+    wo, wl = oracle.decode_f16(q, k, v, list(w.seq_lens))
+    assert_close(out.view(1, *out.shape), lse.view(1, -1), wo, wl)
