@@ -312,6 +312,7 @@ int decode_impl(const void* q, const void* k_cache, const void* v_cache, const v
         p.n_split = n_split;
         p.part_base = 0;
         p.part_stride = n_split;
+        p.write_beyond = merge ? 0 : 1;  // the merge reads only splits inside each length
         p.fixed_len = 0;
         p.n_seq = n_seq;
         p.n_head = n_head;
@@ -522,6 +523,7 @@ void prepare_window_tail(TailPlan& t, const void* q, const void* k_win, const vo
     p.status = reinterpret_cast<uint32_t*>(t.wsb);
     p.n_split = L.n_parts;
     p.part_stride = L.n_parts;
+    p.write_beyond = 1;  // the final merge reads every part slot
     p.n_seq = 1;
     p.n_head = n_head;
     p.n_head_kv = n_head_kv;
@@ -778,6 +780,7 @@ int kvattn_decode_window_tail_direct(const void* q, const void* k_win, const voi
     p.status = reinterpret_cast<uint32_t*>(wsb);
     p.n_split = n_parts;
     p.part_stride = n_parts;
+    p.write_beyond = 1;
     p.n_seq = 1;
     p.n_head = n_head;
     p.n_head_kv = n_head_kv;

@@ -137,12 +137,10 @@ __device__ __forceinline__ void consume_tile(uint32_t kb, uint32_t vb, const uns
                 cb[j][0] = cb[j][1] = cb[j][2] = cb[j][3] = 0.f;
                 const int r = r0 + 8 * j + gq;
                 // block b, half hb: d = 32b + 16hb + 4tq + {0,1 | 2,3}
-                const uint32_t w0 = lds32(sec_addr<SWZ, G::kPadRow>(kb, r, 32 * b + 4 * tq));
-                const uint32_t w1 = lds32(sec_addr<SWZ, G::kPadRow>(kb, r, 32 * b + 16 + 4 * tq));
-                mma_16816(cb[j], qa[2 * b][0], 0u, qa[2 * b][1], 0u, i8pair_to_h2(w0, w0, 0x0100u),
-                          i8pair_to_h2(w0, w0, 0x0302u));
-                mma_16816(cb[j], qa[2 * b + 1][0], 0u, qa[2 * b + 1][1], 0u, i8pair_to_h2(w1, w1, 0x0100u),
-                          i8pair_to_h2(w1, w1, 0x0302u));
+                const uint32_t w0 = lds32(sec_addr<SWZ, G::kPadRow>(kb, r, 32 * b + 4 * tq)) ^ 0x80808080u;
+                const uint32_t w1 = lds32(sec_addr<SWZ, G::kPadRow>(kb, r, 32 * b + 16 + 4 * tq)) ^ 0x80808080u;
+                mma_16816(cb[j], qa[2 * b][0], 0u, qa[2 * b][1], 0u, i8x2_lo(w0), i8x2_hi(w0));
+                mma_16816(cb[j], qa[2 * b + 1][0], 0u, qa[2 * b + 1][1], 0u, i8x2_lo(w1), i8x2_hi(w1));
             }
 #pragma unroll
             for (int j = 0; j < 2; ++j)
@@ -218,17 +216,17 @@ __device__ __forceinline__ void consume_tile(uint32_t kb, uint32_t vb, const uns
             const uint32_t pb0 = pack_half2(pf[0][0] * __half2float(dv0[b]), pf[0][1] * __half2float(dv1[b]));
             const uint32_t pb1 = pack_half2(pf[1][0] * __half2float(dv2[b]), pf[1][1] * __half2float(dv3[b]));
             const int off = 32 * b + 4 * gq;
-            const uint32_t w00 = lds32(sec_addr<SWZ, G::kPadRow>(vb, r0 + 2 * tq, off));
-            const uint32_t w01 = lds32(sec_addr<SWZ, G::kPadRow>(vb, r0 + 2 * tq + 1, off));
-            const uint32_t w10 = lds32(sec_addr<SWZ, G::kPadRow>(vb, r0 + 2 * tq + 8, off));
-            const uint32_t w11 = lds32(sec_addr<SWZ, G::kPadRow>(vb, r0 + 2 * tq + 9, off));
+            const uint32_t w00 = lds32(sec_addr<SWZ, G::kPadRow>(vb, r0 + 2 * tq, off)) ^ 0x80808080u;
+            const uint32_t w01 = lds32(sec_addr<SWZ, G::kPadRow>(vb, r0 + 2 * tq + 1, off)) ^ 0x80808080u;
+            const uint32_t w10 = lds32(sec_addr<SWZ, G::kPadRow>(vb, r0 + 2 * tq + 8, off)) ^ 0x80808080u;
+            const uint32_t w11 = lds32(sec_addr<SWZ, G::kPadRow>(vb, r0 + 2 * tq + 9, off)) ^ 0x80808080u;
+            // interleave the two cells of each pair: bytes 0,1 (hb 0) and bytes 2,3 (hb 1)
+            const uint32_t u0[2] = {prmt_b32(w00, w01, 0x5140u), prmt_b32(w00, w01, 0x7362u)};
+            const uint32_t u1[2] = {prmt_b32(w10, w11, 0x5140u), prmt_b32(w10, w11, 0x7362u)};
 #pragma unroll
-            for (int hb = 0; hb < 2; ++hb) {
-                const uint32_t sel0 = ((4u + 2u * hb) << 8) | (2u * hb);
-                const uint32_t sel1 = ((5u + 2u * hb) << 8) | (2u * hb + 1u);
-                mma_16816(oacc[2 * b + hb], i8pair_to_h2(w00, w01, sel0), i8pair_to_h2(w00, w01, sel1),
-                          i8pair_to_h2(w10, w11, sel0), i8pair_to_h2(w10, w11, sel1), pb0, pb1);
-            }
+            for (int hb = 0; hb < 2; ++hb)
+                mma_16816(oacc[2 * b + hb], i8x2_lo(u0[hb]), i8x2_hi(u0[hb]), i8x2_lo(u1[hb]), i8x2_hi(u1[hb]), pb0,
+                          pb1);
         }
     }
 }
@@ -365,11 +363,9 @@ __device__ __forceinline__ void consume_tile_staged(uint32_t kb, uint32_t vb, co
 #pragma unroll
             for (int j = 0; j < 2; ++j) {
                 cb[j][0] = cb[j][1] = cb[j][2] = cb[j][3] = 0.f;
-                const uint32_t w0 = kw[b][j][0], w1 = kw[b][j][1];
-                mma_16816(cb[j], qa[2 * b][0], 0u, qa[2 * b][1], 0u, i8pair_to_h2(w0, w0, 0x0100u),
-                          i8pair_to_h2(w0, w0, 0x0302u));
-                mma_16816(cb[j], qa[2 * b + 1][0], 0u, qa[2 * b + 1][1], 0u, i8pair_to_h2(w1, w1, 0x0100u),
-                          i8pair_to_h2(w1, w1, 0x0302u));
+                const uint32_t w0 = kw[b][j][0] ^ 0x80808080u, w1 = kw[b][j][1] ^ 0x80808080u;
+                mma_16816(cb[j], qa[2 * b][0], 0u, qa[2 * b][1], 0u, i8x2_lo(w0), i8x2_hi(w0));
+                mma_16816(cb[j], qa[2 * b + 1][0], 0u, qa[2 * b + 1][1], 0u, i8x2_lo(w1), i8x2_hi(w1));
             }
 #pragma unroll
             for (int j = 0; j < 2; ++j)
@@ -391,14 +387,14 @@ __device__ __forceinline__ void consume_tile_staged(uint32_t kb, uint32_t vb, co
         for (int b = 0; b < 4; ++b) {
             const uint32_t pb0 = pack_half2(pf[0][0] * __half2float(dv0[b]), pf[0][1] * __half2float(dv1[b]));
             const uint32_t pb1 = pack_half2(pf[1][0] * __half2float(dv2[b]), pf[1][1] * __half2float(dv3[b]));
+            const uint32_t f0 = vw[b][0] ^ 0x80808080u, f1 = vw[b][1] ^ 0x80808080u;
+            const uint32_t f2 = vw[b][2] ^ 0x80808080u, f3 = vw[b][3] ^ 0x80808080u;
+            const uint32_t u0[2] = {prmt_b32(f0, f1, 0x5140u), prmt_b32(f0, f1, 0x7362u)};
+            const uint32_t u1[2] = {prmt_b32(f2, f3, 0x5140u), prmt_b32(f2, f3, 0x7362u)};
 #pragma unroll
-            for (int hb = 0; hb < 2; ++hb) {
-                const uint32_t sel0 = ((4u + 2u * hb) << 8) | (2u * hb);
-                const uint32_t sel1 = ((5u + 2u * hb) << 8) | (2u * hb + 1u);
-                mma_16816(oacc[2 * b + hb], i8pair_to_h2(vw[b][0], vw[b][1], sel0),
-                          i8pair_to_h2(vw[b][0], vw[b][1], sel1), i8pair_to_h2(vw[b][2], vw[b][3], sel0),
-                          i8pair_to_h2(vw[b][2], vw[b][3], sel1), pb0, pb1);
-            }
+            for (int hb = 0; hb < 2; ++hb)
+                mma_16816(oacc[2 * b + hb], i8x2_lo(u0[hb]), i8x2_hi(u0[hb]), i8x2_lo(u1[hb]), i8x2_hi(u1[hb]), pb0,
+                          pb1);
         }
     }
 }
@@ -447,6 +443,24 @@ __global__ void __launch_bounds__(kThreads) split_decode_kernel(const __grid_con
     const int64_t i1 = (i0 + p.split < L) ? i0 + p.split : L;
     const bool empty = i0 >= i1 || desc_valid == 0;
     const int n_tiles = empty ? 0 : (int)((i1 - i0 + kTileCells - 1) / kTileCells);
+    if (empty) {
+        // Nothing to read.  A fully masked split inside the length still reports (0, -inf)
+        // for the merge; a split past the length writes only when the caller asked for
+        // every partial slot.
+        if (i0 < i1 || p.write_beyond) {
+            const int64_t part = (int64_t)s * p.part_stride + p.part_base + split_idx;
+            const int H = p.n_head;
+            for (int idx = threadIdx.x; idx < p.group * D; idx += kThreads) {
+                const int r = idx / D;
+                const int d = idx - r * D;
+                const int h = g * p.group + r;
+                p.part_o[(part * H + h) * D + d] = 0.f;
+                if (d == 0) p.part_lse[part * H + h] = -INFINITY;
+            }
+        }
+        pdl_launch_dependents();
+        return;
+    }
 
     const int gq = lane >> 2;
     const int tq = lane & 3;

@@ -67,6 +67,7 @@ struct SplitDecodeParams {
     int n_seq, n_head, n_head_kv, group, split;
     int n_stages;
     int use_tma;              // tiles that are one physical run load through tmap_k/tmap_v
+    int write_beyond;         // splits past a sequence's length still write (0, -inf)
     int src_lsu;              // K/V rows arrive by 16-byte cp.async (e.g. straight from pinned
                               // host memory) instead of the TMA engine
     float scale_log2;         // scale * log2(e)
@@ -248,18 +249,26 @@ __device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
     return *reinterpret_cast<uint32_t*>(&h);
 }
 
-// Two int8 lanes of a byte permutation -> exact half2, with the magic-number method of
-// Kim et al. 2022 ("Who Says Elephants Can't Run"): byte b becomes the f16 1024 + (b ^ 0x80),
-// then subtracting 1152 leaves the signed value.  `sel` picks the two bytes into positions
-// 0 and 2 of the prmt result.
-__device__ __forceinline__ uint32_t i8pair_to_h2(uint32_t w0, uint32_t w1, uint32_t sel) {
+// int8 -> exact f16 lanes with the magic-number method of Kim et al. 2022 ("Who Says
+// Elephants Can't Run"), on words whose sign bits were flipped once (w ^ 0x80808080): a
+// byte u = x + 128 paired with 0x64 is the f16 1024 + u, and subtracting 1152 as f16x2
+// leaves x.  _lo converts bytes 0,1 and _hi bytes 2,3.
+__device__ __forceinline__ uint32_t prmt_b32(uint32_t a, uint32_t b, uint32_t sel) {
     uint32_t t;
-    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(t) : "r"(w0), "r"(w1), "r"(sel));
-    t = ((t ^ 0x00800080u) & 0x00FF00FFu) | 0x64006400u;
+    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(t) : "r"(a), "r"(b), "r"(sel));
+    return t;
+}
+__device__ __forceinline__ uint32_t magic_bias_h2(uint32_t t) {
     uint32_t r;
     const uint32_t bias = 0x64806480u;  // (1152, 1152) in f16
     asm("sub.f16x2 %0, %1, %2;" : "=r"(r) : "r"(t), "r"(bias));
     return r;
+}
+__device__ __forceinline__ uint32_t i8x2_lo(uint32_t flipped) {
+    return magic_bias_h2(prmt_b32(flipped, 0x64646464u, 0x4140u));
+}
+__device__ __forceinline__ uint32_t i8x2_hi(uint32_t flipped) {
+    return magic_bias_h2(prmt_b32(flipped, 0x64646464u, 0x4342u));
 }
 
 __device__ __forceinline__ void pdl_wait() {
