@@ -230,19 +230,20 @@ def bench_workloads(K, torch, stream, peak):
             d.update(extra)
         res[name] = d
 
-    flush = torch.empty(512 << 20, dtype=torch.uint8, device="cuda")
-
     def timed(fn, n=iters):
-        ts = []
+        """Mean device time (ms) of n back-to-back calls on `stream`, after one warm-up call.
+
+        Every gated input is larger than the 129 MB L2, so nothing is flushed between calls
+        (a flush by writing a buffer would leave dirty lines whose write-back the next call
+        pays for)."""
+        fn()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
         for _ in range(n):
-            flush.fill_(1)
-            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            a.record(stream)
             fn()
-            b.record(stream)
-            b.synchronize()
-            ts.append(a.elapsed_time(b))
-        return float(np.median(ts))
+        b.record(stream)
+        b.synchronize()
+        return a.elapsed_time(b) / n
 
     # tiny (L2-resident, launch-latency-bound: reported, not gated)
     w = inputs.TINY
@@ -323,9 +324,12 @@ def bench_workloads(K, torch, stream, peak):
                     copy_stream=copy_stream)
     fn()
     torch.cuda.synchronize()
-    host_t0 = time.perf_counter()
     ms_wt = timed(fn, 5)
-    host_ms = (time.perf_counter() - host_t0) * 1e3 / 5
+    host_t0 = time.perf_counter()
+    for _ in range(3):
+        fn()
+    torch.cuda.synchronize()
+    host_ms = (time.perf_counter() - host_t0) * 1e3 / 3
     tail_bytes = n_tail * Hk * D * 4
     win_bytes = w.n_window * Hk * D * 4
     h2d_big, h2d_1mib = h2d_bandwidth(torch)
@@ -350,7 +354,6 @@ def bench_workloads(K, torch, stream, peak):
     res[w.name + "_direct"] = {"ms_per_op": round(ms_d, 3), "tail_bytes": tail_bytes, "tail_gbs": round(gbs_d, 1),
                               "frac_of_measured_h2d": round(gbs_d / h2d_big, 3),
                               "how": "tail rows read in place from pinned host memory by the decode kernel"}
-    del flush
     return res
 
 
@@ -512,7 +515,7 @@ def run_ours(args):
             "frac_of_8tbs": round(value / world / NOMINAL_HBM_GBS, 3),
             "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                          "frac": round(achieved / peak, 3), "traffic": traffic, "peak_kind": peak_kind,
-                         "kernel": "split_decode_kernel<f16,128>", "kernel_us": round(kern_ms * 1e3, 3),
+                         "kernel": "split_decode_f16_d128", "kernel_us": round(kern_ms * 1e3, 3),
                          "algorithmic_bytes_per_launch": data.bytes_per_op},
             "gpu_launches": args.steps * args.layers * 2,
             "clocks": clocks, "parity": parity, "e2e": e2e, "cpu_baseline": cpu, "workloads": workloads,
@@ -559,6 +562,34 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+def profile_workload(args):
+    """A few launches of one decode-attention workload's kvattn_decode_partials, for
+    profilers (no timing, no JSON line).  Inputs are built on the device with torch RNG in
+    the workload's shapes and value ranges."""
+    import torch
+    from kv_cache_decode_02_gb300 import inputs
+    from kv_cache_decode_02_gb300 import kvattn as K
+    w = {"q8_0_n131072_d128": inputs.Q8_LONG_D128, "q8_0_n131072_d256": inputs.Q8_LONG_D256}[args.profile_workload]
+    N, H, Hk, D = w.n_cells, w.n_head, w.n_head_kv, w.head_dim
+    g = torch.Generator(device="cuda")
+    g.manual_seed(2000 + w.number)
+    kq = torch.randint(-127, 128, (N, Hk, D), dtype=torch.int8, device="cuda", generator=g)
+    vq = torch.randint(-127, 128, (N, Hk, D), dtype=torch.int8, device="cuda", generator=g)
+    kd = (torch.rand((N, Hk, D // 32), device="cuda", generator=g) * 0.019 + 0.001).half()
+    vd = (torch.rand((N, Hk, D // 32), device="cuda", generator=g) * 0.019 + 0.001).half()
+    q = torch.from_numpy(inputs.make_q(w)).cuda()
+    lens = torch.tensor([N], dtype=torch.int32, device="cuda")
+    n_split = -(-N // w.split)
+    part_o = torch.empty((1, n_split, H, D), dtype=torch.float32, device="cuda")
+    part_lse = torch.empty((1, n_split, H), dtype=torch.float32, device="cuda")
+    ws = K.decode_workspace(1, H, D, N, w.split)
+    for _ in range(args.kernel_reps):
+        K.kvattn_decode_partials(q, kq, vq, kd, vd, K.KVATTN_KV_Q8_0, N, None, 0, lens, 1, N, H, Hk, D, w.split,
+                                 1 / math.sqrt(D), part_o, part_lse, ws, ws.numel())
+    torch.cuda.synchronize()
+    print(f"{args.profile_workload}: {args.kernel_reps} launches done")
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
@@ -574,7 +605,12 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-parity", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=12.0)
+    ap.add_argument("--profile-workload", choices=["q8_0_n131072_d128", "q8_0_n131072_d256"],
+                    help="only launch this workload's split decode --kernel-reps times (for ncu)")
     args = ap.parse_args()
+    if args.profile_workload:
+        profile_workload(args)
+        return
     if args.warmup < 3:
         args.warmup = 3
     if args.impl == "reference":

@@ -1,5 +1,6 @@
 // C-ABI entry points of kvattn: host-side validation, workspace carving, launch order,
 // and the window + host-tail pipeline.  No entry point allocates device memory.
+#include <algorithm>
 #include <atomic>
 #include <chrono>
 #include <cmath>
@@ -60,25 +61,36 @@ int occupancy(int kv_type, int head_dim, int n_stages) {
     return cache[d][t][h][n_stages];
 }
 
-// Pipeline depth per CTA ("launch bounds and occupancy-aware selection", KVARN item 6):
-// the deepest ring (3 stages or more) whose resident capacity still holds the whole grid
-// in one wave; grids larger than one wave take 2 stages, which keeps the most CTAs per SM
-// (measured on GB300: Q8_0 at 131072 cells 111 -> 91 us, a 4-sequence plan 190 -> 141 us
-// going from the deepest ring to 2 stages).
-int pick_stages(int kv_type, int head_dim, int64_t grid_ctas) {
+// Pipeline depth per CTA ("launch bounds and occupancy-aware selection", KVARN item 6).
+// The kernel is persistent, so the aim is the most resident CTAs the register budget allows
+// (up to the number of work units), then the deepest ring (at most 4 stages) that keeps that
+// many resident.  Deeper rings measured slower on GB300 for the multi-wave Q8_0 and plan
+// workloads (111 vs 91 us at 8 vs 4 stages for Q8_0 over 131072 cells).
+int pick_stages(int kv_type, int head_dim, int64_t n_units) {
     const int forced = env_int("KVATTN_STAGES", 0);
     const int max_st = split_decode_max_stages();
-    const int stage = split_decode_stage_bytes(kv_type, head_dim);
-    const int hdr = split_decode_header_bytes();
     const int limit = split_decode_max_smem();
-    if (forced >= 2 && forced <= max_st && hdr + forced * stage <= limit) return forced;
+    if (forced >= 2 && forced <= max_st && split_decode_smem_bytes(kv_type, head_dim, forced) <= limit)
+        return forced;
     const int64_t n_sm = sm_count();
-    for (int st = max_st; st >= 3; --st) {
-        if (hdr + st * stage > limit) continue;
-        const int b = occupancy(kv_type, head_dim, st);
-        if (b > 0 && (int64_t)b * n_sm >= grid_ctas) return st;
+    const int64_t want = std::min(n_units, (int64_t)occupancy(kv_type, head_dim, 2) * n_sm);
+    for (int st = 4; st >= 3; --st) {
+        if (split_decode_smem_bytes(kv_type, head_dim, st) > limit) continue;
+        if ((int64_t)occupancy(kv_type, head_dim, st) * n_sm >= want) return st;
     }
     return 2;
+}
+
+// Launches the persistent split-decode kernel over n_seq x unit_splits x n_head_kv work
+// units: one CTA per unit, at most as many CTAs as fit on the device at once.
+cudaError_t launch_decode_units(SplitDecodeParams p, int kv_type, int head_dim, int64_t unit_splits,
+                                cudaStream_t stream, bool pdl) {
+    p.unit_splits = unit_splits;
+    const int64_t n_units = (int64_t)p.n_seq * unit_splits * p.n_head_kv;
+    const int64_t resident = (int64_t)std::max(occupancy(kv_type, head_dim, p.n_stages), 1) * sm_count();
+    const int64_t grid = std::min(n_units, resident);
+    if (grid < 1) return cudaSuccess;
+    return launch_split_decode(p, kv_type, head_dim, (unsigned)grid, stream, pdl);
 }
 
 int cuda_status(cudaError_t e) { return e == cudaSuccess ? KVATTN_OK : KVATTN_ERR_CUDA; }
@@ -143,8 +155,8 @@ int check_shape(const DecodeShape& s) {
     if (s.n_head / s.n_head_kv > kMaxGroup) return KVATTN_ERR_UNSUPPORTED;
     if (s.head_dim != 128 && s.head_dim != 256) return KVATTN_ERR_UNSUPPORTED;
     if (s.split % kTileCells != 0) return KVATTN_ERR_UNSUPPORTED;
-    if (s.n_seq > 65535 || s.n_head_kv > 65535) return KVATTN_ERR_UNSUPPORTED;
-    if ((s.max_len + s.split - 1) / s.split > (int64_t)INT32_MAX) return KVATTN_ERR_UNSUPPORTED;
+    if (s.n_seq > 65535) return KVATTN_ERR_UNSUPPORTED;
+    if ((s.max_len + s.split - 1) / s.split * s.n_head_kv > (int64_t)INT32_MAX) return KVATTN_ERR_UNSUPPORTED;
     return KVATTN_OK;
 }
 
@@ -319,12 +331,11 @@ int decode_impl(const void* q, const void* k_cache, const void* v_cache, const v
         p.n_head_kv = n_head_kv;
         p.group = n_head / n_head_kv;
         p.split = split;
-        const dim3 grid((unsigned)n_split, (unsigned)n_head_kv, (unsigned)n_seq);
         p.n_stages = pick_stages(kv_type, head_dim, n_split * n_head_kv * n_seq);
         p.scale_log2 = (float)((double)scale * 1.4426950408889634074);
         apply_debug_hooks(p);
         set_kv_maps(p, kv_type, cell_plan != nullptr ? n_cells : n_cells * (int64_t)n_seq, n_head_kv, head_dim);
-        cudaError_t e = launch_split_decode(p, kv_type, head_dim, grid, s, pdl);
+        cudaError_t e = launch_decode_units(p, kv_type, head_dim, n_split, s, pdl);
         if (e != cudaSuccess) return KVATTN_ERR_CUDA;
     }
     if (!merge) return KVATTN_OK;
@@ -582,8 +593,7 @@ int enqueue_window_tail(kvattn_tail_ctx* ctx, const TailPlan& t, const void* k_t
     if (cudaStreamWaitEvent(xs, ctx->start, 0) != cudaSuccess) return KVATTN_ERR_CUDA;
     // window: resident cells, attended while the first tail tiles are in flight
     if (L.n_split_win > 0) {
-        const dim3 grid((unsigned)L.n_split_win, (unsigned)n_head_kv, 1);
-        if (launch_split_decode(t.window, KVATTN_KV_F16, head_dim, grid, cs, t.pdl) != cudaSuccess)
+        if (launch_decode_units(t.window, KVATTN_KV_F16, head_dim, L.n_split_win, cs, t.pdl) != cudaSuccess)
             return KVATTN_ERR_CUDA;
     }
     // tail: tile i -> staging slot i % 2 on the copy stream, decoded on the compute stream
@@ -607,8 +617,7 @@ int enqueue_window_tail(kvattn_tail_ctx* ctx, const TailPlan& t, const void* k_t
         tp.n_cells = len;
         tp.fixed_len = len;
         tp.part_base = L.n_split_win + i * L.splits_per_tile;
-        const dim3 grid((unsigned)L.splits_per_tile, (unsigned)n_head_kv, 1);
-        if (launch_split_decode(tp, KVATTN_KV_F16, head_dim, grid, cs, false) != cudaSuccess)
+        if (launch_decode_units(tp, KVATTN_KV_F16, head_dim, L.splits_per_tile, cs, false) != cudaSuccess)
             return KVATTN_ERR_CUDA;
         if (cudaEventRecord(ctx->consumed[sl], cs) != cudaSuccess) return KVATTN_ERR_CUDA;
     }
@@ -798,8 +807,7 @@ int kvattn_decode_window_tail_direct(const void* q, const void* k_win, const voi
         w.part_base = 0;
         w.n_stages = pick_stages(KVATTN_KV_F16, head_dim, n_split_win * n_head_kv);
         set_kv_maps(w, KVATTN_KV_F16, n_win, n_head_kv, head_dim);
-        if (launch_split_decode(w, KVATTN_KV_F16, head_dim, dim3((unsigned)n_split_win, (unsigned)n_head_kv, 1),
-                                cs, pdl) != cudaSuccess)
+        if (launch_decode_units(w, KVATTN_KV_F16, head_dim, n_split_win, cs, pdl) != cudaSuccess)
             return KVATTN_ERR_CUDA;
     }
     if (n_split_tail > 0) {
@@ -815,8 +823,7 @@ int kvattn_decode_window_tail_direct(const void* q, const void* k_win, const voi
         t.use_tma = 0;
         t.src_lsu = 1;
         t.n_stages = pick_stages(KVATTN_KV_F16, head_dim, n_split_tail * n_head_kv);
-        if (launch_split_decode(t, KVATTN_KV_F16, head_dim, dim3((unsigned)n_split_tail, (unsigned)n_head_kv, 1),
-                                cs, false) != cudaSuccess)
+        if (launch_decode_units(t, KVATTN_KV_F16, head_dim, n_split_tail, cs, false) != cudaSuccess)
             return KVATTN_ERR_CUDA;
     }
     MergeParams m = {};

@@ -60,10 +60,8 @@ struct Geom {
     static constexpr int kVsOff = kKsOff + kTileCells * kSclBytes;
     static constexpr int kBytes = (kVsOff + kTileCells * kSclBytes + 1023) / 1024 * 1024;
     static constexpr int kArrivals = KVT == KVATTN_KV_Q8_0 ? 64 : 32;  // + cp.async arrivals
-    // end-of-split merge area (aliases stage 0 once every tile is consumed)
-    static constexpr int kOStride = D + 4;
-    static constexpr int kCombineBytes = (2 * kConsumerWarps * 8 + kConsumerWarps * 8 * kOStride) * 4;
-    static_assert(kCombineBytes <= kBytes, "combine area must fit in one stage");
+    // end-of-unit exchange area: warp 1's O fragments ([D/16][32 lanes] float4), max, sum
+    static constexpr int kXchgBytes = ((D / 16) * 32 * 16 + 64 + 1023) / 1024 * 1024;
 };
 
 // Byte address of (row r, byte b) of a K or V section in either layout.
@@ -101,12 +99,105 @@ __device__ __forceinline__ int out_dim(int mt, int hi, int gq) {
     return 32 * (mt >> 1) + 4 * gq + 2 * (mt & 1) + hi;
 }
 
-// One consumer warp's 16 cells of a tile: scores, online softmax, P V.
+// Online-softmax step shared by the consumer paths.  Masks the 2x2 scores a thread holds
+// for query row gq and turns them into probabilities against the running reference max
+// m_run (log2 units).  The reference only moves when some row's new max exceeds it by more
+// than kRescaleSlack, so most tiles skip the rescale of O and l entirely; probabilities
+// then stay below 2^kRescaleSlack, which f16 P and the fp32 accumulators hold exactly as
+// well as values below 1.  Returns true (warp-uniform) when O and l must be scaled by alpha.
+constexpr float kRescaleSlack = 8.f;
+
+__device__ __forceinline__ bool softmax_step(const float (&sacc)[2][4], uint32_t mask, int tq, float scale_log2,
+                                             float& m_run, float& alpha, float (&pf)[2][2]) {
+    float x[2][2];
+    float tmax = -INFINITY;
+#pragma unroll
+    for (int j = 0; j < 2; ++j)
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+            const int c = 8 * j + 2 * tq + e;
+            x[j][e] = ((mask >> c) & 1u) ? sacc[j][e] * scale_log2 : -INFINITY;
+            tmax = fmaxf(tmax, x[j][e]);
+        }
+    tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 1));
+    tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 2));
+    const bool grow = __any_sync(0xffffffffu, tmax > m_run + kRescaleSlack);
+    alpha = 1.f;
+    if (grow) {
+        const float m_new = fmaxf(m_run, tmax);
+        alpha = fast_exp2(m_run - ((m_new == -INFINITY) ? 0.f : m_new));
+        m_run = m_new;
+    }
+    const float m_use = (m_run == -INFINITY) ? 0.f : m_run;
+#pragma unroll
+    for (int j = 0; j < 2; ++j)
+#pragma unroll
+        for (int e = 0; e < 2; ++e) pf[j][e] = fast_exp2(x[j][e] - m_use);
+    return grow;
+}
+
+// O^T accumulators hold rows 2tq, 2tq+1; their alphas come from lanes 8tq and 8tq+4.
+template <int D>
+__device__ __forceinline__ void rescale_o(float (&oacc)[D / 16][4], float alpha, int tq) {
+    const float alpha0 = __shfl_sync(0xffffffffu, alpha, 8 * tq);
+    const float alpha1 = __shfl_sync(0xffffffffu, alpha, 8 * tq + 4);
+#pragma unroll
+    for (int mt = 0; mt < D / 16; ++mt) {
+        oacc[mt][0] *= alpha0;
+        oacc[mt][1] *= alpha1;
+        oacc[mt][2] *= alpha0;
+        oacc[mt][3] *= alpha1;
+    }
+}
+
+// Q8_0 q.K of one 32-element block b for the two 8-cell n-tiles: exact f16 K lanes, one
+// fresh fp32 accumulator per block, then the block's K scale multiplies it into the scores.
+__device__ __forceinline__ void q8_qk_block(float (&sacc)[2][4], const uint32_t (&qa0)[2], const uint32_t (&qa1)[2],
+                                            const uint32_t (&kw)[2][2], const float (&ksc)[2][2]) {
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+        float cb[4] = {0.f, 0.f, 0.f, 0.f};
+        const uint32_t w0 = kw[j][0] ^ 0x80808080u, w1 = kw[j][1] ^ 0x80808080u;
+        mma_16816(cb, qa0[0], 0u, qa0[1], 0u, i8x2_lo(w0), i8x2_hi(w0));
+        mma_16816(cb, qa1[0], 0u, qa1[1], 0u, i8x2_lo(w1), i8x2_hi(w1));
+        sacc[j][0] = fmaf(cb[0], ksc[j][0], sacc[j][0]);
+        sacc[j][1] = fmaf(cb[1], ksc[j][1], sacc[j][1]);
+    }
+}
+
+// Q8_0 O^T += V^T P'^T for block b (m-tiles 2b, 2b+1).  vw holds the block's 4 bytes of
+// head dims 32b + 4gq .. +3 for cells 2tq, 2tq+1, 2tq+8, 2tq+9; pb0/pb1 hold P times the
+// cells' V scales.
+__device__ __forceinline__ void q8_pv_block(float (&o0)[4], float (&o1)[4], const uint32_t (&vw)[4], uint32_t pb0,
+                                            uint32_t pb1) {
+    const uint32_t f0 = vw[0] ^ 0x80808080u, f1 = vw[1] ^ 0x80808080u;
+    const uint32_t f2 = vw[2] ^ 0x80808080u, f3 = vw[3] ^ 0x80808080u;
+    // interleave the two cells of each pair: bytes 0,1 (m-tile 2b) and bytes 2,3 (2b+1)
+    const uint32_t u00 = prmt_b32(f0, f1, 0x5140u), u01 = prmt_b32(f0, f1, 0x7362u);
+    const uint32_t u10 = prmt_b32(f2, f3, 0x5140u), u11 = prmt_b32(f2, f3, 0x7362u);
+    mma_16816(o0, i8x2_lo(u00), i8x2_hi(u00), i8x2_lo(u10), i8x2_hi(u10), pb0, pb1);
+    mma_16816(o1, i8x2_lo(u01), i8x2_hi(u01), i8x2_lo(u11), i8x2_hi(u11), pb0, pb1);
+}
+
+// Half of cell pair's V scales of block b as one f16x2 (cell a in the low lane).
+__device__ __forceinline__ uint32_t scale_pair(uint2 a, uint2 b2, int blk) {
+    const uint32_t wa = (blk >> 1) ? a.y : a.x;
+    const uint32_t wb = (blk >> 1) ? b2.y : b2.x;
+    return prmt_b32(wa, wb, (blk & 1) ? 0x7632u : 0x5410u);
+}
+
+// Scores of one warp's 16 cells for Q8_0 at head_dim 256: scales as 16-byte rows.
+template <int D>
+__device__ __forceinline__ uint32_t scale_word(const unsigned char* sc, int cell, int blk) {
+    return reinterpret_cast<const uint32_t*>(sc + cell * (D / 16))[blk >> 1];
+}
+
+// One consumer warp's 16 cells of a tile (head_dim 256): scores, online softmax, P V.
 template <int KVT, int D, bool SWZ>
 __device__ __forceinline__ void consume_tile(uint32_t kb, uint32_t vb, const unsigned char* ks,
                                              const unsigned char* vs, uint32_t mask, int warp, int lane,
-                                             const uint32_t (&qa)[D / 16][2], float (&oacc)[D / 16][4],
-                                             float& m_run, float& l_run, float scale_log2) {
+                                             const uint32_t (&qa)[D / 16][2], float (&oacc)[D / 16][4], float& m_run, float& l_run,
+                                             float scale_log2) {
     using G = Geom<KVT, D>;
     const int gq = lane >> 2;
     const int tq = lane & 3;
@@ -131,59 +222,28 @@ __device__ __forceinline__ void consume_tile(uint32_t kb, uint32_t vb, const uns
     } else {
 #pragma unroll
         for (int b = 0; b < D / 32; ++b) {
-            float cb[2][4];
+            uint32_t kw[2][2];
+            float ksc[2][2];
 #pragma unroll
             for (int j = 0; j < 2; ++j) {
-                cb[j][0] = cb[j][1] = cb[j][2] = cb[j][3] = 0.f;
                 const int r = r0 + 8 * j + gq;
                 // block b, half hb: d = 32b + 16hb + 4tq + {0,1 | 2,3}
-                const uint32_t w0 = lds32(sec_addr<SWZ, G::kPadRow>(kb, r, 32 * b + 4 * tq)) ^ 0x80808080u;
-                const uint32_t w1 = lds32(sec_addr<SWZ, G::kPadRow>(kb, r, 32 * b + 16 + 4 * tq)) ^ 0x80808080u;
-                mma_16816(cb[j], qa[2 * b][0], 0u, qa[2 * b][1], 0u, i8x2_lo(w0), i8x2_hi(w0));
-                mma_16816(cb[j], qa[2 * b + 1][0], 0u, qa[2 * b + 1][1], 0u, i8x2_lo(w1), i8x2_hi(w1));
+                kw[j][0] = lds32(sec_addr<SWZ, G::kPadRow>(kb, r, 32 * b + 4 * tq));
+                kw[j][1] = lds32(sec_addr<SWZ, G::kPadRow>(kb, r, 32 * b + 16 + 4 * tq));
+#pragma unroll
+                for (int e = 0; e < 2; ++e)
+                    ksc[j][e] = __half2float(
+                        reinterpret_cast<const __half*>(ks + (r0 + 8 * j + 2 * tq + e) * G::kSclBytes)[b]);
             }
-#pragma unroll
-            for (int j = 0; j < 2; ++j)
-#pragma unroll
-                for (int e = 0; e < 2; ++e) {
-                    const int c = r0 + 8 * j + 2 * tq + e;
-                    const __half dk = reinterpret_cast<const __half*>(ks + c * G::kSclBytes)[b];
-                    sacc[j][e] = fmaf(cb[j][e], __half2float(dk), sacc[j][e]);
-                }
+            q8_qk_block(sacc, qa[2 * b], qa[2 * b + 1], kw, ksc);
         }
     }
 
-    // ---- online softmax (log2 domain) ----
-    float x[2][2];
-    float tmax = -INFINITY;
-#pragma unroll
-    for (int j = 0; j < 2; ++j)
-#pragma unroll
-        for (int e = 0; e < 2; ++e) {
-            const int c = 8 * j + 2 * tq + e;
-            x[j][e] = ((mask >> c) & 1u) ? sacc[j][e] * scale_log2 : -INFINITY;
-            tmax = fmaxf(tmax, x[j][e]);
-        }
-    tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 1));
-    tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 2));
-    const float m_new = fmaxf(m_run, tmax);
-    const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
-    const float alpha = fast_exp2(m_run - m_use);
-    m_run = m_new;
-    float pf[2][2];
-#pragma unroll
-    for (int j = 0; j < 2; ++j)
-#pragma unroll
-        for (int e = 0; e < 2; ++e) pf[j][e] = fast_exp2(x[j][e] - m_use);
-
-    const float alpha0 = __shfl_sync(0xffffffffu, alpha, 8 * tq);
-    const float alpha1 = __shfl_sync(0xffffffffu, alpha, 8 * tq + 4);
-#pragma unroll
-    for (int mt = 0; mt < D / 16; ++mt) {
-        oacc[mt][0] *= alpha0;
-        oacc[mt][1] *= alpha1;
-        oacc[mt][2] *= alpha0;
-        oacc[mt][3] *= alpha1;
+    float alpha, pf[2][2];
+    const bool grow = softmax_step(sacc, mask, tq, scale_log2, m_run, alpha, pf);
+    if (grow) {
+        rescale_o<D>(oacc, alpha, tq);
+        l_run *= alpha;
     }
 
     // ---- O^T += V^T P^T ----
@@ -196,7 +256,7 @@ __device__ __forceinline__ void consume_tile(uint32_t kb, uint32_t vb, const uns
             const float2 r = __half22float2(*reinterpret_cast<const __half2*>(&pb[j]));
             psum += r.x + r.y;
         }
-        l_run = l_run * alpha + psum;
+        l_run += psum;
 #pragma unroll
         for (int mt = 0; mt < D / 16; ++mt) {
             uint32_t a0, a1, a2, a3;
@@ -206,67 +266,23 @@ __device__ __forceinline__ void consume_tile(uint32_t kb, uint32_t vb, const uns
             mma_16816(oacc[mt], a0, a1, a2, a3, pb[0], pb[1]);
         }
     } else {
-        l_run = l_run * alpha + (pf[0][0] + pf[0][1] + pf[1][0] + pf[1][1]);
-        const __half* dv0 = reinterpret_cast<const __half*>(vs + (r0 + 2 * tq) * G::kSclBytes);
-        const __half* dv1 = reinterpret_cast<const __half*>(vs + (r0 + 2 * tq + 1) * G::kSclBytes);
-        const __half* dv2 = reinterpret_cast<const __half*>(vs + (r0 + 2 * tq + 8) * G::kSclBytes);
-        const __half* dv3 = reinterpret_cast<const __half*>(vs + (r0 + 2 * tq + 9) * G::kSclBytes);
+        l_run += (pf[0][0] + pf[0][1]) + (pf[1][0] + pf[1][1]);
+        const uint32_t ph0 = pack_half2(pf[0][0], pf[0][1]);
+        const uint32_t ph1 = pack_half2(pf[1][0], pf[1][1]);
+        const int c0 = r0 + 2 * tq;
 #pragma unroll
         for (int b = 0; b < D / 32; ++b) {
-            const uint32_t pb0 = pack_half2(pf[0][0] * __half2float(dv0[b]), pf[0][1] * __half2float(dv1[b]));
-            const uint32_t pb1 = pack_half2(pf[1][0] * __half2float(dv2[b]), pf[1][1] * __half2float(dv3[b]));
+            const uint32_t s01 = prmt_b32(scale_word<D>(vs, c0, b), scale_word<D>(vs, c0 + 1, b),
+                                          (b & 1) ? 0x7632u : 0x5410u);
+            const uint32_t s89 = prmt_b32(scale_word<D>(vs, c0 + 8, b), scale_word<D>(vs, c0 + 9, b),
+                                          (b & 1) ? 0x7632u : 0x5410u);
             const int off = 32 * b + 4 * gq;
-            const uint32_t w00 = lds32(sec_addr<SWZ, G::kPadRow>(vb, r0 + 2 * tq, off)) ^ 0x80808080u;
-            const uint32_t w01 = lds32(sec_addr<SWZ, G::kPadRow>(vb, r0 + 2 * tq + 1, off)) ^ 0x80808080u;
-            const uint32_t w10 = lds32(sec_addr<SWZ, G::kPadRow>(vb, r0 + 2 * tq + 8, off)) ^ 0x80808080u;
-            const uint32_t w11 = lds32(sec_addr<SWZ, G::kPadRow>(vb, r0 + 2 * tq + 9, off)) ^ 0x80808080u;
-            // interleave the two cells of each pair: bytes 0,1 (hb 0) and bytes 2,3 (hb 1)
-            const uint32_t u0[2] = {prmt_b32(w00, w01, 0x5140u), prmt_b32(w00, w01, 0x7362u)};
-            const uint32_t u1[2] = {prmt_b32(w10, w11, 0x5140u), prmt_b32(w10, w11, 0x7362u)};
-#pragma unroll
-            for (int hb = 0; hb < 2; ++hb)
-                mma_16816(oacc[2 * b + hb], i8x2_lo(u0[hb]), i8x2_hi(u0[hb]), i8x2_lo(u1[hb]), i8x2_hi(u1[hb]), pb0,
-                          pb1);
+            const uint32_t vw[4] = {lds32(sec_addr<SWZ, G::kPadRow>(vb, c0, off)),
+                                    lds32(sec_addr<SWZ, G::kPadRow>(vb, c0 + 1, off)),
+                                    lds32(sec_addr<SWZ, G::kPadRow>(vb, c0 + 8, off)),
+                                    lds32(sec_addr<SWZ, G::kPadRow>(vb, c0 + 9, off))};
+            q8_pv_block(oacc[2 * b], oacc[2 * b + 1], vw, hmul2_u32(ph0, s01), hmul2_u32(ph1, s89));
         }
-    }
-}
-
-// Online-softmax step shared by the consumer paths: masks the 2x2 scores a thread holds
-// for query row gq, updates the running max, rescales O, returns the probabilities.
-__device__ __forceinline__ void softmax_step(const float (&sacc)[2][4], uint32_t mask, int tq, float scale_log2,
-                                             float& m_run, float& alpha, float (&pf)[2][2]) {
-    float x[2][2];
-    float tmax = -INFINITY;
-#pragma unroll
-    for (int j = 0; j < 2; ++j)
-#pragma unroll
-        for (int e = 0; e < 2; ++e) {
-            const int c = 8 * j + 2 * tq + e;
-            x[j][e] = ((mask >> c) & 1u) ? sacc[j][e] * scale_log2 : -INFINITY;
-            tmax = fmaxf(tmax, x[j][e]);
-        }
-    tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 1));
-    tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 2));
-    const float m_new = fmaxf(m_run, tmax);
-    const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
-    alpha = fast_exp2(m_run - m_use);
-    m_run = m_new;
-#pragma unroll
-    for (int j = 0; j < 2; ++j)
-#pragma unroll
-        for (int e = 0; e < 2; ++e) pf[j][e] = fast_exp2(x[j][e] - m_use);
-}
-
-template <int D>
-__device__ __forceinline__ void rescale_o(float (&oacc)[D / 16][4], float alpha, int tq) {
-    const float alpha0 = __shfl_sync(0xffffffffu, alpha, 8 * tq);
-    const float alpha1 = __shfl_sync(0xffffffffu, alpha, 8 * tq + 4);
-#pragma unroll
-    for (int mt = 0; mt < D / 16; ++mt) {
-        oacc[mt][0] *= alpha0;
-        oacc[mt][1] *= alpha1;
-        oacc[mt][2] *= alpha0;
-        oacc[mt][3] *= alpha1;
     }
 }
 
@@ -312,8 +328,10 @@ __device__ __forceinline__ void consume_tile_staged(uint32_t kb, uint32_t vb, co
                 mma_16816(sacc[j], qa[2 * kp + 1][0], 0u, qa[2 * kp + 1][1], 0u, kf[j][kp][2], kf[j][kp][3]);
             }
         float alpha, pf[2][2];
-        softmax_step(sacc, mask, tq, scale_log2, m_run, alpha, pf);
-        rescale_o<D>(oacc, alpha, tq);
+        if (softmax_step(sacc, mask, tq, scale_log2, m_run, alpha, pf)) {
+            rescale_o<D>(oacc, alpha, tq);
+            l_run *= alpha;
+        }
         uint32_t pb[2];
         float psum = 0.f;
 #pragma unroll
@@ -322,7 +340,7 @@ __device__ __forceinline__ void consume_tile_staged(uint32_t kb, uint32_t vb, co
             const float2 r = __half22float2(*reinterpret_cast<const __half2*>(&pb[j]));
             psum += r.x + r.y;
         }
-        l_run = l_run * alpha + psum;
+        l_run += psum;
 #pragma unroll
         for (int mt = 0; mt < 8; ++mt) mma_16816(oacc[mt], vf[mt][0], vf[mt][1], vf[mt][2], vf[mt][3], pb[0], pb[1]);
     } else {
@@ -359,71 +377,120 @@ __device__ __forceinline__ void consume_tile_staged(uint32_t kb, uint32_t vb, co
         mbar_arrive(empty_bar);
 #pragma unroll
         for (int b = 0; b < 4; ++b) {
-            float cb[2][4];
-#pragma unroll
-            for (int j = 0; j < 2; ++j) {
-                cb[j][0] = cb[j][1] = cb[j][2] = cb[j][3] = 0.f;
-                const uint32_t w0 = kw[b][j][0] ^ 0x80808080u, w1 = kw[b][j][1] ^ 0x80808080u;
-                mma_16816(cb[j], qa[2 * b][0], 0u, qa[2 * b][1], 0u, i8x2_lo(w0), i8x2_hi(w0));
-                mma_16816(cb[j], qa[2 * b + 1][0], 0u, qa[2 * b + 1][1], 0u, i8x2_lo(w1), i8x2_hi(w1));
-            }
+            float kscf[2][2];
 #pragma unroll
             for (int j = 0; j < 2; ++j)
 #pragma unroll
-                for (int e = 0; e < 2; ++e) {
-                    const __half* sc = reinterpret_cast<const __half*>(&ksc[j][e]);
-                    sacc[j][e] = fmaf(cb[j][e], __half2float(sc[b]), sacc[j][e]);
-                }
+                for (int e = 0; e < 2; ++e)
+                    kscf[j][e] = __half2float(reinterpret_cast<const __half*>(&ksc[j][e])[b]);
+            q8_qk_block(sacc, qa[2 * b], qa[2 * b + 1], kw[b], kscf);
         }
         float alpha, pf[2][2];
-        softmax_step(sacc, mask, tq, scale_log2, m_run, alpha, pf);
-        rescale_o<D>(oacc, alpha, tq);
-        l_run = l_run * alpha + (pf[0][0] + pf[0][1] + pf[1][0] + pf[1][1]);
-        const __half* dv0 = reinterpret_cast<const __half*>(&vsc[0]);
-        const __half* dv1 = reinterpret_cast<const __half*>(&vsc[1]);
-        const __half* dv2 = reinterpret_cast<const __half*>(&vsc[2]);
-        const __half* dv3 = reinterpret_cast<const __half*>(&vsc[3]);
-#pragma unroll
-        for (int b = 0; b < 4; ++b) {
-            const uint32_t pb0 = pack_half2(pf[0][0] * __half2float(dv0[b]), pf[0][1] * __half2float(dv1[b]));
-            const uint32_t pb1 = pack_half2(pf[1][0] * __half2float(dv2[b]), pf[1][1] * __half2float(dv3[b]));
-            const uint32_t f0 = vw[b][0] ^ 0x80808080u, f1 = vw[b][1] ^ 0x80808080u;
-            const uint32_t f2 = vw[b][2] ^ 0x80808080u, f3 = vw[b][3] ^ 0x80808080u;
-            const uint32_t u0[2] = {prmt_b32(f0, f1, 0x5140u), prmt_b32(f0, f1, 0x7362u)};
-            const uint32_t u1[2] = {prmt_b32(f2, f3, 0x5140u), prmt_b32(f2, f3, 0x7362u)};
-#pragma unroll
-            for (int hb = 0; hb < 2; ++hb)
-                mma_16816(oacc[2 * b + hb], i8x2_lo(u0[hb]), i8x2_hi(u0[hb]), i8x2_lo(u1[hb]), i8x2_hi(u1[hb]), pb0,
-                          pb1);
+        if (softmax_step(sacc, mask, tq, scale_log2, m_run, alpha, pf)) {
+            rescale_o<D>(oacc, alpha, tq);
+            l_run *= alpha;
         }
+        l_run += (pf[0][0] + pf[0][1]) + (pf[1][0] + pf[1][1]);
+        const uint32_t ph0 = pack_half2(pf[0][0], pf[0][1]);
+        const uint32_t ph1 = pack_half2(pf[1][0], pf[1][1]);
+#pragma unroll
+        for (int b = 0; b < 4; ++b)
+            q8_pv_block(oacc[2 * b], oacc[2 * b + 1], vw[b], hmul2_u32(ph0, scale_pair(vsc[0], vsc[1], b)),
+                        hmul2_u32(ph1, scale_pair(vsc[2], vsc[3], b)));
     }
 }
 
+// Loads the query fragments of (sequence s, KV head g): the GQA rows of the head fill the
+// first `group` rows of the m16n8k16 A operand (rows 8-15 and rows >= group stay zero).
 template <int KVT, int D>
-__global__ void __launch_bounds__(kThreads) split_decode_kernel(const __grid_constant__ SplitDecodeParams p) {
+__device__ __forceinline__ void load_q_frags(const SplitDecodeParams& p, int s, int g, int gq, int tq,
+                                             uint32_t (&qa)[D / 16][2]) {
+    const bool row_ok = gq < p.group;
+    const int h = g * p.group + (row_ok ? gq : 0);
+    const uint32_t* qrow = reinterpret_cast<const uint32_t*>(p.q + ((int64_t)s * p.n_head + h) * D);
+#pragma unroll
+    for (int kk = 0; kk < D / 16; ++kk) {
+        int d0, d1;
+        if (KVT == KVATTN_KV_F16) {
+            d0 = 16 * kk + 2 * tq;
+            d1 = d0 + 8;
+        } else {
+            d0 = 32 * (kk >> 1) + 16 * (kk & 1) + 4 * tq;
+            d1 = d0 + 2;
+        }
+        qa[kk][0] = row_ok ? __ldg(qrow + d0 / 2) : 0u;
+        qa[kk][1] = row_ok ? __ldg(qrow + d1 / 2) : 0u;
+    }
+}
+
+// One work unit = (sequence, split, KV head).  Units are numbered with the KV head fastest,
+// so the CTAs that run side by side read the rows of every head of the same cells.
+struct Unit {
+    int s, g;
+    int64_t split_idx;
+    int64_t i0, i1;   // plan entries / cells [i0, i1) of the split
+    int n_tiles;      // 0: nothing to read
+    bool write_empty; // an empty unit still reports (0, -inf)
+};
+
+__device__ __forceinline__ Unit unit_at(const SplitDecodeParams& p, int64_t u) {
+    Unit x;
+    x.g = (int)(u % p.n_head_kv);
+    const int64_t r = u / p.n_head_kv;
+    x.split_idx = r % p.unit_splits;
+    x.s = (int)(r / p.unit_splits);
+    const int64_t cap = p.plan ? p.plan_stride : p.n_cells;
+    // (the length and the descriptor are independent loads: issue both before using either)
+    int64_t L = p.seq_lens != nullptr ? (int64_t)__ldg(p.seq_lens + x.s) : p.fixed_len;
+    const int desc_valid = p.desc != nullptr ? __ldg(&p.desc[(int64_t)x.s * p.n_split + x.split_idx].x) : 1;
+    L = L < 0 ? 0 : L;
+    L = L < p.max_len ? L : p.max_len;
+    L = L < cap ? L : cap;
+    x.i0 = x.split_idx * p.split;
+    x.i1 = (x.i0 + p.split < L) ? x.i0 + p.split : L;
+    const bool empty = x.i0 >= x.i1 || desc_valid == 0;
+    x.n_tiles = empty ? 0 : (int)((x.i1 - x.i0 + kTileCells - 1) / kTileCells);
+    // A fully masked split inside the length reports (0, -inf) for the merge; a split past
+    // the length writes only when the caller asked for every partial slot.
+    x.write_empty = empty && (x.i0 < x.i1 || p.write_beyond);
+    return x;
+}
+
+// Persistent split-decode kernel.  Each CTA walks the units blockIdx.x, blockIdx.x + grid,
+// ...; warp 2 streams the 32-cell tiles of those units through a ring of shared-memory
+// stages without stopping between units, warps 0 and 1 attend to 16 cells of every tile.
+// At the end of a unit warp 1 hands its running max, sum and unnormalised O to warp 0
+// through an exchange area guarded by two mbarriers, and warp 0 writes the unit's partial
+// (normalised O and LSE), so no CTA-wide barrier stalls the ring between units.
+template <int KVT, int D>
+__device__ __forceinline__ void split_decode_body(const SplitDecodeParams& p) {
     using G = Geom<KVT, D>;
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     // 1024-byte alignment of the stage ring (the 128-B swizzle repeats every 8 rows)
     unsigned char* smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
     uint64_t* full_bar = reinterpret_cast<uint64_t*>(smem);
     uint64_t* empty_bar = full_bar + kMaxStages;
-    uint32_t* tile_mask = reinterpret_cast<uint32_t*>(empty_bar + kMaxStages);
+    uint64_t* xchg_bar = empty_bar + kMaxStages;  // [0] warp 1's result is posted, [1] area free
+    uint32_t* tile_mask = reinterpret_cast<uint32_t*>(xchg_bar + 2);
     uint32_t* tile_swz = tile_mask + kMaxStages;
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tile_swz + kMaxStages);
-    unsigned char* stages = smem + kHeaderBytes;
+    float4* xo = reinterpret_cast<float4*>(smem + kHeaderBytes);  // [D/16][32 lanes] of warp 1's O
+    float* xm = reinterpret_cast<float*>(xo + (D / 16) * 32);      // [8] warp 1's running max
+    float* xl = xm + 8;                                             // [8] warp 1's running sum
+    unsigned char* stages = smem + kHeaderBytes + G::kXchgBytes;
 
-    const int split_idx = blockIdx.x;
-    const int g = blockIdx.y;
-    const int s = blockIdx.z;
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const int n_stages = p.n_stages;
+    const int64_t n_units = (int64_t)p.n_seq * p.unit_splits * p.n_head_kv;
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < n_stages; ++i) {
             mbar_init(smem_addr(&full_bar[i]), p.src_lsu ? 64 : G::kArrivals);
             mbar_init(smem_addr(&empty_bar[i]), kConsumerWarps * 32);
         }
+        mbar_init(smem_addr(&xchg_bar[0]), 32);
+        mbar_init(smem_addr(&xchg_bar[1]), 32);
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         fence_proxy_async();
@@ -431,368 +498,391 @@ __global__ void __launch_bounds__(kThreads) split_decode_kernel(const __grid_con
     __syncthreads();
     pdl_wait();
 
-    // The split's range of plan entries / cells.
-    // (the length and the descriptor are independent loads: issue both before using either)
-    const int64_t cap = p.plan ? p.plan_stride : p.n_cells;
-    int64_t L = p.seq_lens != nullptr ? (int64_t)p.seq_lens[s] : p.fixed_len;
-    const int desc_valid = p.desc != nullptr ? p.desc[(int64_t)s * p.n_split + split_idx].x : 1;
-    L = L < 0 ? 0 : L;
-    L = L < p.max_len ? L : p.max_len;
-    L = L < cap ? L : cap;
-    const int64_t i0 = (int64_t)split_idx * p.split;
-    const int64_t i1 = (i0 + p.split < L) ? i0 + p.split : L;
-    const bool empty = i0 >= i1 || desc_valid == 0;
-    const int n_tiles = empty ? 0 : (int)((i1 - i0 + kTileCells - 1) / kTileCells);
-    if (empty) {
-        // Nothing to read.  A fully masked split inside the length still reports (0, -inf)
-        // for the merge; a split past the length writes only when the caller asked for
-        // every partial slot.
-        if (i0 < i1 || p.write_beyond) {
-            const int64_t part = (int64_t)s * p.part_stride + p.part_base + split_idx;
-            const int H = p.n_head;
-            for (int idx = threadIdx.x; idx < p.group * D; idx += kThreads) {
-                const int r = idx / D;
-                const int d = idx - r * D;
-                const int h = g * p.group + r;
-                p.part_o[(part * H + h) * D + d] = 0.f;
-                if (d == 0) p.part_lse[part * H + h] = -INFINITY;
-            }
-        }
-        pdl_launch_dependents();
-        return;
-    }
-
     const int gq = lane >> 2;
     const int tq = lane & 3;
-    float oacc[D / 16][4];
-    float m_run = -INFINITY, l_run = 0.f;
-#pragma unroll
-    for (int i = 0; i < D / 16; ++i) oacc[i][0] = oacc[i][1] = oacc[i][2] = oacc[i][3] = 0.f;
+    const int H = p.n_head;
 
     if (warp == kConsumerWarps) {
         // ------------------------------- producer -------------------------------
         const int64_t Hk = p.n_head_kv;
-        bool bad = false;
-        // plan entries of this lane's cell, prefetched four tiles ahead
-        const int32_t* prow = p.plan != nullptr ? p.plan + (int64_t)s * p.plan_stride : nullptr;
-        auto plan_entry = [&](int tt) -> int32_t {
-            const int64_t i = i0 + (int64_t)tt * kTileCells + lane;
-            return (prow != nullptr && tt < n_tiles && i < i1) ? __ldg(prow + i) : -1;
-        };
-        int32_t e0 = plan_entry(0), e1 = plan_entry(1), e2 = plan_entry(2), e3 = plan_entry(3);
-        for (int t = 0; t < n_tiles; ++t) {
-            const int32_t e = e0;
-            e0 = e1;
-            e1 = e2;
-            e2 = e3;
-            e3 = plan_entry(t + 4);
-            const int st = t % n_stages;
-            const int use = t / n_stages;
-            if (use > 0) {
-                const bool ok =
-                    mbar_wait_bounded(smem_addr(&empty_bar[st]), (uint32_t)((use - 1) & 1), abort_flag,
-                                      p.wait_limit_ns);
-                if (!__all_sync(0xffffffffu, ok)) break;  // the whole warp agrees before any collective
-            }
-            const int64_t tile0 = i0 + (int64_t)t * kTileCells;
-            const int64_t i = tile0 + lane;
-            bool valid = i < i1;
-            int64_t cell = 0;
-            if (valid) {
-                if (p.plan != nullptr) {
-                    if (e < -1 || (int64_t)e >= p.n_cells) {
-                        bad = true;
-                        valid = false;
+        bool bad = false, stop = false;
+        uint32_t T = 0;  // tiles issued by this CTA (ring position)
+        for (int64_t u = blockIdx.x; u < n_units && !stop; u += gridDim.x) {
+            const Unit x = unit_at(p, u);
+            if (x.n_tiles == 0) continue;
+            const int s = x.s, g = x.g, n_tiles = x.n_tiles;
+            const int64_t i0 = x.i0, i1 = x.i1;
+            // plan entries of this lane's cell, prefetched four tiles ahead
+            const int32_t* prow = p.plan != nullptr ? p.plan + (int64_t)s * p.plan_stride : nullptr;
+            auto plan_entry = [&](int tt) -> int32_t {
+                const int64_t i = i0 + (int64_t)tt * kTileCells + lane;
+                return (prow != nullptr && tt < n_tiles && i < i1) ? __ldg(prow + i) : -1;
+            };
+            int32_t e0 = plan_entry(0), e1 = plan_entry(1), e2 = plan_entry(2), e3 = plan_entry(3);
+            for (int t = 0; t < n_tiles; ++t, ++T) {
+                const int32_t e = e0;
+                e0 = e1;
+                e1 = e2;
+                e2 = e3;
+                e3 = plan_entry(t + 4);
+                const int st = (int)(T % (uint32_t)n_stages);
+                const uint32_t use = T / (uint32_t)n_stages;
+                if (use > 0) {
+                    const bool ok =
+                        mbar_wait_bounded(smem_addr(&empty_bar[st]), (use - 1) & 1u, abort_flag, p.wait_limit_ns);
+                    if (!__all_sync(0xffffffffu, ok)) {  // the whole warp agrees before any collective
+                        stop = true;
+                        break;
+                    }
+                }
+                const int64_t tile0 = i0 + (int64_t)t * kTileCells;
+                const int64_t i = tile0 + lane;
+                bool valid = i < i1;
+                int64_t cell = 0;
+                if (valid) {
+                    if (p.plan != nullptr) {
+                        if (e < -1 || (int64_t)e >= p.n_cells) {
+                            bad = true;
+                            valid = false;
+                        } else {
+                            valid = e >= 0;
+                            cell = e;
+                        }
                     } else {
-                        valid = e >= 0;
-                        cell = e;
+                        cell = (int64_t)s * p.n_cells + i;
                     }
-                } else {
-                    cell = (int64_t)s * p.n_cells + i;
                 }
-            }
-            const uint32_t mask = __ballot_sync(0xffffffffu, valid);
-            // One physical run?  offset = cell - entry position must be the same for every
-            // valid lane; the box then starts at the cell of the tile's first entry.
-            int64_t base = (int64_t)s * p.n_cells + tile0;  // no plan: always one run
-            bool run = true;
-            if (p.plan != nullptr) {
-                long long off_lo = valid ? (long long)(cell - i) : LLONG_MAX;
-                long long off_hi = valid ? (long long)(cell - i) : LLONG_MIN;
+                const uint32_t mask = __ballot_sync(0xffffffffu, valid);
+                // One physical run?  offset = cell - entry position must be the same for every
+                // valid lane; the box then starts at the cell of the tile's first entry.
+                int64_t base = (int64_t)s * p.n_cells + tile0;  // no plan: always one run
+                bool run = true;
+                if (p.plan != nullptr) {
+                    long long off_lo = valid ? (long long)(cell - i) : LLONG_MAX;
+                    long long off_hi = valid ? (long long)(cell - i) : LLONG_MIN;
 #pragma unroll
-                for (int o = 16; o > 0; o >>= 1) {
-                    off_lo = min(off_lo, __shfl_xor_sync(0xffffffffu, off_lo, o));
-                    off_hi = max(off_hi, __shfl_xor_sync(0xffffffffu, off_hi, o));
+                    for (int o = 16; o > 0; o >>= 1) {
+                        off_lo = min(off_lo, __shfl_xor_sync(0xffffffffu, off_lo, o));
+                        off_hi = max(off_hi, __shfl_xor_sync(0xffffffffu, off_hi, o));
+                    }
+                    run = mask != 0u && off_lo == off_hi;
+                    base = off_lo + tile0;
                 }
-                run = mask != 0u && off_lo == off_hi;
-                base = off_lo + tile0;
-            }
-            const bool use_tma = run && p.use_tma != 0 && mask != 0u && base > INT_MIN / 2 &&
-                                 base < INT_MAX / 2;
-            unsigned char* stage = stages + st * G::kBytes;
-            const uint32_t bar = smem_addr(&full_bar[st]);
-            if (lane == 0) {
-                tile_mask[st] = mask;
-                tile_swz[st] = use_tma ? 1u : 0u;
-                const uint32_t bytes = use_tma     ? (uint32_t)(2 * G::kSwzSection)
-                                       : p.src_lsu ? 0u  // cp.async completions arrive instead
-                                                   : (uint32_t)__popc(mask) * 2u * (uint32_t)G::kRowBytes;
-                mbar_expect_tx(bar, bytes + (t == 0 ? p.stall_tx : 0u));
-            }
-            __syncwarp();
-            if (use_tma) {
+                const bool use_tma = run && p.use_tma != 0 && mask != 0u && base > INT_MIN / 2 &&
+                                     base < INT_MAX / 2;
+                unsigned char* stage = stages + st * G::kBytes;
+                const uint32_t bar = smem_addr(&full_bar[st]);
                 if (lane == 0) {
-                    const uint32_t kdst = smem_addr(stage);
-                    const uint32_t vdst = kdst + G::kSwzSection;
-#pragma unroll
-                    for (int pl = 0; pl < G::kPlanes; ++pl) {
-                        const int x = pl * (KVT == KVATTN_KV_F16 ? 64 : 128);  // elements of 128 B
-                        tma_load_3d(kdst + pl * kPlaneBytes, &p.tmap_k, x, g, (int)base, bar);
-                        tma_load_3d(vdst + pl * kPlaneBytes, &p.tmap_v, x, g, (int)base, bar);
-                    }
+                    tile_mask[st] = mask;
+                    tile_swz[st] = use_tma ? 1u : 0u;
+                    const uint32_t bytes = use_tma     ? (uint32_t)(2 * G::kSwzSection)
+                                           : p.src_lsu ? 0u  // cp.async completions arrive instead
+                                                       : (uint32_t)__popc(mask) * 2u * (uint32_t)G::kRowBytes;
+                    mbar_expect_tx(bar, bytes + (T == 0 ? p.stall_tx : 0u));
                 }
-            }
-            bool wrote = false;  // generic-proxy writes into the stage by this lane
-            if (!use_tma) {
-                unsigned char* krow = stage + lane * G::kPadRow;
-                unsigned char* vrow = stage + G::kPadSection + lane * G::kPadRow;
-                if (p.src_lsu) {
-                    // 16-byte asynchronous loads, a whole row per group of lanes, so every
-                    // request covers full lines (the source may sit across the host link)
-                    constexpr int kLanesPerRow = G::kRowBytes / 16 < 32 ? G::kRowBytes / 16 : 32;
-                    constexpr int kRowsPerPass = 32 / kLanesPerRow;
-                    constexpr int kChunksPerLane = G::kRowBytes / 16 / kLanesPerRow;
-                    const int sub = lane % kLanesPerRow;
-                    for (int r0 = 0; r0 < kTileCells; r0 += kRowsPerPass) {
-                        const int c = r0 + lane / kLanesPerRow;
-                        const bool cv = __shfl_sync(0xffffffffu, valid, c);
-                        const int64_t ccell = __shfl_sync(0xffffffffu, cell, c);
-                        if (cv) {
-                            const int64_t row = ccell * Hk + g;
-                            const char* ksrc = static_cast<const char*>(p.k) + row * G::kRowBytes;
-                            const char* vsrc = static_cast<const char*>(p.v) + row * G::kRowBytes;
-                            unsigned char* kd = stage + c * G::kPadRow;
-                            unsigned char* vd = stage + G::kPadSection + c * G::kPadRow;
+                __syncwarp();
+                if (use_tma) {
+                    if (lane == 0) {
+                        const uint32_t kdst = smem_addr(stage);
+                        const uint32_t vdst = kdst + G::kSwzSection;
 #pragma unroll
-                            for (int j = 0; j < kChunksPerLane; ++j) {
-                                const int off = 16 * (sub + j * kLanesPerRow);
-                                cp_async_16_cg(smem_addr(kd + off), ksrc + off);
-                                cp_async_16_cg(smem_addr(vd + off), vsrc + off);
-                            }
+                        for (int pl = 0; pl < G::kPlanes; ++pl) {
+                            const int xx = pl * (KVT == KVATTN_KV_F16 ? 64 : 128);  // elements of 128 B
+                            tma_load_3d(kdst + pl * kPlaneBytes, &p.tmap_k, xx, g, (int)base, bar);
+                            tma_load_3d(vdst + pl * kPlaneBytes, &p.tmap_v, xx, g, (int)base, bar);
                         }
                     }
                 }
-                if (valid) {
-                    if (!p.src_lsu) {
-                        const int64_t row = cell * Hk + g;
-                        bulk_g2s(smem_addr(krow), static_cast<const char*>(p.k) + row * G::kRowBytes,
-                                 G::kRowBytes, bar);
-                        bulk_g2s(smem_addr(vrow), static_cast<const char*>(p.v) + row * G::kRowBytes,
-                                 G::kRowBytes, bar);
-                    }
-                } else {
-                    uint4* z = reinterpret_cast<uint4*>(vrow);
+                bool wrote = false;  // generic-proxy writes into the stage by this lane
+                if (!use_tma) {
+                    unsigned char* krow = stage + lane * G::kPadRow;
+                    unsigned char* vrow = stage + G::kPadSection + lane * G::kPadRow;
+                    if (p.src_lsu) {
+                        // 16-byte asynchronous loads, a whole row per group of lanes, so every
+                        // request covers full lines (the source may sit across the host link)
+                        constexpr int kLanesPerRow = G::kRowBytes / 16 < 32 ? G::kRowBytes / 16 : 32;
+                        constexpr int kRowsPerPass = 32 / kLanesPerRow;
+                        constexpr int kChunksPerLane = G::kRowBytes / 16 / kLanesPerRow;
+                        const int sub = lane % kLanesPerRow;
+                        for (int r0 = 0; r0 < kTileCells; r0 += kRowsPerPass) {
+                            const int c = r0 + lane / kLanesPerRow;
+                            const bool cv = __shfl_sync(0xffffffffu, valid, c);
+                            const int64_t ccell = __shfl_sync(0xffffffffu, cell, c);
+                            if (cv) {
+                                const int64_t row = ccell * Hk + g;
+                                const char* ksrc = static_cast<const char*>(p.k) + row * G::kRowBytes;
+                                const char* vsrc = static_cast<const char*>(p.v) + row * G::kRowBytes;
+                                unsigned char* kd = stage + c * G::kPadRow;
+                                unsigned char* vd = stage + G::kPadSection + c * G::kPadRow;
 #pragma unroll
-                    for (int k = 0; k < G::kRowBytes / 16; ++k) z[k] = make_uint4(0, 0, 0, 0);
-                    wrote = true;
-                }
-            }
-            if (KVT == KVATTN_KV_Q8_0) {
-                const uint32_t ks = smem_addr(stage + G::kKsOff + lane * G::kSclBytes);
-                unsigned char* vsp = stage + G::kVsOff + lane * G::kSclBytes;
-                if (valid) {
-                    const int64_t row = cell * Hk + g;
-                    const __half* ksrc = p.k_scale + row * (D / 32);
-                    const __half* vsrc = p.v_scale + row * (D / 32);
-                    if (D == 128) {
-                        cp_async_8(ks, ksrc);
-                        cp_async_8(smem_addr(vsp), vsrc);
+                                for (int j = 0; j < kChunksPerLane; ++j) {
+                                    const int off = 16 * (sub + j * kLanesPerRow);
+                                    cp_async_16_cg(smem_addr(kd + off), ksrc + off);
+                                    cp_async_16_cg(smem_addr(vd + off), vsrc + off);
+                                }
+                            }
+                        }
+                    }
+                    if (valid) {
+                        if (!p.src_lsu) {
+                            const int64_t row = cell * Hk + g;
+                            bulk_g2s(smem_addr(krow), static_cast<const char*>(p.k) + row * G::kRowBytes,
+                                     G::kRowBytes, bar);
+                            bulk_g2s(smem_addr(vrow), static_cast<const char*>(p.v) + row * G::kRowBytes,
+                                     G::kRowBytes, bar);
+                        }
                     } else {
-                        cp_async_16(ks, ksrc);
-                        cp_async_16(smem_addr(vsp), vsrc);
-                    }
-                } else {
-                    uint32_t* zs = reinterpret_cast<uint32_t*>(vsp);
+                        uint4* z = reinterpret_cast<uint4*>(vrow);
 #pragma unroll
-                    for (int k = 0; k < G::kSclBytes / 4; ++k) zs[k] = 0u;
-                    wrote = true;
+                        for (int k = 0; k < G::kRowBytes / 16; ++k) z[k] = make_uint4(0, 0, 0, 0);
+                        wrote = true;
+                    }
                 }
+                if (KVT == KVATTN_KV_Q8_0) {
+                    const uint32_t ks = smem_addr(stage + G::kKsOff + lane * G::kSclBytes);
+                    unsigned char* vsp = stage + G::kVsOff + lane * G::kSclBytes;
+                    if (valid) {
+                        const int64_t row = cell * Hk + g;
+                        const __half* ksrc = p.k_scale + row * (D / 32);
+                        const __half* vsrc = p.v_scale + row * (D / 32);
+                        if (D == 128) {
+                            cp_async_8(ks, ksrc);
+                            cp_async_8(smem_addr(vsp), vsrc);
+                        } else {
+                            cp_async_16(ks, ksrc);
+                            cp_async_16(smem_addr(vsp), vsrc);
+                        }
+                    } else {
+                        uint32_t* zs = reinterpret_cast<uint32_t*>(vsp);
+#pragma unroll
+                        for (int k = 0; k < G::kSclBytes / 4; ++k) zs[k] = 0u;
+                        wrote = true;
+                    }
+                }
+                if (KVT == KVATTN_KV_Q8_0 || p.src_lsu) cp_async_arrive_noinc(bar);
+                if (wrote) fence_proxy_async();  // zero-fills before later async writes to this stage
+                mbar_arrive(bar);
             }
-            if (KVT == KVATTN_KV_Q8_0 || p.src_lsu) cp_async_arrive_noinc(bar);
-            if (wrote) fence_proxy_async();  // zero-fills before later async writes to this stage
-            mbar_arrive(bar);
         }
         if (__any_sync(0xffffffffu, bad) && lane == 0) atomicOr(p.status, KVATTN_DEVICE_BAD_PLAN_ENTRY);
     } else {
         // ------------------------------- consumers -------------------------------
-        const int h = g * p.group + gq;
-        const bool row_ok = gq < p.group;
-        const uint32_t* qrow = reinterpret_cast<const uint32_t*>(p.q + ((int64_t)s * p.n_head + h) * D);
         uint32_t qa[D / 16][2];
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-            int d0, d1;
-            if (KVT == KVATTN_KV_F16) {
-                d0 = 16 * kk + 2 * tq;
-                d1 = d0 + 8;
-            } else {
-                d0 = 32 * (kk >> 1) + 16 * (kk & 1) + 4 * tq;
-                d1 = d0 + 2;
+        int64_t qa_unit = -1;  // unit whose query fragments qa holds
+        uint32_t T = 0;        // tiles consumed (ring position)
+        uint32_t X = 0;        // end-of-unit exchanges done
+        bool stop = false;
+        constexpr float kLn2 = 0.69314718055994530942f;
+        for (int64_t u = blockIdx.x; u < n_units && !stop; u += gridDim.x) {
+            const Unit x = unit_at(p, u);
+            const int64_t part = (int64_t)x.s * p.part_stride + p.part_base + x.split_idx;
+            if (x.n_tiles == 0) {
+                if (warp == 0 && x.write_empty) {
+                    for (int idx = lane; idx < p.group * D; idx += 32) {
+                        const int r = idx / D;
+                        const int d = idx - r * D;
+                        const int h = x.g * p.group + r;
+                        p.part_o[(part * H + h) * D + d] = 0.f;
+                        if (d == 0) p.part_lse[part * H + h] = -INFINITY;
+                    }
+                }
+                continue;
             }
-            qa[kk][0] = row_ok ? __ldg(qrow + d0 / 2) : 0u;
-            qa[kk][1] = row_ok ? __ldg(qrow + d1 / 2) : 0u;
-        }
+            if (qa_unit != u) load_q_frags<KVT, D>(p, x.s, x.g, gq, tq, qa);
+            float oacc[D / 16][4];
+            float m_run = -INFINITY, l_run = 0.f;
+#pragma unroll
+            for (int i = 0; i < D / 16; ++i) oacc[i][0] = oacc[i][1] = oacc[i][2] = oacc[i][3] = 0.f;
 
-        for (int t = 0; t < n_tiles; ++t) {
-            const int st = t % n_stages;
-            const int use = t / n_stages;
-            const bool ok =
-                mbar_wait_bounded(smem_addr(&full_bar[st]), (uint32_t)(use & 1), abort_flag, p.wait_limit_ns);
-            if (!__all_sync(0xffffffffu, ok)) break;
-            const uint32_t mask = (tile_mask[st] >> (warp * kWarpCells)) & 0xffffu;
-            const bool swz = tile_swz[st] != 0u;
-            unsigned char* stage = stages + st * G::kBytes;
-            const uint32_t ebar = smem_addr(&empty_bar[st]);
-            bool released = false;
-            if (mask != 0u) {
-                const unsigned char* ks = stage + G::kKsOff;
-                const unsigned char* vs = stage + G::kVsOff;
-                if (swz) {
-                    const uint32_t kb = smem_addr(stage);
-                    const uint32_t vb = kb + G::kSwzSection;
-                    if (mask != 0xffffu) {
-                        // masked rows came in with the box: zero their V rows (every plane)
-                        const int r = warp * kWarpCells + (lane & 15);
-                        if (lane < 16 && !((mask >> lane) & 1u)) {
+            for (int t = 0; t < x.n_tiles; ++t, ++T) {
+                const int st = (int)(T % (uint32_t)n_stages);
+                const uint32_t use = T / (uint32_t)n_stages;
+                const bool ok =
+                    mbar_wait_bounded(smem_addr(&full_bar[st]), use & 1u, abort_flag, p.wait_limit_ns);
+                if (!__all_sync(0xffffffffu, ok)) {
+                    stop = true;
+                    break;
+                }
+                const uint32_t mask = (tile_mask[st] >> (warp * kWarpCells)) & 0xffffu;
+                const bool swz = tile_swz[st] != 0u;
+                unsigned char* stage = stages + st * G::kBytes;
+                const uint32_t ebar = smem_addr(&empty_bar[st]);
+                bool released = false;
+                if (mask != 0u) {
+                    const unsigned char* ks = stage + G::kKsOff;
+                    const unsigned char* vs = stage + G::kVsOff;
+                    if (swz) {
+                        const uint32_t kb = smem_addr(stage);
+                        const uint32_t vb = kb + G::kSwzSection;
+                        if (mask != 0xffffu) {
+                            // masked rows came in with the box: zero their V rows (every plane)
+                            const int r = warp * kWarpCells + (lane & 15);
+                            if (lane < 16 && !((mask >> lane) & 1u)) {
 #pragma unroll
-                            for (int pl = 0; pl < G::kPlanes; ++pl) {
-                                uint4* z = reinterpret_cast<uint4*>(stage + G::kSwzSection + pl * kPlaneBytes +
-                                                                    r * 128);
+                                for (int pl = 0; pl < G::kPlanes; ++pl) {
+                                    uint4* z = reinterpret_cast<uint4*>(stage + G::kSwzSection + pl * kPlaneBytes +
+                                                                        r * 128);
 #pragma unroll
-                                for (int k = 0; k < 8; ++k) z[k] = make_uint4(0, 0, 0, 0);
+                                    for (int k = 0; k < 8; ++k) z[k] = make_uint4(0, 0, 0, 0);
+                                }
+                                fence_proxy_async();
                             }
-                            fence_proxy_async();
+                            __syncwarp();
                         }
-                        __syncwarp();
-                    }
-                    if constexpr (D == 128) {
-                        consume_tile_staged<KVT, true>(kb, vb, ks, vs, mask, warp, lane, ebar, qa, oacc, m_run,
-                                                       l_run, p.scale_log2);
-                        released = true;
+                        if constexpr (D == 128) {
+                            consume_tile_staged<KVT, true>(kb, vb, ks, vs, mask, warp, lane, ebar, qa, oacc, m_run,
+                                                           l_run, p.scale_log2);
+                            released = true;
+                        } else {
+                            consume_tile<KVT, D, true>(kb, vb, ks, vs, mask, warp, lane, qa, oacc, m_run, l_run,
+                                                       p.scale_log2);
+                        }
                     } else {
-                        consume_tile<KVT, D, true>(kb, vb, ks, vs, mask, warp, lane, qa, oacc, m_run, l_run,
-                                                   p.scale_log2);
+                        const uint32_t kb = smem_addr(stage);
+                        const uint32_t vb = kb + G::kPadSection;
+                        if constexpr (D == 128) {
+                            consume_tile_staged<KVT, false>(kb, vb, ks, vs, mask, warp, lane, ebar, qa, oacc, m_run,
+                                                            l_run, p.scale_log2);
+                            released = true;
+                        } else {
+                            consume_tile<KVT, D, false>(kb, vb, ks, vs, mask, warp, lane, qa, oacc, m_run, l_run,
+                                                        p.scale_log2);
+                        }
                     }
-                } else {
-                    const uint32_t kb = smem_addr(stage);
-                    const uint32_t vb = kb + G::kPadSection;
-                    if constexpr (D == 128) {
-                        consume_tile_staged<KVT, false>(kb, vb, ks, vs, mask, warp, lane, ebar, qa, oacc, m_run,
-                                                        l_run, p.scale_log2);
-                        released = true;
-                    } else {
-                        consume_tile<KVT, D, false>(kb, vb, ks, vs, mask, warp, lane, qa, oacc, m_run, l_run,
-                                                    p.scale_log2);
+                }
+                if (!released) {
+                    __syncwarp();
+                    mbar_arrive(ebar);
+                }
+            }
+            if (stop) break;
+            l_run += __shfl_xor_sync(0xffffffffu, l_run, 1);
+            l_run += __shfl_xor_sync(0xffffffffu, l_run, 2);
+            // the next unit's query fragments load while this unit is combined and written
+            const int64_t un = u + gridDim.x;
+            if (un < n_units) {
+                const Unit y = unit_at(p, un);
+                if (y.n_tiles > 0) {
+                    load_q_frags<KVT, D>(p, y.s, y.g, gq, tq, qa);
+                    qa_unit = un;
+                }
+            }
+
+            // ---------------- combine the two consumer warps, write the partial ----------------
+            if (warp == 1) {
+                if (X > 0) {
+                    const bool ok = mbar_wait_bounded(smem_addr(&xchg_bar[1]), (X - 1) & 1u, abort_flag,
+                                                      p.wait_limit_ns);
+                    if (!__all_sync(0xffffffffu, ok)) break;
+                }
+                if (tq == 0) {
+                    xm[gq] = m_run;
+                    xl[gq] = l_run;
+                }
+#pragma unroll
+                for (int mt = 0; mt < D / 16; ++mt)
+                    xo[mt * 32 + lane] = make_float4(oacc[mt][0], oacc[mt][1], oacc[mt][2], oacc[mt][3]);
+                __syncwarp();
+                mbar_arrive(smem_addr(&xchg_bar[0]));
+            } else {
+                const bool ok =
+                    mbar_wait_bounded(smem_addr(&xchg_bar[0]), X & 1u, abort_flag, p.wait_limit_ns);
+                if (!__all_sync(0xffffffffu, ok)) break;
+                // this lane's O rows are 2tq and 2tq+1; their max / sum sit in lanes 8tq, 8tq+4
+                float f0[2], f1[2], inv[2], lse[2];
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    const float m0 = __shfl_sync(0xffffffffu, m_run, 8 * tq + 4 * e);
+                    const float l0 = __shfl_sync(0xffffffffu, l_run, 8 * tq + 4 * e);
+                    const float m1 = xm[2 * tq + e];
+                    const float l1 = xl[2 * tq + e];
+                    const float M = fmaxf(m0, m1);
+                    f0[e] = (m0 == -INFINITY) ? 0.f : fast_exp2(m0 - M);
+                    f1[e] = (m1 == -INFINITY) ? 0.f : fast_exp2(m1 - M);
+                    const float den = l0 * f0[e] + l1 * f1[e];
+                    const bool have = M != -INFINITY && den > 0.f;
+                    inv[e] = have ? 1.f / den : 0.f;
+                    lse[e] = have ? (M + fast_log2(den)) * kLn2 : -INFINITY;
+                }
+#pragma unroll
+                for (int mt = 0; mt < D / 16; ++mt) {
+                    const float4 o1 = xo[mt * 32 + lane];
+                    oacc[mt][0] = (oacc[mt][0] * f0[0] + o1.x * f1[0]) * inv[0];
+                    oacc[mt][1] = (oacc[mt][1] * f0[1] + o1.y * f1[1]) * inv[1];
+                    oacc[mt][2] = (oacc[mt][2] * f0[0] + o1.z * f1[0]) * inv[0];
+                    oacc[mt][3] = (oacc[mt][3] * f0[1] + o1.w * f1[1]) * inv[1];
+                }
+                __syncwarp();
+                mbar_arrive(smem_addr(&xchg_bar[1]));
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    const int r = 2 * tq + e;
+                    if (r < p.group) {
+                        float* orow = p.part_o + (part * H + x.g * p.group + r) * D;
+                        if (KVT == KVATTN_KV_F16) {
+#pragma unroll
+                            for (int mt = 0; mt < D / 16; ++mt) {
+                                orow[out_dim<KVT>(mt, 0, gq)] = oacc[mt][e];
+                                orow[out_dim<KVT>(mt, 1, gq)] = oacc[mt][2 + e];
+                            }
+                        } else {
+                            // m-tiles 2b, 2b+1 hold dims 32b + 4gq + {0,1,2,3}: one 16-byte store
+#pragma unroll
+                            for (int b = 0; b < D / 32; ++b)
+                                *reinterpret_cast<float4*>(orow + 32 * b + 4 * gq) =
+                                    make_float4(oacc[2 * b][e], oacc[2 * b][2 + e], oacc[2 * b + 1][e],
+                                                oacc[2 * b + 1][2 + e]);
+                        }
+                        if (gq == 0) p.part_lse[part * H + x.g * p.group + r] = lse[e];
                     }
                 }
             }
-            if (!released) {
-                __syncwarp();
-                mbar_arrive(ebar);
-            }
+            ++X;
         }
-        l_run += __shfl_xor_sync(0xffffffffu, l_run, 1);
-        l_run += __shfl_xor_sync(0xffffffffu, l_run, 2);
     }
 
-    // ------------------------- combine the consumer warps -------------------------
+    // Every wait above is bounded, so all warps get here; a timed-out wait left abort set.
     __syncthreads();
-    const bool aborted = *abort_flag != 0;
-    const bool have = !aborted && n_tiles > 0;
-    float* cm = reinterpret_cast<float*>(stages);       // [warps][8] running max (log2 units)
-    float* cl = cm + kConsumerWarps * 8;                // [warps][8] running sum
-    float* xm = cl + kConsumerWarps * 8;                // [8] this CTA's max (log2), -inf: no cell
-    float* xl = xm + 8;                                 // [8] this CTA's sum
-    float* co = xl + 8;                                 // [warps][8][D + 4]; warp 0's rows end up
-                                                        // holding the CTA's unnormalised O
-    if (have && warp < kConsumerWarps) {
-        if (tq == 0) {
-            cm[warp * 8 + gq] = m_run;
-            cl[warp * 8 + gq] = l_run;
-        }
-        float* cw = co + warp * 8 * G::kOStride;
-#pragma unroll
-        for (int mt = 0; mt < D / 16; ++mt) {
-            const int d0 = out_dim<KVT>(mt, 0, gq);
-            const int d1 = out_dim<KVT>(mt, 1, gq);
-            cw[(2 * tq) * G::kOStride + d0] = oacc[mt][0];
-            cw[(2 * tq + 1) * G::kOStride + d0] = oacc[mt][1];
-            cw[(2 * tq) * G::kOStride + d1] = oacc[mt][2];
-            cw[(2 * tq + 1) * G::kOStride + d1] = oacc[mt][3];
-        }
-    }
-    __syncthreads();
-    const int G_rows = p.group;
-    if (threadIdx.x < 8) {
-        const int r = threadIdx.x;
-        float M = -INFINITY, den = 0.f;
-        if (have && r < G_rows) {
-#pragma unroll
-            for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, cm[w * 8 + r]);
-            if (M != -INFINITY) {
-#pragma unroll
-                for (int w = 0; w < kConsumerWarps; ++w)
-                    if (cm[w * 8 + r] != -INFINITY) den = fmaf(fast_exp2(cm[w * 8 + r] - M), cl[w * 8 + r], den);
-            }
-        }
-        xm[r] = den > 0.f ? M : -INFINITY;
-        xl[r] = den;
-    }
-    if (have) {
-        for (int idx = threadIdx.x; idx < G_rows * D; idx += kThreads) {
-            const int r = idx / D;
-            const int d = idx - r * D;
-            float M = -INFINITY;
-#pragma unroll
-            for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, cm[w * 8 + r]);
-            float o = 0.f;
-            if (M != -INFINITY) {
-#pragma unroll
-                for (int w = 0; w < kConsumerWarps; ++w)
-                    if (cm[w * 8 + r] != -INFINITY)
-                        o = fmaf(fast_exp2(cm[w * 8 + r] - M), co[(w * 8 + r) * G::kOStride + d], o);
-            }
-            co[r * G::kOStride + d] = o;  // warp 0's slot: read above by this thread only
-        }
-    }
-    __syncthreads();
-
-    constexpr float kLn2 = 0.69314718055994530942f;
-    const int H = p.n_head;
-    if (aborted) {
-        if (threadIdx.x == 0) atomicOr(p.status, KVATTN_DEVICE_WAIT_TIMEOUT);
-    } else {
-        const int64_t part = (int64_t)s * p.part_stride + p.part_base + split_idx;
-        for (int idx = threadIdx.x; idx < G_rows * D; idx += kThreads) {
-            const int r = idx / D;
-            const int d = idx - r * D;
-            const int h = g * G_rows + r;
-            const bool ok = xm[r] != -INFINITY;
-            p.part_o[(part * H + h) * D + d] = ok ? co[r * G::kOStride + d] / xl[r] : 0.f;
-            if (d == 0) p.part_lse[part * H + h] = ok ? (xm[r] + fast_log2(xl[r])) * kLn2 : -INFINITY;
-        }
-    }
+    if (threadIdx.x == 0 && *abort_flag != 0) atomicOr(p.status, KVATTN_DEVICE_WAIT_TIMEOUT);
     pdl_launch_dependents();
 }
 
-template <int KVT, int D>
-const void* kernel_ptr() {
-    return reinterpret_cast<const void*>(split_decode_kernel<KVT, D>);
+#ifndef KVATTN_Q8_D128_MIN_CTAS
+#define KVATTN_Q8_D128_MIN_CTAS 4
+#endif
+#ifndef KVATTN_Q8_D256_MIN_CTAS
+#define KVATTN_Q8_D256_MIN_CTAS 4
+#endif
+#ifndef KVATTN_F16_D256_MIN_CTAS
+#define KVATTN_F16_D256_MIN_CTAS 1
+#endif
+
+// One kernel per (KV type, head_dim), each with its own register budget: the Q8_0 kernels
+// are capped so that four CTAs fit on an SM (their consumers are latency-bound: four
+// resident CTAs measured faster than both three, with more registers, and five or six,
+// which spill).
+__global__ void __launch_bounds__(kThreads) split_decode_f16_d128(const __grid_constant__ SplitDecodeParams p) {
+    split_decode_body<KVATTN_KV_F16, 128>(p);
+}
+__global__ void __launch_bounds__(kThreads, KVATTN_F16_D256_MIN_CTAS)
+    split_decode_f16_d256(const __grid_constant__ SplitDecodeParams p) {
+    split_decode_body<KVATTN_KV_F16, 256>(p);
+}
+__global__ void __launch_bounds__(kThreads, KVATTN_Q8_D128_MIN_CTAS)
+    split_decode_q8_d128(const __grid_constant__ SplitDecodeParams p) {
+    split_decode_body<KVATTN_KV_Q8_0, 128>(p);
+}
+__global__ void __launch_bounds__(kThreads, KVATTN_Q8_D256_MIN_CTAS)
+    split_decode_q8_d256(const __grid_constant__ SplitDecodeParams p) {
+    split_decode_body<KVATTN_KV_Q8_0, 256>(p);
 }
 
 const void* kernel_for(int kv_type, int head_dim) {
-    if (kv_type == KVATTN_KV_F16) return head_dim == 128 ? kernel_ptr<0, 128>() : kernel_ptr<0, 256>();
-    return head_dim == 128 ? kernel_ptr<1, 128>() : kernel_ptr<1, 256>();
+    if (kv_type == KVATTN_KV_F16)
+        return head_dim == 128 ? reinterpret_cast<const void*>(split_decode_f16_d128)
+                               : reinterpret_cast<const void*>(split_decode_f16_d256);
+    return head_dim == 128 ? reinterpret_cast<const void*>(split_decode_q8_d128)
+                           : reinterpret_cast<const void*>(split_decode_q8_d256);
 }
 
 cudaError_t set_smem_attr(const void* fn) {
@@ -808,8 +898,12 @@ int split_decode_stage_bytes(int kv_type, int head_dim) {
     return head_dim == 128 ? Geom<1, 128>::kBytes : Geom<1, 256>::kBytes;
 }
 
-// header + slack for aligning the ring to 1024 bytes
-int split_decode_header_bytes() { return kHeaderBytes + 1024; }
+// Dynamic shared memory of one CTA: header, slack for aligning the ring to 1024 bytes,
+// the end-of-unit exchange area and the stage ring.
+int split_decode_smem_bytes(int kv_type, int head_dim, int n_stages) {
+    const int xchg = head_dim == 128 ? Geom<0, 128>::kXchgBytes : Geom<0, 256>::kXchgBytes;
+    return kHeaderBytes + 1024 + xchg + n_stages * split_decode_stage_bytes(kv_type, head_dim);
+}
 int split_decode_max_stages() { return kMaxStages; }
 int split_decode_threads() { return kThreads; }
 
@@ -817,11 +911,11 @@ cudaError_t split_decode_occupancy(int kv_type, int head_dim, int n_stages, int*
     const void* fn = kernel_for(kv_type, head_dim);
     cudaError_t err = set_smem_attr(fn);
     if (err != cudaSuccess) return err;
-    const int smem = split_decode_header_bytes() + n_stages * split_decode_stage_bytes(kv_type, head_dim);
-    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks, fn, kThreads, smem);
+    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks, fn, kThreads,
+                                                         split_decode_smem_bytes(kv_type, head_dim, n_stages));
 }
 
-cudaError_t launch_split_decode(const SplitDecodeParams& p, int kv_type, int head_dim, dim3 grid,
+cudaError_t launch_split_decode(const SplitDecodeParams& p, int kv_type, int head_dim, unsigned grid_ctas,
                                 cudaStream_t stream, bool pdl) {
     const void* fn = kernel_for(kv_type, head_dim);
     static std::once_flag once[64][4];
@@ -833,10 +927,9 @@ cudaError_t launch_split_decode(const SplitDecodeParams& p, int kv_type, int hea
     std::call_once(once[dev & 63][which], [&] { attr_err[dev & 63][which] = set_smem_attr(fn); });
     if (attr_err[dev & 63][which] != cudaSuccess) return attr_err[dev & 63][which];
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = grid;
+    cfg.gridDim = dim3(grid_ctas, 1, 1);
     cfg.blockDim = dim3(kThreads, 1, 1);
-    cfg.dynamicSmemBytes =
-        split_decode_header_bytes() + p.n_stages * split_decode_stage_bytes(kv_type, head_dim);
+    cfg.dynamicSmemBytes = split_decode_smem_bytes(kv_type, head_dim, p.n_stages);
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;

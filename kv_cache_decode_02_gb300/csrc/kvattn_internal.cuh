@@ -59,6 +59,8 @@ struct SplitDecodeParams {
     int64_t plan_stride;
     int64_t max_len;
     int64_t n_split;          // splits per sequence (descriptor stride)
+    int64_t unit_splits;      // splits per sequence in this launch: the kernel's work units are
+                              // (sequence, split < unit_splits, KV head), KV head fastest
     int64_t part_stride;      // partial slots per sequence
     int64_t part_base;        // first partial index written (window + tail packs several calls)
     int64_t fixed_len;
@@ -96,10 +98,10 @@ struct MergeParams {
 
 // Launchers (return cudaError_t of the launch).
 cudaError_t launch_split_decode(const SplitDecodeParams& p, int kv_type, int head_dim,
-                                dim3 grid, cudaStream_t stream, bool pdl);
+                                unsigned grid_ctas, cudaStream_t stream, bool pdl);
 cudaError_t launch_merge(const MergeParams& p, cudaStream_t stream, bool pdl);
 int split_decode_stage_bytes(int kv_type, int head_dim);
-int split_decode_header_bytes();
+int split_decode_smem_bytes(int kv_type, int head_dim, int n_stages);
 int split_decode_max_stages();
 int split_decode_max_smem();
 int split_decode_threads();
@@ -269,6 +271,12 @@ __device__ __forceinline__ uint32_t i8x2_lo(uint32_t flipped) {
 }
 __device__ __forceinline__ uint32_t i8x2_hi(uint32_t flipped) {
     return magic_bias_h2(prmt_b32(flipped, 0x64646464u, 0x4342u));
+}
+
+__device__ __forceinline__ uint32_t hmul2_u32(uint32_t a, uint32_t b) {
+    uint32_t r;
+    asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+    return r;
 }
 
 __device__ __forceinline__ void pdl_wait() {

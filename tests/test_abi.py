@@ -58,6 +58,7 @@ def call_decode(kvattn, a):
     (dict(head_dim=64), -2),
     (dict(head_dim=96), -2),
     (dict(split=48), -2),                  # not a multiple of the 32-cell tile
+    (dict(n_seq=70000), -2),               # more sequences than a grid dimension holds
     (dict(split=0), -1),
     (dict(q=None), -1),
     (dict(out=None), -1),
