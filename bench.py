@@ -453,18 +453,37 @@ def run_ours(args):
     step_bytes = data.bytes_per_op * args.layers
     value = step_bytes * world / (ms * 1e-3) / 1e9
 
-    # the dominant kernel alone: split-decode launches bracketed by events
-    # average launch duration: back-to-back launches on the stream, events at both ends
+    # the dominant kernel alone: its average launch duration over back-to-back launches
+    # (one per layer buffer, replayed from a CUDA graph so host launch cost cannot gap
+    # them), events on the launching stream at both ends
     for l in range(args.layers):
         data.call_partials(K, l, stream)
-    n_launch = max(1, args.kernel_reps) * args.layers
+    torch.cuda.synchronize()
+    kgraph = None
+    if not args.eager:
+        kgraph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(kgraph):
+            for l in range(args.layers):
+                data.call_partials(K, l, torch.cuda.current_stream())
+        torch.cuda.synchronize()
+
+    def kernel_pass():
+        if kgraph is not None:
+            kgraph.replay()
+        else:
+            for l in range(args.layers):
+                data.call_partials(K, l, stream)
+    kernel_pass()
+    reps = max(1, args.kernel_reps)
+    n_launch = reps * args.layers
     ka, kb = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     ka.record(stream)
-    for i in range(n_launch):
-        data.call_partials(K, i % args.layers, stream)
+    for _ in range(reps):
+        kernel_pass()
     kb.record(stream)
     torch.cuda.synchronize()
     kern_ms = ka.elapsed_time(kb) / n_launch
+    del kgraph
     achieved = data.bytes_per_op / (kern_ms * 1e-3) / 1e9
     traffic = profiled_traffic("split_decode_f16_qwen3_8b_layer.md")
 

@@ -87,6 +87,13 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map
         : "memory");
 }
 
+// L2 prefetch of one tensor-map box (no shared memory, no completion to wait for).
+__device__ __forceinline__ void tma_prefetch_3d(const CUtensorMap* map, int x, int y, int z) {
+    asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(map), "r"(x), "r"(y),
+                 "r"(z)
+                 : "memory");
+}
+
 __device__ __forceinline__ void fence_proxy_async() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
@@ -496,6 +503,32 @@ __device__ __forceinline__ void split_decode_body(const SplitDecodeParams& p) {
         fence_proxy_async();
     }
     __syncthreads();
+    // One wave (a unit per CTA): dependent launches (the merge, the next call) may be
+    // scheduled at once -- they still wait for this grid to complete before reading
+    // anything it writes -- and this CTA pulls its first tiles into L2 while the previous
+    // kernel drains.  Grids of several units per CTA trigger only at exit: their
+    // dependents, placed as slots free up, would otherwise crowd the CTAs that own an
+    // extra unit onto the SMs that freed first (measured slower on GB300), and prefetched
+    // tiles would wait long enough behind the tail to be evicted from L2.
+    const bool one_wave = (int64_t)gridDim.x >= n_units;
+    if (one_wave) pdl_launch_dependents();
+    if (one_wave && warp == kConsumerWarps && lane == 0 && p.use_tma && p.plan == nullptr && !p.src_lsu &&
+        (int64_t)blockIdx.x < n_units) {
+        // The lengths read here may still change before the dependency wait below; they
+        // only steer these hints, never the loads (boxes outside the cache are not fetched).
+        const Unit x = unit_at(p, blockIdx.x);
+        const int n_pre = x.n_tiles < n_stages ? x.n_tiles : n_stages;
+        for (int t = 0; t < n_pre; ++t) {
+            const int64_t base = (int64_t)x.s * p.n_cells + x.i0 + (int64_t)t * kTileCells;
+            if (base >= INT_MAX / 2) break;
+#pragma unroll
+            for (int pl = 0; pl < G::kPlanes; ++pl) {
+                const int xx = pl * (KVT == KVATTN_KV_F16 ? 64 : 128);
+                tma_prefetch_3d(&p.tmap_k, xx, x.g, (int)base);
+                tma_prefetch_3d(&p.tmap_v, xx, x.g, (int)base);
+            }
+        }
+    }
     pdl_wait();
 
     const int gq = lane >> 2;
@@ -844,7 +877,7 @@ __device__ __forceinline__ void split_decode_body(const SplitDecodeParams& p) {
     // Every wait above is bounded, so all warps get here; a timed-out wait left abort set.
     __syncthreads();
     if (threadIdx.x == 0 && *abort_flag != 0) atomicOr(p.status, KVATTN_DEVICE_WAIT_TIMEOUT);
-    pdl_launch_dependents();
+    if (!one_wave) pdl_launch_dependents();
 }
 
 #ifndef KVATTN_Q8_D128_MIN_CTAS

@@ -24,6 +24,7 @@ __global__ void __launch_bounds__(kDescWarps * 32)
     descriptor_kernel(const int32_t* __restrict__ plan, int64_t plan_stride,
                       const int32_t* __restrict__ seq_lens, int n_seq, int64_t max_len, int split,
                       int64_t n_cells, int64_t n_split, int4* __restrict__ desc, uint32_t* status) {
+    pdl_launch_dependents();  // the decode kernel waits for this grid before reading desc
     pdl_wait();
     const int64_t id = (int64_t)blockIdx.x * kDescWarps + (threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;

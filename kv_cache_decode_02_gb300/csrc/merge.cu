@@ -32,6 +32,8 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const MergeParams 
     __shared__ float wts[kWeightCache];
     extern __shared__ float4 acc_smem[];  // [warps][head_dim / 4]
 
+    // let the next kernel start its prologue; it waits for this grid before reading
+    pdl_launch_dependents();
     pdl_wait();
     const int row = blockIdx.x;  // s * n_rows + h
     const int s = row / p.n_rows;
@@ -150,7 +152,6 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const MergeParams 
             out[ci] = t;
         }
         if (threadIdx.x == 0) p.lse[row] = (W > 0.f) ? M + __logf(W) : -INFINITY;
-        pdl_launch_dependents();
         return;
     }
 
@@ -259,7 +260,6 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const MergeParams 
         out[ci] = t;
     }
     if (threadIdx.x == 0) p.lse[row] = (W > 0.f) ? M + __logf(W) : -INFINITY;
-    pdl_launch_dependents();
 }
 
 }  // namespace
