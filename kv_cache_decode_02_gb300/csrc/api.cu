@@ -170,7 +170,7 @@ bool kvattn::encode_kv_tensor_map(CUtensorMap* map, const void* base, int kv_typ
     const cuuint64_t row_bytes = (cuuint64_t)head_dim * (f16 ? 2 : 1);
     const cuuint64_t dims[3] = {(cuuint64_t)head_dim, (cuuint64_t)n_head_kv, (cuuint64_t)cells};
     const cuuint64_t strides[2] = {row_bytes, row_bytes * (cuuint64_t)n_head_kv};
-    const cuuint32_t box[3] = {f16 ? 64u : 128u, 1u, (cuuint32_t)kTileCells};
+    const cuuint32_t box[3] = {f16 ? 64u : 128u, 1u, (cuuint32_t)split_decode_box_cells(kv_type)};
     const cuuint32_t estr[3] = {1, 1, 1};
     const CUresult r = enc(map, f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8, 3,
                            const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,

@@ -65,10 +65,11 @@ struct Geom {
 };
 
 // Byte address of (row r, byte b) of a K or V section in either layout.
-template <bool SWZ, int PAD_ROW>
+// PLANE: bytes between the 128-byte-wide planes of a section (rows per box x 128).
+template <bool SWZ, int PAD_ROW, int PLANE = kPlaneBytes>
 __device__ __forceinline__ uint32_t sec_addr(uint32_t base, int r, int b) {
     if (SWZ)
-        return base + (b >> 7) * kPlaneBytes + r * 128 + ((((b >> 4) & 7) ^ (r & 7)) << 4) + (b & 15);
+        return base + (b >> 7) * PLANE + r * 128 + ((((b >> 4) & 7) ^ (r & 7)) << 4) + (b & 15);
     return base + r * PAD_ROW + b;
 }
 
@@ -186,21 +187,14 @@ __device__ __forceinline__ void q8_pv_block(float (&o0)[4], float (&o1)[4], cons
     mma_16816(o1, i8x2_lo(u01), i8x2_hi(u01), i8x2_lo(u11), i8x2_hi(u11), pb0, pb1);
 }
 
-// Half of cell pair's V scales of block b as one f16x2 (cell a in the low lane).
-__device__ __forceinline__ uint32_t scale_pair(uint2 a, uint2 b2, int blk) {
-    const uint32_t wa = (blk >> 1) ? a.y : a.x;
-    const uint32_t wb = (blk >> 1) ? b2.y : b2.x;
-    return prmt_b32(wa, wb, (blk & 1) ? 0x7632u : 0x5410u);
-}
-
-// Scores of one warp's 16 cells for Q8_0 at head_dim 256: scales as 16-byte rows.
+// Q8_0 scale word (two half scales) of cell `cell` holding block blk.
 template <int D>
 __device__ __forceinline__ uint32_t scale_word(const unsigned char* sc, int cell, int blk) {
     return reinterpret_cast<const uint32_t*>(sc + cell * (D / 16))[blk >> 1];
 }
 
-// One consumer warp's 16 cells of a tile (head_dim 256): scores, online softmax, P V.
-template <int KVT, int D, bool SWZ>
+// One warp's 16 cells of a tile: scores, online softmax, P V (f16 head_dim 256, Q8_0).
+template <int KVT, int D, bool SWZ, int PLANE = kPlaneBytes>
 __device__ __forceinline__ void consume_tile(uint32_t kb, uint32_t vb, const unsigned char* ks,
                                              const unsigned char* vs, uint32_t mask, int warp, int lane,
                                              const uint32_t (&qa)[D / 16][2], float (&oacc)[D / 16][4], float& m_run, float& l_run,
@@ -220,7 +214,7 @@ __device__ __forceinline__ void consume_tile(uint32_t kb, uint32_t vb, const uns
 #pragma unroll
             for (int j = 0; j < 2; ++j) {
                 uint32_t b0, b1, b2, b3;
-                ldsm_x4(sec_addr<SWZ, G::kPadRow>(kb, r0 + 8 * j + (lane & 7), (kk * 16 + 8 * (lane >> 3)) * 2),
+                ldsm_x4(sec_addr<SWZ, G::kPadRow, PLANE>(kb, r0 + 8 * j + (lane & 7), (kk * 16 + 8 * (lane >> 3)) * 2),
                         b0, b1, b2, b3);
                 mma_16816(sacc[j], qa[kk][0], 0u, qa[kk][1], 0u, b0, b1);
                 mma_16816(sacc[j], qa[kk + 1][0], 0u, qa[kk + 1][1], 0u, b2, b3);
@@ -235,8 +229,8 @@ __device__ __forceinline__ void consume_tile(uint32_t kb, uint32_t vb, const uns
             for (int j = 0; j < 2; ++j) {
                 const int r = r0 + 8 * j + gq;
                 // block b, half hb: d = 32b + 16hb + 4tq + {0,1 | 2,3}
-                kw[j][0] = lds32(sec_addr<SWZ, G::kPadRow>(kb, r, 32 * b + 4 * tq));
-                kw[j][1] = lds32(sec_addr<SWZ, G::kPadRow>(kb, r, 32 * b + 16 + 4 * tq));
+                kw[j][0] = lds32(sec_addr<SWZ, G::kPadRow, PLANE>(kb, r, 32 * b + 4 * tq));
+                kw[j][1] = lds32(sec_addr<SWZ, G::kPadRow, PLANE>(kb, r, 32 * b + 16 + 4 * tq));
 #pragma unroll
                 for (int e = 0; e < 2; ++e)
                     ksc[j][e] = __half2float(
@@ -267,7 +261,7 @@ __device__ __forceinline__ void consume_tile(uint32_t kb, uint32_t vb, const uns
 #pragma unroll
         for (int mt = 0; mt < D / 16; ++mt) {
             uint32_t a0, a1, a2, a3;
-            ldsm_x4_trans(sec_addr<SWZ, G::kPadRow>(vb, r0 + (lane & 7) + 8 * (lane >> 4),
+            ldsm_x4_trans(sec_addr<SWZ, G::kPadRow, PLANE>(vb, r0 + (lane & 7) + 8 * (lane >> 4),
                                                     (16 * mt + 8 * ((lane >> 3) & 1)) * 2),
                           a0, a1, a2, a3);
             mma_16816(oacc[mt], a0, a1, a2, a3, pb[0], pb[1]);
@@ -284,127 +278,69 @@ __device__ __forceinline__ void consume_tile(uint32_t kb, uint32_t vb, const uns
             const uint32_t s89 = prmt_b32(scale_word<D>(vs, c0 + 8, b), scale_word<D>(vs, c0 + 9, b),
                                           (b & 1) ? 0x7632u : 0x5410u);
             const int off = 32 * b + 4 * gq;
-            const uint32_t vw[4] = {lds32(sec_addr<SWZ, G::kPadRow>(vb, c0, off)),
-                                    lds32(sec_addr<SWZ, G::kPadRow>(vb, c0 + 1, off)),
-                                    lds32(sec_addr<SWZ, G::kPadRow>(vb, c0 + 8, off)),
-                                    lds32(sec_addr<SWZ, G::kPadRow>(vb, c0 + 9, off))};
+            const uint32_t vw[4] = {lds32(sec_addr<SWZ, G::kPadRow, PLANE>(vb, c0, off)),
+                                    lds32(sec_addr<SWZ, G::kPadRow, PLANE>(vb, c0 + 1, off)),
+                                    lds32(sec_addr<SWZ, G::kPadRow, PLANE>(vb, c0 + 8, off)),
+                                    lds32(sec_addr<SWZ, G::kPadRow, PLANE>(vb, c0 + 9, off))};
             q8_pv_block(oacc[2 * b], oacc[2 * b + 1], vw, hmul2_u32(ph0, s01), hmul2_u32(ph1, s89));
         }
     }
 }
 
-// head_dim 128: the warp copies every K/V fragment (and Q8_0 scale) of its 16 cells into
-// registers, releases the stage to the producer at once, and only then computes, so the
-// stage is refilled while the tensor-core work runs.
-template <int KVT, bool SWZ>
-__device__ __forceinline__ void consume_tile_staged(uint32_t kb, uint32_t vb, const unsigned char* ks,
-                                                    const unsigned char* vs, uint32_t mask, int warp, int lane,
+// f16 head_dim 128: the warp copies every K/V fragment of its 16 cells into registers,
+// releases the stage to the producer at once, and only then computes, so the stage is
+// refilled while the tensor-core work runs.
+template <bool SWZ>
+__device__ __forceinline__ void consume_tile_staged(uint32_t kb, uint32_t vb, uint32_t mask, int warp, int lane,
                                                     uint32_t empty_bar, const uint32_t (&qa)[8][2],
                                                     float (&oacc)[8][4], float& m_run, float& l_run,
                                                     float scale_log2) {
     constexpr int D = 128;
-    using G = Geom<KVT, D>;
-    const int gq = lane >> 2;
+    using G = Geom<KVATTN_KV_F16, D>;
     const int tq = lane & 3;
     const int r0 = warp * kWarpCells;
     float sacc[2][4];
 #pragma unroll
     for (int j = 0; j < 2; ++j) sacc[j][0] = sacc[j][1] = sacc[j][2] = sacc[j][3] = 0.f;
 
-    if (KVT == KVATTN_KV_F16) {
-        uint32_t kf[2][4][4];
-        uint32_t vf[8][4];
+    uint32_t kf[2][4][4];
+    uint32_t vf[8][4];
 #pragma unroll
-        for (int kp = 0; kp < 4; ++kp)
-#pragma unroll
-            for (int j = 0; j < 2; ++j)
-                ldsm_x4(sec_addr<SWZ, G::kPadRow>(kb, r0 + 8 * j + (lane & 7), (2 * kp * 16 + 8 * (lane >> 3)) * 2),
-                        kf[j][kp][0], kf[j][kp][1], kf[j][kp][2], kf[j][kp][3]);
-#pragma unroll
-        for (int mt = 0; mt < 8; ++mt)
-            ldsm_x4_trans(sec_addr<SWZ, G::kPadRow>(vb, r0 + (lane & 7) + 8 * (lane >> 4),
-                                                    (16 * mt + 8 * ((lane >> 3) & 1)) * 2),
-                          vf[mt][0], vf[mt][1], vf[mt][2], vf[mt][3]);
-        __syncwarp();
-        mbar_arrive(empty_bar);  // every lane: its shared-memory reads are done
-#pragma unroll
-        for (int kp = 0; kp < 4; ++kp)
-#pragma unroll
-            for (int j = 0; j < 2; ++j) {
-                mma_16816(sacc[j], qa[2 * kp][0], 0u, qa[2 * kp][1], 0u, kf[j][kp][0], kf[j][kp][1]);
-                mma_16816(sacc[j], qa[2 * kp + 1][0], 0u, qa[2 * kp + 1][1], 0u, kf[j][kp][2], kf[j][kp][3]);
-            }
-        float alpha, pf[2][2];
-        if (softmax_step(sacc, mask, tq, scale_log2, m_run, alpha, pf)) {
-            rescale_o<D>(oacc, alpha, tq);
-            l_run *= alpha;
-        }
-        uint32_t pb[2];
-        float psum = 0.f;
-#pragma unroll
-        for (int j = 0; j < 2; ++j) {
-            pb[j] = pack_half2(pf[j][0], pf[j][1]);
-            const float2 r = __half22float2(*reinterpret_cast<const __half2*>(&pb[j]));
-            psum += r.x + r.y;
-        }
-        l_run += psum;
-#pragma unroll
-        for (int mt = 0; mt < 8; ++mt) mma_16816(oacc[mt], vf[mt][0], vf[mt][1], vf[mt][2], vf[mt][3], pb[0], pb[1]);
-    } else {
-        uint32_t kw[4][2][2];   // [block][n-tile][half]
-        uint32_t vw[4][4];      // [block][cell 2tq, 2tq+1, 2tq+8, 2tq+9]
-        uint2 ksc[2][2];        // 4 half scales of cell r0 + 8j + 2tq + e
-        uint2 vsc[4];           // 4 half scales of cells 2tq, 2tq+1, 2tq+8, 2tq+9
-#pragma unroll
-        for (int b = 0; b < 4; ++b)
-#pragma unroll
-            for (int j = 0; j < 2; ++j) {
-                const int r = r0 + 8 * j + gq;
-                kw[b][j][0] = lds32(sec_addr<SWZ, G::kPadRow>(kb, r, 32 * b + 4 * tq));
-                kw[b][j][1] = lds32(sec_addr<SWZ, G::kPadRow>(kb, r, 32 * b + 16 + 4 * tq));
-            }
-#pragma unroll
-        for (int b = 0; b < 4; ++b) {
-            const int off = 32 * b + 4 * gq;
-            vw[b][0] = lds32(sec_addr<SWZ, G::kPadRow>(vb, r0 + 2 * tq, off));
-            vw[b][1] = lds32(sec_addr<SWZ, G::kPadRow>(vb, r0 + 2 * tq + 1, off));
-            vw[b][2] = lds32(sec_addr<SWZ, G::kPadRow>(vb, r0 + 2 * tq + 8, off));
-            vw[b][3] = lds32(sec_addr<SWZ, G::kPadRow>(vb, r0 + 2 * tq + 9, off));
-        }
+    for (int kp = 0; kp < 4; ++kp)
 #pragma unroll
         for (int j = 0; j < 2; ++j)
+            ldsm_x4(sec_addr<SWZ, G::kPadRow>(kb, r0 + 8 * j + (lane & 7), (2 * kp * 16 + 8 * (lane >> 3)) * 2),
+                    kf[j][kp][0], kf[j][kp][1], kf[j][kp][2], kf[j][kp][3]);
 #pragma unroll
-            for (int e = 0; e < 2; ++e)
-                ksc[j][e] = *reinterpret_cast<const uint2*>(ks + (r0 + 8 * j + 2 * tq + e) * G::kSclBytes);
-        vsc[0] = *reinterpret_cast<const uint2*>(vs + (r0 + 2 * tq) * G::kSclBytes);
-        vsc[1] = *reinterpret_cast<const uint2*>(vs + (r0 + 2 * tq + 1) * G::kSclBytes);
-        vsc[2] = *reinterpret_cast<const uint2*>(vs + (r0 + 2 * tq + 8) * G::kSclBytes);
-        vsc[3] = *reinterpret_cast<const uint2*>(vs + (r0 + 2 * tq + 9) * G::kSclBytes);
-        __syncwarp();
-        mbar_arrive(empty_bar);
+    for (int mt = 0; mt < 8; ++mt)
+        ldsm_x4_trans(sec_addr<SWZ, G::kPadRow>(vb, r0 + (lane & 7) + 8 * (lane >> 4),
+                                                (16 * mt + 8 * ((lane >> 3) & 1)) * 2),
+                      vf[mt][0], vf[mt][1], vf[mt][2], vf[mt][3]);
+    __syncwarp();
+    mbar_arrive(empty_bar);  // every lane: its shared-memory reads are done
 #pragma unroll
-        for (int b = 0; b < 4; ++b) {
-            float kscf[2][2];
+    for (int kp = 0; kp < 4; ++kp)
 #pragma unroll
-            for (int j = 0; j < 2; ++j)
-#pragma unroll
-                for (int e = 0; e < 2; ++e)
-                    kscf[j][e] = __half2float(reinterpret_cast<const __half*>(&ksc[j][e])[b]);
-            q8_qk_block(sacc, qa[2 * b], qa[2 * b + 1], kw[b], kscf);
+        for (int j = 0; j < 2; ++j) {
+            mma_16816(sacc[j], qa[2 * kp][0], 0u, qa[2 * kp][1], 0u, kf[j][kp][0], kf[j][kp][1]);
+            mma_16816(sacc[j], qa[2 * kp + 1][0], 0u, qa[2 * kp + 1][1], 0u, kf[j][kp][2], kf[j][kp][3]);
         }
-        float alpha, pf[2][2];
-        if (softmax_step(sacc, mask, tq, scale_log2, m_run, alpha, pf)) {
-            rescale_o<D>(oacc, alpha, tq);
-            l_run *= alpha;
-        }
-        l_run += (pf[0][0] + pf[0][1]) + (pf[1][0] + pf[1][1]);
-        const uint32_t ph0 = pack_half2(pf[0][0], pf[0][1]);
-        const uint32_t ph1 = pack_half2(pf[1][0], pf[1][1]);
-#pragma unroll
-        for (int b = 0; b < 4; ++b)
-            q8_pv_block(oacc[2 * b], oacc[2 * b + 1], vw[b], hmul2_u32(ph0, scale_pair(vsc[0], vsc[1], b)),
-                        hmul2_u32(ph1, scale_pair(vsc[2], vsc[3], b)));
+    float alpha, pf[2][2];
+    if (softmax_step(sacc, mask, tq, scale_log2, m_run, alpha, pf)) {
+        rescale_o<D>(oacc, alpha, tq);
+        l_run *= alpha;
     }
+    uint32_t pb[2];
+    float psum = 0.f;
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+        pb[j] = pack_half2(pf[j][0], pf[j][1]);
+        const float2 r = __half22float2(*reinterpret_cast<const __half2*>(&pb[j]));
+        psum += r.x + r.y;
+    }
+    l_run += psum;
+#pragma unroll
+    for (int mt = 0; mt < 8; ++mt) mma_16816(oacc[mt], vf[mt][0], vf[mt][1], vf[mt][2], vf[mt][3], pb[0], pb[1]);
 }
 
 // Loads the query fragments of (sequence s, KV head g): the GQA rows of the head fill the
@@ -463,7 +399,8 @@ __device__ __forceinline__ Unit unit_at(const SplitDecodeParams& p, int64_t u) {
     return x;
 }
 
-// Persistent split-decode kernel.  Each CTA walks the units blockIdx.x, blockIdx.x + grid,
+// Persistent split-decode kernel (f16 KV; Q8_0 runs in q8_self_body below).  Each CTA walks
+// the units blockIdx.x, blockIdx.x + grid,
 // ...; warp 2 streams the 32-cell tiles of those units through a ring of shared-memory
 // stages without stopping between units, warps 0 and 1 attend to 16 cells of every tile.
 // At the end of a unit warp 1 hands its running max, sum and unnormalised O to warp 0
@@ -471,6 +408,7 @@ __device__ __forceinline__ Unit unit_at(const SplitDecodeParams& p, int64_t u) {
 // (normalised O and LSE), so no CTA-wide barrier stalls the ring between units.
 template <int KVT, int D>
 __device__ __forceinline__ void split_decode_body(const SplitDecodeParams& p) {
+    static_assert(KVT == KVATTN_KV_F16, "Q8_0 runs in q8_self_body");
     using G = Geom<KVT, D>;
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     // 1024-byte alignment of the stage ring (the 128-B swizzle repeats every 8 rows)
@@ -671,28 +609,7 @@ __device__ __forceinline__ void split_decode_body(const SplitDecodeParams& p) {
                         wrote = true;
                     }
                 }
-                if (KVT == KVATTN_KV_Q8_0) {
-                    const uint32_t ks = smem_addr(stage + G::kKsOff + lane * G::kSclBytes);
-                    unsigned char* vsp = stage + G::kVsOff + lane * G::kSclBytes;
-                    if (valid) {
-                        const int64_t row = cell * Hk + g;
-                        const __half* ksrc = p.k_scale + row * (D / 32);
-                        const __half* vsrc = p.v_scale + row * (D / 32);
-                        if (D == 128) {
-                            cp_async_8(ks, ksrc);
-                            cp_async_8(smem_addr(vsp), vsrc);
-                        } else {
-                            cp_async_16(ks, ksrc);
-                            cp_async_16(smem_addr(vsp), vsrc);
-                        }
-                    } else {
-                        uint32_t* zs = reinterpret_cast<uint32_t*>(vsp);
-#pragma unroll
-                        for (int k = 0; k < G::kSclBytes / 4; ++k) zs[k] = 0u;
-                        wrote = true;
-                    }
-                }
-                if (KVT == KVATTN_KV_Q8_0 || p.src_lsu) cp_async_arrive_noinc(bar);
+                if (p.src_lsu) cp_async_arrive_noinc(bar);
                 if (wrote) fence_proxy_async();  // zero-fills before later async writes to this stage
                 mbar_arrive(bar);
             }
@@ -742,8 +659,6 @@ __device__ __forceinline__ void split_decode_body(const SplitDecodeParams& p) {
                 const uint32_t ebar = smem_addr(&empty_bar[st]);
                 bool released = false;
                 if (mask != 0u) {
-                    const unsigned char* ks = stage + G::kKsOff;
-                    const unsigned char* vs = stage + G::kVsOff;
                     if (swz) {
                         const uint32_t kb = smem_addr(stage);
                         const uint32_t vb = kb + G::kSwzSection;
@@ -763,23 +678,23 @@ __device__ __forceinline__ void split_decode_body(const SplitDecodeParams& p) {
                             __syncwarp();
                         }
                         if constexpr (D == 128) {
-                            consume_tile_staged<KVT, true>(kb, vb, ks, vs, mask, warp, lane, ebar, qa, oacc, m_run,
-                                                           l_run, p.scale_log2);
+                            consume_tile_staged<true>(kb, vb, mask, warp, lane, ebar, qa, oacc, m_run, l_run,
+                                                      p.scale_log2);
                             released = true;
                         } else {
-                            consume_tile<KVT, D, true>(kb, vb, ks, vs, mask, warp, lane, qa, oacc, m_run, l_run,
-                                                       p.scale_log2);
+                            consume_tile<KVT, D, true>(kb, vb, nullptr, nullptr, mask, warp, lane, qa, oacc, m_run,
+                                                       l_run, p.scale_log2);
                         }
                     } else {
                         const uint32_t kb = smem_addr(stage);
                         const uint32_t vb = kb + G::kPadSection;
                         if constexpr (D == 128) {
-                            consume_tile_staged<KVT, false>(kb, vb, ks, vs, mask, warp, lane, ebar, qa, oacc, m_run,
-                                                            l_run, p.scale_log2);
+                            consume_tile_staged<false>(kb, vb, mask, warp, lane, ebar, qa, oacc, m_run, l_run,
+                                                       p.scale_log2);
                             released = true;
                         } else {
-                            consume_tile<KVT, D, false>(kb, vb, ks, vs, mask, warp, lane, qa, oacc, m_run, l_run,
-                                                        p.scale_log2);
+                            consume_tile<KVT, D, false>(kb, vb, nullptr, nullptr, mask, warp, lane, qa, oacc, m_run,
+                                                        l_run, p.scale_log2);
                         }
                     }
                 }
@@ -852,19 +767,10 @@ __device__ __forceinline__ void split_decode_body(const SplitDecodeParams& p) {
                     const int r = 2 * tq + e;
                     if (r < p.group) {
                         float* orow = p.part_o + (part * H + x.g * p.group + r) * D;
-                        if (KVT == KVATTN_KV_F16) {
 #pragma unroll
-                            for (int mt = 0; mt < D / 16; ++mt) {
-                                orow[out_dim<KVT>(mt, 0, gq)] = oacc[mt][e];
-                                orow[out_dim<KVT>(mt, 1, gq)] = oacc[mt][2 + e];
-                            }
-                        } else {
-                            // m-tiles 2b, 2b+1 hold dims 32b + 4gq + {0,1,2,3}: one 16-byte store
-#pragma unroll
-                            for (int b = 0; b < D / 32; ++b)
-                                *reinterpret_cast<float4*>(orow + 32 * b + 4 * gq) =
-                                    make_float4(oacc[2 * b][e], oacc[2 * b][2 + e], oacc[2 * b + 1][e],
-                                                oacc[2 * b + 1][2 + e]);
+                        for (int mt = 0; mt < D / 16; ++mt) {
+                            orow[out_dim<KVT>(mt, 0, gq)] = oacc[mt][e];
+                            orow[out_dim<KVT>(mt, 1, gq)] = oacc[mt][2 + e];
                         }
                         if (gq == 0) p.part_lse[part * H + x.g * p.group + r] = lse[e];
                     }
@@ -880,20 +786,381 @@ __device__ __forceinline__ void split_decode_body(const SplitDecodeParams& p) {
     if (!one_wave) pdl_launch_dependents();
 }
 
-#ifndef KVATTN_Q8_D128_MIN_CTAS
-#define KVATTN_Q8_D128_MIN_CTAS 4
-#endif
-#ifndef KVATTN_Q8_D256_MIN_CTAS
-#define KVATTN_Q8_D256_MIN_CTAS 4
-#endif
+// ---------------------------------------------------------------------------------------
+// Q8_0: self-loading warps.  The Q8_0 kernels are bound by their consumer warps (every K
+// and V byte costs an int8 -> f16 conversion), so they drop the producer warp: each of the
+// CTA's W warps streams its own 16-cell chunks through a private ring of S stages (TMA
+// boxes of 16 rows for one-run chunks, one bulk copy per row otherwise, cp.async for the
+// scales) and attends to them.  The warps of a CTA take interleaved chunks of the same unit
+// (chunk j goes to warp j mod W) and meet in the same end-of-unit exchange as above.  With
+// no producer warp, all the registers of an SM go to warps that compute.
+// ---------------------------------------------------------------------------------------
+constexpr int kChunkCells = 16;
+
+template <int D>
+struct Q8Self {
+    static constexpr int kRowBytes = D;                            // int8 row per (cell, KV head)
+    static constexpr int kPlanes = D / 128;
+    static constexpr int kPlane = kChunkCells * 128;               // one 128-byte-wide plane
+    static constexpr int kSection = kPlanes * kPlane;              // K (or V) rows of a chunk
+    static constexpr int kChunkBytes = 2 * kSection;               // a multiple of 1024
+    static constexpr int kSclBytes = D / 16;                       // D/32 half scales per row
+    static constexpr int kSclChunk = 2 * kChunkCells * kSclBytes;  // K then V scales
+    static constexpr int kXchgSlot = ((D / 16) * 32 * 16 + 64 + 1023) / 1024 * 1024;
+    static_assert(kChunkBytes % 1024 == 0, "stages must keep the 1024-byte swizzle alignment");
+};
+
+template <int D, int W, int S>
+constexpr int q8_self_smem() {
+    return kHeaderBytes + 1024 + (W - 1) * Q8Self<D>::kXchgSlot + W * S * (Q8Self<D>::kChunkBytes + Q8Self<D>::kSclChunk);
+}
+
+// Position of a warp's load stream: unit u (its fields) and chunk j of it.
+struct ChunkCursor {
+    int64_t u, i0, i1;
+    int s, g, j, n_chunks;
+};
+
+__device__ __forceinline__ int unit_chunks(const Unit& x) {
+    return x.n_tiles == 0 ? 0 : (int)((x.i1 - x.i0 + kChunkCells - 1) / kChunkCells);
+}
+
+// Moves c forward (from chunk c.j of unit c.u) to the first chunk this warp owns; c.u >=
+// n_units afterwards when the warp has no more chunks.
+__device__ __forceinline__ void cursor_seek(const SplitDecodeParams& p, ChunkCursor& c, int64_t n_units, int warp) {
+    while (c.u < n_units && c.j >= c.n_chunks) {
+        c.u += gridDim.x;
+        c.j = warp;
+        if (c.u < n_units) {
+            const Unit x = unit_at(p, c.u);
+            c.i0 = x.i0;
+            c.i1 = x.i1;
+            c.s = x.s;
+            c.g = x.g;
+            c.n_chunks = unit_chunks(x);
+        }
+    }
+}
+
+template <int D, int W, int S>
+__device__ __forceinline__ void q8_self_body(const SplitDecodeParams& p) {
+    constexpr int KVT = KVATTN_KV_Q8_0;
+    using Q = Q8Self<D>;
+    using G = Geom<KVT, D>;
+    static_assert(G::kSclBytes == Q::kSclBytes, "scale rows");
+    extern __shared__ __align__(1024) unsigned char smem_raw[];
+    unsigned char* smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
+    uint64_t* full_bar = reinterpret_cast<uint64_t*>(smem);  // [W][S]
+    uint64_t* xchg_bar = full_bar + W * S;                    // [0] W-1 warps posted, [1] area free
+    uint32_t* st_mask = reinterpret_cast<uint32_t*>(xchg_bar + 2);  // [W][S]
+    uint32_t* st_swz = st_mask + W * S;                              // [W][S]
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(st_swz + W * S);
+    unsigned char* xchg = smem + kHeaderBytes;  // W-1 slots: [D/16][32 lanes] float4, max[8], sum[8]
+    unsigned char* rings = xchg + (W - 1) * Q::kXchgSlot;
+    unsigned char* scales = rings + W * S * Q::kChunkBytes;
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int gq = lane >> 2;
+    const int tq = lane & 3;
+    const int H = p.n_head;
+    const int64_t n_units = (int64_t)p.n_seq * p.unit_splits * p.n_head_kv;
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < W * S; ++i) mbar_init(smem_addr(&full_bar[i]), 64);
+        mbar_init(smem_addr(&xchg_bar[0]), 32 * (W - 1 > 0 ? W - 1 : 1));
+        mbar_init(smem_addr(&xchg_bar[1]), 32);
+        *abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        fence_proxy_async();
+    }
+    __syncthreads();
+    const bool one_wave = (int64_t)gridDim.x >= n_units;
+    if (one_wave) pdl_launch_dependents();  // see split_decode_body
+    pdl_wait();
+
+    unsigned char* ring = rings + warp * S * Q::kChunkBytes;
+    unsigned char* sring = scales + warp * S * Q::kSclChunk;
+    uint64_t* fb = full_bar + warp * S;
+    bool bad = false;
+
+    // Issues the loads of chunk c.j of unit c.u into stage st.
+    auto issue = [&](const ChunkCursor& c, int st, uint32_t extra_tx) {
+        const int64_t c0 = c.i0 + (int64_t)c.j * kChunkCells;
+        const int64_t i = c0 + lane;
+        bool valid = lane < kChunkCells && i < c.i1;
+        int64_t cell = 0;
+        if (valid) {
+            if (p.plan != nullptr) {
+                const int32_t e = __ldg(p.plan + (int64_t)c.s * p.plan_stride + i);
+                if (e < -1 || (int64_t)e >= p.n_cells) {
+                    bad = true;
+                    valid = false;
+                } else {
+                    valid = e >= 0;
+                    cell = e;
+                }
+            } else {
+                cell = (int64_t)c.s * p.n_cells + i;
+            }
+        }
+        const uint32_t mask = __ballot_sync(0xffffffffu, valid);
+        int64_t base = (int64_t)c.s * p.n_cells + c0;
+        bool run = true;
+        if (p.plan != nullptr) {
+            long long off_lo = valid ? (long long)(cell - i) : LLONG_MAX;
+            long long off_hi = valid ? (long long)(cell - i) : LLONG_MIN;
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) {
+                off_lo = min(off_lo, __shfl_xor_sync(0xffffffffu, off_lo, o));
+                off_hi = max(off_hi, __shfl_xor_sync(0xffffffffu, off_hi, o));
+            }
+            run = mask != 0u && off_lo == off_hi;
+            base = off_lo + c0;
+        }
+        const bool use_tma = run && p.use_tma != 0 && mask != 0u && base > INT_MIN / 2 && base < INT_MAX / 2;
+        unsigned char* stage = ring + st * Q::kChunkBytes;
+        const uint32_t bar = smem_addr(&fb[st]);
+        if (lane == 0) {
+            st_mask[warp * S + st] = mask;
+            st_swz[warp * S + st] = use_tma ? 1u : 0u;
+            const uint32_t bytes = use_tma ? (uint32_t)Q::kChunkBytes : (uint32_t)__popc(mask) * 2u * (uint32_t)Q::kRowBytes;
+            mbar_expect_tx(bar, bytes + extra_tx);
+        }
+        __syncwarp();
+        const int64_t Hk = p.n_head_kv;
+        if (use_tma) {
+            if (lane == 0) {
+                const uint32_t kdst = smem_addr(stage);
+#pragma unroll
+                for (int pl = 0; pl < Q::kPlanes; ++pl) {
+                    tma_load_3d(kdst + pl * Q::kPlane, &p.tmap_k, pl * 128, c.g, (int)base, bar);
+                    tma_load_3d(kdst + Q::kSection + pl * Q::kPlane, &p.tmap_v, pl * 128, c.g, (int)base, bar);
+                }
+            }
+        } else if (valid) {
+            const int64_t row = cell * Hk + c.g;
+            bulk_g2s(smem_addr(stage + lane * Q::kRowBytes), static_cast<const char*>(p.k) + row * Q::kRowBytes,
+                     Q::kRowBytes, bar);
+            bulk_g2s(smem_addr(stage + Q::kSection + lane * Q::kRowBytes),
+                     static_cast<const char*>(p.v) + row * Q::kRowBytes, Q::kRowBytes, bar);
+        }
+        // scales: a masked cell's are zero, so its (finite) int8 row contributes nothing
+        if (lane < kChunkCells) {
+            unsigned char* ksd = sring + st * Q::kSclChunk + lane * Q::kSclBytes;
+            unsigned char* vsd = ksd + kChunkCells * Q::kSclBytes;
+            if (valid) {
+                const int64_t row = cell * Hk + c.g;
+                if (D == 128) {
+                    cp_async_8(smem_addr(ksd), p.k_scale + row * (D / 32));
+                    cp_async_8(smem_addr(vsd), p.v_scale + row * (D / 32));
+                } else {
+                    cp_async_16(smem_addr(ksd), p.k_scale + row * (D / 32));
+                    cp_async_16(smem_addr(vsd), p.v_scale + row * (D / 32));
+                }
+            } else {
+#pragma unroll
+                for (int k = 0; k < Q::kSclBytes / 4; ++k) {
+                    reinterpret_cast<uint32_t*>(ksd)[k] = 0u;
+                    reinterpret_cast<uint32_t*>(vsd)[k] = 0u;
+                }
+            }
+        }
+        cp_async_arrive_noinc(bar);
+        mbar_arrive(bar);
+    };
+
+    // Prime the ring with this warp's first S chunks.
+    ChunkCursor ld;
+    ld.u = (int64_t)blockIdx.x - gridDim.x;  // seek loads unit blockIdx.x
+    ld.j = 0;
+    ld.n_chunks = 0;
+    cursor_seek(p, ld, n_units, warp);
+    uint32_t L = 0;  // chunks issued
+    for (; L < (uint32_t)S && ld.u < n_units; ++L) {
+        issue(ld, (int)L, L == 0 ? p.stall_tx : 0u);
+        ++ld.j;
+        ld.j += W - 1;
+        cursor_seek(p, ld, n_units, warp);
+    }
+
+    uint32_t qa[D / 16][2];
+    int64_t qa_unit = -1;
+    uint32_t C = 0;  // chunks consumed
+    uint32_t X = 0;  // exchanges
+    bool stop = false;
+    constexpr float kLn2 = 0.69314718055994530942f;
+    for (int64_t u = blockIdx.x; u < n_units && !stop; u += gridDim.x) {
+        const Unit x = unit_at(p, u);
+        const int64_t part = (int64_t)x.s * p.part_stride + p.part_base + x.split_idx;
+        if (x.n_tiles == 0) {
+            if (warp == 0 && x.write_empty) {
+                for (int idx = lane; idx < p.group * D; idx += 32) {
+                    const int r = idx / D;
+                    const int d = idx - r * D;
+                    const int h = x.g * p.group + r;
+                    p.part_o[(part * H + h) * D + d] = 0.f;
+                    if (d == 0) p.part_lse[part * H + h] = -INFINITY;
+                }
+            }
+            continue;
+        }
+        if (qa_unit != u) load_q_frags<KVT, D>(p, x.s, x.g, gq, tq, qa);
+        float oacc[D / 16][4];
+        float m_run = -INFINITY, l_run = 0.f;
+#pragma unroll
+        for (int i = 0; i < D / 16; ++i) oacc[i][0] = oacc[i][1] = oacc[i][2] = oacc[i][3] = 0.f;
+        const int nch = unit_chunks(x);
+        for (int j = warp; j < nch; j += W, ++C) {
+            const int st = (int)(C % (uint32_t)S);
+            const bool ok = mbar_wait_bounded(smem_addr(&fb[st]), (C / (uint32_t)S) & 1u, abort_flag, p.wait_limit_ns);
+            if (!__all_sync(0xffffffffu, ok)) {
+                stop = true;
+                break;
+            }
+            const uint32_t mask = st_mask[warp * S + st] & 0xffffu;
+            const bool swz = st_swz[warp * S + st] != 0u;
+            const uint32_t kb = smem_addr(ring + st * Q::kChunkBytes);
+            const uint32_t vb = kb + Q::kSection;
+            const unsigned char* ks = sring + st * Q::kSclChunk;
+            const unsigned char* vs = ks + kChunkCells * Q::kSclBytes;
+            // (fragments are read straight from the stage: staging them in registers first
+            // measured slower here, the extra registers spill at this CTA count)
+            if (mask != 0u) {
+                if (swz)
+                    consume_tile<KVT, D, true, Q::kPlane>(kb, vb, ks, vs, mask, 0, lane, qa, oacc, m_run, l_run,
+                                                          p.scale_log2);
+                else
+                    consume_tile<KVT, D, false, Q::kPlane>(kb, vb, ks, vs, mask, 0, lane, qa, oacc, m_run, l_run,
+                                                           p.scale_log2);
+            }
+            // refill the stage just read with the chunk S ahead (every lane's reads are done)
+            __syncwarp();
+            if (ld.u < n_units) {
+                fence_proxy_async();
+                issue(ld, st, 0u);
+                ++L;
+                ld.j += W;
+                cursor_seek(p, ld, n_units, warp);
+            }
+        }
+        if (stop) break;
+        l_run += __shfl_xor_sync(0xffffffffu, l_run, 1);
+        l_run += __shfl_xor_sync(0xffffffffu, l_run, 2);
+        const int64_t un = u + gridDim.x;
+        if (un < n_units) {
+            const Unit y = unit_at(p, un);
+            if (y.n_tiles > 0) {
+                load_q_frags<KVT, D>(p, y.s, y.g, gq, tq, qa);
+                qa_unit = un;
+            }
+        }
+        if constexpr (W > 1) {
+            if (warp > 0) {
+                if (X > 0) {
+                    const bool ok = mbar_wait_bounded(smem_addr(&xchg_bar[1]), (X - 1) & 1u, abort_flag, p.wait_limit_ns);
+                    if (!__all_sync(0xffffffffu, ok)) break;
+                }
+                unsigned char* slot = xchg + (warp - 1) * Q::kXchgSlot;
+                float4* xo = reinterpret_cast<float4*>(slot);
+                float* xm = reinterpret_cast<float*>(xo + (D / 16) * 32);
+                if (tq == 0) {
+                    xm[gq] = m_run;
+                    xm[8 + gq] = l_run;
+                }
+#pragma unroll
+                for (int mt = 0; mt < D / 16; ++mt)
+                    xo[mt * 32 + lane] = make_float4(oacc[mt][0], oacc[mt][1], oacc[mt][2], oacc[mt][3]);
+                __syncwarp();
+                mbar_arrive(smem_addr(&xchg_bar[0]));
+                ++X;
+                continue;
+            }
+            const bool ok = mbar_wait_bounded(smem_addr(&xchg_bar[0]), X & 1u, abort_flag, p.wait_limit_ns);
+            if (!__all_sync(0xffffffffu, ok)) break;
+        }
+        // warp 0: combine the W warps' (max, sum, O) for rows 2tq, 2tq+1 and write the partial
+        float mw[W][2], lw[W][2];
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+            mw[0][e] = __shfl_sync(0xffffffffu, m_run, 8 * tq + 4 * e);
+            lw[0][e] = __shfl_sync(0xffffffffu, l_run, 8 * tq + 4 * e);
+#pragma unroll
+            for (int w = 1; w < W; ++w) {
+                const float* xm = reinterpret_cast<const float*>(xchg + (w - 1) * Q::kXchgSlot + (D / 16) * 32 * 16);
+                mw[w][e] = xm[2 * tq + e];
+                lw[w][e] = xm[8 + 2 * tq + e];
+            }
+        }
+        float fw[W][2], inv[2], lse[2];
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+            float M = mw[0][e];
+#pragma unroll
+            for (int w = 1; w < W; ++w) M = fmaxf(M, mw[w][e]);
+            float den = 0.f;
+#pragma unroll
+            for (int w = 0; w < W; ++w) {
+                fw[w][e] = (mw[w][e] == -INFINITY) ? 0.f : fast_exp2(mw[w][e] - M);
+                den = fmaf(lw[w][e], fw[w][e], den);
+            }
+            const bool have = M != -INFINITY && den > 0.f;
+            inv[e] = have ? 1.f / den : 0.f;
+            lse[e] = have ? (M + fast_log2(den)) * kLn2 : -INFINITY;
+        }
+#pragma unroll
+        for (int mt = 0; mt < D / 16; ++mt) {
+            float o0 = oacc[mt][0] * fw[0][0], o1 = oacc[mt][1] * fw[0][1];
+            float o2 = oacc[mt][2] * fw[0][0], o3 = oacc[mt][3] * fw[0][1];
+#pragma unroll
+            for (int w = 1; w < W; ++w) {
+                const float4 t = reinterpret_cast<const float4*>(xchg + (w - 1) * Q::kXchgSlot)[mt * 32 + lane];
+                o0 = fmaf(t.x, fw[w][0], o0);
+                o1 = fmaf(t.y, fw[w][1], o1);
+                o2 = fmaf(t.z, fw[w][0], o2);
+                o3 = fmaf(t.w, fw[w][1], o3);
+            }
+            oacc[mt][0] = o0 * inv[0];
+            oacc[mt][1] = o1 * inv[1];
+            oacc[mt][2] = o2 * inv[0];
+            oacc[mt][3] = o3 * inv[1];
+        }
+        if constexpr (W > 1) {
+            __syncwarp();
+            mbar_arrive(smem_addr(&xchg_bar[1]));
+        }
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+            const int r = 2 * tq + e;
+            if (r < p.group) {
+                float* orow = p.part_o + (part * H + x.g * p.group + r) * D;
+#pragma unroll
+                for (int b = 0; b < D / 32; ++b)
+                    *reinterpret_cast<float4*>(orow + 32 * b + 4 * gq) =
+                        make_float4(oacc[2 * b][e], oacc[2 * b][2 + e], oacc[2 * b + 1][e], oacc[2 * b + 1][2 + e]);
+                if (gq == 0) p.part_lse[part * H + x.g * p.group + r] = lse[e];
+            }
+        }
+        ++X;
+    }
+    if (__any_sync(0xffffffffu, bad) && lane == 0) atomicOr(p.status, KVATTN_DEVICE_BAD_PLAN_ENTRY);
+    // Every wait above is bounded, so all warps get here; a timed-out wait left abort set.
+    __syncthreads();
+    if (threadIdx.x == 0 && *abort_flag != 0) atomicOr(p.status, KVATTN_DEVICE_WAIT_TIMEOUT);
+    if (!one_wave) pdl_launch_dependents();
+}
+
 #ifndef KVATTN_F16_D256_MIN_CTAS
 #define KVATTN_F16_D256_MIN_CTAS 1
 #endif
 
-// One kernel per (KV type, head_dim), each with its own register budget: the Q8_0 kernels
-// are capped so that four CTAs fit on an SM (their consumers are latency-bound: four
-// resident CTAs measured faster than both three, with more registers, and five or six,
-// which spill).
+// Q8_0 geometry: warps per CTA, ring stages per warp, CTAs per SM.  head_dim 128: three
+// warps of 168 registers, four CTAs on an SM (twelve computing warps); head_dim 256: four
+// warps of up to 255 registers, two CTAs (eight computing warps, no spills).
+constexpr int kQ8W128 = 3, kQ8S128 = 3, kQ8B128 = 4;
+constexpr int kQ8W256 = 4, kQ8S256 = 2, kQ8B256 = 2;
+
+// One kernel per (KV type, head_dim), each with its own register budget.
 __global__ void __launch_bounds__(kThreads) split_decode_f16_d128(const __grid_constant__ SplitDecodeParams p) {
     split_decode_body<KVATTN_KV_F16, 128>(p);
 }
@@ -901,13 +1168,13 @@ __global__ void __launch_bounds__(kThreads, KVATTN_F16_D256_MIN_CTAS)
     split_decode_f16_d256(const __grid_constant__ SplitDecodeParams p) {
     split_decode_body<KVATTN_KV_F16, 256>(p);
 }
-__global__ void __launch_bounds__(kThreads, KVATTN_Q8_D128_MIN_CTAS)
+__global__ void __launch_bounds__(kQ8W128 * 32, kQ8B128)
     split_decode_q8_d128(const __grid_constant__ SplitDecodeParams p) {
-    split_decode_body<KVATTN_KV_Q8_0, 128>(p);
+    q8_self_body<128, kQ8W128, kQ8S128>(p);
 }
-__global__ void __launch_bounds__(kThreads, KVATTN_Q8_D256_MIN_CTAS)
+__global__ void __launch_bounds__(kQ8W256 * 32, kQ8B256)
     split_decode_q8_d256(const __grid_constant__ SplitDecodeParams p) {
-    split_decode_body<KVATTN_KV_Q8_0, 256>(p);
+    q8_self_body<256, kQ8W256, kQ8S256>(p);
 }
 
 const void* kernel_for(int kv_type, int head_dim) {
@@ -933,10 +1200,21 @@ int split_decode_stage_bytes(int kv_type, int head_dim) {
 
 // Dynamic shared memory of one CTA: header, slack for aligning the ring to 1024 bytes,
 // the end-of-unit exchange area and the stage ring.
+// Q8_0 kernels have a fixed geometry (n_stages is ignored for them).
 int split_decode_smem_bytes(int kv_type, int head_dim, int n_stages) {
+    if (kv_type == KVATTN_KV_Q8_0)
+        return head_dim == 128 ? q8_self_smem<128, kQ8W128, kQ8S128>() : q8_self_smem<256, kQ8W256, kQ8S256>();
     const int xchg = head_dim == 128 ? Geom<0, 128>::kXchgBytes : Geom<0, 256>::kXchgBytes;
     return kHeaderBytes + 1024 + xchg + n_stages * split_decode_stage_bytes(kv_type, head_dim);
 }
+
+int split_decode_block_threads(int kv_type, int head_dim) {
+    if (kv_type == KVATTN_KV_Q8_0) return (head_dim == 128 ? kQ8W128 : kQ8W256) * 32;
+    return kThreads;
+}
+
+// Cells per TMA box of the kernel's tensor maps.
+int split_decode_box_cells(int kv_type) { return kv_type == KVATTN_KV_Q8_0 ? kChunkCells : kTileCells; }
 int split_decode_max_stages() { return kMaxStages; }
 int split_decode_threads() { return kThreads; }
 
@@ -944,7 +1222,7 @@ cudaError_t split_decode_occupancy(int kv_type, int head_dim, int n_stages, int*
     const void* fn = kernel_for(kv_type, head_dim);
     cudaError_t err = set_smem_attr(fn);
     if (err != cudaSuccess) return err;
-    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks, fn, kThreads,
+    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks, fn, split_decode_block_threads(kv_type, head_dim),
                                                          split_decode_smem_bytes(kv_type, head_dim, n_stages));
 }
 
@@ -961,7 +1239,7 @@ cudaError_t launch_split_decode(const SplitDecodeParams& p, int kv_type, int hea
     if (attr_err[dev & 63][which] != cudaSuccess) return attr_err[dev & 63][which];
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid_ctas, 1, 1);
-    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.blockDim = dim3((unsigned)split_decode_block_threads(kv_type, head_dim), 1, 1);
     cfg.dynamicSmemBytes = split_decode_smem_bytes(kv_type, head_dim, p.n_stages);
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];

@@ -102,6 +102,8 @@ cudaError_t launch_split_decode(const SplitDecodeParams& p, int kv_type, int hea
 cudaError_t launch_merge(const MergeParams& p, cudaStream_t stream, bool pdl);
 int split_decode_stage_bytes(int kv_type, int head_dim);
 int split_decode_smem_bytes(int kv_type, int head_dim, int n_stages);
+int split_decode_block_threads(int kv_type, int head_dim);
+int split_decode_box_cells(int kv_type);
 int split_decode_max_stages();
 int split_decode_max_smem();
 int split_decode_threads();
