@@ -786,6 +786,103 @@ __device__ __forceinline__ void split_decode_body(const SplitDecodeParams& p) {
     if (!one_wave) pdl_launch_dependents();
 }
 
+constexpr int kChunkCells = 16;  // cells per chunk of the Q8_0 self-loading warps
+
+__device__ __forceinline__ uint2 lds64(uint32_t addr) {
+    uint2 v;
+    asm volatile("ld.shared.v2.b32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(addr));
+    return v;
+}
+
+// One warp's 16-cell Q8_0 chunk in the 128-byte-swizzled layout of 16-row planes: scores,
+// online softmax, P V.  In a 1024-byte-aligned plane the byte (row r, column b) sits at
+// r*128 + 16*((b >> 4) ^ (r & 7)) + (b & 15); every address below is a per-lane base whose
+// bits 4-6 already hold the row's swizzle key, XOR-ed with 16*(b >> 4) and offset by
+// immediates, so the swizzle costs one logic op per 16-byte column instead of an index
+// computation per load.  The scales of a cell (D/32 halves) are read once per chunk.
+template <int D>
+__device__ __forceinline__ void q8_chunk_swz(uint32_t kb, uint32_t vb, const unsigned char* ks,
+                                             const unsigned char* vs, uint32_t mask, int lane,
+                                             const uint32_t (&qa)[D / 16][2], float (&oacc)[D / 16][4],
+                                             float& m_run, float& l_run, float scale_log2) {
+    constexpr int kPlane = kChunkCells * 128;
+    constexpr int kScl = D / 16;  // bytes of scales per cell
+    const int gq = lane >> 2;
+    const int tq = lane & 3;
+    // K rows gq (n-tile 0) and 8 + gq (+1024); this lane's bytes 4tq.. of each 16-byte column
+    const uint32_t ka = (kb + 128u * gq + 4u * tq) | (16u * gq);
+    // V rows 2tq and 2tq + 1 (and +8, +9 at +1024); bytes 4(gq & 3).. of column 2blk + (gq >> 2)
+    const uint32_t va0 = (vb + 256u * tq + 4u * (gq & 3)) | (16u * ((gq >> 2) ^ (2 * tq)));
+    const uint32_t va1 = (vb + 256u * tq + 128u + 4u * (gq & 3)) | (16u * ((gq >> 2) ^ (2 * tq + 1)));
+    const uint32_t kss = smem_addr(ks) + 2u * kScl * tq;  // cell 2tq's scales; cell c at + (c - 2tq) * kScl
+    const uint32_t vss = smem_addr(vs) + 2u * kScl * tq;
+
+    float sacc[2][4];
+#pragma unroll
+    for (int j = 0; j < 2; ++j) sacc[j][0] = sacc[j][1] = sacc[j][2] = sacc[j][3] = 0.f;
+    // K scales of cells 8j + 2tq + e: D/32 halves each
+    uint32_t ksw[2][2][D / 64];
+#pragma unroll
+    for (int j = 0; j < 2; ++j)
+#pragma unroll
+        for (int e = 0; e < 2; ++e)
+#pragma unroll
+            for (int h = 0; h < D / 128; ++h) {
+                const uint2 w = lds64(kss + (8 * j + e) * kScl + 8 * h);
+                ksw[j][e][2 * h] = w.x;
+                ksw[j][e][2 * h + 1] = w.y;
+            }
+#pragma unroll
+    for (int b = 0; b < D / 32; ++b) {
+        const uint32_t pl = kPlane * (b >> 2);
+        const uint32_t a0 = (ka ^ (32u * (b & 3))) + pl;      // column 2(b & 3): half 0 of block b
+        const uint32_t a1 = (ka ^ (32u * (b & 3) + 16u)) + pl;  // column 2(b & 3) + 1: half 1
+        uint32_t kw[2][2];
+        float ksc[2][2];
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+            kw[j][0] = lds32(a0 + 1024u * j);
+            kw[j][1] = lds32(a1 + 1024u * j);
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                const uint32_t w = ksw[j][e][b >> 1];
+                ksc[j][e] = __half2float(__ushort_as_half((unsigned short)((b & 1) ? (w >> 16) : (w & 0xffffu))));
+            }
+        }
+        q8_qk_block(sacc, qa[2 * b], qa[2 * b + 1], kw, ksc);
+    }
+
+    float alpha, pf[2][2];
+    if (softmax_step(sacc, mask, tq, scale_log2, m_run, alpha, pf)) {
+        rescale_o<D>(oacc, alpha, tq);
+        l_run *= alpha;
+    }
+    l_run += (pf[0][0] + pf[0][1]) + (pf[1][0] + pf[1][1]);
+    const uint32_t ph0 = pack_half2(pf[0][0], pf[0][1]);
+    const uint32_t ph1 = pack_half2(pf[1][0], pf[1][1]);
+    // V scales of cells 2tq, 2tq + 1, 2tq + 8, 2tq + 9
+    uint32_t vsw[4][D / 64];
+#pragma unroll
+    for (int c = 0; c < 4; ++c)
+#pragma unroll
+        for (int h = 0; h < D / 128; ++h) {
+            const uint2 w = lds64(vss + ((c & 1) + 8 * (c >> 1)) * kScl + 8 * h);
+            vsw[c][2 * h] = w.x;
+            vsw[c][2 * h + 1] = w.y;
+        }
+#pragma unroll
+    for (int b = 0; b < D / 32; ++b) {
+        const uint32_t pl = kPlane * (b >> 2);
+        const uint32_t c0 = (va0 ^ (32u * (b & 3))) + pl;
+        const uint32_t c1 = (va1 ^ (32u * (b & 3))) + pl;
+        const uint32_t vw[4] = {lds32(c0), lds32(c1), lds32(c0 + 1024u), lds32(c1 + 1024u)};
+        const uint32_t sel = (b & 1) ? 0x7632u : 0x5410u;
+        const uint32_t s01 = prmt_b32(vsw[0][b >> 1], vsw[1][b >> 1], sel);
+        const uint32_t s89 = prmt_b32(vsw[2][b >> 1], vsw[3][b >> 1], sel);
+        q8_pv_block(oacc[2 * b], oacc[2 * b + 1], vw, hmul2_u32(ph0, s01), hmul2_u32(ph1, s89));
+    }
+}
+
 // ---------------------------------------------------------------------------------------
 // Q8_0: self-loading warps.  The Q8_0 kernels are bound by their consumer warps (every K
 // and V byte costs an int8 -> f16 conversion), so they drop the producer warp: each of the
@@ -795,8 +892,6 @@ __device__ __forceinline__ void split_decode_body(const SplitDecodeParams& p) {
 // (chunk j goes to warp j mod W) and meet in the same end-of-unit exchange as above.  With
 // no producer warp, all the registers of an SM go to warps that compute.
 // ---------------------------------------------------------------------------------------
-constexpr int kChunkCells = 16;
-
 template <int D>
 struct Q8Self {
     static constexpr int kRowBytes = D;                            // int8 row per (cell, KV head)
@@ -1028,8 +1123,7 @@ __device__ __forceinline__ void q8_self_body(const SplitDecodeParams& p) {
             // measured slower here, the extra registers spill at this CTA count)
             if (mask != 0u) {
                 if (swz)
-                    consume_tile<KVT, D, true, Q::kPlane>(kb, vb, ks, vs, mask, 0, lane, qa, oacc, m_run, l_run,
-                                                          p.scale_log2);
+                    q8_chunk_swz<D>(kb, vb, ks, vs, mask, lane, qa, oacc, m_run, l_run, p.scale_log2);
                 else
                     consume_tile<KVT, D, false, Q::kPlane>(kb, vb, ks, vs, mask, 0, lane, qa, oacc, m_run, l_run,
                                                            p.scale_log2);
