@@ -1248,11 +1248,12 @@ __device__ __forceinline__ void q8_self_body(const SplitDecodeParams& p) {
 #define KVATTN_F16_D256_MIN_CTAS 1
 #endif
 
-// Q8_0 geometry: warps per CTA, ring stages per warp, CTAs per SM.  head_dim 128: three
-// warps of 168 registers, four CTAs on an SM (twelve computing warps); head_dim 256: four
-// warps of up to 255 registers, two CTAs (eight computing warps, no spills).
-constexpr int kQ8W128 = 3, kQ8S128 = 3, kQ8B128 = 4;
-constexpr int kQ8W256 = 4, kQ8S256 = 2, kQ8B256 = 2;
+// Q8_0 geometry: warps per CTA, ring stages per warp, CTAs per SM.  head_dim 128: four
+// warps of 128 registers, four CTAs on an SM (sixteen computing warps; measured faster
+// than twelve warps of 168 registers); head_dim 256: two warps of up to 255 registers,
+// four CTAs (eight computing warps, no spills; measured faster than four warps x two CTAs).
+constexpr int kQ8W128 = 4, kQ8S128 = 2, kQ8B128 = 4;
+constexpr int kQ8W256 = 2, kQ8S256 = 2, kQ8B256 = 4;
 
 // One kernel per (KV type, head_dim), each with its own register budget.
 __global__ void __launch_bounds__(kThreads) split_decode_f16_d128(const __grid_constant__ SplitDecodeParams p) {
