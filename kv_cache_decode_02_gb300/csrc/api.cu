@@ -87,6 +87,7 @@ cudaError_t launch_decode_units(SplitDecodeParams p, int kv_type, int head_dim, 
                                 cudaStream_t stream, bool pdl) {
     p.unit_splits = unit_splits;
     const int64_t n_units = (int64_t)p.n_seq * unit_splits * p.n_head_kv;
+    if (n_units > (int64_t)INT32_MAX) return cudaErrorInvalidValue;  // units are numbered in 32 bits
     const int64_t resident = (int64_t)std::max(occupancy(kv_type, head_dim, p.n_stages), 1) * sm_count();
     const int64_t grid = std::min(n_units, resident);
     if (grid < 1) return cudaSuccess;
@@ -156,7 +157,9 @@ int check_shape(const DecodeShape& s) {
     if (s.head_dim != 128 && s.head_dim != 256) return KVATTN_ERR_UNSUPPORTED;
     if (s.split % kTileCells != 0) return KVATTN_ERR_UNSUPPORTED;
     if (s.n_seq > 65535) return KVATTN_ERR_UNSUPPORTED;
-    if ((s.max_len + s.split - 1) / s.split * s.n_head_kv > (int64_t)INT32_MAX) return KVATTN_ERR_UNSUPPORTED;
+    // work units (sequence, split, KV head) are numbered in 32 bits on the device
+    if ((s.max_len + s.split - 1) / s.split * s.n_head_kv * std::max(s.n_seq, 1) > (int64_t)INT32_MAX)
+        return KVATTN_ERR_UNSUPPORTED;
     return KVATTN_OK;
 }
 

@@ -378,10 +378,13 @@ struct Unit {
 
 __device__ __forceinline__ Unit unit_at(const SplitDecodeParams& p, int64_t u) {
     Unit x;
-    x.g = (int)(u % p.n_head_kv);
-    const int64_t r = u / p.n_head_kv;
-    x.split_idx = r % p.unit_splits;
-    x.s = (int)(r / p.unit_splits);
+    // unit counts fit in 32 bits (checked on the host): 32-bit division is far cheaper
+    const uint32_t uu = (uint32_t)u, hk = (uint32_t)p.n_head_kv, us = (uint32_t)p.unit_splits;
+    const uint32_t r = uu / hk;
+    const uint32_t si = r / us;
+    x.g = (int)(uu - r * hk);
+    x.split_idx = (int64_t)(r - si * us);
+    x.s = (int)si;
     const int64_t cap = p.plan ? p.plan_stride : p.n_cells;
     // (the length and the descriptor are independent loads: issue both before using either)
     int64_t L = p.seq_lens != nullptr ? (int64_t)__ldg(p.seq_lens + x.s) : p.fixed_len;
@@ -980,7 +983,65 @@ __device__ __forceinline__ void q8_self_body(const SplitDecodeParams& p) {
     bool bad = false;
 
     // Issues the loads of chunk c.j of unit c.u into stage st.
-    auto issue = [&](const ChunkCursor& c, int st, uint32_t extra_tx) {
+    // Cache without a plan: the chunk's cells are consecutive rows, so the mask, the box
+    // coordinate and the scale rows follow from 32-bit offsets into the unit.
+    auto issue_contiguous = [&](const ChunkCursor& c, int st, uint32_t extra_tx) {
+        const int off = c.j * kChunkCells;
+        const int rem = (int)(c.i1 - c.i0) - off;  // cells of the unit from this chunk on (>= 1)
+        const bool valid = lane < (rem < kChunkCells ? rem : kChunkCells);
+        const uint32_t mask = rem >= kChunkCells ? 0xffffu : (1u << rem) - 1u;
+        const int64_t base = (int64_t)c.s * p.n_cells + c.i0 + off;
+        const bool use_tma = p.use_tma != 0 && base < INT_MAX / 2;
+        unsigned char* stage = ring + st * Q::kChunkBytes;
+        const uint32_t bar = smem_addr(&fb[st]);
+        if (lane == 0) {
+            st_mask[warp * S + st] = mask;
+            st_swz[warp * S + st] = use_tma ? 1u : 0u;
+            const uint32_t bytes = use_tma ? (uint32_t)Q::kChunkBytes : (uint32_t)__popc(mask) * 2u * (uint32_t)Q::kRowBytes;
+            mbar_expect_tx(bar, bytes + extra_tx);
+        }
+        __syncwarp();
+        const int64_t row = (base + lane) * p.n_head_kv + c.g;  // this lane's (cell, KV head) row
+        if (use_tma) {
+            if (lane == 0) {
+                const uint32_t kdst = smem_addr(stage);
+#pragma unroll
+                for (int pl = 0; pl < Q::kPlanes; ++pl) {
+                    tma_load_3d(kdst + pl * Q::kPlane, &p.tmap_k, pl * 128, c.g, (int)base, bar);
+                    tma_load_3d(kdst + Q::kSection + pl * Q::kPlane, &p.tmap_v, pl * 128, c.g, (int)base, bar);
+                }
+            }
+        } else if (valid) {
+            bulk_g2s(smem_addr(stage + lane * Q::kRowBytes), static_cast<const char*>(p.k) + row * Q::kRowBytes,
+                     Q::kRowBytes, bar);
+            bulk_g2s(smem_addr(stage + Q::kSection + lane * Q::kRowBytes),
+                     static_cast<const char*>(p.v) + row * Q::kRowBytes, Q::kRowBytes, bar);
+        }
+        if (lane < kChunkCells) {
+            unsigned char* ksd = sring + st * Q::kSclChunk + lane * Q::kSclBytes;
+            unsigned char* vsd = ksd + kChunkCells * Q::kSclBytes;
+            if (valid) {
+                if (D == 128) {
+                    cp_async_8(smem_addr(ksd), p.k_scale + row * (D / 32));
+                    cp_async_8(smem_addr(vsd), p.v_scale + row * (D / 32));
+                } else {
+                    cp_async_16(smem_addr(ksd), p.k_scale + row * (D / 32));
+                    cp_async_16(smem_addr(vsd), p.v_scale + row * (D / 32));
+                }
+            } else {
+#pragma unroll
+                for (int k = 0; k < Q::kSclBytes / 4; ++k) {
+                    reinterpret_cast<uint32_t*>(ksd)[k] = 0u;
+                    reinterpret_cast<uint32_t*>(vsd)[k] = 0u;
+                }
+            }
+        }
+        cp_async_arrive_noinc(bar);
+        mbar_arrive(bar);
+    };
+
+    // Any cache: plan entries, the one-run test, TMA or per-row copies.
+    auto issue_general = [&](const ChunkCursor& c, int st, uint32_t extra_tx) {
         const int64_t c0 = c.i0 + (int64_t)c.j * kChunkCells;
         const int64_t i = c0 + lane;
         bool valid = lane < kChunkCells && i < c.i1;
@@ -1063,6 +1124,12 @@ __device__ __forceinline__ void q8_self_body(const SplitDecodeParams& p) {
         }
         cp_async_arrive_noinc(bar);
         mbar_arrive(bar);
+    };
+    auto issue = [&](const ChunkCursor& c, int st, uint32_t extra_tx) {
+        if (p.plan == nullptr)
+            issue_contiguous(c, st, extra_tx);
+        else
+            issue_general(c, st, extra_tx);
     };
 
     // Prime the ring with this warp's first S chunks.
