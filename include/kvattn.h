@@ -237,7 +237,12 @@ size_t kvattn_window_tail_workspace_bytes(int n_head, int n_head_kv, int head_di
  *  tile_cells tail cells per host-to-device tile (a positive multiple of tail_split);
  *             tiles are copied into two device staging slots, one tile ahead of the
  *             compute (double buffering), each copy ordered after the decode that last
- *             read its slot.  The first call with a given set of arguments records the
+ *             read its slot.  A tile moves by one copy kernel that reads the pinned
+ *             buffers through their device mapping (cudaHostGetDevicePointer), or by two
+ *             cudaMemcpyAsync when they are not mapped (or KVATTN_TAIL_COPY=0 is set);
+ *             even tiles go on copy_stream, odd tiles on a stream of the context, so one
+ *             copy ramps up while the previous drains.  The first call with a given set of
+ *             arguments records the
  *             whole pipeline as a CUDA graph (on the context's own streams) and launches it
  *             on compute_stream; later calls with the same arguments replay that graph, so
  *             the host enqueues one launch instead of about three operations per tile.  A

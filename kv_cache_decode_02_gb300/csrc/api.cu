@@ -184,7 +184,7 @@ bool kvattn::encode_kv_tensor_map(CUtensorMap* map, const void* base, int kv_typ
 
 // Everything a captured window + tail graph depends on; a call with the same key replays it.
 struct TailGraphKey {
-    const void *q, *k_win, *v_win, *k_tail, *v_tail;
+    const void *q, *k_win, *v_win, *k_tail, *v_tail, *k_tail_dev, *v_tail_dev;
     int64_t n_win, n_tail, tile_cells;
     int n_head, n_head_kv, head_dim, split, tail_split;
     float scale;
@@ -203,8 +203,11 @@ struct kvattn_tail_ctx {
     cudaEvent_t start;
     cudaEvent_t done;
     cudaEvent_t joined;
+    cudaEvent_t joined2;
+    cudaStream_t copy2;     // private copy stream for odd tiles (the caller's carries even ones)
     cudaStream_t cap_main;  // private streams the pipeline is recorded on
     cudaStream_t cap_fork;
+    cudaStream_t cap_fork2;
     cudaGraphExec_t exec;
     TailGraphKey key;
     int device;
@@ -420,20 +423,21 @@ int kvattn_tail_ctx_create(kvattn_tail_ctx** ctx) {
     kvattn_tail_ctx* c = new (std::nothrow) kvattn_tail_ctx();
     if (c == nullptr) return KVATTN_ERR_INVALID_ARG;
     cudaError_t e = cudaGetDevice(&c->device);
-    cudaEvent_t* evs[7] = {&c->copied[0], &c->copied[1], &c->consumed[0], &c->consumed[1],
-                           &c->start,     &c->done,      &c->joined};
+    cudaEvent_t* evs[8] = {&c->copied[0], &c->copied[1], &c->consumed[0], &c->consumed[1],
+                           &c->start,     &c->done,      &c->joined,      &c->joined2};
     int made = 0;  // events created so far
-    for (; e == cudaSuccess && made < 7; ++made) {
+    for (; e == cudaSuccess && made < 8; ++made) {
         e = cudaEventCreateWithFlags(evs[made], cudaEventDisableTiming);
         if (e != cudaSuccess) break;
     }
-    c->cap_main = c->cap_fork = nullptr;
-    if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&c->cap_main, cudaStreamNonBlocking);
-    if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&c->cap_fork, cudaStreamNonBlocking);
+    cudaStream_t* sts[4] = {&c->copy2, &c->cap_main, &c->cap_fork, &c->cap_fork2};
+    for (cudaStream_t* st : sts) *st = nullptr;
+    for (cudaStream_t* st : sts)
+        if (e == cudaSuccess) e = cudaStreamCreateWithFlags(st, cudaStreamNonBlocking);
     if (e != cudaSuccess) {
         for (int i = 0; i < made; ++i) cudaEventDestroy(*evs[i]);
-        if (c->cap_main) cudaStreamDestroy(c->cap_main);
-        if (c->cap_fork) cudaStreamDestroy(c->cap_fork);
+        for (cudaStream_t* st : sts)
+            if (*st) cudaStreamDestroy(*st);
         delete c;
         return KVATTN_ERR_CUDA;
     }
@@ -446,12 +450,12 @@ int kvattn_tail_ctx_create(kvattn_tail_ctx** ctx) {
 
 int kvattn_tail_ctx_destroy(kvattn_tail_ctx* ctx) {
     if (ctx == nullptr) return KVATTN_ERR_INVALID_ARG;
-    cudaEvent_t evs[7] = {ctx->copied[0], ctx->copied[1], ctx->consumed[0], ctx->consumed[1],
-                          ctx->start,     ctx->done,      ctx->joined};
+    cudaEvent_t evs[8] = {ctx->copied[0], ctx->copied[1], ctx->consumed[0], ctx->consumed[1],
+                          ctx->start,     ctx->done,      ctx->joined,      ctx->joined2};
     int rc = KVATTN_OK;
     if (ctx->exec != nullptr && cudaGraphExecDestroy(ctx->exec) != cudaSuccess) rc = KVATTN_ERR_CUDA;
-    if (cudaStreamDestroy(ctx->cap_main) != cudaSuccess) rc = KVATTN_ERR_CUDA;
-    if (cudaStreamDestroy(ctx->cap_fork) != cudaSuccess) rc = KVATTN_ERR_CUDA;
+    for (cudaStream_t st : {ctx->copy2, ctx->cap_main, ctx->cap_fork, ctx->cap_fork2})
+        if (cudaStreamDestroy(st) != cudaSuccess) rc = KVATTN_ERR_CUDA;
     for (cudaEvent_t ev : evs)
         if (cudaEventDestroy(ev) != cudaSuccess) rc = KVATTN_ERR_CUDA;
     delete ctx;
@@ -508,6 +512,11 @@ bool use_tail_graph() {
     static const bool on = env_int("KVATTN_TAIL_GRAPH", 1) != 0;
     return on;
 }
+
+// Tail tiles move by a copy kernel reading mapped pinned memory (default) or by
+// cudaMemcpyAsync on the copy engine (KVATTN_TAIL_COPY=0, and whenever the host buffers are
+// not mapped into the device's address space).
+bool use_copy_kernel() { return env_int("KVATTN_TAIL_COPY", 1) != 0; }
 
 // Kernel parameters of one window + tail call, fixed before any enqueue or capture.
 struct TailPlan {
@@ -586,7 +595,8 @@ void prepare_window_tail(TailPlan& t, const void* q, const void* k_win, const vo
 
 // Enqueue the window decode, the double-buffered tile pipeline and the final merge.
 int enqueue_window_tail(kvattn_tail_ctx* ctx, const TailPlan& t, const void* k_tail_host, const void* v_tail_host,
-                        int64_t n_tail, int64_t tile_cells, cudaStream_t cs, cudaStream_t xs, int fault) {
+                        const void* k_tail_dev, const void* v_tail_dev, int64_t n_tail, int64_t tile_cells,
+                        cudaStream_t cs, cudaStream_t xs, cudaStream_t xs2, int fault) {
     const TailLayout& L = t.L;
     const int head_dim = t.merge.head_dim;
     const int n_head_kv = t.base.n_head_kv;
@@ -594,27 +604,40 @@ int enqueue_window_tail(kvattn_tail_ctx* ctx, const TailPlan& t, const void* k_t
     // on the compute stream still reads.
     if (cudaEventRecord(ctx->start, cs) != cudaSuccess) return KVATTN_ERR_CUDA;
     if (cudaStreamWaitEvent(xs, ctx->start, 0) != cudaSuccess) return KVATTN_ERR_CUDA;
+    if (cudaStreamWaitEvent(xs2, ctx->start, 0) != cudaSuccess) return KVATTN_ERR_CUDA;
     // window: resident cells, attended while the first tail tiles are in flight
     if (L.n_split_win > 0) {
         if (launch_decode_units(t.window, KVATTN_KV_F16, head_dim, L.n_split_win, cs, t.pdl) != cudaSuccess)
             return KVATTN_ERR_CUDA;
     }
-    // tail: tile i -> staging slot i % 2 on the copy stream, decoded on the compute stream
+    // tail: tile i -> staging slot i % 2, copied on copy stream i % 2 (so one tile's copy
+    // ramps up while the previous one drains), decoded on the compute stream
     SplitDecodeParams slot[2] = {t.slot[0], t.slot[1]};
     for (int64_t i = 0; i < L.n_tiles; ++i) {
         const int sl = (int)(i & 1);
+        cudaStream_t xsi = sl ? xs2 : xs;
         const int64_t c0 = i * tile_cells;
         const int64_t len = (c0 + tile_cells <= n_tail) ? tile_cells : n_tail - c0;
         const size_t bytes = (size_t)len * t.row_bytes;
-        if (i >= 2 && cudaStreamWaitEvent(xs, ctx->consumed[sl], 0) != cudaSuccess) return KVATTN_ERR_CUDA;
+        if (i >= 2 && cudaStreamWaitEvent(xsi, ctx->consumed[sl], 0) != cudaSuccess) return KVATTN_ERR_CUDA;
         if (i == fault) return KVATTN_ERR_CUDA;
-        if (cudaMemcpyAsync(const_cast<void*>(slot[sl].k), static_cast<const char*>(k_tail_host) + (size_t)c0 * t.row_bytes,
-                            bytes, cudaMemcpyHostToDevice, xs) != cudaSuccess)
-            return KVATTN_ERR_CUDA;
-        if (cudaMemcpyAsync(const_cast<void*>(slot[sl].v), static_cast<const char*>(v_tail_host) + (size_t)c0 * t.row_bytes,
-                            bytes, cudaMemcpyHostToDevice, xs) != cudaSuccess)
-            return KVATTN_ERR_CUDA;
-        if (cudaEventRecord(ctx->copied[sl], xs) != cudaSuccess) return KVATTN_ERR_CUDA;
+        if (k_tail_dev != nullptr) {
+            if (launch_tile_copy(static_cast<const char*>(k_tail_dev) + (size_t)c0 * t.row_bytes,
+                                 static_cast<const char*>(v_tail_dev) + (size_t)c0 * t.row_bytes,
+                                 const_cast<void*>(slot[sl].k), const_cast<void*>(slot[sl].v), bytes,
+                                 xsi) != cudaSuccess)
+                return KVATTN_ERR_CUDA;
+        } else {
+            if (cudaMemcpyAsync(const_cast<void*>(slot[sl].k),
+                                static_cast<const char*>(k_tail_host) + (size_t)c0 * t.row_bytes, bytes,
+                                cudaMemcpyHostToDevice, xsi) != cudaSuccess)
+                return KVATTN_ERR_CUDA;
+            if (cudaMemcpyAsync(const_cast<void*>(slot[sl].v),
+                                static_cast<const char*>(v_tail_host) + (size_t)c0 * t.row_bytes, bytes,
+                                cudaMemcpyHostToDevice, xsi) != cudaSuccess)
+                return KVATTN_ERR_CUDA;
+        }
+        if (cudaEventRecord(ctx->copied[sl], xsi) != cudaSuccess) return KVATTN_ERR_CUDA;
         if (cudaStreamWaitEvent(cs, ctx->copied[sl], 0) != cudaSuccess) return KVATTN_ERR_CUDA;
         SplitDecodeParams& tp = slot[sl];
         tp.n_cells = len;
@@ -624,9 +647,11 @@ int enqueue_window_tail(kvattn_tail_ctx* ctx, const TailPlan& t, const void* k_t
             return KVATTN_ERR_CUDA;
         if (cudaEventRecord(ctx->consumed[sl], cs) != cudaSuccess) return KVATTN_ERR_CUDA;
     }
-    // join the copy stream back into the compute stream
+    // join both copy streams back into the compute stream
     if (cudaEventRecord(ctx->joined, xs) != cudaSuccess) return KVATTN_ERR_CUDA;
+    if (cudaEventRecord(ctx->joined2, xs2) != cudaSuccess) return KVATTN_ERR_CUDA;
     if (cudaStreamWaitEvent(cs, ctx->joined, 0) != cudaSuccess) return KVATTN_ERR_CUDA;
+    if (cudaStreamWaitEvent(cs, ctx->joined2, 0) != cudaSuccess) return KVATTN_ERR_CUDA;
     if (launch_merge(t.merge, cs, t.pdl) != cudaSuccess) return KVATTN_ERR_CUDA;
     return KVATTN_OK;
 }
@@ -678,12 +703,28 @@ int kvattn_decode_window_tail(kvattn_tail_ctx* ctx, const void* q, const void* k
     prepare_window_tail(plan, q, k_win, v_win, n_win, n_tail, tile_cells, n_head, n_head_kv, head_dim, split,
                         tail_split, scale, out, lse, ws, L);
     const int fault = fault_tile();
+    // device view of the pinned tail (copy kernel), when the buffers are mapped and aligned
+    const void* k_dev = nullptr;
+    const void* v_dev = nullptr;
+    if (n_tail > 0 && use_copy_kernel() && aligned(k_tail_host, 16) && aligned(v_tail_host, 16) &&
+        ((size_t)tile_cells * plan.row_bytes) % 16 == 0) {
+        void* dk = nullptr;
+        void* dv = nullptr;
+        if (cudaHostGetDevicePointer(&dk, const_cast<void*>(k_tail_host), 0) == cudaSuccess &&
+            cudaHostGetDevicePointer(&dv, const_cast<void*>(v_tail_host), 0) == cudaSuccess) {
+            k_dev = dk;
+            v_dev = dv;
+        } else {
+            cudaGetLastError();  // not mapped: clear the query's error, copy on the copy engine
+        }
+    }
 
     cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
     if (cudaStreamIsCapturing(cs, &cap) != cudaSuccess) return KVATTN_ERR_CUDA;
     const bool use_graph = use_tail_graph() && cap == cudaStreamCaptureStatusNone && fault < 0;
     if (!use_graph) {
-        const int rc = enqueue_window_tail(ctx, plan, k_tail_host, v_tail_host, n_tail, tile_cells, cs, xs, fault);
+        const int rc = enqueue_window_tail(ctx, plan, k_tail_host, v_tail_host, k_dev, v_dev, n_tail, tile_cells, cs,
+                                           xs, ctx->copy2, fault);
         if (rc != KVATTN_OK) return rc;
     } else {
         TailGraphKey key;
@@ -693,6 +734,8 @@ int kvattn_decode_window_tail(kvattn_tail_ctx* ctx, const void* q, const void* k
         key.v_win = v_win;
         key.k_tail = k_tail_host;
         key.v_tail = v_tail_host;
+        key.k_tail_dev = k_dev;
+        key.v_tail_dev = v_dev;
         key.n_win = n_win;
         key.n_tail = n_tail;
         key.tile_cells = tile_cells;
@@ -720,8 +763,8 @@ int kvattn_decode_window_tail(kvattn_tail_ctx* ctx, const void* q, const void* k
             // (recorded on private streams: the caller's may be the legacy default stream)
             if (cudaStreamBeginCapture(ctx->cap_main, cudaStreamCaptureModeThreadLocal) != cudaSuccess)
                 return KVATTN_ERR_CUDA;
-            const int rc = enqueue_window_tail(ctx, plan, k_tail_host, v_tail_host, n_tail, tile_cells, ctx->cap_main,
-                                               ctx->cap_fork, -1);
+            const int rc = enqueue_window_tail(ctx, plan, k_tail_host, v_tail_host, k_dev, v_dev, n_tail, tile_cells,
+                                               ctx->cap_main, ctx->cap_fork, ctx->cap_fork2, -1);
             cudaGraph_t graph = nullptr;
             const cudaError_t ec = cudaStreamEndCapture(ctx->cap_main, &graph);
             if (rc != KVATTN_OK || ec != cudaSuccess || graph == nullptr) {

@@ -100,6 +100,10 @@ struct MergeParams {
 cudaError_t launch_split_decode(const SplitDecodeParams& p, int kv_type, int head_dim,
                                 unsigned grid_ctas, cudaStream_t stream, bool pdl);
 cudaError_t launch_merge(const MergeParams& p, cudaStream_t stream, bool pdl);
+// Copies `bytes` (a multiple of 16) of K and of V from device-visible (e.g. mapped pinned
+// host) memory into device buffers with one kernel launch.
+cudaError_t launch_tile_copy(const void* k_src, const void* v_src, void* k_dst, void* v_dst, size_t bytes,
+                             cudaStream_t stream);
 int split_decode_stage_bytes(int kv_type, int head_dim);
 int split_decode_smem_bytes(int kv_type, int head_dim, int n_stages);
 int split_decode_block_threads(int kv_type, int head_dim);

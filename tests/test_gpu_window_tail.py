@@ -1,6 +1,7 @@
 """Window + pinned-host tail on small cases: ragged last tile, no window, no tail,
 repeated calls reusing the staging slots, host-side fault injection and the bounded
-host wait."""
+host wait.  Tail tiles move by the copy kernel (mapped pinned memory) by default; one
+case forces the copy-engine path."""
 import numpy as np
 import pytest
 
@@ -44,6 +45,20 @@ def test_window_tail_small(kvattn, N, n_win, tile, H, Hk):
     q, k, v = make(rng, N, n_win, H, Hk, 128)
     wt = kvattn.WindowTail()
     out, lse = run(kvattn, wt, q, k, v, n_win, tile)
+    wo, wl = oracle.decode_f16(q, k, v, [N])
+    assert_close(out, lse, wo, wl)
+    wt.close()
+
+
+@pytest.mark.parametrize("copy_kernel", ["0", "1"])
+def test_tile_copy_paths(kvattn, monkeypatch, copy_kernel):
+    """The copy engine (cudaMemcpyAsync per tile) and the copy kernel give the same result."""
+    monkeypatch.setenv("KVATTN_TAIL_COPY", copy_kernel)
+    rng = np.random.default_rng(21)
+    N, n_win, H, Hk = 4500, 300, 32, 8
+    q, k, v = make(rng, N, n_win, H, Hk, 128)
+    wt = kvattn.WindowTail()
+    out, lse = run(kvattn, wt, q, k, v, n_win, 512)
     wo, wl = oracle.decode_f16(q, k, v, [N])
     assert_close(out, lse, wo, wl)
     wt.close()
