@@ -107,9 +107,29 @@ int kvattn_build_descriptors(const int32_t* cell_plan, int64_t plan_stride,
                              const int32_t* seq_lens, int n_seq, int64_t max_len, int split,
                              int64_t n_cells, int32_t* desc, void* stream);
 
-/* Bytes of workspace kvattn_decode needs (partials, descriptors, status word). */
+/* Bytes of workspace kvattn_decode needs (partials, descriptors, status word).  split 0:
+ * enough for whichever split kvattn_decode selects (it sizes for split 64).  Returns 0 on
+ * invalid arguments. */
 size_t kvattn_decode_workspace_bytes(int n_seq, int n_head, int head_dim, int64_t max_len,
                                      int split);
+
+/*
+ * kvattn_select_split_for -- host, pure.  The split kvattn_decode uses when it is given
+ * split 0 ("split-size auto-selector", [KVN] item 6 and its split-64 / split-128 geometry,
+ * re-measured for GB300): the smallest power of two >= 64 such that the work units
+ * n_seq x ceil(max_len / split) x n_head_kv fit in resident_ctas (one wave of the decode
+ * kernel's CTAs); a split that reaches max_len (one split per sequence) or 2^30 ends the
+ * search.  Returns the split, or INVALID_ARG (n_seq < 0, max_len < 0, n_head_kv < 1,
+ * resident_ctas < 1).
+ */
+int kvattn_select_split_for(int n_seq, int64_t max_len, int n_head_kv, int64_t resident_ctas);
+
+/*
+ * kvattn_select_split -- host.  kvattn_select_split_for with the resident CTA count of the
+ * decode kernel for (kv_type, head_dim) on the current device (queries the device; no
+ * work is enqueued).  Errors: INVALID_ARG, UNSUPPORTED (head_dim not 128 or 256).
+ */
+int kvattn_select_split(int kv_type, int n_seq, int64_t max_len, int n_head_kv, int head_dim);
 
 /*
  * kvattn_decode -- device.  Split-KV decode attention ([RKV] sections 1 and 3; [KVN]
@@ -131,7 +151,8 @@ size_t kvattn_decode_workspace_bytes(int n_seq, int n_head, int head_dim, int64_
  *           plan) or plan_stride (plan).
  *  max_len  host bound on the lengths; sizes the grid and the workspace.
  *  n_head, n_head_kv  n_head % n_head_kv == 0 and n_head / n_head_kv <= 8.
- *  head_dim 128 or 256.   split  cells per partial, a positive multiple of 32.
+ *  head_dim 128 or 256.   split  cells per partial, a positive multiple of 32, or 0 to
+ *           use kvattn_select_split (kvattn_decode and kvattn_decode_noalloc only).
  *  scale    softmax scale applied to q . k in fp32 (1/sqrt(head_dim) is usual).
  *  out, lse device float outputs.   ws/ws_bytes  device workspace of at least
  *           kvattn_decode_workspace_bytes(...) bytes, 256-byte aligned, zeroed once

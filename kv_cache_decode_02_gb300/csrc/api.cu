@@ -81,6 +81,19 @@ int pick_stages(int kv_type, int head_dim, int64_t n_units) {
     return 2;
 }
 
+// Split selection ("split-size auto-selector" re-measured on GB300): the smallest power of
+// two >= 64 whose work units (sequences x splits x KV heads) fit in one wave of resident
+// CTAs.  On the Qwen3-8B-shaped decode (32/8 heads, head_dim 128) that choice was the
+// fastest of splits 64-4096 at 1 and 4 sequences of 1K-256K cells (e.g. 16K cells: split
+// 256, 14.9 us against 18.7 us at 128; 64K cells: split 1024, 44.5 us against 48.4 us at 256).
+constexpr int64_t kMinAutoSplit = 64;
+constexpr int64_t kMaxAutoSplit = int64_t(1) << 30;
+
+int64_t auto_split_slots(int kv_type, int head_dim) {
+    const int st = kv_type == KVATTN_KV_F16 ? 3 : 2;  // the one-wave f16 ring; Q8_0 geometry is fixed
+    return (int64_t)std::max(occupancy(kv_type, head_dim, st), 1) * sm_count();
+}
+
 // Launches the persistent split-decode kernel over n_seq x unit_splits x n_head_kv work
 // units: one CTA per unit, at most as many CTAs as fit on the device at once.
 cudaError_t launch_decode_units(SplitDecodeParams p, int kv_type, int head_dim, int64_t unit_splits,
@@ -253,9 +266,26 @@ int kvattn_build_descriptors(const int32_t* cell_plan, int64_t plan_stride, cons
 
 size_t kvattn_decode_workspace_bytes(int n_seq, int n_head, int head_dim, int64_t max_len,
                                      int split) {
-    if (n_seq < 0 || n_head < 1 || head_dim < 1 || max_len < 0 || split < 1) return 0;
+    if (n_seq < 0 || n_head < 1 || head_dim < 1 || max_len < 0 || split < 0) return 0;
+    if (split == 0) split = kMinAutoSplit;  // covers whichever split the call selects
     const int64_t n_split = (max_len + split - 1) / split;
     return decode_ws_layout(n_seq, n_head, head_dim, n_split).total;
+}
+
+int kvattn_select_split_for(int n_seq, int64_t max_len, int n_head_kv, int64_t resident_ctas) {
+    if (n_seq < 0 || max_len < 0 || n_head_kv < 1 || resident_ctas < 1) return KVATTN_ERR_INVALID_ARG;
+    int64_t split = kMinAutoSplit;
+    for (;;) {
+        const int64_t units = (int64_t)n_seq * ((max_len + split - 1) / split) * n_head_kv;
+        if (units <= resident_ctas || split >= max_len || split >= kMaxAutoSplit) return (int)split;
+        split *= 2;
+    }
+}
+
+int kvattn_select_split(int kv_type, int n_seq, int64_t max_len, int n_head_kv, int head_dim) {
+    if (kv_type != KVATTN_KV_F16 && kv_type != KVATTN_KV_Q8_0) return KVATTN_ERR_INVALID_ARG;
+    if (head_dim != 128 && head_dim != 256) return KVATTN_ERR_UNSUPPORTED;
+    return kvattn_select_split_for(n_seq, max_len, n_head_kv, auto_split_slots(kv_type, head_dim));
 }
 
 }  // extern "C"
@@ -270,6 +300,13 @@ int decode_impl(const void* q, const void* k_cache, const void* v_cache, const v
                 int n_head_kv, int head_dim, int split, float scale, float* out, float* lse,
                 float* part_o_user, float* part_lse_user, void* ws, size_t ws_bytes, void* stream) {
     const bool merge = part_o_user == nullptr;
+    if (split == 0 && merge) {  // kvattn_decode picks the split (partials need it fixed)
+        if (kv_type != KVATTN_KV_F16 && kv_type != KVATTN_KV_Q8_0) return KVATTN_ERR_INVALID_ARG;
+        if (head_dim != 128 && head_dim != 256) return KVATTN_ERR_UNSUPPORTED;
+        if (n_head_kv < 1 || n_seq < 0 || max_len < 0) return KVATTN_ERR_INVALID_ARG;
+        split = kvattn_select_split(kv_type, n_seq, max_len, n_head_kv, head_dim);
+        if (split < 0) return split;
+    }
     const DecodeShape shape{n_seq, n_head, n_head_kv, head_dim, split, max_len};
     int st = check_shape(shape);
     if (st != KVATTN_OK) return st;

@@ -49,7 +49,11 @@ extern "C" int kvattn_decode_noalloc(const void* q, const void* k_cache, const v
                                      const int32_t* seq_lens, int n_seq, int64_t max_len, int n_head,
                                      int n_head_kv, int head_dim, int split, float scale, float* out,
                                      float* lse, void* stream) {
-    // Refuse, before touching the device, any call whose scratch would not fit.
+    if (split == 0) {  // the split kvattn_decode would select (a host-side query)
+        split = kvattn_select_split(kv_type, n_seq, max_len, n_head_kv, head_dim);
+        if (split < 0) return split;
+    }
+    // Refuse, before any work reaches the device, a call whose scratch would not fit.
     const size_t need = kvattn_decode_workspace_bytes(n_seq, n_head, head_dim, max_len, split);
     if (need == 0) return KVATTN_ERR_INVALID_ARG;
     if (need > (size_t)KVATTN_NOALLOC_SCRATCH_BYTES) return KVATTN_ERR_WORKSPACE;

@@ -42,6 +42,7 @@ EXPORTED = (
     "kvattn_tail_ctx_destroy", "kvattn_window_tail_workspace_bytes", "kvattn_decode_window_tail",
     "kvattn_tail_wait", "kvattn_workspace_status", "kvattn_decode_noalloc",
     "kvattn_window_tail_direct_workspace_bytes", "kvattn_decode_window_tail_direct",
+    "kvattn_select_split_for", "kvattn_select_split",
 )
 
 _P = ctypes.c_void_p
@@ -60,6 +61,10 @@ lib.kvattn_build_descriptors.argtypes = [_P, _I64, _P, _I, _I64, _I, _I64, _P, _
 lib.kvattn_build_descriptors.restype = _I
 lib.kvattn_decode_workspace_bytes.argtypes = [_I, _I, _I, _I64, _I]
 lib.kvattn_decode_workspace_bytes.restype = _SZ
+lib.kvattn_select_split_for.argtypes = [_I, _I64, _I, _I64]
+lib.kvattn_select_split_for.restype = _I
+lib.kvattn_select_split.argtypes = [_I, _I, _I64, _I, _I]
+lib.kvattn_select_split.restype = _I
 lib.kvattn_decode.argtypes = [_P, _P, _P, _P, _P, _I, _I64, _P, _I64, _P, _I, _I64, _I, _I, _I, _I,
                               _F, _P, _P, _P, _SZ, _P]
 lib.kvattn_decode.restype = _I
@@ -148,6 +153,20 @@ def kvattn_build_descriptors(cell_plan, plan_stride, seq_lens, n_seq, max_len, s
 
 def kvattn_decode_workspace_bytes(n_seq, n_head, head_dim, max_len, split) -> int:
     return lib.kvattn_decode_workspace_bytes(n_seq, n_head, head_dim, max_len, split)
+
+
+def kvattn_select_split_for(n_seq, max_len, n_head_kv, resident_ctas) -> int:
+    rc = lib.kvattn_select_split_for(n_seq, max_len, n_head_kv, resident_ctas)
+    if rc < 0:
+        raise KvattnError(rc, "kvattn_select_split_for")
+    return rc
+
+
+def kvattn_select_split(kv_type, n_seq, max_len, n_head_kv, head_dim) -> int:
+    rc = lib.kvattn_select_split(kv_type, n_seq, max_len, n_head_kv, head_dim)
+    if rc < 0:
+        raise KvattnError(rc, "kvattn_select_split")
+    return rc
 
 
 def kvattn_decode(q, k_cache, v_cache, k_scales, v_scales, kv_type, n_cells, cell_plan, plan_stride,

@@ -59,7 +59,7 @@ def call_decode(kvattn, a):
     (dict(head_dim=96), -2),
     (dict(split=48), -2),                  # not a multiple of the 32-cell tile
     (dict(n_seq=70000), -2),               # more sequences than a grid dimension holds
-    (dict(split=0), -1),
+    (dict(split=-32), -1),                 # (split 0 selects the split: needs a device)
     (dict(q=None), -1),
     (dict(out=None), -1),
     (dict(ws=None), -1),
@@ -101,7 +101,7 @@ def test_decode_workspace_query(kvattn):
     # status word, descriptors, LSE partials and O partials of 64 splits x 32 heads
     assert n >= 64 * 32 * 128 * 4 + 64 * 32 * 4
     assert n % 256 == 0
-    assert kvattn.kvattn_decode_workspace_bytes(1, 32, 128, 16384, 0) == 0
+    assert kvattn.kvattn_decode_workspace_bytes(1, 32, 128, 16384, -32) == 0
     assert call_decode(kvattn, decode_args(max_len=16384, n_cells=16384, ws_bytes=n - 1)) == -3
 
 
