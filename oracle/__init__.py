@@ -143,6 +143,29 @@ def decode_f64(q, k, v, seq_lens, plan=None, scale=None, n_threads=None):
     return out, lse
 
 
+def decode_multi(decode_one, q, seq_lens, *cache, plan=None, scale=None, n_threads=None):
+    """Multi-query decode: n_q new tokens per sequence, each attending causally.
+
+    ``q`` is [S][n_q][H][D].  ``seq_lens[s]`` counts the sequence's cells including the n_q
+    new tokens' own (already appended) cells, so token t sits at logical position
+    L - n_q + t and attends to positions 0 .. L - n_q + t: exactly single-query decode of
+    the first L - n_q + 1 + t positions (fewer than one: no cell, O = 0, LSE = -inf).
+    ``decode_one`` is decode_f16 or decode_q8_0 and ``cache`` its cache arguments.
+    Returns (out [S][n_q][H][D], lse [S][n_q][H])."""
+    q = np.asarray(q)
+    S, n_q, H, D = q.shape
+    lens = np.asarray(seq_lens, dtype=np.int64).reshape(S)
+    out = np.zeros((S, n_q, H, D), dtype=np.float64)
+    lse = np.zeros((S, n_q, H), dtype=np.float64)
+    for t in range(n_q):
+        lens_t = np.maximum(lens - n_q + 1 + t, 0)
+        o, l = decode_one(np.ascontiguousarray(q[:, t]), *cache, lens_t.tolist(), plan=plan, scale=scale,
+                          n_threads=n_threads)
+        out[:, t] = o
+        lse[:, t] = l
+    return out, lse
+
+
 def merge(parts, lses):
     """LSE-weighted merge.  parts [P][R][D], lses [P][R] -> (out [R][D], lse [R])."""
     parts = np.ascontiguousarray(parts, dtype=np.float64)

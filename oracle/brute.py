@@ -49,3 +49,43 @@ def decode(q, k, v, seq_lens, plan=None, scale=None, n_head_kv=None):
         outs.append(o_s)
         lses.append(l_s)
     return outs, lses
+
+
+def decode_multi(q, k, v, seq_lens, plan=None, scale=None, n_head_kv=None):
+    """Causal multi-query decode, written out directly.  q: [S][n_q][H][D]; k, v as in
+    decode().  Query token t of sequence s sits at logical position p = L - n_q + t and
+    sees the entries at positions 0..p (inside the length, not -1)."""
+    S, n_q, H, D = len(q), len(q[0]), len(q[0][0]), len(q[0][0][0])
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    Hk = n_head_kv if n_head_kv is not None else (len(k[0][0]) if plan is None else len(k[0]))
+    G = H // Hk
+    outs, lses = [], []
+    for s in range(S):
+        L = seq_lens[s]
+        o_s, l_s = [], []
+        for t in range(n_q):
+            p = L - n_q + t
+            o_t, l_t = [], []
+            for h in range(H):
+                g = h // G
+                keys, vals = [], []
+                for i in range(L):
+                    if i > p:
+                        continue
+                    if plan is None:
+                        kc, vc = k[s][i][g], v[s][i][g]
+                    else:
+                        if plan[s][i] == -1:
+                            continue
+                        kc, vc = k[plan[s][i]][g], v[plan[s][i]][g]
+                    keys.append([float(x) for x in kc])
+                    vals.append([float(x) for x in vc])
+                o, l = attend([float(x) for x in q[s][t][h]], keys, vals, scale)
+                o_t.append(o)
+                l_t.append(l)
+            o_s.append(o_t)
+            l_s.append(l_t)
+        outs.append(o_s)
+        lses.append(l_s)
+    return outs, lses

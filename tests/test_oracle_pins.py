@@ -280,3 +280,65 @@ def test_rejects_plan_entries_outside_the_cache():
         oracle.decode_f16(q, k, k, [2], plan=np.array([[3, -5]], np.int32))
     with pytest.raises(ValueError):
         oracle.decode_f16(q, k, k, [2], plan=np.array([[3, 10]], np.int32))
+
+
+# ------------------------- multi-query decode (causal, n_q tokens) -------------------------
+
+def _mq_case(rng, S, n_q, N, H, Hk, D):
+    q = rng.standard_normal((S, n_q, H, D)).astype(np.float16)
+    k = rng.standard_normal((S, N, Hk, D)).astype(np.float16)
+    v = rng.standard_normal((S, N, Hk, D)).astype(np.float16)
+    return q, k, v
+
+
+def test_multi_query_matches_brute_force_contiguous():
+    from oracle import brute
+    rng = np.random.default_rng(71)
+    q, k, v = _mq_case(rng, 2, 3, 6, 4, 2, 8)
+    lens = [6, 2]                       # sequence 1: token 0 sees nothing
+    wo, wl = oracle.decode_multi(oracle.decode_f16, q, lens, k, v)
+    bo, bl = brute.decode_multi(q.tolist(), k.tolist(), v.tolist(), lens, n_head_kv=2)
+    assert np.allclose(wo, np.array(bo), atol=1e-12, rtol=0)
+    assert np.array_equal(np.isneginf(wl), np.isneginf(np.array(bl)))
+    fin = np.isfinite(wl)
+    assert np.allclose(wl[fin], np.array(bl)[fin], atol=1e-12, rtol=0)
+    assert np.all(np.isneginf(wl[1, 0])) and np.all(wo[1, 0] == 0)
+
+
+def test_multi_query_matches_brute_force_plan_with_holes():
+    from oracle import brute
+    rng = np.random.default_rng(72)
+    Hk, D, H, n_q = 2, 8, 4, 2
+    n_phys = 20
+    k = rng.standard_normal((n_phys, Hk, D)).astype(np.float16)
+    v = rng.standard_normal((n_phys, Hk, D)).astype(np.float16)
+    q = rng.standard_normal((2, n_q, H, D)).astype(np.float16)
+    plan = np.array([[3, -1, 7, 8, 11, -1, 2], [5, 6, -1, 0, -1, -1, -1]], np.int32)
+    lens = [7, 5]                       # sequence 0's last token at a -1 entry
+    wo, wl = oracle.decode_multi(oracle.decode_f16, q, lens, k, v, plan=plan)
+    bo, bl = brute.decode_multi(q.tolist(), k.tolist(), v.tolist(), lens, plan=plan.tolist(), n_head_kv=2)
+    assert np.allclose(wo, np.array(bo), atol=1e-12, rtol=0)
+    assert np.allclose(wl, np.array(bl), atol=1e-12, rtol=0)
+
+
+def test_multi_query_reductions():
+    rng = np.random.default_rng(73)
+    q, k, v = _mq_case(rng, 3, 4, 50, 8, 2, 16)
+    lens = [50, 3, 0]
+    wo, wl = oracle.decode_multi(oracle.decode_f16, q, lens, k, v)
+    # the last token sees the whole sequence: single-query decode of the full length
+    so, sl = oracle.decode_f16(q[:, -1], k, v, lens)
+    assert np.array_equal(wo[:, -1], so) and np.array_equal(wl[:, -1], sl)
+    # one token is single-query decode
+    o1, l1 = oracle.decode_multi(oracle.decode_f16, q[:, :1], lens, k, v)
+    so1, sl1 = oracle.decode_f16(q[:, 0], k, v, lens)
+    assert np.array_equal(o1[:, 0], so1) and np.array_equal(l1[:, 0], sl1)
+    # a sequence shorter than n_q: tokens 0 (and only 0) of [3] see nothing; [0] none do
+    assert np.all(np.isneginf(wl[1, 0])) and np.all(np.isfinite(wl[1, 1:]))
+    assert np.all(np.isneginf(wl[2])) and np.all(wo[2] == 0)
+    # V constant over the cells of each (sequence, KV head): every token gets that row
+    vc = np.repeat(v[:, :1], v.shape[1], axis=1)
+    co, _ = oracle.decode_multi(oracle.decode_f16, q, [50, 50, 50], k, vc)
+    for s_ in range(3):
+        for h in range(8):
+            assert np.allclose(co[s_, :, h], vc[s_, 0, h // 4].astype(np.float64)[None], atol=1e-12, rtol=0)
