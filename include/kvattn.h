@@ -185,6 +185,31 @@ int kvattn_decode_partials(const void* q, const void* k_cache, const void* v_cac
                            int n_head_kv, int head_dim, int split, float scale, float* part_o,
                            float* part_lse, void* ws, size_t ws_bytes, void* stream);
 
+/* Bytes of workspace kvattn_decode_multi needs (split 0: as kvattn_decode_workspace_bytes). */
+size_t kvattn_decode_multi_workspace_bytes(int n_seq, int n_q, int n_head, int head_dim, int64_t max_len,
+                                           int split);
+
+/*
+ * kvattn_decode_multi -- device.  Causal multi-query decode ("small multi-query decode,
+ * n_q <= 8/16 with a mask", the speculative-verify case of [RKV] section 3 and [KVN] item
+ * 2): n_q new query tokens per sequence, whose own K/V cells are already in the cache.
+ * seq_lens[s] = L counts them, token t sits at logical position L - n_q + t and attends to
+ * the logical positions 0 .. L - n_q + t (plan entries or cells, -1 holes masked); a token
+ * whose window is empty gets O = 0, LSE = -inf.  The G x n_q query rows of each KV head
+ * share every K/V byte read (one 16-row MMA tile).
+ *  q        device half [n_seq][n_q][n_head][head_dim].
+ *  out, lse device float [n_seq][n_q][n_head][head_dim], [n_seq][n_q][n_head].
+ *  Other arguments: as kvattn_decode (f16 KV only; no scales).
+ *  Limits: kv_type f16, head_dim 128, (n_head / n_head_kv) * n_q <= 16 (UNSUPPORTED
+ *  otherwise); n_q >= 1.  ws: kvattn_decode_multi_workspace_bytes(...) bytes.
+ * Errors: as kvattn_decode.
+ */
+int kvattn_decode_multi(const void* q, const void* k_cache, const void* v_cache, int kv_type,
+                        int64_t n_cells, const int32_t* cell_plan, int64_t plan_stride,
+                        const int32_t* seq_lens, int n_seq, int64_t max_len, int n_q, int n_head,
+                        int n_head_kv, int head_dim, int split, float scale, float* out, float* lse,
+                        void* ws, size_t ws_bytes, void* stream);
+
 /*
  * kvattn_merge -- device.  LSE-weighted merge of partial attention results ([KVN]
  * item 9; [RKV] section 3):  M = max_p LSE_p, w_p = exp(LSE_p - M),

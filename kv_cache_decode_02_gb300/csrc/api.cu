@@ -43,22 +43,23 @@ int sm_count() {
     return count[dev % kMaxDevices];
 }
 
-// Resident CTAs per SM of the split-decode kernel for (kv_type, head_dim, n_stages).
-int occupancy(int kv_type, int head_dim, int n_stages) {
+// Resident CTAs per SM of the split-decode kernel for (kv_type, head_dim, n_stages,
+// multi-query kernel).
+int occupancy(int kv_type, int head_dim, int n_stages, bool mq = false) {
     static std::mutex mu;
-    static int cache[kMaxDevices][2][2][16];
-    static bool have[kMaxDevices][2][2][16];
+    static int cache[kMaxDevices][2][2][2][16];
+    static bool have[kMaxDevices][2][2][2][16];
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return 1;
-    const int d = dev % kMaxDevices, t = kv_type ? 1 : 0, h = head_dim == 256 ? 1 : 0;
+    const int d = dev % kMaxDevices, t = kv_type ? 1 : 0, h = head_dim == 256 ? 1 : 0, m = mq ? 1 : 0;
     std::lock_guard<std::mutex> lock(mu);
-    if (!have[d][t][h][n_stages]) {
+    if (!have[d][t][h][m][n_stages]) {
         int blocks = 0;
-        if (split_decode_occupancy(kv_type, head_dim, n_stages, &blocks) != cudaSuccess) blocks = 0;
-        cache[d][t][h][n_stages] = blocks;
-        have[d][t][h][n_stages] = true;
+        if (split_decode_occupancy(kv_type, head_dim, n_stages, mq, &blocks) != cudaSuccess) blocks = 0;
+        cache[d][t][h][m][n_stages] = blocks;
+        have[d][t][h][m][n_stages] = true;
     }
-    return cache[d][t][h][n_stages];
+    return cache[d][t][h][m][n_stages];
 }
 
 // Pipeline depth per CTA ("launch bounds and occupancy-aware selection", KVARN item 6).
@@ -66,17 +67,17 @@ int occupancy(int kv_type, int head_dim, int n_stages) {
 // (up to the number of work units), then the deepest ring (at most 4 stages) that keeps that
 // many resident.  Deeper rings measured slower on GB300 for the multi-wave Q8_0 and plan
 // workloads (111 vs 91 us at 8 vs 4 stages for Q8_0 over 131072 cells).
-int pick_stages(int kv_type, int head_dim, int64_t n_units) {
+int pick_stages(int kv_type, int head_dim, int64_t n_units, bool mq = false) {
     const int forced = env_int("KVATTN_STAGES", 0);
     const int max_st = split_decode_max_stages();
     const int limit = split_decode_max_smem();
-    if (forced >= 2 && forced <= max_st && split_decode_smem_bytes(kv_type, head_dim, forced) <= limit)
+    if (forced >= 2 && forced <= max_st && split_decode_smem_bytes(kv_type, head_dim, forced, mq) <= limit)
         return forced;
     const int64_t n_sm = sm_count();
-    const int64_t want = std::min(n_units, (int64_t)occupancy(kv_type, head_dim, 2) * n_sm);
+    const int64_t want = std::min(n_units, (int64_t)occupancy(kv_type, head_dim, 2, mq) * n_sm);
     for (int st = 4; st >= 3; --st) {
-        if (split_decode_smem_bytes(kv_type, head_dim, st) > limit) continue;
-        if ((int64_t)occupancy(kv_type, head_dim, st) * n_sm >= want) return st;
+        if (split_decode_smem_bytes(kv_type, head_dim, st, mq) > limit) continue;
+        if ((int64_t)occupancy(kv_type, head_dim, st, mq) * n_sm >= want) return st;
     }
     return 2;
 }
@@ -101,7 +102,8 @@ cudaError_t launch_decode_units(SplitDecodeParams p, int kv_type, int head_dim, 
     p.unit_splits = unit_splits;
     const int64_t n_units = (int64_t)p.n_seq * unit_splits * p.n_head_kv;
     if (n_units > (int64_t)INT32_MAX) return cudaErrorInvalidValue;  // units are numbered in 32 bits
-    const int64_t resident = (int64_t)std::max(occupancy(kv_type, head_dim, p.n_stages), 1) * sm_count();
+    const int64_t resident =
+        (int64_t)std::max(occupancy(kv_type, head_dim, p.n_stages, p.mq != 0), 1) * sm_count();
     const int64_t grid = std::min(n_units, resident);
     if (grid < 1) return cudaSuccess;
     return launch_split_decode(p, kv_type, head_dim, (unsigned)grid, stream, pdl);
@@ -264,6 +266,14 @@ int kvattn_build_descriptors(const int32_t* cell_plan, int64_t plan_stride, cons
                                           static_cast<cudaStream_t>(stream)));
 }
 
+size_t kvattn_decode_multi_workspace_bytes(int n_seq, int n_q, int n_head, int head_dim, int64_t max_len,
+                                           int split) {
+    if (n_q < 1 || split < 0 || n_head < 1) return 0;
+    const int64_t rows = (int64_t)n_q * n_head;
+    if (rows > INT32_MAX) return 0;
+    return kvattn_decode_workspace_bytes(n_seq, (int)rows, head_dim, max_len, split);
+}
+
 size_t kvattn_decode_workspace_bytes(int n_seq, int n_head, int head_dim, int64_t max_len,
                                      int split) {
     if (n_seq < 0 || n_head < 1 || head_dim < 1 || max_len < 0 || split < 0) return 0;
@@ -298,7 +308,11 @@ int decode_impl(const void* q, const void* k_cache, const void* v_cache, const v
                 const void* v_scales, int kv_type, int64_t n_cells, const int32_t* cell_plan,
                 int64_t plan_stride, const int32_t* seq_lens, int n_seq, int64_t max_len, int n_head,
                 int n_head_kv, int head_dim, int split, float scale, float* out, float* lse,
-                float* part_o_user, float* part_lse_user, void* ws, size_t ws_bytes, void* stream) {
+                float* part_o_user, float* part_lse_user, void* ws, size_t ws_bytes, void* stream,
+                int n_q = 0) {
+    // n_q = 0: single-query decode; n_q >= 1: the causal multi-query kernel (f16, head_dim 128)
+    const bool multi = n_q > 0;
+    if (!multi) n_q = 1;
     const bool merge = part_o_user == nullptr;
     if (split == 0 && merge) {  // kvattn_decode picks the split (partials need it fixed)
         if (kv_type != KVATTN_KV_F16 && kv_type != KVATTN_KV_Q8_0) return KVATTN_ERR_INVALID_ARG;
@@ -310,6 +324,8 @@ int decode_impl(const void* q, const void* k_cache, const void* v_cache, const v
     const DecodeShape shape{n_seq, n_head, n_head_kv, head_dim, split, max_len};
     int st = check_shape(shape);
     if (st != KVATTN_OK) return st;
+    if (multi && (kv_type != KVATTN_KV_F16 || head_dim != 128 || (n_head / n_head_kv) * n_q > 16))
+        return KVATTN_ERR_UNSUPPORTED;
     if (q == nullptr || k_cache == nullptr || v_cache == nullptr || seq_lens == nullptr || ws == nullptr)
         return KVATTN_ERR_INVALID_ARG;
     if (merge && (out == nullptr || lse == nullptr)) return KVATTN_ERR_INVALID_ARG;
@@ -331,7 +347,7 @@ int decode_impl(const void* q, const void* k_cache, const void* v_cache, const v
         if (!aligned(k_scales, sa) || !aligned(v_scales, sa)) return KVATTN_ERR_INVALID_ARG;
     }
     const int64_t n_split = (max_len + split - 1) / split;
-    const DecodeWsLayout lay = decode_ws_layout(n_seq, n_head, head_dim, n_split);
+    const DecodeWsLayout lay = decode_ws_layout(n_seq, n_q * n_head, head_dim, n_split);
     if (ws_bytes < lay.total) return KVATTN_ERR_WORKSPACE;
     if (n_seq == 0) return KVATTN_OK;
 
@@ -374,7 +390,9 @@ int decode_impl(const void* q, const void* k_cache, const void* v_cache, const v
         p.n_head_kv = n_head_kv;
         p.group = n_head / n_head_kv;
         p.split = split;
-        p.n_stages = pick_stages(kv_type, head_dim, n_split * n_head_kv * n_seq);
+        p.n_q = n_q;
+        p.mq = multi ? 1 : 0;
+        p.n_stages = pick_stages(kv_type, head_dim, n_split * n_head_kv * n_seq, multi);
         p.scale_log2 = (float)((double)scale * 1.4426950408889634074);
         apply_debug_hooks(p);
         set_kv_maps(p, kv_type, cell_plan != nullptr ? n_cells : n_cells * (int64_t)n_seq, n_head_kv, head_dim);
@@ -392,7 +410,7 @@ int decode_impl(const void* q, const void* k_cache, const void* v_cache, const v
     m.max_len = max_len;
     m.len_cap = cell_plan != nullptr ? plan_stride : n_cells;
     m.n_seq = n_seq;
-    m.n_rows = n_head;
+    m.n_rows = n_q * n_head;  // rows (token t, head h) = t * n_head + h
     m.head_dim = head_dim;
     m.split = split;
     m.all_written = 1;
@@ -424,6 +442,16 @@ int kvattn_decode_partials(const void* q, const void* k_cache, const void* v_cac
     return decode_impl(q, k_cache, v_cache, k_scales, v_scales, kv_type, n_cells, cell_plan,
                        plan_stride, seq_lens, n_seq, max_len, n_head, n_head_kv, head_dim, split,
                        scale, nullptr, nullptr, part_o, part_lse, ws, ws_bytes, stream);
+}
+
+int kvattn_decode_multi(const void* q, const void* k_cache, const void* v_cache, int kv_type, int64_t n_cells,
+                        const int32_t* cell_plan, int64_t plan_stride, const int32_t* seq_lens, int n_seq,
+                        int64_t max_len, int n_q, int n_head, int n_head_kv, int head_dim, int split, float scale,
+                        float* out, float* lse, void* ws, size_t ws_bytes, void* stream) {
+    if (n_q < 1) return KVATTN_ERR_INVALID_ARG;
+    return decode_impl(q, k_cache, v_cache, nullptr, nullptr, kv_type, n_cells, cell_plan, plan_stride, seq_lens,
+                       n_seq, max_len, n_head, n_head_kv, head_dim, split, scale, out, lse, nullptr, nullptr, ws,
+                       ws_bytes, stream, n_q);
 }
 
 int kvattn_merge(const float* partials, const float* lses, int n_parts, int n_rows, int head_dim,

@@ -62,6 +62,8 @@ struct Geom {
     static constexpr int kArrivals = KVT == KVATTN_KV_Q8_0 ? 64 : 32;  // + cp.async arrivals
     // end-of-unit exchange area: warp 1's O fragments ([D/16][32 lanes] float4), max, sum
     static constexpr int kXchgBytes = ((D / 16) * 32 * 16 + 64 + 1023) / 1024 * 1024;
+    // multi-query: two O tiles per lane, max and sum of 16 rows
+    static constexpr int kXchgBytesMQ = (2 * (D / 16) * 32 * 16 + 128 + 1023) / 1024 * 1024;
 };
 
 // Byte address of (row r, byte b) of a K or V section in either layout.
@@ -249,15 +251,12 @@ __device__ __forceinline__ void consume_tile(uint32_t kb, uint32_t vb, const uns
 
     // ---- O^T += V^T P^T ----
     if (KVT == KVATTN_KV_F16) {
+        // l sums the fp32 probabilities (the LSE stays exact to fp32 even over a handful of
+        // cells); the MMA weights are their f16 roundings
         uint32_t pb[2];
-        float psum = 0.f;
 #pragma unroll
-        for (int j = 0; j < 2; ++j) {
-            pb[j] = pack_half2(pf[j][0], pf[j][1]);
-            const float2 r = __half22float2(*reinterpret_cast<const __half2*>(&pb[j]));
-            psum += r.x + r.y;
-        }
-        l_run += psum;
+        for (int j = 0; j < 2; ++j) pb[j] = pack_half2(pf[j][0], pf[j][1]);
+        l_run += (pf[0][0] + pf[0][1]) + (pf[1][0] + pf[1][1]);
 #pragma unroll
         for (int mt = 0; mt < D / 16; ++mt) {
             uint32_t a0, a1, a2, a3;
@@ -330,15 +329,11 @@ __device__ __forceinline__ void consume_tile_staged(uint32_t kb, uint32_t vb, ui
         rescale_o<D>(oacc, alpha, tq);
         l_run *= alpha;
     }
+    // l sums the fp32 probabilities; the MMA weights are their f16 roundings
     uint32_t pb[2];
-    float psum = 0.f;
 #pragma unroll
-    for (int j = 0; j < 2; ++j) {
-        pb[j] = pack_half2(pf[j][0], pf[j][1]);
-        const float2 r = __half22float2(*reinterpret_cast<const __half2*>(&pb[j]));
-        psum += r.x + r.y;
-    }
-    l_run += psum;
+    for (int j = 0; j < 2; ++j) pb[j] = pack_half2(pf[j][0], pf[j][1]);
+    l_run += (pf[0][0] + pf[0][1]) + (pf[1][0] + pf[1][1]);
 #pragma unroll
     for (int mt = 0; mt < 8; ++mt) mma_16816(oacc[mt], vf[mt][0], vf[mt][1], vf[mt][2], vf[mt][3], pb[0], pb[1]);
 }
@@ -371,6 +366,7 @@ __device__ __forceinline__ void load_q_frags(const SplitDecodeParams& p, int s, 
 struct Unit {
     int s, g;
     int64_t split_idx;
+    int64_t len;      // the sequence's clamped length
     int64_t i0, i1;   // plan entries / cells [i0, i1) of the split
     int n_tiles;      // 0: nothing to read
     bool write_empty; // an empty unit still reports (0, -inf)
@@ -393,6 +389,7 @@ __device__ __forceinline__ Unit unit_at(const SplitDecodeParams& p, int64_t u) {
     L = L < p.max_len ? L : p.max_len;
     L = L < cap ? L : cap;
     x.i0 = x.split_idx * p.split;
+    x.len = L;
     x.i1 = (x.i0 + p.split < L) ? x.i0 + p.split : L;
     const bool empty = x.i0 >= x.i1 || desc_valid == 0;
     x.n_tiles = empty ? 0 : (int)((x.i1 - x.i0 + kTileCells - 1) / kTileCells);
@@ -402,6 +399,300 @@ __device__ __forceinline__ Unit unit_at(const SplitDecodeParams& p, int64_t u) {
     return x;
 }
 
+// ---------------------------------------------------------------------------------------
+// Causal multi-query decode (f16, head_dim 128).  The G x n_q query rows of a KV head
+// (row r = token r / G, query head g*G + r % G) fill the whole M of the q.K^T MMA -- a
+// lane holds rows gq and gq + 8 -- and two N = 8 tiles of the P V MMA.  Each row keeps its
+// own running max and sum; row r sees the cells at logical positions below
+// L - n_q + 1 + r / G (its token's own position and everything before it).
+// ---------------------------------------------------------------------------------------
+__device__ __forceinline__ void load_q_frags_mq(const SplitDecodeParams& p, int s, int g, int gq, int tq,
+                                                uint32_t (&qa)[8][4]) {
+    constexpr int D = 128;
+    const int rows = p.group * p.n_q;
+#pragma unroll
+    for (int half = 0; half < 2; ++half) {
+        const int r = gq + 8 * half;
+        const bool ok = r < rows;
+        const int t = ok ? r / p.group : 0;
+        const int h = g * p.group + (ok ? r % p.group : 0);
+        const uint32_t* qrow =
+            reinterpret_cast<const uint32_t*>(p.q + (((int64_t)s * p.n_q + t) * p.n_head + h) * D);
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+            const int d0 = 16 * kk + 2 * tq;
+            qa[kk][2 * half] = ok ? __ldg(qrow + d0 / 2) : 0u;
+            qa[kk][2 * half + 1] = ok ? __ldg(qrow + (d0 + 8) / 2) : 0u;
+        }
+    }
+}
+
+// One warp's 16 cells of a tile for the 16 query rows.  lim[hh]: cells c < lim[hh] of the
+// warp's 16 are inside the causal window of the lane's row gq + 8 hh.
+template <bool SWZ>
+__device__ __forceinline__ void mq_tile(uint32_t kb, uint32_t vb, uint32_t mask, int warp, int lane,
+                                        const int (&lim)[2], const uint32_t (&qa)[8][4], float (&oacc)[2][8][4],
+                                        float (&m_run)[2], float (&l_run)[2], float scale_log2) {
+    constexpr int D = 128;
+    using G = Geom<KVATTN_KV_F16, D>;
+    const int tq = lane & 3;
+    const int r0 = warp * kWarpCells;
+    float sacc[2][4];
+#pragma unroll
+    for (int j = 0; j < 2; ++j) sacc[j][0] = sacc[j][1] = sacc[j][2] = sacc[j][3] = 0.f;
+#pragma unroll
+    for (int kk = 0; kk < D / 16; kk += 2) {
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+            uint32_t b0, b1, b2, b3;
+            ldsm_x4(sec_addr<SWZ, G::kPadRow>(kb, r0 + 8 * j + (lane & 7), (kk * 16 + 8 * (lane >> 3)) * 2), b0,
+                    b1, b2, b3);
+            mma_16816(sacc[j], qa[kk][0], qa[kk][2], qa[kk][1], qa[kk][3], b0, b1);
+            mma_16816(sacc[j], qa[kk + 1][0], qa[kk + 1][2], qa[kk + 1][1], qa[kk + 1][3], b2, b3);
+        }
+    }
+    // online softmax, one (max, sum) per row: hh = 0 -> row gq, hh = 1 -> row gq + 8
+    float x[2][2][2];
+    float tmax[2] = {-INFINITY, -INFINITY};
+#pragma unroll
+    for (int hh = 0; hh < 2; ++hh)
+#pragma unroll
+        for (int j = 0; j < 2; ++j)
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                const int c = 8 * j + 2 * tq + e;
+                const bool ok = ((mask >> c) & 1u) && c < lim[hh];
+                x[hh][j][e] = ok ? sacc[j][2 * hh + e] * scale_log2 : -INFINITY;
+                tmax[hh] = fmaxf(tmax[hh], x[hh][j][e]);
+            }
+#pragma unroll
+    for (int hh = 0; hh < 2; ++hh) {
+        tmax[hh] = fmaxf(tmax[hh], __shfl_xor_sync(0xffffffffu, tmax[hh], 1));
+        tmax[hh] = fmaxf(tmax[hh], __shfl_xor_sync(0xffffffffu, tmax[hh], 2));
+    }
+    const bool grow = __any_sync(0xffffffffu, tmax[0] > m_run[0] + kRescaleSlack || tmax[1] > m_run[1] + kRescaleSlack);
+    if (grow) {
+        float alpha[2];
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+            const float m_new = fmaxf(m_run[hh], tmax[hh]);
+            alpha[hh] = fast_exp2(m_run[hh] - ((m_new == -INFINITY) ? 0.f : m_new));
+            m_run[hh] = m_new;
+            l_run[hh] *= alpha[hh];
+        }
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt) {
+            const float a0 = __shfl_sync(0xffffffffu, alpha[nt], 8 * tq);
+            const float a1 = __shfl_sync(0xffffffffu, alpha[nt], 8 * tq + 4);
+#pragma unroll
+            for (int mt = 0; mt < D / 16; ++mt) {
+                oacc[nt][mt][0] *= a0;
+                oacc[nt][mt][1] *= a1;
+                oacc[nt][mt][2] *= a0;
+                oacc[nt][mt][3] *= a1;
+            }
+        }
+    }
+    uint32_t pb[2][2];
+#pragma unroll
+    for (int hh = 0; hh < 2; ++hh) {
+        const float m_use = (m_run[hh] == -INFINITY) ? 0.f : m_run[hh];
+        float psum = 0.f;  // over the fp32 probabilities (the MMA weights are their f16 roundings)
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+            const float p0 = fast_exp2(x[hh][j][0] - m_use), p1 = fast_exp2(x[hh][j][1] - m_use);
+            pb[hh][j] = pack_half2(p0, p1);
+            psum += p0 + p1;
+        }
+        l_run[hh] += psum;
+    }
+#pragma unroll
+    for (int mt = 0; mt < D / 16; ++mt) {
+        uint32_t a0, a1, a2, a3;
+        ldsm_x4_trans(sec_addr<SWZ, G::kPadRow>(vb, r0 + (lane & 7) + 8 * (lane >> 4), (16 * mt + 8 * ((lane >> 3) & 1)) * 2),
+                      a0, a1, a2, a3);
+        mma_16816(oacc[0][mt], a0, a1, a2, a3, pb[0][0], pb[0][1]);
+        mma_16816(oacc[1][mt], a0, a1, a2, a3, pb[1][0], pb[1][1]);
+    }
+}
+
+// The consumer warps of the multi-query kernel: the same ring and unit walk as the
+// single-query consumers, then the doubled end-of-unit exchange and the partial write
+// (partial row of (token t, head h) = t * n_head + h).
+__device__ __forceinline__ void mq_consumers(const SplitDecodeParams& p, uint64_t* full_bar, uint64_t* empty_bar,
+                                             const uint32_t* tile_mask, const uint32_t* tile_swz,
+                                             volatile int* abort_flag, uint64_t* xchg_bar, unsigned char* xchg,
+                                             unsigned char* stages, int n_stages, int64_t n_units, int warp,
+                                             int lane) {
+    constexpr int D = 128;
+    using G = Geom<KVATTN_KV_F16, D>;
+    const int gq = lane >> 2;
+    const int tq = lane & 3;
+    const int H = p.n_head, GQ = p.group, NQ = p.n_q;
+    const int rows = GQ * NQ;
+    const int64_t HR = (int64_t)NQ * H;  // partial rows per (sequence, split)
+    float4* xo = reinterpret_cast<float4*>(xchg);      // [2][D/16][32 lanes]
+    float* xm = reinterpret_cast<float*>(xo + 2 * (D / 16) * 32);  // [16] max
+    float* xl = xm + 16;                                            // [16] sum
+    constexpr float kLn2 = 0.69314718055994530942f;
+    uint32_t qa[8][4];
+    int64_t qa_unit = -1;
+    uint32_t T = 0, X = 0;
+    bool stop = false;
+    for (int64_t u = blockIdx.x; u < n_units && !stop; u += gridDim.x) {
+        const Unit x = unit_at(p, u);
+        const int64_t part = (int64_t)x.s * p.part_stride + p.part_base + x.split_idx;
+        if (x.n_tiles == 0) {
+            if (warp == 0 && x.write_empty) {
+                for (int idx = lane; idx < rows * D; idx += 32) {
+                    const int r = idx / D;
+                    const int d = idx - r * D;
+                    const int64_t row = (int64_t)(r / GQ) * H + x.g * GQ + r % GQ;
+                    p.part_o[(part * HR + row) * D + d] = 0.f;
+                    if (d == 0) p.part_lse[part * HR + row] = -INFINITY;
+                }
+            }
+            continue;
+        }
+        if (qa_unit != u) load_q_frags_mq(p, x.s, x.g, gq, tq, qa);
+        float oacc[2][8][4];
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+            for (int i = 0; i < 8; ++i) oacc[nt][i][0] = oacc[nt][i][1] = oacc[nt][i][2] = oacc[nt][i][3] = 0.f;
+        float m_run[2] = {-INFINITY, -INFINITY}, l_run[2] = {0.f, 0.f};
+        // causal limit (logical position, exclusive) of the lane's rows gq and gq + 8
+        const int64_t lim_row[2] = {x.len - NQ + 1 + gq / GQ, x.len - NQ + 1 + (gq + 8) / GQ};
+        for (int t = 0; t < x.n_tiles; ++t, ++T) {
+            const int st = (int)(T % (uint32_t)n_stages);
+            const uint32_t use = T / (uint32_t)n_stages;
+            const bool ok = mbar_wait_bounded(smem_addr(&full_bar[st]), use & 1u, abort_flag, p.wait_limit_ns);
+            if (!__all_sync(0xffffffffu, ok)) {
+                stop = true;
+                break;
+            }
+            const uint32_t mask = (tile_mask[st] >> (warp * kWarpCells)) & 0xffffu;
+            const bool swz = tile_swz[st] != 0u;
+            unsigned char* stage = stages + st * G::kBytes;
+            if (mask != 0u) {
+                const int64_t p0 = x.i0 + (int64_t)t * kTileCells + warp * kWarpCells;
+                int lim[2];
+#pragma unroll
+                for (int hh = 0; hh < 2; ++hh) {
+                    const int64_t rel = lim_row[hh] - p0;
+                    lim[hh] = rel < 0 ? 0 : (rel > kWarpCells ? kWarpCells : (int)rel);
+                }
+                if (swz) {
+                    const uint32_t kb = smem_addr(stage);
+                    if (mask != 0xffffu) {
+                        const int r = warp * kWarpCells + (lane & 15);
+                        if (lane < 16 && !((mask >> lane) & 1u)) {
+#pragma unroll
+                            for (int pl = 0; pl < G::kPlanes; ++pl) {
+                                uint4* z = reinterpret_cast<uint4*>(stage + G::kSwzSection + pl * kPlaneBytes + r * 128);
+#pragma unroll
+                                for (int k = 0; k < 8; ++k) z[k] = make_uint4(0, 0, 0, 0);
+                            }
+                            fence_proxy_async();
+                        }
+                        __syncwarp();
+                    }
+                    mq_tile<true>(kb, kb + G::kSwzSection, mask, warp, lane, lim, qa, oacc, m_run, l_run, p.scale_log2);
+                } else {
+                    const uint32_t kb = smem_addr(stage);
+                    mq_tile<false>(kb, kb + G::kPadSection, mask, warp, lane, lim, qa, oacc, m_run, l_run,
+                                   p.scale_log2);
+                }
+            }
+            __syncwarp();
+            mbar_arrive(smem_addr(&empty_bar[st]));
+        }
+        if (stop) break;
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+            l_run[hh] += __shfl_xor_sync(0xffffffffu, l_run[hh], 1);
+            l_run[hh] += __shfl_xor_sync(0xffffffffu, l_run[hh], 2);
+        }
+        const int64_t un = u + gridDim.x;
+        if (un < n_units) {
+            const Unit y = unit_at(p, un);
+            if (y.n_tiles > 0) {
+                load_q_frags_mq(p, y.s, y.g, gq, tq, qa);
+                qa_unit = un;
+            }
+        }
+        if (warp == 1) {
+            if (X > 0) {
+                const bool ok = mbar_wait_bounded(smem_addr(&xchg_bar[1]), (X - 1) & 1u, abort_flag, p.wait_limit_ns);
+                if (!__all_sync(0xffffffffu, ok)) break;
+            }
+            if (tq == 0) {
+                xm[gq] = m_run[0];
+                xm[8 + gq] = m_run[1];
+                xl[gq] = l_run[0];
+                xl[8 + gq] = l_run[1];
+            }
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                for (int mt = 0; mt < 8; ++mt)
+                    xo[(nt * 8 + mt) * 32 + lane] =
+                        make_float4(oacc[nt][mt][0], oacc[nt][mt][1], oacc[nt][mt][2], oacc[nt][mt][3]);
+            __syncwarp();
+            mbar_arrive(smem_addr(&xchg_bar[0]));
+        } else {
+            const bool ok = mbar_wait_bounded(smem_addr(&xchg_bar[0]), X & 1u, abort_flag, p.wait_limit_ns);
+            if (!__all_sync(0xffffffffu, ok)) break;
+            float f0[2][2], f1[2][2], inv[2][2], lse[2][2];
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    const int r = 8 * nt + 2 * tq + e;
+                    const float m0 = __shfl_sync(0xffffffffu, m_run[nt], 8 * tq + 4 * e);
+                    const float l0 = __shfl_sync(0xffffffffu, l_run[nt], 8 * tq + 4 * e);
+                    const float m1 = xm[r], l1 = xl[r];
+                    const float M = fmaxf(m0, m1);
+                    f0[nt][e] = (m0 == -INFINITY) ? 0.f : fast_exp2(m0 - M);
+                    f1[nt][e] = (m1 == -INFINITY) ? 0.f : fast_exp2(m1 - M);
+                    const float den = l0 * f0[nt][e] + l1 * f1[nt][e];
+                    const bool have = M != -INFINITY && den > 0.f;
+                    inv[nt][e] = have ? 1.f / den : 0.f;
+                    lse[nt][e] = have ? (M + fast_log2(den)) * kLn2 : -INFINITY;
+                }
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                for (int mt = 0; mt < 8; ++mt) {
+                    const float4 o1 = xo[(nt * 8 + mt) * 32 + lane];
+                    oacc[nt][mt][0] = (oacc[nt][mt][0] * f0[nt][0] + o1.x * f1[nt][0]) * inv[nt][0];
+                    oacc[nt][mt][1] = (oacc[nt][mt][1] * f0[nt][1] + o1.y * f1[nt][1]) * inv[nt][1];
+                    oacc[nt][mt][2] = (oacc[nt][mt][2] * f0[nt][0] + o1.z * f1[nt][0]) * inv[nt][0];
+                    oacc[nt][mt][3] = (oacc[nt][mt][3] * f0[nt][1] + o1.w * f1[nt][1]) * inv[nt][1];
+                }
+            __syncwarp();
+            mbar_arrive(smem_addr(&xchg_bar[1]));
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    const int r = 8 * nt + 2 * tq + e;
+                    if (r < rows) {
+                        const int64_t row = (int64_t)(r / GQ) * H + x.g * GQ + r % GQ;
+                        float* orow = p.part_o + (part * HR + row) * D;
+#pragma unroll
+                        for (int mt = 0; mt < 8; ++mt) {
+                            orow[16 * mt + gq] = oacc[nt][mt][e];
+                            orow[16 * mt + 8 + gq] = oacc[nt][mt][2 + e];
+                        }
+                        if (gq == 0) p.part_lse[part * HR + row] = lse[nt][e];
+                    }
+                }
+        }
+        ++X;
+    }
+}
+
 // Persistent split-decode kernel (f16 KV; Q8_0 runs in q8_self_body below).  Each CTA walks
 // the units blockIdx.x, blockIdx.x + grid,
 // ...; warp 2 streams the 32-cell tiles of those units through a ring of shared-memory
@@ -409,9 +700,10 @@ __device__ __forceinline__ Unit unit_at(const SplitDecodeParams& p, int64_t u) {
 // At the end of a unit warp 1 hands its running max, sum and unnormalised O to warp 0
 // through an exchange area guarded by two mbarriers, and warp 0 writes the unit's partial
 // (normalised O and LSE), so no CTA-wide barrier stalls the ring between units.
-template <int KVT, int D>
+template <int KVT, int D, bool MQ = false>
 __device__ __forceinline__ void split_decode_body(const SplitDecodeParams& p) {
     static_assert(KVT == KVATTN_KV_F16, "Q8_0 runs in q8_self_body");
+    static_assert(!MQ || D == 128, "multi-query decode: head_dim 128");
     using G = Geom<KVT, D>;
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     // 1024-byte alignment of the stage ring (the 128-B swizzle repeats every 8 rows)
@@ -425,7 +717,7 @@ __device__ __forceinline__ void split_decode_body(const SplitDecodeParams& p) {
     float4* xo = reinterpret_cast<float4*>(smem + kHeaderBytes);  // [D/16][32 lanes] of warp 1's O
     float* xm = reinterpret_cast<float*>(xo + (D / 16) * 32);      // [8] warp 1's running max
     float* xl = xm + 8;                                             // [8] warp 1's running sum
-    unsigned char* stages = smem + kHeaderBytes + G::kXchgBytes;
+    unsigned char* stages = smem + kHeaderBytes + (MQ ? G::kXchgBytesMQ : G::kXchgBytes);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -620,6 +912,10 @@ __device__ __forceinline__ void split_decode_body(const SplitDecodeParams& p) {
         if (__any_sync(0xffffffffu, bad) && lane == 0) atomicOr(p.status, KVATTN_DEVICE_BAD_PLAN_ENTRY);
     } else {
         // ------------------------------- consumers -------------------------------
+        if constexpr (MQ) {
+            mq_consumers(p, full_bar, empty_bar, tile_mask, tile_swz, abort_flag, xchg_bar,
+                         reinterpret_cast<unsigned char*>(xo), stages, n_stages, n_units, warp, lane);
+        } else {
         uint32_t qa[D / 16][2];
         int64_t qa_unit = -1;  // unit whose query fragments qa holds
         uint32_t T = 0;        // tiles consumed (ring position)
@@ -781,6 +1077,7 @@ __device__ __forceinline__ void split_decode_body(const SplitDecodeParams& p) {
             }
             ++X;
         }
+        }  // single-query consumers
     }
 
     // Every wait above is bounded, so all warps get here; a timed-out wait left abort set.
@@ -1330,6 +1627,9 @@ __global__ void __launch_bounds__(kThreads, KVATTN_F16_D256_MIN_CTAS)
     split_decode_f16_d256(const __grid_constant__ SplitDecodeParams p) {
     split_decode_body<KVATTN_KV_F16, 256>(p);
 }
+__global__ void __launch_bounds__(kThreads) split_decode_mq_f16_d128(const __grid_constant__ SplitDecodeParams p) {
+    split_decode_body<KVATTN_KV_F16, 128, true>(p);
+}
 __global__ void __launch_bounds__(kQ8W128 * 32, kQ8B128)
     split_decode_q8_d128(const __grid_constant__ SplitDecodeParams p) {
     q8_self_body<128, kQ8W128, kQ8S128>(p);
@@ -1339,7 +1639,8 @@ __global__ void __launch_bounds__(kQ8W256 * 32, kQ8B256)
     q8_self_body<256, kQ8W256, kQ8S256>(p);
 }
 
-const void* kernel_for(int kv_type, int head_dim) {
+const void* kernel_for(int kv_type, int head_dim, bool mq = false) {
+    if (mq) return reinterpret_cast<const void*>(split_decode_mq_f16_d128);
     if (kv_type == KVATTN_KV_F16)
         return head_dim == 128 ? reinterpret_cast<const void*>(split_decode_f16_d128)
                                : reinterpret_cast<const void*>(split_decode_f16_d256);
@@ -1363,10 +1664,12 @@ int split_decode_stage_bytes(int kv_type, int head_dim) {
 // Dynamic shared memory of one CTA: header, slack for aligning the ring to 1024 bytes,
 // the end-of-unit exchange area and the stage ring.
 // Q8_0 kernels have a fixed geometry (n_stages is ignored for them).
-int split_decode_smem_bytes(int kv_type, int head_dim, int n_stages) {
+int split_decode_smem_bytes(int kv_type, int head_dim, int n_stages, bool mq) {
     if (kv_type == KVATTN_KV_Q8_0)
         return head_dim == 128 ? q8_self_smem<128, kQ8W128, kQ8S128>() : q8_self_smem<256, kQ8W256, kQ8S256>();
-    const int xchg = head_dim == 128 ? Geom<0, 128>::kXchgBytes : Geom<0, 256>::kXchgBytes;
+    const int xchg = mq                ? Geom<0, 128>::kXchgBytesMQ
+                     : head_dim == 128 ? Geom<0, 128>::kXchgBytes
+                                       : Geom<0, 256>::kXchgBytes;
     return kHeaderBytes + 1024 + xchg + n_stages * split_decode_stage_bytes(kv_type, head_dim);
 }
 
@@ -1380,29 +1683,30 @@ int split_decode_box_cells(int kv_type) { return kv_type == KVATTN_KV_Q8_0 ? kCh
 int split_decode_max_stages() { return kMaxStages; }
 int split_decode_threads() { return kThreads; }
 
-cudaError_t split_decode_occupancy(int kv_type, int head_dim, int n_stages, int* blocks) {
-    const void* fn = kernel_for(kv_type, head_dim);
+cudaError_t split_decode_occupancy(int kv_type, int head_dim, int n_stages, bool mq, int* blocks) {
+    const void* fn = kernel_for(kv_type, head_dim, mq);
     cudaError_t err = set_smem_attr(fn);
     if (err != cudaSuccess) return err;
     return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks, fn, split_decode_block_threads(kv_type, head_dim),
-                                                         split_decode_smem_bytes(kv_type, head_dim, n_stages));
+                                                         split_decode_smem_bytes(kv_type, head_dim, n_stages, mq));
 }
 
 cudaError_t launch_split_decode(const SplitDecodeParams& p, int kv_type, int head_dim, unsigned grid_ctas,
                                 cudaStream_t stream, bool pdl) {
-    const void* fn = kernel_for(kv_type, head_dim);
-    static std::once_flag once[64][4];
-    static cudaError_t attr_err[64][4];
+    const bool mq = p.mq != 0;
+    const void* fn = kernel_for(kv_type, head_dim, mq);
+    static std::once_flag once[64][5];
+    static cudaError_t attr_err[64][5];
     int dev = 0;
     cudaError_t err = cudaGetDevice(&dev);
     if (err != cudaSuccess) return err;
-    const int which = (kv_type ? 2 : 0) + (head_dim == 256 ? 1 : 0);
+    const int which = mq ? 4 : (kv_type ? 2 : 0) + (head_dim == 256 ? 1 : 0);
     std::call_once(once[dev & 63][which], [&] { attr_err[dev & 63][which] = set_smem_attr(fn); });
     if (attr_err[dev & 63][which] != cudaSuccess) return attr_err[dev & 63][which];
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid_ctas, 1, 1);
     cfg.blockDim = dim3((unsigned)split_decode_block_threads(kv_type, head_dim), 1, 1);
-    cfg.dynamicSmemBytes = split_decode_smem_bytes(kv_type, head_dim, p.n_stages);
+    cfg.dynamicSmemBytes = split_decode_smem_bytes(kv_type, head_dim, p.n_stages, mq);
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;

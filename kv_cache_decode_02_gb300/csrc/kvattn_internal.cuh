@@ -67,6 +67,8 @@ struct SplitDecodeParams {
     uint64_t wait_limit_ns;   // bound on every pipeline wait
     uint32_t stall_tx;        // test hook: extra bytes expected on the first tile (never arrive)
     int n_seq, n_head, n_head_kv, group, split;
+    int n_q;                  // query tokens per sequence (multi-query decode; 1 otherwise)
+    int mq;                   // 1: the multi-query kernel (rows = group x n_q <= 16)
     int n_stages;
     int use_tma;              // tiles that are one physical run load through tmap_k/tmap_v
     int write_beyond;         // splits past a sequence's length still write (0, -inf)
@@ -105,13 +107,13 @@ cudaError_t launch_merge(const MergeParams& p, cudaStream_t stream, bool pdl);
 cudaError_t launch_tile_copy(const void* k_src, const void* v_src, void* k_dst, void* v_dst, size_t bytes,
                              cudaStream_t stream);
 int split_decode_stage_bytes(int kv_type, int head_dim);
-int split_decode_smem_bytes(int kv_type, int head_dim, int n_stages);
+int split_decode_smem_bytes(int kv_type, int head_dim, int n_stages, bool mq = false);
 int split_decode_block_threads(int kv_type, int head_dim);
 int split_decode_box_cells(int kv_type);
 int split_decode_max_stages();
 int split_decode_max_smem();
 int split_decode_threads();
-cudaError_t split_decode_occupancy(int kv_type, int head_dim, int n_stages, int* blocks);
+cudaError_t split_decode_occupancy(int kv_type, int head_dim, int n_stages, bool mq, int* blocks);
 cudaError_t launch_descriptors(const int32_t* plan, int64_t plan_stride, const int32_t* seq_lens,
                                int n_seq, int64_t max_len, int split, int64_t n_cells,
                                int64_t n_split, int4* desc, uint32_t* status,

@@ -42,7 +42,8 @@ EXPORTED = (
     "kvattn_tail_ctx_destroy", "kvattn_window_tail_workspace_bytes", "kvattn_decode_window_tail",
     "kvattn_tail_wait", "kvattn_workspace_status", "kvattn_decode_noalloc",
     "kvattn_window_tail_direct_workspace_bytes", "kvattn_decode_window_tail_direct",
-    "kvattn_select_split_for", "kvattn_select_split",
+    "kvattn_select_split_for", "kvattn_select_split", "kvattn_decode_multi_workspace_bytes",
+    "kvattn_decode_multi",
 )
 
 _P = ctypes.c_void_p
@@ -61,6 +62,11 @@ lib.kvattn_build_descriptors.argtypes = [_P, _I64, _P, _I, _I64, _I, _I64, _P, _
 lib.kvattn_build_descriptors.restype = _I
 lib.kvattn_decode_workspace_bytes.argtypes = [_I, _I, _I, _I64, _I]
 lib.kvattn_decode_workspace_bytes.restype = _SZ
+lib.kvattn_decode_multi_workspace_bytes.argtypes = [_I, _I, _I, _I, _I64, _I]
+lib.kvattn_decode_multi_workspace_bytes.restype = _SZ
+lib.kvattn_decode_multi.argtypes = [_P, _P, _P, _I, _I64, _P, _I64, _P, _I, _I64, _I, _I, _I, _I, _I, _F, _P, _P,
+                                    _P, _SZ, _P]
+lib.kvattn_decode_multi.restype = _I
 lib.kvattn_select_split_for.argtypes = [_I, _I64, _I, _I64]
 lib.kvattn_select_split_for.restype = _I
 lib.kvattn_select_split.argtypes = [_I, _I, _I64, _I, _I]
@@ -153,6 +159,18 @@ def kvattn_build_descriptors(cell_plan, plan_stride, seq_lens, n_seq, max_len, s
 
 def kvattn_decode_workspace_bytes(n_seq, n_head, head_dim, max_len, split) -> int:
     return lib.kvattn_decode_workspace_bytes(n_seq, n_head, head_dim, max_len, split)
+
+
+def kvattn_decode_multi_workspace_bytes(n_seq, n_q, n_head, head_dim, max_len, split) -> int:
+    return lib.kvattn_decode_multi_workspace_bytes(n_seq, n_q, n_head, head_dim, max_len, split)
+
+
+def kvattn_decode_multi(q, k_cache, v_cache, kv_type, n_cells, cell_plan, plan_stride, seq_lens, n_seq, max_len,
+                        n_q, n_head, n_head_kv, head_dim, split, scale, out, lse, ws, ws_bytes, stream=None):
+    rc = lib.kvattn_decode_multi(_ptr(q), _ptr(k_cache), _ptr(v_cache), kv_type, n_cells, _ptr(cell_plan),
+                                 plan_stride, _ptr(seq_lens), n_seq, max_len, n_q, n_head, n_head_kv, head_dim,
+                                 split, scale, _ptr(out), _ptr(lse), _ptr(ws), ws_bytes, _stream(stream))
+    _check(rc, "kvattn_decode_multi")
 
 
 def kvattn_select_split_for(n_seq, max_len, n_head_kv, resident_ctas) -> int:
@@ -320,6 +338,31 @@ def decode(q, k_cache, v_cache, seq_lens, *, split, max_len=None, cell_plan=None
         ws = decode_workspace(S, H, D, max_len, split, device=q.device)
     kvattn_decode(q, k_cache, v_cache, k_scales, v_scales, kv_type, n_cells, cell_plan, plan_stride,
                   seq_lens, S, max_len, H, Hk, D, split, scale, out, lse, ws, ws.numel(), stream)
+    return out, lse
+
+
+def decode_multi(q, k_cache, v_cache, seq_lens, *, split, max_len=None, cell_plan=None, scale=None, n_cells=None,
+                 out=None, lse=None, ws=None, stream=None):
+    """q: half [S][n_q][H][D] (cuda), f16 K/V as the C ABI describes.  Returns (out, lse)."""
+    import torch
+    S, n_q, H, D = q.shape
+    Hk = k_cache.shape[-2]
+    if n_cells is None:
+        n_cells = k_cache.shape[1] if (k_cache.dim() == 4) else k_cache.shape[0]
+    plan_stride = cell_plan.shape[-1] if cell_plan is not None else 0
+    if max_len is None:
+        max_len = plan_stride if cell_plan is not None else n_cells
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    if out is None:
+        out = torch.empty((S, n_q, H, D), dtype=torch.float32, device=q.device)
+    if lse is None:
+        lse = torch.empty((S, n_q, H), dtype=torch.float32, device=q.device)
+    if ws is None:
+        nbytes = kvattn_decode_multi_workspace_bytes(S, n_q, H, D, max_len, split)
+        ws = torch.zeros(max(nbytes, 256), dtype=torch.uint8, device=q.device)
+    kvattn_decode_multi(q, k_cache, v_cache, KVATTN_KV_F16, n_cells, cell_plan, plan_stride, seq_lens, S, max_len,
+                        n_q, H, Hk, D, split, scale, out, lse, ws, ws.numel(), stream)
     return out, lse
 
 

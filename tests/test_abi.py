@@ -163,3 +163,22 @@ def test_window_tail_direct_validation(kvattn):
     assert f(*bad) == -3
     bad = list(base); bad[4] = A + 4100           # tail not 16-byte aligned
     assert f(*bad) == -1
+
+
+def test_multi_query_limits(kvattn):
+    """Checked on the host before any device work."""
+    def call(**over):
+        a = dict(q=A, k=B, v=C, kv_type=0, n_cells=1024, plan=None, plan_stride=0, seq_lens=A + 4096, n_seq=1,
+                 max_len=1024, n_q=4, n_head=32, n_head_kv=8, head_dim=128, split=256, scale=0.0884, out=A + 8192,
+                 lse=A + 16384, ws=A + 65536, ws_bytes=1 << 30, stream=None)
+        a.update(over)
+        return kvattn.lib.kvattn_decode_multi(*a.values())
+    assert call(n_q=5) == kvattn.KVATTN_ERR_UNSUPPORTED            # 4 x 5 = 20 rows > 16
+    assert call(head_dim=256) == kvattn.KVATTN_ERR_UNSUPPORTED
+    assert call(kv_type=1) == kvattn.KVATTN_ERR_UNSUPPORTED
+    assert call(n_q=0) == kvattn.KVATTN_ERR_INVALID_ARG
+    assert call(q=None) == kvattn.KVATTN_ERR_INVALID_ARG
+    assert call(ws_bytes=1000) == kvattn.KVATTN_ERR_WORKSPACE
+    one = kvattn.kvattn_decode_workspace_bytes(2, 4 * 32, 128, 4096, 128)
+    assert kvattn.kvattn_decode_multi_workspace_bytes(2, 4, 32, 128, 4096, 128) == one
+    assert kvattn.kvattn_decode_multi_workspace_bytes(2, 0, 32, 128, 4096, 128) == 0

@@ -1,0 +1,108 @@
+"""GPU parity of causal multi-query decode (kvattn_decode_multi) against the fp64 oracle:
+n_q new tokens per sequence, token t seeing logical positions 0 .. L - n_q + t, the
+G x n_q query rows of a KV head in one 16-row MMA tile."""
+import numpy as np
+import pytest
+
+import oracle
+from oracle import plan_oracle as po
+from tests.gpu_util import TOL_LSE, TOL_O, dev
+
+pytestmark = pytest.mark.gpu
+
+
+def rand_f16(rng, shape):
+    return rng.standard_normal(shape, dtype=np.float32).astype(np.float16)
+
+
+def check(out, lse, wo, wl):
+    o, l = out.cpu().numpy(), lse.cpu().numpy()
+    assert o.shape == wo.shape and l.shape == wl.shape
+    assert np.array_equal(np.isneginf(l), np.isneginf(wl))
+    fin = np.isfinite(wl)
+    assert np.max(np.abs(l[fin] - wl[fin]), initial=0.0) <= TOL_LSE
+    assert np.max(np.abs(o - wo)) <= TOL_O
+    assert np.all(o[~fin] == 0)
+
+
+@pytest.mark.parametrize("n_q,G,Hk,lens,split", [
+    (1, 4, 2, [1000, 37], 128),
+    (2, 4, 2, [1000, 1], 128),          # sequence 1 shorter than n_q: token 0 sees nothing
+    (4, 4, 2, [777, 4, 3], 64),         # 16 rows per KV head
+    (8, 2, 4, [513, 300], 256),
+    (16, 1, 4, [100, 16], 32),          # MHA, 16 tokens
+    (3, 5, 2, [2049, 0], 512),          # 15 rows, an empty sequence
+])
+def test_multi_query_contiguous(kvattn, n_q, G, Hk, lens, split):
+    import torch
+    rng = np.random.default_rng(n_q * 100 + G)
+    S, D = len(lens), 128
+    N = max(max(lens), 1)
+    H = G * Hk
+    q = rand_f16(rng, (S, n_q, H, D))
+    k = rand_f16(rng, (S, N, Hk, D))
+    v = rand_f16(rng, (S, N, Hk, D))
+    out, lse = kvattn.decode_multi(dev(q), dev(k), dev(v), dev(np.array(lens, np.int32)), split=split,
+                                   n_cells=N, max_len=N)
+    torch.cuda.synchronize()
+    wo, wl = oracle.decode_multi(oracle.decode_f16, q, lens, k, v)
+    check(out, lse, wo, wl)
+
+
+def test_multi_query_plan_with_holes(kvattn):
+    import torch
+    rng = np.random.default_rng(9)
+    Hk, G, n_q, D = 4, 4, 4, 128
+    H = Hk * G
+    pool = 30
+    n_cells = pool * 128
+    k = rand_f16(rng, (n_cells, Hk, D))
+    v = rand_f16(rng, (n_cells, Hk, D))
+    perm = rng.permutation(pool)
+    encoded, selected = [], []
+    for recs in (perm[:4], perm[4:5], perm[5:12]):
+        cells = (recs[:, None] * 128 + np.arange(128)[None]).reshape(-1)
+        sel = cells[rng.random(cells.size) >= 0.2]
+        encoded.append(sel.astype(np.int64)[rng.permutation(sel.size)])
+        selected.append(sel)
+    unused = np.setdiff1d(np.arange(n_cells), np.concatenate(selected))
+    k[unused] = np.nan
+    v[unused] = np.nan
+    plan, lens = kvattn.build_cell_plan(encoded, n_cells)
+    q = rand_f16(rng, (3, n_q, H, D))
+    out, lse = kvattn.decode_multi(dev(q), dev(k), dev(v), dev(lens), split=128, cell_plan=dev(plan),
+                                   n_cells=n_cells)
+    torch.cuda.synchronize()
+    wo, wl = oracle.decode_multi(oracle.decode_f16, q, lens.tolist(), k, v, plan=plan)
+    check(out, lse, wo, wl)
+
+
+def test_one_token_equals_single_query_decode(kvattn):
+    import torch
+    rng = np.random.default_rng(10)
+    S, N, H, Hk, D = 2, 3000, 32, 8, 128
+    q = rand_f16(rng, (S, 1, H, D))
+    k = rand_f16(rng, (S, N, Hk, D))
+    v = rand_f16(rng, (S, N, Hk, D))
+    lens = dev(np.array([3000, 1234], np.int32))
+    mo, ml = kvattn.decode_multi(dev(q), dev(k), dev(v), lens, split=256, n_cells=N, max_len=N)
+    so, sl = kvattn.decode(dev(q[:, 0]), dev(k), dev(v), lens, split=256, n_cells=N, max_len=N)
+    torch.cuda.synchronize()
+    assert np.max(np.abs(mo.cpu().numpy()[:, 0] - so.cpu().numpy())) <= 1e-5
+    assert np.max(np.abs(ml.cpu().numpy()[:, 0] - sl.cpu().numpy())) <= 1e-5
+
+
+def test_speculative_verify_qwen3_layer(kvattn):
+    """The Qwen3-8B-shaped layer verifying 4 draft tokens: 16 query rows per KV head."""
+    import torch
+    from kv_cache_decode_02_gb300 import inputs
+    w = inputs.QWEN3_8B_LAYER
+    n_q = 4
+    rng = np.random.default_rng(11)
+    q = rand_f16(rng, (1, n_q, w.n_head, w.head_dim))
+    k, v = inputs.make_kv_f16(w, layer=0)
+    lens = list(w.seq_lens)
+    out, lse = kvattn.decode_multi(dev(q), dev(k), dev(v), dev(np.array(lens, np.int32)), split=w.split)
+    torch.cuda.synchronize()
+    wo, wl = oracle.decode_multi(oracle.decode_f16, q, lens, k, v)
+    check(out, lse, wo, wl)
