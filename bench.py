@@ -382,7 +382,84 @@ def bench_workloads(K, torch, stream, peak):
     res[w.name + "_direct"] = {"ms_per_op": round(ms_d, 3), "tail_bytes": tail_bytes, "tail_gbs": round(gbs_d, 1),
                               "frac_of_measured_h2d": round(gbs_d / h2d_big, 3),
                               "how": "tail rows read in place from pinned host memory by the decode kernel"}
+    del k_win, v_win, k_tail, v_tail, ws, ws_direct
+    for w in (inputs.STACK_TAIL_295MIB, inputs.STACK_TAIL_1815MIB):
+        res[w.name] = bench_layer_stack(K, torch, w, h2d_big)
     return res
+
+
+def bench_layer_stack(K, torch, w, h2d_gbs):
+    """One decode token over a stack of layers that each attend a resident window and stream
+    a pinned host tail, in each way the library offers, against the pages' model
+    t = resident compute + tail bytes / host-link bandwidth."""
+    from kv_cache_decode_02_gb300 import inputs
+    L, H, Hk, D = w.layers, w.n_head, w.n_head_kv, w.head_dim
+    n_win, n_tail = w.n_window, w.n_cells - w.n_window
+    cs, xs = torch.cuda.Stream(), torch.cuda.Stream()
+    kw = [inputs.normal_f16_torch((2000 + w.number, l), (n_win, Hk, D), "cuda") for l in range(L)]
+    vw = [inputs.normal_f16_torch((3000 + w.number, l), (n_win, Hk, D), "cuda") for l in range(L)]
+    kt, vt = [], []
+    for l in range(L):
+        kt.append(inputs.normal_f16_torch((2000 + w.number, L + l), (n_tail, Hk, D), "cuda").cpu().pin_memory())
+        vt.append(inputs.normal_f16_torch((3000 + w.number, L + l), (n_tail, Hk, D), "cuda").cpu().pin_memory())
+    q = torch.cat([torch.from_numpy(inputs.make_q(w, layer=l)) for l in range(L)]).cuda()
+    out = torch.empty((L, H, D), dtype=torch.float32, device="cuda")
+    lse = torch.empty((L, H), dtype=torch.float32, device="cuda")
+    torch.cuda.synchronize()
+
+    def timed(fn, n=3):
+        fn()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(cs)
+        for _ in range(n):
+            fn()
+        b.record(cs)
+        b.synchronize()
+        return a.elapsed_time(b) / n
+
+    def staged(wt, ws, tile, tails=True):
+        for l in range(L):
+            wt(q[l], kw[l], vw[l], kt[l] if tails else None, vt[l] if tails else None, split=w.split,
+               tile_cells=tile, tail_split=w.tail_split, out=out[l], lse=lse[l], ws=ws, compute_stream=cs,
+               copy_stream=xs)
+
+    tail_bytes = L * n_tail * Hk * D * 4
+    ms = {}
+    wt = K.WindowTail()
+    ws = wt.workspace(H, Hk, D, n_win, n_tail, w.split, 512, w.tail_split)
+    ms["resident_only"] = timed(lambda: staged(wt, ws, 512, tails=False))
+    ms["staged_1mib_tiles_graphs"] = timed(lambda: staged(wt, ws, 512))
+    wt.close()
+    wt = K.WindowTail(prefetch=True)
+    ws = wt.workspace(H, Hk, D, n_win, n_tail, w.split, w.tile_cells, w.tail_split)
+    ms["prefetch_layer_tiles"] = timed(lambda: staged(wt, ws, w.tile_cells))
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=cs):
+        staged(wt, ws, w.tile_cells)
+
+    def replay():
+        with torch.cuda.stream(cs):
+            g.replay()
+    ms["prefetch_layer_tiles_captured_step"] = timed(replay)
+    del g
+    wt.close()
+    wsd = torch.zeros(K.kvattn_window_tail_direct_workspace_bytes(H, Hk, D, n_win, n_tail, w.split, w.tail_split),
+                      dtype=torch.uint8, device="cuda")
+
+    def direct():
+        for l in range(L):
+            K.window_tail_direct(q[l], kw[l], vw[l], kt[l], vt[l], split=w.split, tail_split=w.tail_split,
+                                 out=out[l], lse=lse[l], ws=wsd, stream=cs)
+    ms["direct"] = timed(direct)
+    link_ms = tail_bytes / (h2d_gbs * 1e9) * 1e3
+    d = {"layers": L, "n_window": n_win, "n_tail_per_layer": n_tail, "tail_bytes_per_token": tail_bytes,
+         "link_ms": round(link_ms, 3), "model_ms": round(ms["resident_only"] + link_ms, 3)}
+    for k_, v_ in ms.items():
+        d[k_ + "_ms"] = round(v_, 3)
+        if k_ != "resident_only":
+            d[k_ + "_frac_of_link"] = round(link_ms / v_, 3)
+    return d
 
 
 def cpu_baseline_sample(budget_s=12.0):

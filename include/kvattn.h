@@ -269,6 +269,34 @@ typedef struct kvattn_tail_ctx kvattn_tail_ctx;
 int kvattn_tail_ctx_create(kvattn_tail_ctx** ctx);
 int kvattn_tail_ctx_destroy(kvattn_tail_ctx* ctx);
 
+/*
+ * kvattn_tail_ctx_set_flags -- host.  Mode of the later kvattn_decode_window_tail calls
+ * through ctx (0 by default).
+ *
+ * KVATTN_TAIL_PREFETCH: cross-layer prefetch ([RKV] section 1, the cross-layer barrier
+ * between the compute stream and the tail copies; the step-prefetch design).  A model calls
+ * kvattn_decode_window_tail once per layer through one context.  Without the flag every
+ * copy of a call waits for all work enqueued before it on compute_stream, so layer l+1's
+ * tail cannot cross the link while layer l still computes.  With the flag a copy waits only
+ * for
+ *   - the work enqueued before the call on copy_stream (order a device-side write into the
+ *     tail before the call there), and
+ *   - the tile decode that last read its staging slot, in this call or an earlier one
+ *     through the same context,
+ * and the two staging slots alternate across calls, so the next layer's first two tiles
+ * are copied while this layer's window, tiles and merge run.  The first call after the
+ * flag is set, or after a call without it, still orders its copies after compute_stream.
+ * Calls in this mode enqueue the pipeline directly (no CUDA graph), about six operations
+ * per tile: use tiles large enough that a tile's copy outlasts that host work (a whole
+ * layer's tail per tile is a fine choice when two of them fit in device memory).
+ * Contract: a context's calls in this mode run on the same compute_stream and copy_stream,
+ * and a workspace's staging slots are used through one context only.
+ * Errors: INVALID_ARG (null ctx, unknown flag bits).
+ */
+#define KVATTN_TAIL_PREFETCH 1u
+
+int kvattn_tail_ctx_set_flags(kvattn_tail_ctx* ctx, uint32_t flags);
+
 /* Bytes of workspace for kvattn_decode_window_tail: two staging slots of tile_cells rows
  * of K and of V, the partials of the window splits and of every tail tile, status word. */
 size_t kvattn_window_tail_workspace_bytes(int n_head, int n_head_kv, int head_dim,
@@ -288,12 +316,14 @@ size_t kvattn_window_tail_workspace_bytes(int n_head, int n_head_kv, int head_di
  *             cudaMemcpyAsync when they are not mapped (or KVATTN_TAIL_COPY=0 is set);
  *             even tiles go on copy_stream, odd tiles on a stream of the context, so one
  *             copy ramps up while the previous drains.  The first call with a given set of
- *             arguments records the
- *             whole pipeline as a CUDA graph (on the context's own streams) and launches it
- *             on compute_stream; later calls with the same arguments replay that graph, so
- *             the host enqueues one launch instead of about three operations per tile.  A
- *             call on a compute_stream that is itself being captured enqueues the pipeline
- *             on compute_stream and copy_stream directly.
+ *             arguments records the whole pipeline as a CUDA graph (on the context's own
+ *             streams) and launches it on compute_stream; later calls with the same
+ *             arguments replay that graph, so the host enqueues one launch instead of about
+ *             six operations per tile.  A context keeps the graphs of its 64 most recently
+ *             used argument sets (one per layer of a model that shares the context).  A
+ *             call on a compute_stream that is itself being captured, or in
+ *             KVATTN_TAIL_PREFETCH mode, enqueues the pipeline on compute_stream and
+ *             copy_stream directly.
  *  split      cells per partial over the window; tail_split  cells per partial inside a
  *             tile.  Both positive multiples of 32.
  *  out, lse   device float [n_head][head_dim], [n_head].

@@ -212,6 +212,16 @@ struct TailGraphKey {
     bool operator==(const TailGraphKey& o) const { return std::memcmp(this, &o, sizeof(*this)) == 0; }
 };
 
+// Recorded pipelines kept per context: a model with one context for all its layers replays
+// one graph per layer instead of recording a new one on every call.
+constexpr int kTailGraphSlots = 64;
+
+struct TailGraphEntry {
+    TailGraphKey key;
+    cudaGraphExec_t exec;
+    uint64_t last_use;
+};
+
 struct kvattn_tail_ctx {
     cudaEvent_t copied[2];
     cudaEvent_t consumed[2];
@@ -223,8 +233,13 @@ struct kvattn_tail_ctx {
     cudaStream_t cap_main;  // private streams the pipeline is recorded on
     cudaStream_t cap_fork;
     cudaStream_t cap_fork2;
-    cudaGraphExec_t exec;
-    TailGraphKey key;
+    TailGraphEntry graphs[kTailGraphSlots];
+    int n_graphs;
+    uint64_t use_clock;
+    uint32_t flags;          // KVATTN_TAIL_*
+    uint64_t tiles_issued;   // staging-slot sequence carried from call to call (prefetch mode)
+    bool carry_valid;        // consumed[] hold the last readers of both slots (prefetch mode)
+    unsigned long long carry_capture;  // the stream capture those records belong to (0: none)
     int device;
     bool pending;
 };
@@ -507,9 +522,19 @@ int kvattn_tail_ctx_create(kvattn_tail_ctx** ctx) {
         return KVATTN_ERR_CUDA;
     }
     c->pending = false;
-    c->exec = nullptr;
-    std::memset(&c->key, 0, sizeof(c->key));
+    c->n_graphs = 0;
+    c->use_clock = 0;
+    c->flags = 0;
+    c->tiles_issued = 0;
+    c->carry_valid = false;
+    c->carry_capture = 0;
     *ctx = c;
+    return KVATTN_OK;
+}
+
+int kvattn_tail_ctx_set_flags(kvattn_tail_ctx* ctx, uint32_t flags) {
+    if (ctx == nullptr || (flags & ~(uint32_t)KVATTN_TAIL_PREFETCH) != 0u) return KVATTN_ERR_INVALID_ARG;
+    ctx->flags = flags;
     return KVATTN_OK;
 }
 
@@ -518,7 +543,8 @@ int kvattn_tail_ctx_destroy(kvattn_tail_ctx* ctx) {
     cudaEvent_t evs[8] = {ctx->copied[0], ctx->copied[1], ctx->consumed[0], ctx->consumed[1],
                           ctx->start,     ctx->done,      ctx->joined,      ctx->joined2};
     int rc = KVATTN_OK;
-    if (ctx->exec != nullptr && cudaGraphExecDestroy(ctx->exec) != cudaSuccess) rc = KVATTN_ERR_CUDA;
+    for (int i = 0; i < ctx->n_graphs; ++i)
+        if (cudaGraphExecDestroy(ctx->graphs[i].exec) != cudaSuccess) rc = KVATTN_ERR_CUDA;
     for (cudaStream_t st : {ctx->copy2, ctx->cap_main, ctx->cap_fork, ctx->cap_fork2})
         if (cudaStreamDestroy(st) != cudaSuccess) rc = KVATTN_ERR_CUDA;
     for (cudaEvent_t ev : evs)
@@ -659,17 +685,42 @@ void prepare_window_tail(TailPlan& t, const void* q, const void* k_win, const vo
 }
 
 // Enqueue the window decode, the double-buffered tile pipeline and the final merge.
+//
+// carry = false: every copy is ordered after all work enqueued before the call on the
+// compute stream (so no staging slot is overwritten while an earlier call still reads it),
+// and tile i goes to slot i % 2.
+// carry = true (prefetch mode): copies are ordered only after earlier work on the copy
+// stream and after the decode that last read their slot -- possibly one of an earlier call,
+// whose consumed[] record is the newest -- and the slot sequence continues from the earlier
+// call (first tile -> slot slot0).  The next layer's tiles then cross the link while this
+// layer's window, tiles and merge still run on the compute stream.
 int enqueue_window_tail(kvattn_tail_ctx* ctx, const TailPlan& t, const void* k_tail_host, const void* v_tail_host,
                         const void* k_tail_dev, const void* v_tail_dev, int64_t n_tail, int64_t tile_cells,
-                        cudaStream_t cs, cudaStream_t xs, cudaStream_t xs2, int fault) {
+                        cudaStream_t cs, cudaStream_t xs, cudaStream_t xs2, int fault, bool prefetch = false,
+                        bool carry = false, int slot0 = 0, bool capturing = false) {
     const TailLayout& L = t.L;
     const int head_dim = t.merge.head_dim;
     const int n_head_kv = t.base.n_head_kv;
-    // The copy stream may not overwrite a staging slot that an earlier call's tile decode
-    // on the compute stream still reads.
-    if (cudaEventRecord(ctx->start, cs) != cudaSuccess) return KVATTN_ERR_CUDA;
-    if (cudaStreamWaitEvent(xs, ctx->start, 0) != cudaSuccess) return KVATTN_ERR_CUDA;
-    if (cudaStreamWaitEvent(xs2, ctx->start, 0) != cudaSuccess) return KVATTN_ERR_CUDA;
+    if (!carry) {
+        // The copy stream may not overwrite a staging slot that an earlier call's tile decode
+        // on the compute stream still reads.
+        if (cudaEventRecord(ctx->start, cs) != cudaSuccess) return KVATTN_ERR_CUDA;
+        if (cudaStreamWaitEvent(xs, ctx->start, 0) != cudaSuccess) return KVATTN_ERR_CUDA;
+        if (cudaStreamWaitEvent(xs2, ctx->start, 0) != cudaSuccess) return KVATTN_ERR_CUDA;
+        if (prefetch) {
+            // Start the carried slot sequence: a slot this call leaves unused must still be
+            // guarded for the next call by a record that follows every earlier reader (a
+            // replayed graph's readers never record the context's events, and a record made
+            // before a stream capture cannot be waited on inside it).
+            if (cudaEventRecord(ctx->consumed[0], cs) != cudaSuccess) return KVATTN_ERR_CUDA;
+            if (cudaEventRecord(ctx->consumed[1], cs) != cudaSuccess) return KVATTN_ERR_CUDA;
+        }
+    } else if (L.n_tiles > 0) {
+        // the context's copy stream follows the caller's: whatever the caller ordered before
+        // the call on copy_stream (a write into the tail, say) precedes every copy
+        if (cudaEventRecord(ctx->start, xs) != cudaSuccess) return KVATTN_ERR_CUDA;
+        if (cudaStreamWaitEvent(xs2, ctx->start, 0) != cudaSuccess) return KVATTN_ERR_CUDA;
+    }
     // window: resident cells, attended while the first tail tiles are in flight
     if (L.n_split_win > 0) {
         if (launch_decode_units(t.window, KVATTN_KV_F16, head_dim, L.n_split_win, cs, t.pdl) != cudaSuccess)
@@ -679,12 +730,13 @@ int enqueue_window_tail(kvattn_tail_ctx* ctx, const TailPlan& t, const void* k_t
     // ramps up while the previous one drains), decoded on the compute stream
     SplitDecodeParams slot[2] = {t.slot[0], t.slot[1]};
     for (int64_t i = 0; i < L.n_tiles; ++i) {
-        const int sl = (int)(i & 1);
+        const int sl = (int)((i + slot0) & 1);
         cudaStream_t xsi = sl ? xs2 : xs;
         const int64_t c0 = i * tile_cells;
         const int64_t len = (c0 + tile_cells <= n_tail) ? tile_cells : n_tail - c0;
         const size_t bytes = (size_t)len * t.row_bytes;
-        if (i >= 2 && cudaStreamWaitEvent(xsi, ctx->consumed[sl], 0) != cudaSuccess) return KVATTN_ERR_CUDA;
+        if ((i >= 2 || carry) && cudaStreamWaitEvent(xsi, ctx->consumed[sl], 0) != cudaSuccess)
+            return KVATTN_ERR_CUDA;
         if (i == fault) return KVATTN_ERR_CUDA;
         if (k_tail_dev != nullptr) {
             if (launch_tile_copy(static_cast<const char*>(k_tail_dev) + (size_t)c0 * t.row_bytes,
@@ -712,11 +764,15 @@ int enqueue_window_tail(kvattn_tail_ctx* ctx, const TailPlan& t, const void* k_t
             return KVATTN_ERR_CUDA;
         if (cudaEventRecord(ctx->consumed[sl], cs) != cudaSuccess) return KVATTN_ERR_CUDA;
     }
-    // join both copy streams back into the compute stream
-    if (cudaEventRecord(ctx->joined, xs) != cudaSuccess) return KVATTN_ERR_CUDA;
-    if (cudaEventRecord(ctx->joined2, xs2) != cudaSuccess) return KVATTN_ERR_CUDA;
-    if (cudaStreamWaitEvent(cs, ctx->joined, 0) != cudaSuccess) return KVATTN_ERR_CUDA;
-    if (cudaStreamWaitEvent(cs, ctx->joined2, 0) != cudaSuccess) return KVATTN_ERR_CUDA;
+    if (!carry || capturing) {
+        // join both copy streams back into the compute stream (a recorded graph must end
+        // on the stream it began on; otherwise, with carry, the compute stream already
+        // waited for every copy of this call through copied[])
+        if (cudaEventRecord(ctx->joined, xs) != cudaSuccess) return KVATTN_ERR_CUDA;
+        if (cudaEventRecord(ctx->joined2, xs2) != cudaSuccess) return KVATTN_ERR_CUDA;
+        if (cudaStreamWaitEvent(cs, ctx->joined, 0) != cudaSuccess) return KVATTN_ERR_CUDA;
+        if (cudaStreamWaitEvent(cs, ctx->joined2, 0) != cudaSuccess) return KVATTN_ERR_CUDA;
+    }
     if (launch_merge(t.merge, cs, t.pdl) != cudaSuccess) return KVATTN_ERR_CUDA;
     return KVATTN_OK;
 }
@@ -785,13 +841,32 @@ int kvattn_decode_window_tail(kvattn_tail_ctx* ctx, const void* q, const void* k
     }
 
     cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
-    if (cudaStreamIsCapturing(cs, &cap) != cudaSuccess) return KVATTN_ERR_CUDA;
-    const bool use_graph = use_tail_graph() && cap == cudaStreamCaptureStatusNone && fault < 0;
+    unsigned long long capture_id = 0;
+    if (cudaStreamGetCaptureInfo(cs, &cap, &capture_id) != cudaSuccess) return KVATTN_ERR_CUDA;
+    if (cap != cudaStreamCaptureStatusActive) capture_id = 0;
+    // Prefetch mode enqueues directly: a graph launched on the compute stream could not
+    // start its copies before the compute stream reached it.  Its first call through a
+    // context (or the first after a call in the other mode) still orders its copies after
+    // the compute stream, since the slots' last readers are not known yet; so does the first
+    // call of a stream capture (the readers' records lie outside it) -- a whole decode step
+    // captured with its layers in this mode replays as one graph whose copies run ahead
+    // across layers.
+    const bool prefetch = (ctx->flags & KVATTN_TAIL_PREFETCH) != 0u;
+    const bool carry = prefetch && ctx->carry_valid && ctx->carry_capture == capture_id;
+    const bool use_graph = !prefetch && use_tail_graph() && cap == cudaStreamCaptureStatusNone && fault < 0;
     if (!use_graph) {
+        const int slot0 = prefetch ? (int)(ctx->tiles_issued & 1u) : 0;
+        ctx->carry_valid = false;  // until this call's records are all enqueued
         const int rc = enqueue_window_tail(ctx, plan, k_tail_host, v_tail_host, k_dev, v_dev, n_tail, tile_cells, cs,
-                                           xs, ctx->copy2, fault);
+                                           xs, ctx->copy2, fault, prefetch, carry, slot0, capture_id != 0);
         if (rc != KVATTN_OK) return rc;
+        if (prefetch) {
+            ctx->tiles_issued += (uint64_t)plan.L.n_tiles;
+            ctx->carry_valid = true;
+            ctx->carry_capture = capture_id;
+        }
     } else {
+        ctx->carry_valid = false;
         TailGraphKey key;
         std::memset(&key, 0, sizeof(key));
         key.q = q;
@@ -818,10 +893,21 @@ int kvattn_decode_window_tail(kvattn_tail_ctx* ctx, const void* q, const void* k
         key.wait_limit_ns = plan.base.wait_limit_ns;
         key.pdl = plan.pdl ? 1 : 0;
         cudaGetDevice(&key.device);
-        if (ctx->exec == nullptr || !(ctx->key == key)) {
-            if (ctx->exec != nullptr) {
-                cudaGraphExecDestroy(ctx->exec);
-                ctx->exec = nullptr;
+        TailGraphEntry* hit = nullptr;
+        for (int i = 0; i < ctx->n_graphs && hit == nullptr; ++i)
+            if (ctx->graphs[i].key == key) hit = &ctx->graphs[i];
+        if (hit == nullptr) {
+            // a free entry, or the least recently used one
+            TailGraphEntry* slot = nullptr;
+            if (ctx->n_graphs < kTailGraphSlots) {
+                slot = &ctx->graphs[ctx->n_graphs];
+            } else {
+                slot = &ctx->graphs[0];
+                for (int i = 1; i < ctx->n_graphs; ++i)
+                    if (ctx->graphs[i].last_use < slot->last_use) slot = &ctx->graphs[i];
+                cudaGraphExecDestroy(slot->exec);
+                *slot = ctx->graphs[--ctx->n_graphs];
+                slot = &ctx->graphs[ctx->n_graphs];
             }
             // Record the pipeline once as a graph: ~3 operations per tile would otherwise
             // cost more host time per call than the host-to-device copies themselves.
@@ -840,10 +926,13 @@ int kvattn_decode_window_tail(kvattn_tail_ctx* ctx, const void* q, const void* k
             const cudaError_t ei = cudaGraphInstantiate(&exec, graph, 0);
             cudaGraphDestroy(graph);
             if (ei != cudaSuccess) return KVATTN_ERR_CUDA;
-            ctx->exec = exec;
-            ctx->key = key;
+            slot->key = key;
+            slot->exec = exec;
+            ++ctx->n_graphs;
+            hit = slot;
         }
-        if (cudaGraphLaunch(ctx->exec, cs) != cudaSuccess) return KVATTN_ERR_CUDA;
+        hit->last_use = ++ctx->use_clock;
+        if (cudaGraphLaunch(hit->exec, cs) != cudaSuccess) return KVATTN_ERR_CUDA;
     }
     if (cudaEventRecord(ctx->done, cs) != cudaSuccess) return KVATTN_ERR_CUDA;
     ctx->pending = true;

@@ -16,8 +16,8 @@ Layouts (all row-major, C order):
 
 Workloads follow the five decode-attention shapes used throughout the tests and
 the benchmark: a tiny GQA-4 case, a Qwen3-8B-shaped layer, a four-sequence GQA-6
-unified cache read through a compact cell plan, a Q8_0 long-context cache and a
-window + host-tail overflow cache.  Seeds: 1000+w for q, 2000+w for K, 3000+w
+unified cache read through a compact cell plan, a Q8_0 long-context cache, a
+window + host-tail overflow cache, and 36-layer stacks of window + host tail.  Seeds: 1000+w for q, 2000+w for K, 3000+w
 for V, 4000+w for the record layout and holes (w = workload number).
 """
 from __future__ import annotations
@@ -66,8 +66,20 @@ Q8_LONG_D256 = Workload("q8_0_n131072_d256", 4, 1, 131072, 32, 8, 256, 512,
 WINDOW_TAIL = Workload("window_tail_n524288", 5, 1, 524288, 40, 8, 128, 256,
                        seq_lens=(524288,), n_window=16384, tile_cells=512, tail_split=128)
 
+# Layer stacks of window + host tail at the two overflow operating points of the pages'
+# Qwen3-8B table (36 layers that all stream a tail; ~13.1k-token prompt): 11008 resident
+# cells and ~2.1k tail cells per layer (295 MiB of tail per token), and the 256-cell window
+# floor with ~12.9k tail cells per layer (1815 MiB).  tile_cells holds a layer's whole tail.
+STACK_TAIL_295MIB = Workload("qwen3_8b_x36_tail_295mib", 6, 1, 11008 + 2100, 32, 8, 128, 256,
+                             seq_lens=(11008 + 2100,), n_window=11008, tile_cells=2176, tail_split=128,
+                             layers=36)
+STACK_TAIL_1815MIB = Workload("qwen3_8b_x36_tail_1815mib", 7, 1, 256 + 12900, 32, 8, 128, 256,
+                              seq_lens=(256 + 12900,), n_window=256, tile_cells=12928, tail_split=128,
+                              layers=36)
+
 WORKLOADS = {w.name: w for w in
-             (TINY, QWEN3_8B_LAYER, MULTISLOT_PLAN, Q8_LONG_D128, Q8_LONG_D256, WINDOW_TAIL)}
+             (TINY, QWEN3_8B_LAYER, MULTISLOT_PLAN, Q8_LONG_D128, Q8_LONG_D256, WINDOW_TAIL,
+              STACK_TAIL_295MIB, STACK_TAIL_1815MIB)}
 
 
 def _rng(*seed) -> np.random.Generator:

@@ -34,6 +34,7 @@ KVATTN_KV_F16 = 0
 KVATTN_KV_Q8_0 = 1
 KVATTN_DEVICE_WAIT_TIMEOUT = 1
 KVATTN_DEVICE_BAD_PLAN_ENTRY = 2
+KVATTN_TAIL_PREFETCH = 1
 
 EXPORTED = (
     "kvattn_status_string", "kvattn_version", "kvattn_build_cell_plan", "kvattn_build_descriptors",
@@ -43,7 +44,7 @@ EXPORTED = (
     "kvattn_tail_wait", "kvattn_workspace_status", "kvattn_decode_noalloc",
     "kvattn_window_tail_direct_workspace_bytes", "kvattn_decode_window_tail_direct",
     "kvattn_select_split_for", "kvattn_select_split", "kvattn_decode_multi_workspace_bytes",
-    "kvattn_decode_multi",
+    "kvattn_decode_multi", "kvattn_tail_ctx_set_flags",
 )
 
 _P = ctypes.c_void_p
@@ -86,6 +87,8 @@ lib.kvattn_tail_ctx_create.argtypes = [ctypes.POINTER(_P)]
 lib.kvattn_tail_ctx_create.restype = _I
 lib.kvattn_tail_ctx_destroy.argtypes = [_P]
 lib.kvattn_tail_ctx_destroy.restype = _I
+lib.kvattn_tail_ctx_set_flags.argtypes = [_P, ctypes.c_uint32]
+lib.kvattn_tail_ctx_set_flags.restype = _I
 lib.kvattn_window_tail_workspace_bytes.argtypes = [_I, _I, _I, _I64, _I64, _I, _I64, _I]
 lib.kvattn_window_tail_workspace_bytes.restype = _SZ
 lib.kvattn_decode_window_tail.argtypes = [_P, _P, _P, _P, _I64, _P, _P, _I64, _I64, _I, _I, _I, _I,
@@ -234,6 +237,10 @@ def kvattn_tail_ctx_create() -> int:
 
 def kvattn_tail_ctx_destroy(ctx: int) -> None:
     _check(lib.kvattn_tail_ctx_destroy(ctx), "kvattn_tail_ctx_destroy")
+
+
+def kvattn_tail_ctx_set_flags(ctx: int, flags: int) -> None:
+    _check(lib.kvattn_tail_ctx_set_flags(ctx, flags), "kvattn_tail_ctx_set_flags")
 
 
 def kvattn_window_tail_workspace_bytes(n_head, n_head_kv, head_dim, n_win, n_tail, split, tile_cells,
@@ -396,10 +403,16 @@ def build_cell_plan(encoded_per_seq, capacity_cells, plan_stride=None):
 
 
 class WindowTail:
-    """Owns a tail context (events only) and runs kvattn_decode_window_tail."""
+    """Owns a tail context (events only) and runs kvattn_decode_window_tail.
 
-    def __init__(self):
+    ``prefetch=True`` sets KVATTN_TAIL_PREFETCH: one context serves every layer of a model,
+    and a layer's tail copies wait only for the decode that last read their staging slot,
+    not for the layers before it."""
+
+    def __init__(self, prefetch=False):
         self.ctx = kvattn_tail_ctx_create()
+        if prefetch:
+            kvattn_tail_ctx_set_flags(self.ctx, KVATTN_TAIL_PREFETCH)
 
     def close(self):
         if self.ctx:

@@ -144,6 +144,7 @@ def test_window_tail_validation(kvattn):
     bad = list(base); bad[0] = None               # no context
     assert f(*bad) == -1
     assert kvattn.lib.kvattn_tail_ctx_destroy(None) == -1
+    assert kvattn.lib.kvattn_tail_ctx_set_flags(None, kvattn.KVATTN_TAIL_PREFETCH) == -1
     assert kvattn.lib.kvattn_tail_wait(None, 10) == -1
 
 
