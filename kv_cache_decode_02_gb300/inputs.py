@@ -11,6 +11,10 @@ Layouts (all row-major, C order):
 * K, V (f16)   f16  [n_cells][n_head_kv][head_dim]          (cell-major rows)
 * K, V (Q8_0)  qs int8 [n_cells][n_head_kv][head_dim] plus
                d  f16  [n_cells][n_head_kv][head_dim // 32]  (value = d * qs)
+* K, V (Q4_0)  packed uint8 [n_cells][n_head_kv][head_dim // 2] plus
+               d  f16  [n_cells][n_head_kv][head_dim // 32]
+               (byte j of block b: element 32b + j low nibble, 32b + 16 + j high;
+               value = d * (nibble - 8))
 * encoded cells for the plan builder: int64, low 32 bits = physical cell,
   high 32 bits = a stage-slot tag that the read plan ignores.
 
@@ -112,6 +116,16 @@ def q8_0_planes(rng: np.random.Generator, n_cells: int, n_head_kv: int, head_dim
     qs = rng.integers(-127, 128, size=(n_cells, n_head_kv, head_dim), dtype=np.int8)
     d = rng.uniform(0.001, 0.02, size=(n_cells, n_head_kv, head_dim // 32)).astype(np.float16)
     return qs, d
+
+
+def q4_0_planes(rng: np.random.Generator, n_cells: int, n_head_kv: int, head_dim: int):
+    """Q4_0 SoA planes: packed bytes uniform in [0, 255] (two 4-bit values each, so every
+    value 0..15 is equally likely), f16 scales ~U(0.001, 0.3) (values up to ~2.4 in
+    magnitude, as for Q8_0)."""
+    assert head_dim % 32 == 0
+    packed = rng.integers(0, 256, size=(n_cells, n_head_kv, head_dim // 2), dtype=np.uint8)
+    d = rng.uniform(0.001, 0.3, size=(n_cells, n_head_kv, head_dim // 32)).astype(np.float16)
+    return packed, d
 
 
 def make_q(w: Workload, layer: int = 0, seed: int | None = None) -> np.ndarray:

@@ -52,7 +52,10 @@ def _load():
             lib.oracle_decode_f16.argtypes = [P, P, P] + common
             lib.oracle_decode_q8_0.argtypes = [P, P, P, P, P] + common
             lib.oracle_decode_f64.argtypes = [P, P, P] + common
-            for f in (lib.oracle_decode_f16, lib.oracle_decode_q8_0, lib.oracle_decode_f64):
+            lib.oracle_decode_q8_0_q4_0.argtypes = [P, P, P, P, P] + common
+            lib.oracle_decode_q4_0.argtypes = [P, P, P, P, P] + common
+            for f in (lib.oracle_decode_f16, lib.oracle_decode_q8_0, lib.oracle_decode_f64,
+                      lib.oracle_decode_q8_0_q4_0, lib.oracle_decode_q4_0):
                 f.restype = ctypes.c_int
             lib.oracle_merge.argtypes = [P, P, i32, i32, i32, P, P]
             lib.oracle_merge.restype = ctypes.c_int
@@ -131,6 +134,39 @@ def decode_q8_0(q, k_qs, k_d, v_qs, v_d, seq_lens, plan=None, scale=None, n_thre
     return out, lse
 
 
+def decode_q8_0_q4_0(q, k_qs, k_d, v_q4, v_d, seq_lens, plan=None, scale=None, n_threads=None):
+    """fp64 decode attention over Q8_0 keys and Q4_0 values.  v_q4: uint8 [cells][Hk][D/2]
+    (block b of a row = bytes 16b..16b+15; byte j: element j low nibble, j+16 high), v_d:
+    f16 [cells][Hk][D/32]; element value d * (nibble - 8)."""
+    q = np.ascontiguousarray(q, dtype=np.float16)
+    k_qs = np.ascontiguousarray(k_qs, dtype=np.int8)
+    v_q4 = np.ascontiguousarray(v_q4, dtype=np.uint8)
+    k_d = np.ascontiguousarray(k_d, dtype=np.float16)
+    v_d = np.ascontiguousarray(v_d, dtype=np.float16)
+    assert v_q4.shape[:-1] == k_qs.shape[:-1] and 2 * v_q4.shape[-1] == k_qs.shape[-1]
+    args, out, lse, keep = _common(q, k_qs.shape, seq_lens, plan, scale, n_threads)
+    rc = _load().oracle_decode_q8_0_q4_0(_ptr(q), _ptr(k_qs), _ptr(k_d), _ptr(v_q4), _ptr(v_d), *args)
+    if rc != 0:
+        raise ValueError("oracle_decode_q8_0_q4_0 rejected its arguments")
+    return out, lse
+
+
+def decode_q4_0(q, k_q4, k_d, v_q4, v_d, seq_lens, plan=None, scale=None, n_threads=None):
+    """fp64 decode attention over Q4_0 keys and values (layout as decode_q8_0_q4_0's V)."""
+    q = np.ascontiguousarray(q, dtype=np.float16)
+    k_q4 = np.ascontiguousarray(k_q4, dtype=np.uint8)
+    v_q4 = np.ascontiguousarray(v_q4, dtype=np.uint8)
+    k_d = np.ascontiguousarray(k_d, dtype=np.float16)
+    v_d = np.ascontiguousarray(v_d, dtype=np.float16)
+    assert k_q4.shape == v_q4.shape
+    shape = k_q4.shape[:-1] + (2 * k_q4.shape[-1],)
+    args, out, lse, keep = _common(q, shape, seq_lens, plan, scale, n_threads)
+    rc = _load().oracle_decode_q4_0(_ptr(q), _ptr(k_q4), _ptr(k_d), _ptr(v_q4), _ptr(v_d), *args)
+    if rc != 0:
+        raise ValueError("oracle_decode_q4_0 rejected its arguments")
+    return out, lse
+
+
 def decode_f64(q, k, v, seq_lens, plan=None, scale=None, n_threads=None):
     """fp64 decode attention over fp64 inputs (no storage-format front end)."""
     q = np.ascontiguousarray(q, dtype=np.float64)
@@ -182,6 +218,18 @@ def merge(parts, lses):
 
 def f16_to_f64(bits: int) -> float:
     return _load().oracle_f16_to_f64(bits)
+
+
+def dequant_q4_0(packed, d):
+    """Explicit fp64 dequantisation of Q4_0 planes (used only to pin the oracle): packed
+    uint8 [..., D/2], d f16 [..., D/32] -> float64 [..., D]."""
+    packed = np.asarray(packed, dtype=np.uint8)
+    d = np.asarray(d).astype(np.float64)
+    blocks = packed.reshape(packed.shape[:-1] + (-1, 16))
+    lo = (blocks & 0x0F).astype(np.float64) - 8.0    # elements 0..15 of each block
+    hi = (blocks >> 4).astype(np.float64) - 8.0      # elements 16..31
+    vals = np.concatenate([lo, hi], axis=-1)         # [..., D/32, 32]
+    return (vals * d[..., None]).reshape(packed.shape[:-1] + (2 * packed.shape[-1],))
 
 
 def dequant_q8_0(qs, d):

@@ -24,7 +24,15 @@
  *
  * An empty valid set gives O = 0 and LSE = -inf.  Every stored element is turned into
  * its exact fp64 value first: f16 by the IEEE 754 binary16 definition, Q8_0 as
- * d * qs with d an f16 scale shared by 32 consecutive head_dim elements.
+ * d * qs with d an f16 scale shared by 32 consecutive head_dim elements, Q4_0 as
+ * d * (n - 8) with n an unsigned 4-bit value and d an f16 scale per 32 elements.  The
+ * pages name the q4_0 type (the mixed "q8_0K/q4_0V" cache of the Rolling-KV evaluation's
+ * resident-compression anchors, and a q4_0 cache in its section 5a) without its bytes;
+ * the reading taken is the llama.cpp q4_0 block -- 32 elements share one f16 scale and
+ * 16 bytes, byte j of a block holding element j in its low nibble and element j + 16 in
+ * its high nibble -- with the values and the scales kept in two planes:
+ *     values uint8 [cells][Hk][D/2] (block b of a row = bytes 16b .. 16b+15),
+ *     scales f16   [cells][Hk][D/32].
  *
  * The merge follows the same definition over partial results:
  *     M = max_p LSE_p;  w_p = exp(LSE_p - M);
@@ -39,6 +47,7 @@
 #define ORACLE_KV_F16 0
 #define ORACLE_KV_Q8_0 1
 #define ORACLE_KV_F64 2
+#define ORACLE_KV_Q4_0 3
 
 /* IEEE 754 binary16 -> binary64, from the format's definition (exact). */
 double oracle_f16_to_f64(uint16_t h) {
@@ -70,8 +79,8 @@ static void f16_table_init(void) {
 /* One K or V source: element (cell, kv_head, dim) -> exact fp64 value. */
 typedef struct {
     int kind;
-    const void* data;        /* f16 bits / int8 / double, [cells][Hk][D] */
-    const uint16_t* scale;   /* Q8_0 only: f16 bits [cells][Hk][D/32] */
+    const void* data;        /* f16 bits / int8 / double [cells][Hk][D]; Q4_0: uint8 [cells][Hk][D/2] */
+    const uint16_t* scale;   /* Q8_0 and Q4_0: f16 bits [cells][Hk][D/32] */
 } kv_source;
 
 static double kv_value(const kv_source* src, int64_t cell, int g, int d, int Hk, int D) {
@@ -83,6 +92,14 @@ static double kv_value(const kv_source* src, int64_t cell, int g, int d, int Hk,
         double qs = (double)((const int8_t*)src->data)[idx];
         int64_t sidx = (cell * Hk + g) * (int64_t)(D / 32) + d / 32;
         return f16_table[src->scale[sidx]] * qs;
+    }
+    case ORACLE_KV_Q4_0: {
+        int j = d % 32;                             /* position inside the 32-element block */
+        int64_t byte_idx = (cell * Hk + g) * (int64_t)(D / 2) + 16 * (d / 32) + j % 16;
+        unsigned byte = ((const uint8_t*)src->data)[byte_idx];
+        unsigned n = (j < 16) ? (byte & 15u) : (byte >> 4);
+        int64_t sidx = (cell * Hk + g) * (int64_t)(D / 32) + d / 32;
+        return f16_table[src->scale[sidx]] * ((double)n - 8.0);
     }
     default:
         return ((const double*)src->data)[idx];
@@ -194,6 +211,32 @@ int oracle_decode_q8_0(const uint16_t* q, const int8_t* k_qs, const uint16_t* k_
                        double* out, double* lse, int n_threads) {
     if (D % 32 != 0) return -1;
     kv_source K = {ORACLE_KV_Q8_0, k_qs, k_d}, V = {ORACLE_KV_Q8_0, v_qs, v_d};
+    return oracle_decode(q, 0, &K, &V, n_cells_phys, per_seq_cells, plan, plan_stride, seq_lens,
+                         S, H, Hk, D, scale, out, lse, n_threads);
+}
+
+/* Q8_0 keys and Q4_0 values (the mixed cache); values uint8 [cells][Hk][D/2]. */
+int oracle_decode_q8_0_q4_0(const uint16_t* q, const int8_t* k_qs, const uint16_t* k_d,
+                            const uint8_t* v_q4, const uint16_t* v_d,
+                            int64_t n_cells_phys, int64_t per_seq_cells,
+                            const int32_t* plan, int64_t plan_stride, const int64_t* seq_lens,
+                            int S, int H, int Hk, int D, double scale,
+                            double* out, double* lse, int n_threads) {
+    if (D % 32 != 0) return -1;
+    kv_source K = {ORACLE_KV_Q8_0, k_qs, k_d}, V = {ORACLE_KV_Q4_0, v_q4, v_d};
+    return oracle_decode(q, 0, &K, &V, n_cells_phys, per_seq_cells, plan, plan_stride, seq_lens,
+                         S, H, Hk, D, scale, out, lse, n_threads);
+}
+
+/* Q4_0 keys and values. */
+int oracle_decode_q4_0(const uint16_t* q, const uint8_t* k_q4, const uint16_t* k_d,
+                       const uint8_t* v_q4, const uint16_t* v_d,
+                       int64_t n_cells_phys, int64_t per_seq_cells,
+                       const int32_t* plan, int64_t plan_stride, const int64_t* seq_lens,
+                       int S, int H, int Hk, int D, double scale,
+                       double* out, double* lse, int n_threads) {
+    if (D % 32 != 0) return -1;
+    kv_source K = {ORACLE_KV_Q4_0, k_q4, k_d}, V = {ORACLE_KV_Q4_0, v_q4, v_d};
     return oracle_decode(q, 0, &K, &V, n_cells_phys, per_seq_cells, plan, plan_stride, seq_lens,
                          S, H, Hk, D, scale, out, lse, n_threads);
 }

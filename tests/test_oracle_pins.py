@@ -247,6 +247,65 @@ def test_q8_0_front_end_equals_explicit_dequant(D):
     assert not np.allclose(o9, o8)
 
 
+def test_q4_0_block_worked_by_hand():
+    """q4_0 as the llama.cpp block defines it: 32 elements, one f16 scale, byte j holding
+    element j in its low nibble and element j + 16 in its high nibble, value d * (n - 8).
+    Bytes j | (15 - j) << 4 with d = 0.5 give elements 0..15 = 0.5 (j - 8) and elements
+    16..31 = 0.5 (7 - j), written out below.  A single cell reduces attention to O = V, so
+    the C oracle's Q4_0 front end is pinned to the same literal row."""
+    expected = [-4.0, -3.5, -3.0, -2.5, -2.0, -1.5, -1.0, -0.5, 0.0, 0.5, 1.0, 1.5, 2.0, 2.5, 3.0, 3.5,
+                3.5, 3.0, 2.5, 2.0, 1.5, 1.0, 0.5, 0.0, -0.5, -1.0, -1.5, -2.0, -2.5, -3.0, -3.5, -4.0]
+    row = np.array([j | ((15 - j) << 4) for j in range(16)], dtype=np.uint8)
+    d = np.array([0.5], dtype=np.float16)
+    np.testing.assert_array_equal(oracle.dequant_q4_0(row, d), expected)
+    # D = 128: four blocks with scales 0.5, 1, 2, -0.25 over the same bytes
+    D = 128
+    v4 = np.tile(row, 4).reshape(1, 1, D // 2)
+    vd = np.array([[[0.5, 1.0, 2.0, -0.25]]], dtype=np.float16)
+    kq = np.ones((1, 1, D), dtype=np.int8)
+    kd = np.full((1, 1, D // 32), 0.01, dtype=np.float16)
+    q = np.ones((1, 1, D), dtype=np.float16)
+    out, lse = oracle.decode_q8_0_q4_0(q, kq, kd, v4, vd, [1])
+    want = np.concatenate([np.array(expected) * f for f in (1.0, 2.0, 4.0, -0.5)])
+    np.testing.assert_array_equal(out[0, 0], want)
+    # x = scale * sum_d 1 * 0.01 (f16) = the single cell's logit = its LSE
+    assert lse[0, 0] == pytest.approx(float(np.float16(0.01)) * D / math.sqrt(D), rel=1e-15)
+    o4, _ = oracle.decode_q4_0(q, np.tile(row, 4).reshape(1, 1, D // 2), vd, v4, vd, [1])
+    np.testing.assert_array_equal(o4[0, 0], want)
+
+
+@pytest.mark.parametrize("D", [128, 256])
+def test_q4_0_front_ends_equal_explicit_dequant(D):
+    rng = np.random.default_rng(16)
+    N, H, Hk = 90, 6, 2
+    q = rand_f16(rng, (1, H, D))
+    kq = rng.integers(-127, 128, (N, Hk, D), dtype=np.int8)
+    k4 = rng.integers(0, 256, (N, Hk, D // 2), dtype=np.uint8)
+    v4 = rng.integers(0, 256, (N, Hk, D // 2), dtype=np.uint8)
+    kd = rng.uniform(0.001, 0.02, (N, Hk, D // 32)).astype(np.float16)
+    vd = rng.uniform(0.001, 0.02, (N, Hk, D // 32)).astype(np.float16)
+    om, lm = oracle.decode_q8_0_q4_0(q, kq, kd, v4, vd, [N])
+    of, lf = oracle.decode_f64(q.astype(np.float64), oracle.dequant_q8_0(kq, kd), oracle.dequant_q4_0(v4, vd), [N])
+    np.testing.assert_array_equal(om, of)
+    np.testing.assert_array_equal(lm, lf)
+    o4, l4 = oracle.decode_q4_0(q, k4, kd * 8, v4, vd, [N])
+    of, lf = oracle.decode_f64(q.astype(np.float64), oracle.dequant_q4_0(k4, kd * 8), oracle.dequant_q4_0(v4, vd),
+                               [N])
+    np.testing.assert_array_equal(o4, of)
+    np.testing.assert_array_equal(l4, lf)
+    # nibble value 8 is zero: O = 0 and the LSE is that of the keys alone
+    eights = np.full_like(v4, 0x88)
+    oz, lz = oracle.decode_q8_0_q4_0(q, kq, kd, eights, vd, [N])
+    assert np.all(oz == 0.0)
+    np.testing.assert_array_equal(lz, lm)
+    # a block's scale reaches its own 32 elements only
+    vd2 = vd.copy()
+    vd2[:, :, 1] *= 2
+    o9, _ = oracle.decode_q8_0_q4_0(q, kq, kd, v4, vd2, [N])
+    changed = np.any(o9 != om, axis=(0, 1))
+    assert changed[32:64].all() and not changed[:32].any() and not changed[64:].any()
+
+
 def test_merge_special_cases():
     rng = np.random.default_rng(16)
     R, D = 3, 8
