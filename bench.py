@@ -220,6 +220,24 @@ def h2d_bandwidth(torch):
     return n / (min(big) * 1e-3) / 1e9, n / (min(small) * 1e-3) / 1e9
 
 
+def quantized_kv_torch(torch, w):
+    """Device K/V planes of a Q8_0 or Q8_0-key / Q4_0-value workload, drawn with a seeded torch
+    generator in the value ranges of the seeded numpy generators (int8 in [-127, 127], Q8_0
+    scales U(0.001, 0.02); 4-bit pairs as bytes in [0, 255], Q4_0 scales U(0.001, 0.3))."""
+    N, Hk, D = w.n_cells, w.n_head_kv, w.head_dim
+    g = torch.Generator(device="cuda")
+    g.manual_seed(2000 + w.number)
+    kq = torch.randint(-127, 128, (N, Hk, D), dtype=torch.int8, device="cuda", generator=g)
+    kd = (torch.rand((N, Hk, D // 32), device="cuda", generator=g) * 0.019 + 0.001).half()
+    if w.kv_type == "q8_0_q4_0":
+        vq = torch.randint(0, 256, (N, Hk, D // 2), dtype=torch.uint8, device="cuda", generator=g)
+        vd = (torch.rand((N, Hk, D // 32), device="cuda", generator=g) * 0.299 + 0.001).half()
+    else:
+        vq = torch.randint(-127, 128, (N, Hk, D), dtype=torch.int8, device="cuda", generator=g)
+        vd = (torch.rand((N, Hk, D // 32), device="cuda", generator=g) * 0.019 + 0.001).half()
+    return kq, vq, kd, vd
+
+
 def bench_workloads(K, torch, stream, peak):
     """Secondary measurements of the other decode-attention workloads (device-timed)."""
     from kv_cache_decode_02_gb300 import inputs
@@ -308,24 +326,22 @@ def bench_workloads(K, torch, stream, peak):
                                                                  "plan_entries": int(plens.sum())})
     del kk, vv
 
-    # Q8_0 long context, head_dim 128 and 256
-    for w in (inputs.Q8_LONG_D128, inputs.Q8_LONG_D256):
+    # Q8_0 long context, head_dim 128 and 256; and Q8_0 keys with Q4_0 values
+    for w in (inputs.Q8_LONG_D128, inputs.Q8_LONG_D256, inputs.Q8Q4_LONG_D128, inputs.Q8Q4_LONG_D256):
         N, Hk, D = w.n_cells, w.n_head_kv, w.head_dim
-        g = torch.Generator(device="cuda")
-        g.manual_seed(2000 + w.number)
-        kq = torch.randint(-127, 128, (N, Hk, D), dtype=torch.int8, device="cuda", generator=g)
-        vq = torch.randint(-127, 128, (N, Hk, D), dtype=torch.int8, device="cuda", generator=g)
-        kd = (torch.rand((N, Hk, D // 32), device="cuda", generator=g) * 0.019 + 0.001).half()
-        vd = (torch.rand((N, Hk, D // 32), device="cuda", generator=g) * 0.019 + 0.001).half()
+        kq, vq, kd, vd = quantized_kv_torch(torch, w)
+        q4 = w.kv_type == "q8_0_q4_0"
         q = torch.from_numpy(inputs.make_q(w)).cuda()
         lens = torch.tensor([N], dtype=torch.int32, device="cuda")
         ws = K.decode_workspace(1, w.n_head, D, N, w.split)
         out = torch.empty((1, w.n_head, D), dtype=torch.float32, device="cuda")
         lse = torch.empty((1, w.n_head), dtype=torch.float32, device="cuda")
-        fn = lambda: K.kvattn_decode(q, kq, vq, kd, vd, 1, N, None, 0, lens, 1, N, w.n_head, Hk, D, w.split,
-                                     1 / math.sqrt(D), out, lse, ws, ws.numel(), stream)
+        fn = lambda: K.kvattn_decode(q, kq, vq, kd, vd, 2 if q4 else 1, N, None, 0, lens, 1, N, w.n_head, Hk, D,
+                                     w.split, 1 / math.sqrt(D), out, lse, ws, ws.numel(), stream)
         fn()
-        add(w.name, N * Hk * (D + D // 16) * 2, timed(fn))
+        # K: D int8 + D/32 f16 scales per (cell, head); V: the same, or D/2 bytes + scales
+        kv_bytes = N * Hk * ((D + D // 16) + ((D // 2 if q4 else D) + D // 16))
+        add(w.name, kv_bytes, timed(fn))
         del kq, vq, kd, vd
 
     # window + pinned-host tail
@@ -713,14 +729,11 @@ def profile_workload(args):
     import torch
     from kv_cache_decode_02_gb300 import inputs
     from kv_cache_decode_02_gb300 import kvattn as K
-    w = {"q8_0_n131072_d128": inputs.Q8_LONG_D128, "q8_0_n131072_d256": inputs.Q8_LONG_D256}[args.profile_workload]
+    w = {x.name: x for x in (inputs.Q8_LONG_D128, inputs.Q8_LONG_D256, inputs.Q8Q4_LONG_D128,
+                             inputs.Q8Q4_LONG_D256)}[args.profile_workload]
     N, H, Hk, D = w.n_cells, w.n_head, w.n_head_kv, w.head_dim
-    g = torch.Generator(device="cuda")
-    g.manual_seed(2000 + w.number)
-    kq = torch.randint(-127, 128, (N, Hk, D), dtype=torch.int8, device="cuda", generator=g)
-    vq = torch.randint(-127, 128, (N, Hk, D), dtype=torch.int8, device="cuda", generator=g)
-    kd = (torch.rand((N, Hk, D // 32), device="cuda", generator=g) * 0.019 + 0.001).half()
-    vd = (torch.rand((N, Hk, D // 32), device="cuda", generator=g) * 0.019 + 0.001).half()
+    kq, vq, kd, vd = quantized_kv_torch(torch, w)
+    kv_type = K.KVATTN_KV_Q8_0_Q4_0 if w.kv_type == "q8_0_q4_0" else K.KVATTN_KV_Q8_0
     q = torch.from_numpy(inputs.make_q(w)).cuda()
     lens = torch.tensor([N], dtype=torch.int32, device="cuda")
     n_split = -(-N // w.split)
@@ -728,7 +741,7 @@ def profile_workload(args):
     part_lse = torch.empty((1, n_split, H), dtype=torch.float32, device="cuda")
     ws = K.decode_workspace(1, H, D, N, w.split)
     for _ in range(args.kernel_reps):
-        K.kvattn_decode_partials(q, kq, vq, kd, vd, K.KVATTN_KV_Q8_0, N, None, 0, lens, 1, N, H, Hk, D, w.split,
+        K.kvattn_decode_partials(q, kq, vq, kd, vd, kv_type, N, None, 0, lens, 1, N, H, Hk, D, w.split,
                                  1 / math.sqrt(D), part_o, part_lse, ws, ws.numel())
     torch.cuda.synchronize()
     print(f"{args.profile_workload}: {args.kernel_reps} launches done")
@@ -749,7 +762,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-parity", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=12.0)
-    ap.add_argument("--profile-workload", choices=["q8_0_n131072_d128", "q8_0_n131072_d256"],
+    ap.add_argument("--profile-workload", choices=["q8_0_n131072_d128", "q8_0_n131072_d256", "q8_0_q4_0_n131072_d128",
+                                                   "q8_0_q4_0_n131072_d256"],
                     help="only launch this workload's split decode --kernel-reps times (for ncu)")
     args = ap.parse_args()
     if args.profile_workload:

@@ -47,11 +47,11 @@ int sm_count() {
 // multi-query kernel).
 int occupancy(int kv_type, int head_dim, int n_stages, bool mq = false) {
     static std::mutex mu;
-    static int cache[kMaxDevices][2][2][2][16];
-    static bool have[kMaxDevices][2][2][2][16];
+    static int cache[kMaxDevices][3][2][2][16];
+    static bool have[kMaxDevices][3][2][2][16];
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return 1;
-    const int d = dev % kMaxDevices, t = kv_type ? 1 : 0, h = head_dim == 256 ? 1 : 0, m = mq ? 1 : 0;
+    const int d = dev % kMaxDevices, t = kv_type, h = head_dim == 256 ? 1 : 0, m = mq ? 1 : 0;
     std::lock_guard<std::mutex> lock(mu);
     if (!have[d][t][h][m][n_stages]) {
         int blocks = 0;
@@ -91,7 +91,7 @@ constexpr int64_t kMinAutoSplit = 64;
 constexpr int64_t kMaxAutoSplit = int64_t(1) << 30;
 
 int64_t auto_split_slots(int kv_type, int head_dim) {
-    const int st = kv_type == KVATTN_KV_F16 ? 3 : 2;  // the one-wave f16 ring; Q8_0 geometry is fixed
+    const int st = kv_type == KVATTN_KV_F16 ? 3 : 2;  // the one-wave f16 ring; quantised geometry is fixed
     return (int64_t)std::max(occupancy(kv_type, head_dim, st), 1) * sm_count();
 }
 
@@ -138,9 +138,13 @@ bool use_tma_env() {
 void set_kv_maps(SplitDecodeParams& p, int kv_type, int64_t cells, int n_head_kv, int head_dim) {
     p.use_tma = 0;
     if (!use_tma_env()) return;
-    if (encode_kv_tensor_map(&p.tmap_k, p.k, kv_type, cells, n_head_kv, head_dim) &&
-        encode_kv_tensor_map(&p.tmap_v, p.v, kv_type, cells, n_head_kv, head_dim))
+    if (encode_kv_tensor_map(&p.tmap_k, p.k, kv_type, cells, n_head_kv, head_dim, false) &&
+        encode_kv_tensor_map(&p.tmap_v, p.v, kv_type, cells, n_head_kv, head_dim, true))
         p.use_tma = 1;
+}
+
+bool valid_kv_type(int kv_type) {
+    return kv_type == KVATTN_KV_F16 || kv_type == KVATTN_KV_Q8_0 || kv_type == KVATTN_KV_Q8_0_Q4_0;
 }
 
 // Failure-detection test hook (host-side switch, read on every call): with
@@ -181,19 +185,24 @@ int check_shape(const DecodeShape& s) {
 }  // namespace
 
 bool kvattn::encode_kv_tensor_map(CUtensorMap* map, const void* base, int kv_type, int64_t cells,
-                                  int n_head_kv, int head_dim) {
+                                  int n_head_kv, int head_dim, bool v_side) {
     EncodeTiledFn enc = tensor_map_encoder();
     if (enc == nullptr || base == nullptr || cells < 1 || !aligned(base, 16)) return false;
     const bool f16 = kv_type == KVATTN_KV_F16;
-    const cuuint64_t row_bytes = (cuuint64_t)head_dim * (f16 ? 2 : 1);
-    const cuuint64_t dims[3] = {(cuuint64_t)head_dim, (cuuint64_t)n_head_kv, (cuuint64_t)cells};
+    const bool q4 = v_side && kv_type == KVATTN_KV_Q8_0_Q4_0;  // two 4-bit values per byte
+    const cuuint64_t row_elems = q4 ? (cuuint64_t)head_dim / 2 : (cuuint64_t)head_dim;
+    const cuuint64_t row_bytes = row_elems * (f16 ? 2 : 1);
+    const cuuint64_t dims[3] = {row_elems, (cuuint64_t)n_head_kv, (cuuint64_t)cells};
     const cuuint64_t strides[2] = {row_bytes, row_bytes * (cuuint64_t)n_head_kv};
-    const cuuint32_t box[3] = {f16 ? 64u : 128u, 1u, (cuuint32_t)split_decode_box_cells(kv_type)};
+    // box: 128 bytes of a row (64 or 128 bytes for a whole 4-bit row), one head, the kernel's
+    // cells; the swizzle spans the box's width (64-byte rows take the 64-byte swizzle)
+    const cuuint32_t inner = f16 ? 64u : (q4 ? (cuuint32_t)row_elems : 128u);
+    const cuuint32_t box[3] = {inner, 1u, (cuuint32_t)split_decode_box_cells(kv_type)};
     const cuuint32_t estr[3] = {1, 1, 1};
     const CUresult r = enc(map, f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8, 3,
                            const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                           CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+                           inner == 64u && !f16 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B,
+                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
 }
 
@@ -308,7 +317,7 @@ int kvattn_select_split_for(int n_seq, int64_t max_len, int n_head_kv, int64_t r
 }
 
 int kvattn_select_split(int kv_type, int n_seq, int64_t max_len, int n_head_kv, int head_dim) {
-    if (kv_type != KVATTN_KV_F16 && kv_type != KVATTN_KV_Q8_0) return KVATTN_ERR_INVALID_ARG;
+    if (!valid_kv_type(kv_type)) return KVATTN_ERR_INVALID_ARG;
     if (head_dim != 128 && head_dim != 256) return KVATTN_ERR_UNSUPPORTED;
     return kvattn_select_split_for(n_seq, max_len, n_head_kv, auto_split_slots(kv_type, head_dim));
 }
@@ -330,7 +339,7 @@ int decode_impl(const void* q, const void* k_cache, const void* v_cache, const v
     if (!multi) n_q = 1;
     const bool merge = part_o_user == nullptr;
     if (split == 0 && merge) {  // kvattn_decode picks the split (partials need it fixed)
-        if (kv_type != KVATTN_KV_F16 && kv_type != KVATTN_KV_Q8_0) return KVATTN_ERR_INVALID_ARG;
+        if (!valid_kv_type(kv_type)) return KVATTN_ERR_INVALID_ARG;
         if (head_dim != 128 && head_dim != 256) return KVATTN_ERR_UNSUPPORTED;
         if (n_head_kv < 1 || n_seq < 0 || max_len < 0) return KVATTN_ERR_INVALID_ARG;
         split = kvattn_select_split(kv_type, n_seq, max_len, n_head_kv, head_dim);
@@ -346,8 +355,8 @@ int decode_impl(const void* q, const void* k_cache, const void* v_cache, const v
     if (merge && (out == nullptr || lse == nullptr)) return KVATTN_ERR_INVALID_ARG;
     if (!merge && (part_lse_user == nullptr || !aligned(part_o_user, 16) || !aligned(part_lse_user, 4)))
         return KVATTN_ERR_INVALID_ARG;
-    if (kv_type != KVATTN_KV_F16 && kv_type != KVATTN_KV_Q8_0) return KVATTN_ERR_INVALID_ARG;
-    if (kv_type == KVATTN_KV_Q8_0 && (k_scales == nullptr || v_scales == nullptr))
+    if (!valid_kv_type(kv_type)) return KVATTN_ERR_INVALID_ARG;
+    if (kv_type != KVATTN_KV_F16 && (k_scales == nullptr || v_scales == nullptr))
         return KVATTN_ERR_INVALID_ARG;
     if (kv_type == KVATTN_KV_F16 && (k_scales != nullptr || v_scales != nullptr))
         return KVATTN_ERR_INVALID_ARG;
@@ -357,7 +366,7 @@ int decode_impl(const void* q, const void* k_cache, const void* v_cache, const v
         (merge && (!aligned(out, 16) || !aligned(lse, 4))) || !aligned(ws, kWsAlign) ||
         (cell_plan && !aligned(cell_plan, 4)) || !aligned(seq_lens, 4))
         return KVATTN_ERR_INVALID_ARG;
-    if (kv_type == KVATTN_KV_Q8_0) {
+    if (kv_type != KVATTN_KV_F16) {
         const size_t sa = head_dim == 128 ? 8 : 16;
         if (!aligned(k_scales, sa) || !aligned(v_scales, sa)) return KVATTN_ERR_INVALID_ARG;
     }

@@ -1183,6 +1183,165 @@ __device__ __forceinline__ void q8_chunk_swz(uint32_t kb, uint32_t vb, const uns
     }
 }
 
+__device__ __forceinline__ uint32_t lds16(uint32_t addr) {
+    unsigned short v;
+    asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(addr));
+    return v;
+}
+
+// Q4_0 values -> exact f16 pairs.  w holds, for two cells, one byte each in bits 0-7 and
+// 16-23 (a byte: element e in its low nibble, element e + 16 in its high nibble).  With the
+// f16 bit pattern 0x6400 (1024) OR-ed in, a low nibble n reads as 1024 + n and a high
+// nibble as 1024 + 16 n; subtracting 1032, or scaling by 1/16 and subtracting 72, leaves
+// n - 8 exactly (the same magic-number idea as the int8 conversion).
+__device__ __forceinline__ uint32_t q4x2_lo(uint32_t w) {
+    uint32_t t, r;
+    asm("lop3.b32 %0, %1, 0x000f000f, 0x64006400, 0xea;" : "=r"(t) : "r"(w));  // (w & m) | c
+    asm("sub.f16x2 %0, %1, %2;" : "=r"(r) : "r"(t), "r"(0x64086408u));
+    return r;
+}
+__device__ __forceinline__ uint32_t q4x2_hi(uint32_t w) {
+    uint32_t t, r;
+    asm("lop3.b32 %0, %1, 0x00f000f0, 0x64006400, 0xea;" : "=r"(t) : "r"(w));
+    asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(r) : "r"(t), "r"(0x2c002c00u), "r"(0xd480d480u));  // x/16 - 72
+    return r;
+}
+
+// One warp's 16-cell chunk of Q8_0 keys and Q4_0 values: scores, online softmax, P V.
+// SWZ: the chunk came by TMA boxes (K in 128-byte-wide planes under the 128-byte swizzle as
+// for Q8_0, V in one box of D/2-byte rows under the swizzle of that width); otherwise by one
+// copy per row into plain rows.
+// V operand (O^T += V^T P'^T, head_dim in M): a lane reads the 16-bit word at bytes
+// 2gq, 2gq+1 of block b for cells 2tq, 2tq+1, 2tq+8, 2tq+9 -- elements 2gq, 2gq+1 in the low
+// nibbles and 2gq+16, 2gq+17 in the high ones -- so m-tile 2b holds dims 32b + 2gq (row gq)
+// and 32b + 2gq + 1 (row gq + 8), and m-tile 2b+1 the same plus 16.  Every dim of an m-tile
+// lies in block b, whose V scale multiplies P as in the Q8_0 path.
+template <int D, bool SWZ>
+__device__ __forceinline__ void q8q4_chunk(uint32_t kb, uint32_t vb, const unsigned char* ks,
+                                           const unsigned char* vs, uint32_t mask, int lane,
+                                           const uint32_t (&qa)[D / 16][2], float (&oacc)[D / 16][4],
+                                           float& m_run, float& l_run, float scale_log2) {
+    constexpr int kPlane = kChunkCells * 128;
+    constexpr int kScl = D / 16;  // bytes of scales per cell
+    constexpr int kVRow = D / 2;  // bytes of a 4-bit V row
+    const int gq = lane >> 2;
+    const int tq = lane & 3;
+    // K rows gq and 8 + gq: swizzled planes (see q8_chunk_swz) or plain D-byte rows
+    const uint32_t ka = SWZ ? ((kb + 128u * gq + 4u * tq) | (16u * gq)) : (kb + (uint32_t)D * gq + 4u * tq);
+    // V: base addresses whose XOR with 16b (plus immediates) give cells 2tq, 2tq+1, 2tq+8, 2tq+9
+    // of block b.  head_dim 256 (128-byte rows, 128-byte swizzle): the 16-byte column of
+    // (row c, byte x) is (x >> 4) ^ (c & 7).  head_dim 128 (64-byte rows, 64-byte swizzle):
+    // the column of byte offset a = 64c + x is (a >> 4 & 3) ^ (a >> 7 & 3) = (x >> 4) ^ (c >> 1 & 3).
+    uint32_t va0, va1;
+    if (SWZ) {
+        if (D == 128) {  // cells 2tq, 2tq+1 (and 2tq+8, 2tq+9) share the key tq
+            va0 = (vb + 128u * tq + 2u * gq) | (16u * tq);
+            va1 = va0 + 64u;
+        } else {  // 128-byte rows: line c, key c & 7
+            va0 = (vb + 256u * tq + 2u * gq) | (32u * tq);
+            va1 = (vb + 256u * tq + 128u + 2u * gq) | (16u * (2 * tq + 1));
+        }
+    } else {
+        va0 = vb + (uint32_t)kVRow * (2 * tq) + 2u * gq;
+        va1 = va0 + kVRow;
+    }
+    const uint32_t kss = smem_addr(ks) + 2u * kScl * tq;
+    const uint32_t vss = smem_addr(vs) + 2u * kScl * tq;
+
+    float sacc[2][4];
+#pragma unroll
+    for (int j = 0; j < 2; ++j) sacc[j][0] = sacc[j][1] = sacc[j][2] = sacc[j][3] = 0.f;
+    uint32_t ksw[2][2][D / 64];
+#pragma unroll
+    for (int j = 0; j < 2; ++j)
+#pragma unroll
+        for (int e = 0; e < 2; ++e)
+#pragma unroll
+            for (int h = 0; h < D / 128; ++h) {
+                const uint2 w = lds64(kss + (8 * j + e) * kScl + 8 * h);
+                ksw[j][e][2 * h] = w.x;
+                ksw[j][e][2 * h + 1] = w.y;
+            }
+#pragma unroll
+    for (int b = 0; b < D / 32; ++b) {
+        uint32_t a0, a1, rs;
+        if (SWZ) {
+            const uint32_t pl = kPlane * (b >> 2);
+            a0 = (ka ^ (32u * (b & 3))) + pl;
+            a1 = (ka ^ (32u * (b & 3) + 16u)) + pl;
+            rs = 1024u;  // rows 8..15 of the plane
+        } else {
+            a0 = ka + 32u * b;
+            a1 = a0 + 16u;
+            rs = 8u * D;
+        }
+        uint32_t kw[2][2];
+        float ksc[2][2];
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+            kw[j][0] = lds32(a0 + rs * j);
+            kw[j][1] = lds32(a1 + rs * j);
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                const uint32_t w = ksw[j][e][b >> 1];
+                ksc[j][e] = __half2float(__ushort_as_half((unsigned short)((b & 1) ? (w >> 16) : (w & 0xffffu))));
+            }
+        }
+        q8_qk_block(sacc, qa[2 * b], qa[2 * b + 1], kw, ksc);
+    }
+
+    float alpha, pf[2][2];
+    if (softmax_step(sacc, mask, tq, scale_log2, m_run, alpha, pf)) {
+        rescale_o<D>(oacc, alpha, tq);
+        l_run *= alpha;
+    }
+    l_run += (pf[0][0] + pf[0][1]) + (pf[1][0] + pf[1][1]);
+    const uint32_t ph0 = pack_half2(pf[0][0], pf[0][1]);
+    const uint32_t ph1 = pack_half2(pf[1][0], pf[1][1]);
+    uint32_t vsw[4][D / 64];
+#pragma unroll
+    for (int c = 0; c < 4; ++c)
+#pragma unroll
+        for (int h = 0; h < D / 128; ++h) {
+            const uint2 w = lds64(vss + ((c & 1) + 8 * (c >> 1)) * kScl + 8 * h);
+            vsw[c][2 * h] = w.x;
+            vsw[c][2 * h + 1] = w.y;
+        }
+#pragma unroll
+    for (int b = 0; b < D / 32; ++b) {
+        uint32_t c0, c1, c8, c9;  // 16-bit words of cells 2tq, 2tq+1, 2tq+8, 2tq+9
+        if (SWZ) {
+            if (D == 128) {
+                const uint32_t x = va0 ^ (16u * b);
+                c0 = lds16(x);
+                c1 = lds16(x + 64u);
+                c8 = lds16(x + 512u);
+                c9 = lds16(x + 576u);
+            } else {
+                const uint32_t x0 = va0 ^ (16u * b), x1 = va1 ^ (16u * b);
+                c0 = lds16(x0);
+                c1 = lds16(x1);
+                c8 = lds16(x0 + 1024u);
+                c9 = lds16(x1 + 1024u);
+            }
+        } else {
+            const uint32_t x = va0 + 16u * b;
+            c0 = lds16(x);
+            c1 = lds16(x + kVRow);
+            c8 = lds16(x + 8u * kVRow);
+            c9 = lds16(x + 9u * kVRow);
+        }
+        // byte 0 of both cells of a pair in bits 0-7 / 16-23 (w), byte 1 likewise (x)
+        const uint32_t w01 = prmt_b32(c0, c1, 0x5410u), x01 = prmt_b32(c0, c1, 0x5511u);
+        const uint32_t w89 = prmt_b32(c8, c9, 0x5410u), x89 = prmt_b32(c8, c9, 0x5511u);
+        const uint32_t sel = (b & 1) ? 0x7632u : 0x5410u;
+        const uint32_t pb0 = hmul2_u32(ph0, prmt_b32(vsw[0][b >> 1], vsw[1][b >> 1], sel));
+        const uint32_t pb1 = hmul2_u32(ph1, prmt_b32(vsw[2][b >> 1], vsw[3][b >> 1], sel));
+        mma_16816(oacc[2 * b], q4x2_lo(w01), q4x2_lo(x01), q4x2_lo(w89), q4x2_lo(x89), pb0, pb1);
+        mma_16816(oacc[2 * b + 1], q4x2_hi(w01), q4x2_hi(x01), q4x2_hi(w89), q4x2_hi(x89), pb0, pb1);
+    }
+}
+
 // ---------------------------------------------------------------------------------------
 // Q8_0: self-loading warps.  The Q8_0 kernels are bound by their consumer warps (every K
 // and V byte costs an int8 -> f16 conversion), so they drop the producer warp: each of the
@@ -1192,22 +1351,25 @@ __device__ __forceinline__ void q8_chunk_swz(uint32_t kb, uint32_t vb, const uns
 // (chunk j goes to warp j mod W) and meet in the same end-of-unit exchange as above.  With
 // no producer warp, all the registers of an SM go to warps that compute.
 // ---------------------------------------------------------------------------------------
-template <int D>
+template <int D, bool VQ4 = false>
 struct Q8Self {
-    static constexpr int kRowBytes = D;                            // int8 row per (cell, KV head)
+    static constexpr int kRowBytes = D;                            // int8 K row per (cell, KV head)
+    static constexpr int kVRowBytes = VQ4 ? D / 2 : D;             // V row: int8, or two 4-bit values a byte
     static constexpr int kPlanes = D / 128;
     static constexpr int kPlane = kChunkCells * 128;               // one 128-byte-wide plane
-    static constexpr int kSection = kPlanes * kPlane;              // K (or V) rows of a chunk
-    static constexpr int kChunkBytes = 2 * kSection;               // a multiple of 1024
+    static constexpr int kSection = kPlanes * kPlane;              // K rows of a chunk (V rows follow)
+    static constexpr int kVSection = kChunkCells * kVRowBytes;     // V rows of a chunk
+    static constexpr int kChunkBytes = kSection + kVSection;       // a multiple of 1024
     static constexpr int kSclBytes = D / 16;                       // D/32 half scales per row
     static constexpr int kSclChunk = 2 * kChunkCells * kSclBytes;  // K then V scales
     static constexpr int kXchgSlot = ((D / 16) * 32 * 16 + 64 + 1023) / 1024 * 1024;
     static_assert(kChunkBytes % 1024 == 0, "stages must keep the 1024-byte swizzle alignment");
 };
 
-template <int D, int W, int S>
+template <int D, int W, int S, bool VQ4 = false>
 constexpr int q8_self_smem() {
-    return kHeaderBytes + 1024 + (W - 1) * Q8Self<D>::kXchgSlot + W * S * (Q8Self<D>::kChunkBytes + Q8Self<D>::kSclChunk);
+    using Q = Q8Self<D, VQ4>;
+    return kHeaderBytes + 1024 + (W - 1) * Q::kXchgSlot + W * S * (Q::kChunkBytes + Q::kSclChunk);
 }
 
 // Position of a warp's load stream: unit u (its fields) and chunk j of it.
@@ -1237,10 +1399,10 @@ __device__ __forceinline__ void cursor_seek(const SplitDecodeParams& p, ChunkCur
     }
 }
 
-template <int D, int W, int S>
+template <int D, int W, int S, bool VQ4 = false>
 __device__ __forceinline__ void q8_self_body(const SplitDecodeParams& p) {
-    constexpr int KVT = KVATTN_KV_Q8_0;
-    using Q = Q8Self<D>;
+    constexpr int KVT = KVATTN_KV_Q8_0;  // the keys (and the query fragment order)
+    using Q = Q8Self<D, VQ4>;
     using G = Geom<KVT, D>;
     static_assert(G::kSclBytes == Q::kSclBytes, "scale rows");
     extern __shared__ __align__(1024) unsigned char smem_raw[];
@@ -1294,7 +1456,8 @@ __device__ __forceinline__ void q8_self_body(const SplitDecodeParams& p) {
         if (lane == 0) {
             st_mask[warp * S + st] = mask;
             st_swz[warp * S + st] = use_tma ? 1u : 0u;
-            const uint32_t bytes = use_tma ? (uint32_t)Q::kChunkBytes : (uint32_t)__popc(mask) * 2u * (uint32_t)Q::kRowBytes;
+            const uint32_t bytes =
+                use_tma ? (uint32_t)Q::kChunkBytes : (uint32_t)__popc(mask) * (uint32_t)(Q::kRowBytes + Q::kVRowBytes);
             mbar_expect_tx(bar, bytes + extra_tx);
         }
         __syncwarp();
@@ -1305,14 +1468,16 @@ __device__ __forceinline__ void q8_self_body(const SplitDecodeParams& p) {
 #pragma unroll
                 for (int pl = 0; pl < Q::kPlanes; ++pl) {
                     tma_load_3d(kdst + pl * Q::kPlane, &p.tmap_k, pl * 128, c.g, (int)base, bar);
-                    tma_load_3d(kdst + Q::kSection + pl * Q::kPlane, &p.tmap_v, pl * 128, c.g, (int)base, bar);
+                    if (!VQ4) tma_load_3d(kdst + Q::kSection + pl * Q::kPlane, &p.tmap_v, pl * 128, c.g, (int)base, bar);
                 }
+                // 4-bit V: one box of the chunk's D/2-byte rows (64 or 128 bytes wide)
+                if (VQ4) tma_load_3d(kdst + Q::kSection, &p.tmap_v, 0, c.g, (int)base, bar);
             }
         } else if (valid) {
             bulk_g2s(smem_addr(stage + lane * Q::kRowBytes), static_cast<const char*>(p.k) + row * Q::kRowBytes,
                      Q::kRowBytes, bar);
-            bulk_g2s(smem_addr(stage + Q::kSection + lane * Q::kRowBytes),
-                     static_cast<const char*>(p.v) + row * Q::kRowBytes, Q::kRowBytes, bar);
+            bulk_g2s(smem_addr(stage + Q::kSection + lane * Q::kVRowBytes),
+                     static_cast<const char*>(p.v) + row * Q::kVRowBytes, Q::kVRowBytes, bar);
         }
         if (lane < kChunkCells) {
             unsigned char* ksd = sring + st * Q::kSclChunk + lane * Q::kSclBytes;
@@ -1377,7 +1542,8 @@ __device__ __forceinline__ void q8_self_body(const SplitDecodeParams& p) {
         if (lane == 0) {
             st_mask[warp * S + st] = mask;
             st_swz[warp * S + st] = use_tma ? 1u : 0u;
-            const uint32_t bytes = use_tma ? (uint32_t)Q::kChunkBytes : (uint32_t)__popc(mask) * 2u * (uint32_t)Q::kRowBytes;
+            const uint32_t bytes =
+                use_tma ? (uint32_t)Q::kChunkBytes : (uint32_t)__popc(mask) * (uint32_t)(Q::kRowBytes + Q::kVRowBytes);
             mbar_expect_tx(bar, bytes + extra_tx);
         }
         __syncwarp();
@@ -1388,15 +1554,17 @@ __device__ __forceinline__ void q8_self_body(const SplitDecodeParams& p) {
 #pragma unroll
                 for (int pl = 0; pl < Q::kPlanes; ++pl) {
                     tma_load_3d(kdst + pl * Q::kPlane, &p.tmap_k, pl * 128, c.g, (int)base, bar);
-                    tma_load_3d(kdst + Q::kSection + pl * Q::kPlane, &p.tmap_v, pl * 128, c.g, (int)base, bar);
+                    if (!VQ4) tma_load_3d(kdst + Q::kSection + pl * Q::kPlane, &p.tmap_v, pl * 128, c.g, (int)base, bar);
                 }
+                // 4-bit V: one box of the chunk's D/2-byte rows (64 or 128 bytes wide)
+                if (VQ4) tma_load_3d(kdst + Q::kSection, &p.tmap_v, 0, c.g, (int)base, bar);
             }
         } else if (valid) {
             const int64_t row = cell * Hk + c.g;
             bulk_g2s(smem_addr(stage + lane * Q::kRowBytes), static_cast<const char*>(p.k) + row * Q::kRowBytes,
                      Q::kRowBytes, bar);
-            bulk_g2s(smem_addr(stage + Q::kSection + lane * Q::kRowBytes),
-                     static_cast<const char*>(p.v) + row * Q::kRowBytes, Q::kRowBytes, bar);
+            bulk_g2s(smem_addr(stage + Q::kSection + lane * Q::kVRowBytes),
+                     static_cast<const char*>(p.v) + row * Q::kVRowBytes, Q::kVRowBytes, bar);
         }
         // scales: a masked cell's are zero, so its (finite) int8 row contributes nothing
         if (lane < kChunkCells) {
@@ -1486,11 +1654,18 @@ __device__ __forceinline__ void q8_self_body(const SplitDecodeParams& p) {
             // (fragments are read straight from the stage: staging them in registers first
             // measured slower here, the extra registers spill at this CTA count)
             if (mask != 0u) {
-                if (swz)
-                    q8_chunk_swz<D>(kb, vb, ks, vs, mask, lane, qa, oacc, m_run, l_run, p.scale_log2);
-                else
-                    consume_tile<KVT, D, false, Q::kPlane>(kb, vb, ks, vs, mask, 0, lane, qa, oacc, m_run, l_run,
-                                                           p.scale_log2);
+                if constexpr (VQ4) {
+                    if (swz)
+                        q8q4_chunk<D, true>(kb, vb, ks, vs, mask, lane, qa, oacc, m_run, l_run, p.scale_log2);
+                    else
+                        q8q4_chunk<D, false>(kb, vb, ks, vs, mask, lane, qa, oacc, m_run, l_run, p.scale_log2);
+                } else {
+                    if (swz)
+                        q8_chunk_swz<D>(kb, vb, ks, vs, mask, lane, qa, oacc, m_run, l_run, p.scale_log2);
+                    else
+                        consume_tile<KVT, D, false, Q::kPlane>(kb, vb, ks, vs, mask, 0, lane, qa, oacc, m_run,
+                                                               l_run, p.scale_log2);
+                }
             }
             // refill the stage just read with the chunk S ahead (every lane's reads are done)
             __syncwarp();
@@ -1593,9 +1768,17 @@ __device__ __forceinline__ void q8_self_body(const SplitDecodeParams& p) {
             if (r < p.group) {
                 float* orow = p.part_o + (part * H + x.g * p.group + r) * D;
 #pragma unroll
-                for (int b = 0; b < D / 32; ++b)
-                    *reinterpret_cast<float4*>(orow + 32 * b + 4 * gq) =
-                        make_float4(oacc[2 * b][e], oacc[2 * b][2 + e], oacc[2 * b + 1][e], oacc[2 * b + 1][2 + e]);
+                for (int b = 0; b < D / 32; ++b) {
+                    if constexpr (VQ4) {
+                        // 4-bit V: m-tile 2b holds dims 32b + 2gq (+1), m-tile 2b+1 dims 32b + 16 + 2gq (+1)
+                        *reinterpret_cast<float2*>(orow + 32 * b + 2 * gq) = make_float2(oacc[2 * b][e], oacc[2 * b][2 + e]);
+                        *reinterpret_cast<float2*>(orow + 32 * b + 16 + 2 * gq) =
+                            make_float2(oacc[2 * b + 1][e], oacc[2 * b + 1][2 + e]);
+                    } else {
+                        *reinterpret_cast<float4*>(orow + 32 * b + 4 * gq) =
+                            make_float4(oacc[2 * b][e], oacc[2 * b][2 + e], oacc[2 * b + 1][e], oacc[2 * b + 1][2 + e]);
+                    }
+                }
                 if (gq == 0) p.part_lse[part * H + x.g * p.group + r] = lse[e];
             }
         }
@@ -1638,12 +1821,24 @@ __global__ void __launch_bounds__(kQ8W256 * 32, kQ8B256)
     split_decode_q8_d256(const __grid_constant__ SplitDecodeParams p) {
     q8_self_body<256, kQ8W256, kQ8S256>(p);
 }
+// Q8_0 keys, Q4_0 values: the Q8_0 kernels with the second dequantisation on the V side.
+__global__ void __launch_bounds__(kQ8W128 * 32, kQ8B128)
+    split_decode_q8q4_d128(const __grid_constant__ SplitDecodeParams p) {
+    q8_self_body<128, kQ8W128, kQ8S128, true>(p);
+}
+__global__ void __launch_bounds__(kQ8W256 * 32, kQ8B256)
+    split_decode_q8q4_d256(const __grid_constant__ SplitDecodeParams p) {
+    q8_self_body<256, kQ8W256, kQ8S256, true>(p);
+}
 
 const void* kernel_for(int kv_type, int head_dim, bool mq = false) {
     if (mq) return reinterpret_cast<const void*>(split_decode_mq_f16_d128);
     if (kv_type == KVATTN_KV_F16)
         return head_dim == 128 ? reinterpret_cast<const void*>(split_decode_f16_d128)
                                : reinterpret_cast<const void*>(split_decode_f16_d256);
+    if (kv_type == KVATTN_KV_Q8_0_Q4_0)
+        return head_dim == 128 ? reinterpret_cast<const void*>(split_decode_q8q4_d128)
+                               : reinterpret_cast<const void*>(split_decode_q8q4_d256);
     return head_dim == 128 ? reinterpret_cast<const void*>(split_decode_q8_d128)
                            : reinterpret_cast<const void*>(split_decode_q8_d256);
 }
@@ -1667,6 +1862,9 @@ int split_decode_stage_bytes(int kv_type, int head_dim) {
 int split_decode_smem_bytes(int kv_type, int head_dim, int n_stages, bool mq) {
     if (kv_type == KVATTN_KV_Q8_0)
         return head_dim == 128 ? q8_self_smem<128, kQ8W128, kQ8S128>() : q8_self_smem<256, kQ8W256, kQ8S256>();
+    if (kv_type == KVATTN_KV_Q8_0_Q4_0)
+        return head_dim == 128 ? q8_self_smem<128, kQ8W128, kQ8S128, true>()
+                               : q8_self_smem<256, kQ8W256, kQ8S256, true>();
     const int xchg = mq                ? Geom<0, 128>::kXchgBytesMQ
                      : head_dim == 128 ? Geom<0, 128>::kXchgBytes
                                        : Geom<0, 256>::kXchgBytes;
@@ -1674,12 +1872,12 @@ int split_decode_smem_bytes(int kv_type, int head_dim, int n_stages, bool mq) {
 }
 
 int split_decode_block_threads(int kv_type, int head_dim) {
-    if (kv_type == KVATTN_KV_Q8_0) return (head_dim == 128 ? kQ8W128 : kQ8W256) * 32;
+    if (kv_type != KVATTN_KV_F16) return (head_dim == 128 ? kQ8W128 : kQ8W256) * 32;
     return kThreads;
 }
 
 // Cells per TMA box of the kernel's tensor maps.
-int split_decode_box_cells(int kv_type) { return kv_type == KVATTN_KV_Q8_0 ? kChunkCells : kTileCells; }
+int split_decode_box_cells(int kv_type) { return kv_type == KVATTN_KV_F16 ? kTileCells : kChunkCells; }
 int split_decode_max_stages() { return kMaxStages; }
 int split_decode_threads() { return kThreads; }
 
@@ -1695,12 +1893,12 @@ cudaError_t launch_split_decode(const SplitDecodeParams& p, int kv_type, int hea
                                 cudaStream_t stream, bool pdl) {
     const bool mq = p.mq != 0;
     const void* fn = kernel_for(kv_type, head_dim, mq);
-    static std::once_flag once[64][5];
-    static cudaError_t attr_err[64][5];
+    static std::once_flag once[64][7];
+    static cudaError_t attr_err[64][7];
     int dev = 0;
     cudaError_t err = cudaGetDevice(&dev);
     if (err != cudaSuccess) return err;
-    const int which = mq ? 4 : (kv_type ? 2 : 0) + (head_dim == 256 ? 1 : 0);
+    const int which = mq ? 6 : 2 * kv_type + (head_dim == 256 ? 1 : 0);
     std::call_once(once[dev & 63][which], [&] { attr_err[dev & 63][which] = set_smem_attr(fn); });
     if (attr_err[dev & 63][which] != cudaSuccess) return attr_err[dev & 63][which];
     cudaLaunchConfig_t cfg = {};

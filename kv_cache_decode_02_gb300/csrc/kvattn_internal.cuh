@@ -78,10 +78,11 @@ struct SplitDecodeParams {
 };
 
 // Fill a 3-D tensor map {row elements, n_head_kv, cells} over a cell-major cache with
-// 32-cell x 128-byte boxes and the 128-byte swizzle.  Returns false if the driver's
-// encoder is unavailable or rejects the geometry (the caller then loads per cell).
+// boxes of the kernel's cells x 128 bytes (a whole 64- or 128-byte row for 4-bit V rows,
+// v_side with KVATTN_KV_Q8_0_Q4_0) and the 128-byte swizzle.  Returns false if the
+// driver's encoder is unavailable or rejects the geometry (the caller then loads per cell).
 bool encode_kv_tensor_map(CUtensorMap* map, const void* base, int kv_type, int64_t cells,
-                          int n_head_kv, int head_dim);
+                          int n_head_kv, int head_dim, bool v_side);
 
 struct MergeParams {
     const float* part_o;      // parts: o[(base + p) * row_stride_parts ...]

@@ -43,7 +43,7 @@ class Workload:
     n_head_kv: int
     head_dim: int
     split: int
-    kv_type: str = "f16"     # "f16" or "q8_0"
+    kv_type: str = "f16"     # "f16", "q8_0" or "q8_0_q4_0"
     seq_lens: tuple = ()
     hole_prob: float = 0.0
     pool_records: int = 0
@@ -81,9 +81,16 @@ STACK_TAIL_1815MIB = Workload("qwen3_8b_x36_tail_1815mib", 7, 1, 256 + 12900, 32
                               seq_lens=(256 + 12900,), n_window=256, tile_cells=12928, tail_split=128,
                               layers=36)
 
+# The mixed cache of the pages' resident-compression anchors: Q8_0 keys, Q4_0 values, at the
+# Q8_0 long-context shape.
+Q8Q4_LONG_D128 = Workload("q8_0_q4_0_n131072_d128", 8, 1, 131072, 32, 8, 128, 512, kv_type="q8_0_q4_0",
+                          seq_lens=(131072,))
+Q8Q4_LONG_D256 = Workload("q8_0_q4_0_n131072_d256", 8, 1, 131072, 32, 8, 256, 512, kv_type="q8_0_q4_0",
+                          seq_lens=(131072,))
+
 WORKLOADS = {w.name: w for w in
              (TINY, QWEN3_8B_LAYER, MULTISLOT_PLAN, Q8_LONG_D128, Q8_LONG_D256, WINDOW_TAIL,
-              STACK_TAIL_295MIB, STACK_TAIL_1815MIB)}
+              STACK_TAIL_295MIB, STACK_TAIL_1815MIB, Q8Q4_LONG_D128, Q8Q4_LONG_D256)}
 
 
 def _rng(*seed) -> np.random.Generator:
@@ -145,6 +152,13 @@ def make_kv_f16(w: Workload, layer: int = 0, n_cells: int | None = None, seed_k=
 def make_kv_q8(w: Workload, layer: int = 0):
     k = q8_0_planes(_rng(2000 + w.number, layer, w.head_dim), w.n_cells, w.n_head_kv, w.head_dim)
     v = q8_0_planes(_rng(3000 + w.number, layer, w.head_dim), w.n_cells, w.n_head_kv, w.head_dim)
+    return k, v
+
+
+def make_kv_q8q4(w: Workload, layer: int = 0):
+    """Q8_0 key planes and Q4_0 value planes: ((k_qs, k_d), (v_packed, v_d))."""
+    k = q8_0_planes(_rng(2000 + w.number, layer, w.head_dim), w.n_cells, w.n_head_kv, w.head_dim)
+    v = q4_0_planes(_rng(3000 + w.number, layer, w.head_dim), w.n_cells, w.n_head_kv, w.head_dim)
     return k, v
 
 

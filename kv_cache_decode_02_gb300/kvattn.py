@@ -32,6 +32,7 @@ KVATTN_ERR_CUDA = -5
 KVATTN_ERR_TIMEOUT = -6
 KVATTN_KV_F16 = 0
 KVATTN_KV_Q8_0 = 1
+KVATTN_KV_Q8_0_Q4_0 = 2
 KVATTN_DEVICE_WAIT_TIMEOUT = 1
 KVATTN_DEVICE_BAD_PLAN_ENTRY = 2
 KVATTN_TAIL_PREFETCH = 1
@@ -318,15 +319,21 @@ def decode_workspace(n_seq, n_head, head_dim, max_len, split, device="cuda"):
 
 
 def decode(q, k_cache, v_cache, seq_lens, *, split, max_len=None, cell_plan=None, k_scales=None,
-           v_scales=None, scale=None, n_cells=None, out=None, lse=None, ws=None, stream=None):
+           v_scales=None, scale=None, n_cells=None, out=None, lse=None, ws=None, stream=None, kv_type=None):
     """q: half [S][H][D] (cuda); K/V as the C ABI describes; seq_lens int32 [S] (cuda).
 
-    ``n_cells`` defaults to K's cell dimension (dim 0 for a unified cache or a single
-    sequence, dim 1 for a per-sequence [S][N][Hk][D] cache).  Returns (out, lse).
+    ``kv_type`` defaults to f16 without scales, to Q8_0_Q4_0 when V's rows hold head_dim / 2
+    bytes, and to Q8_0 otherwise.  ``n_cells`` defaults to K's cell dimension (dim 0 for a
+    unified cache or a single sequence, dim 1 for a per-sequence [S][N][Hk][D] cache).
+    Returns (out, lse).
     """
     import torch
     S, H, D = q.shape
-    kv_type = KVATTN_KV_F16 if k_scales is None else KVATTN_KV_Q8_0
+    if kv_type is None:
+        if k_scales is None:
+            kv_type = KVATTN_KV_F16
+        else:
+            kv_type = KVATTN_KV_Q8_0_Q4_0 if v_cache.shape[-1] * 2 == D else KVATTN_KV_Q8_0
     Hk = k_cache.shape[-2]
     if n_cells is None:
         n_cells = k_cache.shape[1] if (k_cache.dim() == 4) else k_cache.shape[0]
