@@ -52,6 +52,21 @@ def dist_env():
         int(os.environ.get("LOCAL_RANK", 0))
 
 
+def max_over_ranks(torch, ms, world, device):
+    """The slowest rank's time (ms): every replica's work counts only once all are done."""
+    if world > 1:
+        t = torch.tensor([float(ms)], dtype=torch.float64, device=device)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms = float(t.item())
+    return ms
+
+
+def whole_job_gbs(bytes_per_rank_step, world, ms_per_step):
+    """Whole-job throughput: the bytes every rank processed per step over the slowest rank's
+    step time."""
+    return bytes_per_rank_step * world / (ms_per_step * 1e-3) / 1e9
+
+
 def measured_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -566,13 +581,9 @@ def run_ours(args):
     if world > 1:
         torch.distributed.barrier()
     clocks = sampler.stop()
-    ms = ev0.elapsed_time(ev1) / args.steps
-    if world > 1:
-        t = torch.tensor([ms], device="cuda")
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(torch, ev0.elapsed_time(ev1) / args.steps, world, "cuda")
     step_bytes = data.bytes_per_op * args.layers
-    value = step_bytes * world / (ms * 1e-3) / 1e9
+    value = whole_job_gbs(step_bytes, world, ms)
 
     # the dominant kernel alone: its average launch duration over back-to-back launches
     # (one per layer buffer, replayed from a CUDA graph so host launch cost cannot gap
