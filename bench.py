@@ -236,15 +236,19 @@ def h2d_bandwidth(torch):
 
 
 def quantized_kv_torch(torch, w):
-    """Device K/V planes of a Q8_0 or Q8_0-key / Q4_0-value workload, drawn with a seeded torch
+    """Device K/V planes of a Q8_0, Q8_0-key / Q4_0-value or Q4_0 workload, drawn with a seeded torch
     generator in the value ranges of the seeded numpy generators (int8 in [-127, 127], Q8_0
     scales U(0.001, 0.02); 4-bit pairs as bytes in [0, 255], Q4_0 scales U(0.001, 0.3))."""
     N, Hk, D = w.n_cells, w.n_head_kv, w.head_dim
     g = torch.Generator(device="cuda")
     g.manual_seed(2000 + w.number)
-    kq = torch.randint(-127, 128, (N, Hk, D), dtype=torch.int8, device="cuda", generator=g)
-    kd = (torch.rand((N, Hk, D // 32), device="cuda", generator=g) * 0.019 + 0.001).half()
-    if w.kv_type == "q8_0_q4_0":
+    if w.kv_type == "q4_0":
+        kq = torch.randint(0, 256, (N, Hk, D // 2), dtype=torch.uint8, device="cuda", generator=g)
+        kd = (torch.rand((N, Hk, D // 32), device="cuda", generator=g) * 0.299 + 0.001).half()
+    else:
+        kq = torch.randint(-127, 128, (N, Hk, D), dtype=torch.int8, device="cuda", generator=g)
+        kd = (torch.rand((N, Hk, D // 32), device="cuda", generator=g) * 0.019 + 0.001).half()
+    if w.kv_type in ("q8_0_q4_0", "q4_0"):
         vq = torch.randint(0, 256, (N, Hk, D // 2), dtype=torch.uint8, device="cuda", generator=g)
         vd = (torch.rand((N, Hk, D // 32), device="cuda", generator=g) * 0.299 + 0.001).half()
     else:
@@ -342,20 +346,22 @@ def bench_workloads(K, torch, stream, peak):
     del kk, vv
 
     # Q8_0 long context, head_dim 128 and 256; and Q8_0 keys with Q4_0 values
-    for w in (inputs.Q8_LONG_D128, inputs.Q8_LONG_D256, inputs.Q8Q4_LONG_D128, inputs.Q8Q4_LONG_D256):
+    for w in (inputs.Q8_LONG_D128, inputs.Q8_LONG_D256, inputs.Q8Q4_LONG_D128, inputs.Q8Q4_LONG_D256,
+              inputs.Q4_LONG_D128, inputs.Q4_LONG_D256):
         N, Hk, D = w.n_cells, w.n_head_kv, w.head_dim
         kq, vq, kd, vd = quantized_kv_torch(torch, w)
-        q4 = w.kv_type == "q8_0_q4_0"
+        kv_type = {"q8_0": 1, "q8_0_q4_0": 2, "q4_0": 3}[w.kv_type]
         q = torch.from_numpy(inputs.make_q(w)).cuda()
         lens = torch.tensor([N], dtype=torch.int32, device="cuda")
         ws = K.decode_workspace(1, w.n_head, D, N, w.split)
         out = torch.empty((1, w.n_head, D), dtype=torch.float32, device="cuda")
         lse = torch.empty((1, w.n_head), dtype=torch.float32, device="cuda")
-        fn = lambda: K.kvattn_decode(q, kq, vq, kd, vd, 2 if q4 else 1, N, None, 0, lens, 1, N, w.n_head, Hk, D,
+        fn = lambda: K.kvattn_decode(q, kq, vq, kd, vd, kv_type, N, None, 0, lens, 1, N, w.n_head, Hk, D,
                                      w.split, 1 / math.sqrt(D), out, lse, ws, ws.numel(), stream)
         fn()
-        # K: D int8 + D/32 f16 scales per (cell, head); V: the same, or D/2 bytes + scales
-        kv_bytes = N * Hk * ((D + D // 16) + ((D // 2 if q4 else D) + D // 16))
+        # per (cell, head): K and V rows of D int8 (or D/2 bytes of 4-bit values) + D/32 f16 scales
+        kb, vb = (D // 2 if kv_type == 3 else D), (D if kv_type == 1 else D // 2)
+        kv_bytes = N * Hk * ((kb + D // 16) + (vb + D // 16))
         add(w.name, kv_bytes, timed(fn))
         del kq, vq, kd, vd
 
@@ -733,6 +739,11 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+def PROFILE_WORKLOADS(inputs):
+    return (inputs.Q8_LONG_D128, inputs.Q8_LONG_D256, inputs.Q8Q4_LONG_D128, inputs.Q8Q4_LONG_D256,
+            inputs.Q4_LONG_D128, inputs.Q4_LONG_D256)
+
+
 def profile_workload(args):
     """A few launches of one decode-attention workload's kvattn_decode_partials, for
     profilers (no timing, no JSON line).  Inputs are built on the device with torch RNG in
@@ -740,11 +751,10 @@ def profile_workload(args):
     import torch
     from kv_cache_decode_02_gb300 import inputs
     from kv_cache_decode_02_gb300 import kvattn as K
-    w = {x.name: x for x in (inputs.Q8_LONG_D128, inputs.Q8_LONG_D256, inputs.Q8Q4_LONG_D128,
-                             inputs.Q8Q4_LONG_D256)}[args.profile_workload]
+    w = {x.name: x for x in PROFILE_WORKLOADS(inputs)}[args.profile_workload]
     N, H, Hk, D = w.n_cells, w.n_head, w.n_head_kv, w.head_dim
     kq, vq, kd, vd = quantized_kv_torch(torch, w)
-    kv_type = K.KVATTN_KV_Q8_0_Q4_0 if w.kv_type == "q8_0_q4_0" else K.KVATTN_KV_Q8_0
+    kv_type = {"q8_0": K.KVATTN_KV_Q8_0, "q8_0_q4_0": K.KVATTN_KV_Q8_0_Q4_0, "q4_0": K.KVATTN_KV_Q4_0}[w.kv_type]
     q = torch.from_numpy(inputs.make_q(w)).cuda()
     lens = torch.tensor([N], dtype=torch.int32, device="cuda")
     n_split = -(-N // w.split)
@@ -774,7 +784,8 @@ def main():
     ap.add_argument("--no-parity", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=12.0)
     ap.add_argument("--profile-workload", choices=["q8_0_n131072_d128", "q8_0_n131072_d256", "q8_0_q4_0_n131072_d128",
-                                                   "q8_0_q4_0_n131072_d256"],
+                                                   "q8_0_q4_0_n131072_d256", "q4_0_n131072_d128",
+                                                   "q4_0_n131072_d256"],
                     help="only launch this workload's split decode --kernel-reps times (for ncu)")
     args = ap.parse_args()
     if args.profile_workload:

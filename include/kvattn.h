@@ -36,6 +36,7 @@
  *         scale and 16 bytes; byte j of block b (byte 16b + j of the row) holds element
  *         32b + j in its low nibble and 32b + 16 + j in its high nibble; value =
  *         scale * (nibble - 8) (the llama.cpp q4_0 block, values and scales in two planes).
+ *  Q4_0 : K and V both as the Q4_0 values above ([RKV] section 5a, the q4_0 cache).
  *  q    : half  [n_seq][n_head][head_dim];  out: float [n_seq][n_head][head_dim];
  *  lse  : float [n_seq][n_head] (natural log).
  */
@@ -59,7 +60,12 @@ typedef enum {
     KVATTN_ERR_TIMEOUT = -6        /* a bounded host wait ran out */
 } kvattn_status;
 
-typedef enum { KVATTN_KV_F16 = 0, KVATTN_KV_Q8_0 = 1, KVATTN_KV_Q8_0_Q4_0 = 2 } kvattn_kv_type;
+typedef enum {
+    KVATTN_KV_F16 = 0,
+    KVATTN_KV_Q8_0 = 1,
+    KVATTN_KV_Q8_0_Q4_0 = 2,
+    KVATTN_KV_Q4_0 = 3
+} kvattn_kv_type;
 
 /* Sticky device-side status bits, read with kvattn_workspace_status. */
 #define KVATTN_DEVICE_WAIT_TIMEOUT 1u   /* a bounded pipeline wait gave up; results invalid */
@@ -145,8 +151,9 @@ int kvattn_select_split(int kv_type, int n_seq, int64_t max_len, int n_head_kv, 
  *
  *  q        device half [n_seq][n_head][head_dim].
  *  k_cache, v_cache  device, 16-byte aligned.  f16: half rows.  Q8_0: int8 rows.
- *           Q8_0_Q4_0: int8 K rows, packed 4-bit V rows of head_dim / 2 bytes.
- *  k_scales, v_scales  device half scale planes for Q8_0 and Q8_0_Q4_0 (8-byte aligned
+ *           Q8_0_Q4_0: int8 K rows, packed 4-bit V rows of head_dim / 2 bytes.  Q4_0: packed
+ *           4-bit K and V rows.
+ *  k_scales, v_scales  device half scale planes of the quantised types (8-byte aligned
  *           for head_dim 128, 16-byte for 256); must be NULL for f16.
  *  kv_type  a kvattn_kv_type.
  *  n_cells  rows per sequence when cell_plan is NULL (sequence s reads rows

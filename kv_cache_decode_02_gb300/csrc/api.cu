@@ -47,8 +47,8 @@ int sm_count() {
 // multi-query kernel).
 int occupancy(int kv_type, int head_dim, int n_stages, bool mq = false) {
     static std::mutex mu;
-    static int cache[kMaxDevices][3][2][2][16];
-    static bool have[kMaxDevices][3][2][2][16];
+    static int cache[kMaxDevices][4][2][2][16];
+    static bool have[kMaxDevices][4][2][2][16];
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return 1;
     const int d = dev % kMaxDevices, t = kv_type, h = head_dim == 256 ? 1 : 0, m = mq ? 1 : 0;
@@ -144,7 +144,8 @@ void set_kv_maps(SplitDecodeParams& p, int kv_type, int64_t cells, int n_head_kv
 }
 
 bool valid_kv_type(int kv_type) {
-    return kv_type == KVATTN_KV_F16 || kv_type == KVATTN_KV_Q8_0 || kv_type == KVATTN_KV_Q8_0_Q4_0;
+    return kv_type == KVATTN_KV_F16 || kv_type == KVATTN_KV_Q8_0 || kv_type == KVATTN_KV_Q8_0_Q4_0 ||
+           kv_type == KVATTN_KV_Q4_0;
 }
 
 // Failure-detection test hook (host-side switch, read on every call): with
@@ -189,7 +190,7 @@ bool kvattn::encode_kv_tensor_map(CUtensorMap* map, const void* base, int kv_typ
     EncodeTiledFn enc = tensor_map_encoder();
     if (enc == nullptr || base == nullptr || cells < 1 || !aligned(base, 16)) return false;
     const bool f16 = kv_type == KVATTN_KV_F16;
-    const bool q4 = v_side && kv_type == KVATTN_KV_Q8_0_Q4_0;  // two 4-bit values per byte
+    const bool q4 = kv_type == KVATTN_KV_Q4_0 || (v_side && kv_type == KVATTN_KV_Q8_0_Q4_0);  // 4-bit rows
     const cuuint64_t row_elems = q4 ? (cuuint64_t)head_dim / 2 : (cuuint64_t)head_dim;
     const cuuint64_t row_bytes = row_elems * (f16 ? 2 : 1);
     const cuuint64_t dims[3] = {row_elems, (cuuint64_t)n_head_kv, (cuuint64_t)cells};

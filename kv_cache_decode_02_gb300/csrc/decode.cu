@@ -361,6 +361,25 @@ __device__ __forceinline__ void load_q_frags(const SplitDecodeParams& p, int s, 
     }
 }
 
+// Query fragments in the element order of the Q4_0 key path (q4_qk_block): for the MMA of
+// block b, half h, the k pairs (2tq, 2tq+1) and (2tq+8, 2tq+9) hold elements (e, e+2) and
+// (e+1, e+3) with e = 32b + 16h + 4tq.
+template <int D>
+__device__ __forceinline__ void load_q_frags_q4k(const SplitDecodeParams& p, int s, int g, int gq, int tq,
+                                                 uint32_t (&qa)[D / 16][2]) {
+    const bool row_ok = gq < p.group;
+    const int h = g * p.group + (row_ok ? gq : 0);
+    const uint32_t* qrow = reinterpret_cast<const uint32_t*>(p.q + ((int64_t)s * p.n_head + h) * D);
+#pragma unroll
+    for (int kk = 0; kk < D / 16; ++kk) {
+        const int e = 32 * (kk >> 1) + 16 * (kk & 1) + 4 * tq;
+        const uint32_t w0 = row_ok ? __ldg(qrow + e / 2) : 0u;      // elements e, e+1
+        const uint32_t w1 = row_ok ? __ldg(qrow + e / 2 + 1) : 0u;  // elements e+2, e+3
+        qa[kk][0] = prmt_b32(w0, w1, 0x5410u);  // (e, e+2)
+        qa[kk][1] = prmt_b32(w0, w1, 0x7632u);  // (e+1, e+3)
+    }
+}
+
 // One work unit = (sequence, split, KV head).  Units are numbered with the KV head fastest,
 // so the CTAs that run side by side read the rows of every head of the same cells.
 struct Unit {
@@ -1207,17 +1226,36 @@ __device__ __forceinline__ uint32_t q4x2_hi(uint32_t w) {
     return r;
 }
 
-// One warp's 16-cell chunk of Q8_0 keys and Q4_0 values: scores, online softmax, P V.
-// SWZ: the chunk came by TMA boxes (K in 128-byte-wide planes under the 128-byte swizzle as
-// for Q8_0, V in one box of D/2-byte rows under the swizzle of that width); otherwise by one
-// copy per row into plain rows.
+// Q4_0 q.K of one 32-element block b for the two 8-cell n-tiles.  kw[j] is the 32-bit word at
+// bytes 4tq .. 4tq+3 of the block for cell 8j + gq: low nibbles = elements 4tq .. 4tq+3, high
+// nibbles = elements 16 + 4tq .. 16 + 4tq+3.  The mask-and-convert step pairs bytes 0 and 2
+// (and 1 and 3, after a shift), so the MMA k pairs (2tq, 2tq+1) and (2tq+8, 2tq+9) are the
+// element pairs (4tq, 4tq+2) and (4tq+1, 4tq+3) -- the query fragments are loaded in that
+// order (load_q_frags_q4k).
+__device__ __forceinline__ void q4_qk_block(float (&sacc)[2][4], const uint32_t (&qa0)[2], const uint32_t (&qa1)[2],
+                                            const uint32_t (&kw)[2], const float (&ksc)[2][2]) {
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+        float cb[4] = {0.f, 0.f, 0.f, 0.f};
+        const uint32_t w = kw[j], x = kw[j] >> 8;
+        mma_16816(cb, qa0[0], 0u, qa0[1], 0u, q4x2_lo(w), q4x2_lo(x));
+        mma_16816(cb, qa1[0], 0u, qa1[1], 0u, q4x2_hi(w), q4x2_hi(x));
+        sacc[j][0] = fmaf(cb[0], ksc[j][0], sacc[j][0]);
+        sacc[j][1] = fmaf(cb[1], ksc[j][1], sacc[j][1]);
+    }
+}
+
+// One warp's 16-cell chunk of Q8_0 or Q4_0 keys (KQ4) and Q4_0 values: scores, online
+// softmax, P V.  SWZ: the chunk came by TMA boxes (8-bit K in 128-byte-wide planes under the
+// 128-byte swizzle as for Q8_0; 4-bit K and V each in one box of D/2-byte rows under the
+// swizzle of that width); otherwise by one copy per row into plain rows.
 // V operand (O^T += V^T P'^T, head_dim in M): a lane reads the 16-bit word at bytes
 // 2gq, 2gq+1 of block b for cells 2tq, 2tq+1, 2tq+8, 2tq+9 -- elements 2gq, 2gq+1 in the low
 // nibbles and 2gq+16, 2gq+17 in the high ones -- so m-tile 2b holds dims 32b + 2gq (row gq)
 // and 32b + 2gq + 1 (row gq + 8), and m-tile 2b+1 the same plus 16.  Every dim of an m-tile
 // lies in block b, whose V scale multiplies P as in the Q8_0 path.
-template <int D, bool SWZ>
-__device__ __forceinline__ void q8q4_chunk(uint32_t kb, uint32_t vb, const unsigned char* ks,
+template <int D, bool SWZ, bool KQ4>
+__device__ __forceinline__ void q4v_chunk(uint32_t kb, uint32_t vb, const unsigned char* ks,
                                            const unsigned char* vs, uint32_t mask, int lane,
                                            const uint32_t (&qa)[D / 16][2], float (&oacc)[D / 16][4],
                                            float& m_run, float& l_run, float scale_log2) {
@@ -1226,8 +1264,18 @@ __device__ __forceinline__ void q8q4_chunk(uint32_t kb, uint32_t vb, const unsig
     constexpr int kVRow = D / 2;  // bytes of a 4-bit V row
     const int gq = lane >> 2;
     const int tq = lane & 3;
-    // K rows gq and 8 + gq: swizzled planes (see q8_chunk_swz) or plain D-byte rows
-    const uint32_t ka = SWZ ? ((kb + 128u * gq + 4u * tq) | (16u * gq)) : (kb + (uint32_t)D * gq + 4u * tq);
+    // K rows gq and 8 + gq.  8-bit: swizzled planes (see q8_chunk_swz) or plain D-byte rows.
+    // 4-bit: the word at bytes 16b + 4tq of the row; under the swizzle its 16-byte column is
+    // b ^ (gq >> 1 & 3) (64-byte rows) or b ^ gq (128-byte rows), the same for row gq + 8.
+    uint32_t ka;
+    if (KQ4) {
+        if (SWZ)
+            ka = D == 128 ? ((kb + 64u * gq + 4u * tq) | (16u * ((gq >> 1) & 3))) : ((kb + 128u * gq + 4u * tq) | (16u * gq));
+        else
+            ka = kb + (uint32_t)kVRow * gq + 4u * tq;
+    } else {
+        ka = SWZ ? ((kb + 128u * gq + 4u * tq) | (16u * gq)) : (kb + (uint32_t)D * gq + 4u * tq);
+    }
     // V: base addresses whose XOR with 16b (plus immediates) give cells 2tq, 2tq+1, 2tq+8, 2tq+9
     // of block b.  head_dim 256 (128-byte rows, 128-byte swizzle): the 16-byte column of
     // (row c, byte x) is (x >> 4) ^ (c & 7).  head_dim 128 (64-byte rows, 64-byte swizzle):
@@ -1264,30 +1312,39 @@ __device__ __forceinline__ void q8q4_chunk(uint32_t kb, uint32_t vb, const unsig
             }
 #pragma unroll
     for (int b = 0; b < D / 32; ++b) {
-        uint32_t a0, a1, rs;
-        if (SWZ) {
-            const uint32_t pl = kPlane * (b >> 2);
-            a0 = (ka ^ (32u * (b & 3))) + pl;
-            a1 = (ka ^ (32u * (b & 3) + 16u)) + pl;
-            rs = 1024u;  // rows 8..15 of the plane
-        } else {
-            a0 = ka + 32u * b;
-            a1 = a0 + 16u;
-            rs = 8u * D;
-        }
-        uint32_t kw[2][2];
         float ksc[2][2];
 #pragma unroll
-        for (int j = 0; j < 2; ++j) {
-            kw[j][0] = lds32(a0 + rs * j);
-            kw[j][1] = lds32(a1 + rs * j);
+        for (int j = 0; j < 2; ++j)
 #pragma unroll
             for (int e = 0; e < 2; ++e) {
                 const uint32_t w = ksw[j][e][b >> 1];
                 ksc[j][e] = __half2float(__ushort_as_half((unsigned short)((b & 1) ? (w >> 16) : (w & 0xffffu))));
             }
+        if constexpr (KQ4) {
+            const uint32_t a = SWZ ? (ka ^ (16u * b)) : (ka + 16u * b);
+            const uint32_t rs = SWZ ? (D == 128 ? 512u : 1024u) : 8u * kVRow;  // rows 8..15
+            const uint32_t kw[2] = {lds32(a), lds32(a + rs)};
+            q4_qk_block(sacc, qa[2 * b], qa[2 * b + 1], kw, ksc);
+        } else {
+            uint32_t a0, a1, rs;
+            if (SWZ) {
+                const uint32_t pl = kPlane * (b >> 2);
+                a0 = (ka ^ (32u * (b & 3))) + pl;
+                a1 = (ka ^ (32u * (b & 3) + 16u)) + pl;
+                rs = 1024u;  // rows 8..15 of the plane
+            } else {
+                a0 = ka + 32u * b;
+                a1 = a0 + 16u;
+                rs = 8u * D;
+            }
+            uint32_t kw[2][2];
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+                kw[j][0] = lds32(a0 + rs * j);
+                kw[j][1] = lds32(a1 + rs * j);
+            }
+            q8_qk_block(sacc, qa[2 * b], qa[2 * b + 1], kw, ksc);
         }
-        q8_qk_block(sacc, qa[2 * b], qa[2 * b + 1], kw, ksc);
     }
 
     float alpha, pf[2][2];
@@ -1351,13 +1408,13 @@ __device__ __forceinline__ void q8q4_chunk(uint32_t kb, uint32_t vb, const unsig
 // (chunk j goes to warp j mod W) and meet in the same end-of-unit exchange as above.  With
 // no producer warp, all the registers of an SM go to warps that compute.
 // ---------------------------------------------------------------------------------------
-template <int D, bool VQ4 = false>
+template <int D, bool VQ4 = false, bool KQ4 = false>
 struct Q8Self {
-    static constexpr int kRowBytes = D;                            // int8 K row per (cell, KV head)
+    static constexpr int kRowBytes = KQ4 ? D / 2 : D;              // K row per (cell, KV head): int8 or 4-bit
     static constexpr int kVRowBytes = VQ4 ? D / 2 : D;             // V row: int8, or two 4-bit values a byte
     static constexpr int kPlanes = D / 128;
     static constexpr int kPlane = kChunkCells * 128;               // one 128-byte-wide plane
-    static constexpr int kSection = kPlanes * kPlane;              // K rows of a chunk (V rows follow)
+    static constexpr int kSection = KQ4 ? kChunkCells * kRowBytes : kPlanes * kPlane;  // K rows (V rows follow)
     static constexpr int kVSection = kChunkCells * kVRowBytes;     // V rows of a chunk
     static constexpr int kChunkBytes = kSection + kVSection;       // a multiple of 1024
     static constexpr int kSclBytes = D / 16;                       // D/32 half scales per row
@@ -1366,9 +1423,9 @@ struct Q8Self {
     static_assert(kChunkBytes % 1024 == 0, "stages must keep the 1024-byte swizzle alignment");
 };
 
-template <int D, int W, int S, bool VQ4 = false>
+template <int D, int W, int S, bool VQ4 = false, bool KQ4 = false>
 constexpr int q8_self_smem() {
-    using Q = Q8Self<D, VQ4>;
+    using Q = Q8Self<D, VQ4, KQ4>;
     return kHeaderBytes + 1024 + (W - 1) * Q::kXchgSlot + W * S * (Q::kChunkBytes + Q::kSclChunk);
 }
 
@@ -1399,10 +1456,11 @@ __device__ __forceinline__ void cursor_seek(const SplitDecodeParams& p, ChunkCur
     }
 }
 
-template <int D, int W, int S, bool VQ4 = false>
+template <int D, int W, int S, bool VQ4 = false, bool KQ4 = false>
 __device__ __forceinline__ void q8_self_body(const SplitDecodeParams& p) {
-    constexpr int KVT = KVATTN_KV_Q8_0;  // the keys (and the query fragment order)
-    using Q = Q8Self<D, VQ4>;
+    static_assert(VQ4 || !KQ4, "4-bit keys come with 4-bit values");
+    constexpr int KVT = KVATTN_KV_Q8_0;  // 8-bit keys' query fragment order (load_q_frags)
+    using Q = Q8Self<D, VQ4, KQ4>;
     using G = Geom<KVT, D>;
     static_assert(G::kSclBytes == Q::kSclBytes, "scale rows");
     extern __shared__ __align__(1024) unsigned char smem_raw[];
@@ -1465,10 +1523,15 @@ __device__ __forceinline__ void q8_self_body(const SplitDecodeParams& p) {
         if (use_tma) {
             if (lane == 0) {
                 const uint32_t kdst = smem_addr(stage);
+                if (KQ4) {
+                    tma_load_3d(kdst, &p.tmap_k, 0, c.g, (int)base, bar);
+                } else {
 #pragma unroll
-                for (int pl = 0; pl < Q::kPlanes; ++pl) {
-                    tma_load_3d(kdst + pl * Q::kPlane, &p.tmap_k, pl * 128, c.g, (int)base, bar);
-                    if (!VQ4) tma_load_3d(kdst + Q::kSection + pl * Q::kPlane, &p.tmap_v, pl * 128, c.g, (int)base, bar);
+                    for (int pl = 0; pl < Q::kPlanes; ++pl) {
+                        tma_load_3d(kdst + pl * Q::kPlane, &p.tmap_k, pl * 128, c.g, (int)base, bar);
+                        if (!VQ4)
+                            tma_load_3d(kdst + Q::kSection + pl * Q::kPlane, &p.tmap_v, pl * 128, c.g, (int)base, bar);
+                    }
                 }
                 // 4-bit V: one box of the chunk's D/2-byte rows (64 or 128 bytes wide)
                 if (VQ4) tma_load_3d(kdst + Q::kSection, &p.tmap_v, 0, c.g, (int)base, bar);
@@ -1551,10 +1614,15 @@ __device__ __forceinline__ void q8_self_body(const SplitDecodeParams& p) {
         if (use_tma) {
             if (lane == 0) {
                 const uint32_t kdst = smem_addr(stage);
+                if (KQ4) {
+                    tma_load_3d(kdst, &p.tmap_k, 0, c.g, (int)base, bar);
+                } else {
 #pragma unroll
-                for (int pl = 0; pl < Q::kPlanes; ++pl) {
-                    tma_load_3d(kdst + pl * Q::kPlane, &p.tmap_k, pl * 128, c.g, (int)base, bar);
-                    if (!VQ4) tma_load_3d(kdst + Q::kSection + pl * Q::kPlane, &p.tmap_v, pl * 128, c.g, (int)base, bar);
+                    for (int pl = 0; pl < Q::kPlanes; ++pl) {
+                        tma_load_3d(kdst + pl * Q::kPlane, &p.tmap_k, pl * 128, c.g, (int)base, bar);
+                        if (!VQ4)
+                            tma_load_3d(kdst + Q::kSection + pl * Q::kPlane, &p.tmap_v, pl * 128, c.g, (int)base, bar);
+                    }
                 }
                 // 4-bit V: one box of the chunk's D/2-byte rows (64 or 128 bytes wide)
                 if (VQ4) tma_load_3d(kdst + Q::kSection, &p.tmap_v, 0, c.g, (int)base, bar);
@@ -1632,7 +1700,12 @@ __device__ __forceinline__ void q8_self_body(const SplitDecodeParams& p) {
             }
             continue;
         }
-        if (qa_unit != u) load_q_frags<KVT, D>(p, x.s, x.g, gq, tq, qa);
+        if (qa_unit != u) {
+            if (KQ4)
+                load_q_frags_q4k<D>(p, x.s, x.g, gq, tq, qa);
+            else
+                load_q_frags<KVT, D>(p, x.s, x.g, gq, tq, qa);
+        }
         float oacc[D / 16][4];
         float m_run = -INFINITY, l_run = 0.f;
 #pragma unroll
@@ -1656,9 +1729,9 @@ __device__ __forceinline__ void q8_self_body(const SplitDecodeParams& p) {
             if (mask != 0u) {
                 if constexpr (VQ4) {
                     if (swz)
-                        q8q4_chunk<D, true>(kb, vb, ks, vs, mask, lane, qa, oacc, m_run, l_run, p.scale_log2);
+                        q4v_chunk<D, true, KQ4>(kb, vb, ks, vs, mask, lane, qa, oacc, m_run, l_run, p.scale_log2);
                     else
-                        q8q4_chunk<D, false>(kb, vb, ks, vs, mask, lane, qa, oacc, m_run, l_run, p.scale_log2);
+                        q4v_chunk<D, false, KQ4>(kb, vb, ks, vs, mask, lane, qa, oacc, m_run, l_run, p.scale_log2);
                 } else {
                     if (swz)
                         q8_chunk_swz<D>(kb, vb, ks, vs, mask, lane, qa, oacc, m_run, l_run, p.scale_log2);
@@ -1684,7 +1757,10 @@ __device__ __forceinline__ void q8_self_body(const SplitDecodeParams& p) {
         if (un < n_units) {
             const Unit y = unit_at(p, un);
             if (y.n_tiles > 0) {
-                load_q_frags<KVT, D>(p, y.s, y.g, gq, tq, qa);
+                if (KQ4)
+                    load_q_frags_q4k<D>(p, y.s, y.g, gq, tq, qa);
+                else
+                    load_q_frags<KVT, D>(p, y.s, y.g, gq, tq, qa);
                 qa_unit = un;
             }
         }
@@ -1830,6 +1906,15 @@ __global__ void __launch_bounds__(kQ8W256 * 32, kQ8B256)
     split_decode_q8q4_d256(const __grid_constant__ SplitDecodeParams p) {
     q8_self_body<256, kQ8W256, kQ8S256, true>(p);
 }
+// Q4_0 keys and values.
+__global__ void __launch_bounds__(kQ8W128 * 32, kQ8B128)
+    split_decode_q4_d128(const __grid_constant__ SplitDecodeParams p) {
+    q8_self_body<128, kQ8W128, kQ8S128, true, true>(p);
+}
+__global__ void __launch_bounds__(kQ8W256 * 32, kQ8B256)
+    split_decode_q4_d256(const __grid_constant__ SplitDecodeParams p) {
+    q8_self_body<256, kQ8W256, kQ8S256, true, true>(p);
+}
 
 const void* kernel_for(int kv_type, int head_dim, bool mq = false) {
     if (mq) return reinterpret_cast<const void*>(split_decode_mq_f16_d128);
@@ -1839,6 +1924,9 @@ const void* kernel_for(int kv_type, int head_dim, bool mq = false) {
     if (kv_type == KVATTN_KV_Q8_0_Q4_0)
         return head_dim == 128 ? reinterpret_cast<const void*>(split_decode_q8q4_d128)
                                : reinterpret_cast<const void*>(split_decode_q8q4_d256);
+    if (kv_type == KVATTN_KV_Q4_0)
+        return head_dim == 128 ? reinterpret_cast<const void*>(split_decode_q4_d128)
+                               : reinterpret_cast<const void*>(split_decode_q4_d256);
     return head_dim == 128 ? reinterpret_cast<const void*>(split_decode_q8_d128)
                            : reinterpret_cast<const void*>(split_decode_q8_d256);
 }
@@ -1865,6 +1953,9 @@ int split_decode_smem_bytes(int kv_type, int head_dim, int n_stages, bool mq) {
     if (kv_type == KVATTN_KV_Q8_0_Q4_0)
         return head_dim == 128 ? q8_self_smem<128, kQ8W128, kQ8S128, true>()
                                : q8_self_smem<256, kQ8W256, kQ8S256, true>();
+    if (kv_type == KVATTN_KV_Q4_0)
+        return head_dim == 128 ? q8_self_smem<128, kQ8W128, kQ8S128, true, true>()
+                               : q8_self_smem<256, kQ8W256, kQ8S256, true, true>();
     const int xchg = mq                ? Geom<0, 128>::kXchgBytesMQ
                      : head_dim == 128 ? Geom<0, 128>::kXchgBytes
                                        : Geom<0, 256>::kXchgBytes;
@@ -1893,12 +1984,12 @@ cudaError_t launch_split_decode(const SplitDecodeParams& p, int kv_type, int hea
                                 cudaStream_t stream, bool pdl) {
     const bool mq = p.mq != 0;
     const void* fn = kernel_for(kv_type, head_dim, mq);
-    static std::once_flag once[64][7];
-    static cudaError_t attr_err[64][7];
+    static std::once_flag once[64][9];
+    static cudaError_t attr_err[64][9];
     int dev = 0;
     cudaError_t err = cudaGetDevice(&dev);
     if (err != cudaSuccess) return err;
-    const int which = mq ? 6 : 2 * kv_type + (head_dim == 256 ? 1 : 0);
+    const int which = mq ? 8 : 2 * kv_type + (head_dim == 256 ? 1 : 0);
     std::call_once(once[dev & 63][which], [&] { attr_err[dev & 63][which] = set_smem_attr(fn); });
     if (attr_err[dev & 63][which] != cudaSuccess) return attr_err[dev & 63][which];
     cudaLaunchConfig_t cfg = {};

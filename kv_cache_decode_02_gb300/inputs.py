@@ -43,7 +43,7 @@ class Workload:
     n_head_kv: int
     head_dim: int
     split: int
-    kv_type: str = "f16"     # "f16", "q8_0" or "q8_0_q4_0"
+    kv_type: str = "f16"     # "f16", "q8_0", "q8_0_q4_0" or "q4_0"
     seq_lens: tuple = ()
     hole_prob: float = 0.0
     pool_records: int = 0
@@ -88,9 +88,14 @@ Q8Q4_LONG_D128 = Workload("q8_0_q4_0_n131072_d128", 8, 1, 131072, 32, 8, 128, 51
 Q8Q4_LONG_D256 = Workload("q8_0_q4_0_n131072_d256", 8, 1, 131072, 32, 8, 256, 512, kv_type="q8_0_q4_0",
                           seq_lens=(131072,))
 
+# The pages' q4_0 cache (keys and values), same shape.
+Q4_LONG_D128 = Workload("q4_0_n131072_d128", 9, 1, 131072, 32, 8, 128, 512, kv_type="q4_0", seq_lens=(131072,))
+Q4_LONG_D256 = Workload("q4_0_n131072_d256", 9, 1, 131072, 32, 8, 256, 512, kv_type="q4_0", seq_lens=(131072,))
+
 WORKLOADS = {w.name: w for w in
              (TINY, QWEN3_8B_LAYER, MULTISLOT_PLAN, Q8_LONG_D128, Q8_LONG_D256, WINDOW_TAIL,
-              STACK_TAIL_295MIB, STACK_TAIL_1815MIB, Q8Q4_LONG_D128, Q8Q4_LONG_D256)}
+              STACK_TAIL_295MIB, STACK_TAIL_1815MIB, Q8Q4_LONG_D128, Q8Q4_LONG_D256, Q4_LONG_D128,
+              Q4_LONG_D256)}
 
 
 def _rng(*seed) -> np.random.Generator:
@@ -152,6 +157,13 @@ def make_kv_f16(w: Workload, layer: int = 0, n_cells: int | None = None, seed_k=
 def make_kv_q8(w: Workload, layer: int = 0):
     k = q8_0_planes(_rng(2000 + w.number, layer, w.head_dim), w.n_cells, w.n_head_kv, w.head_dim)
     v = q8_0_planes(_rng(3000 + w.number, layer, w.head_dim), w.n_cells, w.n_head_kv, w.head_dim)
+    return k, v
+
+
+def make_kv_q4(w: Workload, layer: int = 0):
+    """Q4_0 key and value planes: ((k_packed, k_d), (v_packed, v_d))."""
+    k = q4_0_planes(_rng(2000 + w.number, layer, w.head_dim), w.n_cells, w.n_head_kv, w.head_dim)
+    v = q4_0_planes(_rng(3000 + w.number, layer, w.head_dim), w.n_cells, w.n_head_kv, w.head_dim)
     return k, v
 
 

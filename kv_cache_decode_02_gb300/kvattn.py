@@ -33,6 +33,7 @@ KVATTN_ERR_TIMEOUT = -6
 KVATTN_KV_F16 = 0
 KVATTN_KV_Q8_0 = 1
 KVATTN_KV_Q8_0_Q4_0 = 2
+KVATTN_KV_Q4_0 = 3
 KVATTN_DEVICE_WAIT_TIMEOUT = 1
 KVATTN_DEVICE_BAD_PLAN_ENTRY = 2
 KVATTN_TAIL_PREFETCH = 1
@@ -322,8 +323,8 @@ def decode(q, k_cache, v_cache, seq_lens, *, split, max_len=None, cell_plan=None
            v_scales=None, scale=None, n_cells=None, out=None, lse=None, ws=None, stream=None, kv_type=None):
     """q: half [S][H][D] (cuda); K/V as the C ABI describes; seq_lens int32 [S] (cuda).
 
-    ``kv_type`` defaults to f16 without scales, to Q8_0_Q4_0 when V's rows hold head_dim / 2
-    bytes, and to Q8_0 otherwise.  ``n_cells`` defaults to K's cell dimension (dim 0 for a
+    ``kv_type`` defaults to f16 without scales, to Q4_0 when K's rows hold head_dim / 2 bytes,
+    to Q8_0_Q4_0 when only V's do, and to Q8_0 otherwise.  ``n_cells`` defaults to K's cell dimension (dim 0 for a
     unified cache or a single sequence, dim 1 for a per-sequence [S][N][Hk][D] cache).
     Returns (out, lse).
     """
@@ -333,7 +334,10 @@ def decode(q, k_cache, v_cache, seq_lens, *, split, max_len=None, cell_plan=None
         if k_scales is None:
             kv_type = KVATTN_KV_F16
         else:
-            kv_type = KVATTN_KV_Q8_0_Q4_0 if v_cache.shape[-1] * 2 == D else KVATTN_KV_Q8_0
+            if k_cache.shape[-1] * 2 == D:
+                kv_type = KVATTN_KV_Q4_0
+            else:
+                kv_type = KVATTN_KV_Q8_0_Q4_0 if v_cache.shape[-1] * 2 == D else KVATTN_KV_Q8_0
     Hk = k_cache.shape[-2]
     if n_cells is None:
         n_cells = k_cache.shape[1] if (k_cache.dim() == 4) else k_cache.shape[0]

@@ -70,6 +70,8 @@ def call_decode(kvattn, a):
     (dict(kv_type=1), -1),                 # Q8_0 without scales
     (dict(kv_type=2), -1),                 # Q8_0 K + Q4_0 V without scales
     (dict(kv_type=2, ks=A, vs=A + 4), -1),  # scale planes not 8-byte aligned
+    (dict(kv_type=3), -1),                 # Q4_0 without scales
+    (dict(kv_type=4, ks=A, vs=A), -1),     # no such type
     (dict(ks=A, vs=A), -1),                # f16 with scales
     (dict(kv_type=7), -1),
     (dict(n_cells=0), -1),
