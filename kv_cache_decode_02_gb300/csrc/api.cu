@@ -1006,8 +1006,8 @@ int kvattn_decode_window_tail_direct(const void* q, const void* k_win, const voi
     p.group = n_head / n_head_kv;
     p.scale_log2 = (float)((double)scale * 1.4426950408889634074);
     apply_debug_hooks(p);
+    SplitDecodeParams w = p;
     if (n_split_win > 0) {
-        SplitDecodeParams w = p;
         w.k = k_win;
         w.v = v_win;
         w.n_cells = n_win;
@@ -1017,12 +1017,10 @@ int kvattn_decode_window_tail_direct(const void* q, const void* k_win, const voi
         w.part_base = 0;
         w.n_stages = pick_stages(KVATTN_KV_F16, head_dim, n_split_win * n_head_kv);
         set_kv_maps(w, KVATTN_KV_F16, n_win, n_head_kv, head_dim);
-        if (launch_decode_units(w, KVATTN_KV_F16, head_dim, n_split_win, cs, pdl) != cudaSuccess)
-            return KVATTN_ERR_CUDA;
     }
+    SplitDecodeParams t = p;
     if (n_split_tail > 0) {
         // the tail's rows cross the host link once, straight into shared memory
-        SplitDecodeParams t = p;
         t.k = dk;
         t.v = dv;
         t.n_cells = n_tail;
@@ -1033,7 +1031,27 @@ int kvattn_decode_window_tail_direct(const void* q, const void* k_win, const voi
         t.use_tma = 0;
         t.src_lsu = 1;
         t.n_stages = pick_stages(KVATTN_KV_F16, head_dim, n_split_tail * n_head_kv);
+    }
+    // When the tail's units fit in one wave, its decode (bound by the host link) goes first
+    // with a full dependency on the work before it, triggers its dependents at entry, and the
+    // window's decode (bound by HBM) follows as that programmatic dependent: reading nothing
+    // the tail writes, it skips the dependency wait, so both run at once; the merge then
+    // waits for both (ordinary launch).  Otherwise the window goes first and each launch
+    // waits for the one before it.
+    const bool overlap =
+        pdl && n_split_win > 0 && n_split_tail > 0 &&
+        n_split_tail * n_head_kv <= (int64_t)occupancy(KVATTN_KV_F16, head_dim, t.n_stages) * sm_count();
+    if (overlap) {
         if (launch_decode_units(t, KVATTN_KV_F16, head_dim, n_split_tail, cs, false) != cudaSuccess)
+            return KVATTN_ERR_CUDA;
+        w.no_dep_wait = 1;
+        if (launch_decode_units(w, KVATTN_KV_F16, head_dim, n_split_win, cs, true) != cudaSuccess)
+            return KVATTN_ERR_CUDA;
+    } else {
+        if (n_split_win > 0 && launch_decode_units(w, KVATTN_KV_F16, head_dim, n_split_win, cs, pdl) != cudaSuccess)
+            return KVATTN_ERR_CUDA;
+        if (n_split_tail > 0 &&
+            launch_decode_units(t, KVATTN_KV_F16, head_dim, n_split_tail, cs, false) != cudaSuccess)
             return KVATTN_ERR_CUDA;
     }
     MergeParams m = {};
@@ -1047,7 +1065,8 @@ int kvattn_decode_window_tail_direct(const void* q, const void* k_win, const voi
     m.head_dim = head_dim;
     m.split = 1;
     m.all_written = 1;
-    return cuda_status(launch_merge(m, cs, pdl && n_parts > 0));
+    // after the overlapped decodes the merge must follow both: an ordinary launch
+    return cuda_status(launch_merge(m, cs, pdl && n_parts > 0 && !overlap));
 }
 
 int kvattn_tail_wait(kvattn_tail_ctx* ctx, int timeout_ms) {

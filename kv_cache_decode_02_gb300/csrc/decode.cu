@@ -781,7 +781,7 @@ __device__ __forceinline__ void split_decode_body(const SplitDecodeParams& p) {
             }
         }
     }
-    pdl_wait();
+    if (!p.no_dep_wait) pdl_wait();
 
     const int gq = lane >> 2;
     const int tq = lane & 3;
