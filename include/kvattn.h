@@ -170,7 +170,10 @@ int kvattn_select_split(int kv_type, int n_seq, int64_t max_len, int n_head_kv, 
  *  scale    softmax scale applied to q . k in fp32 (1/sqrt(head_dim) is usual).
  *  out, lse device float outputs.   ws/ws_bytes  device workspace of at least
  *           kvattn_decode_workspace_bytes(...) bytes, 256-byte aligned, zeroed once
- *           after allocation (its first word is the sticky status word).
+ *           after allocation (its first word is the sticky status word).  After a call
+ *           with a cell_plan, bytes [256, 256 + 16 n_seq n_split) hold the per-split
+ *           descriptors int32 {n_valid, lo, hi, flags} [n_seq][n_split] (n_split =
+ *           ceil(max_len / split)) exactly as kvattn_build_descriptors computes them.
  *  stream   cudaStream_t.
  * Errors: INVALID_ARG, UNSUPPORTED, WORKSPACE (before any launch); CUDA.
  */

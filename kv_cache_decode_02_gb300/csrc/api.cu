@@ -384,11 +384,22 @@ int decode_impl(const void* q, const void* k_cache, const void* v_cache, const v
     int4* desc = nullptr;
     const bool pdl = use_pdl();
     if (n_split > 0) {
+        // Per-split descriptors of a plan.  The f16 kernels compute them in their producer warp
+        // from the plan entries it reads anyway (no launch on the critical path; a fully
+        // masked split then costs its plan reads and no K/V load); the quantised kernels,
+        // whose warps each see a part of a split, read them from a descriptor launch first
+        // and skip fully masked splits before touching their plan entries.
+        int4* desc_out = nullptr;
         if (cell_plan != nullptr) {
-            desc = reinterpret_cast<int4*>(wsb + lay.desc_off);
-            cudaError_t e = launch_descriptors(cell_plan, plan_stride, seq_lens, n_seq, max_len,
-                                               split, n_cells, n_split, desc, status, s);
-            if (e != cudaSuccess) return KVATTN_ERR_CUDA;
+            int4* d = reinterpret_cast<int4*>(wsb + lay.desc_off);
+            if (kv_type == KVATTN_KV_F16) {
+                desc_out = d;
+            } else {
+                desc = d;
+                cudaError_t e = launch_descriptors(cell_plan, plan_stride, seq_lens, n_seq, max_len,
+                                                   split, n_cells, n_split, desc, status, s);
+                if (e != cudaSuccess) return KVATTN_ERR_CUDA;
+            }
         }
         SplitDecodeParams p = {};
         p.q = static_cast<const __half*>(q);
@@ -399,6 +410,7 @@ int decode_impl(const void* q, const void* k_cache, const void* v_cache, const v
         p.plan = cell_plan;
         p.seq_lens = seq_lens;
         p.desc = desc;
+        p.desc_out = desc_out;
         p.part_o = part_o;
         p.part_lse = part_lse;
         p.status = status;

@@ -794,7 +794,18 @@ __device__ __forceinline__ void split_decode_body(const SplitDecodeParams& p) {
         uint32_t T = 0;  // tiles issued by this CTA (ring position)
         for (int64_t u = blockIdx.x; u < n_units && !stop; u += gridDim.x) {
             const Unit x = unit_at(p, u);
-            if (x.n_tiles == 0) continue;
+            // The split's descriptor (the same for every KV head) is written by its head-0 unit
+            // from the plan entries this warp reads anyway: count, smallest and largest valid
+            // cell, the (cell - position) range, out-of-range entries seen.
+            const bool emit_desc = p.desc_out != nullptr && x.g == 0;
+            if (x.n_tiles == 0) {
+                if (emit_desc && lane == 0)
+                    p.desc_out[(int64_t)x.s * p.n_split + x.split_idx] = make_int4(0, -1, -1, x.i0 >= x.len ? 9 : 1);
+                continue;
+            }
+            int d_lo = INT_MAX, d_hi = -1, d_count = 0;
+            long long d_off_lo = LLONG_MAX, d_off_hi = LLONG_MIN;
+            bool d_bad = false;
             const int s = x.s, g = x.g, n_tiles = x.n_tiles;
             const int64_t i0 = x.i0, i1 = x.i1;
             // plan entries of this lane's cell, prefetched four tiles ahead
@@ -828,6 +839,7 @@ __device__ __forceinline__ void split_decode_body(const SplitDecodeParams& p) {
                     if (p.plan != nullptr) {
                         if (e < -1 || (int64_t)e >= p.n_cells) {
                             bad = true;
+                            d_bad = true;
                             valid = false;
                         } else {
                             valid = e >= 0;
@@ -852,6 +864,15 @@ __device__ __forceinline__ void split_decode_body(const SplitDecodeParams& p) {
                     }
                     run = mask != 0u && off_lo == off_hi;
                     base = off_lo + tile0;
+                    if (emit_desc) {
+                        d_off_lo = min(d_off_lo, off_lo);
+                        d_off_hi = max(d_off_hi, off_hi);
+                        d_count += __popc(mask);
+                        if (valid) {
+                            d_lo = min(d_lo, (int)cell);
+                            d_hi = max(d_hi, (int)cell);
+                        }
+                    }
                 }
                 const bool use_tma = run && p.use_tma != 0 && mask != 0u && base > INT_MIN / 2 &&
                                      base < INT_MAX / 2;
@@ -926,6 +947,19 @@ __device__ __forceinline__ void split_decode_body(const SplitDecodeParams& p) {
                 if (p.src_lsu) cp_async_arrive_noinc(bar);
                 if (wrote) fence_proxy_async();  // zero-fills before later async writes to this stage
                 mbar_arrive(bar);
+            }
+            if (emit_desc && !stop) {
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) {
+                    d_lo = min(d_lo, __shfl_xor_sync(0xffffffffu, d_lo, o));
+                    d_hi = max(d_hi, __shfl_xor_sync(0xffffffffu, d_hi, o));
+                }
+                const bool any_bad = __any_sync(0xffffffffu, d_bad);
+                if (lane == 0) {
+                    const int flags = (d_count == 0 ? 1 : (d_off_lo == d_off_hi ? 2 : 0)) | (any_bad ? 4 : 0);
+                    p.desc_out[(int64_t)s * p.n_split + x.split_idx] =
+                        make_int4(d_count, d_count ? d_lo : -1, d_count ? d_hi : -1, flags);
+                }
             }
         }
         if (__any_sync(0xffffffffu, bad) && lane == 0) atomicOr(p.status, KVATTN_DEVICE_BAD_PLAN_ENTRY);

@@ -5,8 +5,9 @@
 // with an entry e valid when 0 <= e < n_cells, lo/hi the smallest/largest valid cell,
 // flags 1 = no valid entry, 2 = linear (e - i is the same for every valid entry: one
 // physical run with positional holes), 4 = an entry outside [-1, n_cells) seen,
-// 8 = the split starts at or beyond L.  The decode kernel reads n_valid to skip a split
-// before touching its plan entries or its K/V rows.
+// 8 = the split starts at or beyond L.  The quantised decode kernels read n_valid to skip a
+// split before touching its plan entries or its K/V rows; the f16 decode kernels build the
+// same descriptors in their producer warp instead (split_decode_body, desc_out).
 //
 // One warp per descriptor: lanes stride over the split's entries and reduce count,
 // min, max and the min/max of (e - i) with shuffles, so no division sits in the scan.

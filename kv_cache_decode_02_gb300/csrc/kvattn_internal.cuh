@@ -74,6 +74,8 @@ struct SplitDecodeParams {
     int write_beyond;         // splits past a sequence's length still write (0, -inf)
     int src_lsu;              // K/V rows arrive by 16-byte cp.async (e.g. straight from pinned
                               // host memory) instead of the TMA engine
+    int4* desc_out;           // nullable: per-split descriptors written by the f16 producer
+                              // ([n_seq][n_split], as descriptor_kernel computes them)
     int no_dep_wait;          // 1: launched as a programmatic dependent of a grid whose results
                               // it does not read, and itself launched only after everything it
                               // does read was complete: skip the dependency wait (run beside it)

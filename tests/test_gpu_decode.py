@@ -161,6 +161,48 @@ def test_descriptors_bit_exact(kvattn):
         assert np.array_equal(desc.cpu().numpy(), want)
 
 
+@pytest.mark.parametrize("kv", ["f16", "q8_0"])
+def test_decode_leaves_the_split_descriptors_in_the_workspace(kvattn, kv):
+    """kvattn_decode with a plan leaves every split's descriptor at byte 256 of the
+    workspace, bit-exact with the CPU mirror (the f16 kernels compute them in their producer
+    warp, the quantised ones read them from a descriptor launch): out-of-range entries, a
+    fully masked split, splits past a sequence's length, max_len below the plan stride."""
+    import torch
+    rng = np.random.default_rng(12)
+    q, k, v, encoded, n_cells = small_unified(rng)
+    plan, lens = kvattn.build_cell_plan(encoded, n_cells, plan_stride=1200)
+    plan[0, 5] = -7
+    plan[1, 300] = n_cells + 3
+    plan[1, 128:256] = -1        # a fully masked split (128..255 of a 896-entry row)
+    S, H, D = q.shape
+    Hk = k.shape[1]
+    masked = plan.copy()
+    masked[(masked < -1) | (masked >= n_cells)] = -1
+    for split, max_len in [(128, 1200), (64, 1100), (32, 500)]:
+        n_split = -(-max_len // split)
+        ws = kvattn.decode_workspace(S, H, D, max_len, split)
+        ws.fill_(0xEE)
+        ws[:256].zero_()
+        if kv == "f16":
+            out, lse = kvattn.decode(dev(q), dev(k), dev(v), dev(lens), split=split, cell_plan=dev(plan),
+                                     n_cells=n_cells, max_len=max_len, ws=ws)
+            wo, wl = oracle.decode_f16(q, k, v, np.minimum(lens, max_len).tolist(), plan=masked)
+        else:
+            kq = rng.integers(-127, 128, (n_cells, Hk, D), dtype=np.int8)
+            vq = rng.integers(-127, 128, (n_cells, Hk, D), dtype=np.int8)
+            kd = rng.uniform(0.001, 0.02, (n_cells, Hk, D // 32)).astype(np.float16)
+            vd = rng.uniform(0.001, 0.02, (n_cells, Hk, D // 32)).astype(np.float16)
+            out, lse = kvattn.decode(dev(q), dev(kq), dev(vq), dev(lens), split=split, cell_plan=dev(plan),
+                                     n_cells=n_cells, max_len=max_len, ws=ws, k_scales=dev(kd), v_scales=dev(vd))
+            wo, wl = oracle.decode_q8_0(q, kq, kd, vq, vd, np.minimum(lens, max_len).tolist(), plan=masked)
+        torch.cuda.synchronize()
+        got = ws[256:256 + S * n_split * 16].view(torch.int32).view(S, n_split, 4).cpu().numpy()
+        want = po.descriptors(plan, lens, max_len, split, n_cells)
+        assert np.array_equal(got, want), (split, max_len)
+        assert kvattn.kvattn_workspace_status(ws) & kvattn.KVATTN_DEVICE_BAD_PLAN_ENTRY
+        assert_close(out, lse, wo, wl)
+
+
 def test_bad_plan_entries_are_masked_and_flagged(kvattn):
     import torch
     rng = np.random.default_rng(10)
