@@ -9,8 +9,9 @@
 // One CTA of 8 warps per row.  Latency, not bandwidth, bounds this kernel (a row has a
 // few KB to a few MB of partials sitting in L2), so it avoids dependent load chains.
 //  * partials written by the decode kernels (every O written, 0 for empty parts): warp w
-//    reads parts w, w+8, ... eight at a time, LSE and O in the same round, and keeps a
-//    running (max, sum, O); the warps are then combined with the same rescaling.
+//    reads parts w, w+8, ... eight (head_dim 256: four) at a time, LSE and O in the same
+//    round, and keeps a running (max, sum, O); the warps are then combined with the same
+//    rescaling.
 //  * caller partials (kvattn_merge: an empty part's O may be anything): pass 1 loads every
 //    LSE in parallel and reduces the maximum, pass 2 turns them into weights in shared
 //    memory, pass 3 sums the O rows of non-empty parts only, several loads in flight.
@@ -27,7 +28,64 @@ constexpr int kMergeThreads = kMergeWarps * 32;
 constexpr int kMaxChunks = 8;      // head_dim <= 1024: float4 chunks per lane (public merge)
 constexpr int kWeightCache = 4096; // parts whose weights stay in shared memory
 
-__global__ void __launch_bounds__(kMergeThreads) merge_kernel(const MergeParams p) {
+// Partials written by the decode kernels: warp w reads parts w, w + 8, ... BATCH at a time,
+// LSE and O in the same round of independent loads (an empty part's O is 0), and folds
+// them into a running (max, sum, O) with the decode kernel's rescaling.  CPL: float4 chunks
+// of a row per lane; each round keeps BATCH x CPL loads in flight per lane.
+template <int CPL, int BATCH>
+__device__ __forceinline__ void merge_written_rounds(const float* lse_base, const float* o_base, int64_t lse_stride,
+                                                     int64_t o_stride, int64_t n_parts, int chunks, int warp, int lane,
+                                                     float& mw, float& sw, float4 (&acc)[2]) {
+    for (int64_t q0 = warp; q0 < n_parts; q0 += (int64_t)kMergeWarps * BATCH) {
+        float l[BATCH];
+#pragma unroll
+        for (int u = 0; u < BATCH; ++u) {
+            const int64_t q = q0 + (int64_t)u * kMergeWarps;
+            l[u] = q < n_parts ? __ldg(lse_base + q * lse_stride) : -INFINITY;
+        }
+        float4 v[BATCH][CPL];
+#pragma unroll
+        for (int u = 0; u < BATCH; ++u) {
+            const int64_t q = q0 + (int64_t)u * kMergeWarps;
+#pragma unroll
+            for (int c = 0; c < CPL; ++c) {
+                const int ci = lane + 32 * c;
+                v[u][c] = (q < n_parts && ci < chunks)
+                              ? __ldg(reinterpret_cast<const float4*>(o_base + q * o_stride) + ci)
+                              : make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+        }
+        float bm = -INFINITY;
+#pragma unroll
+        for (int u = 0; u < BATCH; ++u) bm = fmaxf(bm, l[u]);
+        const float nm = fmaxf(mw, bm);
+        if (nm == -INFINITY) continue;
+        const float keep = __expf(mw - nm);  // 0 when nothing was accumulated yet
+        sw *= keep;
+#pragma unroll
+        for (int c = 0; c < CPL; ++c) {
+            acc[c].x *= keep;
+            acc[c].y *= keep;
+            acc[c].z *= keep;
+            acc[c].w *= keep;
+        }
+#pragma unroll
+        for (int u = 0; u < BATCH; ++u) {
+            const float w = l[u] == -INFINITY ? 0.f : __expf(l[u] - nm);
+            sw += w;
+#pragma unroll
+            for (int c = 0; c < CPL; ++c) {
+                acc[c].x = fmaf(w, v[u][c].x, acc[c].x);
+                acc[c].y = fmaf(w, v[u][c].y, acc[c].y);
+                acc[c].z = fmaf(w, v[u][c].z, acc[c].z);
+                acc[c].w = fmaf(w, v[u][c].w, acc[c].w);
+            }
+        }
+        mw = nm;
+    }
+}
+
+__global__ void __launch_bounds__(kMergeThreads, 2) merge_kernel(const MergeParams p) {
     __shared__ float red[kMergeWarps];
     __shared__ float wts[kWeightCache];
     extern __shared__ float4 acc_smem[];  // [warps][head_dim / 4]
@@ -56,61 +114,20 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const MergeParams 
     const int64_t o_stride = (int64_t)p.n_rows * p.head_dim;
 
     if (p.all_written) {
-        // One round of loads per batch: warp w reads parts w, w+8, ... eight at a time, LSE
-        // and O together (the decode path writes O = 0 for empty parts), and folds them into
-        // a running (max, sum, O) with the same rescaling the decode kernel uses.
-        constexpr int kBatch = 8;
         float mw = -INFINITY, sw = 0.f;
-        float4 acc[kMaxChunks];
-#pragma unroll
-        for (int c = 0; c < kMaxChunks; ++c) acc[c] = make_float4(0.f, 0.f, 0.f, 0.f);
-        for (int64_t q0 = warp; q0 < n_parts; q0 += (int64_t)kMergeWarps * kBatch) {
-            float l[kBatch];
-#pragma unroll
-            for (int u = 0; u < kBatch; ++u) {
-                const int64_t q = q0 + (int64_t)u * kMergeWarps;
-                l[u] = q < n_parts ? __ldg(lse_base + q * lse_stride) : -INFINITY;
-            }
-            float4 v[kBatch][2];
-#pragma unroll
-            for (int u = 0; u < kBatch; ++u) {
-                const int64_t q = q0 + (int64_t)u * kMergeWarps;
-#pragma unroll
-                for (int c = 0; c < 2; ++c) {
-                    const int ci = lane + 32 * c;
-                    v[u][c] = (q < n_parts && ci < chunks)
-                                  ? __ldg(reinterpret_cast<const float4*>(o_base + q * o_stride) + ci)
-                                  : make_float4(0.f, 0.f, 0.f, 0.f);
-                }
-            }
-            float bm = -INFINITY;
-#pragma unroll
-            for (int u = 0; u < kBatch; ++u) bm = fmaxf(bm, l[u]);
-            const float nm = fmaxf(mw, bm);
-            if (nm == -INFINITY) continue;
-            const float keep = __expf(mw - nm);  // 0 when nothing was accumulated yet
-            sw *= keep;
-#pragma unroll
-            for (int c = 0; c < 2; ++c) {
-                acc[c].x *= keep;
-                acc[c].y *= keep;
-                acc[c].z *= keep;
-                acc[c].w *= keep;
-            }
-#pragma unroll
-            for (int u = 0; u < kBatch; ++u) {
-                const float w = l[u] == -INFINITY ? 0.f : __expf(l[u] - nm);
-                sw += w;
-#pragma unroll
-                for (int c = 0; c < 2; ++c) {
-                    acc[c].x = fmaf(w, v[u][c].x, acc[c].x);
-                    acc[c].y = fmaf(w, v[u][c].y, acc[c].y);
-                    acc[c].z = fmaf(w, v[u][c].z, acc[c].z);
-                    acc[c].w = fmaf(w, v[u][c].w, acc[c].w);
-                }
-            }
-            mw = nm;
-        }
+        float4 acc[2];  // decode partials: head_dim <= 256, at most two float4 chunks per lane
+        acc[0] = acc[1] = make_float4(0.f, 0.f, 0.f, 0.f);
+        // head_dim <= 128: one float4 per lane and part, eight parts a round; 256: two, four.
+        // 128 registers, two CTAs per SM: the 192 rows of a four-sequence GQA-6 plan merge in
+        // one wave (105.3 -> 103.4 us for the whole op), and a CTA launched early under
+        // programmatic dependence leaves room for two decode CTAs of the next call beside it
+        // while it waits (at 244 registers it left none: 14.7 -> 16.2 us per Qwen3-8B layer).
+        if (chunks <= 32)
+            merge_written_rounds<1, 8>(lse_base, o_base, lse_stride, o_stride, n_parts, chunks, warp, lane, mw, sw,
+                                        acc);
+        else
+            merge_written_rounds<2, 4>(lse_base, o_base, lse_stride, o_stride, n_parts, chunks, warp, lane, mw, sw,
+                                       acc);
         if (lane == 0) {
             red[warp] = mw;
             wts[warp] = sw;
