@@ -9,6 +9,13 @@
  * it touches CUDA and returns a kvattn_status; it never aborts and never prints.
  * Device calls are asynchronous on the given stream(s).
  *
+ * Host threads: every entry point may be called from several threads at once (the
+ * library's per-device caches -- SM count, occupancy, kernel attributes, the tensor-map
+ * encoder -- are filled once under a lock), except that one kvattn_tail_ctx serves one
+ * thread at a time: it holds the window + tail pipeline's events, slot sequence and
+ * recorded graphs.  Work that shares a workspace must be ordered on the device by the
+ * caller (one stream, or events).
+ *
  * Sources (web pages, cited by title and section):
  *  [RKV]  "Rolling-KV -- overflow throughput evaluations (consolidated)",
  *         opencoti-llamafile docs/evaluations/rolling_kv.md
