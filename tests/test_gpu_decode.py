@@ -386,3 +386,45 @@ def test_split_zero_selects_a_split(kvattn, kv, D, S, N):
         torch.cuda.synchronize()
         wo, wl = oracle.decode_q8_0(q, kq, kd, vq, vd, lens.tolist())
     assert_close(out, lse, wo, wl)
+
+
+def test_calls_from_several_host_threads(kvattn):
+    """Four host threads, each with its own stream and workspace, decode at once (the first
+    calls on a fresh process race to fill the library's per-device caches)."""
+    import threading
+
+    import torch
+    rng = np.random.default_rng(13)
+    cases = []
+    for t in range(4):
+        N, D = 900 + 300 * t, (128, 256)[t % 2]
+        q = rand_f16(rng, (1, 16, D))
+        k = rand_f16(rng, (N, 4, D))
+        v = rand_f16(rng, (N, 4, D))
+        cases.append((q, k, v, N))
+    results = [None] * 4
+    errors = []
+
+    def work(t):
+        try:
+            q, k, v, N = cases[t]
+            s = torch.cuda.Stream()
+            with torch.cuda.stream(s):
+                qd, kd, vd = dev(q), dev(k), dev(v)
+                lens = dev(np.array([N], np.int32))
+                for _ in range(5):
+                    out, lse = kvattn.decode(qd, kd, vd, lens, split=0, stream=s)
+                s.synchronize()
+                results[t] = (out.cpu().numpy(), lse.cpu().numpy())
+        except Exception as e:  # reported below
+            errors.append(repr(e))
+
+    threads = [threading.Thread(target=work, args=(t,)) for t in range(4)]
+    for th in threads:
+        th.start()
+    for th in threads:
+        th.join()
+    assert not errors, errors
+    for (q, k, v, N), (o, l) in zip(cases, results):
+        wo, wl = oracle.decode_f16(q, k, v, [N])
+        assert np.max(np.abs(o - wo)) <= TOL_O and np.max(np.abs(l - wl)) <= 1e-4
