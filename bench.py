@@ -300,28 +300,31 @@ def bench_workloads(K, torch, stream, peak):
     fn()
     add(w.name, w.n_cells * w.n_head_kv * w.head_dim * 4, timed(fn), {"gated": False})
 
-    # causal multi-query decode: the Qwen3-8B-shaped layer verifying 4 draft tokens (16 query
-    # rows per KV head read every K/V byte once); 8 rotating layer buffers exceed L2
+    # causal multi-query decode: the Qwen3-8B-shaped layer verifying 4 and 8 draft tokens (16
+    # and 32 query rows per KV head read every K/V byte once); 8 rotating layer buffers
+    # exceed L2
     w = inputs.QWEN3_8B_LAYER
-    n_q, n_buf = 4, 8
+    n_buf = 8
     kvs = [(inputs.normal_f16_torch((2000 + w.number, l), (w.n_cells, w.n_head_kv, w.head_dim), "cuda"),
             inputs.normal_f16_torch((3000 + w.number, l), (w.n_cells, w.n_head_kv, w.head_dim), "cuda"))
            for l in range(n_buf)]
-    qm = torch.randn((1, n_q, w.n_head, w.head_dim), device="cuda").half()
     lens = torch.tensor(w.seq_lens, dtype=torch.int32, device="cuda")
-    wsm = torch.zeros(K.kvattn_decode_multi_workspace_bytes(1, n_q, w.n_head, w.head_dim, w.n_cells, w.split),
-                      dtype=torch.uint8, device="cuda")
-    om = torch.empty((1, n_q, w.n_head, w.head_dim), dtype=torch.float32, device="cuda")
-    lm = torch.empty((1, n_q, w.n_head), dtype=torch.float32, device="cuda")
-    it = [0]
+    for n_q in (4, 8):
+        qm = torch.randn((1, n_q, w.n_head, w.head_dim), device="cuda").half()
+        wsm = torch.zeros(K.kvattn_decode_multi_workspace_bytes(1, n_q, w.n_head, w.head_dim, w.n_cells, w.split),
+                          dtype=torch.uint8, device="cuda")
+        om = torch.empty((1, n_q, w.n_head, w.head_dim), dtype=torch.float32, device="cuda")
+        lm = torch.empty((1, n_q, w.n_head), dtype=torch.float32, device="cuda")
+        it = [0]
 
-    def mq():
-        kb, vb = kvs[it[0] % n_buf]
-        it[0] += 1
-        K.kvattn_decode_multi(qm, kb, vb, 0, w.n_cells, None, 0, lens, 1, w.n_cells, n_q, w.n_head, w.n_head_kv,
-                              w.head_dim, w.split, 1 / math.sqrt(w.head_dim), om, lm, wsm, wsm.numel(), stream)
-    add("qwen3_8b_layer_verify_nq4", w.n_cells * w.n_head_kv * w.head_dim * 4, timed(mq, 40),
-        {"n_q": n_q, "query_rows_per_kv_head": n_q * w.n_head // w.n_head_kv})
+        def mq():
+            kb, vb = kvs[it[0] % n_buf]
+            it[0] += 1
+            K.kvattn_decode_multi(qm, kb, vb, 0, w.n_cells, None, 0, lens, 1, w.n_cells, n_q, w.n_head,
+                                  w.n_head_kv, w.head_dim, w.split, 1 / math.sqrt(w.head_dim), om, lm, wsm,
+                                  wsm.numel(), stream)
+        add(f"qwen3_8b_layer_verify_nq{n_q}", w.n_cells * w.n_head_kv * w.head_dim * 4, timed(mq, 40),
+            {"n_q": n_q, "query_rows_per_kv_head": n_q * w.n_head // w.n_head_kv})
     del kvs
 
     # multi-slot GQA-6 through the compact plan (descriptors + decode + merge)

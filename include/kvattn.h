@@ -215,17 +215,19 @@ size_t kvattn_decode_multi_workspace_bytes(int n_seq, int n_q, int n_head, int h
 
 /*
  * kvattn_decode_multi -- device.  Causal multi-query decode ("small multi-query decode,
- * n_q <= 8/16 with a mask", the speculative-verify case of [RKV] section 3 and [KVN] item
- * 2): n_q new query tokens per sequence, whose own K/V cells are already in the cache.
- * seq_lens[s] = L counts them, token t sits at logical position L - n_q + t and attends to
- * the logical positions 0 .. L - n_q + t (plan entries or cells, -1 holes masked); a token
- * whose window is empty gets O = 0, LSE = -inf.  The G x n_q query rows of each KV head
- * share every K/V byte read (one 16-row MMA tile).
+ * n_q <= 8/16 with a mask", the speculative-verify case of [RKV] section 3 and [KVN] items
+ * 2 and 7, split decode eligible through n_q <= 8 with an attention mask): n_q new query
+ * tokens per sequence, whose own K/V cells are already in the cache.  seq_lens[s] = L
+ * counts them, token t sits at logical position L - n_q + t and attends to the logical
+ * positions 0 .. L - n_q + t (plan entries or cells, -1 holes masked); a token whose window
+ * is empty gets O = 0, LSE = -inf.  The G x n_q query rows of each KV head share every K/V
+ * byte read from HBM (one or two 16-row MMA tiles).
  *  q        device half [n_seq][n_q][n_head][head_dim].
  *  out, lse device float [n_seq][n_q][n_head][head_dim], [n_seq][n_q][n_head].
  *  Other arguments: as kvattn_decode (f16 KV only; no scales).
- *  Limits: kv_type f16, head_dim 128, (n_head / n_head_kv) * n_q <= 16 (UNSUPPORTED
- *  otherwise); n_q >= 1.  ws: kvattn_decode_multi_workspace_bytes(...) bytes.
+ *  Limits: kv_type f16, head_dim 128, (n_head / n_head_kv) * n_q <= 32 (e.g. n_q <= 8
+ *  at 4 query heads per KV head; UNSUPPORTED otherwise); n_q >= 1.
+ *  ws: kvattn_decode_multi_workspace_bytes(...) bytes.
  * Errors: as kvattn_decode.
  */
 int kvattn_decode_multi(const void* q, const void* k_cache, const void* v_cache, int kv_type,

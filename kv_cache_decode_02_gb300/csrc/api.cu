@@ -349,7 +349,7 @@ int decode_impl(const void* q, const void* k_cache, const void* v_cache, const v
     const DecodeShape shape{n_seq, n_head, n_head_kv, head_dim, split, max_len};
     int st = check_shape(shape);
     if (st != KVATTN_OK) return st;
-    if (multi && (kv_type != KVATTN_KV_F16 || head_dim != 128 || (n_head / n_head_kv) * n_q > 16))
+    if (multi && (kv_type != KVATTN_KV_F16 || head_dim != 128 || (n_head / n_head_kv) * n_q > 32))
         return KVATTN_ERR_UNSUPPORTED;
     if (q == nullptr || k_cache == nullptr || v_cache == nullptr || seq_lens == nullptr || ws == nullptr)
         return KVATTN_ERR_INVALID_ARG;

@@ -426,12 +426,12 @@ __device__ __forceinline__ Unit unit_at(const SplitDecodeParams& p, int64_t u) {
 // L - n_q + 1 + r / G (its token's own position and everything before it).
 // ---------------------------------------------------------------------------------------
 __device__ __forceinline__ void load_q_frags_mq(const SplitDecodeParams& p, int s, int g, int gq, int tq,
-                                                uint32_t (&qa)[8][4]) {
+                                                int row0, uint32_t (&qa)[8][4]) {
     constexpr int D = 128;
     const int rows = p.group * p.n_q;
 #pragma unroll
     for (int half = 0; half < 2; ++half) {
-        const int r = gq + 8 * half;
+        const int r = row0 + gq + 8 * half;
         const bool ok = r < rows;
         const int t = ok ? r / p.group : 0;
         const int h = g * p.group + (ok ? r % p.group : 0);
@@ -536,8 +536,10 @@ __device__ __forceinline__ void mq_tile(uint32_t kb, uint32_t vb, uint32_t mask,
 }
 
 // The consumer warps of the multi-query kernel: the same ring and unit walk as the
-// single-query consumers, then the doubled end-of-unit exchange and the partial write
-// (partial row of (token t, head h) = t * n_head + h).
+// single-query consumers (partial row of (token t, head h) = t * n_head + h).  Up to 16 query
+// rows per KV head, each warp attends to its 16 cells of every tile for all rows and the
+// two warps meet in the doubled end-of-unit exchange; with 17 to 32 rows, warp w takes rows
+// 16w .. 16w+15 over all 32 cells of every tile and writes them itself (no exchange).
 __device__ __forceinline__ void mq_consumers(const SplitDecodeParams& p, uint64_t* full_bar, uint64_t* empty_bar,
                                              const uint32_t* tile_mask, const uint32_t* tile_swz,
                                              volatile int* abort_flag, uint64_t* xchg_bar, unsigned char* xchg,
@@ -549,6 +551,8 @@ __device__ __forceinline__ void mq_consumers(const SplitDecodeParams& p, uint64_
     const int tq = lane & 3;
     const int H = p.n_head, GQ = p.group, NQ = p.n_q;
     const int rows = GQ * NQ;
+    const bool rsplit = rows > 16;       // the warps split the rows instead of the cells
+    const int row0 = rsplit ? 16 * warp : 0;
     const int64_t HR = (int64_t)NQ * H;  // partial rows per (sequence, split)
     float4* xo = reinterpret_cast<float4*>(xchg);      // [2][D/16][32 lanes]
     float* xm = reinterpret_cast<float*>(xo + 2 * (D / 16) * 32);  // [16] max
@@ -573,15 +577,15 @@ __device__ __forceinline__ void mq_consumers(const SplitDecodeParams& p, uint64_
             }
             continue;
         }
-        if (qa_unit != u) load_q_frags_mq(p, x.s, x.g, gq, tq, qa);
+        if (qa_unit != u) load_q_frags_mq(p, x.s, x.g, gq, tq, row0, qa);
         float oacc[2][8][4];
 #pragma unroll
         for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
             for (int i = 0; i < 8; ++i) oacc[nt][i][0] = oacc[nt][i][1] = oacc[nt][i][2] = oacc[nt][i][3] = 0.f;
         float m_run[2] = {-INFINITY, -INFINITY}, l_run[2] = {0.f, 0.f};
-        // causal limit (logical position, exclusive) of the lane's rows gq and gq + 8
-        const int64_t lim_row[2] = {x.len - NQ + 1 + gq / GQ, x.len - NQ + 1 + (gq + 8) / GQ};
+        // causal limit (logical position, exclusive) of the lane's rows row0 + gq and row0 + gq + 8
+        const int64_t lim_row[2] = {x.len - NQ + 1 + (row0 + gq) / GQ, x.len - NQ + 1 + (row0 + gq + 8) / GQ};
         for (int t = 0; t < x.n_tiles; ++t, ++T) {
             const int st = (int)(T % (uint32_t)n_stages);
             const uint32_t use = T / (uint32_t)n_stages;
@@ -590,11 +594,13 @@ __device__ __forceinline__ void mq_consumers(const SplitDecodeParams& p, uint64_
                 stop = true;
                 break;
             }
-            const uint32_t mask = (tile_mask[st] >> (warp * kWarpCells)) & 0xffffu;
             const bool swz = tile_swz[st] != 0u;
             unsigned char* stage = stages + st * G::kBytes;
-            if (mask != 0u) {
-                const int64_t p0 = x.i0 + (int64_t)t * kTileCells + warp * kWarpCells;
+            // hw: the 16-cell half of the tile
+            auto half = [&](int hw) {
+                const uint32_t mask = (tile_mask[st] >> (hw * kWarpCells)) & 0xffffu;
+                if (mask == 0u) return;
+                const int64_t p0 = x.i0 + (int64_t)t * kTileCells + hw * kWarpCells;
                 int lim[2];
 #pragma unroll
                 for (int hh = 0; hh < 2; ++hh) {
@@ -604,7 +610,9 @@ __device__ __forceinline__ void mq_consumers(const SplitDecodeParams& p, uint64_
                 if (swz) {
                     const uint32_t kb = smem_addr(stage);
                     if (mask != 0xffffu) {
-                        const int r = warp * kWarpCells + (lane & 15);
+                        // masked rows came in with the box: zero their V rows (with split rows
+                        // both warps write the same zeros, each before its own reads)
+                        const int r = hw * kWarpCells + (lane & 15);
                         if (lane < 16 && !((mask >> lane) & 1u)) {
 #pragma unroll
                             for (int pl = 0; pl < G::kPlanes; ++pl) {
@@ -616,12 +624,18 @@ __device__ __forceinline__ void mq_consumers(const SplitDecodeParams& p, uint64_
                         }
                         __syncwarp();
                     }
-                    mq_tile<true>(kb, kb + G::kSwzSection, mask, warp, lane, lim, qa, oacc, m_run, l_run, p.scale_log2);
+                    mq_tile<true>(kb, kb + G::kSwzSection, mask, hw, lane, lim, qa, oacc, m_run, l_run, p.scale_log2);
                 } else {
                     const uint32_t kb = smem_addr(stage);
-                    mq_tile<false>(kb, kb + G::kPadSection, mask, warp, lane, lim, qa, oacc, m_run, l_run,
+                    mq_tile<false>(kb, kb + G::kPadSection, mask, hw, lane, lim, qa, oacc, m_run, l_run,
                                    p.scale_log2);
                 }
+            };
+            if (rsplit) {
+                half(0);
+                half(1);
+            } else {
+                half(warp);
             }
             __syncwarp();
             mbar_arrive(smem_addr(&empty_bar[st]));
@@ -636,9 +650,33 @@ __device__ __forceinline__ void mq_consumers(const SplitDecodeParams& p, uint64_
         if (un < n_units) {
             const Unit y = unit_at(p, un);
             if (y.n_tiles > 0) {
-                load_q_frags_mq(p, y.s, y.g, gq, tq, qa);
+                load_q_frags_mq(p, y.s, y.g, gq, tq, row0, qa);
                 qa_unit = un;
             }
+        }
+        if (rsplit) {
+            // this warp's 16 rows are complete: normalise and write them
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    const int r = row0 + 8 * nt + 2 * tq + e;
+                    const float m = __shfl_sync(0xffffffffu, m_run[nt], 8 * tq + 4 * e);
+                    const float l = __shfl_sync(0xffffffffu, l_run[nt], 8 * tq + 4 * e);
+                    const bool have = m != -INFINITY && l > 0.f;
+                    const float inv = have ? 1.f / l : 0.f;
+                    if (r < rows) {
+                        const int64_t row = (int64_t)(r / GQ) * H + x.g * GQ + r % GQ;
+                        float* orow = p.part_o + (part * HR + row) * D;
+#pragma unroll
+                        for (int mt = 0; mt < 8; ++mt) {
+                            orow[16 * mt + gq] = oacc[nt][mt][e] * inv;
+                            orow[16 * mt + 8 + gq] = oacc[nt][mt][2 + e] * inv;
+                        }
+                        if (gq == 0) p.part_lse[part * HR + row] = have ? (m + fast_log2(l)) * kLn2 : -INFINITY;
+                    }
+                }
+            continue;
         }
         if (warp == 1) {
             if (X > 0) {

@@ -178,7 +178,7 @@ def test_multi_query_limits(kvattn):
                  lse=A + 16384, ws=A + 65536, ws_bytes=1 << 30, stream=None)
         a.update(over)
         return kvattn.lib.kvattn_decode_multi(*a.values())
-    assert call(n_q=5) == kvattn.KVATTN_ERR_UNSUPPORTED            # 4 x 5 = 20 rows > 16
+    assert call(n_q=9) == kvattn.KVATTN_ERR_UNSUPPORTED            # 4 x 9 = 36 rows > 32
     assert call(head_dim=256) == kvattn.KVATTN_ERR_UNSUPPORTED
     assert call(kv_type=1) == kvattn.KVATTN_ERR_UNSUPPORTED
     assert call(n_q=0) == kvattn.KVATTN_ERR_INVALID_ARG

@@ -1,6 +1,7 @@
 """GPU parity of causal multi-query decode (kvattn_decode_multi) against the fp64 oracle:
 n_q new tokens per sequence, token t seeing logical positions 0 .. L - n_q + t, the
-G x n_q query rows of a KV head in one 16-row MMA tile."""
+G x n_q query rows of a KV head in one 16-row MMA tile (up to 16 rows: the two consumer warps
+split the cells) or two (17 to 32 rows: they split the rows)."""
 import numpy as np
 import pytest
 
@@ -32,6 +33,10 @@ def check(out, lse, wo, wl):
     (8, 2, 4, [513, 300], 256),
     (16, 1, 4, [100, 16], 32),          # MHA, 16 tokens
     (3, 5, 2, [2049, 0], 512),          # 15 rows, an empty sequence
+    (8, 4, 2, [1500, 9, 5], 128),       # 32 rows: each warp takes 16 rows over all cells
+    (5, 5, 2, [640, 33], 64),           # 25 rows: the second warp's last 7 rows are padding
+    (17, 1, 2, [300, 17], 32),          # MHA, 17 tokens
+    (3, 6, 2, [2047], 256),             # 18 rows (GQA-6)
 ])
 def test_multi_query_contiguous(kvattn, n_q, G, Hk, lens, split):
     import torch
@@ -49,10 +54,11 @@ def test_multi_query_contiguous(kvattn, n_q, G, Hk, lens, split):
     check(out, lse, wo, wl)
 
 
-def test_multi_query_plan_with_holes(kvattn):
+@pytest.mark.parametrize("n_q", [4, 8])
+def test_multi_query_plan_with_holes(kvattn, n_q):
     import torch
     rng = np.random.default_rng(9)
-    Hk, G, n_q, D = 4, 4, 4, 128
+    Hk, G, D = 4, 4, 128
     H = Hk * G
     pool = 30
     n_cells = pool * 128
@@ -92,12 +98,13 @@ def test_one_token_equals_single_query_decode(kvattn):
     assert np.max(np.abs(ml.cpu().numpy()[:, 0] - sl.cpu().numpy())) <= 1e-5
 
 
-def test_speculative_verify_qwen3_layer(kvattn):
-    """The Qwen3-8B-shaped layer verifying 4 draft tokens: 16 query rows per KV head."""
+@pytest.mark.parametrize("n_q", [4, 8])
+def test_speculative_verify_qwen3_layer(kvattn, n_q):
+    """The Qwen3-8B-shaped layer verifying 4 or 8 draft tokens: 16 or 32 query rows per KV
+    head."""
     import torch
     from kv_cache_decode_02_gb300 import inputs
     w = inputs.QWEN3_8B_LAYER
-    n_q = 4
     rng = np.random.default_rng(11)
     q = rand_f16(rng, (1, n_q, w.n_head, w.head_dim))
     k, v = inputs.make_kv_f16(w, layer=0)
