@@ -320,7 +320,7 @@ def bench_workloads(K, torch, stream, peak):
         def mq():
             kb, vb = kvs[it[0] % n_buf]
             it[0] += 1
-            K.kvattn_decode_multi(qm, kb, vb, 0, w.n_cells, None, 0, lens, 1, w.n_cells, n_q, w.n_head,
+            K.kvattn_decode_multi(qm, kb, vb, None, None, 0, w.n_cells, None, 0, lens, 1, w.n_cells, n_q, w.n_head,
                                   w.n_head_kv, w.head_dim, w.split, 1 / math.sqrt(w.head_dim), om, lm, wsm,
                                   wsm.numel(), stream)
         add(f"qwen3_8b_layer_verify_nq{n_q}", w.n_cells * w.n_head_kv * w.head_dim * 4, timed(mq, 40),
@@ -366,6 +366,18 @@ def bench_workloads(K, torch, stream, peak):
         kb, vb = (D // 2 if kv_type == 3 else D), (D if kv_type == 1 else D // 2)
         kv_bytes = N * Hk * ((kb + D // 16) + (vb + D // 16))
         add(w.name, kv_bytes, timed(fn))
+        if w is inputs.Q8_LONG_D128:
+            # the same cache verifying 4 draft tokens (16 query rows per KV head)
+            n_q = 4
+            qm = torch.randn((1, n_q, w.n_head, D), device="cuda").half()
+            wsm = torch.zeros(K.kvattn_decode_multi_workspace_bytes(1, n_q, w.n_head, D, N, w.split),
+                              dtype=torch.uint8, device="cuda")
+            om = torch.empty((1, n_q, w.n_head, D), dtype=torch.float32, device="cuda")
+            lm = torch.empty((1, n_q, w.n_head), dtype=torch.float32, device="cuda")
+            fm = lambda: K.kvattn_decode_multi(qm, kq, vq, kd, vd, kv_type, N, None, 0, lens, 1, N, n_q, w.n_head,
+                                               Hk, D, w.split, 1 / math.sqrt(D), om, lm, wsm, wsm.numel(), stream)
+            fm()
+            add(w.name + "_verify_nq4", kv_bytes, timed(fm), {"n_q": n_q, "query_rows_per_kv_head": 16})
         del kq, vq, kd, vd
 
     # window + pinned-host tail

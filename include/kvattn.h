@@ -224,17 +224,19 @@ size_t kvattn_decode_multi_workspace_bytes(int n_seq, int n_q, int n_head, int h
  * byte read from HBM (one or two 16-row MMA tiles).
  *  q        device half [n_seq][n_q][n_head][head_dim].
  *  out, lse device float [n_seq][n_q][n_head][head_dim], [n_seq][n_q][n_head].
- *  Other arguments: as kvattn_decode (f16 KV only; no scales).
- *  Limits: kv_type f16, head_dim 128, (n_head / n_head_kv) * n_q <= 32 (e.g. n_q <= 8
- *  at 4 query heads per KV head; UNSUPPORTED otherwise); n_q >= 1.
+ *  Other arguments: as kvattn_decode.
+ *  Limits: head_dim 128; kv_type f16 with (n_head / n_head_kv) * n_q <= 32 (e.g. n_q <= 8
+ *  at 4 query heads per KV head) or Q8_0 with (n_head / n_head_kv) * n_q <= 16
+ *  (UNSUPPORTED otherwise); n_q >= 1.
  *  ws: kvattn_decode_multi_workspace_bytes(...) bytes.
  * Errors: as kvattn_decode.
  */
-int kvattn_decode_multi(const void* q, const void* k_cache, const void* v_cache, int kv_type,
-                        int64_t n_cells, const int32_t* cell_plan, int64_t plan_stride,
-                        const int32_t* seq_lens, int n_seq, int64_t max_len, int n_q, int n_head,
-                        int n_head_kv, int head_dim, int split, float scale, float* out, float* lse,
-                        void* ws, size_t ws_bytes, void* stream);
+int kvattn_decode_multi(const void* q, const void* k_cache, const void* v_cache,
+                        const void* k_scales, const void* v_scales, int kv_type, int64_t n_cells,
+                        const int32_t* cell_plan, int64_t plan_stride, const int32_t* seq_lens,
+                        int n_seq, int64_t max_len, int n_q, int n_head, int n_head_kv, int head_dim,
+                        int split, float scale, float* out, float* lse, void* ws, size_t ws_bytes,
+                        void* stream);
 
 /*
  * kvattn_merge -- device.  LSE-weighted merge of partial attention results ([KVN]

@@ -349,7 +349,9 @@ int decode_impl(const void* q, const void* k_cache, const void* v_cache, const v
     const DecodeShape shape{n_seq, n_head, n_head_kv, head_dim, split, max_len};
     int st = check_shape(shape);
     if (st != KVATTN_OK) return st;
-    if (multi && (kv_type != KVATTN_KV_F16 || head_dim != 128 || (n_head / n_head_kv) * n_q > 32))
+    // multi-query: f16 up to 32 query rows per KV head, Q8_0 up to 16; head_dim 128
+    if (multi && (head_dim != 128 || (kv_type != KVATTN_KV_F16 && kv_type != KVATTN_KV_Q8_0) ||
+                  (n_head / n_head_kv) * n_q > (kv_type == KVATTN_KV_F16 ? 32 : 16)))
         return KVATTN_ERR_UNSUPPORTED;
     if (q == nullptr || k_cache == nullptr || v_cache == nullptr || seq_lens == nullptr || ws == nullptr)
         return KVATTN_ERR_INVALID_ARG;
@@ -481,12 +483,13 @@ int kvattn_decode_partials(const void* q, const void* k_cache, const void* v_cac
                        scale, nullptr, nullptr, part_o, part_lse, ws, ws_bytes, stream);
 }
 
-int kvattn_decode_multi(const void* q, const void* k_cache, const void* v_cache, int kv_type, int64_t n_cells,
-                        const int32_t* cell_plan, int64_t plan_stride, const int32_t* seq_lens, int n_seq,
-                        int64_t max_len, int n_q, int n_head, int n_head_kv, int head_dim, int split, float scale,
-                        float* out, float* lse, void* ws, size_t ws_bytes, void* stream) {
+int kvattn_decode_multi(const void* q, const void* k_cache, const void* v_cache, const void* k_scales,
+                        const void* v_scales, int kv_type, int64_t n_cells, const int32_t* cell_plan,
+                        int64_t plan_stride, const int32_t* seq_lens, int n_seq, int64_t max_len, int n_q, int n_head,
+                        int n_head_kv, int head_dim, int split, float scale, float* out, float* lse, void* ws,
+                        size_t ws_bytes, void* stream) {
     if (n_q < 1) return KVATTN_ERR_INVALID_ARG;
-    return decode_impl(q, k_cache, v_cache, nullptr, nullptr, kv_type, n_cells, cell_plan, plan_stride, seq_lens,
+    return decode_impl(q, k_cache, v_cache, k_scales, v_scales, kv_type, n_cells, cell_plan, plan_stride, seq_lens,
                        n_seq, max_len, n_head, n_head_kv, head_dim, split, scale, out, lse, nullptr, nullptr, ws,
                        ws_bytes, stream, n_q);
 }

@@ -1471,6 +1471,197 @@ __device__ __forceinline__ void q4v_chunk(uint32_t kb, uint32_t vb, const unsign
     }
 }
 
+// Query fragments of the multi-query Q8_0 kernel: rows gq (qa[kk][0..1]) and gq + 8
+// (qa[kk][2..3]) of the KV head's G x n_q rows, in the Q8_0 element order of load_q_frags.
+template <int D>
+__device__ __forceinline__ void load_q_frags_mq_q8(const SplitDecodeParams& p, int s, int g, int gq, int tq,
+                                                   uint32_t (&qa)[D / 16][4]) {
+    const int rows = p.group * p.n_q;
+#pragma unroll
+    for (int half = 0; half < 2; ++half) {
+        const int r = gq + 8 * half;
+        const bool ok = r < rows;
+        const int t = ok ? r / p.group : 0;
+        const int h = g * p.group + (ok ? r % p.group : 0);
+        const uint32_t* qrow = reinterpret_cast<const uint32_t*>(p.q + (((int64_t)s * p.n_q + t) * p.n_head + h) * D);
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+            const int d0 = 32 * (kk >> 1) + 16 * (kk & 1) + 4 * tq;
+            qa[kk][2 * half] = ok ? __ldg(qrow + d0 / 2) : 0u;
+            qa[kk][2 * half + 1] = ok ? __ldg(qrow + d0 / 2 + 1) : 0u;
+        }
+    }
+}
+
+// One warp's 16-cell Q8_0 chunk for up to 16 query rows (multi-query decode): q.K with the
+// whole M = 16 of the MMA, an online softmax per row (row gq + 8 hh, causal limit lim[hh]
+// cells of the chunk), and P V into two N = 8 tiles that share every converted V fragment.
+// SWZ: the 128-byte-swizzled TMA layout (see q8_chunk_swz), else plain D-byte rows.
+template <int D, bool SWZ>
+__device__ __forceinline__ void q8_mq_chunk(uint32_t kb, uint32_t vb, const unsigned char* ks,
+                                            const unsigned char* vs, uint32_t mask, int lane, const int (&lim)[2],
+                                            const uint32_t (&qa)[D / 16][4], float (&oacc)[2][D / 16][4],
+                                            float (&m_run)[2], float (&l_run)[2], float scale_log2) {
+    constexpr int kPlane = kChunkCells * 128;
+    constexpr int kScl = D / 16;
+    const int gq = lane >> 2;
+    const int tq = lane & 3;
+    const uint32_t ka = SWZ ? ((kb + 128u * gq + 4u * tq) | (16u * gq)) : (kb + (uint32_t)D * gq + 4u * tq);
+    uint32_t va0, va1;
+    if (SWZ) {
+        va0 = (vb + 256u * tq + 4u * (gq & 3)) | (16u * ((gq >> 2) ^ (2 * tq)));
+        va1 = (vb + 256u * tq + 128u + 4u * (gq & 3)) | (16u * ((gq >> 2) ^ (2 * tq + 1)));
+    } else {
+        va0 = vb + (uint32_t)D * (2 * tq) + 4u * gq;
+        va1 = va0 + D;
+    }
+    const uint32_t kss = smem_addr(ks) + 2u * kScl * tq;
+    const uint32_t vss = smem_addr(vs) + 2u * kScl * tq;
+
+    float sacc[2][4];
+#pragma unroll
+    for (int j = 0; j < 2; ++j) sacc[j][0] = sacc[j][1] = sacc[j][2] = sacc[j][3] = 0.f;
+    uint32_t ksw[2][2][D / 64];
+#pragma unroll
+    for (int j = 0; j < 2; ++j)
+#pragma unroll
+        for (int e = 0; e < 2; ++e)
+#pragma unroll
+            for (int h = 0; h < D / 128; ++h) {
+                const uint2 w = lds64(kss + (8 * j + e) * kScl + 8 * h);
+                ksw[j][e][2 * h] = w.x;
+                ksw[j][e][2 * h + 1] = w.y;
+            }
+#pragma unroll
+    for (int b = 0; b < D / 32; ++b) {
+        uint32_t a0, a1, rs;
+        if (SWZ) {
+            const uint32_t pl = kPlane * (b >> 2);
+            a0 = (ka ^ (32u * (b & 3))) + pl;
+            a1 = (ka ^ (32u * (b & 3) + 16u)) + pl;
+            rs = 1024u;
+        } else {
+            a0 = ka + 32u * b;
+            a1 = a0 + 16u;
+            rs = 8u * D;
+        }
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+            const uint32_t w0 = lds32(a0 + rs * j) ^ 0x80808080u, w1 = lds32(a1 + rs * j) ^ 0x80808080u;
+            float cb[4] = {0.f, 0.f, 0.f, 0.f};
+            mma_16816(cb, qa[2 * b][0], qa[2 * b][2], qa[2 * b][1], qa[2 * b][3], i8x2_lo(w0), i8x2_hi(w0));
+            mma_16816(cb, qa[2 * b + 1][0], qa[2 * b + 1][2], qa[2 * b + 1][1], qa[2 * b + 1][3], i8x2_lo(w1),
+                      i8x2_hi(w1));
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                const uint32_t w = ksw[j][e][b >> 1];
+                const float sc = __half2float(__ushort_as_half((unsigned short)((b & 1) ? (w >> 16) : (w & 0xffffu))));
+                sacc[j][e] = fmaf(cb[e], sc, sacc[j][e]);          // row gq
+                sacc[j][2 + e] = fmaf(cb[2 + e], sc, sacc[j][2 + e]);  // row gq + 8
+            }
+        }
+    }
+
+    // online softmax, one (max, sum) per row: hh = 0 -> row gq, hh = 1 -> row gq + 8
+    float x[2][2][2];
+    float tmax[2] = {-INFINITY, -INFINITY};
+#pragma unroll
+    for (int hh = 0; hh < 2; ++hh)
+#pragma unroll
+        for (int j = 0; j < 2; ++j)
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                const int c = 8 * j + 2 * tq + e;
+                const bool ok = ((mask >> c) & 1u) && c < lim[hh];
+                x[hh][j][e] = ok ? sacc[j][2 * hh + e] * scale_log2 : -INFINITY;
+                tmax[hh] = fmaxf(tmax[hh], x[hh][j][e]);
+            }
+#pragma unroll
+    for (int hh = 0; hh < 2; ++hh) {
+        tmax[hh] = fmaxf(tmax[hh], __shfl_xor_sync(0xffffffffu, tmax[hh], 1));
+        tmax[hh] = fmaxf(tmax[hh], __shfl_xor_sync(0xffffffffu, tmax[hh], 2));
+    }
+    if (__any_sync(0xffffffffu, tmax[0] > m_run[0] + kRescaleSlack || tmax[1] > m_run[1] + kRescaleSlack)) {
+        float alpha[2];
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+            const float m_new = fmaxf(m_run[hh], tmax[hh]);
+            alpha[hh] = fast_exp2(m_run[hh] - ((m_new == -INFINITY) ? 0.f : m_new));
+            m_run[hh] = m_new;
+            l_run[hh] *= alpha[hh];
+        }
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt) {
+            const float a0 = __shfl_sync(0xffffffffu, alpha[nt], 8 * tq);
+            const float a1 = __shfl_sync(0xffffffffu, alpha[nt], 8 * tq + 4);
+#pragma unroll
+            for (int mt = 0; mt < D / 16; ++mt) {
+                oacc[nt][mt][0] *= a0;
+                oacc[nt][mt][1] *= a1;
+                oacc[nt][mt][2] *= a0;
+                oacc[nt][mt][3] *= a1;
+            }
+        }
+    }
+    uint32_t ph[2][2];
+#pragma unroll
+    for (int hh = 0; hh < 2; ++hh) {
+        const float m_use = (m_run[hh] == -INFINITY) ? 0.f : m_run[hh];
+        float psum = 0.f;
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+            const float p0 = fast_exp2(x[hh][j][0] - m_use), p1 = fast_exp2(x[hh][j][1] - m_use);
+            ph[hh][j] = pack_half2(p0, p1);
+            psum += p0 + p1;
+        }
+        l_run[hh] += psum;
+    }
+    // V scales of cells 2tq, 2tq + 1, 2tq + 8, 2tq + 9
+    uint32_t vsw[4][D / 64];
+#pragma unroll
+    for (int c = 0; c < 4; ++c)
+#pragma unroll
+        for (int h = 0; h < D / 128; ++h) {
+            const uint2 w = lds64(vss + ((c & 1) + 8 * (c >> 1)) * kScl + 8 * h);
+            vsw[c][2 * h] = w.x;
+            vsw[c][2 * h + 1] = w.y;
+        }
+#pragma unroll
+    for (int b = 0; b < D / 32; ++b) {
+        uint32_t vw[4];
+        if (SWZ) {
+            const uint32_t pl = kPlane * (b >> 2);
+            const uint32_t c0 = (va0 ^ (32u * (b & 3))) + pl;
+            const uint32_t c1 = (va1 ^ (32u * (b & 3))) + pl;
+            vw[0] = lds32(c0);
+            vw[1] = lds32(c1);
+            vw[2] = lds32(c0 + 1024u);
+            vw[3] = lds32(c1 + 1024u);
+        } else {
+            const uint32_t c0 = va0 + 32u * b;
+            vw[0] = lds32(c0);
+            vw[1] = lds32(c0 + D);
+            vw[2] = lds32(c0 + 8u * D);
+            vw[3] = lds32(c0 + 9u * D);
+        }
+        const uint32_t sel = (b & 1) ? 0x7632u : 0x5410u;
+        const uint32_t s01 = prmt_b32(vsw[0][b >> 1], vsw[1][b >> 1], sel);
+        const uint32_t s89 = prmt_b32(vsw[2][b >> 1], vsw[3][b >> 1], sel);
+        const uint32_t f0 = vw[0] ^ 0x80808080u, f1 = vw[1] ^ 0x80808080u;
+        const uint32_t f2 = vw[2] ^ 0x80808080u, f3 = vw[3] ^ 0x80808080u;
+        const uint32_t u00 = prmt_b32(f0, f1, 0x5140u), u01 = prmt_b32(f0, f1, 0x7362u);
+        const uint32_t u10 = prmt_b32(f2, f3, 0x5140u), u11 = prmt_b32(f2, f3, 0x7362u);
+        const uint32_t A0[4] = {i8x2_lo(u00), i8x2_hi(u00), i8x2_lo(u10), i8x2_hi(u10)};
+        const uint32_t A1[4] = {i8x2_lo(u01), i8x2_hi(u01), i8x2_lo(u11), i8x2_hi(u11)};
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt) {
+            const uint32_t pb0 = hmul2_u32(ph[nt][0], s01), pb1 = hmul2_u32(ph[nt][1], s89);
+            mma_16816(oacc[nt][2 * b], A0[0], A0[1], A0[2], A0[3], pb0, pb1);
+            mma_16816(oacc[nt][2 * b + 1], A1[0], A1[1], A1[2], A1[3], pb0, pb1);
+        }
+    }
+}
+
 // ---------------------------------------------------------------------------------------
 // Q8_0: self-loading warps.  The Q8_0 kernels are bound by their consumer warps (every K
 // and V byte costs an int8 -> f16 conversion), so they drop the producer warp: each of the
@@ -1480,7 +1671,7 @@ __device__ __forceinline__ void q4v_chunk(uint32_t kb, uint32_t vb, const unsign
 // (chunk j goes to warp j mod W) and meet in the same end-of-unit exchange as above.  With
 // no producer warp, all the registers of an SM go to warps that compute.
 // ---------------------------------------------------------------------------------------
-template <int D, bool VQ4 = false, bool KQ4 = false>
+template <int D, bool VQ4 = false, bool KQ4 = false, bool MQ = false>
 struct Q8Self {
     static constexpr int kRowBytes = KQ4 ? D / 2 : D;              // K row per (cell, KV head): int8 or 4-bit
     static constexpr int kVRowBytes = VQ4 ? D / 2 : D;             // V row: int8, or two 4-bit values a byte
@@ -1491,13 +1682,14 @@ struct Q8Self {
     static constexpr int kChunkBytes = kSection + kVSection;       // a multiple of 1024
     static constexpr int kSclBytes = D / 16;                       // D/32 half scales per row
     static constexpr int kSclChunk = 2 * kChunkCells * kSclBytes;  // K then V scales
-    static constexpr int kXchgSlot = ((D / 16) * 32 * 16 + 64 + 1023) / 1024 * 1024;
+    // exchange slot of a warp: its O fragments ([N tiles][D/16][32 lanes] float4), max, sum
+    static constexpr int kXchgSlot = ((MQ ? 2 : 1) * (D / 16) * 32 * 16 + (MQ ? 128 : 64) + 1023) / 1024 * 1024;
     static_assert(kChunkBytes % 1024 == 0, "stages must keep the 1024-byte swizzle alignment");
 };
 
-template <int D, int W, int S, bool VQ4 = false, bool KQ4 = false>
+template <int D, int W, int S, bool VQ4 = false, bool KQ4 = false, bool MQ = false>
 constexpr int q8_self_smem() {
-    using Q = Q8Self<D, VQ4, KQ4>;
+    using Q = Q8Self<D, VQ4, KQ4, MQ>;
     return kHeaderBytes + 1024 + (W - 1) * Q::kXchgSlot + W * S * (Q::kChunkBytes + Q::kSclChunk);
 }
 
@@ -1528,11 +1720,12 @@ __device__ __forceinline__ void cursor_seek(const SplitDecodeParams& p, ChunkCur
     }
 }
 
-template <int D, int W, int S, bool VQ4 = false, bool KQ4 = false>
+template <int D, int W, int S, bool VQ4 = false, bool KQ4 = false, bool MQ = false>
 __device__ __forceinline__ void q8_self_body(const SplitDecodeParams& p) {
     static_assert(VQ4 || !KQ4, "4-bit keys come with 4-bit values");
+    static_assert(!MQ || (D == 128 && !VQ4), "multi-query: Q8_0, head_dim 128");
     constexpr int KVT = KVATTN_KV_Q8_0;  // 8-bit keys' query fragment order (load_q_frags)
-    using Q = Q8Self<D, VQ4, KQ4>;
+    using Q = Q8Self<D, VQ4, KQ4, MQ>;
     using G = Geom<KVT, D>;
     static_assert(G::kSclBytes == Q::kSclBytes, "scale rows");
     extern __shared__ __align__(1024) unsigned char smem_raw[];
@@ -1751,186 +1944,373 @@ __device__ __forceinline__ void q8_self_body(const SplitDecodeParams& p) {
         cursor_seek(p, ld, n_units, warp);
     }
 
-    uint32_t qa[D / 16][2];
-    int64_t qa_unit = -1;
-    uint32_t C = 0;  // chunks consumed
-    uint32_t X = 0;  // exchanges
-    bool stop = false;
-    constexpr float kLn2 = 0.69314718055994530942f;
-    for (int64_t u = blockIdx.x; u < n_units && !stop; u += gridDim.x) {
-        const Unit x = unit_at(p, u);
-        const int64_t part = (int64_t)x.s * p.part_stride + p.part_base + x.split_idx;
-        if (x.n_tiles == 0) {
-            if (warp == 0 && x.write_empty) {
-                for (int idx = lane; idx < p.group * D; idx += 32) {
-                    const int r = idx / D;
-                    const int d = idx - r * D;
-                    const int h = x.g * p.group + r;
-                    p.part_o[(part * H + h) * D + d] = 0.f;
-                    if (d == 0) p.part_lse[part * H + h] = -INFINITY;
-                }
-            }
-            continue;
-        }
-        if (qa_unit != u) {
-            if (KQ4)
-                load_q_frags_q4k<D>(p, x.s, x.g, gq, tq, qa);
-            else
-                load_q_frags<KVT, D>(p, x.s, x.g, gq, tq, qa);
-        }
-        float oacc[D / 16][4];
-        float m_run = -INFINITY, l_run = 0.f;
-#pragma unroll
-        for (int i = 0; i < D / 16; ++i) oacc[i][0] = oacc[i][1] = oacc[i][2] = oacc[i][3] = 0.f;
-        const int nch = unit_chunks(x);
-        for (int j = warp; j < nch; j += W, ++C) {
-            const int st = (int)(C % (uint32_t)S);
-            const bool ok = mbar_wait_bounded(smem_addr(&fb[st]), (C / (uint32_t)S) & 1u, abort_flag, p.wait_limit_ns);
-            if (!__all_sync(0xffffffffu, ok)) {
-                stop = true;
-                break;
-            }
-            const uint32_t mask = st_mask[warp * S + st] & 0xffffu;
-            const bool swz = st_swz[warp * S + st] != 0u;
-            const uint32_t kb = smem_addr(ring + st * Q::kChunkBytes);
-            const uint32_t vb = kb + Q::kSection;
-            const unsigned char* ks = sring + st * Q::kSclChunk;
-            const unsigned char* vs = ks + kChunkCells * Q::kSclBytes;
-            // (fragments are read straight from the stage: staging them in registers first
-            // measured slower here, the extra registers spill at this CTA count)
-            if (mask != 0u) {
-                if constexpr (VQ4) {
-                    if (swz)
-                        q4v_chunk<D, true, KQ4>(kb, vb, ks, vs, mask, lane, qa, oacc, m_run, l_run, p.scale_log2);
-                    else
-                        q4v_chunk<D, false, KQ4>(kb, vb, ks, vs, mask, lane, qa, oacc, m_run, l_run, p.scale_log2);
-                } else {
-                    if (swz)
-                        q8_chunk_swz<D>(kb, vb, ks, vs, mask, lane, qa, oacc, m_run, l_run, p.scale_log2);
-                    else
-                        consume_tile<KVT, D, false, Q::kPlane>(kb, vb, ks, vs, mask, 0, lane, qa, oacc, m_run,
-                                                               l_run, p.scale_log2);
-                }
-            }
-            // refill the stage just read with the chunk S ahead (every lane's reads are done)
-            __syncwarp();
-            if (ld.u < n_units) {
-                fence_proxy_async();
-                issue(ld, st, 0u);
-                ++L;
-                ld.j += W;
-                cursor_seek(p, ld, n_units, warp);
-            }
-        }
-        if (stop) break;
-        l_run += __shfl_xor_sync(0xffffffffu, l_run, 1);
-        l_run += __shfl_xor_sync(0xffffffffu, l_run, 2);
-        const int64_t un = u + gridDim.x;
-        if (un < n_units) {
-            const Unit y = unit_at(p, un);
-            if (y.n_tiles > 0) {
-                if (KQ4)
-                    load_q_frags_q4k<D>(p, y.s, y.g, gq, tq, qa);
-                else
-                    load_q_frags<KVT, D>(p, y.s, y.g, gq, tq, qa);
-                qa_unit = un;
-            }
-        }
-        if constexpr (W > 1) {
-            if (warp > 0) {
-                if (X > 0) {
-                    const bool ok = mbar_wait_bounded(smem_addr(&xchg_bar[1]), (X - 1) & 1u, abort_flag, p.wait_limit_ns);
-                    if (!__all_sync(0xffffffffu, ok)) break;
-                }
-                unsigned char* slot = xchg + (warp - 1) * Q::kXchgSlot;
-                float4* xo = reinterpret_cast<float4*>(slot);
-                float* xm = reinterpret_cast<float*>(xo + (D / 16) * 32);
-                if (tq == 0) {
-                    xm[gq] = m_run;
-                    xm[8 + gq] = l_run;
-                }
-#pragma unroll
-                for (int mt = 0; mt < D / 16; ++mt)
-                    xo[mt * 32 + lane] = make_float4(oacc[mt][0], oacc[mt][1], oacc[mt][2], oacc[mt][3]);
-                __syncwarp();
-                mbar_arrive(smem_addr(&xchg_bar[0]));
-                ++X;
-                continue;
-            }
-            const bool ok = mbar_wait_bounded(smem_addr(&xchg_bar[0]), X & 1u, abort_flag, p.wait_limit_ns);
-            if (!__all_sync(0xffffffffu, ok)) break;
-        }
-        // warp 0: combine the W warps' (max, sum, O) for rows 2tq, 2tq+1 and write the partial
-        float mw[W][2], lw[W][2];
-#pragma unroll
-        for (int e = 0; e < 2; ++e) {
-            mw[0][e] = __shfl_sync(0xffffffffu, m_run, 8 * tq + 4 * e);
-            lw[0][e] = __shfl_sync(0xffffffffu, l_run, 8 * tq + 4 * e);
-#pragma unroll
-            for (int w = 1; w < W; ++w) {
-                const float* xm = reinterpret_cast<const float*>(xchg + (w - 1) * Q::kXchgSlot + (D / 16) * 32 * 16);
-                mw[w][e] = xm[2 * tq + e];
-                lw[w][e] = xm[8 + 2 * tq + e];
-            }
-        }
-        float fw[W][2], inv[2], lse[2];
-#pragma unroll
-        for (int e = 0; e < 2; ++e) {
-            float M = mw[0][e];
-#pragma unroll
-            for (int w = 1; w < W; ++w) M = fmaxf(M, mw[w][e]);
-            float den = 0.f;
-#pragma unroll
-            for (int w = 0; w < W; ++w) {
-                fw[w][e] = (mw[w][e] == -INFINITY) ? 0.f : fast_exp2(mw[w][e] - M);
-                den = fmaf(lw[w][e], fw[w][e], den);
-            }
-            const bool have = M != -INFINITY && den > 0.f;
-            inv[e] = have ? 1.f / den : 0.f;
-            lse[e] = have ? (M + fast_log2(den)) * kLn2 : -INFINITY;
-        }
-#pragma unroll
-        for (int mt = 0; mt < D / 16; ++mt) {
-            float o0 = oacc[mt][0] * fw[0][0], o1 = oacc[mt][1] * fw[0][1];
-            float o2 = oacc[mt][2] * fw[0][0], o3 = oacc[mt][3] * fw[0][1];
-#pragma unroll
-            for (int w = 1; w < W; ++w) {
-                const float4 t = reinterpret_cast<const float4*>(xchg + (w - 1) * Q::kXchgSlot)[mt * 32 + lane];
-                o0 = fmaf(t.x, fw[w][0], o0);
-                o1 = fmaf(t.y, fw[w][1], o1);
-                o2 = fmaf(t.z, fw[w][0], o2);
-                o3 = fmaf(t.w, fw[w][1], o3);
-            }
-            oacc[mt][0] = o0 * inv[0];
-            oacc[mt][1] = o1 * inv[1];
-            oacc[mt][2] = o2 * inv[0];
-            oacc[mt][3] = o3 * inv[1];
-        }
-        if constexpr (W > 1) {
-            __syncwarp();
-            mbar_arrive(smem_addr(&xchg_bar[1]));
-        }
-#pragma unroll
-        for (int e = 0; e < 2; ++e) {
-            const int r = 2 * tq + e;
-            if (r < p.group) {
-                float* orow = p.part_o + (part * H + x.g * p.group + r) * D;
-#pragma unroll
-                for (int b = 0; b < D / 32; ++b) {
-                    if constexpr (VQ4) {
-                        // 4-bit V: m-tile 2b holds dims 32b + 2gq (+1), m-tile 2b+1 dims 32b + 16 + 2gq (+1)
-                        *reinterpret_cast<float2*>(orow + 32 * b + 2 * gq) = make_float2(oacc[2 * b][e], oacc[2 * b][2 + e]);
-                        *reinterpret_cast<float2*>(orow + 32 * b + 16 + 2 * gq) =
-                            make_float2(oacc[2 * b + 1][e], oacc[2 * b + 1][2 + e]);
-                    } else {
-                        *reinterpret_cast<float4*>(orow + 32 * b + 4 * gq) =
-                            make_float4(oacc[2 * b][e], oacc[2 * b][2 + e], oacc[2 * b + 1][e], oacc[2 * b + 1][2 + e]);
+    if constexpr (MQ) {
+        // ---- causal multi-query consumers: 16 query rows (token r / G, head g G + r % G) ----
+        const int GQ = p.group, NQ = p.n_q;
+        const int rows = GQ * NQ;
+        const int64_t HR = (int64_t)NQ * H;  // partial rows per (sequence, split)
+        uint32_t qa[D / 16][4];
+        int64_t qa_unit = -1;
+        uint32_t C = 0, X = 0;
+        bool stop = false;
+        constexpr float kLn2 = 0.69314718055994530942f;
+        for (int64_t u = blockIdx.x; u < n_units && !stop; u += gridDim.x) {
+            const Unit x = unit_at(p, u);
+            const int64_t part = (int64_t)x.s * p.part_stride + p.part_base + x.split_idx;
+            if (x.n_tiles == 0) {
+                if (warp == 0 && x.write_empty) {
+                    for (int idx = lane; idx < rows * D; idx += 32) {
+                        const int r = idx / D;
+                        const int d = idx - r * D;
+                        const int64_t row = (int64_t)(r / GQ) * H + x.g * GQ + r % GQ;
+                        p.part_o[(part * HR + row) * D + d] = 0.f;
+                        if (d == 0) p.part_lse[part * HR + row] = -INFINITY;
                     }
                 }
-                if (gq == 0) p.part_lse[part * H + x.g * p.group + r] = lse[e];
+                continue;
             }
+            if (qa_unit != u) load_q_frags_mq_q8<D>(p, x.s, x.g, gq, tq, qa);
+            float oacc[2][D / 16][4];
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                for (int i = 0; i < D / 16; ++i) oacc[nt][i][0] = oacc[nt][i][1] = oacc[nt][i][2] = oacc[nt][i][3] = 0.f;
+            float m_run[2] = {-INFINITY, -INFINITY}, l_run[2] = {0.f, 0.f};
+            // causal limit (logical position, exclusive) of the lane's rows gq and gq + 8
+            const int64_t lim_row[2] = {x.len - NQ + 1 + gq / GQ, x.len - NQ + 1 + (gq + 8) / GQ};
+            const int nch = unit_chunks(x);
+            for (int j = warp; j < nch; j += W, ++C) {
+                const int st = (int)(C % (uint32_t)S);
+                const bool ok = mbar_wait_bounded(smem_addr(&fb[st]), (C / (uint32_t)S) & 1u, abort_flag, p.wait_limit_ns);
+                if (!__all_sync(0xffffffffu, ok)) {
+                    stop = true;
+                    break;
+                }
+                const uint32_t mask = st_mask[warp * S + st] & 0xffffu;
+                const bool swz = st_swz[warp * S + st] != 0u;
+                const uint32_t kb = smem_addr(ring + st * Q::kChunkBytes);
+                const uint32_t vb = kb + Q::kSection;
+                const unsigned char* ks = sring + st * Q::kSclChunk;
+                const unsigned char* vs = ks + kChunkCells * Q::kSclBytes;
+                if (mask != 0u) {
+                    const int64_t p0 = x.i0 + (int64_t)j * kChunkCells;
+                    int lim[2];
+#pragma unroll
+                    for (int hh = 0; hh < 2; ++hh) {
+                        const int64_t rel = lim_row[hh] - p0;
+                        lim[hh] = rel < 0 ? 0 : (rel > kChunkCells ? kChunkCells : (int)rel);
+                    }
+                    if (swz)
+                        q8_mq_chunk<D, true>(kb, vb, ks, vs, mask, lane, lim, qa, oacc, m_run, l_run, p.scale_log2);
+                    else
+                        q8_mq_chunk<D, false>(kb, vb, ks, vs, mask, lane, lim, qa, oacc, m_run, l_run, p.scale_log2);
+                }
+                // refill the stage just read with the chunk S ahead (every lane's reads are done)
+                __syncwarp();
+                if (ld.u < n_units) {
+                    fence_proxy_async();
+                    issue(ld, st, 0u);
+                    ++L;
+                    ld.j += W;
+                    cursor_seek(p, ld, n_units, warp);
+                }
+            }
+            if (stop) break;
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) {
+                l_run[hh] += __shfl_xor_sync(0xffffffffu, l_run[hh], 1);
+                l_run[hh] += __shfl_xor_sync(0xffffffffu, l_run[hh], 2);
+            }
+            const int64_t un = u + gridDim.x;
+            if (un < n_units) {
+                const Unit y = unit_at(p, un);
+                if (y.n_tiles > 0) {
+                    load_q_frags_mq_q8<D>(p, y.s, y.g, gq, tq, qa);
+                    qa_unit = un;
+                }
+            }
+            if constexpr (W > 1) {
+                if (warp > 0) {
+                    if (X > 0) {
+                        const bool ok = mbar_wait_bounded(smem_addr(&xchg_bar[1]), (X - 1) & 1u, abort_flag, p.wait_limit_ns);
+                        if (!__all_sync(0xffffffffu, ok)) break;
+                    }
+                    unsigned char* slot = xchg + (warp - 1) * Q::kXchgSlot;
+                    float4* xo = reinterpret_cast<float4*>(slot);
+                    float* xm = reinterpret_cast<float*>(xo + 2 * (D / 16) * 32);
+                    if (tq == 0) {
+                        xm[gq] = m_run[0];
+                        xm[8 + gq] = m_run[1];
+                        xm[16 + gq] = l_run[0];
+                        xm[24 + gq] = l_run[1];
+                    }
+#pragma unroll
+                    for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                        for (int mt = 0; mt < D / 16; ++mt)
+                            xo[(nt * (D / 16) + mt) * 32 + lane] =
+                                make_float4(oacc[nt][mt][0], oacc[nt][mt][1], oacc[nt][mt][2], oacc[nt][mt][3]);
+                    __syncwarp();
+                    mbar_arrive(smem_addr(&xchg_bar[0]));
+                    ++X;
+                    continue;
+                }
+                const bool ok = mbar_wait_bounded(smem_addr(&xchg_bar[0]), X & 1u, abort_flag, p.wait_limit_ns);
+                if (!__all_sync(0xffffffffu, ok)) break;
+            }
+            // warp 0: combine the W warps' (max, sum, O) of query rows 8nt + 2tq + e, write them
+            float fw[W][2][2], inv[2][2], lse[2][2];
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    const int r = 8 * nt + 2 * tq + e;
+                    float mw[W], lw[W];
+                    mw[0] = __shfl_sync(0xffffffffu, m_run[nt], 8 * tq + 4 * e);
+                    lw[0] = __shfl_sync(0xffffffffu, l_run[nt], 8 * tq + 4 * e);
+#pragma unroll
+                    for (int w = 1; w < W; ++w) {
+                        const float* xm = reinterpret_cast<const float*>(xchg + (w - 1) * Q::kXchgSlot +
+                                                                         2 * (D / 16) * 32 * 16);
+                        mw[w] = xm[r];
+                        lw[w] = xm[16 + r];
+                    }
+                    float M = mw[0];
+#pragma unroll
+                    for (int w = 1; w < W; ++w) M = fmaxf(M, mw[w]);
+                    float den = 0.f;
+#pragma unroll
+                    for (int w = 0; w < W; ++w) {
+                        fw[w][nt][e] = (mw[w] == -INFINITY) ? 0.f : fast_exp2(mw[w] - M);
+                        den = fmaf(lw[w], fw[w][nt][e], den);
+                    }
+                    const bool have = M != -INFINITY && den > 0.f;
+                    inv[nt][e] = have ? 1.f / den : 0.f;
+                    lse[nt][e] = have ? (M + fast_log2(den)) * kLn2 : -INFINITY;
+                }
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                for (int mt = 0; mt < D / 16; ++mt) {
+                    float o0 = oacc[nt][mt][0] * fw[0][nt][0], o1 = oacc[nt][mt][1] * fw[0][nt][1];
+                    float o2 = oacc[nt][mt][2] * fw[0][nt][0], o3 = oacc[nt][mt][3] * fw[0][nt][1];
+#pragma unroll
+                    for (int w = 1; w < W; ++w) {
+                        const float4 t = reinterpret_cast<const float4*>(xchg + (w - 1) * Q::kXchgSlot)
+                            [(nt * (D / 16) + mt) * 32 + lane];
+                        o0 = fmaf(t.x, fw[w][nt][0], o0);
+                        o1 = fmaf(t.y, fw[w][nt][1], o1);
+                        o2 = fmaf(t.z, fw[w][nt][0], o2);
+                        o3 = fmaf(t.w, fw[w][nt][1], o3);
+                    }
+                    oacc[nt][mt][0] = o0 * inv[nt][0];
+                    oacc[nt][mt][1] = o1 * inv[nt][1];
+                    oacc[nt][mt][2] = o2 * inv[nt][0];
+                    oacc[nt][mt][3] = o3 * inv[nt][1];
+                }
+            if constexpr (W > 1) {
+                __syncwarp();
+                mbar_arrive(smem_addr(&xchg_bar[1]));
+            }
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    const int r = 8 * nt + 2 * tq + e;
+                    if (r < rows) {
+                        const int64_t row = (int64_t)(r / GQ) * H + x.g * GQ + r % GQ;
+                        float* orow = p.part_o + (part * HR + row) * D;
+#pragma unroll
+                        for (int b = 0; b < D / 32; ++b)
+                            *reinterpret_cast<float4*>(orow + 32 * b + 4 * gq) = make_float4(
+                                oacc[nt][2 * b][e], oacc[nt][2 * b][2 + e], oacc[nt][2 * b + 1][e], oacc[nt][2 * b + 1][2 + e]);
+                        if (gq == 0) p.part_lse[part * HR + row] = lse[nt][e];
+                    }
+                }
+            ++X;
         }
-        ++X;
+    } else {
+        uint32_t qa[D / 16][2];
+        int64_t qa_unit = -1;
+        uint32_t C = 0;  // chunks consumed
+        uint32_t X = 0;  // exchanges
+        bool stop = false;
+        constexpr float kLn2 = 0.69314718055994530942f;
+        for (int64_t u = blockIdx.x; u < n_units && !stop; u += gridDim.x) {
+            const Unit x = unit_at(p, u);
+            const int64_t part = (int64_t)x.s * p.part_stride + p.part_base + x.split_idx;
+            if (x.n_tiles == 0) {
+                if (warp == 0 && x.write_empty) {
+                    for (int idx = lane; idx < p.group * D; idx += 32) {
+                        const int r = idx / D;
+                        const int d = idx - r * D;
+                        const int h = x.g * p.group + r;
+                        p.part_o[(part * H + h) * D + d] = 0.f;
+                        if (d == 0) p.part_lse[part * H + h] = -INFINITY;
+                    }
+                }
+                continue;
+            }
+            if (qa_unit != u) {
+                if (KQ4)
+                    load_q_frags_q4k<D>(p, x.s, x.g, gq, tq, qa);
+                else
+                    load_q_frags<KVT, D>(p, x.s, x.g, gq, tq, qa);
+            }
+            float oacc[D / 16][4];
+            float m_run = -INFINITY, l_run = 0.f;
+#pragma unroll
+            for (int i = 0; i < D / 16; ++i) oacc[i][0] = oacc[i][1] = oacc[i][2] = oacc[i][3] = 0.f;
+            const int nch = unit_chunks(x);
+            for (int j = warp; j < nch; j += W, ++C) {
+                const int st = (int)(C % (uint32_t)S);
+                const bool ok = mbar_wait_bounded(smem_addr(&fb[st]), (C / (uint32_t)S) & 1u, abort_flag, p.wait_limit_ns);
+                if (!__all_sync(0xffffffffu, ok)) {
+                    stop = true;
+                    break;
+                }
+                const uint32_t mask = st_mask[warp * S + st] & 0xffffu;
+                const bool swz = st_swz[warp * S + st] != 0u;
+                const uint32_t kb = smem_addr(ring + st * Q::kChunkBytes);
+                const uint32_t vb = kb + Q::kSection;
+                const unsigned char* ks = sring + st * Q::kSclChunk;
+                const unsigned char* vs = ks + kChunkCells * Q::kSclBytes;
+                // (fragments are read straight from the stage: staging them in registers first
+                // measured slower here, the extra registers spill at this CTA count)
+                if (mask != 0u) {
+                    if constexpr (VQ4) {
+                        if (swz)
+                            q4v_chunk<D, true, KQ4>(kb, vb, ks, vs, mask, lane, qa, oacc, m_run, l_run, p.scale_log2);
+                        else
+                            q4v_chunk<D, false, KQ4>(kb, vb, ks, vs, mask, lane, qa, oacc, m_run, l_run, p.scale_log2);
+                    } else {
+                        if (swz)
+                            q8_chunk_swz<D>(kb, vb, ks, vs, mask, lane, qa, oacc, m_run, l_run, p.scale_log2);
+                        else
+                            consume_tile<KVT, D, false, Q::kPlane>(kb, vb, ks, vs, mask, 0, lane, qa, oacc, m_run,
+                                                                   l_run, p.scale_log2);
+                    }
+                }
+                // refill the stage just read with the chunk S ahead (every lane's reads are done)
+                __syncwarp();
+                if (ld.u < n_units) {
+                    fence_proxy_async();
+                    issue(ld, st, 0u);
+                    ++L;
+                    ld.j += W;
+                    cursor_seek(p, ld, n_units, warp);
+                }
+            }
+            if (stop) break;
+            l_run += __shfl_xor_sync(0xffffffffu, l_run, 1);
+            l_run += __shfl_xor_sync(0xffffffffu, l_run, 2);
+            const int64_t un = u + gridDim.x;
+            if (un < n_units) {
+                const Unit y = unit_at(p, un);
+                if (y.n_tiles > 0) {
+                    if (KQ4)
+                        load_q_frags_q4k<D>(p, y.s, y.g, gq, tq, qa);
+                    else
+                        load_q_frags<KVT, D>(p, y.s, y.g, gq, tq, qa);
+                    qa_unit = un;
+                }
+            }
+            if constexpr (W > 1) {
+                if (warp > 0) {
+                    if (X > 0) {
+                        const bool ok = mbar_wait_bounded(smem_addr(&xchg_bar[1]), (X - 1) & 1u, abort_flag, p.wait_limit_ns);
+                        if (!__all_sync(0xffffffffu, ok)) break;
+                    }
+                    unsigned char* slot = xchg + (warp - 1) * Q::kXchgSlot;
+                    float4* xo = reinterpret_cast<float4*>(slot);
+                    float* xm = reinterpret_cast<float*>(xo + (D / 16) * 32);
+                    if (tq == 0) {
+                        xm[gq] = m_run;
+                        xm[8 + gq] = l_run;
+                    }
+#pragma unroll
+                    for (int mt = 0; mt < D / 16; ++mt)
+                        xo[mt * 32 + lane] = make_float4(oacc[mt][0], oacc[mt][1], oacc[mt][2], oacc[mt][3]);
+                    __syncwarp();
+                    mbar_arrive(smem_addr(&xchg_bar[0]));
+                    ++X;
+                    continue;
+                }
+                const bool ok = mbar_wait_bounded(smem_addr(&xchg_bar[0]), X & 1u, abort_flag, p.wait_limit_ns);
+                if (!__all_sync(0xffffffffu, ok)) break;
+            }
+            // warp 0: combine the W warps' (max, sum, O) for rows 2tq, 2tq+1 and write the partial
+            float mw[W][2], lw[W][2];
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                mw[0][e] = __shfl_sync(0xffffffffu, m_run, 8 * tq + 4 * e);
+                lw[0][e] = __shfl_sync(0xffffffffu, l_run, 8 * tq + 4 * e);
+#pragma unroll
+                for (int w = 1; w < W; ++w) {
+                    const float* xm = reinterpret_cast<const float*>(xchg + (w - 1) * Q::kXchgSlot + (D / 16) * 32 * 16);
+                    mw[w][e] = xm[2 * tq + e];
+                    lw[w][e] = xm[8 + 2 * tq + e];
+                }
+            }
+            float fw[W][2], inv[2], lse[2];
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                float M = mw[0][e];
+#pragma unroll
+                for (int w = 1; w < W; ++w) M = fmaxf(M, mw[w][e]);
+                float den = 0.f;
+#pragma unroll
+                for (int w = 0; w < W; ++w) {
+                    fw[w][e] = (mw[w][e] == -INFINITY) ? 0.f : fast_exp2(mw[w][e] - M);
+                    den = fmaf(lw[w][e], fw[w][e], den);
+                }
+                const bool have = M != -INFINITY && den > 0.f;
+                inv[e] = have ? 1.f / den : 0.f;
+                lse[e] = have ? (M + fast_log2(den)) * kLn2 : -INFINITY;
+            }
+#pragma unroll
+            for (int mt = 0; mt < D / 16; ++mt) {
+                float o0 = oacc[mt][0] * fw[0][0], o1 = oacc[mt][1] * fw[0][1];
+                float o2 = oacc[mt][2] * fw[0][0], o3 = oacc[mt][3] * fw[0][1];
+#pragma unroll
+                for (int w = 1; w < W; ++w) {
+                    const float4 t = reinterpret_cast<const float4*>(xchg + (w - 1) * Q::kXchgSlot)[mt * 32 + lane];
+                    o0 = fmaf(t.x, fw[w][0], o0);
+                    o1 = fmaf(t.y, fw[w][1], o1);
+                    o2 = fmaf(t.z, fw[w][0], o2);
+                    o3 = fmaf(t.w, fw[w][1], o3);
+                }
+                oacc[mt][0] = o0 * inv[0];
+                oacc[mt][1] = o1 * inv[1];
+                oacc[mt][2] = o2 * inv[0];
+                oacc[mt][3] = o3 * inv[1];
+            }
+            if constexpr (W > 1) {
+                __syncwarp();
+                mbar_arrive(smem_addr(&xchg_bar[1]));
+            }
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                const int r = 2 * tq + e;
+                if (r < p.group) {
+                    float* orow = p.part_o + (part * H + x.g * p.group + r) * D;
+#pragma unroll
+                    for (int b = 0; b < D / 32; ++b) {
+                        if constexpr (VQ4) {
+                            // 4-bit V: m-tile 2b holds dims 32b + 2gq (+1), m-tile 2b+1 dims 32b + 16 + 2gq (+1)
+                            *reinterpret_cast<float2*>(orow + 32 * b + 2 * gq) = make_float2(oacc[2 * b][e], oacc[2 * b][2 + e]);
+                            *reinterpret_cast<float2*>(orow + 32 * b + 16 + 2 * gq) =
+                                make_float2(oacc[2 * b + 1][e], oacc[2 * b + 1][2 + e]);
+                        } else {
+                            *reinterpret_cast<float4*>(orow + 32 * b + 4 * gq) =
+                                make_float4(oacc[2 * b][e], oacc[2 * b][2 + e], oacc[2 * b + 1][e], oacc[2 * b + 1][2 + e]);
+                        }
+                    }
+                    if (gq == 0) p.part_lse[part * H + x.g * p.group + r] = lse[e];
+                }
+            }
+            ++X;
+        }
     }
     if (__any_sync(0xffffffffu, bad) && lane == 0) atomicOr(p.status, KVATTN_DEVICE_BAD_PLAN_ENTRY);
     // Every wait above is bounded, so all warps get here; a timed-out wait left abort set.
@@ -1949,6 +2329,10 @@ __device__ __forceinline__ void q8_self_body(const SplitDecodeParams& p) {
 // four CTAs (eight computing warps, no spills; measured faster than four warps x two CTAs).
 constexpr int kQ8W128 = 4, kQ8S128 = 2, kQ8B128 = 4;
 constexpr int kQ8W256 = 2, kQ8S256 = 2, kQ8B256 = 4;
+// Q8_0 multi-query (head_dim 128, up to 16 query rows): two warps of up to 255 registers,
+// four CTAs per SM -- the two output tiles and the 16-row query fragments do not fit the
+// single-query kernel's 128 registers.
+constexpr int kQ8WMQ = 2, kQ8SMQ = 2, kQ8BMQ = 4;
 
 // One kernel per (KV type, head_dim), each with its own register budget.
 __global__ void __launch_bounds__(kThreads) split_decode_f16_d128(const __grid_constant__ SplitDecodeParams p) {
@@ -1978,6 +2362,10 @@ __global__ void __launch_bounds__(kQ8W256 * 32, kQ8B256)
     split_decode_q8q4_d256(const __grid_constant__ SplitDecodeParams p) {
     q8_self_body<256, kQ8W256, kQ8S256, true>(p);
 }
+__global__ void __launch_bounds__(kQ8WMQ * 32, kQ8BMQ)
+    split_decode_mq_q8_d128(const __grid_constant__ SplitDecodeParams p) {
+    q8_self_body<128, kQ8WMQ, kQ8SMQ, false, false, true>(p);
+}
 // Q4_0 keys and values.
 __global__ void __launch_bounds__(kQ8W128 * 32, kQ8B128)
     split_decode_q4_d128(const __grid_constant__ SplitDecodeParams p) {
@@ -1989,7 +2377,9 @@ __global__ void __launch_bounds__(kQ8W256 * 32, kQ8B256)
 }
 
 const void* kernel_for(int kv_type, int head_dim, bool mq = false) {
-    if (mq) return reinterpret_cast<const void*>(split_decode_mq_f16_d128);
+    if (mq)
+        return kv_type == KVATTN_KV_Q8_0 ? reinterpret_cast<const void*>(split_decode_mq_q8_d128)
+                                         : reinterpret_cast<const void*>(split_decode_mq_f16_d128);
     if (kv_type == KVATTN_KV_F16)
         return head_dim == 128 ? reinterpret_cast<const void*>(split_decode_f16_d128)
                                : reinterpret_cast<const void*>(split_decode_f16_d256);
@@ -2020,6 +2410,7 @@ int split_decode_stage_bytes(int kv_type, int head_dim) {
 // the end-of-unit exchange area and the stage ring.
 // Q8_0 kernels have a fixed geometry (n_stages is ignored for them).
 int split_decode_smem_bytes(int kv_type, int head_dim, int n_stages, bool mq) {
+    if (kv_type == KVATTN_KV_Q8_0 && mq) return q8_self_smem<128, kQ8WMQ, kQ8SMQ, false, false, true>();
     if (kv_type == KVATTN_KV_Q8_0)
         return head_dim == 128 ? q8_self_smem<128, kQ8W128, kQ8S128>() : q8_self_smem<256, kQ8W256, kQ8S256>();
     if (kv_type == KVATTN_KV_Q8_0_Q4_0)
@@ -2034,7 +2425,8 @@ int split_decode_smem_bytes(int kv_type, int head_dim, int n_stages, bool mq) {
     return kHeaderBytes + 1024 + xchg + n_stages * split_decode_stage_bytes(kv_type, head_dim);
 }
 
-int split_decode_block_threads(int kv_type, int head_dim) {
+int split_decode_block_threads(int kv_type, int head_dim, bool mq) {
+    if (kv_type == KVATTN_KV_Q8_0 && mq) return kQ8WMQ * 32;
     if (kv_type != KVATTN_KV_F16) return (head_dim == 128 ? kQ8W128 : kQ8W256) * 32;
     return kThreads;
 }
@@ -2048,7 +2440,7 @@ cudaError_t split_decode_occupancy(int kv_type, int head_dim, int n_stages, bool
     const void* fn = kernel_for(kv_type, head_dim, mq);
     cudaError_t err = set_smem_attr(fn);
     if (err != cudaSuccess) return err;
-    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks, fn, split_decode_block_threads(kv_type, head_dim),
+    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks, fn, split_decode_block_threads(kv_type, head_dim, mq),
                                                          split_decode_smem_bytes(kv_type, head_dim, n_stages, mq));
 }
 
@@ -2056,17 +2448,17 @@ cudaError_t launch_split_decode(const SplitDecodeParams& p, int kv_type, int hea
                                 cudaStream_t stream, bool pdl) {
     const bool mq = p.mq != 0;
     const void* fn = kernel_for(kv_type, head_dim, mq);
-    static std::once_flag once[64][9];
-    static cudaError_t attr_err[64][9];
+    static std::once_flag once[64][10];
+    static cudaError_t attr_err[64][10];
     int dev = 0;
     cudaError_t err = cudaGetDevice(&dev);
     if (err != cudaSuccess) return err;
-    const int which = mq ? 8 : 2 * kv_type + (head_dim == 256 ? 1 : 0);
+    const int which = mq ? (kv_type == KVATTN_KV_F16 ? 8 : 9) : 2 * kv_type + (head_dim == 256 ? 1 : 0);
     std::call_once(once[dev & 63][which], [&] { attr_err[dev & 63][which] = set_smem_attr(fn); });
     if (attr_err[dev & 63][which] != cudaSuccess) return attr_err[dev & 63][which];
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid_ctas, 1, 1);
-    cfg.blockDim = dim3((unsigned)split_decode_block_threads(kv_type, head_dim), 1, 1);
+    cfg.blockDim = dim3((unsigned)split_decode_block_threads(kv_type, head_dim, mq), 1, 1);
     cfg.dynamicSmemBytes = split_decode_smem_bytes(kv_type, head_dim, p.n_stages, mq);
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];

@@ -114,7 +114,7 @@ cudaError_t launch_tile_copy(const void* k_src, const void* v_src, void* k_dst, 
                              cudaStream_t stream);
 int split_decode_stage_bytes(int kv_type, int head_dim);
 int split_decode_smem_bytes(int kv_type, int head_dim, int n_stages, bool mq = false);
-int split_decode_block_threads(int kv_type, int head_dim);
+int split_decode_block_threads(int kv_type, int head_dim, bool mq = false);
 int split_decode_box_cells(int kv_type);
 int split_decode_max_stages();
 int split_decode_max_smem();

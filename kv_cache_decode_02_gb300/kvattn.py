@@ -67,8 +67,8 @@ lib.kvattn_decode_workspace_bytes.argtypes = [_I, _I, _I, _I64, _I]
 lib.kvattn_decode_workspace_bytes.restype = _SZ
 lib.kvattn_decode_multi_workspace_bytes.argtypes = [_I, _I, _I, _I, _I64, _I]
 lib.kvattn_decode_multi_workspace_bytes.restype = _SZ
-lib.kvattn_decode_multi.argtypes = [_P, _P, _P, _I, _I64, _P, _I64, _P, _I, _I64, _I, _I, _I, _I, _I, _F, _P, _P,
-                                    _P, _SZ, _P]
+lib.kvattn_decode_multi.argtypes = [_P, _P, _P, _P, _P, _I, _I64, _P, _I64, _P, _I, _I64, _I, _I, _I, _I, _I, _F,
+                                    _P, _P, _P, _SZ, _P]
 lib.kvattn_decode_multi.restype = _I
 lib.kvattn_select_split_for.argtypes = [_I, _I64, _I, _I64]
 lib.kvattn_select_split_for.restype = _I
@@ -170,11 +170,13 @@ def kvattn_decode_multi_workspace_bytes(n_seq, n_q, n_head, head_dim, max_len, s
     return lib.kvattn_decode_multi_workspace_bytes(n_seq, n_q, n_head, head_dim, max_len, split)
 
 
-def kvattn_decode_multi(q, k_cache, v_cache, kv_type, n_cells, cell_plan, plan_stride, seq_lens, n_seq, max_len,
-                        n_q, n_head, n_head_kv, head_dim, split, scale, out, lse, ws, ws_bytes, stream=None):
-    rc = lib.kvattn_decode_multi(_ptr(q), _ptr(k_cache), _ptr(v_cache), kv_type, n_cells, _ptr(cell_plan),
-                                 plan_stride, _ptr(seq_lens), n_seq, max_len, n_q, n_head, n_head_kv, head_dim,
-                                 split, scale, _ptr(out), _ptr(lse), _ptr(ws), ws_bytes, _stream(stream))
+def kvattn_decode_multi(q, k_cache, v_cache, k_scales, v_scales, kv_type, n_cells, cell_plan, plan_stride, seq_lens,
+                        n_seq, max_len, n_q, n_head, n_head_kv, head_dim, split, scale, out, lse, ws, ws_bytes,
+                        stream=None):
+    rc = lib.kvattn_decode_multi(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(k_scales), _ptr(v_scales), kv_type,
+                                 n_cells, _ptr(cell_plan), plan_stride, _ptr(seq_lens), n_seq, max_len, n_q, n_head,
+                                 n_head_kv, head_dim, split, scale, _ptr(out), _ptr(lse), _ptr(ws), ws_bytes,
+                                 _stream(stream))
     _check(rc, "kvattn_decode_multi")
 
 
@@ -360,8 +362,9 @@ def decode(q, k_cache, v_cache, seq_lens, *, split, max_len=None, cell_plan=None
 
 
 def decode_multi(q, k_cache, v_cache, seq_lens, *, split, max_len=None, cell_plan=None, scale=None, n_cells=None,
-                 out=None, lse=None, ws=None, stream=None):
-    """q: half [S][n_q][H][D] (cuda), f16 K/V as the C ABI describes.  Returns (out, lse)."""
+                 out=None, lse=None, ws=None, stream=None, k_scales=None, v_scales=None):
+    """q: half [S][n_q][H][D] (cuda); f16 K/V, or Q8_0 with k_scales / v_scales, as the C ABI
+    describes.  Returns (out, lse)."""
     import torch
     S, n_q, H, D = q.shape
     Hk = k_cache.shape[-2]
@@ -379,8 +382,9 @@ def decode_multi(q, k_cache, v_cache, seq_lens, *, split, max_len=None, cell_pla
     if ws is None:
         nbytes = kvattn_decode_multi_workspace_bytes(S, n_q, H, D, max_len, split)
         ws = torch.zeros(max(nbytes, 256), dtype=torch.uint8, device=q.device)
-    kvattn_decode_multi(q, k_cache, v_cache, KVATTN_KV_F16, n_cells, cell_plan, plan_stride, seq_lens, S, max_len,
-                        n_q, H, Hk, D, split, scale, out, lse, ws, ws.numel(), stream)
+    kv_type = KVATTN_KV_F16 if k_scales is None else KVATTN_KV_Q8_0
+    kvattn_decode_multi(q, k_cache, v_cache, k_scales, v_scales, kv_type, n_cells, cell_plan, plan_stride, seq_lens,
+                        S, max_len, n_q, H, Hk, D, split, scale, out, lse, ws, ws.numel(), stream)
     return out, lse
 
 

@@ -173,14 +173,16 @@ def test_window_tail_direct_validation(kvattn):
 def test_multi_query_limits(kvattn):
     """Checked on the host before any device work."""
     def call(**over):
-        a = dict(q=A, k=B, v=C, kv_type=0, n_cells=1024, plan=None, plan_stride=0, seq_lens=A + 4096, n_seq=1,
-                 max_len=1024, n_q=4, n_head=32, n_head_kv=8, head_dim=128, split=256, scale=0.0884, out=A + 8192,
-                 lse=A + 16384, ws=A + 65536, ws_bytes=1 << 30, stream=None)
+        a = dict(q=A, k=B, v=C, ks=None, vs=None, kv_type=0, n_cells=1024, plan=None, plan_stride=0,
+                 seq_lens=A + 4096, n_seq=1, max_len=1024, n_q=4, n_head=32, n_head_kv=8, head_dim=128, split=256,
+                 scale=0.0884, out=A + 8192, lse=A + 16384, ws=A + 65536, ws_bytes=1 << 30, stream=None)
         a.update(over)
         return kvattn.lib.kvattn_decode_multi(*a.values())
     assert call(n_q=9) == kvattn.KVATTN_ERR_UNSUPPORTED            # 4 x 9 = 36 rows > 32
     assert call(head_dim=256) == kvattn.KVATTN_ERR_UNSUPPORTED
-    assert call(kv_type=1) == kvattn.KVATTN_ERR_UNSUPPORTED
+    assert call(kv_type=1, ks=A, vs=A, n_q=5) == kvattn.KVATTN_ERR_UNSUPPORTED  # Q8_0: 20 rows > 16
+    assert call(kv_type=2, ks=A, vs=A, n_q=2) == kvattn.KVATTN_ERR_UNSUPPORTED  # Q4_0 values
+    assert call(kv_type=1) == kvattn.KVATTN_ERR_INVALID_ARG                   # Q8_0 without scales
     assert call(n_q=0) == kvattn.KVATTN_ERR_INVALID_ARG
     assert call(q=None) == kvattn.KVATTN_ERR_INVALID_ARG
     assert call(ws_bytes=1000) == kvattn.KVATTN_ERR_WORKSPACE

@@ -113,3 +113,81 @@ def test_speculative_verify_qwen3_layer(kvattn, n_q):
     torch.cuda.synchronize()
     wo, wl = oracle.decode_multi(oracle.decode_f16, q, lens, k, v)
     check(out, lse, wo, wl)
+
+
+def q8_cache(rng, shape):
+    *lead, D = shape
+    kq = rng.integers(-127, 128, shape, dtype=np.int8)
+    vq = rng.integers(-127, 128, shape, dtype=np.int8)
+    kd = rng.uniform(0.001, 0.02, tuple(lead) + (D // 32,)).astype(np.float16)
+    vd = rng.uniform(0.001, 0.02, tuple(lead) + (D // 32,)).astype(np.float16)
+    return kq, kd, vq, vd
+
+
+@pytest.mark.parametrize("n_q,G,Hk,lens,split", [
+    (1, 4, 2, [1000, 37], 128),
+    (2, 4, 2, [1000, 1], 128),          # sequence 1 shorter than n_q
+    (4, 4, 2, [777, 4, 3], 64),         # 16 rows per KV head
+    (8, 2, 4, [513, 300], 256),
+    (16, 1, 2, [100, 16], 32),          # MHA, 16 tokens
+    (3, 5, 2, [2049, 0], 512),          # 15 rows, an empty sequence
+])
+def test_multi_query_q8_0_contiguous(kvattn, n_q, G, Hk, lens, split):
+    """Q8_0 cache: the self-loading kernel with the whole 16-row M of the MMA."""
+    import torch
+    rng = np.random.default_rng(n_q * 100 + G + 7)
+    S, D = len(lens), 128
+    N = max(max(lens), 1)
+    H = G * Hk
+    q = rand_f16(rng, (S, n_q, H, D))
+    kq, kd, vq, vd = q8_cache(rng, (S, N, Hk, D))
+    out, lse = kvattn.decode_multi(dev(q), dev(kq), dev(vq), dev(np.array(lens, np.int32)), split=split,
+                                   n_cells=N, max_len=N, k_scales=dev(kd), v_scales=dev(vd))
+    torch.cuda.synchronize()
+    wo, wl = oracle.decode_multi(oracle.decode_q8_0, q, lens, kq, kd, vq, vd)
+    check(out, lse, wo, wl)
+
+
+def test_multi_query_q8_0_plan_with_holes(kvattn):
+    """Scattered and record-aligned plan entries with -1 holes over NaN-scaled cells."""
+    import torch
+    rng = np.random.default_rng(19)
+    Hk, G, n_q, D = 4, 4, 4, 128
+    H = Hk * G
+    pool = 30
+    n_cells = pool * 128
+    kq, kd, vq, vd = q8_cache(rng, (n_cells, Hk, D))
+    perm = rng.permutation(pool)
+    encoded, selected = [], []
+    for recs in (perm[:4], perm[4:5], perm[5:12]):
+        cells = (recs[:, None] * 128 + np.arange(128)[None]).reshape(-1)
+        sel = cells[rng.random(cells.size) >= 0.2]
+        encoded.append(sel.astype(np.int64)[rng.permutation(sel.size)])
+        selected.append(sel)
+    unused = np.setdiff1d(np.arange(n_cells), np.concatenate(selected))
+    kd[unused] = np.nan
+    vd[unused] = np.nan
+    plan, lens = kvattn.build_cell_plan(encoded, n_cells)
+    plan[0, 40:200] = plan[0, 40:200][rng.permutation(160)]  # no longer one physical run: per-row copies
+    q = rand_f16(rng, (3, n_q, H, D))
+    out, lse = kvattn.decode_multi(dev(q), dev(kq), dev(vq), dev(lens), split=128, cell_plan=dev(plan),
+                                   n_cells=n_cells, k_scales=dev(kd), v_scales=dev(vd))
+    torch.cuda.synchronize()
+    wo, wl = oracle.decode_multi(oracle.decode_q8_0, q, lens.tolist(), kq, kd, vq, vd, plan=plan)
+    check(out, lse, wo, wl)
+
+
+def test_multi_query_q8_0_one_token_equals_single_query(kvattn):
+    import torch
+    rng = np.random.default_rng(20)
+    S, N, H, Hk, D = 2, 3000, 32, 8, 128
+    q = rand_f16(rng, (S, 1, H, D))
+    kq, kd, vq, vd = q8_cache(rng, (S, N, Hk, D))
+    lens = dev(np.array([3000, 1234], np.int32))
+    mo, ml = kvattn.decode_multi(dev(q), dev(kq), dev(vq), lens, split=256, n_cells=N, max_len=N,
+                                 k_scales=dev(kd), v_scales=dev(vd))
+    so, sl = kvattn.decode(dev(q[:, 0]), dev(kq), dev(vq), lens, split=256, n_cells=N, max_len=N,
+                           k_scales=dev(kd), v_scales=dev(vd))
+    torch.cuda.synchronize()
+    assert np.max(np.abs(mo.cpu().numpy()[:, 0] - so.cpu().numpy())) <= 1e-4
+    assert np.max(np.abs(ml.cpu().numpy()[:, 0] - sl.cpu().numpy())) <= 1e-5
