@@ -349,8 +349,8 @@ int decode_impl(const void* q, const void* k_cache, const void* v_cache, const v
     const DecodeShape shape{n_seq, n_head, n_head_kv, head_dim, split, max_len};
     int st = check_shape(shape);
     if (st != KVATTN_OK) return st;
-    // multi-query: f16 up to 32 query rows per KV head, Q8_0 up to 16; head_dim 128
-    if (multi && (head_dim != 128 || (kv_type != KVATTN_KV_F16 && kv_type != KVATTN_KV_Q8_0) ||
+    // multi-query: f16 up to 32 query rows per KV head, the quantised caches up to 16; head_dim 128
+    if (multi && (head_dim != 128 || !valid_kv_type(kv_type) ||
                   (n_head / n_head_kv) * n_q > (kv_type == KVATTN_KV_F16 ? 32 : 16)))
         return KVATTN_ERR_UNSUPPORTED;
     if (q == nullptr || k_cache == nullptr || v_cache == nullptr || seq_lens == nullptr || ws == nullptr)

@@ -1471,9 +1471,10 @@ __device__ __forceinline__ void q4v_chunk(uint32_t kb, uint32_t vb, const unsign
     }
 }
 
-// Query fragments of the multi-query Q8_0 kernel: rows gq (qa[kk][0..1]) and gq + 8
-// (qa[kk][2..3]) of the KV head's G x n_q rows, in the Q8_0 element order of load_q_frags.
-template <int D>
+// Query fragments of the multi-query quantised kernels: rows gq (qa[kk][0..1]) and gq + 8
+// (qa[kk][2..3]) of the KV head's G x n_q rows, in the element order of load_q_frags (8-bit
+// keys) or load_q_frags_q4k (4-bit keys).
+template <int D, bool KQ4>
 __device__ __forceinline__ void load_q_frags_mq_q8(const SplitDecodeParams& p, int s, int g, int gq, int tq,
                                                    uint32_t (&qa)[D / 16][4]) {
     const int rows = p.group * p.n_q;
@@ -1487,28 +1488,39 @@ __device__ __forceinline__ void load_q_frags_mq_q8(const SplitDecodeParams& p, i
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
             const int d0 = 32 * (kk >> 1) + 16 * (kk & 1) + 4 * tq;
-            qa[kk][2 * half] = ok ? __ldg(qrow + d0 / 2) : 0u;
-            qa[kk][2 * half + 1] = ok ? __ldg(qrow + d0 / 2 + 1) : 0u;
+            const uint32_t w0 = ok ? __ldg(qrow + d0 / 2) : 0u;      // elements d0, d0+1
+            const uint32_t w1 = ok ? __ldg(qrow + d0 / 2 + 1) : 0u;  // elements d0+2, d0+3
+            qa[kk][2 * half] = KQ4 ? prmt_b32(w0, w1, 0x5410u) : w0;
+            qa[kk][2 * half + 1] = KQ4 ? prmt_b32(w0, w1, 0x7632u) : w1;
         }
     }
 }
 
-// One warp's 16-cell Q8_0 chunk for up to 16 query rows (multi-query decode): q.K with the
-// whole M = 16 of the MMA, an online softmax per row (row gq + 8 hh, causal limit lim[hh]
+// One warp's 16-cell quantised chunk for up to 16 query rows (multi-query decode): q.K with
+// the whole M = 16 of the MMA, an online softmax per row (row gq + 8 hh, causal limit lim[hh]
 // cells of the chunk), and P V into two N = 8 tiles that share every converted V fragment.
-// SWZ: the 128-byte-swizzled TMA layout (see q8_chunk_swz), else plain D-byte rows.
-template <int D, bool SWZ>
+// Keys 8-bit or 4-bit (KQ4), values 8-bit or 4-bit (VQ4), in the layouts of q8_chunk_swz and
+// q4v_chunk: SWZ the TMA boxes' swizzled layout, else plain rows.
+template <int D, bool SWZ, bool VQ4 = false, bool KQ4 = false>
 __device__ __forceinline__ void q8_mq_chunk(uint32_t kb, uint32_t vb, const unsigned char* ks,
                                             const unsigned char* vs, uint32_t mask, int lane, const int (&lim)[2],
                                             const uint32_t (&qa)[D / 16][4], float (&oacc)[2][D / 16][4],
                                             float (&m_run)[2], float (&l_run)[2], float scale_log2) {
     constexpr int kPlane = kChunkCells * 128;
     constexpr int kScl = D / 16;
+    constexpr int kHalfRow = D / 2;  // bytes of a 4-bit row
     const int gq = lane >> 2;
     const int tq = lane & 3;
-    const uint32_t ka = SWZ ? ((kb + 128u * gq + 4u * tq) | (16u * gq)) : (kb + (uint32_t)D * gq + 4u * tq);
+    uint32_t ka;
+    if (KQ4)
+        ka = SWZ ? ((kb + 64u * gq + 4u * tq) | (16u * ((gq >> 1) & 3))) : (kb + (uint32_t)kHalfRow * gq + 4u * tq);
+    else
+        ka = SWZ ? ((kb + 128u * gq + 4u * tq) | (16u * gq)) : (kb + (uint32_t)D * gq + 4u * tq);
     uint32_t va0, va1;
-    if (SWZ) {
+    if (VQ4) {
+        va0 = SWZ ? ((vb + 128u * tq + 2u * gq) | (16u * tq)) : (vb + (uint32_t)kHalfRow * (2 * tq) + 2u * gq);
+        va1 = 0u;
+    } else if (SWZ) {
         va0 = (vb + 256u * tq + 4u * (gq & 3)) | (16u * ((gq >> 2) ^ (2 * tq)));
         va1 = (vb + 256u * tq + 128u + 4u * (gq & 3)) | (16u * ((gq >> 2) ^ (2 * tq + 1)));
     } else {
@@ -1535,7 +1547,11 @@ __device__ __forceinline__ void q8_mq_chunk(uint32_t kb, uint32_t vb, const unsi
 #pragma unroll
     for (int b = 0; b < D / 32; ++b) {
         uint32_t a0, a1, rs;
-        if (SWZ) {
+        if (KQ4) {
+            a0 = SWZ ? (ka ^ (16u * b)) : (ka + 16u * b);
+            a1 = 0u;
+            rs = SWZ ? 512u : 8u * kHalfRow;
+        } else if (SWZ) {
             const uint32_t pl = kPlane * (b >> 2);
             a0 = (ka ^ (32u * (b & 3))) + pl;
             a1 = (ka ^ (32u * (b & 3) + 16u)) + pl;
@@ -1547,11 +1563,23 @@ __device__ __forceinline__ void q8_mq_chunk(uint32_t kb, uint32_t vb, const unsi
         }
 #pragma unroll
         for (int j = 0; j < 2; ++j) {
-            const uint32_t w0 = lds32(a0 + rs * j) ^ 0x80808080u, w1 = lds32(a1 + rs * j) ^ 0x80808080u;
+            uint32_t b00, b01, b10, b11;  // B operands of the block's two MMAs
+            if (KQ4) {
+                const uint32_t w = lds32(a0 + rs * j), x = w >> 8;
+                b00 = q4x2_lo(w);
+                b01 = q4x2_lo(x);
+                b10 = q4x2_hi(w);
+                b11 = q4x2_hi(x);
+            } else {
+                const uint32_t w0 = lds32(a0 + rs * j) ^ 0x80808080u, w1 = lds32(a1 + rs * j) ^ 0x80808080u;
+                b00 = i8x2_lo(w0);
+                b01 = i8x2_hi(w0);
+                b10 = i8x2_lo(w1);
+                b11 = i8x2_hi(w1);
+            }
             float cb[4] = {0.f, 0.f, 0.f, 0.f};
-            mma_16816(cb, qa[2 * b][0], qa[2 * b][2], qa[2 * b][1], qa[2 * b][3], i8x2_lo(w0), i8x2_hi(w0));
-            mma_16816(cb, qa[2 * b + 1][0], qa[2 * b + 1][2], qa[2 * b + 1][1], qa[2 * b + 1][3], i8x2_lo(w1),
-                      i8x2_hi(w1));
+            mma_16816(cb, qa[2 * b][0], qa[2 * b][2], qa[2 * b][1], qa[2 * b][3], b00, b01);
+            mma_16816(cb, qa[2 * b + 1][0], qa[2 * b + 1][2], qa[2 * b + 1][1], qa[2 * b + 1][3], b10, b11);
 #pragma unroll
             for (int e = 0; e < 2; ++e) {
                 const uint32_t w = ksw[j][e][b >> 1];
@@ -1628,31 +1656,66 @@ __device__ __forceinline__ void q8_mq_chunk(uint32_t kb, uint32_t vb, const unsi
         }
 #pragma unroll
     for (int b = 0; b < D / 32; ++b) {
-        uint32_t vw[4];
-        if (SWZ) {
-            const uint32_t pl = kPlane * (b >> 2);
-            const uint32_t c0 = (va0 ^ (32u * (b & 3))) + pl;
-            const uint32_t c1 = (va1 ^ (32u * (b & 3))) + pl;
-            vw[0] = lds32(c0);
-            vw[1] = lds32(c1);
-            vw[2] = lds32(c0 + 1024u);
-            vw[3] = lds32(c1 + 1024u);
+        uint32_t A0[4], A1[4];  // V^T operands of m-tiles 2b and 2b + 1
+        if (VQ4) {
+            // 16-bit words of cells 2tq, 2tq+1, 2tq+8, 2tq+9 (layout as in q4v_chunk)
+            uint32_t c0, c1, c8, c9;
+            if (SWZ) {
+                const uint32_t x = va0 ^ (16u * b);
+                c0 = lds16(x);
+                c1 = lds16(x + 64u);
+                c8 = lds16(x + 512u);
+                c9 = lds16(x + 576u);
+            } else {
+                const uint32_t x = va0 + 16u * b;
+                c0 = lds16(x);
+                c1 = lds16(x + kHalfRow);
+                c8 = lds16(x + 8u * kHalfRow);
+                c9 = lds16(x + 9u * kHalfRow);
+            }
+            const uint32_t w01 = prmt_b32(c0, c1, 0x5410u), x01 = prmt_b32(c0, c1, 0x5511u);
+            const uint32_t w89 = prmt_b32(c8, c9, 0x5410u), x89 = prmt_b32(c8, c9, 0x5511u);
+            A0[0] = q4x2_lo(w01);
+            A0[1] = q4x2_lo(x01);
+            A0[2] = q4x2_lo(w89);
+            A0[3] = q4x2_lo(x89);
+            A1[0] = q4x2_hi(w01);
+            A1[1] = q4x2_hi(x01);
+            A1[2] = q4x2_hi(w89);
+            A1[3] = q4x2_hi(x89);
         } else {
-            const uint32_t c0 = va0 + 32u * b;
-            vw[0] = lds32(c0);
-            vw[1] = lds32(c0 + D);
-            vw[2] = lds32(c0 + 8u * D);
-            vw[3] = lds32(c0 + 9u * D);
+            uint32_t vw[4];
+            if (SWZ) {
+                const uint32_t pl = kPlane * (b >> 2);
+                const uint32_t c0 = (va0 ^ (32u * (b & 3))) + pl;
+                const uint32_t c1 = (va1 ^ (32u * (b & 3))) + pl;
+                vw[0] = lds32(c0);
+                vw[1] = lds32(c1);
+                vw[2] = lds32(c0 + 1024u);
+                vw[3] = lds32(c1 + 1024u);
+            } else {
+                const uint32_t c0 = va0 + 32u * b;
+                vw[0] = lds32(c0);
+                vw[1] = lds32(c0 + D);
+                vw[2] = lds32(c0 + 8u * D);
+                vw[3] = lds32(c0 + 9u * D);
+            }
+            const uint32_t f0 = vw[0] ^ 0x80808080u, f1 = vw[1] ^ 0x80808080u;
+            const uint32_t f2 = vw[2] ^ 0x80808080u, f3 = vw[3] ^ 0x80808080u;
+            const uint32_t u00 = prmt_b32(f0, f1, 0x5140u), u01 = prmt_b32(f0, f1, 0x7362u);
+            const uint32_t u10 = prmt_b32(f2, f3, 0x5140u), u11 = prmt_b32(f2, f3, 0x7362u);
+            A0[0] = i8x2_lo(u00);
+            A0[1] = i8x2_hi(u00);
+            A0[2] = i8x2_lo(u10);
+            A0[3] = i8x2_hi(u10);
+            A1[0] = i8x2_lo(u01);
+            A1[1] = i8x2_hi(u01);
+            A1[2] = i8x2_lo(u11);
+            A1[3] = i8x2_hi(u11);
         }
         const uint32_t sel = (b & 1) ? 0x7632u : 0x5410u;
         const uint32_t s01 = prmt_b32(vsw[0][b >> 1], vsw[1][b >> 1], sel);
         const uint32_t s89 = prmt_b32(vsw[2][b >> 1], vsw[3][b >> 1], sel);
-        const uint32_t f0 = vw[0] ^ 0x80808080u, f1 = vw[1] ^ 0x80808080u;
-        const uint32_t f2 = vw[2] ^ 0x80808080u, f3 = vw[3] ^ 0x80808080u;
-        const uint32_t u00 = prmt_b32(f0, f1, 0x5140u), u01 = prmt_b32(f0, f1, 0x7362u);
-        const uint32_t u10 = prmt_b32(f2, f3, 0x5140u), u11 = prmt_b32(f2, f3, 0x7362u);
-        const uint32_t A0[4] = {i8x2_lo(u00), i8x2_hi(u00), i8x2_lo(u10), i8x2_hi(u10)};
-        const uint32_t A1[4] = {i8x2_lo(u01), i8x2_hi(u01), i8x2_lo(u11), i8x2_hi(u11)};
 #pragma unroll
         for (int nt = 0; nt < 2; ++nt) {
             const uint32_t pb0 = hmul2_u32(ph[nt][0], s01), pb1 = hmul2_u32(ph[nt][1], s89);
@@ -1723,7 +1786,7 @@ __device__ __forceinline__ void cursor_seek(const SplitDecodeParams& p, ChunkCur
 template <int D, int W, int S, bool VQ4 = false, bool KQ4 = false, bool MQ = false>
 __device__ __forceinline__ void q8_self_body(const SplitDecodeParams& p) {
     static_assert(VQ4 || !KQ4, "4-bit keys come with 4-bit values");
-    static_assert(!MQ || (D == 128 && !VQ4), "multi-query: Q8_0, head_dim 128");
+    static_assert(!MQ || D == 128, "multi-query: head_dim 128");
     constexpr int KVT = KVATTN_KV_Q8_0;  // 8-bit keys' query fragment order (load_q_frags)
     using Q = Q8Self<D, VQ4, KQ4, MQ>;
     using G = Geom<KVT, D>;
@@ -1969,7 +2032,7 @@ __device__ __forceinline__ void q8_self_body(const SplitDecodeParams& p) {
                 }
                 continue;
             }
-            if (qa_unit != u) load_q_frags_mq_q8<D>(p, x.s, x.g, gq, tq, qa);
+            if (qa_unit != u) load_q_frags_mq_q8<D, KQ4>(p, x.s, x.g, gq, tq, qa);
             float oacc[2][D / 16][4];
 #pragma unroll
             for (int nt = 0; nt < 2; ++nt)
@@ -2001,9 +2064,11 @@ __device__ __forceinline__ void q8_self_body(const SplitDecodeParams& p) {
                         lim[hh] = rel < 0 ? 0 : (rel > kChunkCells ? kChunkCells : (int)rel);
                     }
                     if (swz)
-                        q8_mq_chunk<D, true>(kb, vb, ks, vs, mask, lane, lim, qa, oacc, m_run, l_run, p.scale_log2);
+                        q8_mq_chunk<D, true, VQ4, KQ4>(kb, vb, ks, vs, mask, lane, lim, qa, oacc, m_run, l_run,
+                                                       p.scale_log2);
                     else
-                        q8_mq_chunk<D, false>(kb, vb, ks, vs, mask, lane, lim, qa, oacc, m_run, l_run, p.scale_log2);
+                        q8_mq_chunk<D, false, VQ4, KQ4>(kb, vb, ks, vs, mask, lane, lim, qa, oacc, m_run, l_run,
+                                                        p.scale_log2);
                 }
                 // refill the stage just read with the chunk S ahead (every lane's reads are done)
                 __syncwarp();
@@ -2025,7 +2090,7 @@ __device__ __forceinline__ void q8_self_body(const SplitDecodeParams& p) {
             if (un < n_units) {
                 const Unit y = unit_at(p, un);
                 if (y.n_tiles > 0) {
-                    load_q_frags_mq_q8<D>(p, y.s, y.g, gq, tq, qa);
+                    load_q_frags_mq_q8<D, KQ4>(p, y.s, y.g, gq, tq, qa);
                     qa_unit = un;
                 }
             }
@@ -2121,9 +2186,18 @@ __device__ __forceinline__ void q8_self_body(const SplitDecodeParams& p) {
                         const int64_t row = (int64_t)(r / GQ) * H + x.g * GQ + r % GQ;
                         float* orow = p.part_o + (part * HR + row) * D;
 #pragma unroll
-                        for (int b = 0; b < D / 32; ++b)
-                            *reinterpret_cast<float4*>(orow + 32 * b + 4 * gq) = make_float4(
-                                oacc[nt][2 * b][e], oacc[nt][2 * b][2 + e], oacc[nt][2 * b + 1][e], oacc[nt][2 * b + 1][2 + e]);
+                        for (int b = 0; b < D / 32; ++b) {
+                            if constexpr (VQ4) {
+                                *reinterpret_cast<float2*>(orow + 32 * b + 2 * gq) =
+                                    make_float2(oacc[nt][2 * b][e], oacc[nt][2 * b][2 + e]);
+                                *reinterpret_cast<float2*>(orow + 32 * b + 16 + 2 * gq) =
+                                    make_float2(oacc[nt][2 * b + 1][e], oacc[nt][2 * b + 1][2 + e]);
+                            } else {
+                                *reinterpret_cast<float4*>(orow + 32 * b + 4 * gq) =
+                                    make_float4(oacc[nt][2 * b][e], oacc[nt][2 * b][2 + e], oacc[nt][2 * b + 1][e],
+                                                oacc[nt][2 * b + 1][2 + e]);
+                            }
+                        }
                         if (gq == 0) p.part_lse[part * HR + row] = lse[nt][e];
                     }
                 }
@@ -2366,6 +2440,14 @@ __global__ void __launch_bounds__(kQ8WMQ * 32, kQ8BMQ)
     split_decode_mq_q8_d128(const __grid_constant__ SplitDecodeParams p) {
     q8_self_body<128, kQ8WMQ, kQ8SMQ, false, false, true>(p);
 }
+__global__ void __launch_bounds__(kQ8WMQ * 32, kQ8BMQ)
+    split_decode_mq_q8q4_d128(const __grid_constant__ SplitDecodeParams p) {
+    q8_self_body<128, kQ8WMQ, kQ8SMQ, true, false, true>(p);
+}
+__global__ void __launch_bounds__(kQ8WMQ * 32, kQ8BMQ)
+    split_decode_mq_q4_d128(const __grid_constant__ SplitDecodeParams p) {
+    q8_self_body<128, kQ8WMQ, kQ8SMQ, true, true, true>(p);
+}
 // Q4_0 keys and values.
 __global__ void __launch_bounds__(kQ8W128 * 32, kQ8B128)
     split_decode_q4_d128(const __grid_constant__ SplitDecodeParams p) {
@@ -2377,9 +2459,12 @@ __global__ void __launch_bounds__(kQ8W256 * 32, kQ8B256)
 }
 
 const void* kernel_for(int kv_type, int head_dim, bool mq = false) {
-    if (mq)
-        return kv_type == KVATTN_KV_Q8_0 ? reinterpret_cast<const void*>(split_decode_mq_q8_d128)
-                                         : reinterpret_cast<const void*>(split_decode_mq_f16_d128);
+    if (mq) {
+        if (kv_type == KVATTN_KV_Q8_0) return reinterpret_cast<const void*>(split_decode_mq_q8_d128);
+        if (kv_type == KVATTN_KV_Q8_0_Q4_0) return reinterpret_cast<const void*>(split_decode_mq_q8q4_d128);
+        if (kv_type == KVATTN_KV_Q4_0) return reinterpret_cast<const void*>(split_decode_mq_q4_d128);
+        return reinterpret_cast<const void*>(split_decode_mq_f16_d128);
+    }
     if (kv_type == KVATTN_KV_F16)
         return head_dim == 128 ? reinterpret_cast<const void*>(split_decode_f16_d128)
                                : reinterpret_cast<const void*>(split_decode_f16_d256);
@@ -2411,6 +2496,8 @@ int split_decode_stage_bytes(int kv_type, int head_dim) {
 // Q8_0 kernels have a fixed geometry (n_stages is ignored for them).
 int split_decode_smem_bytes(int kv_type, int head_dim, int n_stages, bool mq) {
     if (kv_type == KVATTN_KV_Q8_0 && mq) return q8_self_smem<128, kQ8WMQ, kQ8SMQ, false, false, true>();
+    if (kv_type == KVATTN_KV_Q8_0_Q4_0 && mq) return q8_self_smem<128, kQ8WMQ, kQ8SMQ, true, false, true>();
+    if (kv_type == KVATTN_KV_Q4_0 && mq) return q8_self_smem<128, kQ8WMQ, kQ8SMQ, true, true, true>();
     if (kv_type == KVATTN_KV_Q8_0)
         return head_dim == 128 ? q8_self_smem<128, kQ8W128, kQ8S128>() : q8_self_smem<256, kQ8W256, kQ8S256>();
     if (kv_type == KVATTN_KV_Q8_0_Q4_0)
@@ -2426,7 +2513,7 @@ int split_decode_smem_bytes(int kv_type, int head_dim, int n_stages, bool mq) {
 }
 
 int split_decode_block_threads(int kv_type, int head_dim, bool mq) {
-    if (kv_type == KVATTN_KV_Q8_0 && mq) return kQ8WMQ * 32;
+    if (kv_type != KVATTN_KV_F16 && mq) return kQ8WMQ * 32;
     if (kv_type != KVATTN_KV_F16) return (head_dim == 128 ? kQ8W128 : kQ8W256) * 32;
     return kThreads;
 }
@@ -2448,12 +2535,12 @@ cudaError_t launch_split_decode(const SplitDecodeParams& p, int kv_type, int hea
                                 cudaStream_t stream, bool pdl) {
     const bool mq = p.mq != 0;
     const void* fn = kernel_for(kv_type, head_dim, mq);
-    static std::once_flag once[64][10];
-    static cudaError_t attr_err[64][10];
+    static std::once_flag once[64][12];
+    static cudaError_t attr_err[64][12];
     int dev = 0;
     cudaError_t err = cudaGetDevice(&dev);
     if (err != cudaSuccess) return err;
-    const int which = mq ? (kv_type == KVATTN_KV_F16 ? 8 : 9) : 2 * kv_type + (head_dim == 256 ? 1 : 0);
+    const int which = mq ? 8 + kv_type : 2 * kv_type + (head_dim == 256 ? 1 : 0);
     std::call_once(once[dev & 63][which], [&] { attr_err[dev & 63][which] = set_smem_attr(fn); });
     if (attr_err[dev & 63][which] != cudaSuccess) return attr_err[dev & 63][which];
     cudaLaunchConfig_t cfg = {};

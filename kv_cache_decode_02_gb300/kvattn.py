@@ -363,8 +363,9 @@ def decode(q, k_cache, v_cache, seq_lens, *, split, max_len=None, cell_plan=None
 
 def decode_multi(q, k_cache, v_cache, seq_lens, *, split, max_len=None, cell_plan=None, scale=None, n_cells=None,
                  out=None, lse=None, ws=None, stream=None, k_scales=None, v_scales=None):
-    """q: half [S][n_q][H][D] (cuda); f16 K/V, or Q8_0 with k_scales / v_scales, as the C ABI
-    describes.  Returns (out, lse)."""
+    """q: half [S][n_q][H][D] (cuda); f16 K/V, or a quantised cache with k_scales / v_scales
+    (the type inferred from the row widths as in decode), as the C ABI describes.  Returns
+    (out, lse)."""
     import torch
     S, n_q, H, D = q.shape
     Hk = k_cache.shape[-2]
@@ -382,7 +383,12 @@ def decode_multi(q, k_cache, v_cache, seq_lens, *, split, max_len=None, cell_pla
     if ws is None:
         nbytes = kvattn_decode_multi_workspace_bytes(S, n_q, H, D, max_len, split)
         ws = torch.zeros(max(nbytes, 256), dtype=torch.uint8, device=q.device)
-    kv_type = KVATTN_KV_F16 if k_scales is None else KVATTN_KV_Q8_0
+    if k_scales is None:
+        kv_type = KVATTN_KV_F16
+    elif k_cache.shape[-1] * 2 == D:
+        kv_type = KVATTN_KV_Q4_0
+    else:
+        kv_type = KVATTN_KV_Q8_0_Q4_0 if v_cache.shape[-1] * 2 == D else KVATTN_KV_Q8_0
     kvattn_decode_multi(q, k_cache, v_cache, k_scales, v_scales, kv_type, n_cells, cell_plan, plan_stride, seq_lens,
                         S, max_len, n_q, H, Hk, D, split, scale, out, lse, ws, ws.numel(), stream)
     return out, lse

@@ -181,7 +181,7 @@ def test_multi_query_limits(kvattn):
     assert call(n_q=9) == kvattn.KVATTN_ERR_UNSUPPORTED            # 4 x 9 = 36 rows > 32
     assert call(head_dim=256) == kvattn.KVATTN_ERR_UNSUPPORTED
     assert call(kv_type=1, ks=A, vs=A, n_q=5) == kvattn.KVATTN_ERR_UNSUPPORTED  # Q8_0: 20 rows > 16
-    assert call(kv_type=2, ks=A, vs=A, n_q=2) == kvattn.KVATTN_ERR_UNSUPPORTED  # Q4_0 values
+    assert call(kv_type=3, ks=A, vs=A, n_q=5) == kvattn.KVATTN_ERR_UNSUPPORTED  # Q4_0: 20 rows > 16
     assert call(kv_type=1) == kvattn.KVATTN_ERR_INVALID_ARG                   # Q8_0 without scales
     assert call(n_q=0) == kvattn.KVATTN_ERR_INVALID_ARG
     assert call(q=None) == kvattn.KVATTN_ERR_INVALID_ARG

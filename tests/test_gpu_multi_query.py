@@ -115,15 +115,29 @@ def test_speculative_verify_qwen3_layer(kvattn, n_q):
     check(out, lse, wo, wl)
 
 
-def q8_cache(rng, shape):
+def q8_cache(rng, shape, kind="q8"):
+    """Quantised K and V planes: kind q8 (int8 K and V), q8k_q4v (int8 K, 4-bit V) or q4kv."""
     *lead, D = shape
-    kq = rng.integers(-127, 128, shape, dtype=np.int8)
-    vq = rng.integers(-127, 128, shape, dtype=np.int8)
-    kd = rng.uniform(0.001, 0.02, tuple(lead) + (D // 32,)).astype(np.float16)
-    vd = rng.uniform(0.001, 0.02, tuple(lead) + (D // 32,)).astype(np.float16)
+    lead = tuple(lead)
+    if kind == "q4kv":
+        kq = rng.integers(0, 256, lead + (D // 2,), dtype=np.uint8)
+        kd = rng.uniform(0.001, 0.3, lead + (D // 32,)).astype(np.float16)
+    else:
+        kq = rng.integers(-127, 128, shape, dtype=np.int8)
+        kd = rng.uniform(0.001, 0.02, lead + (D // 32,)).astype(np.float16)
+    if kind == "q8":
+        vq = rng.integers(-127, 128, shape, dtype=np.int8)
+        vd = rng.uniform(0.001, 0.02, lead + (D // 32,)).astype(np.float16)
+    else:
+        vq = rng.integers(0, 256, lead + (D // 2,), dtype=np.uint8)
+        vd = rng.uniform(0.001, 0.3, lead + (D // 32,)).astype(np.float16)
     return kq, kd, vq, vd
 
 
+ORACLE = {"q8": oracle.decode_q8_0, "q8k_q4v": oracle.decode_q8_0_q4_0, "q4kv": oracle.decode_q4_0}
+
+
+@pytest.mark.parametrize("kind", ["q8", "q8k_q4v", "q4kv"])
 @pytest.mark.parametrize("n_q,G,Hk,lens,split", [
     (1, 4, 2, [1000, 37], 128),
     (2, 4, 2, [1000, 1], 128),          # sequence 1 shorter than n_q
@@ -132,23 +146,24 @@ def q8_cache(rng, shape):
     (16, 1, 2, [100, 16], 32),          # MHA, 16 tokens
     (3, 5, 2, [2049, 0], 512),          # 15 rows, an empty sequence
 ])
-def test_multi_query_q8_0_contiguous(kvattn, n_q, G, Hk, lens, split):
-    """Q8_0 cache: the self-loading kernel with the whole 16-row M of the MMA."""
+def test_multi_query_quantised_contiguous(kvattn, n_q, G, Hk, lens, split, kind):
+    """Quantised caches: the self-loading kernels with the whole 16-row M of the MMA."""
     import torch
     rng = np.random.default_rng(n_q * 100 + G + 7)
     S, D = len(lens), 128
     N = max(max(lens), 1)
     H = G * Hk
     q = rand_f16(rng, (S, n_q, H, D))
-    kq, kd, vq, vd = q8_cache(rng, (S, N, Hk, D))
+    kq, kd, vq, vd = q8_cache(rng, (S, N, Hk, D), kind)
     out, lse = kvattn.decode_multi(dev(q), dev(kq), dev(vq), dev(np.array(lens, np.int32)), split=split,
                                    n_cells=N, max_len=N, k_scales=dev(kd), v_scales=dev(vd))
     torch.cuda.synchronize()
-    wo, wl = oracle.decode_multi(oracle.decode_q8_0, q, lens, kq, kd, vq, vd)
+    wo, wl = oracle.decode_multi(ORACLE[kind], q, lens, kq, kd, vq, vd)
     check(out, lse, wo, wl)
 
 
-def test_multi_query_q8_0_plan_with_holes(kvattn):
+@pytest.mark.parametrize("kind", ["q8", "q8k_q4v", "q4kv"])
+def test_multi_query_quantised_plan_with_holes(kvattn, kind):
     """Scattered and record-aligned plan entries with -1 holes over NaN-scaled cells."""
     import torch
     rng = np.random.default_rng(19)
@@ -156,7 +171,7 @@ def test_multi_query_q8_0_plan_with_holes(kvattn):
     H = Hk * G
     pool = 30
     n_cells = pool * 128
-    kq, kd, vq, vd = q8_cache(rng, (n_cells, Hk, D))
+    kq, kd, vq, vd = q8_cache(rng, (n_cells, Hk, D), kind)
     perm = rng.permutation(pool)
     encoded, selected = [], []
     for recs in (perm[:4], perm[4:5], perm[5:12]):
@@ -173,16 +188,17 @@ def test_multi_query_q8_0_plan_with_holes(kvattn):
     out, lse = kvattn.decode_multi(dev(q), dev(kq), dev(vq), dev(lens), split=128, cell_plan=dev(plan),
                                    n_cells=n_cells, k_scales=dev(kd), v_scales=dev(vd))
     torch.cuda.synchronize()
-    wo, wl = oracle.decode_multi(oracle.decode_q8_0, q, lens.tolist(), kq, kd, vq, vd, plan=plan)
+    wo, wl = oracle.decode_multi(ORACLE[kind], q, lens.tolist(), kq, kd, vq, vd, plan=plan)
     check(out, lse, wo, wl)
 
 
-def test_multi_query_q8_0_one_token_equals_single_query(kvattn):
+@pytest.mark.parametrize("kind", ["q8", "q8k_q4v", "q4kv"])
+def test_multi_query_quantised_one_token_equals_single_query(kvattn, kind):
     import torch
     rng = np.random.default_rng(20)
     S, N, H, Hk, D = 2, 3000, 32, 8, 128
     q = rand_f16(rng, (S, 1, H, D))
-    kq, kd, vq, vd = q8_cache(rng, (S, N, Hk, D))
+    kq, kd, vq, vd = q8_cache(rng, (S, N, Hk, D), kind)
     lens = dev(np.array([3000, 1234], np.int32))
     mo, ml = kvattn.decode_multi(dev(q), dev(kq), dev(vq), lens, split=256, n_cells=N, max_len=N,
                                  k_scales=dev(kd), v_scales=dev(vd))
