@@ -348,6 +348,23 @@ def bench_workloads(K, torch, stream, peak):
                                                                  "plan_entries": int(plens.sum())})
     del kk, vv
 
+    # f16 head_dim 256 long context, the automatic split
+    w = inputs.F16_D256_LONG
+    kk = inputs.normal_f16_torch((2000 + w.number, 0), (w.n_cells, w.n_head_kv, w.head_dim), "cuda")
+    vv = inputs.normal_f16_torch((3000 + w.number, 0), (w.n_cells, w.n_head_kv, w.head_dim), "cuda")
+    q = torch.from_numpy(inputs.make_q(w)).cuda()
+    lens = torch.tensor(w.seq_lens, dtype=torch.int32, device="cuda")
+    sp = K.kvattn_select_split(0, 1, w.n_cells, w.n_head_kv, w.head_dim)
+    ws = K.decode_workspace(1, w.n_head, w.head_dim, w.n_cells, sp)
+    out = torch.empty((1, w.n_head, w.head_dim), dtype=torch.float32, device="cuda")
+    lse = torch.empty((1, w.n_head), dtype=torch.float32, device="cuda")
+    fn = lambda: K.kvattn_decode(q, kk, vv, None, None, 0, w.n_cells, None, 0, lens, 1, w.n_cells, w.n_head,
+                                 w.n_head_kv, w.head_dim, 0, 1 / math.sqrt(w.head_dim), out, lse, ws, ws.numel(),
+                                 stream)
+    fn()
+    add(w.name, w.n_cells * w.n_head_kv * w.head_dim * 4, timed(fn), {"split": sp})
+    del kk, vv
+
     # Q8_0 long context, head_dim 128 and 256; and Q8_0 keys with Q4_0 values
     for w in (inputs.Q8_LONG_D128, inputs.Q8_LONG_D256, inputs.Q8Q4_LONG_D128, inputs.Q8Q4_LONG_D256,
               inputs.Q4_LONG_D128, inputs.Q4_LONG_D256):

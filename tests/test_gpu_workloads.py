@@ -48,6 +48,18 @@ def test_multislot_plan_gqa6(kvattn):
     assert np.array_equal(desc.cpu().numpy(), po.descriptors(plan, lens, plan.shape[1], w.split, w.n_cells))
 
 
+def test_f16_head_dim_256_long_context(kvattn):
+    """65536 cells at head_dim 256 with the automatic split (the bench's configuration)."""
+    import torch
+    w = inputs.F16_D256_LONG
+    q = inputs.make_q(w)
+    k, v = inputs.make_kv_f16(w)
+    out, lse = kvattn.decode(dev(q), dev(k), dev(v), dev(np.array(w.seq_lens, np.int32)), split=0)
+    torch.cuda.synchronize()
+    wo, wl = oracle.decode_f16(q, k, v, list(w.seq_lens))
+    assert_close(out, lse, wo, wl)
+
+
 @pytest.mark.parametrize("w", [inputs.Q8_LONG_D128, inputs.Q8_LONG_D256], ids=lambda w: w.name)
 def test_q8_0_long_context(kvattn, w):
     import torch
