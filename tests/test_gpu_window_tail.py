@@ -179,3 +179,27 @@ def test_direct_tail_reads(kvattn, N, n_win, H, Hk, tail_split):
     torch.cuda.synchronize()
     wo, wl = oracle.decode_f16(q, k, v, [N])
     assert_close(out.view(1, H, 128), lse.view(1, H), wo, wl)
+
+
+@pytest.mark.parametrize("mode", ["staged", "direct"])
+def test_window_tail_head_dim_256(kvattn, mode):
+    """head_dim 256 (512-byte rows): a ragged last tile, GQA-2."""
+    import torch
+    rng = np.random.default_rng(31)
+    N, n_win, H, Hk, D = 3000, 500, 16, 8, 256
+    q, k, v = make(rng, N, n_win, H, Hk, D)
+    n_tail = N - n_win
+    k_tail = torch.from_numpy(k[:n_tail]).pin_memory()
+    v_tail = torch.from_numpy(v[:n_tail]).pin_memory()
+    if mode == "staged":
+        wt = kvattn.WindowTail()
+        out, lse = wt(dev(q[0]), dev(k[n_tail:]), dev(v[n_tail:]), k_tail, v_tail, split=128, tile_cells=384,
+                      tail_split=128, copy_stream=torch.cuda.Stream())
+        kvattn.kvattn_tail_wait(wt.ctx, 30000)
+        wt.close()
+    else:
+        out, lse = kvattn.window_tail_direct(dev(q[0]), dev(k[n_tail:]), dev(v[n_tail:]), k_tail, v_tail, split=128,
+                                             tail_split=128)
+    torch.cuda.synchronize()
+    wo, wl = oracle.decode_f16(q, k, v, [N])
+    assert_close(out.view(1, H, D), lse.view(1, H), wo, wl)
