@@ -120,7 +120,7 @@ int kvattn_build_cell_plan(const int64_t* cells, const int64_t* offsets, int n_s
  *             flags: 1 = no valid entry, 2 = linear (e - i constant over valid entries),
  *             4 = an entry outside [-1, n_cells) was seen, 8 = split starts at/after L.
  * Errors: INVALID_ARG (null pointers, n_seq < 0, split < 1, max_len < 0, n_cells < 1,
- * plan_stride < 1, more than 65535 sequences); CUDA.
+ * plan_stride < 1); CUDA.
  */
 int kvattn_build_descriptors(const int32_t* cell_plan, int64_t plan_stride,
                              const int32_t* seq_lens, int n_seq, int64_t max_len, int split,
@@ -182,6 +182,8 @@ int kvattn_select_split(int kv_type, int n_seq, int64_t max_len, int n_head_kv, 
  *           descriptors int32 {n_valid, lo, hi, flags} [n_seq][n_split] (n_split =
  *           ceil(max_len / split)) exactly as kvattn_build_descriptors computes them.
  *  stream   cudaStream_t.
+ *  Size limits (UNSUPPORTED beyond them): n_seq x n_head output rows and n_seq x
+ *  ceil(max_len / split) x n_head_kv work units each below 2^31.
  * Errors: INVALID_ARG, UNSUPPORTED, WORKSPACE (before any launch); CUDA.
  */
 int kvattn_decode(const void* q, const void* k_cache, const void* v_cache,

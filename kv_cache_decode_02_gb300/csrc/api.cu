@@ -176,7 +176,8 @@ int check_shape(const DecodeShape& s) {
     if (s.n_head / s.n_head_kv > kMaxGroup) return KVATTN_ERR_UNSUPPORTED;
     if (s.head_dim != 128 && s.head_dim != 256) return KVATTN_ERR_UNSUPPORTED;
     if (s.split % kTileCells != 0) return KVATTN_ERR_UNSUPPORTED;
-    if (s.n_seq > 65535) return KVATTN_ERR_UNSUPPORTED;
+    // merge rows (sequence, head) are numbered in 32 bits
+    if ((int64_t)s.n_seq * s.n_head > (int64_t)INT32_MAX) return KVATTN_ERR_UNSUPPORTED;
     // work units (sequence, split, KV head) are numbered in 32 bits on the device
     if ((s.max_len + s.split - 1) / s.split * s.n_head_kv * std::max(s.n_seq, 1) > (int64_t)INT32_MAX)
         return KVATTN_ERR_UNSUPPORTED;
@@ -280,7 +281,7 @@ int kvattn_build_cell_plan(const int64_t* cells, const int64_t* offsets, int n_s
 int kvattn_build_descriptors(const int32_t* cell_plan, int64_t plan_stride, const int32_t* seq_lens,
                              int n_seq, int64_t max_len, int split, int64_t n_cells, int32_t* desc,
                              void* stream) {
-    if (n_seq < 0 || split < 1 || max_len < 0 || n_cells < 1 || plan_stride < 1 || n_seq > 65535)
+    if (n_seq < 0 || split < 1 || max_len < 0 || n_cells < 1 || plan_stride < 1)
         return KVATTN_ERR_INVALID_ARG;
     const int64_t n_split = (max_len + split - 1) / split;
     if (n_seq == 0 || n_split == 0) return KVATTN_OK;
@@ -349,6 +350,7 @@ int decode_impl(const void* q, const void* k_cache, const void* v_cache, const v
     const DecodeShape shape{n_seq, n_head, n_head_kv, head_dim, split, max_len};
     int st = check_shape(shape);
     if (st != KVATTN_OK) return st;
+    if (multi && (int64_t)n_seq * n_q * n_head > (int64_t)INT32_MAX) return KVATTN_ERR_UNSUPPORTED;
     // multi-query: f16 up to 32 query rows per KV head, the quantised caches up to 16; head_dim 128
     if (multi && (head_dim != 128 || !valid_kv_type(kv_type) ||
                   (n_head / n_head_kv) * n_q > (kv_type == KVATTN_KV_F16 ? 32 : 16)))

@@ -284,10 +284,11 @@ __global__ void __launch_bounds__(kMergeThreads, 2) merge_kernel(const MergePara
 cudaError_t launch_merge(const MergeParams& params, cudaStream_t stream, bool pdl) {
     MergeParams p = params;
     if (p.head_dim > 256) p.all_written = 0;  // the one-round path holds two float4 per lane
-    const int rows = p.n_seq * p.n_rows;
+    const int64_t rows = (int64_t)p.n_seq * p.n_rows;  // one CTA per row, numbered in 32 bits
     if (rows == 0) return cudaSuccess;
+    if (rows > (int64_t)INT32_MAX) return cudaErrorInvalidValue;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(rows, 1, 1);
+    cfg.gridDim = dim3((unsigned)rows, 1, 1);
     cfg.blockDim = dim3(kMergeThreads, 1, 1);
     cfg.dynamicSmemBytes = kMergeWarps * p.head_dim * sizeof(float);
     cfg.stream = stream;

@@ -58,7 +58,7 @@ def call_decode(kvattn, a):
     (dict(head_dim=64), -2),
     (dict(head_dim=96), -2),
     (dict(split=48), -2),                  # not a multiple of the 32-cell tile
-    (dict(n_seq=70000), -2),               # more sequences than a grid dimension holds
+    (dict(n_seq=70_000_000), -2),          # (sequence, head) rows and work units beyond 32 bits
     (dict(split=-32), -1),                 # (split 0 selects the split: needs a device)
     (dict(q=None), -1),
     (dict(out=None), -1),

@@ -428,3 +428,25 @@ def test_calls_from_several_host_threads(kvattn):
     for (q, k, v, N), (o, l) in zip(cases, results):
         wo, wl = oracle.decode_f16(q, k, v, [N])
         assert np.max(np.abs(o - wo)) <= TOL_O and np.max(np.abs(l - wl)) <= 1e-4
+
+
+def test_more_than_65535_sequences(kvattn):
+    """70000 short sequences in one call (a batch far past the 16-bit grid limit of older
+    designs): units and merge rows are numbered in 32 bits; a sample of rows against the
+    oracle, the rest against the sequences' own properties (finite, empty where empty)."""
+    import torch
+    rng = np.random.default_rng(14)
+    S, N, H, Hk, D = 70000, 24, 2, 1, 128
+    lens = rng.integers(0, N + 1, S).astype(np.int32)
+    lens[:3] = [N, 0, 1]
+    k = rand_f16(rng, (S, N, Hk, D))
+    v = rand_f16(rng, (S, N, Hk, D))
+    q = rand_f16(rng, (S, H, D))
+    out, lse = kvattn.decode(dev(q), dev(k), dev(v), dev(lens), split=32, n_cells=N, max_len=N)
+    torch.cuda.synchronize()
+    o, l = out.cpu().numpy(), lse.cpu().numpy()
+    assert np.array_equal(np.isneginf(l), (lens == 0)[:, None].repeat(H, 1))
+    assert np.all(np.isfinite(o)) and np.all(o[lens == 0] == 0)
+    pick = np.concatenate([[0, 1, 2], rng.choice(S, 200, replace=False), [S - 1]])
+    wo, wl = oracle.decode_f16(q[pick], k[pick], v[pick], lens[pick].tolist())
+    assert_close(out[pick], lse[pick], wo, wl)
