@@ -348,6 +348,23 @@ def bench_workloads(K, torch, stream, peak):
                                                                  "plan_entries": int(plens.sum())})
     del kk, vv
 
+    # a serving batch: 64 sequences x 4096 cells in one call, the automatic split
+    w = inputs.BATCH64
+    S, N = w.n_seq, w.n_cells
+    kk = inputs.normal_f16_torch((2000 + w.number, 0), (S, N, w.n_head_kv, w.head_dim), "cuda")
+    vv = inputs.normal_f16_torch((3000 + w.number, 0), (S, N, w.n_head_kv, w.head_dim), "cuda")
+    q = torch.from_numpy(inputs.make_q(w)).cuda()
+    lens = torch.tensor(w.seq_lens, dtype=torch.int32, device="cuda")
+    sp = K.kvattn_select_split(0, S, N, w.n_head_kv, w.head_dim)
+    ws = K.decode_workspace(S, w.n_head, w.head_dim, N, sp)
+    out = torch.empty((S, w.n_head, w.head_dim), dtype=torch.float32, device="cuda")
+    lse = torch.empty((S, w.n_head), dtype=torch.float32, device="cuda")
+    fn = lambda: K.kvattn_decode(q, kk, vv, None, None, 0, N, None, 0, lens, S, N, w.n_head, w.n_head_kv,
+                                 w.head_dim, 0, 1 / math.sqrt(w.head_dim), out, lse, ws, ws.numel(), stream)
+    fn()
+    add(w.name, S * N * w.n_head_kv * w.head_dim * 4, timed(fn), {"split": sp, "n_seq": S})
+    del kk, vv
+
     # f16 head_dim 256 long context, the automatic split
     w = inputs.F16_D256_LONG
     kk = inputs.normal_f16_torch((2000 + w.number, 0), (w.n_cells, w.n_head_kv, w.head_dim), "cuda")

@@ -88,6 +88,10 @@ Q8Q4_LONG_D128 = Workload("q8_0_q4_0_n131072_d128", 8, 1, 131072, 32, 8, 128, 51
 Q8Q4_LONG_D256 = Workload("q8_0_q4_0_n131072_d256", 8, 1, 131072, 32, 8, 256, 512, kv_type="q8_0_q4_0",
                           seq_lens=(131072,))
 
+# A serving batch: 64 sequences of 4096 cells each through one call (Qwen3-8B-shaped heads, a
+# per-sequence cache), the automatic split.
+BATCH64 = Workload("qwen3_8b_batch64_n4096", 11, 64, 4096, 32, 8, 128, 0, seq_lens=(4096,) * 64)
+
 # head_dim 256 (as the global layers of the pages' Gemma-family model): 16/8 heads, 65536 cells,
 # the automatic split.
 F16_D256_LONG = Workload("f16_n65536_d256", 10, 1, 65536, 16, 8, 256, 0, seq_lens=(65536,))
@@ -99,7 +103,7 @@ Q4_LONG_D256 = Workload("q4_0_n131072_d256", 9, 1, 131072, 32, 8, 256, 512, kv_t
 WORKLOADS = {w.name: w for w in
              (TINY, QWEN3_8B_LAYER, MULTISLOT_PLAN, Q8_LONG_D128, Q8_LONG_D256, WINDOW_TAIL,
               STACK_TAIL_295MIB, STACK_TAIL_1815MIB, Q8Q4_LONG_D128, Q8Q4_LONG_D256, Q4_LONG_D128,
-              Q4_LONG_D256, F16_D256_LONG)}
+              Q4_LONG_D256, F16_D256_LONG, BATCH64)}
 
 
 def _rng(*seed) -> np.random.Generator:

@@ -48,6 +48,23 @@ def test_multislot_plan_gqa6(kvattn):
     assert np.array_equal(desc.cpu().numpy(), po.descriptors(plan, lens, plan.shape[1], w.split, w.n_cells))
 
 
+def test_serving_batch_of_64_sequences(kvattn):
+    """64 sequences x 4096 cells in one call with the automatic split (the bench's
+    configuration): a sample of sequences against the oracle."""
+    import torch
+    w = inputs.BATCH64
+    q = inputs.make_q(w)
+    rng = np.random.default_rng(2000 + w.number)
+    k = rng.standard_normal((w.n_seq, w.n_cells, w.n_head_kv, w.head_dim), dtype=np.float32).astype(np.float16)
+    v = rng.standard_normal((w.n_seq, w.n_cells, w.n_head_kv, w.head_dim), dtype=np.float32).astype(np.float16)
+    lens = np.array(w.seq_lens, np.int32)
+    out, lse = kvattn.decode(dev(q), dev(k), dev(v), dev(lens), split=0, n_cells=w.n_cells, max_len=w.n_cells)
+    torch.cuda.synchronize()
+    pick = np.array([0, 1, 17, 40, 63])
+    wo, wl = oracle.decode_f16(q[pick], k[pick], v[pick], lens[pick].tolist())
+    assert_close(out[pick], lse[pick], wo, wl)
+
+
 def test_f16_head_dim_256_long_context(kvattn):
     """65536 cells at head_dim 256 with the automatic split (the bench's configuration)."""
     import torch
