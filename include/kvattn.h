@@ -337,7 +337,9 @@ size_t kvattn_window_tail_workspace_bytes(int n_head, int n_head_kv, int head_di
  *  q          device half [n_head][head_dim].
  *  k_win, v_win  device half [n_win][n_head_kv][head_dim] -- the resident window.
  *  k_tail_host, v_tail_host  PINNED host half [n_tail][n_head_kv][head_dim] -- the older
- *             tail (cudaHostAlloc / cudaHostRegister memory).
+ *             tail (cudaHostAlloc / cudaHostRegister memory).  Pageable memory is accepted
+ *             but slow: its copies stage through the driver and are never recorded into a
+ *             graph.
  *  tile_cells tail cells per host-to-device tile (a positive multiple of tail_split);
  *             tiles are copied into two device staging slots, one tile ahead of the
  *             compute (double buffering), each copy ordered after the decode that last

@@ -866,6 +866,19 @@ int kvattn_decode_window_tail(kvattn_tail_ctx* ctx, const void* q, const void* k
             cudaGetLastError();  // not mapped: clear the query's error, copy on the copy engine
         }
     }
+    // Pageable (unregistered) tail memory still works through cudaMemcpyAsync, which then
+    // stages it through the driver, but such copies cannot be recorded into a graph.
+    bool tail_pinned = true;
+    for (const void* ptr : {k_tail_host, v_tail_host}) {
+        if (n_tail == 0 || ptr == nullptr) continue;
+        cudaPointerAttributes attr;
+        if (cudaPointerGetAttributes(&attr, ptr) != cudaSuccess) {
+            cudaGetLastError();
+            tail_pinned = false;
+        } else if (attr.type == cudaMemoryTypeUnregistered) {
+            tail_pinned = false;
+        }
+    }
 
     cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
     unsigned long long capture_id = 0;
@@ -880,7 +893,8 @@ int kvattn_decode_window_tail(kvattn_tail_ctx* ctx, const void* q, const void* k
     // across layers.
     const bool prefetch = (ctx->flags & KVATTN_TAIL_PREFETCH) != 0u;
     const bool carry = prefetch && ctx->carry_valid && ctx->carry_capture == capture_id;
-    const bool use_graph = !prefetch && use_tail_graph() && cap == cudaStreamCaptureStatusNone && fault < 0;
+    const bool use_graph =
+        !prefetch && tail_pinned && use_tail_graph() && cap == cudaStreamCaptureStatusNone && fault < 0;
     if (!use_graph) {
         const int slot0 = prefetch ? (int)(ctx->tiles_issued & 1u) : 0;
         ctx->carry_valid = false;  // until this call's records are all enqueued

@@ -203,3 +203,38 @@ def test_window_tail_head_dim_256(kvattn, mode):
     torch.cuda.synchronize()
     wo, wl = oracle.decode_f16(q, k, v, [N])
     assert_close(out.view(1, H, D), lse.view(1, H), wo, wl)
+
+
+def test_unpinned_tail(kvattn):
+    """Pageable host memory: the staged path copies it with cudaMemcpyAsync (the copy kernel
+    needs a device mapping) and records no graph.  The direct path needs a device address
+    for the tail: where the platform gives pageable memory one (a coherent host such as
+    Grace, through address translation) it reads the tail in place and must be right,
+    elsewhere it refuses the call before any launch."""
+    import torch
+    rng = np.random.default_rng(41)
+    N, n_win, H, Hk, D = 1500, 300, 16, 4, 128
+    q, k, v = make(rng, N, n_win, H, Hk, D)
+    n_tail = N - n_win
+    k_tail = torch.from_numpy(k[:n_tail].copy())  # not pinned
+    v_tail = torch.from_numpy(v[:n_tail].copy())
+    wt = kvattn.WindowTail()
+    out, lse = wt(dev(q[0]), dev(k[n_tail:]), dev(v[n_tail:]), k_tail, v_tail, split=128, tile_cells=256,
+                  tail_split=64, copy_stream=torch.cuda.Stream())
+    kvattn.kvattn_tail_wait(wt.ctx, 30000)
+    torch.cuda.synchronize()
+    wo, wl = oracle.decode_f16(q, k, v, [N])
+    assert_close(out.view(1, H, D), lse.view(1, H), wo, wl)
+    wt.close()
+    try:
+        out, lse = kvattn.window_tail_direct(dev(q[0]), dev(k[n_tail:]), dev(v[n_tail:]), k_tail, v_tail,
+                                             split=128, tail_split=64)
+        torch.cuda.synchronize()
+        assert_close(out.view(1, H, D), lse.view(1, H), wo, wl)
+    except kvattn.KvattnError as e:
+        assert e.status == kvattn.KVATTN_ERR_INVALID_ARG
+    # the context is still usable
+    out, lse = kvattn.window_tail_direct(dev(q[0]), dev(k[n_tail:]), dev(v[n_tail:]), k_tail.pin_memory(),
+                                         v_tail.pin_memory(), split=128, tail_split=64)
+    torch.cuda.synchronize()
+    assert_close(out.view(1, H, D), lse.view(1, H), wo, wl)
