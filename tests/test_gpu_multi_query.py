@@ -207,3 +207,35 @@ def test_multi_query_quantised_one_token_equals_single_query(kvattn, kind):
     torch.cuda.synchronize()
     assert np.max(np.abs(mo.cpu().numpy()[:, 0] - so.cpu().numpy())) <= 1e-4
     assert np.max(np.abs(ml.cpu().numpy()[:, 0] - sl.cpu().numpy())) <= 1e-5
+
+
+@pytest.mark.parametrize("kind", ["f16", "q8"])
+def test_multi_query_bounded_wait_reports_timeout_and_context_survives(kvattn, monkeypatch, kind):
+    """The multi-query kernels' pipeline waits are bounded: a first tile that expects bytes
+    no copy delivers (host test switch) ends in the timeout status bit, and the next call is
+    clean."""
+    import torch
+    rng = np.random.default_rng(23)
+    S, N, H, Hk, D, n_q = 1, 600, 16, 4, 128, 4
+    q = rand_f16(rng, (S, n_q, H, D))
+    if kind == "f16":
+        k, v = rand_f16(rng, (S, N, Hk, D)), rand_f16(rng, (S, N, Hk, D))
+        extra = {}
+        want = oracle.decode_multi(oracle.decode_f16, q, [N], k, v)
+    else:
+        k, kd, v, vd = q8_cache(rng, (S, N, Hk, D))
+        extra = {"k_scales": dev(kd), "v_scales": dev(vd)}
+        want = oracle.decode_multi(oracle.decode_q8_0, q, [N], k, kd, v, vd)
+    ws = torch.zeros(kvattn.kvattn_decode_multi_workspace_bytes(S, n_q, H, D, N, 128), dtype=torch.uint8,
+                     device="cuda")
+    lens = dev(np.array([N], np.int32))
+    monkeypatch.setenv("KVATTN_DEBUG_STALL_TX", "16")
+    monkeypatch.setenv("KVATTN_DEBUG_WAIT_MS", "20")
+    kvattn.decode_multi(dev(q), dev(k), dev(v), lens, split=128, n_cells=N, max_len=N, ws=ws, **extra)
+    torch.cuda.synchronize()
+    assert kvattn.kvattn_workspace_status(ws, clear=True) & kvattn.KVATTN_DEVICE_WAIT_TIMEOUT
+    monkeypatch.delenv("KVATTN_DEBUG_STALL_TX")
+    out, lse = kvattn.decode_multi(dev(q), dev(k), dev(v), lens, split=128, n_cells=N, max_len=N, ws=ws, **extra)
+    torch.cuda.synchronize()
+    assert kvattn.kvattn_workspace_status(ws) == 0
+    check(out, lse, *want)
