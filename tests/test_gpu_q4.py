@@ -210,3 +210,27 @@ def test_q8q4_long_context(kvattn, w):
     torch.cuda.synchronize()
     wo, wl = want(q, kq, kd, v4, vd, list(w.seq_lens))
     assert_close(out, lse, wo, wl)
+
+
+@pytest.mark.parametrize("kind", KINDS)
+def test_q4_bounded_wait_reports_timeout_and_context_survives(kvattn, monkeypatch, kind):
+    import torch
+    rng = np.random.default_rng(960)
+    N, Hk, G, D = 512, 2, 4, 128
+    H = Hk * G
+    kq, v4, kd, vd = q8q4_cache(rng, N, Hk, D, kind)
+    q = rng.standard_normal((1, H, D), dtype=np.float32).astype(np.float16)
+    ws = kvattn.decode_workspace(1, H, D, N, 128)
+    monkeypatch.setenv("KVATTN_DEBUG_STALL_TX", "16")
+    monkeypatch.setenv("KVATTN_DEBUG_WAIT_MS", "20")
+    kvattn.decode(dev(q), dev(kq), dev(v4), dev(np.array([N], np.int32)), split=128, k_scales=dev(kd),
+                  v_scales=dev(vd), ws=ws, kv_type=kv_type_of(kvattn, kq, v4))
+    torch.cuda.synchronize()
+    assert kvattn.kvattn_workspace_status(ws, clear=True) & kvattn.KVATTN_DEVICE_WAIT_TIMEOUT
+    monkeypatch.delenv("KVATTN_DEBUG_STALL_TX")
+    out, lse = kvattn.decode(dev(q), dev(kq), dev(v4), dev(np.array([N], np.int32)), split=128, k_scales=dev(kd),
+                             v_scales=dev(vd), ws=ws, kv_type=kv_type_of(kvattn, kq, v4))
+    torch.cuda.synchronize()
+    assert kvattn.kvattn_workspace_status(ws) == 0
+    wo, wl = want(q, kq, kd, v4, vd, [N])
+    assert_close(out, lse, wo, wl)
