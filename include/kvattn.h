@@ -6,7 +6,9 @@
  * memory.  Streams are passed as `void*` holding a cudaStream_t (NULL = the legacy
  * default stream).  The caller owns every buffer; the library allocates no device
  * memory on any decode path.  Every call validates its arguments on the host before
- * it touches CUDA and returns a kvattn_status; it never aborts and never prints.
+ * it touches CUDA and returns a kvattn_status; it never aborts, and it prints nothing
+ * unless the environment variable KVATTN_LOG=1 asks for one line on stderr per launching
+ * call (the chosen split, grid, ring depth, descriptor path, tail mode).
  * Device calls are asynchronous on the given stream(s).
  *
  * Host threads: every entry point may be called from several threads at once (the

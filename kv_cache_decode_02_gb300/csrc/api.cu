@@ -4,6 +4,8 @@
 #include <atomic>
 #include <chrono>
 #include <cmath>
+#include <cstdarg>
+#include <cstdio>
 #include <cstdlib>
 #include <cstring>
 #include <mutex>
@@ -28,6 +30,19 @@ int env_int(const char* name, int dflt) {
 bool use_pdl() {
     static const bool on = env_int("KVATTN_PDL", 1) != 0;
     return on;
+}
+
+// Opt-in trace of launch decisions: with KVATTN_LOG=1 (read on every call) each entry point
+// that launches work prints one line on stderr.  Otherwise the library never prints.
+bool log_on() { return env_int("KVATTN_LOG", 0) != 0; }
+
+void log_line(const char* fmt, ...) {
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    std::vsnprintf(buf, sizeof(buf), fmt, ap);
+    va_end(ap);
+    std::fprintf(stderr, "kvattn: %s\n", buf);
 }
 
 int sm_count() {
@@ -439,6 +454,16 @@ int decode_impl(const void* q, const void* k_cache, const void* v_cache, const v
         set_kv_maps(p, kv_type, cell_plan != nullptr ? n_cells : n_cells * (int64_t)n_seq, n_head_kv, head_dim);
         cudaError_t e = launch_decode_units(p, kv_type, head_dim, n_split, s, pdl);
         if (e != cudaSuccess) return KVATTN_ERR_CUDA;
+        if (log_on()) {
+            const int64_t units = (int64_t)n_seq * n_split * n_head_kv;
+            const int64_t resident = (int64_t)std::max(occupancy(kv_type, head_dim, p.n_stages, multi), 1) * sm_count();
+            log_line("%s kv_type=%d n_seq=%d n_q=%d n_head=%d/%d head_dim=%d max_len=%lld split=%d n_split=%lld "
+                     "plan=%d descriptors=%s units=%lld grid=%lld stages=%d tma=%d merge=%d",
+                     multi ? "decode_multi" : (merge ? "decode" : "decode_partials"), kv_type, n_seq, n_q, n_head,
+                     n_head_kv, head_dim, (long long)max_len, split, (long long)n_split, cell_plan != nullptr,
+                     cell_plan == nullptr ? "none" : (desc_out != nullptr ? "in-kernel" : "kernel"),
+                     (long long)units, (long long)std::min(units, resident), p.n_stages, p.use_tma, merge ? 1 : 0);
+        }
     }
     if (!merge) return KVATTN_OK;
     MergeParams m = {};
@@ -975,6 +1000,11 @@ int kvattn_decode_window_tail(kvattn_tail_ctx* ctx, const void* q, const void* k
         hit->last_use = ++ctx->use_clock;
         if (cudaGraphLaunch(hit->exec, cs) != cudaSuccess) return KVATTN_ERR_CUDA;
     }
+    if (log_on())
+        log_line("window_tail n_win=%lld n_tail=%lld tiles=%lld tile_cells=%lld mode=%s copy=%s graphs_cached=%d",
+                 (long long)n_win, (long long)n_tail, (long long)plan.L.n_tiles, (long long)tile_cells,
+                 use_graph ? "graph" : (prefetch ? (carry ? "prefetch-carried" : "prefetch-first") : "direct-enqueue"),
+                 k_dev != nullptr ? "kernel" : "engine", ctx->n_graphs);
     if (cudaEventRecord(ctx->done, cs) != cudaSuccess) return KVATTN_ERR_CUDA;
     ctx->pending = true;
     return KVATTN_OK;
@@ -1085,6 +1115,9 @@ int kvattn_decode_window_tail_direct(const void* q, const void* k_win, const voi
             launch_decode_units(t, KVATTN_KV_F16, head_dim, n_split_tail, cs, false) != cudaSuccess)
             return KVATTN_ERR_CUDA;
     }
+    if (log_on())
+        log_line("window_tail_direct n_win=%lld n_tail=%lld window_splits=%lld tail_splits=%lld overlap=%d",
+                 (long long)n_win, (long long)n_tail, (long long)n_split_win, (long long)n_split_tail, overlap ? 1 : 0);
     MergeParams m = {};
     m.part_o = p.part_o;
     m.part_lse = p.part_lse;

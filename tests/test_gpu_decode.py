@@ -450,3 +450,26 @@ def test_more_than_65535_sequences(kvattn):
     pick = np.concatenate([[0, 1, 2], rng.choice(S, 200, replace=False), [S - 1]])
     wo, wl = oracle.decode_f16(q[pick], k[pick], v[pick], lens[pick].tolist())
     assert_close(out[pick], lse[pick], wo, wl)
+
+
+def test_launch_trace_only_on_request(kvattn, monkeypatch, capfd):
+    """KVATTN_LOG=1: one stderr line per launching call with the decisions taken; silent
+    otherwise."""
+    import torch
+    rng = np.random.default_rng(15)
+    N, H, Hk, D = 4096, 32, 8, 128
+    q, k, v = rand_f16(rng, (1, H, D)), rand_f16(rng, (N, Hk, D)), rand_f16(rng, (N, Hk, D))
+    args = (dev(q), dev(k), dev(v), dev(np.array([N], np.int32)))
+    capfd.readouterr()
+    kvattn.decode(*args, split=256)
+    torch.cuda.synchronize()
+    assert capfd.readouterr().err == ""
+    monkeypatch.setenv("KVATTN_LOG", "1")
+    kvattn.decode(*args, split=0)
+    torch.cuda.synchronize()
+    err = capfd.readouterr().err
+    monkeypatch.delenv("KVATTN_LOG")
+    lines = [ln for ln in err.splitlines() if ln.startswith("kvattn: decode ")]
+    assert len(lines) == 1, err
+    sp = kvattn.kvattn_select_split(0, 1, N, Hk, D)
+    assert f"split={sp} " in lines[0] and f"n_split={-(-N // sp)} " in lines[0] and "plan=0" in lines[0]
