@@ -229,9 +229,10 @@ size_t kvattn_decode_multi_workspace_bytes(int n_seq, int n_q, int n_head, int h
  *  q        device half [n_seq][n_q][n_head][head_dim].
  *  out, lse device float [n_seq][n_q][n_head][head_dim], [n_seq][n_q][n_head].
  *  Other arguments: as kvattn_decode.
- *  Limits: head_dim 128; kv_type f16 with (n_head / n_head_kv) * n_q <= 32 (e.g. n_q <= 8
- *  at 4 query heads per KV head) or a quantised type (Q8_0, Q8_0_Q4_0, Q4_0) with
- *  (n_head / n_head_kv) * n_q <= 16 (UNSUPPORTED otherwise); n_q >= 1.
+ *  Limits (UNSUPPORTED otherwise): head_dim 128 with kv_type f16 and
+ *  (n_head / n_head_kv) * n_q <= 32 (e.g. n_q <= 8 at 4 query heads per KV head), or a
+ *  quantised type (Q8_0, Q8_0_Q4_0, Q4_0) with (n_head / n_head_kv) * n_q <= 16;
+ *  head_dim 256 with kv_type f16 and (n_head / n_head_kv) * n_q <= 16.  n_q >= 1.
  *  ws: kvattn_decode_multi_workspace_bytes(...) bytes.
  * Errors: as kvattn_decode.
  */

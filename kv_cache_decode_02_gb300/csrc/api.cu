@@ -366,10 +366,15 @@ int decode_impl(const void* q, const void* k_cache, const void* v_cache, const v
     int st = check_shape(shape);
     if (st != KVATTN_OK) return st;
     if (multi && (int64_t)n_seq * n_q * n_head > (int64_t)INT32_MAX) return KVATTN_ERR_UNSUPPORTED;
-    // multi-query: f16 up to 32 query rows per KV head, the quantised caches up to 16; head_dim 128
-    if (multi && (head_dim != 128 || !valid_kv_type(kv_type) ||
-                  (n_head / n_head_kv) * n_q > (kv_type == KVATTN_KV_F16 ? 32 : 16)))
-        return KVATTN_ERR_UNSUPPORTED;
+    // multi-query: head_dim 128 -- f16 up to 32 query rows per KV head, the quantised caches up
+    // to 16; head_dim 256 -- f16 up to 16
+    if (multi) {
+        const int rows = (n_head / n_head_kv) * n_q;
+        const bool ok = valid_kv_type(kv_type) &&
+                        ((head_dim == 128 && rows <= (kv_type == KVATTN_KV_F16 ? 32 : 16)) ||
+                         (head_dim == 256 && kv_type == KVATTN_KV_F16 && rows <= 16));
+        if (!ok) return KVATTN_ERR_UNSUPPORTED;
+    }
     if (q == nullptr || k_cache == nullptr || v_cache == nullptr || seq_lens == nullptr || ws == nullptr)
         return KVATTN_ERR_INVALID_ARG;
     if (merge && (out == nullptr || lse == nullptr)) return KVATTN_ERR_INVALID_ARG;

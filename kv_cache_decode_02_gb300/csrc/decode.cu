@@ -750,6 +750,142 @@ __device__ __forceinline__ void mq_consumers(const SplitDecodeParams& p, uint64_
     }
 }
 
+// Multi-query consumers at head_dim 256 (up to 16 query rows per KV head): warp w takes rows
+// 8w .. 8w+7 (M = 16 of the q.K^T MMA with rows 8-15 zero, N = 8 of the P V MMA, as the
+// single-query kernel) over both 16-cell halves of every tile, folding each row's causal
+// limit into its lanes' cell mask, and writes its rows at the unit's end (no exchange).
+template <int D>
+__device__ __forceinline__ void mq_consumers_rows8(const SplitDecodeParams& p, uint64_t* full_bar, uint64_t* empty_bar,
+                                                   const uint32_t* tile_mask, const uint32_t* tile_swz,
+                                                   volatile int* abort_flag, unsigned char* stages, int n_stages,
+                                                   int64_t n_units, int warp, int lane) {
+    using G = Geom<KVATTN_KV_F16, D>;
+    const int gq = lane >> 2;
+    const int tq = lane & 3;
+    const int H = p.n_head, GQ = p.group, NQ = p.n_q;
+    const int rows = GQ * NQ;
+    const int64_t HR = (int64_t)NQ * H;
+    const int row0 = 8 * warp;
+    constexpr float kLn2 = 0.69314718055994530942f;
+    auto load_q = [&](int s, int g, uint32_t (&qa)[D / 16][2]) {
+        const int r = row0 + gq;
+        const bool ok = r < rows;
+        const int t = ok ? r / GQ : 0;
+        const int h = g * GQ + (ok ? r % GQ : 0);
+        const uint32_t* qrow = reinterpret_cast<const uint32_t*>(p.q + (((int64_t)s * NQ + t) * H + h) * D);
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+            const int d0 = 16 * kk + 2 * tq;
+            qa[kk][0] = ok ? __ldg(qrow + d0 / 2) : 0u;
+            qa[kk][1] = ok ? __ldg(qrow + (d0 + 8) / 2) : 0u;
+        }
+    };
+    uint32_t qa[D / 16][2];
+    int64_t qa_unit = -1;
+    uint32_t T = 0;
+    bool stop = false;
+    for (int64_t u = blockIdx.x; u < n_units && !stop; u += gridDim.x) {
+        const Unit x = unit_at(p, u);
+        const int64_t part = (int64_t)x.s * p.part_stride + p.part_base + x.split_idx;
+        if (x.n_tiles == 0) {
+            if (x.write_empty) {
+                for (int idx = lane; idx < 8 * D; idx += 32) {
+                    const int r = row0 + idx / D;
+                    const int d = idx % D;
+                    if (r < rows) {
+                        const int64_t row = (int64_t)(r / GQ) * H + x.g * GQ + r % GQ;
+                        p.part_o[(part * HR + row) * D + d] = 0.f;
+                        if (d == 0) p.part_lse[part * HR + row] = -INFINITY;
+                    }
+                }
+            }
+            continue;
+        }
+        if (qa_unit != u) load_q(x.s, x.g, qa);
+        float oacc[D / 16][4];
+        float m_run = -INFINITY, l_run = 0.f;
+#pragma unroll
+        for (int i = 0; i < D / 16; ++i) oacc[i][0] = oacc[i][1] = oacc[i][2] = oacc[i][3] = 0.f;
+        // causal limit (logical position, exclusive) of the lane's row row0 + gq
+        const int64_t lim_row = x.len - NQ + 1 + (row0 + gq) / GQ;
+        for (int t = 0; t < x.n_tiles; ++t, ++T) {
+            const int st = (int)(T % (uint32_t)n_stages);
+            const uint32_t use = T / (uint32_t)n_stages;
+            const bool ok = mbar_wait_bounded(smem_addr(&full_bar[st]), use & 1u, abort_flag, p.wait_limit_ns);
+            if (!__all_sync(0xffffffffu, ok)) {
+                stop = true;
+                break;
+            }
+            const bool swz = tile_swz[st] != 0u;
+            unsigned char* stage = stages + st * G::kBytes;
+#pragma unroll 1
+            for (int hw = 0; hw < 2; ++hw) {
+                const uint32_t mask = (tile_mask[st] >> (hw * kWarpCells)) & 0xffffu;
+                if (mask == 0u) continue;
+                const int64_t rel = lim_row - (x.i0 + (int64_t)t * kTileCells + hw * kWarpCells);
+                const int lim = rel < 0 ? 0 : (rel > kWarpCells ? kWarpCells : (int)rel);
+                const uint32_t lane_mask = mask & ((lim >= 32 ? 0xffffffffu : (1u << lim)) - 1u);
+                if (swz) {
+                    const uint32_t kb = smem_addr(stage);
+                    if (mask != 0xffffu) {
+                        // masked rows came in with the box: zero their V rows (both warps write
+                        // the same zeros, each before its own reads)
+                        const int r = hw * kWarpCells + (lane & 15);
+                        if (lane < 16 && !((mask >> lane) & 1u)) {
+#pragma unroll
+                            for (int pl = 0; pl < G::kPlanes; ++pl) {
+                                uint4* z = reinterpret_cast<uint4*>(stage + G::kSwzSection + pl * kPlaneBytes + r * 128);
+#pragma unroll
+                                for (int k = 0; k < 8; ++k) z[k] = make_uint4(0, 0, 0, 0);
+                            }
+                            fence_proxy_async();
+                        }
+                        __syncwarp();
+                    }
+                    consume_tile<KVATTN_KV_F16, D, true>(kb, kb + G::kSwzSection, nullptr, nullptr, lane_mask, hw,
+                                                         lane, qa, oacc, m_run, l_run, p.scale_log2);
+                } else {
+                    const uint32_t kb = smem_addr(stage);
+                    consume_tile<KVATTN_KV_F16, D, false>(kb, kb + G::kPadSection, nullptr, nullptr, lane_mask, hw,
+                                                          lane, qa, oacc, m_run, l_run, p.scale_log2);
+                }
+            }
+            __syncwarp();
+            mbar_arrive(smem_addr(&empty_bar[st]));
+        }
+        if (stop) break;
+        l_run += __shfl_xor_sync(0xffffffffu, l_run, 1);
+        l_run += __shfl_xor_sync(0xffffffffu, l_run, 2);
+        const int64_t un = u + gridDim.x;
+        if (un < n_units) {
+            const Unit y = unit_at(p, un);
+            if (y.n_tiles > 0) {
+                load_q(y.s, y.g, qa);
+                qa_unit = un;
+            }
+        }
+        // this lane's O rows are 8w + 2tq + e; their max / sum sit in lanes 8tq + 4e
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+            const int r = row0 + 2 * tq + e;
+            const float m = __shfl_sync(0xffffffffu, m_run, 8 * tq + 4 * e);
+            const float l = __shfl_sync(0xffffffffu, l_run, 8 * tq + 4 * e);
+            const bool have = m != -INFINITY && l > 0.f;
+            const float inv = have ? 1.f / l : 0.f;
+            if (r < rows) {
+                const int64_t row = (int64_t)(r / GQ) * H + x.g * GQ + r % GQ;
+                float* orow = p.part_o + (part * HR + row) * D;
+#pragma unroll
+                for (int mt = 0; mt < D / 16; ++mt) {
+                    orow[out_dim<KVATTN_KV_F16>(mt, 0, gq)] = oacc[mt][e] * inv;
+                    orow[out_dim<KVATTN_KV_F16>(mt, 1, gq)] = oacc[mt][2 + e] * inv;
+                }
+                if (gq == 0) p.part_lse[part * HR + row] = have ? (m + fast_log2(l)) * kLn2 : -INFINITY;
+            }
+        }
+    }
+}
+
 // Persistent split-decode kernel (f16 KV; Q8_0 runs in q8_self_body below).  Each CTA walks
 // the units blockIdx.x, blockIdx.x + grid,
 // ...; warp 2 streams the 32-cell tiles of those units through a ring of shared-memory
@@ -760,7 +896,7 @@ __device__ __forceinline__ void mq_consumers(const SplitDecodeParams& p, uint64_
 template <int KVT, int D, bool MQ = false>
 __device__ __forceinline__ void split_decode_body(const SplitDecodeParams& p) {
     static_assert(KVT == KVATTN_KV_F16, "Q8_0 runs in q8_self_body");
-    static_assert(!MQ || D == 128, "multi-query decode: head_dim 128");
+    static_assert(!MQ || D == 128 || D == 256, "multi-query decode: head_dim 128 or 256");
     using G = Geom<KVT, D>;
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     // 1024-byte alignment of the stage ring (the 128-B swizzle repeats every 8 rows)
@@ -774,7 +910,8 @@ __device__ __forceinline__ void split_decode_body(const SplitDecodeParams& p) {
     float4* xo = reinterpret_cast<float4*>(smem + kHeaderBytes);  // [D/16][32 lanes] of warp 1's O
     float* xm = reinterpret_cast<float*>(xo + (D / 16) * 32);      // [8] warp 1's running max
     float* xl = xm + 8;                                             // [8] warp 1's running sum
-    unsigned char* stages = smem + kHeaderBytes + (MQ ? G::kXchgBytesMQ : G::kXchgBytes);
+    // (the head_dim-256 multi-query consumers split the rows and exchange nothing)
+    unsigned char* stages = smem + kHeaderBytes + (MQ && D == 128 ? G::kXchgBytesMQ : G::kXchgBytes);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -1003,7 +1140,10 @@ __device__ __forceinline__ void split_decode_body(const SplitDecodeParams& p) {
         if (__any_sync(0xffffffffu, bad) && lane == 0) atomicOr(p.status, KVATTN_DEVICE_BAD_PLAN_ENTRY);
     } else {
         // ------------------------------- consumers -------------------------------
-        if constexpr (MQ) {
+        if constexpr (MQ && D == 256) {
+            mq_consumers_rows8<D>(p, full_bar, empty_bar, tile_mask, tile_swz, abort_flag, stages, n_stages, n_units,
+                                  warp, lane);
+        } else if constexpr (MQ) {
             mq_consumers(p, full_bar, empty_bar, tile_mask, tile_swz, abort_flag, xchg_bar,
                          reinterpret_cast<unsigned char*>(xo), stages, n_stages, n_units, warp, lane);
         } else {
@@ -2419,6 +2559,10 @@ __global__ void __launch_bounds__(kThreads, KVATTN_F16_D256_MIN_CTAS)
 __global__ void __launch_bounds__(kThreads) split_decode_mq_f16_d128(const __grid_constant__ SplitDecodeParams p) {
     split_decode_body<KVATTN_KV_F16, 128, true>(p);
 }
+__global__ void __launch_bounds__(kThreads, KVATTN_F16_D256_MIN_CTAS)
+    split_decode_mq_f16_d256(const __grid_constant__ SplitDecodeParams p) {
+    split_decode_body<KVATTN_KV_F16, 256, true>(p);
+}
 __global__ void __launch_bounds__(kQ8W128 * 32, kQ8B128)
     split_decode_q8_d128(const __grid_constant__ SplitDecodeParams p) {
     q8_self_body<128, kQ8W128, kQ8S128>(p);
@@ -2463,7 +2607,8 @@ const void* kernel_for(int kv_type, int head_dim, bool mq = false) {
         if (kv_type == KVATTN_KV_Q8_0) return reinterpret_cast<const void*>(split_decode_mq_q8_d128);
         if (kv_type == KVATTN_KV_Q8_0_Q4_0) return reinterpret_cast<const void*>(split_decode_mq_q8q4_d128);
         if (kv_type == KVATTN_KV_Q4_0) return reinterpret_cast<const void*>(split_decode_mq_q4_d128);
-        return reinterpret_cast<const void*>(split_decode_mq_f16_d128);
+        return head_dim == 256 ? reinterpret_cast<const void*>(split_decode_mq_f16_d256)
+                               : reinterpret_cast<const void*>(split_decode_mq_f16_d128);
     }
     if (kv_type == KVATTN_KV_F16)
         return head_dim == 128 ? reinterpret_cast<const void*>(split_decode_f16_d128)
@@ -2506,9 +2651,9 @@ int split_decode_smem_bytes(int kv_type, int head_dim, int n_stages, bool mq) {
     if (kv_type == KVATTN_KV_Q4_0)
         return head_dim == 128 ? q8_self_smem<128, kQ8W128, kQ8S128, true, true>()
                                : q8_self_smem<256, kQ8W256, kQ8S256, true, true>();
-    const int xchg = mq                ? Geom<0, 128>::kXchgBytesMQ
-                     : head_dim == 128 ? Geom<0, 128>::kXchgBytes
-                                       : Geom<0, 256>::kXchgBytes;
+    const int xchg = mq && head_dim == 128 ? Geom<0, 128>::kXchgBytesMQ
+                     : head_dim == 128       ? Geom<0, 128>::kXchgBytes
+                                             : Geom<0, 256>::kXchgBytes;
     return kHeaderBytes + 1024 + xchg + n_stages * split_decode_stage_bytes(kv_type, head_dim);
 }
 
@@ -2535,12 +2680,12 @@ cudaError_t launch_split_decode(const SplitDecodeParams& p, int kv_type, int hea
                                 cudaStream_t stream, bool pdl) {
     const bool mq = p.mq != 0;
     const void* fn = kernel_for(kv_type, head_dim, mq);
-    static std::once_flag once[64][12];
-    static cudaError_t attr_err[64][12];
+    static std::once_flag once[64][16];
+    static cudaError_t attr_err[64][16];
     int dev = 0;
     cudaError_t err = cudaGetDevice(&dev);
     if (err != cudaSuccess) return err;
-    const int which = mq ? 8 + kv_type : 2 * kv_type + (head_dim == 256 ? 1 : 0);
+    const int which = (mq ? 8 : 0) + 2 * kv_type + (head_dim == 256 ? 1 : 0);
     std::call_once(once[dev & 63][which], [&] { attr_err[dev & 63][which] = set_smem_attr(fn); });
     if (attr_err[dev & 63][which] != cudaSuccess) return attr_err[dev & 63][which];
     cudaLaunchConfig_t cfg = {};
