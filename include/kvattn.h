@@ -225,12 +225,14 @@ size_t kvattn_decode_multi_workspace_bytes(int n_seq, int n_q, int n_head, int h
  * counts them, token t sits at logical position L - n_q + t and attends to the logical
  * positions 0 .. L - n_q + t (plan entries or cells, -1 holes masked); a token whose window
  * is empty gets O = 0, LSE = -inf.  The G x n_q query rows of each KV head share every K/V
- * byte read from HBM (one or two 16-row MMA tiles).
+ * byte read from HBM (one or two 16-row MMA tiles, up to 32 rows).
  *  q        device half [n_seq][n_q][n_head][head_dim].
  *  out, lse device float [n_seq][n_q][n_head][head_dim], [n_seq][n_q][n_head].
  *  Other arguments: as kvattn_decode.
  *  Limits (UNSUPPORTED otherwise): head_dim 128 with kv_type f16 and
- *  (n_head / n_head_kv) * n_q <= 32 (e.g. n_q <= 8 at 4 query heads per KV head), or a
+ *  (n_head / n_head_kv) * n_q <= 64 (n_q <= 8 at up to 8 query heads per KV head; beyond 32
+ *  rows the rows run as groups of 32, each group reading the split's K/V, the second
+ *  mostly from L2), or a
  *  quantised type (Q8_0, Q8_0_Q4_0, Q4_0) with (n_head / n_head_kv) * n_q <= 16;
  *  head_dim 256 with kv_type f16 and (n_head / n_head_kv) * n_q <= 16.  n_q >= 1.
  *  ws: kvattn_decode_multi_workspace_bytes(...) bytes.

@@ -115,7 +115,7 @@ int64_t auto_split_slots(int kv_type, int head_dim) {
 cudaError_t launch_decode_units(SplitDecodeParams p, int kv_type, int head_dim, int64_t unit_splits,
                                 cudaStream_t stream, bool pdl) {
     p.unit_splits = unit_splits;
-    const int64_t n_units = (int64_t)p.n_seq * unit_splits * p.n_head_kv;
+    const int64_t n_units = (int64_t)p.n_seq * unit_splits * p.n_head_kv * (p.n_rg > 1 ? p.n_rg : 1);
     if (n_units > (int64_t)INT32_MAX) return cudaErrorInvalidValue;  // units are numbered in 32 bits
     const int64_t resident =
         (int64_t)std::max(occupancy(kv_type, head_dim, p.n_stages, p.mq != 0), 1) * sm_count();
@@ -351,29 +351,36 @@ int decode_impl(const void* q, const void* k_cache, const void* v_cache, const v
                 int n_head_kv, int head_dim, int split, float scale, float* out, float* lse,
                 float* part_o_user, float* part_lse_user, void* ws, size_t ws_bytes, void* stream,
                 int n_q = 0) {
-    // n_q = 0: single-query decode; n_q >= 1: the causal multi-query kernel (f16, head_dim 128)
+    // n_q = 0: single-query decode; n_q >= 1: the causal multi-query kernels
     const bool multi = n_q > 0;
     if (!multi) n_q = 1;
     const bool merge = part_o_user == nullptr;
+    // multi-query rows per KV head beyond 32 run as row groups of 32 (units of their own)
+    const int mq_rows = (n_head_kv >= 1 && n_head >= n_head_kv) ? (n_head / n_head_kv) * n_q : 0;
+    const int n_rg = (multi && mq_rows > 32) ? (mq_rows + 31) / 32 : 1;
     if (split == 0 && merge) {  // kvattn_decode picks the split (partials need it fixed)
         if (!valid_kv_type(kv_type)) return KVATTN_ERR_INVALID_ARG;
         if (head_dim != 128 && head_dim != 256) return KVATTN_ERR_UNSUPPORTED;
         if (n_head_kv < 1 || n_seq < 0 || max_len < 0) return KVATTN_ERR_INVALID_ARG;
-        split = kvattn_select_split(kv_type, n_seq, max_len, n_head_kv, head_dim);
+        split = n_rg > 1 ? kvattn_select_split_for(n_seq, max_len, n_head_kv * n_rg,
+                                                   auto_split_slots(kv_type, head_dim))
+                         : kvattn_select_split(kv_type, n_seq, max_len, n_head_kv, head_dim);
         if (split < 0) return split;
     }
     const DecodeShape shape{n_seq, n_head, n_head_kv, head_dim, split, max_len};
     int st = check_shape(shape);
     if (st != KVATTN_OK) return st;
     if (multi && (int64_t)n_seq * n_q * n_head > (int64_t)INT32_MAX) return KVATTN_ERR_UNSUPPORTED;
-    // multi-query: head_dim 128 -- f16 up to 32 query rows per KV head, the quantised caches up
-    // to 16; head_dim 256 -- f16 up to 16
+    // multi-query: head_dim 128 -- f16 up to 64 query rows per KV head (two row groups), the
+    // quantised caches up to 16; head_dim 256 -- f16 up to 16
     if (multi) {
-        const int rows = (n_head / n_head_kv) * n_q;
+        const int rows = mq_rows;
         const bool ok = valid_kv_type(kv_type) &&
-                        ((head_dim == 128 && rows <= (kv_type == KVATTN_KV_F16 ? 32 : 16)) ||
+                        ((head_dim == 128 && rows <= (kv_type == KVATTN_KV_F16 ? 64 : 16)) ||
                          (head_dim == 256 && kv_type == KVATTN_KV_F16 && rows <= 16));
         if (!ok) return KVATTN_ERR_UNSUPPORTED;
+        if ((int64_t)n_seq * ((max_len + split - 1) / split) * n_head_kv * n_rg > (int64_t)INT32_MAX)
+            return KVATTN_ERR_UNSUPPORTED;
     }
     if (q == nullptr || k_cache == nullptr || v_cache == nullptr || seq_lens == nullptr || ws == nullptr)
         return KVATTN_ERR_INVALID_ARG;
@@ -453,14 +460,15 @@ int decode_impl(const void* q, const void* k_cache, const void* v_cache, const v
         p.split = split;
         p.n_q = n_q;
         p.mq = multi ? 1 : 0;
-        p.n_stages = pick_stages(kv_type, head_dim, n_split * n_head_kv * n_seq, multi);
+        p.n_rg = n_rg;
+        p.n_stages = pick_stages(kv_type, head_dim, n_split * n_head_kv * n_rg * n_seq, multi);
         p.scale_log2 = (float)((double)scale * 1.4426950408889634074);
         apply_debug_hooks(p);
         set_kv_maps(p, kv_type, cell_plan != nullptr ? n_cells : n_cells * (int64_t)n_seq, n_head_kv, head_dim);
         cudaError_t e = launch_decode_units(p, kv_type, head_dim, n_split, s, pdl);
         if (e != cudaSuccess) return KVATTN_ERR_CUDA;
         if (log_on()) {
-            const int64_t units = (int64_t)n_seq * n_split * n_head_kv;
+            const int64_t units = (int64_t)n_seq * n_split * n_head_kv * n_rg;
             const int64_t resident = (int64_t)std::max(occupancy(kv_type, head_dim, p.n_stages, multi), 1) * sm_count();
             log_line("%s kv_type=%d n_seq=%d n_q=%d n_head=%d/%d head_dim=%d max_len=%lld split=%d n_split=%lld "
                      "plan=%d descriptors=%s units=%lld grid=%lld stages=%d tma=%d merge=%d",

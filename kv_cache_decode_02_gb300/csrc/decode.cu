@@ -384,6 +384,7 @@ __device__ __forceinline__ void load_q_frags_q4k(const SplitDecodeParams& p, int
 // so the CTAs that run side by side read the rows of every head of the same cells.
 struct Unit {
     int s, g;
+    int rg;           // multi-query row group (0 without row groups)
     int64_t split_idx;
     int64_t len;      // the sequence's clamped length
     int64_t i0, i1;   // plan entries / cells [i0, i1) of the split
@@ -394,10 +395,21 @@ struct Unit {
 __device__ __forceinline__ Unit unit_at(const SplitDecodeParams& p, int64_t u) {
     Unit x;
     // unit counts fit in 32 bits (checked on the host): 32-bit division is far cheaper
-    const uint32_t uu = (uint32_t)u, hk = (uint32_t)p.n_head_kv, us = (uint32_t)p.unit_splits;
-    const uint32_t r = uu / hk;
+    const uint32_t uu = (uint32_t)u, us = (uint32_t)p.unit_splits;
+    uint32_t r;
+    if (p.n_rg > 1) {
+        const uint32_t nrg = (uint32_t)p.n_rg, hkv = (uint32_t)p.n_head_kv * nrg;
+        r = uu / hkv;
+        const uint32_t gv = uu - r * hkv;
+        x.g = (int)(gv / nrg);
+        x.rg = (int)(gv - (uint32_t)x.g * nrg);
+    } else {
+        const uint32_t hk = (uint32_t)p.n_head_kv;
+        r = uu / hk;
+        x.g = (int)(uu - r * hk);
+        x.rg = 0;
+    }
     const uint32_t si = r / us;
-    x.g = (int)(uu - r * hk);
     x.split_idx = (int64_t)(r - si * us);
     x.s = (int)si;
     const int64_t cap = p.plan ? p.plan_stride : p.n_cells;
@@ -539,7 +551,9 @@ __device__ __forceinline__ void mq_tile(uint32_t kb, uint32_t vb, uint32_t mask,
 // single-query consumers (partial row of (token t, head h) = t * n_head + h).  Up to 16 query
 // rows per KV head, each warp attends to its 16 cells of every tile for all rows and the
 // two warps meet in the doubled end-of-unit exchange; with 17 to 32 rows, warp w takes rows
-// 16w .. 16w+15 over all 32 cells of every tile and writes them itself (no exchange).
+// 16w .. 16w+15 over all 32 cells of every tile and writes them itself (no exchange); with
+// 33 to 64 rows, each group of 32 rows is a unit of its own in the same way (the groups of
+// a split are neighbouring units, so the second reads the split's K/V from L2).
 __device__ __forceinline__ void mq_consumers(const SplitDecodeParams& p, uint64_t* full_bar, uint64_t* empty_bar,
                                              const uint32_t* tile_mask, const uint32_t* tile_swz,
                                              volatile int* abort_flag, uint64_t* xchg_bar, unsigned char* xchg,
@@ -552,7 +566,8 @@ __device__ __forceinline__ void mq_consumers(const SplitDecodeParams& p, uint64_
     const int H = p.n_head, GQ = p.group, NQ = p.n_q;
     const int rows = GQ * NQ;
     const bool rsplit = rows > 16;       // the warps split the rows instead of the cells
-    const int row0 = rsplit ? 16 * warp : 0;
+    // first row of this warp in a unit: 32 rows per row group (more than 32 rows per KV head)
+    auto first_row = [&](const Unit& y) { return 32 * y.rg + (rsplit ? 16 * warp : 0); };
     const int64_t HR = (int64_t)NQ * H;  // partial rows per (sequence, split)
     float4* xo = reinterpret_cast<float4*>(xchg);      // [2][D/16][32 lanes]
     float* xm = reinterpret_cast<float*>(xo + 2 * (D / 16) * 32);  // [16] max
@@ -565,11 +580,15 @@ __device__ __forceinline__ void mq_consumers(const SplitDecodeParams& p, uint64_
     for (int64_t u = blockIdx.x; u < n_units && !stop; u += gridDim.x) {
         const Unit x = unit_at(p, u);
         const int64_t part = (int64_t)x.s * p.part_stride + p.part_base + x.split_idx;
+        const int row0 = first_row(x);
         if (x.n_tiles == 0) {
             if (warp == 0 && x.write_empty) {
-                for (int idx = lane; idx < rows * D; idx += 32) {
-                    const int r = idx / D;
-                    const int d = idx - r * D;
+                // the unit's rows: its row group's 32, or every row without row groups
+                const int rb = 32 * x.rg;
+                const int n_rows = p.n_rg > 1 ? (rows - rb < 32 ? rows - rb : 32) : rows;
+                for (int idx = lane; idx < n_rows * D; idx += 32) {
+                    const int r = rb + idx / D;
+                    const int d = idx % D;
                     const int64_t row = (int64_t)(r / GQ) * H + x.g * GQ + r % GQ;
                     p.part_o[(part * HR + row) * D + d] = 0.f;
                     if (d == 0) p.part_lse[part * HR + row] = -INFINITY;
@@ -650,7 +669,7 @@ __device__ __forceinline__ void mq_consumers(const SplitDecodeParams& p, uint64_
         if (un < n_units) {
             const Unit y = unit_at(p, un);
             if (y.n_tiles > 0) {
-                load_q_frags_mq(p, y.s, y.g, gq, tq, row0, qa);
+                load_q_frags_mq(p, y.s, y.g, gq, tq, first_row(y), qa);
                 qa_unit = un;
             }
         }
@@ -916,7 +935,7 @@ __device__ __forceinline__ void split_decode_body(const SplitDecodeParams& p) {
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const int n_stages = p.n_stages;
-    const int64_t n_units = (int64_t)p.n_seq * p.unit_splits * p.n_head_kv;
+    const int64_t n_units = (int64_t)p.n_seq * p.unit_splits * p.n_head_kv * (p.n_rg > 1 ? p.n_rg : 1);
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < n_stages; ++i) {
@@ -972,7 +991,7 @@ __device__ __forceinline__ void split_decode_body(const SplitDecodeParams& p) {
             // The split's descriptor (the same for every KV head) is written by its head-0 unit
             // from the plan entries this warp reads anyway: count, smallest and largest valid
             // cell, the (cell - position) range, out-of-range entries seen.
-            const bool emit_desc = p.desc_out != nullptr && x.g == 0;
+            const bool emit_desc = p.desc_out != nullptr && x.g == 0 && x.rg == 0;
             if (x.n_tiles == 0) {
                 if (emit_desc && lane == 0)
                     p.desc_out[(int64_t)x.s * p.n_split + x.split_idx] = make_int4(0, -1, -1, x.i0 >= x.len ? 9 : 1);

@@ -68,7 +68,11 @@ struct SplitDecodeParams {
     uint32_t stall_tx;        // test hook: extra bytes expected on the first tile (never arrive)
     int n_seq, n_head, n_head_kv, group, split;
     int n_q;                  // query tokens per sequence (multi-query decode; 1 otherwise)
-    int mq;                   // 1: the multi-query kernel (rows = group x n_q <= 16)
+    int mq;                   // 1: the multi-query kernel
+    int n_rg;                 // multi-query row groups of 32 rows per KV head (0 or 1: one group
+                              // holding every row); the units become (sequence, split, KV head,
+                              // row group), row group fastest, so the groups of one split run
+                              // side by side and share its K/V bytes through L2
     int n_stages;
     int use_tma;              // tiles that are one physical run load through tmap_k/tmap_v
     int write_beyond;         // splits past a sequence's length still write (0, -inf)

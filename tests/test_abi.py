@@ -178,7 +178,7 @@ def test_multi_query_limits(kvattn):
                  scale=0.0884, out=A + 8192, lse=A + 16384, ws=A + 65536, ws_bytes=1 << 30, stream=None)
         a.update(over)
         return kvattn.lib.kvattn_decode_multi(*a.values())
-    assert call(n_q=9) == kvattn.KVATTN_ERR_UNSUPPORTED            # 4 x 9 = 36 rows > 32
+    assert call(n_q=17) == kvattn.KVATTN_ERR_UNSUPPORTED           # 4 x 17 = 68 rows > 64
     assert call(head_dim=256, n_q=5) == kvattn.KVATTN_ERR_UNSUPPORTED  # head_dim 256: 20 rows > 16
     assert call(head_dim=256, kv_type=1, ks=A, vs=A) == kvattn.KVATTN_ERR_UNSUPPORTED  # f16 only at 256
     assert call(head_dim=64) == kvattn.KVATTN_ERR_UNSUPPORTED

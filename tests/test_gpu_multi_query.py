@@ -1,8 +1,9 @@
 """GPU parity of causal multi-query decode (kvattn_decode_multi) against the fp64 oracle:
 n_q new tokens per sequence, token t seeing logical positions 0 .. L - n_q + t, the
 G x n_q query rows of a KV head in one 16-row MMA tile (up to 16 rows: the two consumer warps
-split the cells) or two (17 to 32 rows: they split the rows); at head_dim 256 each consumer
-warp takes 8 of up to 16 rows."""
+split the cells) or two (17 to 32 rows: they split the rows), or in row groups of 32 that
+are units of their own (33 to 64 rows); at head_dim 256 each consumer warp takes 8 of up to
+16 rows."""
 import numpy as np
 import pytest
 
@@ -38,6 +39,11 @@ def check(out, lse, wo, wl):
     (5, 5, 2, [640, 33], 64),           # 25 rows: the second warp's last 7 rows are padding
     (17, 1, 2, [300, 17], 32),          # MHA, 17 tokens
     (3, 6, 2, [2047], 256),             # 18 rows (GQA-6)
+    (9, 4, 2, [1000, 9, 4], 128),       # 36 rows: two row groups (32 + 4)
+    (8, 6, 2, [1537, 0], 64),           # 48 rows (GQA-6 verifying 8 tokens), an empty sequence
+    (8, 8, 1, [700, 3], 256),           # 64 rows (GQA-8 verifying 8 tokens), a sequence shorter than n_q
+    (16, 4, 2, [300, 16], 32),          # 64 rows: 16 tokens at GQA-4
+    (33, 1, 2, [200, 40], 32),          # MHA, 33 tokens: the second group holds one row
 ])
 def test_multi_query_contiguous(kvattn, n_q, G, Hk, lens, split):
     import torch
@@ -80,11 +86,11 @@ def test_multi_query_contiguous_d256(kvattn, n_q, G, Hk, lens, split):
     check(out, lse, wo, wl)
 
 
-@pytest.mark.parametrize("n_q,D", [(4, 128), (8, 128), (4, 256)])
-def test_multi_query_plan_with_holes(kvattn, n_q, D):
+@pytest.mark.parametrize("n_q,D,G", [(4, 128, 4), (8, 128, 4), (4, 256, 4), (8, 128, 6), (16, 128, 4)])
+def test_multi_query_plan_with_holes(kvattn, n_q, D, G):
     import torch
     rng = np.random.default_rng(9)
-    Hk, G = 4, 4
+    Hk = 4
     H = Hk * G
     pool = 30
     n_cells = pool * 128
