@@ -106,6 +106,8 @@ struct MergeParams {
     int64_t len_cap;          // clamp for seq_lens (n_cells or plan_stride)
     int n_seq, n_rows;        // rows per sequence (= n_head)
     int head_dim, split;
+    int64_t wide_rows_max;    // decode partials of at most this many rows in all may merge with
+                              // 16-warp CTAs (one per SM); 0: always 8 warps
 };
 
 // Launchers (return cudaError_t of the launch).

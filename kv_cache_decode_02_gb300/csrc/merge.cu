@@ -32,21 +32,21 @@ constexpr int kWeightCache = 4096; // parts whose weights stay in shared memory
 // LSE and O in the same round of independent loads (an empty part's O is 0), and folds
 // them into a running (max, sum, O) with the decode kernel's rescaling.  CPL: float4 chunks
 // of a row per lane; each round keeps BATCH x CPL loads in flight per lane.
-template <int CPL, int BATCH>
+template <int WARPS, int CPL, int BATCH>
 __device__ __forceinline__ void merge_written_rounds(const float* lse_base, const float* o_base, int64_t lse_stride,
                                                      int64_t o_stride, int64_t n_parts, int chunks, int warp, int lane,
                                                      float& mw, float& sw, float4 (&acc)[2]) {
-    for (int64_t q0 = warp; q0 < n_parts; q0 += (int64_t)kMergeWarps * BATCH) {
+    for (int64_t q0 = warp; q0 < n_parts; q0 += (int64_t)WARPS * BATCH) {
         float l[BATCH];
 #pragma unroll
         for (int u = 0; u < BATCH; ++u) {
-            const int64_t q = q0 + (int64_t)u * kMergeWarps;
+            const int64_t q = q0 + (int64_t)u * WARPS;
             l[u] = q < n_parts ? __ldg(lse_base + q * lse_stride) : -INFINITY;
         }
         float4 v[BATCH][CPL];
 #pragma unroll
         for (int u = 0; u < BATCH; ++u) {
-            const int64_t q = q0 + (int64_t)u * kMergeWarps;
+            const int64_t q = q0 + (int64_t)u * WARPS;
 #pragma unroll
             for (int c = 0; c < CPL; ++c) {
                 const int ci = lane + 32 * c;
@@ -85,8 +85,9 @@ __device__ __forceinline__ void merge_written_rounds(const float* lse_base, cons
     }
 }
 
-__global__ void __launch_bounds__(kMergeThreads, 2) merge_kernel(const MergeParams p) {
-    __shared__ float red[kMergeWarps];
+template <int WARPS>
+__global__ void __launch_bounds__(WARPS * 32, 16 / WARPS) merge_kernel(const MergeParams p) {
+    __shared__ float red[WARPS];
     __shared__ float wts[kWeightCache];
     extern __shared__ float4 acc_smem[];  // [warps][head_dim / 4]
 
@@ -123,10 +124,10 @@ __global__ void __launch_bounds__(kMergeThreads, 2) merge_kernel(const MergePara
         // programmatic dependence leaves room for two decode CTAs of the next call beside it
         // while it waits (at 244 registers it left none: 14.7 -> 16.2 us per Qwen3-8B layer).
         if (chunks <= 32)
-            merge_written_rounds<1, 8>(lse_base, o_base, lse_stride, o_stride, n_parts, chunks, warp, lane, mw, sw,
+            merge_written_rounds<WARPS, 1, 8>(lse_base, o_base, lse_stride, o_stride, n_parts, chunks, warp, lane, mw, sw,
                                         acc);
         else
-            merge_written_rounds<2, 4>(lse_base, o_base, lse_stride, o_stride, n_parts, chunks, warp, lane, mw, sw,
+            merge_written_rounds<WARPS, 2, 4>(lse_base, o_base, lse_stride, o_stride, n_parts, chunks, warp, lane, mw, sw,
                                        acc);
         if (lane == 0) {
             red[warp] = mw;
@@ -140,20 +141,20 @@ __global__ void __launch_bounds__(kMergeThreads, 2) merge_kernel(const MergePara
         __syncthreads();
         float M = -INFINITY;
 #pragma unroll
-        for (int w = 0; w < kMergeWarps; ++w) M = fmaxf(M, red[w]);
+        for (int w = 0; w < WARPS; ++w) M = fmaxf(M, red[w]);
         float W = 0.f;
-        float scw[kMergeWarps];
+        float scw[WARPS];
 #pragma unroll
-        for (int w = 0; w < kMergeWarps; ++w) {
+        for (int w = 0; w < WARPS; ++w) {
             scw[w] = (M == -INFINITY || red[w] == -INFINITY) ? 0.f : __expf(red[w] - M);
             W = fmaf(scw[w], wts[w], W);
         }
         float4* out = reinterpret_cast<float4*>(p.out + (int64_t)row * p.head_dim);
-        for (int ci = threadIdx.x; ci < chunks; ci += kMergeThreads) {
+        for (int ci = threadIdx.x; ci < chunks; ci += (WARPS * 32)) {
             float4 t = make_float4(0.f, 0.f, 0.f, 0.f);
             if (W > 0.f) {
 #pragma unroll
-                for (int w = 0; w < kMergeWarps; ++w) {
+                for (int w = 0; w < WARPS; ++w) {
                     const float4 a = acc_smem[w * chunks + ci];
                     t.x = fmaf(scw[w], a.x, t.x);
                     t.y = fmaf(scw[w], a.y, t.y);
@@ -174,7 +175,7 @@ __global__ void __launch_bounds__(kMergeThreads, 2) merge_kernel(const MergePara
 
     // pass 1: maximum LSE (all loads independent)
     float m = -INFINITY;
-    for (int64_t q = threadIdx.x; q < n_parts; q += kMergeThreads) {
+    for (int64_t q = threadIdx.x; q < n_parts; q += (WARPS * 32)) {
         const float l = __ldg(lse_base + q * lse_stride);
         if (q < kWeightCache) wts[q] = l;
         m = fmaxf(m, l);
@@ -185,13 +186,13 @@ __global__ void __launch_bounds__(kMergeThreads, 2) merge_kernel(const MergePara
     __syncthreads();
     float M = red[0];
 #pragma unroll
-    for (int w = 1; w < kMergeWarps; ++w) M = fmaxf(M, red[w]);
+    for (int w = 1; w < WARPS; ++w) M = fmaxf(M, red[w]);
     __syncthreads();
 
     // pass 2: weights exp(LSE_p - M) (0 for empty parts) and their sum
     float wsum = 0.f;
     if (M != -INFINITY) {
-        for (int64_t q = threadIdx.x; q < n_parts; q += kMergeThreads) {
+        for (int64_t q = threadIdx.x; q < n_parts; q += (WARPS * 32)) {
             const float l = q < kWeightCache ? wts[q] : __ldg(lse_base + q * lse_stride);
             const float w = (l == -INFINITY) ? 0.f : __expf(l - M);
             if (q < kWeightCache) wts[q] = w;
@@ -204,7 +205,7 @@ __global__ void __launch_bounds__(kMergeThreads, 2) merge_kernel(const MergePara
     __syncthreads();
     float W = 0.f;
 #pragma unroll
-    for (int w = 0; w < kMergeWarps; ++w) W += red[w];
+    for (int w = 0; w < WARPS; ++w) W += red[w];
 
     // pass 3: weighted sum of the O rows
     float4 acc[kMaxChunks];
@@ -212,11 +213,11 @@ __global__ void __launch_bounds__(kMergeThreads, 2) merge_kernel(const MergePara
     for (int c = 0; c < kMaxChunks; ++c) acc[c] = make_float4(0.f, 0.f, 0.f, 0.f);
     if (W > 0.f) {
         constexpr int kUnroll = 4;
-        for (int64_t q0 = warp; q0 < n_parts; q0 += kMergeWarps * kUnroll) {
+        for (int64_t q0 = warp; q0 < n_parts; q0 += WARPS * kUnroll) {
             float w[kUnroll];
 #pragma unroll
             for (int u = 0; u < kUnroll; ++u) {
-                const int64_t q = q0 + (int64_t)u * kMergeWarps;
+                const int64_t q = q0 + (int64_t)u * WARPS;
                 float wq = 0.f;
                 if (q < n_parts) {
                     if (q < kWeightCache) {
@@ -235,7 +236,7 @@ __global__ void __launch_bounds__(kMergeThreads, 2) merge_kernel(const MergePara
                     float4 v[kUnroll];
 #pragma unroll
                     for (int u = 0; u < kUnroll; ++u) {
-                        const int64_t q = q0 + (int64_t)u * kMergeWarps;
+                        const int64_t q = q0 + (int64_t)u * WARPS;
                         v[u] = w[u] != 0.f ? __ldg(reinterpret_cast<const float4*>(o_base + q * o_stride) + ci)
                                            : make_float4(0.f, 0.f, 0.f, 0.f);
                     }
@@ -257,11 +258,11 @@ __global__ void __launch_bounds__(kMergeThreads, 2) merge_kernel(const MergePara
     }
     __syncthreads();
     float4* out = reinterpret_cast<float4*>(p.out + (int64_t)row * p.head_dim);
-    for (int ci = threadIdx.x; ci < chunks; ci += kMergeThreads) {
+    for (int ci = threadIdx.x; ci < chunks; ci += (WARPS * 32)) {
         float4 t = make_float4(0.f, 0.f, 0.f, 0.f);
         if (W > 0.f) {
 #pragma unroll
-            for (int w = 0; w < kMergeWarps; ++w) {
+            for (int w = 0; w < WARPS; ++w) {
                 const float4 v = acc_smem[w * chunks + ci];
                 t.x += v.x;
                 t.y += v.y;
@@ -289,15 +290,23 @@ cudaError_t launch_merge(const MergeParams& params, cudaStream_t stream, bool pd
     if (rows > (int64_t)INT32_MAX) return cudaErrorInvalidValue;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)rows, 1, 1);
-    cfg.blockDim = dim3(kMergeThreads, 1, 1);
-    cfg.dynamicSmemBytes = kMergeWarps * p.head_dim * sizeof(float);
+    // Rows of decode partials with more than one round of parts for 8 warps (64 parts at
+    // head_dim <= 128, 32 at 256) take 16 warps, half the dependent rounds of loads, when
+    // the rows fit one CTA per SM (such a CTA holds a whole SM's registers, so it runs only
+    // on SMs the decode has left; two waves of them would cost more than the rounds saved).
+    const int64_t round8 = (int64_t)kMergeWarps * (p.head_dim <= 128 ? 8 : 4);
+    const bool wide = p.all_written && p.n_parts > round8 && rows <= p.wide_rows_max;
+    const int warps = wide ? 2 * kMergeWarps : kMergeWarps;
+    cfg.blockDim = dim3(warps * 32, 1, 1);
+    cfg.dynamicSmemBytes = warps * p.head_dim * sizeof(float);
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = pdl ? 1 : 0;
-    return cudaLaunchKernelEx(&cfg, merge_kernel, p);
+    return wide ? cudaLaunchKernelEx(&cfg, merge_kernel<2 * kMergeWarps>, p)
+                : cudaLaunchKernelEx(&cfg, merge_kernel<kMergeWarps>, p);
 }
 
 }  // namespace kvattn
