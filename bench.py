@@ -415,19 +415,9 @@ def bench_workloads(K, torch, stream, peak):
         del kq, vq, kd, vd
 
     # window + pinned-host tail
-    w = inputs.WINDOW_TAIL
+    w, q, k_win, v_win, k_tail, v_tail = window_tail_inputs(torch, inputs)
     N, Hk, D, H = w.n_cells, w.n_head_kv, w.head_dim, w.n_head
     n_tail = N - w.n_window
-    k_win = inputs.normal_f16_torch((2000 + w.number, 1), (w.n_window, Hk, D), "cuda")
-    v_win = inputs.normal_f16_torch((3000 + w.number, 1), (w.n_window, Hk, D), "cuda")
-    k_tail = torch.empty((n_tail, Hk, D), dtype=torch.float16).pin_memory()
-    v_tail = torch.empty((n_tail, Hk, D), dtype=torch.float16).pin_memory()
-    chunk = 65536
-    for lo in range(0, n_tail, chunk):
-        hi = min(n_tail, lo + chunk)
-        k_tail[lo:hi].copy_(inputs.normal_f16_torch((2000 + w.number, 2, lo), (hi - lo, Hk, D), "cuda"))
-        v_tail[lo:hi].copy_(inputs.normal_f16_torch((3000 + w.number, 2, lo), (hi - lo, Hk, D), "cuda"))
-    q = torch.from_numpy(inputs.make_q(w)[0]).cuda()
     wt = K.WindowTail()
     ws = wt.workspace(H, Hk, D, w.n_window, n_tail, w.split, w.tile_cells, w.tail_split)
     out = torch.empty((H, D), dtype=torch.float32, device="cuda")
@@ -789,6 +779,56 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+def window_tail_inputs(torch, inputs):
+    """The window + tail workload: the resident window on the device, the older tail in
+    pinned host memory (filled through the device in 64K-cell pieces), and q."""
+    w = inputs.WINDOW_TAIL
+    N, Hk, D = w.n_cells, w.n_head_kv, w.head_dim
+    n_tail = N - w.n_window
+    k_win = inputs.normal_f16_torch((2000 + w.number, 1), (w.n_window, Hk, D), "cuda")
+    v_win = inputs.normal_f16_torch((3000 + w.number, 1), (w.n_window, Hk, D), "cuda")
+    k_tail = torch.empty((n_tail, Hk, D), dtype=torch.float16).pin_memory()
+    v_tail = torch.empty((n_tail, Hk, D), dtype=torch.float16).pin_memory()
+    chunk = 65536
+    for lo in range(0, n_tail, chunk):
+        hi = min(n_tail, lo + chunk)
+        k_tail[lo:hi].copy_(inputs.normal_f16_torch((2000 + w.number, 2, lo), (hi - lo, Hk, D), "cuda"))
+        v_tail[lo:hi].copy_(inputs.normal_f16_torch((3000 + w.number, 2, lo), (hi - lo, Hk, D), "cuda"))
+    q = torch.from_numpy(inputs.make_q(w)[0]).cuda()
+    return w, q, k_win, v_win, k_tail, v_tail
+
+
+def profile_window_tail(args):
+    """--kernel-reps calls of the window + tail op (staged 1 MiB tiles through the copy
+    kernel, or the tail read in place), for profilers (no timing, no JSON line)."""
+    import torch
+    from kv_cache_decode_02_gb300 import inputs
+    from kv_cache_decode_02_gb300 import kvattn as K
+    w, q, k_win, v_win, k_tail, v_tail = window_tail_inputs(torch, inputs)
+    Hk, D, H = w.n_head_kv, w.head_dim, w.n_head
+    n_tail = w.n_cells - w.n_window
+    out = torch.empty((H, D), dtype=torch.float32, device="cuda")
+    lse = torch.empty((H,), dtype=torch.float32, device="cuda")
+    stream = torch.cuda.current_stream()
+    if args.profile_workload.endswith("_direct"):
+        ws = torch.zeros(K.kvattn_window_tail_direct_workspace_bytes(H, Hk, D, w.n_window, n_tail, w.split,
+                                                                     w.tail_split), dtype=torch.uint8, device="cuda")
+        for _ in range(args.kernel_reps):
+            K.window_tail_direct(q, k_win, v_win, k_tail, v_tail, split=w.split, tail_split=w.tail_split,
+                                 out=out, lse=lse, ws=ws, stream=stream)
+    else:
+        wt = K.WindowTail()
+        ws = wt.workspace(H, Hk, D, w.n_window, n_tail, w.split, w.tile_cells, w.tail_split)
+        copy_stream = torch.cuda.Stream()
+        for _ in range(args.kernel_reps):
+            wt(q, k_win, v_win, k_tail, v_tail, split=w.split, tile_cells=w.tile_cells, tail_split=w.tail_split,
+               out=out, lse=lse, ws=ws, compute_stream=stream, copy_stream=copy_stream)
+        torch.cuda.synchronize()
+        wt.close()
+    torch.cuda.synchronize()
+    print(f"{args.profile_workload}: {args.kernel_reps} calls done")
+
+
 def PROFILE_WORKLOADS(inputs):
     return (inputs.Q8_LONG_D128, inputs.Q8_LONG_D256, inputs.Q8Q4_LONG_D128, inputs.Q8Q4_LONG_D256,
             inputs.Q4_LONG_D128, inputs.Q4_LONG_D256)
@@ -835,11 +875,16 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=12.0)
     ap.add_argument("--profile-workload", choices=["q8_0_n131072_d128", "q8_0_n131072_d256", "q8_0_q4_0_n131072_d128",
                                                    "q8_0_q4_0_n131072_d256", "q4_0_n131072_d128",
-                                                   "q4_0_n131072_d256"],
-                    help="only launch this workload's split decode --kernel-reps times (for ncu)")
+                                                   "q4_0_n131072_d256", "window_tail_n524288",
+                                                   "window_tail_n524288_direct"],
+                    help="only launch this workload's split decode (window + tail: the whole op) "
+                         "--kernel-reps times (for ncu)")
     args = ap.parse_args()
     if args.profile_workload:
-        profile_workload(args)
+        if args.profile_workload.startswith("window_tail"):
+            profile_window_tail(args)
+        else:
+            profile_workload(args)
         return
     if args.warmup < 3:
         args.warmup = 3
