@@ -9,7 +9,7 @@ import pytest
 
 import oracle
 from oracle import plan_oracle as po
-from tests.gpu_util import TOL_LSE, TOL_O, dev
+from tests.gpu_util import TOL_LSE, TOL_O, TOL_RMSE_O, dev
 
 pytestmark = pytest.mark.gpu
 
@@ -25,6 +25,7 @@ def check(out, lse, wo, wl):
     fin = np.isfinite(wl)
     assert np.max(np.abs(l[fin] - wl[fin]), initial=0.0) <= TOL_LSE
     assert np.max(np.abs(o - wo)) <= TOL_O
+    assert np.sqrt(np.mean((o.astype(np.float64) - wo) ** 2)) <= TOL_RMSE_O
     assert np.all(o[~fin] == 0)
 
 
