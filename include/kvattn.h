@@ -234,7 +234,8 @@ size_t kvattn_decode_multi_workspace_bytes(int n_seq, int n_q, int n_head, int h
  *  rows the rows run as groups of 32, each group reading the split's K/V, the second
  *  mostly from L2), or a
  *  quantised type (Q8_0, Q8_0_Q4_0, Q4_0) with (n_head / n_head_kv) * n_q <= 16;
- *  head_dim 256 with kv_type f16 and (n_head / n_head_kv) * n_q <= 16.  n_q >= 1.
+ *  head_dim 256 with kv_type f16 and (n_head / n_head_kv) * n_q <= 64 (row groups of 16).
+ *  n_q >= 1.
  *  ws: kvattn_decode_multi_workspace_bytes(...) bytes.
  * Errors: as kvattn_decode.
  */

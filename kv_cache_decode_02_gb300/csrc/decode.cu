@@ -769,8 +769,9 @@ __device__ __forceinline__ void mq_consumers(const SplitDecodeParams& p, uint64_
     }
 }
 
-// Multi-query consumers at head_dim 256 (up to 16 query rows per KV head): warp w takes rows
-// 8w .. 8w+7 (M = 16 of the q.K^T MMA with rows 8-15 zero, N = 8 of the P V MMA, as the
+// Multi-query consumers at head_dim 256 (up to 16 query rows per KV head; beyond that, row
+// groups of 16 that are units of their own): warp w takes rows 8w .. 8w+7 of its unit's
+// group (M = 16 of the q.K^T MMA with rows 8-15 zero, N = 8 of the P V MMA, as the
 // single-query kernel) over both 16-cell halves of every tile, folding each row's causal
 // limit into its lanes' cell mask, and writes its rows at the unit's end (no exchange).
 template <int D>
@@ -784,9 +785,10 @@ __device__ __forceinline__ void mq_consumers_rows8(const SplitDecodeParams& p, u
     const int H = p.n_head, GQ = p.group, NQ = p.n_q;
     const int rows = GQ * NQ;
     const int64_t HR = (int64_t)NQ * H;
-    const int row0 = 8 * warp;
+    // first row of this warp in a unit: 16 rows per row group (more than 16 rows per KV head)
+    auto first_row = [&](const Unit& y) { return 16 * y.rg + 8 * warp; };
     constexpr float kLn2 = 0.69314718055994530942f;
-    auto load_q = [&](int s, int g, uint32_t (&qa)[D / 16][2]) {
+    auto load_q = [&](int s, int g, int row0, uint32_t (&qa)[D / 16][2]) {
         const int r = row0 + gq;
         const bool ok = r < rows;
         const int t = ok ? r / GQ : 0;
@@ -806,6 +808,7 @@ __device__ __forceinline__ void mq_consumers_rows8(const SplitDecodeParams& p, u
     for (int64_t u = blockIdx.x; u < n_units && !stop; u += gridDim.x) {
         const Unit x = unit_at(p, u);
         const int64_t part = (int64_t)x.s * p.part_stride + p.part_base + x.split_idx;
+        const int row0 = first_row(x);
         if (x.n_tiles == 0) {
             if (x.write_empty) {
                 for (int idx = lane; idx < 8 * D; idx += 32) {
@@ -820,7 +823,7 @@ __device__ __forceinline__ void mq_consumers_rows8(const SplitDecodeParams& p, u
             }
             continue;
         }
-        if (qa_unit != u) load_q(x.s, x.g, qa);
+        if (qa_unit != u) load_q(x.s, x.g, row0, qa);
         float oacc[D / 16][4];
         float m_run = -INFINITY, l_run = 0.f;
 #pragma unroll
@@ -879,7 +882,7 @@ __device__ __forceinline__ void mq_consumers_rows8(const SplitDecodeParams& p, u
         if (un < n_units) {
             const Unit y = unit_at(p, un);
             if (y.n_tiles > 0) {
-                load_q(y.s, y.g, qa);
+                load_q(y.s, y.g, first_row(y), qa);
                 qa_unit = un;
             }
         }

@@ -69,9 +69,13 @@ def test_multi_query_contiguous(kvattn, n_q, G, Hk, lens, split):
     (3, 3, 2, [513, 0], 256),           # 9 rows (the second warp holds one), an empty sequence
     (16, 1, 2, [100, 16], 32),          # MHA, 16 tokens
     (5, 2, 4, [2049], 512),             # 10 rows over a ragged last split
+    (5, 4, 2, [300, 5, 2], 32),         # 20 rows: row groups of 16 and 4
+    (8, 4, 2, [777, 8], 128),           # 32 rows (GQA-4 verifying 8 tokens): two row groups
+    (8, 8, 1, [500, 3, 0], 64),         # 64 rows: four row groups, short and empty sequences
 ])
 def test_multi_query_contiguous_d256(kvattn, n_q, G, Hk, lens, split):
-    """head_dim 256 (Gemma-family layers): up to 16 query rows, 8 per consumer warp."""
+    """head_dim 256 (Gemma-family layers): 8 query rows per consumer warp, row groups of 16
+    beyond 16 rows."""
     import torch
     rng = np.random.default_rng(n_q * 100 + G + 3)
     S, D = len(lens), 256
@@ -87,7 +91,8 @@ def test_multi_query_contiguous_d256(kvattn, n_q, G, Hk, lens, split):
     check(out, lse, wo, wl)
 
 
-@pytest.mark.parametrize("n_q,D,G", [(4, 128, 4), (8, 128, 4), (4, 256, 4), (8, 128, 6), (16, 128, 4)])
+@pytest.mark.parametrize("n_q,D,G", [(4, 128, 4), (8, 128, 4), (4, 256, 4), (8, 128, 6), (16, 128, 4),
+                                     (8, 256, 4)])
 def test_multi_query_plan_with_holes(kvattn, n_q, D, G):
     import torch
     rng = np.random.default_rng(9)
