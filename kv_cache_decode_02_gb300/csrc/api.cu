@@ -355,10 +355,10 @@ int decode_impl(const void* q, const void* k_cache, const void* v_cache, const v
     const bool multi = n_q > 0;
     if (!multi) n_q = 1;
     const bool merge = part_o_user == nullptr;
-    // multi-query rows per KV head beyond one unit's (32 at head_dim 128, 16 at 256) run as
-    // row groups of that size, units of their own
+    // multi-query rows per KV head beyond one unit's (f16: 32 at head_dim 128, 16 at 256;
+    // quantised: 16) run as row groups of that size, units of their own
     const int mq_rows = (n_head_kv >= 1 && n_head >= n_head_kv) ? (n_head / n_head_kv) * n_q : 0;
-    const int rg_rows = head_dim == 256 ? 16 : 32;
+    const int rg_rows = (head_dim == 256 || kv_type != KVATTN_KV_F16) ? 16 : 32;
     const int n_rg = (multi && mq_rows > rg_rows) ? (mq_rows + rg_rows - 1) / rg_rows : 1;
     if (split == 0 && merge) {  // kvattn_decode picks the split (partials need it fixed)
         if (!valid_kv_type(kv_type)) return KVATTN_ERR_INVALID_ARG;
@@ -373,13 +373,12 @@ int decode_impl(const void* q, const void* k_cache, const void* v_cache, const v
     int st = check_shape(shape);
     if (st != KVATTN_OK) return st;
     if (multi && (int64_t)n_seq * n_q * n_head > (int64_t)INT32_MAX) return KVATTN_ERR_UNSUPPORTED;
-    // multi-query: head_dim 128 -- f16 up to 64 query rows per KV head (two row groups), the
-    // quantised caches up to 16; head_dim 256 -- f16 up to 64 (four row groups)
+    // multi-query: up to 64 query rows per KV head -- head_dim 128 with any cache type, head_dim
+    // 256 with f16
     if (multi) {
         const int rows = mq_rows;
-        const bool ok = valid_kv_type(kv_type) &&
-                        ((head_dim == 128 && rows <= (kv_type == KVATTN_KV_F16 ? 64 : 16)) ||
-                         (head_dim == 256 && kv_type == KVATTN_KV_F16 && rows <= 64));
+        const bool ok = valid_kv_type(kv_type) && rows <= 64 &&
+                        (head_dim == 128 || (head_dim == 256 && kv_type == KVATTN_KV_F16));
         if (!ok) return KVATTN_ERR_UNSUPPORTED;
         if ((int64_t)n_seq * ((max_len + split - 1) / split) * n_head_kv * n_rg > (int64_t)INT32_MAX)
             return KVATTN_ERR_UNSUPPORTED;

@@ -1638,11 +1638,11 @@ __device__ __forceinline__ void q4v_chunk(uint32_t kb, uint32_t vb, const unsign
 // keys) or load_q_frags_q4k (4-bit keys).
 template <int D, bool KQ4>
 __device__ __forceinline__ void load_q_frags_mq_q8(const SplitDecodeParams& p, int s, int g, int gq, int tq,
-                                                   uint32_t (&qa)[D / 16][4]) {
+                                                   int row0, uint32_t (&qa)[D / 16][4]) {
     const int rows = p.group * p.n_q;
 #pragma unroll
     for (int half = 0; half < 2; ++half) {
-        const int r = gq + 8 * half;
+        const int r = row0 + gq + 8 * half;
         const bool ok = r < rows;
         const int t = ok ? r / p.group : 0;
         const int h = g * p.group + (ok ? r % p.group : 0);
@@ -1969,7 +1969,7 @@ __device__ __forceinline__ void q8_self_body(const SplitDecodeParams& p) {
     const int gq = lane >> 2;
     const int tq = lane & 3;
     const int H = p.n_head;
-    const int64_t n_units = (int64_t)p.n_seq * p.unit_splits * p.n_head_kv;
+    const int64_t n_units = (int64_t)p.n_seq * p.unit_splits * p.n_head_kv * (p.n_rg > 1 ? p.n_rg : 1);
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < W * S; ++i) mbar_init(smem_addr(&full_bar[i]), 64);
@@ -2170,7 +2170,8 @@ __device__ __forceinline__ void q8_self_body(const SplitDecodeParams& p) {
     }
 
     if constexpr (MQ) {
-        // ---- causal multi-query consumers: 16 query rows (token r / G, head g G + r % G) ----
+        // ---- causal multi-query consumers: 16 query rows (token r / G, head g G + r % G), or
+        // row groups of 16 that are units of their own beyond that ----
         const int GQ = p.group, NQ = p.n_q;
         const int rows = GQ * NQ;
         const int64_t HR = (int64_t)NQ * H;  // partial rows per (sequence, split)
@@ -2182,11 +2183,13 @@ __device__ __forceinline__ void q8_self_body(const SplitDecodeParams& p) {
         for (int64_t u = blockIdx.x; u < n_units && !stop; u += gridDim.x) {
             const Unit x = unit_at(p, u);
             const int64_t part = (int64_t)x.s * p.part_stride + p.part_base + x.split_idx;
+            const int row0 = 16 * x.rg;  // the unit's first query row
             if (x.n_tiles == 0) {
                 if (warp == 0 && x.write_empty) {
-                    for (int idx = lane; idx < rows * D; idx += 32) {
-                        const int r = idx / D;
-                        const int d = idx - r * D;
+                    const int n_rows = rows - row0 < 16 ? rows - row0 : 16;
+                    for (int idx = lane; idx < n_rows * D; idx += 32) {
+                        const int r = row0 + idx / D;
+                        const int d = idx % D;
                         const int64_t row = (int64_t)(r / GQ) * H + x.g * GQ + r % GQ;
                         p.part_o[(part * HR + row) * D + d] = 0.f;
                         if (d == 0) p.part_lse[part * HR + row] = -INFINITY;
@@ -2194,15 +2197,15 @@ __device__ __forceinline__ void q8_self_body(const SplitDecodeParams& p) {
                 }
                 continue;
             }
-            if (qa_unit != u) load_q_frags_mq_q8<D, KQ4>(p, x.s, x.g, gq, tq, qa);
+            if (qa_unit != u) load_q_frags_mq_q8<D, KQ4>(p, x.s, x.g, gq, tq, row0, qa);
             float oacc[2][D / 16][4];
 #pragma unroll
             for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
                 for (int i = 0; i < D / 16; ++i) oacc[nt][i][0] = oacc[nt][i][1] = oacc[nt][i][2] = oacc[nt][i][3] = 0.f;
             float m_run[2] = {-INFINITY, -INFINITY}, l_run[2] = {0.f, 0.f};
-            // causal limit (logical position, exclusive) of the lane's rows gq and gq + 8
-            const int64_t lim_row[2] = {x.len - NQ + 1 + gq / GQ, x.len - NQ + 1 + (gq + 8) / GQ};
+            // causal limit (logical position, exclusive) of the lane's rows row0 + gq and row0 + gq + 8
+            const int64_t lim_row[2] = {x.len - NQ + 1 + (row0 + gq) / GQ, x.len - NQ + 1 + (row0 + gq + 8) / GQ};
             const int nch = unit_chunks(x);
             for (int j = warp; j < nch; j += W, ++C) {
                 const int st = (int)(C % (uint32_t)S);
@@ -2252,7 +2255,7 @@ __device__ __forceinline__ void q8_self_body(const SplitDecodeParams& p) {
             if (un < n_units) {
                 const Unit y = unit_at(p, un);
                 if (y.n_tiles > 0) {
-                    load_q_frags_mq_q8<D, KQ4>(p, y.s, y.g, gq, tq, qa);
+                    load_q_frags_mq_q8<D, KQ4>(p, y.s, y.g, gq, tq, 16 * y.rg, qa);
                     qa_unit = un;
                 }
             }
@@ -2343,7 +2346,7 @@ __device__ __forceinline__ void q8_self_body(const SplitDecodeParams& p) {
             for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
                 for (int e = 0; e < 2; ++e) {
-                    const int r = 8 * nt + 2 * tq + e;
+                    const int r = row0 + 8 * nt + 2 * tq + e;
                     if (r < rows) {
                         const int64_t row = (int64_t)(r / GQ) * H + x.g * GQ + r % GQ;
                         float* orow = p.part_o + (part * HR + row) * D;

@@ -188,9 +188,13 @@ ORACLE = {"q8": oracle.decode_q8_0, "q8k_q4v": oracle.decode_q8_0_q4_0, "q4kv": 
     (8, 2, 4, [513, 300], 256),
     (16, 1, 2, [100, 16], 32),          # MHA, 16 tokens
     (3, 5, 2, [2049, 0], 512),          # 15 rows, an empty sequence
+    (5, 4, 2, [300, 5, 2], 32),         # 20 rows: row groups of 16 and 4
+    (8, 4, 2, [777, 8, 3], 64),         # 32 rows (GQA-4 verifying 8 tokens): two row groups
+    (8, 8, 1, [513, 0], 128),           # 64 rows: four row groups, an empty sequence
 ])
 def test_multi_query_quantised_contiguous(kvattn, n_q, G, Hk, lens, split, kind):
-    """Quantised caches: the self-loading kernels with the whole 16-row M of the MMA."""
+    """Quantised caches: the self-loading kernels with the whole 16-row M of the MMA, row
+    groups of 16 beyond 16 rows."""
     import torch
     rng = np.random.default_rng(n_q * 100 + G + 7)
     S, D = len(lens), 128
@@ -205,12 +209,13 @@ def test_multi_query_quantised_contiguous(kvattn, n_q, G, Hk, lens, split, kind)
     check(out, lse, wo, wl)
 
 
+@pytest.mark.parametrize("n_q", [4, 8])
 @pytest.mark.parametrize("kind", ["q8", "q8k_q4v", "q4kv"])
-def test_multi_query_quantised_plan_with_holes(kvattn, kind):
+def test_multi_query_quantised_plan_with_holes(kvattn, kind, n_q):
     """Scattered and record-aligned plan entries with -1 holes over NaN-scaled cells."""
     import torch
     rng = np.random.default_rng(19)
-    Hk, G, n_q, D = 4, 4, 4, 128
+    Hk, G, D = 4, 4, 128
     H = Hk * G
     pool = 30
     n_cells = pool * 128
