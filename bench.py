@@ -801,6 +801,27 @@ def window_tail_inputs(torch, inputs):
     return w, q, k_win, v_win, k_tail, v_tail
 
 
+def profile_verify(args):
+    """--kernel-reps calls of causal multi-query decode on the Qwen3-8B-shaped layer (16384
+    cells, 32/8 heads, split 256) verifying 4 or 8 draft tokens, for profilers."""
+    import torch
+    from kv_cache_decode_02_gb300 import inputs
+    from kv_cache_decode_02_gb300 import kvattn as K
+    w = inputs.QWEN3_8B_LAYER
+    n_q = int(args.profile_workload.rsplit("nq", 1)[1])
+    N, H, Hk, D = w.n_cells, w.n_head, w.n_head_kv, w.head_dim
+    k = inputs.normal_f16_torch((2000 + w.number, 0), (N, Hk, D), "cuda")
+    v = inputs.normal_f16_torch((3000 + w.number, 0), (N, Hk, D), "cuda")
+    q = inputs.normal_f16_torch((1000 + w.number, 9), (1, n_q, H, D), "cuda")
+    lens = torch.tensor([N], dtype=torch.int32, device="cuda")
+    ws = torch.zeros(K.kvattn_decode_multi_workspace_bytes(1, n_q, H, D, N, w.split), dtype=torch.uint8,
+                     device="cuda")
+    for _ in range(args.kernel_reps):
+        K.decode_multi(q, k, v, lens, split=w.split, ws=ws)
+    torch.cuda.synchronize()
+    print(f"{args.profile_workload}: {args.kernel_reps} calls done")
+
+
 def profile_window_tail(args):
     """--kernel-reps calls of the window + tail op (staged 1 MiB tiles through the copy
     kernel, or the tail read in place), for profilers (no timing, no JSON line)."""
@@ -879,13 +900,16 @@ def main():
     ap.add_argument("--profile-workload", choices=["q8_0_n131072_d128", "q8_0_n131072_d256", "q8_0_q4_0_n131072_d128",
                                                    "q8_0_q4_0_n131072_d256", "q4_0_n131072_d128",
                                                    "q4_0_n131072_d256", "window_tail_n524288",
-                                                   "window_tail_n524288_direct"],
+                                                   "window_tail_n524288_direct", "qwen3_8b_layer_verify_nq4",
+                                                   "qwen3_8b_layer_verify_nq8"],
                     help="only launch this workload's split decode (window + tail: the whole op) "
                          "--kernel-reps times (for ncu)")
     args = ap.parse_args()
     if args.profile_workload:
         if args.profile_workload.startswith("window_tail"):
             profile_window_tail(args)
+        elif args.profile_workload.startswith("qwen3_8b_layer_verify"):
+            profile_verify(args)
         else:
             profile_workload(args)
         return

@@ -358,6 +358,8 @@ int decode_impl(const void* q, const void* k_cache, const void* v_cache, const v
     // multi-query rows per KV head beyond one unit's (f16: 32 at head_dim 128, 16 at 256;
     // quantised: 16) run as row groups of that size, units of their own
     const int mq_rows = (n_head_kv >= 1 && n_head >= n_head_kv) ? (n_head / n_head_kv) * n_q : 0;
+    // (f16 head_dim 128 in groups of 16 instead, each group a cell-split unit: 33.4 against
+    // 29.3 us for 32 rows, 49.8 against 41.6 us for 64, on a 16384-cell 8-KV-head layer)
     const int rg_rows = (head_dim == 256 || kv_type != KVATTN_KV_F16) ? 16 : 32;
     const int n_rg = (multi && mq_rows > rg_rows) ? (mq_rows + rg_rows - 1) / rg_rows : 1;
     if (split == 0 && merge) {  // kvattn_decode picks the split (partials need it fixed)
@@ -462,6 +464,7 @@ int decode_impl(const void* q, const void* k_cache, const void* v_cache, const v
         p.n_q = n_q;
         p.mq = multi ? 1 : 0;
         p.n_rg = n_rg;
+        p.rg_rows = rg_rows;
         p.n_stages = pick_stages(kv_type, head_dim, n_split * n_head_kv * n_rg * n_seq, multi);
         p.scale_log2 = (float)((double)scale * 1.4426950408889634074);
         apply_debug_hooks(p);

@@ -565,9 +565,10 @@ __device__ __forceinline__ void mq_consumers(const SplitDecodeParams& p, uint64_
     const int tq = lane & 3;
     const int H = p.n_head, GQ = p.group, NQ = p.n_q;
     const int rows = GQ * NQ;
-    const bool rsplit = rows > 16;       // the warps split the rows instead of the cells
-    // first row of this warp in a unit: 32 rows per row group (more than 32 rows per KV head)
-    auto first_row = [&](const Unit& y) { return 32 * y.rg + (rsplit ? 16 * warp : 0); };
+    const int grp = p.n_rg > 1 ? p.rg_rows : rows;  // rows of one unit (a row group's, or all)
+    const bool rsplit = grp > 16;  // the warps split the rows instead of the cells
+    // first row of this warp in a unit
+    auto first_row = [&](const Unit& y) { return p.rg_rows * y.rg + (rsplit ? 16 * warp : 0); };
     const int64_t HR = (int64_t)NQ * H;  // partial rows per (sequence, split)
     float4* xo = reinterpret_cast<float4*>(xchg);      // [2][D/16][32 lanes]
     float* xm = reinterpret_cast<float*>(xo + 2 * (D / 16) * 32);  // [16] max
@@ -583,9 +584,9 @@ __device__ __forceinline__ void mq_consumers(const SplitDecodeParams& p, uint64_
         const int row0 = first_row(x);
         if (x.n_tiles == 0) {
             if (warp == 0 && x.write_empty) {
-                // the unit's rows: its row group's 32, or every row without row groups
-                const int rb = 32 * x.rg;
-                const int n_rows = p.n_rg > 1 ? (rows - rb < 32 ? rows - rb : 32) : rows;
+                // the unit's rows: its row group's, or every row without row groups
+                const int rb = p.rg_rows * x.rg;
+                const int n_rows = rows - rb < grp ? rows - rb : grp;
                 for (int idx = lane; idx < n_rows * D; idx += 32) {
                     const int r = rb + idx / D;
                     const int d = idx % D;
@@ -752,7 +753,7 @@ __device__ __forceinline__ void mq_consumers(const SplitDecodeParams& p, uint64_
             for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
                 for (int e = 0; e < 2; ++e) {
-                    const int r = 8 * nt + 2 * tq + e;
+                    const int r = row0 + 8 * nt + 2 * tq + e;
                     if (r < rows) {
                         const int64_t row = (int64_t)(r / GQ) * H + x.g * GQ + r % GQ;
                         float* orow = p.part_o + (part * HR + row) * D;
@@ -786,7 +787,7 @@ __device__ __forceinline__ void mq_consumers_rows8(const SplitDecodeParams& p, u
     const int rows = GQ * NQ;
     const int64_t HR = (int64_t)NQ * H;
     // first row of this warp in a unit: 16 rows per row group (more than 16 rows per KV head)
-    auto first_row = [&](const Unit& y) { return 16 * y.rg + 8 * warp; };
+    auto first_row = [&](const Unit& y) { return p.rg_rows * y.rg + 8 * warp; };
     constexpr float kLn2 = 0.69314718055994530942f;
     auto load_q = [&](int s, int g, int row0, uint32_t (&qa)[D / 16][2]) {
         const int r = row0 + gq;
@@ -2183,10 +2184,10 @@ __device__ __forceinline__ void q8_self_body(const SplitDecodeParams& p) {
         for (int64_t u = blockIdx.x; u < n_units && !stop; u += gridDim.x) {
             const Unit x = unit_at(p, u);
             const int64_t part = (int64_t)x.s * p.part_stride + p.part_base + x.split_idx;
-            const int row0 = 16 * x.rg;  // the unit's first query row
+            const int row0 = p.rg_rows * x.rg;  // the unit's first query row
             if (x.n_tiles == 0) {
                 if (warp == 0 && x.write_empty) {
-                    const int n_rows = rows - row0 < 16 ? rows - row0 : 16;
+                    const int n_rows = p.n_rg > 1 ? (rows - row0 < p.rg_rows ? rows - row0 : p.rg_rows) : rows;
                     for (int idx = lane; idx < n_rows * D; idx += 32) {
                         const int r = row0 + idx / D;
                         const int d = idx % D;
@@ -2255,7 +2256,7 @@ __device__ __forceinline__ void q8_self_body(const SplitDecodeParams& p) {
             if (un < n_units) {
                 const Unit y = unit_at(p, un);
                 if (y.n_tiles > 0) {
-                    load_q_frags_mq_q8<D, KQ4>(p, y.s, y.g, gq, tq, 16 * y.rg, qa);
+                    load_q_frags_mq_q8<D, KQ4>(p, y.s, y.g, gq, tq, p.rg_rows * y.rg, qa);
                     qa_unit = un;
                 }
             }

@@ -69,10 +69,11 @@ struct SplitDecodeParams {
     int n_seq, n_head, n_head_kv, group, split;
     int n_q;                  // query tokens per sequence (multi-query decode; 1 otherwise)
     int mq;                   // 1: the multi-query kernel
-    int n_rg;                 // multi-query row groups of 32 rows per KV head (0 or 1: one group
-                              // holding every row); the units become (sequence, split, KV head,
-                              // row group), row group fastest, so the groups of one split run
-                              // side by side and share its K/V bytes through L2
+    int n_rg;                 // multi-query row groups per KV head (0 or 1: one group holding
+                              // every row); the units become (sequence, split, KV head, row
+                              // group), row group fastest, so the groups of one split run side
+                              // by side and share its K/V bytes through L2
+    int rg_rows;              // query rows per row group (when n_rg > 1)
     int n_stages;
     int use_tma;              // tiles that are one physical run load through tmap_k/tmap_v
     int write_beyond;         // splits past a sequence's length still write (0, -inf)
