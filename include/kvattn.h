@@ -230,11 +230,11 @@ size_t kvattn_decode_multi_workspace_bytes(int n_seq, int n_q, int n_head, int h
  *  out, lse device float [n_seq][n_q][n_head][head_dim], [n_seq][n_q][n_head].
  *  Other arguments: as kvattn_decode.
  *  Limits (UNSUPPORTED otherwise): n_q >= 1 and (n_head / n_head_kv) * n_q <= 64 query
- *  rows per KV head (n_q <= 8 at up to 8 query heads per KV head), with head_dim 128 and
- *  any kv_type, or head_dim 256 and kv_type f16.  Rows beyond one unit's share (f16 head_dim
- *  128: 32; f16 head_dim 256 and the quantised types: 16) run as row groups, units of
- *  their own that read the split's K/V again, mostly from L2 (the groups of a split run
- *  side by side).
+ *  rows per KV head (n_q <= 8 at up to 8 query heads per KV head); any kv_type; head_dim
+ *  128 or 256.  Rows beyond one unit's share (f16: 32 at head_dim 128, 16 at 256; the
+ *  quantised types: 16 at head_dim 128, 8 at 256) run as row groups, units of their own
+ *  that read the split's K/V again, mostly from L2 (the groups of a split run side by
+ *  side).
  *  ws: kvattn_decode_multi_workspace_bytes(...) bytes.
  * Errors: as kvattn_decode.
  */

@@ -356,11 +356,12 @@ int decode_impl(const void* q, const void* k_cache, const void* v_cache, const v
     if (!multi) n_q = 1;
     const bool merge = part_o_user == nullptr;
     // multi-query rows per KV head beyond one unit's (f16: 32 at head_dim 128, 16 at 256;
-    // quantised: 16) run as row groups of that size, units of their own
+    // quantised: 16 at head_dim 128, 8 at 256) run as row groups of that size, units of their
+    // own
     const int mq_rows = (n_head_kv >= 1 && n_head >= n_head_kv) ? (n_head / n_head_kv) * n_q : 0;
     // (f16 head_dim 128 in groups of 16 instead, each group a cell-split unit: 33.4 against
     // 29.3 us for 32 rows, 49.8 against 41.6 us for 64, on a 16384-cell 8-KV-head layer)
-    const int rg_rows = (head_dim == 256 || kv_type != KVATTN_KV_F16) ? 16 : 32;
+    const int rg_rows = kv_type == KVATTN_KV_F16 ? (head_dim == 256 ? 16 : 32) : (head_dim == 256 ? 8 : 16);
     const int n_rg = (multi && mq_rows > rg_rows) ? (mq_rows + rg_rows - 1) / rg_rows : 1;
     if (split == 0 && merge) {  // kvattn_decode picks the split (partials need it fixed)
         if (!valid_kv_type(kv_type)) return KVATTN_ERR_INVALID_ARG;
@@ -375,12 +376,10 @@ int decode_impl(const void* q, const void* k_cache, const void* v_cache, const v
     int st = check_shape(shape);
     if (st != KVATTN_OK) return st;
     if (multi && (int64_t)n_seq * n_q * n_head > (int64_t)INT32_MAX) return KVATTN_ERR_UNSUPPORTED;
-    // multi-query: up to 64 query rows per KV head -- head_dim 128 with any cache type, head_dim
-    // 256 with f16
+    // multi-query: up to 64 query rows per KV head, any cache type, head_dim 128 or 256
     if (multi) {
         const int rows = mq_rows;
-        const bool ok = valid_kv_type(kv_type) && rows <= 64 &&
-                        (head_dim == 128 || (head_dim == 256 && kv_type == KVATTN_KV_F16));
+        const bool ok = valid_kv_type(kv_type) && rows <= 64 && (head_dim == 128 || head_dim == 256);
         if (!ok) return KVATTN_ERR_UNSUPPORTED;
         if ((int64_t)n_seq * ((max_len + split - 1) / split) * n_head_kv * n_rg > (int64_t)INT32_MAX)
             return KVATTN_ERR_UNSUPPORTED;

@@ -338,14 +338,31 @@ __device__ __forceinline__ void consume_tile_staged(uint32_t kb, uint32_t vb, ui
     for (int mt = 0; mt < 8; ++mt) mma_16816(oacc[mt], vf[mt][0], vf[mt][1], vf[mt][2], vf[mt][3], pb[0], pb[1]);
 }
 
+// Query row of lane row gq: single-query (rg < 0) the query head g G + gq of sequence s; in
+// the 8-row multi-query units of the quantised head_dim-256 kernels, row r = 8 rg + gq of
+// the unit's KV head, token r / G, query head g G + r % G.  ok: the row exists.
+template <int D>
+__device__ __forceinline__ const uint32_t* q_row_ptr(const SplitDecodeParams& p, int s, int g, int gq, int rg,
+                                                     bool& ok) {
+    if (rg < 0) {
+        ok = gq < p.group;
+        const int h = g * p.group + (ok ? gq : 0);
+        return reinterpret_cast<const uint32_t*>(p.q + ((int64_t)s * p.n_head + h) * D);
+    }
+    const int r = 8 * rg + gq;
+    ok = r < p.group * p.n_q;
+    const int t = ok ? r / p.group : 0;
+    const int h = g * p.group + (ok ? r % p.group : 0);
+    return reinterpret_cast<const uint32_t*>(p.q + (((int64_t)s * p.n_q + t) * p.n_head + h) * D);
+}
+
 // Loads the query fragments of (sequence s, KV head g): the GQA rows of the head fill the
 // first `group` rows of the m16n8k16 A operand (rows 8-15 and rows >= group stay zero).
 template <int KVT, int D>
 __device__ __forceinline__ void load_q_frags(const SplitDecodeParams& p, int s, int g, int gq, int tq,
-                                             uint32_t (&qa)[D / 16][2]) {
-    const bool row_ok = gq < p.group;
-    const int h = g * p.group + (row_ok ? gq : 0);
-    const uint32_t* qrow = reinterpret_cast<const uint32_t*>(p.q + ((int64_t)s * p.n_head + h) * D);
+                                             uint32_t (&qa)[D / 16][2], int rg = -1) {
+    bool row_ok;
+    const uint32_t* qrow = q_row_ptr<D>(p, s, g, gq, rg, row_ok);
 #pragma unroll
     for (int kk = 0; kk < D / 16; ++kk) {
         int d0, d1;
@@ -366,10 +383,9 @@ __device__ __forceinline__ void load_q_frags(const SplitDecodeParams& p, int s, 
 // (e+1, e+3) with e = 32b + 16h + 4tq.
 template <int D>
 __device__ __forceinline__ void load_q_frags_q4k(const SplitDecodeParams& p, int s, int g, int gq, int tq,
-                                                 uint32_t (&qa)[D / 16][2]) {
-    const bool row_ok = gq < p.group;
-    const int h = g * p.group + (row_ok ? gq : 0);
-    const uint32_t* qrow = reinterpret_cast<const uint32_t*>(p.q + ((int64_t)s * p.n_head + h) * D);
+                                                 uint32_t (&qa)[D / 16][2], int rg = -1) {
+    bool row_ok;
+    const uint32_t* qrow = q_row_ptr<D>(p, s, g, gq, rg, row_ok);
 #pragma unroll
     for (int kk = 0; kk < D / 16; ++kk) {
         const int e = 32 * (kk >> 1) + 16 * (kk & 1) + 4 * tq;
@@ -1946,10 +1962,14 @@ __device__ __forceinline__ void cursor_seek(const SplitDecodeParams& p, ChunkCur
     }
 }
 
-template <int D, int W, int S, bool VQ4 = false, bool KQ4 = false, bool MQ = false>
+// MQ: multi-query units of up to 16 query rows (head_dim 128).  MQ8: multi-query units of up
+// to 8 rows on the single-query geometry (head_dim 256), rows 8 rg .. 8 rg + 7 of the unit's
+// row group rg, each lane's cell mask cut at its row's causal limit.
+template <int D, int W, int S, bool VQ4 = false, bool KQ4 = false, bool MQ = false, bool MQ8 = false>
 __device__ __forceinline__ void q8_self_body(const SplitDecodeParams& p) {
     static_assert(VQ4 || !KQ4, "4-bit keys come with 4-bit values");
     static_assert(!MQ || D == 128, "multi-query: head_dim 128");
+    static_assert(!(MQ && MQ8), "one multi-query layout");
     constexpr int KVT = KVATTN_KV_Q8_0;  // 8-bit keys' query fragment order (load_q_frags)
     using Q = Q8Self<D, VQ4, KQ4, MQ>;
     using G = Geom<KVT, D>;
@@ -2376,27 +2396,49 @@ __device__ __forceinline__ void q8_self_body(const SplitDecodeParams& p) {
         uint32_t X = 0;  // exchanges
         bool stop = false;
         constexpr float kLn2 = 0.69314718055994530942f;
+        // multi-query units (MQ8): row r = 8 rg + r_local of the unit's KV head is partial row
+        // (r / G) H + g G + r % G of n_q H per (sequence, split)
+        auto mq_row = [&](const Unit& y, int r_local, bool& ok) -> int64_t {
+            const int r = 8 * y.rg + r_local;
+            ok = r < p.group * p.n_q;
+            return (int64_t)(r / p.group) * H + y.g * p.group + r % p.group;
+        };
         for (int64_t u = blockIdx.x; u < n_units && !stop; u += gridDim.x) {
             const Unit x = unit_at(p, u);
             const int64_t part = (int64_t)x.s * p.part_stride + p.part_base + x.split_idx;
             if (x.n_tiles == 0) {
                 if (warp == 0 && x.write_empty) {
-                    for (int idx = lane; idx < p.group * D; idx += 32) {
-                        const int r = idx / D;
-                        const int d = idx - r * D;
-                        const int h = x.g * p.group + r;
-                        p.part_o[(part * H + h) * D + d] = 0.f;
-                        if (d == 0) p.part_lse[part * H + h] = -INFINITY;
+                    if constexpr (MQ8) {
+                        const int64_t HR = (int64_t)p.n_q * H;
+                        for (int idx = lane; idx < 8 * D; idx += 32) {
+                            bool ok;
+                            const int64_t row = mq_row(x, idx / D, ok);
+                            const int d = idx % D;
+                            if (ok) {
+                                p.part_o[(part * HR + row) * D + d] = 0.f;
+                                if (d == 0) p.part_lse[part * HR + row] = -INFINITY;
+                            }
+                        }
+                    } else {
+                        for (int idx = lane; idx < p.group * D; idx += 32) {
+                            const int r = idx / D;
+                            const int d = idx - r * D;
+                            const int h = x.g * p.group + r;
+                            p.part_o[(part * H + h) * D + d] = 0.f;
+                            if (d == 0) p.part_lse[part * H + h] = -INFINITY;
+                        }
                     }
                 }
                 continue;
             }
             if (qa_unit != u) {
                 if (KQ4)
-                    load_q_frags_q4k<D>(p, x.s, x.g, gq, tq, qa);
+                    load_q_frags_q4k<D>(p, x.s, x.g, gq, tq, qa, MQ8 ? x.rg : -1);
                 else
-                    load_q_frags<KVT, D>(p, x.s, x.g, gq, tq, qa);
+                    load_q_frags<KVT, D>(p, x.s, x.g, gq, tq, qa, MQ8 ? x.rg : -1);
             }
+            // MQ8: causal limit (logical position, exclusive) of the lane's row 8 rg + gq
+            const int64_t lim_row = MQ8 ? x.len - p.n_q + 1 + (8 * x.rg + gq) / p.group : 0;
             float oacc[D / 16][4];
             float m_run = -INFINITY, l_run = 0.f;
 #pragma unroll
@@ -2418,16 +2460,22 @@ __device__ __forceinline__ void q8_self_body(const SplitDecodeParams& p) {
                 // (fragments are read straight from the stage: staging them in registers first
                 // measured slower here, the extra registers spill at this CTA count)
                 if (mask != 0u) {
+                    uint32_t lmask = mask;  // this lane's cells
+                    if constexpr (MQ8) {    // the lane's row sees the chunk's cells below its limit
+                        const int64_t rel = lim_row - (x.i0 + (int64_t)j * kChunkCells);
+                        const int lim = rel < 0 ? 0 : (rel > kChunkCells ? kChunkCells : (int)rel);
+                        lmask &= (1u << lim) - 1u;
+                    }
                     if constexpr (VQ4) {
                         if (swz)
-                            q4v_chunk<D, true, KQ4>(kb, vb, ks, vs, mask, lane, qa, oacc, m_run, l_run, p.scale_log2);
+                            q4v_chunk<D, true, KQ4>(kb, vb, ks, vs, lmask, lane, qa, oacc, m_run, l_run, p.scale_log2);
                         else
-                            q4v_chunk<D, false, KQ4>(kb, vb, ks, vs, mask, lane, qa, oacc, m_run, l_run, p.scale_log2);
+                            q4v_chunk<D, false, KQ4>(kb, vb, ks, vs, lmask, lane, qa, oacc, m_run, l_run, p.scale_log2);
                     } else {
                         if (swz)
-                            q8_chunk_swz<D>(kb, vb, ks, vs, mask, lane, qa, oacc, m_run, l_run, p.scale_log2);
+                            q8_chunk_swz<D>(kb, vb, ks, vs, lmask, lane, qa, oacc, m_run, l_run, p.scale_log2);
                         else
-                            consume_tile<KVT, D, false, Q::kPlane>(kb, vb, ks, vs, mask, 0, lane, qa, oacc, m_run,
+                            consume_tile<KVT, D, false, Q::kPlane>(kb, vb, ks, vs, lmask, 0, lane, qa, oacc, m_run,
                                                                    l_run, p.scale_log2);
                     }
                 }
@@ -2449,9 +2497,9 @@ __device__ __forceinline__ void q8_self_body(const SplitDecodeParams& p) {
                 const Unit y = unit_at(p, un);
                 if (y.n_tiles > 0) {
                     if (KQ4)
-                        load_q_frags_q4k<D>(p, y.s, y.g, gq, tq, qa);
+                        load_q_frags_q4k<D>(p, y.s, y.g, gq, tq, qa, MQ8 ? y.rg : -1);
                     else
-                        load_q_frags<KVT, D>(p, y.s, y.g, gq, tq, qa);
+                        load_q_frags<KVT, D>(p, y.s, y.g, gq, tq, qa, MQ8 ? y.rg : -1);
                     qa_unit = un;
                 }
             }
@@ -2531,9 +2579,18 @@ __device__ __forceinline__ void q8_self_body(const SplitDecodeParams& p) {
             }
 #pragma unroll
             for (int e = 0; e < 2; ++e) {
-                const int r = 2 * tq + e;
-                if (r < p.group) {
-                    float* orow = p.part_o + (part * H + x.g * p.group + r) * D;
+                bool ok;
+                int64_t prow;  // partial row index (part, row)
+                if constexpr (MQ8) {
+                    const int64_t row = mq_row(x, 2 * tq + e, ok);
+                    prow = part * ((int64_t)p.n_q * H) + row;
+                } else {
+                    const int r = 2 * tq + e;
+                    ok = r < p.group;
+                    prow = part * H + x.g * p.group + r;
+                }
+                if (ok) {
+                    float* orow = p.part_o + prow * D;
 #pragma unroll
                     for (int b = 0; b < D / 32; ++b) {
                         if constexpr (VQ4) {
@@ -2546,7 +2603,7 @@ __device__ __forceinline__ void q8_self_body(const SplitDecodeParams& p) {
                                 make_float4(oacc[2 * b][e], oacc[2 * b][2 + e], oacc[2 * b + 1][e], oacc[2 * b + 1][2 + e]);
                         }
                     }
-                    if (gq == 0) p.part_lse[part * H + x.g * p.group + r] = lse[e];
+                    if (gq == 0) p.part_lse[prow] = lse[e];
                 }
             }
             ++X;
@@ -2618,6 +2675,20 @@ __global__ void __launch_bounds__(kQ8WMQ * 32, kQ8BMQ)
     split_decode_mq_q4_d128(const __grid_constant__ SplitDecodeParams p) {
     q8_self_body<128, kQ8WMQ, kQ8SMQ, true, true, true>(p);
 }
+// Multi-query decode over the quantised caches at head_dim 256: 8-row units on the
+// single-query geometry.
+__global__ void __launch_bounds__(kQ8W256 * 32, kQ8B256)
+    split_decode_mq_q8_d256(const __grid_constant__ SplitDecodeParams p) {
+    q8_self_body<256, kQ8W256, kQ8S256, false, false, false, true>(p);
+}
+__global__ void __launch_bounds__(kQ8W256 * 32, kQ8B256)
+    split_decode_mq_q8q4_d256(const __grid_constant__ SplitDecodeParams p) {
+    q8_self_body<256, kQ8W256, kQ8S256, true, false, false, true>(p);
+}
+__global__ void __launch_bounds__(kQ8W256 * 32, kQ8B256)
+    split_decode_mq_q4_d256(const __grid_constant__ SplitDecodeParams p) {
+    q8_self_body<256, kQ8W256, kQ8S256, true, true, false, true>(p);
+}
 // Q4_0 keys and values.
 __global__ void __launch_bounds__(kQ8W128 * 32, kQ8B128)
     split_decode_q4_d128(const __grid_constant__ SplitDecodeParams p) {
@@ -2630,9 +2701,16 @@ __global__ void __launch_bounds__(kQ8W256 * 32, kQ8B256)
 
 const void* kernel_for(int kv_type, int head_dim, bool mq = false) {
     if (mq) {
-        if (kv_type == KVATTN_KV_Q8_0) return reinterpret_cast<const void*>(split_decode_mq_q8_d128);
-        if (kv_type == KVATTN_KV_Q8_0_Q4_0) return reinterpret_cast<const void*>(split_decode_mq_q8q4_d128);
-        if (kv_type == KVATTN_KV_Q4_0) return reinterpret_cast<const void*>(split_decode_mq_q4_d128);
+        const bool d256 = head_dim == 256;
+        if (kv_type == KVATTN_KV_Q8_0)
+            return d256 ? reinterpret_cast<const void*>(split_decode_mq_q8_d256)
+                        : reinterpret_cast<const void*>(split_decode_mq_q8_d128);
+        if (kv_type == KVATTN_KV_Q8_0_Q4_0)
+            return d256 ? reinterpret_cast<const void*>(split_decode_mq_q8q4_d256)
+                        : reinterpret_cast<const void*>(split_decode_mq_q8q4_d128);
+        if (kv_type == KVATTN_KV_Q4_0)
+            return d256 ? reinterpret_cast<const void*>(split_decode_mq_q4_d256)
+                        : reinterpret_cast<const void*>(split_decode_mq_q4_d128);
         return head_dim == 256 ? reinterpret_cast<const void*>(split_decode_mq_f16_d256)
                                : reinterpret_cast<const void*>(split_decode_mq_f16_d128);
     }
@@ -2666,9 +2744,11 @@ int split_decode_stage_bytes(int kv_type, int head_dim) {
 // the end-of-unit exchange area and the stage ring.
 // Q8_0 kernels have a fixed geometry (n_stages is ignored for them).
 int split_decode_smem_bytes(int kv_type, int head_dim, int n_stages, bool mq) {
-    if (kv_type == KVATTN_KV_Q8_0 && mq) return q8_self_smem<128, kQ8WMQ, kQ8SMQ, false, false, true>();
-    if (kv_type == KVATTN_KV_Q8_0_Q4_0 && mq) return q8_self_smem<128, kQ8WMQ, kQ8SMQ, true, false, true>();
-    if (kv_type == KVATTN_KV_Q4_0 && mq) return q8_self_smem<128, kQ8WMQ, kQ8SMQ, true, true, true>();
+    // (the head_dim-256 multi-query kernels run on the single-query geometry)
+    const bool mq128 = mq && head_dim == 128;
+    if (kv_type == KVATTN_KV_Q8_0 && mq128) return q8_self_smem<128, kQ8WMQ, kQ8SMQ, false, false, true>();
+    if (kv_type == KVATTN_KV_Q8_0_Q4_0 && mq128) return q8_self_smem<128, kQ8WMQ, kQ8SMQ, true, false, true>();
+    if (kv_type == KVATTN_KV_Q4_0 && mq128) return q8_self_smem<128, kQ8WMQ, kQ8SMQ, true, true, true>();
     if (kv_type == KVATTN_KV_Q8_0)
         return head_dim == 128 ? q8_self_smem<128, kQ8W128, kQ8S128>() : q8_self_smem<256, kQ8W256, kQ8S256>();
     if (kv_type == KVATTN_KV_Q8_0_Q4_0)
@@ -2684,7 +2764,7 @@ int split_decode_smem_bytes(int kv_type, int head_dim, int n_stages, bool mq) {
 }
 
 int split_decode_block_threads(int kv_type, int head_dim, bool mq) {
-    if (kv_type != KVATTN_KV_F16 && mq) return kQ8WMQ * 32;
+    if (kv_type != KVATTN_KV_F16 && mq && head_dim == 128) return kQ8WMQ * 32;
     if (kv_type != KVATTN_KV_F16) return (head_dim == 128 ? kQ8W128 : kQ8W256) * 32;
     return kThreads;
 }

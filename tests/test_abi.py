@@ -180,7 +180,7 @@ def test_multi_query_limits(kvattn):
         return kvattn.lib.kvattn_decode_multi(*a.values())
     assert call(n_q=17) == kvattn.KVATTN_ERR_UNSUPPORTED           # 4 x 17 = 68 rows > 64
     assert call(head_dim=256, n_q=17) == kvattn.KVATTN_ERR_UNSUPPORTED  # head_dim 256: 68 rows > 64
-    assert call(head_dim=256, kv_type=1, ks=A, vs=A) == kvattn.KVATTN_ERR_UNSUPPORTED  # f16 only at 256
+    assert call(head_dim=256, kv_type=1, ks=A, vs=A, n_q=17) == kvattn.KVATTN_ERR_UNSUPPORTED  # 68 rows
     assert call(head_dim=64) == kvattn.KVATTN_ERR_UNSUPPORTED
     assert call(kv_type=1, ks=A, vs=A, n_q=17) == kvattn.KVATTN_ERR_UNSUPPORTED  # Q8_0: 68 rows > 64
     assert call(kv_type=3, ks=A, vs=A, n_q=17) == kvattn.KVATTN_ERR_UNSUPPORTED  # Q4_0: 68 rows > 64

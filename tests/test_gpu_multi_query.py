@@ -241,10 +241,65 @@ def test_multi_query_quantised_plan_with_holes(kvattn, kind, n_q):
 
 
 @pytest.mark.parametrize("kind", ["q8", "q8k_q4v", "q4kv"])
-def test_multi_query_quantised_one_token_equals_single_query(kvattn, kind):
+@pytest.mark.parametrize("n_q,G,Hk,lens,split", [
+    (1, 4, 2, [1000, 37], 128),         # 4 rows
+    (2, 4, 2, [700, 1], 64),            # 8 rows, a sequence shorter than n_q
+    (4, 4, 2, [777, 4, 3], 64),         # 16 rows: two 8-row groups
+    (3, 5, 2, [2049, 0], 512),          # 15 rows, an empty sequence
+    (5, 2, 4, [300], 32),               # 10 rows: groups of 8 and 2
+    (8, 8, 1, [500, 3], 64),            # 64 rows: eight groups
+])
+def test_multi_query_quantised_d256(kvattn, n_q, G, Hk, lens, split, kind):
+    """head_dim 256 over the quantised caches: 8-row units on the single-query geometry,
+    each lane's cells cut at its row's causal limit."""
+    import torch
+    rng = np.random.default_rng(n_q * 100 + G + 11)
+    S, D = len(lens), 256
+    N = max(max(lens), 1)
+    H = G * Hk
+    q = rand_f16(rng, (S, n_q, H, D))
+    kq, kd, vq, vd = q8_cache(rng, (S, N, Hk, D), kind)
+    out, lse = kvattn.decode_multi(dev(q), dev(kq), dev(vq), dev(np.array(lens, np.int32)), split=split,
+                                   n_cells=N, max_len=N, k_scales=dev(kd), v_scales=dev(vd))
+    torch.cuda.synchronize()
+    wo, wl = oracle.decode_multi(ORACLE[kind], q, lens, kq, kd, vq, vd)
+    check(out, lse, wo, wl)
+
+
+@pytest.mark.parametrize("kind", ["q8", "q8k_q4v", "q4kv"])
+def test_multi_query_quantised_d256_plan_with_holes(kvattn, kind):
+    import torch
+    rng = np.random.default_rng(29)
+    Hk, G, n_q, D = 2, 4, 4, 256
+    H = Hk * G
+    pool = 20
+    n_cells = pool * 128
+    kq, kd, vq, vd = q8_cache(rng, (n_cells, Hk, D), kind)
+    perm = rng.permutation(pool)
+    encoded, selected = [], []
+    for recs in (perm[:3], perm[3:4], perm[4:9]):
+        cells = (recs[:, None] * 128 + np.arange(128)[None]).reshape(-1)
+        sel = cells[rng.random(cells.size) >= 0.2]
+        encoded.append(sel.astype(np.int64)[rng.permutation(sel.size)])
+        selected.append(sel)
+    unused = np.setdiff1d(np.arange(n_cells), np.concatenate(selected))
+    kd[unused] = np.nan
+    vd[unused] = np.nan
+    plan, lens = kvattn.build_cell_plan(encoded, n_cells)
+    q = rand_f16(rng, (3, n_q, H, D))
+    out, lse = kvattn.decode_multi(dev(q), dev(kq), dev(vq), dev(lens), split=128, cell_plan=dev(plan),
+                                   n_cells=n_cells, k_scales=dev(kd), v_scales=dev(vd))
+    torch.cuda.synchronize()
+    wo, wl = oracle.decode_multi(ORACLE[kind], q, lens.tolist(), kq, kd, vq, vd, plan=plan)
+    check(out, lse, wo, wl)
+
+
+@pytest.mark.parametrize("D", [128, 256])
+@pytest.mark.parametrize("kind", ["q8", "q8k_q4v", "q4kv"])
+def test_multi_query_quantised_one_token_equals_single_query(kvattn, kind, D):
     import torch
     rng = np.random.default_rng(20)
-    S, N, H, Hk, D = 2, 3000, 32, 8, 128
+    S, N, H, Hk = 2, 3000, 32, 8
     q = rand_f16(rng, (S, 1, H, D))
     kq, kd, vq, vd = q8_cache(rng, (S, N, Hk, D), kind)
     lens = dev(np.array([3000, 1234], np.int32))
