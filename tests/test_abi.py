@@ -184,6 +184,10 @@ def test_multi_query_limits(kvattn):
     assert call(head_dim=64) == kvattn.KVATTN_ERR_UNSUPPORTED
     assert call(kv_type=1, ks=A, vs=A, n_q=17) == kvattn.KVATTN_ERR_UNSUPPORTED  # Q8_0: 68 rows > 64
     assert call(kv_type=3, ks=A, vs=A, n_q=17) == kvattn.KVATTN_ERR_UNSUPPORTED  # Q4_0: 68 rows > 64
+    # 100000 sequences x 2048 splits x 8 KV heads fit 32 bits, x 2 row groups (64 rows) do not
+    big = dict(n_seq=100000, max_len=65536, n_cells=65536, split=32)
+    assert call(n_q=16, **big) == kvattn.KVATTN_ERR_UNSUPPORTED
+    assert call(n_q=8, **big) == kvattn.KVATTN_ERR_WORKSPACE                  # one group: only the workspace
     assert call(kv_type=1) == kvattn.KVATTN_ERR_INVALID_ARG                   # Q8_0 without scales
     assert call(n_q=0) == kvattn.KVATTN_ERR_INVALID_ARG
     assert call(q=None) == kvattn.KVATTN_ERR_INVALID_ARG
