@@ -346,6 +346,21 @@ def bench_workloads(K, torch, stream, peak):
     valid = int((plan >= 0).sum())
     add(w.name, valid * w.n_head_kv * w.head_dim * 4, timed(fn), {"valid_cells": valid,
                                                                  "plan_entries": int(plens.sum())})
+    # the same slots verifying 8 draft tokens each: 48 query rows per KV head (two row groups);
+    # split 512 (the partials of 8 tokens x 48 heads per split make split 128 cost 394 us
+    # against 311 us at 256 or 512)
+    n_q, vsplit = 8, 512
+    qm = inputs.normal_f16_torch((1000 + w.number, 8), (w.n_seq, n_q, w.n_head, w.head_dim), "cuda")
+    wsm = torch.zeros(K.kvattn_decode_multi_workspace_bytes(w.n_seq, n_q, w.n_head, w.head_dim, plan.shape[1],
+                                                            vsplit), dtype=torch.uint8, device="cuda")
+    om = torch.empty((w.n_seq, n_q, w.n_head, w.head_dim), dtype=torch.float32, device="cuda")
+    lm = torch.empty((w.n_seq, n_q, w.n_head), dtype=torch.float32, device="cuda")
+    fm = lambda: K.kvattn_decode_multi(qm, kk, vv, None, None, 0, w.n_cells, plan_d, plan.shape[1], lens_d,
+                                       w.n_seq, plan.shape[1], n_q, w.n_head, w.n_head_kv, w.head_dim, vsplit,
+                                       1 / math.sqrt(w.head_dim), om, lm, wsm, wsm.numel(), stream)
+    fm()
+    add(w.name + "_verify_nq8", valid * w.n_head_kv * w.head_dim * 4, timed(fm),
+        {"n_q": n_q, "query_rows_per_kv_head": n_q * w.n_head // w.n_head_kv, "split": vsplit})
     del kk, vv
 
     # a serving batch: 64 sequences x 4096 cells in one call, the automatic split

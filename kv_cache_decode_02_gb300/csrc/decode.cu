@@ -943,7 +943,10 @@ __device__ __forceinline__ void mq_consumers_rows8(const SplitDecodeParams& p, u
 // At the end of a unit warp 1 hands its running max, sum and unnormalised O to warp 0
 // through an exchange area guarded by two mbarriers, and warp 0 writes the unit's partial
 // (normalised O and LSE), so no CTA-wide barrier stalls the ring between units.
-template <int KVT, int D, bool MQ = false>
+// MQ8: multi-query units of up to 8 query rows on the single-query consumers (row r = 8 rg +
+// gq of the unit's KV head, token r / G, head g G + r % G; each lane's cells cut at its row's
+// causal limit), for small verification batches.
+template <int KVT, int D, bool MQ = false, bool MQ8 = false>
 __device__ __forceinline__ void split_decode_body(const SplitDecodeParams& p) {
     static_assert(KVT == KVATTN_KV_F16, "Q8_0 runs in q8_self_body");
     static_assert(!MQ || D == 128 || D == 256, "multi-query decode: head_dim 128 or 256");
@@ -1213,17 +1216,32 @@ __device__ __forceinline__ void split_decode_body(const SplitDecodeParams& p) {
             const int64_t part = (int64_t)x.s * p.part_stride + p.part_base + x.split_idx;
             if (x.n_tiles == 0) {
                 if (warp == 0 && x.write_empty) {
-                    for (int idx = lane; idx < p.group * D; idx += 32) {
-                        const int r = idx / D;
-                        const int d = idx - r * D;
-                        const int h = x.g * p.group + r;
-                        p.part_o[(part * H + h) * D + d] = 0.f;
-                        if (d == 0) p.part_lse[part * H + h] = -INFINITY;
+                    if constexpr (MQ8) {
+                        const int64_t HR = (int64_t)p.n_q * H;
+                        for (int idx = lane; idx < 8 * D; idx += 32) {
+                            const int r = 8 * x.rg + idx / D;
+                            const int d = idx % D;
+                            if (r < p.group * p.n_q) {
+                                const int64_t row = (int64_t)(r / p.group) * H + x.g * p.group + r % p.group;
+                                p.part_o[(part * HR + row) * D + d] = 0.f;
+                                if (d == 0) p.part_lse[part * HR + row] = -INFINITY;
+                            }
+                        }
+                    } else {
+                        for (int idx = lane; idx < p.group * D; idx += 32) {
+                            const int r = idx / D;
+                            const int d = idx - r * D;
+                            const int h = x.g * p.group + r;
+                            p.part_o[(part * H + h) * D + d] = 0.f;
+                            if (d == 0) p.part_lse[part * H + h] = -INFINITY;
+                        }
                     }
                 }
                 continue;
             }
-            if (qa_unit != u) load_q_frags<KVT, D>(p, x.s, x.g, gq, tq, qa);
+            if (qa_unit != u) load_q_frags<KVT, D>(p, x.s, x.g, gq, tq, qa, MQ8 ? x.rg : -1);
+            // MQ8: causal limit (logical position, exclusive) of the lane's row 8 rg + gq
+            const int64_t lim_row = MQ8 ? x.len - p.n_q + 1 + (8 * x.rg + gq) / p.group : 0;
             float oacc[D / 16][4];
             float m_run = -INFINITY, l_run = 0.f;
 #pragma unroll
@@ -1243,6 +1261,12 @@ __device__ __forceinline__ void split_decode_body(const SplitDecodeParams& p) {
                 unsigned char* stage = stages + st * G::kBytes;
                 const uint32_t ebar = smem_addr(&empty_bar[st]);
                 bool released = false;
+                uint32_t lmask = mask;  // this lane's cells
+                if constexpr (MQ8) {
+                    const int64_t rel = lim_row - (x.i0 + (int64_t)t * kTileCells + warp * kWarpCells);
+                    const int lim = rel < 0 ? 0 : (rel > kWarpCells ? kWarpCells : (int)rel);
+                    lmask &= (lim >= 32 ? 0xffffffffu : (1u << lim)) - 1u;
+                }
                 if (mask != 0u) {
                     if (swz) {
                         const uint32_t kb = smem_addr(stage);
@@ -1263,22 +1287,22 @@ __device__ __forceinline__ void split_decode_body(const SplitDecodeParams& p) {
                             __syncwarp();
                         }
                         if constexpr (D == 128) {
-                            consume_tile_staged<true>(kb, vb, mask, warp, lane, ebar, qa, oacc, m_run, l_run,
+                            consume_tile_staged<true>(kb, vb, lmask, warp, lane, ebar, qa, oacc, m_run, l_run,
                                                       p.scale_log2);
                             released = true;
                         } else {
-                            consume_tile<KVT, D, true>(kb, vb, nullptr, nullptr, mask, warp, lane, qa, oacc, m_run,
+                            consume_tile<KVT, D, true>(kb, vb, nullptr, nullptr, lmask, warp, lane, qa, oacc, m_run,
                                                        l_run, p.scale_log2);
                         }
                     } else {
                         const uint32_t kb = smem_addr(stage);
                         const uint32_t vb = kb + G::kPadSection;
                         if constexpr (D == 128) {
-                            consume_tile_staged<false>(kb, vb, mask, warp, lane, ebar, qa, oacc, m_run, l_run,
+                            consume_tile_staged<false>(kb, vb, lmask, warp, lane, ebar, qa, oacc, m_run, l_run,
                                                        p.scale_log2);
                             released = true;
                         } else {
-                            consume_tile<KVT, D, false>(kb, vb, nullptr, nullptr, mask, warp, lane, qa, oacc, m_run,
+                            consume_tile<KVT, D, false>(kb, vb, nullptr, nullptr, lmask, warp, lane, qa, oacc, m_run,
                                                         l_run, p.scale_log2);
                         }
                     }
@@ -1296,7 +1320,7 @@ __device__ __forceinline__ void split_decode_body(const SplitDecodeParams& p) {
             if (un < n_units) {
                 const Unit y = unit_at(p, un);
                 if (y.n_tiles > 0) {
-                    load_q_frags<KVT, D>(p, y.s, y.g, gq, tq, qa);
+                    load_q_frags<KVT, D>(p, y.s, y.g, gq, tq, qa, MQ8 ? y.rg : -1);
                     qa_unit = un;
                 }
             }
@@ -1349,15 +1373,26 @@ __device__ __forceinline__ void split_decode_body(const SplitDecodeParams& p) {
                 mbar_arrive(smem_addr(&xchg_bar[1]));
 #pragma unroll
                 for (int e = 0; e < 2; ++e) {
-                    const int r = 2 * tq + e;
-                    if (r < p.group) {
-                        float* orow = p.part_o + (part * H + x.g * p.group + r) * D;
+                    bool ok;
+                    int64_t prow;  // partial row index (part, row)
+                    if constexpr (MQ8) {
+                        const int r = 8 * x.rg + 2 * tq + e;
+                        ok = r < p.group * p.n_q;
+                        prow = part * ((int64_t)p.n_q * H) + (int64_t)(r / p.group) * H + x.g * p.group +
+                               r % p.group;
+                    } else {
+                        const int r = 2 * tq + e;
+                        ok = r < p.group;
+                        prow = part * H + x.g * p.group + r;
+                    }
+                    if (ok) {
+                        float* orow = p.part_o + prow * D;
 #pragma unroll
                         for (int mt = 0; mt < D / 16; ++mt) {
                             orow[out_dim<KVT>(mt, 0, gq)] = oacc[mt][e];
                             orow[out_dim<KVT>(mt, 1, gq)] = oacc[mt][2 + e];
                         }
-                        if (gq == 0) p.part_lse[part * H + x.g * p.group + r] = lse[e];
+                        if (gq == 0) p.part_lse[prow] = lse[e];
                     }
                 }
             }
@@ -2664,6 +2699,14 @@ __global__ void __launch_bounds__(kThreads, KVATTN_F16_D256_MIN_CTAS)
 __global__ void __launch_bounds__(kThreads) split_decode_mq_f16_d128(const __grid_constant__ SplitDecodeParams p) {
     split_decode_body<KVATTN_KV_F16, 128, true>(p);
 }
+// Up to 8 query rows per unit on the single-query geometry (small verification batches).
+__global__ void __launch_bounds__(kThreads) split_decode_mq8_f16_d128(const __grid_constant__ SplitDecodeParams p) {
+    split_decode_body<KVATTN_KV_F16, 128, false, true>(p);
+}
+__global__ void __launch_bounds__(kThreads, KVATTN_F16_D256_MIN_CTAS)
+    split_decode_mq8_f16_d256(const __grid_constant__ SplitDecodeParams p) {
+    split_decode_body<KVATTN_KV_F16, 256, false, true>(p);
+}
 __global__ void __launch_bounds__(kThreads, KVATTN_F16_D256_MIN_CTAS)
     split_decode_mq_f16_d256(const __grid_constant__ SplitDecodeParams p) {
     split_decode_body<KVATTN_KV_F16, 256, true>(p);
@@ -2721,7 +2764,13 @@ __global__ void __launch_bounds__(kQ8W256 * 32, kQ8B256)
     q8_self_body<256, kQ8W256, kQ8S256, true, true>(p);
 }
 
-const void* kernel_for(int kv_type, int head_dim, bool mq = false) {
+// mode: 0 single-query, 1 multi-query, 2 f16 multi-query of up to 8 rows per unit on the
+// single-query geometry (same resources as mode 0).
+const void* kernel_for(int kv_type, int head_dim, int mode = 0) {
+    if (mode == 2)
+        return head_dim == 256 ? reinterpret_cast<const void*>(split_decode_mq8_f16_d256)
+                               : reinterpret_cast<const void*>(split_decode_mq8_f16_d128);
+    const bool mq = mode == 1;
     if (mq) {
         const bool d256 = head_dim == 256;
         if (kv_type == KVATTN_KV_Q8_0)
@@ -2797,7 +2846,7 @@ int split_decode_max_stages() { return kMaxStages; }
 int split_decode_threads() { return kThreads; }
 
 cudaError_t split_decode_occupancy(int kv_type, int head_dim, int n_stages, bool mq, int* blocks) {
-    const void* fn = kernel_for(kv_type, head_dim, mq);
+    const void* fn = kernel_for(kv_type, head_dim, mq ? 1 : 0);
     cudaError_t err = set_smem_attr(fn);
     if (err != cudaSuccess) return err;
     return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks, fn, split_decode_block_threads(kv_type, head_dim, mq),
@@ -2806,14 +2855,14 @@ cudaError_t split_decode_occupancy(int kv_type, int head_dim, int n_stages, bool
 
 cudaError_t launch_split_decode(const SplitDecodeParams& p, int kv_type, int head_dim, unsigned grid_ctas,
                                 cudaStream_t stream, bool pdl) {
-    const bool mq = p.mq != 0;
-    const void* fn = kernel_for(kv_type, head_dim, mq);
-    static std::once_flag once[64][16];
-    static cudaError_t attr_err[64][16];
+    const bool mq = p.mq == 1;  // (mode 2 has the single-query resources)
+    const void* fn = kernel_for(kv_type, head_dim, p.mq);
+    static std::once_flag once[64][18];
+    static cudaError_t attr_err[64][18];
     int dev = 0;
     cudaError_t err = cudaGetDevice(&dev);
     if (err != cudaSuccess) return err;
-    const int which = (mq ? 8 : 0) + 2 * kv_type + (head_dim == 256 ? 1 : 0);
+    const int which = p.mq == 2 ? 16 + (head_dim == 256 ? 1 : 0) : (mq ? 8 : 0) + 2 * kv_type + (head_dim == 256 ? 1 : 0);
     std::call_once(once[dev & 63][which], [&] { attr_err[dev & 63][which] = set_smem_attr(fn); });
     if (attr_err[dev & 63][which] != cudaSuccess) return attr_err[dev & 63][which];
     cudaLaunchConfig_t cfg = {};

@@ -68,7 +68,8 @@ struct SplitDecodeParams {
     uint32_t stall_tx;        // test hook: extra bytes expected on the first tile (never arrive)
     int n_seq, n_head, n_head_kv, group, split;
     int n_q;                  // query tokens per sequence (multi-query decode; 1 otherwise)
-    int mq;                   // 1: the multi-query kernel
+    int mq;                   // 1: the multi-query kernels; 2: f16 multi-query units of up to 8
+                              // rows on the single-query kernels (single-query resources)
     int n_rg;                 // multi-query row groups per KV head (0 or 1: one group holding
                               // every row); the units become (sequence, split, KV head, row
                               // group), row group fastest, so the groups of one split run side

@@ -30,8 +30,10 @@ def check(out, lse, wo, wl):
 
 
 @pytest.mark.parametrize("n_q,G,Hk,lens,split", [
-    (1, 4, 2, [1000, 37], 128),
-    (2, 4, 2, [1000, 1], 128),          # sequence 1 shorter than n_q: token 0 sees nothing
+    (1, 4, 2, [1000, 37], 128),         # one token: the single-query kernels
+    (2, 4, 2, [1000, 1], 128),          # 8 rows (single-query kernels, per-row causal masks); sequence 1 shorter than n_q
+    (3, 2, 4, [515, 2, 0], 64),         # 6 rows, ragged, an empty sequence
+    (8, 1, 2, [97, 8], 32),             # MHA, 8 tokens: 8 rows
     (4, 4, 2, [777, 4, 3], 64),         # 16 rows per KV head
     (8, 2, 4, [513, 300], 256),
     (16, 1, 4, [100, 16], 32),          # MHA, 16 tokens
@@ -312,14 +314,15 @@ def test_multi_query_quantised_one_token_equals_single_query(kvattn, kind, D):
     assert np.max(np.abs(ml.cpu().numpy()[:, 0] - sl.cpu().numpy())) <= 1e-5
 
 
-@pytest.mark.parametrize("kind", ["f16", "f16_d256", "q8"])
+@pytest.mark.parametrize("kind", ["f16", "f16_d256", "q8", "f16_8rows"])
 def test_multi_query_bounded_wait_reports_timeout_and_context_survives(kvattn, monkeypatch, kind):
     """The multi-query kernels' pipeline waits are bounded: a first tile that expects bytes
     no copy delivers (host test switch) ends in the timeout status bit, and the next call is
-    clean."""
+    clean.  (f16_8rows: 8 query rows per KV head, the single-query kernels' multi-query mode.)"""
     import torch
     rng = np.random.default_rng(23)
-    S, N, H, Hk, n_q = 1, 600, 16, 4, 4
+    S, N, H, Hk = 1, 600, 16, 4
+    n_q = 2 if kind == "f16_8rows" else 4
     D = 256 if kind == "f16_d256" else 128
     q = rand_f16(rng, (S, n_q, H, D))
     if kind.startswith("f16"):
