@@ -225,7 +225,8 @@ size_t kvattn_decode_multi_workspace_bytes(int n_seq, int n_q, int n_head, int h
  * counts them, token t sits at logical position L - n_q + t and attends to the logical
  * positions 0 .. L - n_q + t (plan entries or cells, -1 holes masked); a token whose window
  * is empty gets O = 0, LSE = -inf.  The G x n_q query rows of each KV head share every K/V
- * byte read from HBM (one or two 16-row MMA tiles, up to 32 rows).
+ * byte read from HBM (one or two 16-row MMA tiles, up to 32 rows).  n_q = 1 is exactly
+ * kvattn_decode (and runs its kernels).
  *  q        device half [n_seq][n_q][n_head][head_dim].
  *  out, lse device float [n_seq][n_q][n_head][head_dim], [n_seq][n_q][n_head].
  *  Other arguments: as kvattn_decode.
