@@ -464,9 +464,10 @@ int decode_impl(const void* q, const void* k_cache, const void* v_cache, const v
         p.group = n_head / n_head_kv;
         p.split = split;
         p.n_q = n_q;
-        // up to 8 f16 query rows per KV head: the single-query kernels with per-row causal masks
-        // (one 8-row output tile instead of two)
-        const bool mq8 = multi && kv_type == KVATTN_KV_F16 && mq_rows <= 8;
+        // up to 8 query rows per KV head: the single-query kernels with per-row causal masks
+        // (one 8-row output tile instead of two; the quantised head_dim-256 multi-query kernels
+        // are of that form already)
+        const bool mq8 = multi && mq_rows <= 8 && (kv_type == KVATTN_KV_F16 || head_dim == 128);
         p.mq = multi ? (mq8 ? 2 : 1) : 0;
         p.n_rg = n_rg;
         p.rg_rows = rg_rows;

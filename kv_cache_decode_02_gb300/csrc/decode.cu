@@ -2740,8 +2740,20 @@ __global__ void __launch_bounds__(kQ8WMQ * 32, kQ8BMQ)
     split_decode_mq_q4_d128(const __grid_constant__ SplitDecodeParams p) {
     q8_self_body<128, kQ8WMQ, kQ8SMQ, true, true, true>(p);
 }
-// Multi-query decode over the quantised caches at head_dim 256: 8-row units on the
-// single-query geometry.
+// Multi-query decode over the quantised caches, 8-row units on the single-query geometry:
+// every row count at head_dim 256, up to 8 rows at head_dim 128.
+__global__ void __launch_bounds__(kQ8W128 * 32, kQ8B128)
+    split_decode_mq8_q8_d128(const __grid_constant__ SplitDecodeParams p) {
+    q8_self_body<128, kQ8W128, kQ8S128, false, false, false, true>(p);
+}
+__global__ void __launch_bounds__(kQ8W128 * 32, kQ8B128)
+    split_decode_mq8_q8q4_d128(const __grid_constant__ SplitDecodeParams p) {
+    q8_self_body<128, kQ8W128, kQ8S128, true, false, false, true>(p);
+}
+__global__ void __launch_bounds__(kQ8W128 * 32, kQ8B128)
+    split_decode_mq8_q4_d128(const __grid_constant__ SplitDecodeParams p) {
+    q8_self_body<128, kQ8W128, kQ8S128, true, true, false, true>(p);
+}
 __global__ void __launch_bounds__(kQ8W256 * 32, kQ8B256)
     split_decode_mq_q8_d256(const __grid_constant__ SplitDecodeParams p) {
     q8_self_body<256, kQ8W256, kQ8S256, false, false, false, true>(p);
@@ -2767,9 +2779,13 @@ __global__ void __launch_bounds__(kQ8W256 * 32, kQ8B256)
 // mode: 0 single-query, 1 multi-query, 2 f16 multi-query of up to 8 rows per unit on the
 // single-query geometry (same resources as mode 0).
 const void* kernel_for(int kv_type, int head_dim, int mode = 0) {
-    if (mode == 2)
+    if (mode == 2) {
+        if (kv_type == KVATTN_KV_Q8_0) return reinterpret_cast<const void*>(split_decode_mq8_q8_d128);
+        if (kv_type == KVATTN_KV_Q8_0_Q4_0) return reinterpret_cast<const void*>(split_decode_mq8_q8q4_d128);
+        if (kv_type == KVATTN_KV_Q4_0) return reinterpret_cast<const void*>(split_decode_mq8_q4_d128);
         return head_dim == 256 ? reinterpret_cast<const void*>(split_decode_mq8_f16_d256)
                                : reinterpret_cast<const void*>(split_decode_mq8_f16_d128);
+    }
     const bool mq = mode == 1;
     if (mq) {
         const bool d256 = head_dim == 256;
@@ -2857,12 +2873,13 @@ cudaError_t launch_split_decode(const SplitDecodeParams& p, int kv_type, int hea
                                 cudaStream_t stream, bool pdl) {
     const bool mq = p.mq == 1;  // (mode 2 has the single-query resources)
     const void* fn = kernel_for(kv_type, head_dim, p.mq);
-    static std::once_flag once[64][18];
-    static cudaError_t attr_err[64][18];
+    static std::once_flag once[64][24];
+    static cudaError_t attr_err[64][24];
     int dev = 0;
     cudaError_t err = cudaGetDevice(&dev);
     if (err != cudaSuccess) return err;
-    const int which = p.mq == 2 ? 16 + (head_dim == 256 ? 1 : 0) : (mq ? 8 : 0) + 2 * kv_type + (head_dim == 256 ? 1 : 0);
+    const int which = p.mq == 2 ? 16 + 2 * kv_type + (head_dim == 256 ? 1 : 0)
+                                : (mq ? 8 : 0) + 2 * kv_type + (head_dim == 256 ? 1 : 0);
     std::call_once(once[dev & 63][which], [&] { attr_err[dev & 63][which] = set_smem_attr(fn); });
     if (attr_err[dev & 63][which] != cudaSuccess) return attr_err[dev & 63][which];
     cudaLaunchConfig_t cfg = {};
