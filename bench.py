@@ -395,6 +395,19 @@ def bench_workloads(K, torch, stream, peak):
                                  stream)
     fn()
     add(w.name, w.n_cells * w.n_head_kv * w.head_dim * 4, timed(fn), {"split": sp})
+    # the same cache verifying 4 draft tokens (8 query rows per KV head), the same split
+    n_q = 4
+    qm = torch.randn((1, n_q, w.n_head, w.head_dim), device="cuda").half()
+    wsm = torch.zeros(K.kvattn_decode_multi_workspace_bytes(1, n_q, w.n_head, w.head_dim, w.n_cells, sp),
+                      dtype=torch.uint8, device="cuda")
+    om = torch.empty((1, n_q, w.n_head, w.head_dim), dtype=torch.float32, device="cuda")
+    lm = torch.empty((1, n_q, w.n_head), dtype=torch.float32, device="cuda")
+    fm = lambda: K.kvattn_decode_multi(qm, kk, vv, None, None, 0, w.n_cells, None, 0, lens, 1, w.n_cells, n_q,
+                                       w.n_head, w.n_head_kv, w.head_dim, sp, 1 / math.sqrt(w.head_dim), om, lm,
+                                       wsm, wsm.numel(), stream)
+    fm()
+    add(w.name + "_verify_nq4", w.n_cells * w.n_head_kv * w.head_dim * 4, timed(fm),
+        {"n_q": n_q, "query_rows_per_kv_head": n_q * w.n_head // w.n_head_kv, "split": sp})
     del kk, vv
 
     # Q8_0 long context, head_dim 128 and 256; and Q8_0 keys with Q4_0 values
@@ -415,7 +428,7 @@ def bench_workloads(K, torch, stream, peak):
         kb, vb = (D // 2 if kv_type == 3 else D), (D if kv_type == 1 else D // 2)
         kv_bytes = N * Hk * ((kb + D // 16) + (vb + D // 16))
         add(w.name, kv_bytes, timed(fn))
-        if w is inputs.Q8_LONG_D128:
+        if w is inputs.Q8_LONG_D128 or w is inputs.Q8_LONG_D256:
             # the same cache verifying 4 draft tokens (16 query rows per KV head)
             n_q = 4
             qm = torch.randn((1, n_q, w.n_head, D), device="cuda").half()
