@@ -282,8 +282,11 @@ int kvattn_merge(const float* partials, const float* lses, int n_parts, int n_ro
  *         contents (each call clears the status word it needs at zero).  Calls whose work
  *         overlaps on the GPU -- on different streams, or from different threads without
  *         ordering -- race on the array and give wrong results; order them on one stream.
+ *  Device: the array used is the current device's, so `stream` must belong to the current
+ *         device (as for every entry point of this library).
  *  Device-side status bits of this path are not reported.
- * Errors: INVALID_ARG, UNSUPPORTED, WORKSPACE (before any launch); CUDA.
+ * Errors: INVALID_ARG, UNSUPPORTED, WORKSPACE (all checked before the array's address is
+ *         looked up and before anything is enqueued); CUDA.
  */
 #define KVATTN_NOALLOC_SCRATCH_BYTES (16u * 1024u * 1024u)
 

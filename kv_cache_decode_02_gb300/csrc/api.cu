@@ -350,8 +350,9 @@ int decode_impl(const void* q, const void* k_cache, const void* v_cache, const v
                 int64_t plan_stride, const int32_t* seq_lens, int n_seq, int64_t max_len, int n_head,
                 int n_head_kv, int head_dim, int split, float scale, float* out, float* lse,
                 float* part_o_user, float* part_lse_user, void* ws, size_t ws_bytes, void* stream,
-                int n_q = 0) {
+                int n_q = 0, const kvattn::LibraryScratch* lib_scratch = nullptr) {
     // n_q = 0: single-query decode; n_q >= 1: causal multi-query decode
+    // lib_scratch: the workspace is the library's own array (ws and ws_bytes are unused)
     // One token is single-query decode (its causal window is the whole sequence, and the
     // output and partial layouts coincide): the single-query kernels, which carry one 8-row
     // output tile instead of two (four GQA-6 sequences through a plan: 139.8 -> 98.8 us).
@@ -387,7 +388,8 @@ int decode_impl(const void* q, const void* k_cache, const void* v_cache, const v
         if ((int64_t)n_seq * ((max_len + split - 1) / split) * n_head_kv * n_rg > (int64_t)INT32_MAX)
             return KVATTN_ERR_UNSUPPORTED;
     }
-    if (q == nullptr || k_cache == nullptr || v_cache == nullptr || seq_lens == nullptr || ws == nullptr)
+    if (q == nullptr || k_cache == nullptr || v_cache == nullptr || seq_lens == nullptr ||
+        (ws == nullptr && lib_scratch == nullptr))
         return KVATTN_ERR_INVALID_ARG;
     if (merge && (out == nullptr || lse == nullptr)) return KVATTN_ERR_INVALID_ARG;
     if (!merge && (part_lse_user == nullptr || !aligned(part_o_user, 16) || !aligned(part_lse_user, 4)))
@@ -400,7 +402,7 @@ int decode_impl(const void* q, const void* k_cache, const void* v_cache, const v
     if (n_cells < 1 || (cell_plan != nullptr && plan_stride < 1) || !std::isfinite(scale))
         return KVATTN_ERR_INVALID_ARG;
     if (!aligned(q, 4) || !aligned(k_cache, 16) || !aligned(v_cache, 16) ||
-        (merge && (!aligned(out, 16) || !aligned(lse, 4))) || !aligned(ws, kWsAlign) ||
+        (merge && (!aligned(out, 16) || !aligned(lse, 4))) || (lib_scratch == nullptr && !aligned(ws, kWsAlign)) ||
         (cell_plan && !aligned(cell_plan, 4)) || !aligned(seq_lens, 4))
         return KVATTN_ERR_INVALID_ARG;
     if (kv_type != KVATTN_KV_F16) {
@@ -409,10 +411,16 @@ int decode_impl(const void* q, const void* k_cache, const void* v_cache, const v
     }
     const int64_t n_split = (max_len + split - 1) / split;
     const DecodeWsLayout lay = decode_ws_layout(n_seq, n_q * n_head, head_dim, n_split);
-    if (ws_bytes < lay.total) return KVATTN_ERR_WORKSPACE;
+    if ((lib_scratch != nullptr ? lib_scratch->bytes : ws_bytes) < lay.total) return KVATTN_ERR_WORKSPACE;
     if (n_seq == 0) return KVATTN_OK;
 
     cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (lib_scratch != nullptr) {
+        // every check passed: only now the array's address, and the status word cleared (the
+        // array keeps the previous call's bytes; descriptors and partials are rewritten)
+        if (lib_scratch->address(&ws) != cudaSuccess || ws == nullptr) return KVATTN_ERR_CUDA;
+        if (cudaMemsetAsync(ws, 0, sizeof(uint32_t), s) != cudaSuccess) return KVATTN_ERR_CUDA;
+    }
     char* wsb = static_cast<char*>(ws);
     uint32_t* status = reinterpret_cast<uint32_t*>(wsb);
     float* part_o = merge ? reinterpret_cast<float*>(wsb + lay.o_off) : part_o_user;
@@ -544,6 +552,22 @@ int kvattn_decode_multi(const void* q, const void* k_cache, const void* v_cache,
                        n_seq, max_len, n_head, n_head_kv, head_dim, split, scale, out, lse, nullptr, nullptr, ws,
                        ws_bytes, stream, n_q);
 }
+
+}  // extern "C"
+
+int kvattn::decode_with_library_scratch(const void* q, const void* k_cache, const void* v_cache,
+                                        const void* k_scales, const void* v_scales, int kv_type, int64_t n_cells,
+                                        const int32_t* cell_plan, int64_t plan_stride, const int32_t* seq_lens,
+                                        int n_seq, int64_t max_len, int n_head, int n_head_kv, int head_dim,
+                                        int split, float scale, float* out, float* lse,
+                                        const LibraryScratch& scratch, void* stream) {
+    if (out == nullptr || lse == nullptr) return KVATTN_ERR_INVALID_ARG;
+    return decode_impl(q, k_cache, v_cache, k_scales, v_scales, kv_type, n_cells, cell_plan, plan_stride, seq_lens,
+                       n_seq, max_len, n_head, n_head_kv, head_dim, split, scale, out, lse, nullptr, nullptr,
+                       nullptr, 0, stream, 0, &scratch);
+}
+
+extern "C" {
 
 int kvattn_merge(const float* partials, const float* lses, int n_parts, int n_rows, int head_dim,
                  float* out, float* lse, void* stream) {

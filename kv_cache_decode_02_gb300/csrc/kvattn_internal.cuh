@@ -133,6 +133,22 @@ cudaError_t launch_descriptors(const int32_t* plan, int64_t plan_stride, const i
                                int64_t n_split, int4* desc, uint32_t* status,
                                cudaStream_t stream);
 
+// Scratch the library owns (a file-scope device array), for callers that cannot allocate:
+// its size, and a host function that yields its device address on the current device.
+struct LibraryScratch {
+    size_t bytes;
+    cudaError_t (*address)(void** ptr);
+};
+
+// kvattn_decode with the workspace taken from `scratch` (api.cu): every argument check,
+// the size check included, runs before the address lookup and before any device work; the
+// status word is then cleared on the stream, because the array keeps the last call's bytes.
+int decode_with_library_scratch(const void* q, const void* k_cache, const void* v_cache, const void* k_scales,
+                                const void* v_scales, int kv_type, int64_t n_cells, const int32_t* cell_plan,
+                                int64_t plan_stride, const int32_t* seq_lens, int n_seq, int64_t max_len,
+                                int n_head, int n_head_kv, int head_dim, int split, float scale, float* out,
+                                float* lse, const LibraryScratch& scratch, void* stream);
+
 // Host plan builder (plan.cpp).
 int build_cell_plan_host(const int64_t* cells, const int64_t* offsets, int n_seq,
                          int64_t capacity_cells, int32_t* plan, int64_t plan_stride,

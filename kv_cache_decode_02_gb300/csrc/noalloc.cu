@@ -49,21 +49,12 @@ extern "C" int kvattn_decode_noalloc(const void* q, const void* k_cache, const v
                                      const int32_t* seq_lens, int n_seq, int64_t max_len, int n_head,
                                      int n_head_kv, int head_dim, int split, float scale, float* out,
                                      float* lse, void* stream) {
-    if (split == 0) {  // the split kvattn_decode would select (a host-side query)
-        split = kvattn_select_split(kv_type, n_seq, max_len, n_head_kv, head_dim);
-        if (split < 0) return split;
-    }
-    // Refuse, before any work reaches the device, a call whose scratch would not fit.
-    const size_t need = kvattn_decode_workspace_bytes(n_seq, n_head, head_dim, max_len, split);
-    if (need == 0) return KVATTN_ERR_INVALID_ARG;
-    if (need > (size_t)KVATTN_NOALLOC_SCRATCH_BYTES) return KVATTN_ERR_WORKSPACE;
-    void* scratch = nullptr;
-    if (scratch_address(&scratch) != cudaSuccess || scratch == nullptr) return KVATTN_ERR_CUDA;
-    // The scratch keeps the previous call's contents; only the status word must start at
-    // zero (descriptors and partials are fully rewritten by every call).
-    if (cudaMemsetAsync(scratch, 0, kvattn::kStatusBytes, static_cast<cudaStream_t>(stream)) != cudaSuccess)
-        return KVATTN_ERR_CUDA;
-    return kvattn_decode(q, k_cache, v_cache, k_scales, v_scales, kv_type, n_cells, cell_plan, plan_stride,
-                         seq_lens, n_seq, max_len, n_head, n_head_kv, head_dim, split, scale, out, lse, scratch,
-                         (size_t)KVATTN_NOALLOC_SCRATCH_BYTES, stream);
+    // Every argument and size check (a call whose scratch would not fit the array is
+    // refused with KVATTN_ERR_WORKSPACE) runs before the array's address is looked up and
+    // before anything is put on the stream; the status word is then cleared on the stream
+    // (the array keeps the previous call's bytes; descriptors and partials are rewritten).
+    const kvattn::LibraryScratch scratch{(size_t)KVATTN_NOALLOC_SCRATCH_BYTES, scratch_address};
+    return kvattn::decode_with_library_scratch(q, k_cache, v_cache, k_scales, v_scales, kv_type, n_cells, cell_plan,
+                                               plan_stride, seq_lens, n_seq, max_len, n_head, n_head_kv, head_dim,
+                                               split, scale, out, lse, scratch, stream);
 }
