@@ -16,8 +16,13 @@ attention over all 36 layers: 36 kvattn_decode calls on 36 distinct layer buffer
               synchronize per step; the step's calls and copies are recorded once as a
               CUDA graph and replayed (e2e_eager: the same with every call launched from
               Python).
+  us_per_op_interleaved  the layer's cost when other kernels run between the attention
+              calls (a stand-in projection GEMV before each call, so no attention launch
+              overlaps the previous one): step time with attention minus the stand-ins' own.
   workloads   the other decode-attention workloads (tiny, multi-slot plan, Q8_0 long
-              context, window + host tail) timed the same way.
+              context, window + host tail) timed the same way; each carries its own
+              cpu_baseline (the oracle on all host cores and on one thread).  The tiny
+              workload also reports device time per call from a replayed CUDA graph.
   cpu_baseline  the fp64 oracle on the host cores over a bounded sample of the workload.
 
 --impl reference times the oracle (the plain CPU implementation) on the same metric.
@@ -298,7 +303,31 @@ def bench_workloads(K, torch, stream, peak):
                                  w.n_head_kv, w.head_dim, w.split, 1 / math.sqrt(w.head_dim), out, lse, ws,
                                  ws.numel(), stream)
     fn()
-    add(w.name, w.n_cells * w.n_head_kv * w.head_dim * 4, timed(fn), {"gated": False})
+    ms_eager = timed(fn)
+    # the same calls recorded as one CUDA graph of 64 back-to-back calls and replayed: device
+    # time per call without the host's enqueue (the eager figure above is bound by it)
+    n_rec = 64
+    g_tiny = torch.cuda.CUDAGraph()
+    side = torch.cuda.Stream()
+    side.wait_stream(stream)
+    with torch.cuda.stream(side):
+        fn_side = lambda: K.kvattn_decode(q, k, v, None, None, 0, w.n_cells, None, 0, lens, 1, w.n_cells, w.n_head,
+                                          w.n_head_kv, w.head_dim, w.split, 1 / math.sqrt(w.head_dim), out, lse, ws,
+                                          ws.numel(), side)
+        fn_side()
+    torch.cuda.synchronize()
+    with torch.cuda.graph(g_tiny):
+        cur = torch.cuda.current_stream()
+        for _ in range(n_rec):
+            K.kvattn_decode(q, k, v, None, None, 0, w.n_cells, None, 0, lens, 1, w.n_cells, w.n_head, w.n_head_kv,
+                            w.head_dim, w.split, 1 / math.sqrt(w.head_dim), out, lse, ws, ws.numel(), cur)
+    torch.cuda.synchronize()
+    ms_graph = timed(lambda: g_tiny.replay(), 10) / n_rec
+    del g_tiny
+    add(w.name, w.n_cells * w.n_head_kv * w.head_dim * 4, ms_eager,
+        {"gated": False, "how": "eager ctypes calls, back to back (host enqueue bound)",
+         "us_per_op_graph": round(ms_graph * 1e3, 3),
+         "graph_how": f"{n_rec} calls recorded in one CUDA graph, replayed; device time per call"})
 
     # causal multi-query decode: the Qwen3-8B-shaped layer verifying 4 and 8 draft tokens (16
     # and 32 query rows per KV head read every K/V byte once); 8 rotating layer buffers
@@ -597,6 +626,143 @@ def cpu_baseline_sample(budget_s=12.0):
                             "sample": f"{reps1} repetition(s) in {el1:.1f} s on one thread"}}
 
 
+def interleaved_layer_cost(K, torch, data, reps=20):
+    """The headline layer's cost inside a decode step, where other kernels run between the
+    attention calls.  A stand-in for the rest of a layer -- one token through a 4096 x 12288
+    bf16 projection (100 MB of weights; four rotating matrices, so L2 holds none of them) --
+    runs before each of the kvattn_decode calls, so no attention launch overlaps the previous
+    one (the stand-in neither lets dependents start early nor waits for them).  Both step
+    forms -- stand-ins alone, stand-ins with attention -- are captured as CUDA graphs and
+    replayed; the attention's cost per layer is their difference over the layers."""
+    L = data.layers
+    x = torch.randn((1, 4096), device="cuda", dtype=torch.bfloat16)
+    Ws = [torch.randn((4096, 12288), device="cuda", dtype=torch.bfloat16) for _ in range(4)]
+    y = torch.empty((1, 12288), device="cuda", dtype=torch.bfloat16)
+
+    def standins(st):
+        for l in range(L):
+            torch.mm(x, Ws[l % 4], out=y)
+
+    def with_attention(st):
+        for l in range(L):
+            torch.mm(x, Ws[l % 4], out=y)
+            data.call(K, l, st)
+
+    graphs = {}
+    for name, fn in (("standins", standins), ("interleaved", with_attention)):
+        side = torch.cuda.Stream()
+        side.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(side):
+            fn(side)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            fn(torch.cuda.current_stream())
+        torch.cuda.synchronize()
+        graphs[name] = g
+    cur = torch.cuda.current_stream()
+    best = {name: float("inf") for name in graphs}
+    for _ in range(3):                       # alternate the two forms, keep each one's best
+        for name, g in graphs.items():
+            for _ in range(3):
+                g.replay()
+            best[name] = min(best[name], time_events(torch, cur, g.replay, reps))
+    del graphs, Ws
+    us = (best["interleaved"] - best["standins"]) * 1e3 / L
+    return {"us_per_op_interleaved": round(us, 3),
+            "kv_gbs_interleaved": round(data.bytes_per_op / (us * 1e-6) / 1e9, 1),
+            "step_ms_standins": round(best["standins"], 4), "step_ms_with_attention": round(best["interleaved"], 4),
+            "how": (f"{L} x (stand-in bf16 GEMV 1x4096 @ 4096x12288, then kvattn_decode), CUDA graph, minus "
+                    f"{L} stand-ins alone; per layer")}
+
+
+def oracle_workload_baselines(budget_s=1.0):
+    """The fp64 oracle (as it stands) on each workload of the decode-attention configurations,
+    on this host's cores: all the cores of the process's affinity set over the whole op
+    (repeated for about budget_s seconds, at least once), and one thread over an eighth of
+    the cells of the larger workloads (the oracle's cost is linear in cells), scaled to the
+    whole op.  Inputs come from the seeded numpy generators; the window + tail op is sampled
+    on 65536 of its cells on all cores as well."""
+    import oracle
+    from oracle import plan_oracle as po
+    from kv_cache_decode_02_gb300 import inputs
+    threads = oracle.default_threads()
+    res = {}
+
+    def measure(name, fn, nbytes, sample, frac_all=1.0, frac_one=1.0):
+        """fn(threads, frac): one oracle call over that fraction of the op's cells."""
+        reps, t0 = 0, time.perf_counter()
+        while True:
+            fn(threads, frac_all)
+            reps += 1
+            if time.perf_counter() - t0 >= budget_s:
+                break
+        ms_all = (time.perf_counter() - t0) * 1e3 / reps / frac_all
+        t1 = time.perf_counter()
+        fn(1, frac_one)
+        ms_one = (time.perf_counter() - t1) * 1e3 / frac_one
+        res[name] = {"ms_per_op": round(ms_all, 3), "kv_gbs": round(nbytes / (ms_all * 1e-3) / 1e9, 3),
+                     "cores": threads, "kind": "oracle",
+                     "sample": (f"{sample}; {reps} call(s) on {threads} threads" +
+                                (f" over {frac_all:g} of the cells" if frac_all < 1 else "") +
+                                (f"; one thread over {frac_one:g} of the cells, scaled" if frac_one < 1 else "")),
+                     "single_core": {"ms_per_op": round(ms_one, 3),
+                                     "kv_gbs": round(nbytes / (ms_one * 1e-3) / 1e9, 3)}}
+
+    def lens_frac(lens, frac):
+        return [max(1, int(round(L * frac))) for L in lens]
+
+    for w in (inputs.TINY, inputs.QWEN3_8B_LAYER, inputs.F16_D256_LONG):
+        q = inputs.make_q(w)
+        k, v = inputs.make_kv_f16(w)
+        measure(w.name, lambda t, f: oracle.decode_f16(q, k, v, lens_frac(w.seq_lens, f), n_threads=t),
+                w.n_cells * w.n_head_kv * w.head_dim * 4, "fp64 C oracle", frac_one=1.0 if w is inputs.TINY else 0.125)
+    w = inputs.BATCH64
+    q = inputs.make_q(w)
+    k, v = inputs.make_kv_f16(w)
+    # one thread: 8 of the 64 sequences
+    measure(w.name, lambda t, f: oracle.decode_f16(q[:max(1, int(w.n_seq * f))], k[:max(1, int(w.n_seq * f))],
+                                                   v[:max(1, int(w.n_seq * f))], list(w.seq_lens)[:max(1, int(w.n_seq * f))],
+                                                   n_threads=t),
+            w.n_seq * w.n_cells * w.n_head_kv * w.head_dim * 4, "fp64 C oracle", frac_one=0.125)
+    del k, v
+
+    w = inputs.MULTISLOT_PLAN
+    lay = inputs.make_unified_layout(w)
+    plan, plens = po.build_cell_plan(lay.encoded_cells, w.n_cells)
+    q = inputs.make_q(w)
+    k = inputs.normal_f16(np.random.default_rng([2000 + w.number, 0]), (w.n_cells, w.n_head_kv, w.head_dim))
+    v = inputs.normal_f16(np.random.default_rng([3000 + w.number, 0]), (w.n_cells, w.n_head_kv, w.head_dim))
+    inputs.nan_fill_unselected(k, v, np.concatenate(lay.selected))
+    valid = int((plan >= 0).sum())
+    measure(w.name, lambda t, f: oracle.decode_f16(q, k, v, lens_frac(plens, f), plan=plan, n_threads=t),
+            valid * w.n_head_kv * w.head_dim * 4, "fp64 C oracle through the plan", frac_one=0.125)
+    del k, v
+
+    for w, make, fn in ((inputs.Q8_LONG_D128, inputs.make_kv_q8, oracle.decode_q8_0),
+                        (inputs.Q8_LONG_D256, inputs.make_kv_q8, oracle.decode_q8_0),
+                        (inputs.Q8Q4_LONG_D128, inputs.make_kv_q8q4, oracle.decode_q8_0_q4_0),
+                        (inputs.Q8Q4_LONG_D256, inputs.make_kv_q8q4, oracle.decode_q8_0_q4_0),
+                        (inputs.Q4_LONG_D128, inputs.make_kv_q4, oracle.decode_q4_0),
+                        (inputs.Q4_LONG_D256, inputs.make_kv_q4, oracle.decode_q4_0)):
+        D = w.head_dim
+        q = inputs.make_q(w)
+        (kq, kd), (vq, vd) = make(w)
+        nbytes = w.n_cells * w.n_head_kv * ((kq.shape[-1] + D // 16) + (vq.shape[-1] + D // 16))
+        measure(w.name, lambda t, f: fn(q, kq, kd, vq, vd, lens_frac(w.seq_lens, f), n_threads=t), nbytes,
+                "fp64 C oracle", frac_one=0.125)
+        del kq, kd, vq, vd
+
+    w = inputs.WINDOW_TAIL
+    n_s = 65536
+    q = inputs.make_q(w)
+    k, v = inputs.make_kv_f16(w, n_cells=n_s)
+    measure(w.name, lambda t, f: oracle.decode_f16(q, k, v, [max(1, int(w.n_cells * f))], n_threads=t),
+            w.n_cells * w.n_head_kv * w.head_dim * 4, "fp64 C oracle on the sequence fully resident",
+            frac_all=n_s / w.n_cells, frac_one=n_s / w.n_cells / 8)
+    return res
+
+
 def run_ours(args):
     import torch
     from kv_cache_decode_02_gb300 import kvattn as K
@@ -706,6 +872,11 @@ def run_ours(args):
     achieved = data.bytes_per_op / (kern_ms * 1e-3) / 1e9
     traffic = profiled_traffic("split_decode_f16_qwen3_8b_layer.md")
 
+    # the layer with other kernels between the attention calls (no cross-call overlap)
+    inter = None
+    if not args.no_interleaved and not args.eager:
+        inter = interleaved_layer_cost(K, torch, data)
+
     # end to end through the API with host buffers
     e2e = e2e_eager = None
     if not args.no_e2e:
@@ -755,6 +926,12 @@ def run_ours(args):
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
         cpu = cpu_baseline_sample(args.cpu_budget)
+        if workloads is not None and not args.no_workload_cpu:
+            for name, d in oracle_workload_baselines().items():
+                if name in workloads:
+                    workloads[name]["cpu_baseline"] = d
+                elif name == "qwen3_8b_layer_n16384":
+                    cpu["per_layer_oracle"] = d
 
     if rank == 0:
         line = {
@@ -768,6 +945,8 @@ def run_ours(args):
                        "launch": "eager" if args.eager else f"CUDA graph of {args.layers} x kvattn_decode",
                        "parallelism": f"replicas x{world}"},
             "us_per_op": round(ms * 1e3 / args.layers, 3),
+            "us_per_op_interleaved": inter["us_per_op_interleaved"] if inter else None,
+            "interleaved": inter,
             "us_per_token_36_layers": round(ms * 1e3 * 36 / args.layers, 2),
             "frac_of_8tbs": round(value / world / NOMINAL_HBM_GBS, 3),
             "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
@@ -820,10 +999,15 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
-def window_tail_inputs(torch, inputs):
+def window_tail_inputs(torch, inputs, n_tail=None):
     """The window + tail workload: the resident window on the device, the older tail in
-    pinned host memory (filled through the device in 64K-cell pieces), and q."""
+    pinned host memory (filled through the device in 64K-cell pieces), and q.  n_tail: a
+    shorter tail (profiling the host link on a small case); the window is unchanged."""
+    import dataclasses
     w = inputs.WINDOW_TAIL
+    if n_tail is not None:
+        w = dataclasses.replace(w, name=f"window_tail_n{w.n_window + n_tail}", n_cells=w.n_window + n_tail,
+                                seq_lens=(w.n_window + n_tail,))
     N, Hk, D = w.n_cells, w.n_head_kv, w.head_dim
     n_tail = N - w.n_window
     k_win = inputs.normal_f16_torch((2000 + w.number, 1), (w.n_window, Hk, D), "cuda")
@@ -860,13 +1044,37 @@ def profile_verify(args):
     print(f"{args.profile_workload}: {args.kernel_reps} calls done")
 
 
+def profile_interleaved(args):
+    """--kernel-reps decode steps of the headline layers with the stand-in projection before
+    each kvattn_decode call (launched eagerly), for an ncu launch list."""
+    import torch
+    from kv_cache_decode_02_gb300 import kvattn as K
+    data = Qwen3Layers(K, torch, args.layers)
+    x = torch.randn((1, 4096), device="cuda", dtype=torch.bfloat16)
+    Ws = [torch.randn((4096, 12288), device="cuda", dtype=torch.bfloat16) for _ in range(4)]
+    y = torch.empty((1, 12288), device="cuda", dtype=torch.bfloat16)
+    st = torch.cuda.current_stream()
+    torch.cuda.synchronize()
+    torch.cuda.profiler.start()          # a profiler started with --profile-from-start off sees only the steps
+    for _ in range(args.kernel_reps):
+        for l in range(args.layers):
+            torch.mm(x, Ws[l % 4], out=y)
+            data.call(K, l, st)
+    torch.cuda.synchronize()
+    torch.cuda.profiler.stop()
+    print(f"qwen3_8b_interleaved: {args.kernel_reps} steps done")
+
+
 def profile_window_tail(args):
     """--kernel-reps calls of the window + tail op (staged 1 MiB tiles through the copy
-    kernel, or the tail read in place), for profilers (no timing, no JSON line)."""
+    kernel, or the tail read in place), for profilers (no timing, no JSON line).  The
+    window_tail_n81920 names keep the 16384-cell window with a 65536-cell tail (268 MB of
+    pinned host memory), small enough for multi-pass counter captures."""
     import torch
     from kv_cache_decode_02_gb300 import inputs
     from kv_cache_decode_02_gb300 import kvattn as K
-    w, q, k_win, v_win, k_tail, v_tail = window_tail_inputs(torch, inputs)
+    small = args.profile_workload.startswith("window_tail_n81920")
+    w, q, k_win, v_win, k_tail, v_tail = window_tail_inputs(torch, inputs, 65536 if small else None)
     Hk, D, H = w.n_head_kv, w.head_dim, w.n_head
     n_tail = w.n_cells - w.n_window
     out = torch.empty((H, D), dtype=torch.float32, device="cuda")
@@ -935,16 +1143,21 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-parity", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=12.0)
-    ap.add_argument("--profile-workload", choices=["q8_0_n131072_d128", "q8_0_n131072_d256", "q8_0_q4_0_n131072_d128",
+    ap.add_argument("--no-workload-cpu", action="store_true", help="skip the oracle on each secondary workload")
+    ap.add_argument("--no-interleaved", action="store_true")
+    ap.add_argument("--profile-workload", choices=["qwen3_8b_interleaved", "q8_0_n131072_d128", "q8_0_n131072_d256", "q8_0_q4_0_n131072_d128",
                                                    "q8_0_q4_0_n131072_d256", "q4_0_n131072_d128",
                                                    "q4_0_n131072_d256", "window_tail_n524288",
-                                                   "window_tail_n524288_direct", "qwen3_8b_layer_verify_nq4",
+                                                   "window_tail_n524288_direct", "window_tail_n81920",
+                                                   "window_tail_n81920_direct", "qwen3_8b_layer_verify_nq4",
                                                    "qwen3_8b_layer_verify_nq8"],
                     help="only launch this workload's split decode (window + tail: the whole op) "
                          "--kernel-reps times (for ncu)")
     args = ap.parse_args()
     if args.profile_workload:
-        if args.profile_workload.startswith("window_tail"):
+        if args.profile_workload == "qwen3_8b_interleaved":
+            profile_interleaved(args)
+        elif args.profile_workload.startswith("window_tail"):
             profile_window_tail(args)
         elif args.profile_workload.startswith("qwen3_8b_layer_verify"):
             profile_verify(args)
