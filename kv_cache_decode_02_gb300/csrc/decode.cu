@@ -95,6 +95,16 @@ __device__ __forceinline__ void tma_load_3d_hint(uint32_t dst, const CUtensorMap
         : "memory");
 }
 
+// TMA load of one 2-D tensor-map box (the scale planes of the quantised caches).
+__device__ __forceinline__ void tma_load_2d_hint(uint32_t dst, const CUtensorMap* map, int x, int y, uint32_t bar,
+                                                 uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1, "
+        "{%2, %3}], [%4], %5;" ::"r"(dst),
+        "l"(map), "r"(x), "r"(y), "r"(bar), "l"(policy)
+        : "memory");
+}
+
 __device__ __forceinline__ uint64_t l2_evict_first_policy() {
     uint64_t pol;
     asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
@@ -200,14 +210,16 @@ __device__ __forceinline__ void q8_pv_block(float (&o0)[4], float (&o1)[4], cons
     mma_16816(o1, i8x2_lo(u01), i8x2_hi(u01), i8x2_lo(u11), i8x2_hi(u11), pb0, pb1);
 }
 
-// Q8_0 scale word (two half scales) of cell `cell` holding block blk.
-template <int D>
+// Q8_0 scale word (two half scales) of cell `cell` holding block blk; SROW bytes between
+// two cells' scale rows.
+template <int SROW>
 __device__ __forceinline__ uint32_t scale_word(const unsigned char* sc, int cell, int blk) {
-    return reinterpret_cast<const uint32_t*>(sc + cell * (D / 16))[blk >> 1];
+    return reinterpret_cast<const uint32_t*>(sc + cell * SROW)[blk >> 1];
 }
 
 // One warp's 16 cells of a tile: scores, online softmax, P V (f16 head_dim 256, Q8_0).
-template <int KVT, int D, bool SWZ, int PLANE = kPlaneBytes>
+// SROW: bytes between two cells' scale rows (Q8_0).
+template <int KVT, int D, bool SWZ, int PLANE = kPlaneBytes, int SROW = Geom<KVT, D>::kSclBytes>
 __device__ __forceinline__ void consume_tile(uint32_t kb, uint32_t vb, const unsigned char* ks,
                                              const unsigned char* vs, uint32_t mask, int warp, int lane,
                                              const uint32_t (&qa)[D / 16][2], float (&oacc)[D / 16][4], float& m_run, float& l_run,
@@ -247,7 +259,7 @@ __device__ __forceinline__ void consume_tile(uint32_t kb, uint32_t vb, const uns
 #pragma unroll
                 for (int e = 0; e < 2; ++e)
                     ksc[j][e] = __half2float(
-                        reinterpret_cast<const __half*>(ks + (r0 + 8 * j + 2 * tq + e) * G::kSclBytes)[b]);
+                        reinterpret_cast<const __half*>(ks + (r0 + 8 * j + 2 * tq + e) * SROW)[b]);
             }
             q8_qk_block(sacc, qa[2 * b], qa[2 * b + 1], kw, ksc);
         }
@@ -283,9 +295,9 @@ __device__ __forceinline__ void consume_tile(uint32_t kb, uint32_t vb, const uns
         const int c0 = r0 + 2 * tq;
 #pragma unroll
         for (int b = 0; b < D / 32; ++b) {
-            const uint32_t s01 = prmt_b32(scale_word<D>(vs, c0, b), scale_word<D>(vs, c0 + 1, b),
+            const uint32_t s01 = prmt_b32(scale_word<SROW>(vs, c0, b), scale_word<SROW>(vs, c0 + 1, b),
                                           (b & 1) ? 0x7632u : 0x5410u);
-            const uint32_t s89 = prmt_b32(scale_word<D>(vs, c0 + 8, b), scale_word<D>(vs, c0 + 9, b),
+            const uint32_t s89 = prmt_b32(scale_word<SROW>(vs, c0 + 8, b), scale_word<SROW>(vs, c0 + 9, b),
                                           (b & 1) ? 0x7632u : 0x5410u);
             const int off = 32 * b + 4 * gq;
             const uint32_t vw[4] = {lds32(sec_addr<SWZ, G::kPadRow, PLANE>(vb, c0, off)),
@@ -404,6 +416,35 @@ __device__ __forceinline__ void load_q_frags_q4k(const SplitDecodeParams& p, int
         const uint32_t w1 = row_ok ? __ldg(qrow + e / 2 + 1) : 0u;  // elements e+2, e+3
         qa[kk][0] = prmt_b32(w0, w1, 0x5410u);  // (e, e+2)
         qa[kk][1] = prmt_b32(w0, w1, 0x7632u);  // (e+1, e+3)
+    }
+}
+
+// Query fragments of a head-pair unit (the head_dim-256 kernels reading a head_dim-128 cache
+// as 256-byte rows of KV heads 2g2 and 2g2+1): rows gq < G are query heads 2 g2 G + gq of the
+// first head and fill dims 0-127, rows G .. 2G-1 belong to the second head and fill dims
+// 128-255; the other half of every row is zero, so each score is its own head's q.K.  The
+// element order is load_q_frags' (8-bit keys) or load_q_frags_q4k's (4-bit keys).
+template <bool KQ4>
+__device__ __forceinline__ void load_q_frags_pair(const SplitDecodeParams& p, int s, int g2, int gq, int tq,
+                                                  uint32_t (&qa)[16][2]) {
+    const int G = p.group >> 1;
+    const bool ok = gq < p.group;
+    const int hi = gq >= G ? 1 : 0;
+    const int h = g2 * p.group + (ok ? gq : 0);
+    const uint32_t* qrow = reinterpret_cast<const uint32_t*>(p.q + ((int64_t)s * p.n_head + h) * 128);
+#pragma unroll
+    for (int kk = 0; kk < 16; ++kk) {
+        const bool mine = ok && (kk >= 8) == (hi != 0);
+        const int e = (32 * (kk >> 1) + 16 * (kk & 1) + 4 * tq) & 127;  // element within the row's half
+        if (KQ4) {
+            const uint32_t w0 = mine ? __ldg(qrow + e / 2) : 0u;
+            const uint32_t w1 = mine ? __ldg(qrow + e / 2 + 1) : 0u;
+            qa[kk][0] = prmt_b32(w0, w1, 0x5410u);
+            qa[kk][1] = prmt_b32(w0, w1, 0x7632u);
+        } else {
+            qa[kk][0] = mine ? __ldg(qrow + e / 2) : 0u;
+            qa[kk][1] = mine ? __ldg(qrow + (e + 2) / 2) : 0u;
+        }
     }
 }
 
@@ -1427,7 +1468,7 @@ __device__ __forceinline__ void q8_chunk_swz(uint32_t kb, uint32_t vb, const uns
                                              const uint32_t (&qa)[D / 16][2], float (&oacc)[D / 16][4],
                                              float& m_run, float& l_run, float scale_log2) {
     constexpr int kPlane = kChunkCells * 128;
-    constexpr int kScl = D / 16;  // bytes of scales per cell
+    constexpr int kScl = 16;  // bytes between two cells' scale rows in the stage
     const int gq = lane >> 2;
     const int tq = lane & 3;
     // K rows gq (n-tile 0) and 8 + gq (+1024); this lane's bytes 4tq.. of each 16-byte column
@@ -1562,7 +1603,7 @@ __device__ __forceinline__ void q4v_chunk(uint32_t kb, uint32_t vb, const unsign
                                            const uint32_t (&qa)[D / 16][2], float (&oacc)[D / 16][4],
                                            float& m_run, float& l_run, float scale_log2) {
     constexpr int kPlane = kChunkCells * 128;
-    constexpr int kScl = D / 16;  // bytes of scales per cell
+    constexpr int kScl = 16;      // bytes between two cells' scale rows in the stage
     constexpr int kVRow = D / 2;  // bytes of a 4-bit V row
     const int gq = lane >> 2;
     const int tq = lane & 3;
@@ -1737,7 +1778,7 @@ __device__ __forceinline__ void q8_mq_chunk(uint32_t kb, uint32_t vb, const unsi
                                             const uint32_t (&qa)[D / 16][4], float (&oacc)[2][D / 16][4],
                                             float (&m_run)[2], float (&l_run)[2], float scale_log2) {
     constexpr int kPlane = kChunkCells * 128;
-    constexpr int kScl = D / 16;
+    constexpr int kScl = 16;         // bytes between two cells' scale rows in the stage
     constexpr int kHalfRow = D / 2;  // bytes of a 4-bit row
     const int gq = lane >> 2;
     const int tq = lane & 3;
@@ -1964,6 +2005,17 @@ __device__ __forceinline__ void q8_mq_chunk(uint32_t kb, uint32_t vb, const unsi
 // (chunk j goes to warp j mod W) and meet in the same end-of-unit exchange as above.  With
 // no producer warp, all the registers of an SM go to warps that compute.
 // ---------------------------------------------------------------------------------------
+// Byte offset of KV head g's scales within its cell's 16-byte stage row, and the first
+// element (in halves) of the 16-byte scale box that holds them.
+template <int D>
+__device__ __forceinline__ int scl_off(int g) {
+    return 2 * ((g * (D / 32)) & 7);
+}
+template <int D>
+__device__ __forceinline__ int scl_box_x(int g) {
+    return (g * (D / 32)) & ~7;
+}
+
 template <int D, bool VQ4 = false, bool KQ4 = false, bool MQ = false>
 struct Q8Self {
     static constexpr int kRowBytes = KQ4 ? D / 2 : D;              // K row per (cell, KV head): int8 or 4-bit
@@ -1974,7 +2026,11 @@ struct Q8Self {
     static constexpr int kVSection = kChunkCells * kVRowBytes;     // V rows of a chunk
     static constexpr int kChunkBytes = kSection + kVSection;       // a multiple of 1024
     static constexpr int kSclBytes = D / 16;                       // D/32 half scales per row
-    static constexpr int kSclChunk = 2 * kChunkCells * kSclBytes;  // K then V scales
+    // scales in a stage: one 16-byte row per cell (the tensor-map box row), K rows then V
+    // rows; a head's D/32 halves sit at byte scl_off(g) of its cell's row (head_dim 128: the
+    // rows hold the scales of the KV-head pair g & ~1, g | 1)
+    static constexpr int kSclRow = 16;
+    static constexpr int kSclChunk = 2 * kChunkCells * kSclRow;  // K then V scales
     // exchange slot of a warp: its O fragments ([N tiles][D/16][32 lanes] float4), max, sum
     static constexpr int kXchgSlot = ((MQ ? 2 : 1) * (D / 16) * 32 * 16 + (MQ ? 128 : 64) + 1023) / 1024 * 1024;
     static_assert(kChunkBytes % 1024 == 0, "stages must keep the 1024-byte swizzle alignment");
@@ -1986,9 +2042,12 @@ constexpr int q8_self_smem() {
     return kHeaderBytes + 1024 + (W - 1) * Q::kXchgSlot + W * S * (Q::kChunkBytes + Q::kSclChunk);
 }
 
-// Position of a warp's load stream: unit u (its fields) and chunk j of it.
+// Position of a warp's load stream: unit u (its fields) and chunk j of it.  Units are
+// numbered in 32 bits (checked on the host); a unit holds at most `split` cells.
 struct ChunkCursor {
-    int64_t u, i0, i1;
+    int64_t i0;          // first plan entry / cell of the unit
+    uint32_t u;
+    int len;             // entries of the unit (i1 - i0)
     int s, g, j, n_chunks;
 };
 
@@ -1998,14 +2057,22 @@ __device__ __forceinline__ int unit_chunks(const Unit& x) {
 
 // Moves c forward (from chunk c.j of unit c.u) to the first chunk this warp owns; c.u >=
 // n_units afterwards when the warp has no more chunks.
-__device__ __forceinline__ void cursor_seek(const SplitDecodeParams& p, ChunkCursor& c, int64_t n_units, int warp) {
+__device__ __forceinline__ void cursor_fill(const SplitDecodeParams& p, ChunkCursor& c) {
+    const Unit x = unit_at(p, c.u);
+    c.i0 = x.i0;
+    c.len = (int)(x.i1 - x.i0);
+    c.s = x.s;
+    c.g = x.g;
+    c.n_chunks = unit_chunks(x);
+}
+__device__ __forceinline__ void cursor_seek(const SplitDecodeParams& p, ChunkCursor& c, uint32_t n_units, int warp) {
     while (c.u < n_units && c.j >= c.n_chunks) {
         c.u += gridDim.x;
         c.j = warp;
         if (c.u < n_units) {
             const Unit x = unit_at(p, c.u);
             c.i0 = x.i0;
-            c.i1 = x.i1;
+            c.len = (int)(x.i1 - x.i0);
             c.s = x.s;
             c.g = x.g;
             c.n_chunks = unit_chunks(x);
@@ -2041,7 +2108,8 @@ __device__ __forceinline__ void q8_self_body(const SplitDecodeParams& p) {
     const int gq = lane >> 2;
     const int tq = lane & 3;
     const int H = p.n_head;
-    const int64_t n_units = (int64_t)p.n_seq * p.unit_splits * p.n_head_kv * (p.n_rg > 1 ? p.n_rg : 1);
+    // work units are numbered in 32 bits (checked on the host)
+    const uint32_t n_units = (uint32_t)((int64_t)p.n_seq * p.unit_splits * p.n_head_kv * (p.n_rg > 1 ? p.n_rg : 1));
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < W * S; ++i) mbar_init(smem_addr(&full_bar[i]), 64);
@@ -2066,18 +2134,49 @@ __device__ __forceinline__ void q8_self_body(const SplitDecodeParams& p) {
     // coordinate and the scale rows follow from 32-bit offsets into the unit.
     auto issue_contiguous = [&](const ChunkCursor& c, int st, uint32_t extra_tx) {
         const int off = c.j * kChunkCells;
-        const int rem = (int)(c.i1 - c.i0) - off;  // cells of the unit from this chunk on (>= 1)
-        const bool valid = lane < (rem < kChunkCells ? rem : kChunkCells);
+        const int rem = c.len - off;  // cells of the unit from this chunk on (>= 1)
         const uint32_t mask = rem >= kChunkCells ? 0xffffu : (1u << rem) - 1u;
         const int64_t base = (int64_t)c.s * p.n_cells + c.i0 + off;
         const bool use_tma = p.use_tma != 0 && base < INT_MAX / 2;
         unsigned char* stage = ring + st * Q::kChunkBytes;
         const uint32_t bar = smem_addr(&fb[st]);
+        if (use_tma && p.scl_tma != 0) {
+            // every byte of the chunk comes by TMA: one lane issues, the others only arrive
+            if (lane == 0) {
+                st_mask[warp * S + st] = mask;
+                st_swz[warp * S + st] = 1u;
+                mbar_expect_tx(bar, (uint32_t)(Q::kChunkBytes + Q::kSclChunk) + extra_tx);
+                const uint64_t pol = l2_evict_first_policy();
+                const uint32_t kdst = smem_addr(stage);
+                if (KQ4) {
+                    tma_load_3d_hint(kdst, &p.tmap_k, 0, c.g, (int)base, bar, pol);
+                } else {
+#pragma unroll
+                    for (int pl = 0; pl < Q::kPlanes; ++pl) {
+                        tma_load_3d_hint(kdst + pl * Q::kPlane, &p.tmap_k, pl * 128, c.g, (int)base, bar, pol);
+                        if (!VQ4)
+                            tma_load_3d_hint(kdst + Q::kSection + pl * Q::kPlane, &p.tmap_v, pl * 128, c.g, (int)base,
+                                             bar, pol);
+                    }
+                }
+                if (VQ4) tma_load_3d_hint(kdst + Q::kSection, &p.tmap_v, 0, c.g, (int)base, bar, pol);
+                const uint32_t sdst = smem_addr(sring + st * Q::kSclChunk);
+                tma_load_2d_hint(sdst, &p.tmap_ks, scl_box_x<D>(c.g), (int)base, bar, pol);
+                tma_load_2d_hint(sdst + kChunkCells * Q::kSclRow, &p.tmap_vs, scl_box_x<D>(c.g), (int)base, bar, pol);
+            }
+            __syncwarp();
+            cp_async_arrive_noinc(bar);  // (no copies pending: the barrier's 64 arrivals)
+            mbar_arrive(bar);
+            return;
+        }
+        const bool valid = lane < (rem < kChunkCells ? rem : kChunkCells);
+        const bool scl_tma = use_tma && p.scl_tma != 0;
         if (lane == 0) {
             st_mask[warp * S + st] = mask;
             st_swz[warp * S + st] = use_tma ? 1u : 0u;
             const uint32_t bytes =
-                use_tma ? (uint32_t)Q::kChunkBytes : (uint32_t)__popc(mask) * (uint32_t)(Q::kRowBytes + Q::kVRowBytes);
+                use_tma ? (uint32_t)(Q::kChunkBytes + (scl_tma ? Q::kSclChunk : 0))
+                        : (uint32_t)__popc(mask) * (uint32_t)(Q::kRowBytes + Q::kVRowBytes);
             mbar_expect_tx(bar, bytes + extra_tx);
         }
         __syncwarp();
@@ -2100,6 +2199,12 @@ __device__ __forceinline__ void q8_self_body(const SplitDecodeParams& p) {
                 // 4-bit V: one box of the chunk's D/2-byte rows (64 or 128 bytes wide)
                 if (VQ4)
                     tma_load_3d_hint(kdst + Q::kSection, &p.tmap_v, 0, c.g, (int)base, bar, l2_evict_first_policy());
+                if (scl_tma) {
+                    const uint32_t sdst = smem_addr(sring + st * Q::kSclChunk);
+                    tma_load_2d_hint(sdst, &p.tmap_ks, scl_box_x<D>(c.g), (int)base, bar, l2_evict_first_policy());
+                    tma_load_2d_hint(sdst + kChunkCells * Q::kSclRow, &p.tmap_vs, scl_box_x<D>(c.g), (int)base, bar,
+                                     l2_evict_first_policy());
+                }
             }
         } else if (valid) {
             bulk_g2s(smem_addr(stage + lane * Q::kRowBytes), static_cast<const char*>(p.k) + row * Q::kRowBytes,
@@ -2107,9 +2212,9 @@ __device__ __forceinline__ void q8_self_body(const SplitDecodeParams& p) {
             bulk_g2s(smem_addr(stage + Q::kSection + lane * Q::kVRowBytes),
                      static_cast<const char*>(p.v) + row * Q::kVRowBytes, Q::kVRowBytes, bar);
         }
-        if (lane < kChunkCells) {
-            unsigned char* ksd = sring + st * Q::kSclChunk + lane * Q::kSclBytes;
-            unsigned char* vsd = ksd + kChunkCells * Q::kSclBytes;
+        if (lane < kChunkCells && !scl_tma) {
+            unsigned char* ksd = sring + st * Q::kSclChunk + lane * Q::kSclRow + scl_off<D>(c.g);
+            unsigned char* vsd = ksd + kChunkCells * Q::kSclRow;
             if (valid) {
                 if (D == 128) {
                     cp_async_8(smem_addr(ksd), p.k_scale + row * (D / 32));
@@ -2134,7 +2239,7 @@ __device__ __forceinline__ void q8_self_body(const SplitDecodeParams& p) {
     auto issue_general = [&](const ChunkCursor& c, int st, uint32_t extra_tx) {
         const int64_t c0 = c.i0 + (int64_t)c.j * kChunkCells;
         const int64_t i = c0 + lane;
-        bool valid = lane < kChunkCells && i < c.i1;
+        bool valid = lane < kChunkCells && c.j * kChunkCells + lane < c.len;
         int64_t cell = 0;
         if (valid) {
             if (p.plan != nullptr) {
@@ -2165,13 +2270,15 @@ __device__ __forceinline__ void q8_self_body(const SplitDecodeParams& p) {
             base = off_lo + c0;
         }
         const bool use_tma = run && p.use_tma != 0 && mask != 0u && base > INT_MIN / 2 && base < INT_MAX / 2;
+        const bool scl_tma = use_tma && p.scl_tma != 0;
         unsigned char* stage = ring + st * Q::kChunkBytes;
         const uint32_t bar = smem_addr(&fb[st]);
         if (lane == 0) {
             st_mask[warp * S + st] = mask;
             st_swz[warp * S + st] = use_tma ? 1u : 0u;
             const uint32_t bytes =
-                use_tma ? (uint32_t)Q::kChunkBytes : (uint32_t)__popc(mask) * (uint32_t)(Q::kRowBytes + Q::kVRowBytes);
+                use_tma ? (uint32_t)(Q::kChunkBytes + (scl_tma ? Q::kSclChunk : 0))
+                        : (uint32_t)__popc(mask) * (uint32_t)(Q::kRowBytes + Q::kVRowBytes);
             mbar_expect_tx(bar, bytes + extra_tx);
         }
         __syncwarp();
@@ -2194,6 +2301,12 @@ __device__ __forceinline__ void q8_self_body(const SplitDecodeParams& p) {
                 // 4-bit V: one box of the chunk's D/2-byte rows (64 or 128 bytes wide)
                 if (VQ4)
                     tma_load_3d_hint(kdst + Q::kSection, &p.tmap_v, 0, c.g, (int)base, bar, l2_evict_first_policy());
+                if (scl_tma) {
+                    const uint32_t sdst = smem_addr(sring + st * Q::kSclChunk);
+                    tma_load_2d_hint(sdst, &p.tmap_ks, scl_box_x<D>(c.g), (int)base, bar, l2_evict_first_policy());
+                    tma_load_2d_hint(sdst + kChunkCells * Q::kSclRow, &p.tmap_vs, scl_box_x<D>(c.g), (int)base, bar,
+                                     l2_evict_first_policy());
+                }
             }
         } else if (valid) {
             const int64_t row = cell * Hk + c.g;
@@ -2203,9 +2316,9 @@ __device__ __forceinline__ void q8_self_body(const SplitDecodeParams& p) {
                      static_cast<const char*>(p.v) + row * Q::kVRowBytes, Q::kVRowBytes, bar);
         }
         // scales: a masked cell's are zero, so its (finite) int8 row contributes nothing
-        if (lane < kChunkCells) {
-            unsigned char* ksd = sring + st * Q::kSclChunk + lane * Q::kSclBytes;
-            unsigned char* vsd = ksd + kChunkCells * Q::kSclBytes;
+        if (lane < kChunkCells && !scl_tma) {
+            unsigned char* ksd = sring + st * Q::kSclChunk + lane * Q::kSclRow + scl_off<D>(c.g);
+            unsigned char* vsd = ksd + kChunkCells * Q::kSclRow;
             if (valid) {
                 const int64_t row = cell * Hk + c.g;
                 if (D == 128) {
@@ -2235,9 +2348,10 @@ __device__ __forceinline__ void q8_self_body(const SplitDecodeParams& p) {
 
     // Prime the ring with this warp's first S chunks.
     ChunkCursor ld;
-    ld.u = (int64_t)blockIdx.x - gridDim.x;  // seek loads unit blockIdx.x
-    ld.j = 0;
+    ld.u = blockIdx.x;
+    ld.j = warp;
     ld.n_chunks = 0;
+    if (ld.u < n_units) cursor_fill(p, ld);
     cursor_seek(p, ld, n_units, warp);
     uint32_t L = 0;  // chunks issued
     for (; L < (uint32_t)S && ld.u < n_units; ++L) {
@@ -2258,7 +2372,7 @@ __device__ __forceinline__ void q8_self_body(const SplitDecodeParams& p) {
         uint32_t C = 0, X = 0;
         bool stop = false;
         constexpr float kLn2 = 0.69314718055994530942f;
-        for (int64_t u = blockIdx.x; u < n_units && !stop; u += gridDim.x) {
+        for (uint32_t u = blockIdx.x; u < n_units && !stop; u += gridDim.x) {
             const Unit x = unit_at(p, u);
             const int64_t part = (int64_t)x.s * p.part_stride + p.part_base + x.split_idx;
             const int row0 = p.rg_rows * x.rg;  // the unit's first query row
@@ -2296,8 +2410,18 @@ __device__ __forceinline__ void q8_self_body(const SplitDecodeParams& p) {
                 const bool swz = st_swz[warp * S + st] != 0u;
                 const uint32_t kb = smem_addr(ring + st * Q::kChunkBytes);
                 const uint32_t vb = kb + Q::kSection;
-                const unsigned char* ks = sring + st * Q::kSclChunk;
-                const unsigned char* vs = ks + kChunkCells * Q::kSclBytes;
+                const unsigned char* ks = sring + st * Q::kSclChunk + scl_off<D>(x.g);
+                const unsigned char* vs = ks + kChunkCells * Q::kSclRow;
+                if (swz && p.scl_tma != 0 && mask != 0xffffu) {
+                    // the scale box brought masked cells' rows too (plan holes, cells past the
+                    // unit): zero them, so that P = 0 never meets a non-finite V scale
+                    if (lane < kChunkCells && !((mask >> lane) & 1u)) {
+                        uint4* z = reinterpret_cast<uint4*>(sring + st * Q::kSclChunk + lane * Q::kSclRow);
+                        z[0] = make_uint4(0u, 0u, 0u, 0u);
+                        z[kChunkCells] = make_uint4(0u, 0u, 0u, 0u);
+                    }
+                    __syncwarp();
+                }
                 if (mask != 0u) {
                     const int64_t p0 = x.i0 + (int64_t)j * kChunkCells;
                     int lim[2];
@@ -2460,7 +2584,22 @@ __device__ __forceinline__ void q8_self_body(const SplitDecodeParams& p) {
             ok = r < p.group * p.n_q;
             return (int64_t)(r / p.group) * H + y.g * p.group + r % p.group;
         };
-        for (int64_t u = blockIdx.x; u < n_units && !stop; u += gridDim.x) {
+        // head-pair units (head_dim 256 only): the partials keep head_dim 128
+        const bool pair = D == 256 && !MQ8 && p.pair != 0;
+        const int DO = pair ? D / 2 : D;
+        auto load_q = [&](const Unit& y) {
+            if constexpr (D == 256 && !MQ8) {
+                if (pair) {
+                    load_q_frags_pair<KQ4>(p, y.s, y.g, gq, tq, qa);
+                    return;
+                }
+            }
+            if (KQ4)
+                load_q_frags_q4k<D>(p, y.s, y.g, gq, tq, qa, MQ8 ? y.rg : -1);
+            else
+                load_q_frags<KVT, D>(p, y.s, y.g, gq, tq, qa, MQ8 ? y.rg : -1);
+        };
+        for (uint32_t u = blockIdx.x; u < n_units && !stop; u += gridDim.x) {
             const Unit x = unit_at(p, u);
             const int64_t part = (int64_t)x.s * p.part_stride + p.part_base + x.split_idx;
             if (x.n_tiles == 0) {
@@ -2477,23 +2616,18 @@ __device__ __forceinline__ void q8_self_body(const SplitDecodeParams& p) {
                             }
                         }
                     } else {
-                        for (int idx = lane; idx < p.group * D; idx += 32) {
-                            const int r = idx / D;
-                            const int d = idx - r * D;
+                        for (int idx = lane; idx < p.group * DO; idx += 32) {
+                            const int r = idx / DO;
+                            const int d = idx - r * DO;
                             const int h = x.g * p.group + r;
-                            p.part_o[(part * H + h) * D + d] = 0.f;
+                            p.part_o[(part * H + h) * DO + d] = 0.f;
                             if (d == 0) p.part_lse[part * H + h] = -INFINITY;
                         }
                     }
                 }
                 continue;
             }
-            if (qa_unit != u) {
-                if (KQ4)
-                    load_q_frags_q4k<D>(p, x.s, x.g, gq, tq, qa, MQ8 ? x.rg : -1);
-                else
-                    load_q_frags<KVT, D>(p, x.s, x.g, gq, tq, qa, MQ8 ? x.rg : -1);
-            }
+            if (qa_unit != u) load_q(x);
             // MQ8: causal limit (logical position, exclusive) of the lane's row 8 rg + gq
             const int64_t lim_row = MQ8 ? x.len - p.n_q + 1 + (8 * x.rg + gq) / p.group : 0;
             float oacc[D / 16][4];
@@ -2512,8 +2646,18 @@ __device__ __forceinline__ void q8_self_body(const SplitDecodeParams& p) {
                 const bool swz = st_swz[warp * S + st] != 0u;
                 const uint32_t kb = smem_addr(ring + st * Q::kChunkBytes);
                 const uint32_t vb = kb + Q::kSection;
-                const unsigned char* ks = sring + st * Q::kSclChunk;
-                const unsigned char* vs = ks + kChunkCells * Q::kSclBytes;
+                const unsigned char* ks = sring + st * Q::kSclChunk + scl_off<D>(x.g);
+                const unsigned char* vs = ks + kChunkCells * Q::kSclRow;
+                if (swz && p.scl_tma != 0 && mask != 0xffffu) {
+                    // the scale box brought masked cells' rows too (plan holes, cells past the
+                    // unit): zero them, so that P = 0 never meets a non-finite V scale
+                    if (lane < kChunkCells && !((mask >> lane) & 1u)) {
+                        uint4* z = reinterpret_cast<uint4*>(sring + st * Q::kSclChunk + lane * Q::kSclRow);
+                        z[0] = make_uint4(0u, 0u, 0u, 0u);
+                        z[kChunkCells] = make_uint4(0u, 0u, 0u, 0u);
+                    }
+                    __syncwarp();
+                }
                 // (fragments are read straight from the stage: staging them in registers first
                 // measured slower here, the extra registers spill at this CTA count)
                 if (mask != 0u) {
@@ -2532,7 +2676,7 @@ __device__ __forceinline__ void q8_self_body(const SplitDecodeParams& p) {
                         if (swz)
                             q8_chunk_swz<D>(kb, vb, ks, vs, lmask, lane, qa, oacc, m_run, l_run, p.scale_log2);
                         else
-                            consume_tile<KVT, D, false, Q::kPlane>(kb, vb, ks, vs, lmask, 0, lane, qa, oacc, m_run,
+                            consume_tile<KVT, D, false, Q::kPlane, Q::kSclRow>(kb, vb, ks, vs, lmask, 0, lane, qa, oacc, m_run,
                                                                    l_run, p.scale_log2);
                     }
                 }
@@ -2553,10 +2697,7 @@ __device__ __forceinline__ void q8_self_body(const SplitDecodeParams& p) {
             if (un < n_units) {
                 const Unit y = unit_at(p, un);
                 if (y.n_tiles > 0) {
-                    if (KQ4)
-                        load_q_frags_q4k<D>(p, y.s, y.g, gq, tq, qa, MQ8 ? y.rg : -1);
-                    else
-                        load_q_frags<KVT, D>(p, y.s, y.g, gq, tq, qa, MQ8 ? y.rg : -1);
+                    load_q(y);
                     qa_unit = un;
                 }
             }
@@ -2647,16 +2788,20 @@ __device__ __forceinline__ void q8_self_body(const SplitDecodeParams& p) {
                     prow = part * H + x.g * p.group + r;
                 }
                 if (ok) {
-                    float* orow = p.part_o + prow * D;
+                    float* orow = p.part_o + prow * DO;
+                    // head pairs: row 2tq + e keeps only its own head's half of the 256 dims
+                    const int own = pair ? ((2 * tq + e) >= (p.group >> 1) ? 1 : 0) : -1;
 #pragma unroll
                     for (int b = 0; b < D / 32; ++b) {
+                        if (own >= 0 && (b >= D / 64 ? 1 : 0) != own) continue;
+                        float* ob = orow + 32 * (own >= 0 ? b - own * (D / 64) : b);
                         if constexpr (VQ4) {
                             // 4-bit V: m-tile 2b holds dims 32b + 2gq (+1), m-tile 2b+1 dims 32b + 16 + 2gq (+1)
-                            *reinterpret_cast<float2*>(orow + 32 * b + 2 * gq) = make_float2(oacc[2 * b][e], oacc[2 * b][2 + e]);
-                            *reinterpret_cast<float2*>(orow + 32 * b + 16 + 2 * gq) =
+                            *reinterpret_cast<float2*>(ob + 2 * gq) = make_float2(oacc[2 * b][e], oacc[2 * b][2 + e]);
+                            *reinterpret_cast<float2*>(ob + 16 + 2 * gq) =
                                 make_float2(oacc[2 * b + 1][e], oacc[2 * b + 1][2 + e]);
                         } else {
-                            *reinterpret_cast<float4*>(orow + 32 * b + 4 * gq) =
+                            *reinterpret_cast<float4*>(ob + 4 * gq) =
                                 make_float4(oacc[2 * b][e], oacc[2 * b][2 + e], oacc[2 * b + 1][e], oacc[2 * b + 1][2 + e]);
                         }
                     }

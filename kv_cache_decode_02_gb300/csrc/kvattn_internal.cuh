@@ -44,6 +44,8 @@ inline DecodeWsLayout decode_ws_layout(int n_seq, int n_head, int head_dim, int6
 struct SplitDecodeParams {
     CUtensorMap tmap_k;       // 3-D {row elements, KV heads, cells} views of the caches for
     CUtensorMap tmap_v;       // the TMA path (valid when use_tma != 0)
+    CUtensorMap tmap_ks;      // 2-D {n_head_kv * head_dim / 32 halves, cells} views of the
+    CUtensorMap tmap_vs;      // quantised caches' scales (valid when scl_tma != 0)
     const __half* q;          // [S][H][D]
     const void* k;            // [cells][Hk][D] (f16 or int8)
     const void* v;
@@ -77,6 +79,9 @@ struct SplitDecodeParams {
     int rg_rows;              // query rows per row group (when n_rg > 1)
     int n_stages;
     int use_tma;              // tiles that are one physical run load through tmap_k/tmap_v
+    int scl_tma;              // ... and their scale rows through tmap_ks/tmap_vs: one 16-byte
+                              // box row per cell (for head_dim 128 the KV-head pair g & ~1,
+                              // g | 1: the scale rows of one head are 8 bytes)
     int write_beyond;         // splits past a sequence's length still write (0, -inf)
     int src_lsu;              // K/V rows arrive by 16-byte cp.async (e.g. straight from pinned
                               // host memory) instead of the TMA engine
@@ -85,9 +90,19 @@ struct SplitDecodeParams {
     int no_dep_wait;          // 1: launched as a programmatic dependent of a grid whose results
                               // it does not read, and itself launched only after everything it
                               // does read was complete: skip the dependency wait (run beside it)
+    int pair;                 // head-pair units (quantised head_dim-128 caches, G <= 4, an even
+                              // number of KV heads): the head_dim-256 kernels read 256-byte rows
+                              // of the KV-head pair 2g, 2g+1; n_head_kv and group count pairs and
+                              // the pair's 2G query rows, q and the partials keep head_dim 128
     float scale_log2;         // scale * log2(e)
 };
 
+// Fill a 2-D tensor map {n_head_kv * head_dim / 32 halves, cells} over a scale plane with
+// boxes of 8 halves (16 bytes) x the kernel's cells, no swizzle.  Returns false when the
+// geometry does not allow it (the base not 16-byte aligned, rows not a multiple of 16
+// bytes) or the encoder rejects it.
+bool encode_scale_tensor_map(CUtensorMap* map, const void* base, int64_t cells, int n_head_kv, int head_dim,
+                             int box_cells);
 // Fill a 3-D tensor map {row elements, n_head_kv, cells} over a cell-major cache with
 // boxes of the kernel's cells x 128 bytes (a whole 64- or 128-byte row for 4-bit V rows,
 // v_side with KVATTN_KV_Q8_0_Q4_0) and the 128-byte swizzle.  Returns false if the

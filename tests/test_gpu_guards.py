@@ -6,7 +6,8 @@ GQA row written as if it were a real head -- the out-of-bounds access the pages 
 ("KVARN KV Performance optimizations", item 2) -- lands in a sentinel.
 
 Cases: every cache type at head_dim 128 and 256, ragged lengths and an empty sequence,
-G = 5, 6 and 7 (query rows padded to eight), compact plans with holes, the partials entry
+G = 5, 6 and 7 (query rows padded to eight), the quantised head_dim-128 caches as KV-head
+pairs (G = 2, 3, 4: each query row keeps its own head's half), compact plans with holes, the partials entry
 point, multi-query row layouts and row groups, window + tail (staged tiles with a ragged
 last tile, and the tail read in place) and the merge.  Results are also checked against the
 oracle so that a guard cannot pass on a call that did nothing.
@@ -144,6 +145,10 @@ SINGLE = [
     ("q8q4", 256, 7, [515, 64], 128),
     ("q4", 128, 5, [2049, 3], 512),
     ("q4", 256, 6, [800, 0], 128),
+    # head_dim 128 with G <= 4 and an even KV-head count: KV-head pairs on the 256 kernels
+    ("q8", 128, 4, [1100, 17, 0], 128),
+    ("q8q4", 128, 3, [515, 64], 64),
+    ("q4", 128, 2, [2049, 3], 512),
 ]
 
 
@@ -174,7 +179,8 @@ def test_guards_single_query(kvattn, kind, D, G, lens, split):
     assert_close(out.inner, lse.inner, wo, wl)
 
 
-@pytest.mark.parametrize("kind,D,G", [("f16", 128, 6), ("f16", 256, 5), ("q8", 128, 7), ("q4", 256, 6)])
+@pytest.mark.parametrize("kind,D,G", [("f16", 128, 6), ("f16", 256, 5), ("q8", 128, 7), ("q4", 256, 6),
+                                     ("q8q4", 128, 4)])
 def test_guards_plan_and_partials(kvattn, kind, D, G):
     """A compact plan with holes (descriptors written into the workspace), decoded once
     through kvattn_decode and once through kvattn_decode_partials into guarded caller

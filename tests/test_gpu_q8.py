@@ -157,3 +157,53 @@ def test_q8_0_bounded_wait_reports_timeout_and_context_survives(kvattn, monkeypa
     assert kvattn.kvattn_workspace_status(ws) == 0
     wo, wl = oracle.decode_q8_0(q, kq, kd, vq, vd, [N])
     assert_close(out, lse, wo, wl)
+
+
+@pytest.mark.parametrize("kv", ["q8", "q8q4", "q4"])
+@pytest.mark.parametrize("G,Hk", [(4, 8), (2, 2), (1, 4)])
+def test_head_pairs_equal_single_heads(kvattn, monkeypatch, kv, G, Hk):
+    """KV-head pairs (the default for head_dim 128, G <= 4, even KV-head counts) and one KV
+    head per work unit (KVATTN_PAIR=0) both match the oracle and agree with each other to
+    rounding; a compact plan with holes over NaN-scaled cells, ragged lengths."""
+    import torch
+    import oracle
+    from oracle import plan_oracle as po
+    rng = np.random.default_rng([37, G, Hk, len(kv)])
+    D, pool = 128, 16
+    H = G * Hk
+    n_cells = pool * 128
+    kq = (rng.integers(0, 256, (n_cells, Hk, D // 2), dtype=np.uint8) if kv == "q4"
+          else rng.integers(-127, 128, (n_cells, Hk, D), dtype=np.int8))
+    kd = rng.uniform(0.001, 0.3 if kv == "q4" else 0.02, (n_cells, Hk, D // 32)).astype(np.float16)
+    vq = (rng.integers(-127, 128, (n_cells, Hk, D), dtype=np.int8) if kv == "q8"
+          else rng.integers(0, 256, (n_cells, Hk, D // 2), dtype=np.uint8))
+    vd = rng.uniform(0.001, 0.02 if kv == "q8" else 0.3, (n_cells, Hk, D // 32)).astype(np.float16)
+    perm = rng.permutation(pool)
+    encoded, selected = [], []
+    for recs in (perm[:5], perm[5:6], perm[6:12]):
+        cells = (recs[:, None] * 128 + np.arange(128)[None]).reshape(-1)
+        sel = cells[rng.random(cells.size) >= 0.25]
+        encoded.append(sel.astype(np.int64)[rng.permutation(sel.size)])
+        selected.append(sel)
+    unused = np.setdiff1d(np.arange(n_cells), np.concatenate(selected))
+    kd[unused] = np.nan
+    vd[unused] = np.nan
+    plan, lens = kvattn.build_cell_plan(encoded, n_cells)
+    q = rng.standard_normal((3, H, D), dtype=np.float32).astype(np.float16)
+    kt = {"q8": kvattn.KVATTN_KV_Q8_0, "q8q4": kvattn.KVATTN_KV_Q8_0_Q4_0, "q4": kvattn.KVATTN_KV_Q4_0}[kv]
+    res = []
+    for pair in ("1", "0"):
+        monkeypatch.setenv("KVATTN_PAIR", pair)
+        out, lse = kvattn.decode(dev(q), dev(kq), dev(vq), dev(lens), split=128, k_scales=dev(kd), v_scales=dev(vd),
+                                 cell_plan=dev(plan), n_cells=n_cells, kv_type=kt)
+        torch.cuda.synchronize()
+        res.append((out.cpu().numpy(), lse.cpu().numpy()))
+    fn = {"q8": oracle.decode_q8_0, "q8q4": oracle.decode_q8_0_q4_0, "q4": oracle.decode_q4_0}[kv]
+    wo, wl = fn(q, kq, kd, vq, vd, lens.tolist(), plan=plan)
+    for o, l in res:
+        assert_close(torch.from_numpy(o), torch.from_numpy(l), wo, wl)
+    # the two geometries give a warp different cells (two warps per pair unit, four per
+    # single-head unit), so their running maxima and the f16 roundings of P differ: the
+    # results agree to rounding, not bit for bit
+    assert np.max(np.abs(res[0][0] - res[1][0])) <= 1e-3
+    assert np.max(np.abs(res[0][1] - res[1][1])) <= 1e-4

@@ -354,3 +354,22 @@ def test_merge_extreme_lses(kvattn, centre, spread):
     # the oracle merges the same fp32 values in fp64
     wo, wl = oracle.merge(parts.astype(np.float32), lses.astype(np.float32))
     assert_close(out, lse, wo, wl)
+
+
+@pytest.mark.parametrize("case", ["ramp_split", "ramp_global", "dominant_last", "dominant_mid", "q_x16", "scale_1",
+                                  "offset_p200", "offset_m200"])
+@pytest.mark.parametrize("kind,G", [("q8", 4), ("q8q4", 3), ("q4", 2), ("q8", 1)])
+def test_rescale_head_pairs(kvattn, kind, G, case):
+    """Quantised head_dim-128 caches with at most four query heads per KV head and an even
+    number of KV heads run as KV-head pairs on the head_dim-256 kernels (each query row
+    keeps its own head's half of the 256 dimensions)."""
+    rng = np.random.default_rng([36, G, CASES.index(case), list(KIND_ORACLE).index(kind)])
+    S, N, Hk, D, split = 2, 2048, 4, 128, 512
+    H = Hk * G
+    lens = [N, 1459]
+    kc0, kc1, a_nat, b_nat, qmul, scale = controls(case, lens, N, split)
+    q = make_q(rng, (S, H), D, a_nat, b_nat, qmul, scale)
+    cache = make_cache(rng, kind, (S, N, Hk), D, kc0, kc1)
+    out, lse = gpu_decode(kvattn, kind, q, cache, lens, split, scale, N, N)
+    wo, wl = KIND_ORACLE[kind](q, *cache, lens, scale=scale)
+    assert_close(out, lse, wo, wl)
