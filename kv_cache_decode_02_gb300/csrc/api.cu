@@ -551,6 +551,7 @@ int decode_impl(const void* q, const void* k_cache, const void* v_cache, const v
     m.head_dim = head_dim;
     m.split = split;
     m.all_written = 1;
+    m.allow_slices = env_int("KVATTN_MERGE_SLICES", 1) != 0;
     m.wide_rows_max = sm_count();
     return cuda_status(launch_merge(m, s, pdl && n_split > 0));
 }
@@ -821,6 +822,7 @@ void prepare_window_tail(TailPlan& t, const void* q, const void* k_win, const vo
     m.head_dim = head_dim;
     m.split = 1;
     m.all_written = 1;
+    m.allow_slices = env_int("KVATTN_MERGE_SLICES", 1) != 0;
     m.wide_rows_max = sm_count();
     (void)n_tail;
 }
@@ -1218,6 +1220,7 @@ int kvattn_decode_window_tail_direct(const void* q, const void* k_win, const voi
     m.head_dim = head_dim;
     m.split = 1;
     m.all_written = 1;
+    m.allow_slices = env_int("KVATTN_MERGE_SLICES", 1) != 0;
     m.wide_rows_max = sm_count();
     // after the overlapped decodes the merge must follow both: an ordinary launch
     return cuda_status(launch_merge(m, cs, pdl && n_parts > 0 && !overlap));

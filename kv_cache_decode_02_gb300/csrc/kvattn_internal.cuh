@@ -125,6 +125,8 @@ struct MergeParams {
     int head_dim, split;
     int64_t wide_rows_max;    // decode partials of at most this many rows in all may merge with
                               // 16-warp CTAs (one per SM); 0: always 8 warps
+    int allow_slices;         // decode partials of rows with many parts may spread each row's
+                              // head_dim over several CTAs
 };
 
 // Launchers (return cudaError_t of the launch).

@@ -280,6 +280,129 @@ __global__ void __launch_bounds__(WARPS * 32, 16 / WARPS) merge_kernel(const Mer
     if (threadIdx.x == 0) p.lse[row] = (W > 0.f) ? M + __logf(W) : -INFINITY;
 }
 
+// Decode partials of rows with many parts, one row spread over several CTAs: CTA (row,
+// slice) merges float4 chunks [slice CW, slice CW + CW) of the row's O over all parts
+// (CW = 8, 16 or 32; each
+// CTA reads every LSE and computes the same weights).  Lanes form 32 / CW groups of CW
+// lanes; group k of warp w reads parts w G + k, w G + k + WARPS G, ... (G groups a warp),
+// BATCH parts per group and round, so one load instruction covers G parts.  The groups of a
+// warp, then the warps, combine their (max, sum, O) with the usual rescaling.
+template <int WARPS, int CW, int BATCH>
+__global__ void __launch_bounds__(WARPS * 32) merge_slices_kernel(const MergeParams p) {
+    constexpr int G = 32 / CW;
+    __shared__ float red_m[WARPS], red_s[WARPS];
+    __shared__ float4 acc_smem[WARPS][CW];
+    pdl_launch_dependents();
+    pdl_wait();
+    const int row = blockIdx.x;  // s * n_rows + h
+    const int s = row / p.n_rows;
+    const int h = row - s * p.n_rows;
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int grp = lane / CW;
+    const int c = blockIdx.y * CW + (lane - grp * CW);  // this lane's float4 chunk of the row
+
+    int64_t n_parts = p.n_parts;
+    if (p.seq_lens != nullptr) {
+        int64_t L = p.seq_lens[s];
+        L = L < 0 ? 0 : L;
+        L = L < p.max_len ? L : p.max_len;
+        L = L < p.len_cap ? L : p.len_cap;
+        n_parts = (L + p.split - 1) / p.split;
+    }
+    const float* lse_base = p.part_lse + (int64_t)s * p.n_parts * p.n_rows + h;
+    const float4* o_base =
+        reinterpret_cast<const float4*>(p.part_o + ((int64_t)s * p.n_parts * p.n_rows + h) * p.head_dim) + c;
+    const int64_t lse_stride = p.n_rows;
+    const int64_t o_stride = (int64_t)p.n_rows * p.head_dim / 4;  // in float4
+
+    float mw = -INFINITY, sw = 0.f;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int64_t q0 = (int64_t)warp * G + grp; q0 < n_parts; q0 += (int64_t)WARPS * G * BATCH) {
+        float l[BATCH];
+        float4 v[BATCH];
+#pragma unroll
+        for (int u = 0; u < BATCH; ++u) {
+            const int64_t q = q0 + (int64_t)u * WARPS * G;
+            l[u] = q < n_parts ? __ldg(lse_base + q * lse_stride) : -INFINITY;
+            v[u] = q < n_parts ? __ldg(o_base + q * o_stride) : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+        float bm = -INFINITY;
+#pragma unroll
+        for (int u = 0; u < BATCH; ++u) bm = fmaxf(bm, l[u]);
+        const float nm = fmaxf(mw, bm);
+        if (nm == -INFINITY) continue;
+        const float keep = __expf(mw - nm);  // 0 when nothing was accumulated yet
+        sw *= keep;
+        acc.x *= keep;
+        acc.y *= keep;
+        acc.z *= keep;
+        acc.w *= keep;
+#pragma unroll
+        for (int u = 0; u < BATCH; ++u) {
+            const float w = l[u] == -INFINITY ? 0.f : __expf(l[u] - nm);
+            sw += w;
+            acc.x = fmaf(w, v[u].x, acc.x);
+            acc.y = fmaf(w, v[u].y, acc.y);
+            acc.z = fmaf(w, v[u].z, acc.z);
+            acc.w = fmaf(w, v[u].w, acc.w);
+        }
+        mw = nm;
+    }
+    // the lane groups of the warp (lanes CW apart hold the same chunk)
+#pragma unroll
+    for (int o = 16; o >= CW; o >>= 1) {
+        const float m2 = __shfl_xor_sync(0xffffffffu, mw, o);
+        const float s2 = __shfl_xor_sync(0xffffffffu, sw, o);
+        float4 a2;
+        a2.x = __shfl_xor_sync(0xffffffffu, acc.x, o);
+        a2.y = __shfl_xor_sync(0xffffffffu, acc.y, o);
+        a2.z = __shfl_xor_sync(0xffffffffu, acc.z, o);
+        a2.w = __shfl_xor_sync(0xffffffffu, acc.w, o);
+        const float nm = fmaxf(mw, m2);
+        const float f1 = mw == -INFINITY ? 0.f : __expf(mw - nm);
+        const float f2 = m2 == -INFINITY ? 0.f : __expf(m2 - nm);
+        sw = sw * f1 + s2 * f2;
+        acc.x = acc.x * f1 + a2.x * f2;
+        acc.y = acc.y * f1 + a2.y * f2;
+        acc.z = acc.z * f1 + a2.z * f2;
+        acc.w = acc.w * f1 + a2.w * f2;
+        mw = nm;
+    }
+    if (lane == 0) {
+        red_m[warp] = mw;
+        red_s[warp] = sw;
+    }
+    if (lane < CW) acc_smem[warp][lane] = acc;
+    __syncthreads();
+    if (threadIdx.x < CW) {
+        float M = -INFINITY;
+#pragma unroll
+        for (int w = 0; w < WARPS; ++w) M = fmaxf(M, red_m[w]);
+        float W = 0.f;
+        float4 t = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (M != -INFINITY) {
+#pragma unroll
+            for (int w = 0; w < WARPS; ++w) {
+                const float f = red_m[w] == -INFINITY ? 0.f : __expf(red_m[w] - M);
+                W = fmaf(f, red_s[w], W);
+                const float4 a = acc_smem[w][threadIdx.x];
+                t.x = fmaf(f, a.x, t.x);
+                t.y = fmaf(f, a.y, t.y);
+                t.z = fmaf(f, a.z, t.z);
+                t.w = fmaf(f, a.w, t.w);
+            }
+        }
+        const float inv = W > 0.f ? 1.f / W : 0.f;
+        t.x *= inv;
+        t.y *= inv;
+        t.z *= inv;
+        t.w *= inv;
+        reinterpret_cast<float4*>(p.out + (int64_t)row * p.head_dim)[blockIdx.y * CW + threadIdx.x] = t;
+        if (blockIdx.y == 0 && threadIdx.x == 0) p.lse[row] = (W > 0.f) ? M + __logf(W) : -INFINITY;
+    }
+}
+
 }  // namespace
 
 cudaError_t launch_merge(const MergeParams& params, cudaStream_t stream, bool pdl) {
@@ -289,6 +412,32 @@ cudaError_t launch_merge(const MergeParams& params, cudaStream_t stream, bool pd
     if (rows == 0) return cudaSuccess;
     if (rows > (int64_t)INT32_MAX) return cudaErrorInvalidValue;
     cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    cfg.stream = stream;
+    // Decode partials of head_dim-128 rows with more parts than one round of a CTA (64) and
+    // too few rows to fill the SMs: each row's head_dim is split over several CTAs (slices of
+    // 8 to 32 float4 chunks, at most one CTA per SM in all), so that more SMs read the parts
+    // from L2 at once (Q8_0 over 131072 cells at split 512, 256 parts a row: 66.2 -> 64.9 us
+    // per op).  At head_dim 256 the same split measured slower (114.7 -> 122.7 us), so those
+    // rows keep one CTA each.
+    const int chunks = p.head_dim / 4;
+    if (p.all_written && p.allow_slices && p.head_dim == 128 && p.n_parts > 64) {
+        int slices = chunks / 8;
+        while (slices > 1 && rows * slices > p.wide_rows_max) slices >>= 1;
+        const int cw = chunks / slices;  // float4 chunks per slice: 8, 16 or 32
+        if (slices > 1 && chunks % slices == 0 && cw <= 32 && rows * (int64_t)slices <= (int64_t)INT32_MAX) {
+            cfg.gridDim = dim3((unsigned)rows, (unsigned)slices, 1);
+            cfg.blockDim = dim3(kMergeWarps * 32, 1, 1);
+            cfg.dynamicSmemBytes = 0;
+            if (cw == 8) return cudaLaunchKernelEx(&cfg, merge_slices_kernel<kMergeWarps, 8, 8>, p);
+            if (cw == 16) return cudaLaunchKernelEx(&cfg, merge_slices_kernel<kMergeWarps, 16, 8>, p);
+            return cudaLaunchKernelEx(&cfg, merge_slices_kernel<kMergeWarps, 32, 8>, p);
+        }
+    }
     cfg.gridDim = dim3((unsigned)rows, 1, 1);
     // Rows of decode partials with more than one round of parts for 8 warps (64 parts at
     // head_dim <= 128, 32 at 256) take 16 warps, half the dependent rounds of loads, when
@@ -299,12 +448,6 @@ cudaError_t launch_merge(const MergeParams& params, cudaStream_t stream, bool pd
     const int warps = wide ? 2 * kMergeWarps : kMergeWarps;
     cfg.blockDim = dim3(warps * 32, 1, 1);
     cfg.dynamicSmemBytes = warps * p.head_dim * sizeof(float);
-    cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = pdl ? 1 : 0;
     return wide ? cudaLaunchKernelEx(&cfg, merge_kernel<2 * kMergeWarps>, p)
                 : cudaLaunchKernelEx(&cfg, merge_kernel<kMergeWarps>, p);
 }

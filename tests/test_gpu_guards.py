@@ -149,6 +149,9 @@ SINGLE = [
     ("q8", 128, 4, [1100, 17, 0], 128),
     ("q8q4", 128, 3, [515, 64], 64),
     ("q4", 128, 2, [2049, 3], 512),
+    # 125 parts a row at head_dim 128: each row's merge spread over several CTAs
+    ("f16", 128, 4, [4000, 1000, 0], 32),
+    ("q8", 128, 4, [4000, 77], 32),
 ]
 
 
