@@ -615,6 +615,98 @@ __device__ __forceinline__ void mq_tile(uint32_t kb, uint32_t vb, uint32_t mask,
     }
 }
 
+// A whole 32-cell tile for the warp's 16 query rows (the row-split layouts): four
+// independent q.K^T accumulator chains instead of two per 16-cell half, one max and sum
+// reduction per row and tile, and P V over k = 32 cells.  lim[hh]: cells c < lim[hh] of the
+// tile are inside the causal window of the lane's row gq + 8 hh.  The caller has zeroed the
+// V rows of masked cells that came in with a TMA box.
+template <bool SWZ>
+__device__ __forceinline__ void mq_tile32(uint32_t kb, uint32_t vb, uint32_t mask, int lane, const int (&lim)[2],
+                                          const uint32_t (&qa)[8][4], float (&oacc)[2][8][4], float (&m_run)[2],
+                                          float (&l_run)[2], float scale_log2) {
+    constexpr int D = 128;
+    using G = Geom<KVATTN_KV_F16, D>;
+    const int tq = lane & 3;
+    float sacc[4][4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) sacc[j][0] = sacc[j][1] = sacc[j][2] = sacc[j][3] = 0.f;
+#pragma unroll
+    for (int kk = 0; kk < D / 16; kk += 2) {
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            uint32_t b0, b1, b2, b3;
+            ldsm_x4(sec_addr<SWZ, G::kPadRow>(kb, 8 * j + (lane & 7), (kk * 16 + 8 * (lane >> 3)) * 2), b0, b1, b2, b3);
+            mma_16816(sacc[j], qa[kk][0], qa[kk][2], qa[kk][1], qa[kk][3], b0, b1);
+            mma_16816(sacc[j], qa[kk + 1][0], qa[kk + 1][2], qa[kk + 1][1], qa[kk + 1][3], b2, b3);
+        }
+    }
+    float x[2][4][2];
+    float tmax[2] = {-INFINITY, -INFINITY};
+#pragma unroll
+    for (int hh = 0; hh < 2; ++hh)
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                const int c = 8 * j + 2 * tq + e;
+                const bool ok = ((mask >> c) & 1u) && c < lim[hh];
+                x[hh][j][e] = ok ? sacc[j][2 * hh + e] * scale_log2 : -INFINITY;
+                tmax[hh] = fmaxf(tmax[hh], x[hh][j][e]);
+            }
+#pragma unroll
+    for (int hh = 0; hh < 2; ++hh) {
+        tmax[hh] = fmaxf(tmax[hh], __shfl_xor_sync(0xffffffffu, tmax[hh], 1));
+        tmax[hh] = fmaxf(tmax[hh], __shfl_xor_sync(0xffffffffu, tmax[hh], 2));
+    }
+    const bool grow = __any_sync(0xffffffffu, tmax[0] > m_run[0] + kRescaleSlack || tmax[1] > m_run[1] + kRescaleSlack);
+    if (grow) {
+        float alpha[2];
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+            const float m_new = fmaxf(m_run[hh], tmax[hh]);
+            alpha[hh] = fast_exp2(m_run[hh] - ((m_new == -INFINITY) ? 0.f : m_new));
+            m_run[hh] = m_new;
+            l_run[hh] *= alpha[hh];
+        }
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt) {
+            const float a0 = __shfl_sync(0xffffffffu, alpha[nt], 8 * tq);
+            const float a1 = __shfl_sync(0xffffffffu, alpha[nt], 8 * tq + 4);
+#pragma unroll
+            for (int mt = 0; mt < D / 16; ++mt) {
+                oacc[nt][mt][0] *= a0;
+                oacc[nt][mt][1] *= a1;
+                oacc[nt][mt][2] *= a0;
+                oacc[nt][mt][3] *= a1;
+            }
+        }
+    }
+    uint32_t pb[2][4];
+#pragma unroll
+    for (int hh = 0; hh < 2; ++hh) {
+        const float m_use = (m_run[hh] == -INFINITY) ? 0.f : m_run[hh];
+        float psum = 0.f;  // over the fp32 probabilities (the MMA weights are their f16 roundings)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const float p0 = fast_exp2(x[hh][j][0] - m_use), p1 = fast_exp2(x[hh][j][1] - m_use);
+            pb[hh][j] = pack_half2(p0, p1);
+            psum += p0 + p1;
+        }
+        l_run[hh] += psum;
+    }
+#pragma unroll
+    for (int mt = 0; mt < D / 16; ++mt)
+#pragma unroll
+        for (int ks = 0; ks < 2; ++ks) {
+            uint32_t a0, a1, a2, a3;
+            ldsm_x4_trans(sec_addr<SWZ, G::kPadRow>(vb, 16 * ks + (lane & 7) + 8 * (lane >> 4),
+                                                    (16 * mt + 8 * ((lane >> 3) & 1)) * 2),
+                          a0, a1, a2, a3);
+            mma_16816(oacc[0][mt], a0, a1, a2, a3, pb[0][2 * ks], pb[0][2 * ks + 1]);
+            mma_16816(oacc[1][mt], a0, a1, a2, a3, pb[1][2 * ks], pb[1][2 * ks + 1]);
+        }
+}
+
 // The consumer warps of the multi-query kernel: the same ring and unit walk as the
 // single-query consumers (partial row of (token t, head h) = t * n_head + h).  Up to 16 query
 // rows per KV head, each warp attends to its 16 cells of every tile for all rows and the
@@ -720,8 +812,38 @@ __device__ __forceinline__ void mq_consumers(const SplitDecodeParams& p, uint64_
                 }
             };
             if (rsplit) {
-                half(0);
-                half(1);
+                // the whole tile: zero the V rows of masked cells that came with the box (every
+                // warp writes the same zeros, each before its own reads), then one 32-cell pass
+                const uint32_t mask = tile_mask[st];
+                if (mask != 0u) {
+                    const int64_t p0 = x.i0 + (int64_t)t * kTileCells;
+                    int lim[2];
+#pragma unroll
+                    for (int hh = 0; hh < 2; ++hh) {
+                        const int64_t rel = lim_row[hh] - p0;
+                        lim[hh] = rel < 0 ? 0 : (rel > kTileCells ? kTileCells : (int)rel);
+                    }
+                    const uint32_t kb = smem_addr(stage);
+                    if (swz) {
+                        if (mask != 0xffffffffu) {
+                            if (!((mask >> lane) & 1u)) {
+#pragma unroll
+                                for (int pl = 0; pl < G::kPlanes; ++pl) {
+                                    uint4* z = reinterpret_cast<uint4*>(stage + G::kSwzSection + pl * kPlaneBytes +
+                                                                        lane * 128);
+#pragma unroll
+                                    for (int k = 0; k < 8; ++k) z[k] = make_uint4(0, 0, 0, 0);
+                                }
+                                fence_proxy_async();
+                            }
+                            __syncwarp();
+                        }
+                        mq_tile32<true>(kb, kb + G::kSwzSection, mask, lane, lim, qa, oacc, m_run, l_run, p.scale_log2);
+                    } else {
+                        mq_tile32<false>(kb, kb + G::kPadSection, mask, lane, lim, qa, oacc, m_run, l_run,
+                                         p.scale_log2);
+                    }
+                }
             } else {
                 half(warp);
             }
