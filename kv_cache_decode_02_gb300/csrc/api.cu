@@ -60,17 +60,19 @@ int sm_count() {
 
 // Resident CTAs per SM of the split-decode kernel for (kv_type, head_dim, n_stages,
 // multi-query kernel).
-int occupancy(int kv_type, int head_dim, int n_stages, bool mq = false) {
+// mode: the launch's resources (0 single-query, 1 multi-query kernels, 3 the three-consumer
+// multi-query kernel).
+int occupancy(int kv_type, int head_dim, int n_stages, int mode = 0) {
     static std::mutex mu;
-    static int cache[kMaxDevices][4][2][2][16];
-    static bool have[kMaxDevices][4][2][2][16];
+    static int cache[kMaxDevices][4][2][5][16];
+    static bool have[kMaxDevices][4][2][5][16];
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return 1;
-    const int d = dev % kMaxDevices, t = kv_type, h = head_dim == 256 ? 1 : 0, m = mq ? 1 : 0;
+    const int d = dev % kMaxDevices, t = kv_type, h = head_dim == 256 ? 1 : 0, m = mode < 0 || mode > 4 ? 0 : mode;
     std::lock_guard<std::mutex> lock(mu);
     if (!have[d][t][h][m][n_stages]) {
         int blocks = 0;
-        if (split_decode_occupancy(kv_type, head_dim, n_stages, mq, &blocks) != cudaSuccess) blocks = 0;
+        if (split_decode_occupancy(kv_type, head_dim, n_stages, mode, &blocks) != cudaSuccess) blocks = 0;
         cache[d][t][h][m][n_stages] = blocks;
         have[d][t][h][m][n_stages] = true;
     }
@@ -82,7 +84,7 @@ int occupancy(int kv_type, int head_dim, int n_stages, bool mq = false) {
 // (up to the number of work units), then the deepest ring (at most 4 stages) that keeps that
 // many resident.  Deeper rings measured slower on GB300 for the multi-wave Q8_0 and plan
 // workloads (111 vs 91 us at 8 vs 4 stages for Q8_0 over 131072 cells).
-int pick_stages(int kv_type, int head_dim, int64_t n_units, bool mq = false) {
+int pick_stages(int kv_type, int head_dim, int64_t n_units, int mq = 0) {
     const int forced = env_int("KVATTN_STAGES", 0);
     const int max_st = split_decode_max_stages();
     const int limit = split_decode_max_smem();
@@ -118,7 +120,7 @@ cudaError_t launch_decode_units(SplitDecodeParams p, int kv_type, int head_dim, 
     const int64_t n_units = (int64_t)p.n_seq * unit_splits * p.n_head_kv * (p.n_rg > 1 ? p.n_rg : 1);
     if (n_units > (int64_t)INT32_MAX) return cudaErrorInvalidValue;  // units are numbered in 32 bits
     const int64_t resident =
-        (int64_t)std::max(occupancy(kv_type, head_dim, p.n_stages, p.mq == 1), 1) * sm_count();
+        (int64_t)std::max(occupancy(kv_type, head_dim, p.n_stages, p.mq == 2 ? 0 : p.mq), 1) * sm_count();
     const int64_t grid = std::min(n_units, resident);
     if (grid < 1) return cudaSuccess;
     return launch_split_decode(p, kv_type, head_dim, (unsigned)grid, stream, pdl);
@@ -388,7 +390,18 @@ int decode_impl(const void* q, const void* k_cache, const void* v_cache, const v
     const int mq_rows = (n_head_kv >= 1 && n_head >= n_head_kv) ? (n_head / n_head_kv) * n_q : 0;
     // (f16 head_dim 128 in groups of 16 instead, each group a cell-split unit: 33.4 against
     // 29.3 us for 32 rows, 49.8 against 41.6 us for 64, on a 16384-cell 8-KV-head layer)
-    const int rg_rows = kv_type == KVATTN_KV_F16 ? (head_dim == 256 ? 16 : 32) : (head_dim == 256 ? 8 : 16);
+    // f16 head_dim 128 with 33 to 48 rows: one unit whose three consumer warps take 16 rows
+    // each, so every tile is read once for all the rows instead of once per row group of 32
+    // (four GQA-6 sequences through a plan verifying 8 tokens, 48 rows: 276 -> 202 us).  Four
+    // consumer warps for 49 to 64 rows measured slower than two row groups (39.4 against
+    // 37.9 us on a 16384-cell layer), which keep that range.
+    const int mq_wide = (multi && kv_type == KVATTN_KV_F16 && head_dim == 128 && mq_rows > 32 && mq_rows <= 48 &&
+                         env_int("KVATTN_MQ_WIDE", 1) != 0)
+                            ? 3
+                            : 0;
+    const int rg_rows = mq_wide ? 16 * mq_wide
+                        : kv_type == KVATTN_KV_F16 ? (head_dim == 256 ? 16 : 32)
+                                                   : (head_dim == 256 ? 8 : 16);
     const int n_rg = (multi && mq_rows > rg_rows) ? (mq_rows + rg_rows - 1) / rg_rows : 1;
     if (split == 0 && merge) {  // kvattn_decode picks the split (partials need it fixed)
         if (!valid_kv_type(kv_type)) return KVATTN_ERR_INVALID_ARG;
@@ -499,7 +512,7 @@ int decode_impl(const void* q, const void* k_cache, const void* v_cache, const v
         // (one 8-row output tile instead of two; the quantised head_dim-256 multi-query kernels
         // are of that form already)
         const bool mq8 = multi && mq_rows <= 8 && (kv_type == KVATTN_KV_F16 || head_dim == 128);
-        p.mq = multi ? (mq8 ? 2 : 1) : 0;
+        p.mq = multi ? (mq_wide ? mq_wide : mq8 ? 2 : 1) : 0;
         p.n_rg = n_rg;
         p.rg_rows = rg_rows;
         // Quantised head_dim-128 caches with at most four query heads per KV head and an even
@@ -518,7 +531,7 @@ int decode_impl(const void* q, const void* k_cache, const void* v_cache, const v
         p.pair = pair ? 1 : 0;
         p.n_head_kv = k_hkv;
         p.group = (n_head / n_head_kv) * (pair ? 2 : 1);
-        p.n_stages = pick_stages(kv_type, k_hd, n_split * k_hkv * n_rg * n_seq, p.mq == 1);
+        p.n_stages = pick_stages(kv_type, k_hd, n_split * k_hkv * n_rg * n_seq, p.mq == 2 ? 0 : p.mq);
         p.scale_log2 = (float)((double)scale * 1.4426950408889634074);
         apply_debug_hooks(p);
         set_kv_maps(p, kv_type, cell_plan != nullptr ? n_cells : n_cells * (int64_t)n_seq, k_hkv, k_hd);
@@ -526,7 +539,8 @@ int decode_impl(const void* q, const void* k_cache, const void* v_cache, const v
         if (e != cudaSuccess) return KVATTN_ERR_CUDA;
         if (log_on()) {
             const int64_t units = (int64_t)n_seq * n_split * k_hkv * n_rg;
-            const int64_t resident = (int64_t)std::max(occupancy(kv_type, k_hd, p.n_stages, p.mq == 1), 1) * sm_count();
+            const int64_t resident =
+                (int64_t)std::max(occupancy(kv_type, k_hd, p.n_stages, p.mq == 2 ? 0 : p.mq), 1) * sm_count();
             log_line("%s kv_type=%d n_seq=%d n_q=%d n_head=%d/%d head_dim=%d max_len=%lld split=%d n_split=%lld "
                      "plan=%d descriptors=%s units=%lld grid=%lld stages=%d tma=%d scale_tma=%d head_pairs=%d merge=%d",
                      multi ? "decode_multi" : (merge ? "decode" : "decode_partials"), kv_type, n_seq, n_q, n_head,

@@ -1109,7 +1109,9 @@ __device__ __forceinline__ void mq_consumers_rows8(const SplitDecodeParams& p, u
 // MQ8: multi-query units of up to 8 query rows on the single-query consumers (row r = 8 rg +
 // gq of the unit's KV head, token r / G, head g G + r % G; each lane's cells cut at its row's
 // causal limit), for small verification batches.
-template <int KVT, int D, bool MQ = false, bool MQ8 = false>
+// NCW: consumer warps (warp NCW produces).  Two, except the multi-query kernel for 33 to 48
+// rows per KV head at head_dim 128, whose three consumer warps take 16 rows each.
+template <int KVT, int D, bool MQ = false, bool MQ8 = false, int NCW = kConsumerWarps>
 __device__ __forceinline__ void split_decode_body(const SplitDecodeParams& p) {
     static_assert(KVT == KVATTN_KV_F16, "Q8_0 runs in q8_self_body");
     static_assert(!MQ || D == 128 || D == 256, "multi-query decode: head_dim 128 or 256");
@@ -1137,7 +1139,7 @@ __device__ __forceinline__ void split_decode_body(const SplitDecodeParams& p) {
     if (threadIdx.x == 0) {
         for (int i = 0; i < n_stages; ++i) {
             mbar_init(smem_addr(&full_bar[i]), p.src_lsu ? 64 : G::kArrivals);
-            mbar_init(smem_addr(&empty_bar[i]), kConsumerWarps * 32);
+            mbar_init(smem_addr(&empty_bar[i]), NCW * 32);
         }
         mbar_init(smem_addr(&xchg_bar[0]), 32);
         mbar_init(smem_addr(&xchg_bar[1]), 32);
@@ -1155,7 +1157,7 @@ __device__ __forceinline__ void split_decode_body(const SplitDecodeParams& p) {
     // tiles would wait long enough behind the tail to be evicted from L2.
     const bool one_wave = (int64_t)gridDim.x >= n_units;
     if (one_wave) pdl_launch_dependents();
-    if (one_wave && warp == kConsumerWarps && lane == 0 && p.use_tma && p.plan == nullptr && !p.src_lsu &&
+    if (one_wave && warp == NCW && lane == 0 && p.use_tma && p.plan == nullptr && !p.src_lsu &&
         (int64_t)blockIdx.x < n_units) {
         // The lengths read here may still change before the dependency wait below; they
         // only steer these hints, never the loads (boxes outside the cache are not fetched).
@@ -1182,7 +1184,7 @@ __device__ __forceinline__ void split_decode_body(const SplitDecodeParams& p) {
     const int tq = lane & 3;
     const int H = p.n_head;
 
-    if (warp == kConsumerWarps) {
+    if (warp == NCW) {
         // ------------------------------- producer -------------------------------
         const int64_t Hk = p.n_head_kv;
         bool bad = false, stop = false;
@@ -2967,6 +2969,10 @@ __global__ void __launch_bounds__(kThreads) split_decode_mq_f16_d128(const __gri
     split_decode_body<KVATTN_KV_F16, 128, true>(p);
 }
 // Up to 8 query rows per unit on the single-query geometry (small verification batches).
+// 33 to 48 query rows per KV head: three consumer warps of 16 rows read each tile once.
+__global__ void __launch_bounds__(4 * 32, 3) split_decode_mq3_f16_d128(const __grid_constant__ SplitDecodeParams p) {
+    split_decode_body<KVATTN_KV_F16, 128, true, false, 3>(p);
+}
 __global__ void __launch_bounds__(kThreads) split_decode_mq8_f16_d128(const __grid_constant__ SplitDecodeParams p) {
     split_decode_body<KVATTN_KV_F16, 128, false, true>(p);
 }
@@ -3046,6 +3052,7 @@ __global__ void __launch_bounds__(kQ8W256 * 32, kQ8B256)
 // mode: 0 single-query, 1 multi-query, 2 f16 multi-query of up to 8 rows per unit on the
 // single-query geometry (same resources as mode 0).
 const void* kernel_for(int kv_type, int head_dim, int mode = 0) {
+    if (mode == 3) return reinterpret_cast<const void*>(split_decode_mq3_f16_d128);
     if (mode == 2) {
         if (kv_type == KVATTN_KV_Q8_0) return reinterpret_cast<const void*>(split_decode_mq8_q8_d128);
         if (kv_type == KVATTN_KV_Q8_0_Q4_0) return reinterpret_cast<const void*>(split_decode_mq8_q8q4_d128);
@@ -3097,8 +3104,9 @@ int split_decode_stage_bytes(int kv_type, int head_dim) {
 // Dynamic shared memory of one CTA: header, slack for aligning the ring to 1024 bytes,
 // the end-of-unit exchange area and the stage ring.
 // Q8_0 kernels have a fixed geometry (n_stages is ignored for them).
-int split_decode_smem_bytes(int kv_type, int head_dim, int n_stages, bool mq) {
+int split_decode_smem_bytes(int kv_type, int head_dim, int n_stages, int mode) {
     // (the head_dim-256 multi-query kernels run on the single-query geometry)
+    const bool mq = mode == 1 || mode == 3;
     const bool mq128 = mq && head_dim == 128;
     if (kv_type == KVATTN_KV_Q8_0 && mq128) return q8_self_smem<128, kQ8WMQ, kQ8SMQ, false, false, true>();
     if (kv_type == KVATTN_KV_Q8_0_Q4_0 && mq128) return q8_self_smem<128, kQ8WMQ, kQ8SMQ, true, false, true>();
@@ -3117,7 +3125,9 @@ int split_decode_smem_bytes(int kv_type, int head_dim, int n_stages, bool mq) {
     return kHeaderBytes + 1024 + xchg + n_stages * split_decode_stage_bytes(kv_type, head_dim);
 }
 
-int split_decode_block_threads(int kv_type, int head_dim, bool mq) {
+int split_decode_block_threads(int kv_type, int head_dim, int mode) {
+    const bool mq = mode == 1;
+    if (mode == 3) return 4 * 32;
     if (kv_type != KVATTN_KV_F16 && mq && head_dim == 128) return kQ8WMQ * 32;
     if (kv_type != KVATTN_KV_F16) return (head_dim == 128 ? kQ8W128 : kQ8W256) * 32;
     return kThreads;
@@ -3128,31 +3138,30 @@ int split_decode_box_cells(int kv_type) { return kv_type == KVATTN_KV_F16 ? kTil
 int split_decode_max_stages() { return kMaxStages; }
 int split_decode_threads() { return kThreads; }
 
-cudaError_t split_decode_occupancy(int kv_type, int head_dim, int n_stages, bool mq, int* blocks) {
-    const void* fn = kernel_for(kv_type, head_dim, mq ? 1 : 0);
+cudaError_t split_decode_occupancy(int kv_type, int head_dim, int n_stages, int mode, int* blocks) {
+    const void* fn = kernel_for(kv_type, head_dim, mode);
     cudaError_t err = set_smem_attr(fn);
     if (err != cudaSuccess) return err;
-    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks, fn, split_decode_block_threads(kv_type, head_dim, mq),
-                                                         split_decode_smem_bytes(kv_type, head_dim, n_stages, mq));
+    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks, fn, split_decode_block_threads(kv_type, head_dim, mode),
+                                                         split_decode_smem_bytes(kv_type, head_dim, n_stages, mode));
 }
 
 cudaError_t launch_split_decode(const SplitDecodeParams& p, int kv_type, int head_dim, unsigned grid_ctas,
                                 cudaStream_t stream, bool pdl) {
-    const bool mq = p.mq == 1;  // (mode 2 has the single-query resources)
+    const int res = p.mq == 2 ? 0 : p.mq;  // resources (mode 2 has the single-query ones)
     const void* fn = kernel_for(kv_type, head_dim, p.mq);
-    static std::once_flag once[64][24];
-    static cudaError_t attr_err[64][24];
+    static std::once_flag once[64][40];
+    static cudaError_t attr_err[64][40];
     int dev = 0;
     cudaError_t err = cudaGetDevice(&dev);
     if (err != cudaSuccess) return err;
-    const int which = p.mq == 2 ? 16 + 2 * kv_type + (head_dim == 256 ? 1 : 0)
-                                : (mq ? 8 : 0) + 2 * kv_type + (head_dim == 256 ? 1 : 0);
+    const int which = 8 * p.mq + 2 * kv_type + (head_dim == 256 ? 1 : 0);
     std::call_once(once[dev & 63][which], [&] { attr_err[dev & 63][which] = set_smem_attr(fn); });
     if (attr_err[dev & 63][which] != cudaSuccess) return attr_err[dev & 63][which];
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid_ctas, 1, 1);
-    cfg.blockDim = dim3((unsigned)split_decode_block_threads(kv_type, head_dim, mq), 1, 1);
-    cfg.dynamicSmemBytes = split_decode_smem_bytes(kv_type, head_dim, p.n_stages, mq);
+    cfg.blockDim = dim3((unsigned)split_decode_block_threads(kv_type, head_dim, res), 1, 1);
+    cfg.dynamicSmemBytes = split_decode_smem_bytes(kv_type, head_dim, p.n_stages, res);
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;

@@ -138,13 +138,15 @@ cudaError_t launch_merge(const MergeParams& p, cudaStream_t stream, bool pdl);
 cudaError_t launch_tile_copy(const void* k_src, const void* v_src, void* k_dst, void* v_dst, size_t bytes,
                              cudaStream_t stream);
 int split_decode_stage_bytes(int kv_type, int head_dim);
-int split_decode_smem_bytes(int kv_type, int head_dim, int n_stages, bool mq = false);
-int split_decode_block_threads(int kv_type, int head_dim, bool mq = false);
+// mode: 0 single-query, 1 multi-query kernels, 3 the three-consumer multi-query kernel (the
+// multi-query units of up to 8 rows, mode 2, use the single-query resources)
+int split_decode_smem_bytes(int kv_type, int head_dim, int n_stages, int mode = 0);
+int split_decode_block_threads(int kv_type, int head_dim, int mode = 0);
 int split_decode_box_cells(int kv_type);
 int split_decode_max_stages();
 int split_decode_max_smem();
 int split_decode_threads();
-cudaError_t split_decode_occupancy(int kv_type, int head_dim, int n_stages, bool mq, int* blocks);
+cudaError_t split_decode_occupancy(int kv_type, int head_dim, int n_stages, int mode, int* blocks);
 cudaError_t launch_descriptors(const int32_t* plan, int64_t plan_stride, const int32_t* seq_lens,
                                int n_seq, int64_t max_len, int split, int64_t n_cells,
                                int64_t n_split, int4* desc, uint32_t* status,

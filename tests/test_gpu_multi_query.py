@@ -314,15 +314,16 @@ def test_multi_query_quantised_one_token_equals_single_query(kvattn, kind, D):
     assert np.max(np.abs(ml.cpu().numpy()[:, 0] - sl.cpu().numpy())) <= 1e-5
 
 
-@pytest.mark.parametrize("kind", ["f16", "f16_d256", "q8", "f16_8rows"])
+@pytest.mark.parametrize("kind", ["f16", "f16_d256", "q8", "f16_8rows", "f16_48rows"])
 def test_multi_query_bounded_wait_reports_timeout_and_context_survives(kvattn, monkeypatch, kind):
     """The multi-query kernels' pipeline waits are bounded: a first tile that expects bytes
     no copy delivers (host test switch) ends in the timeout status bit, and the next call is
-    clean.  (f16_8rows: 8 query rows per KV head, the single-query kernels' multi-query mode.)"""
+    clean.  (f16_8rows: 8 query rows per KV head, the single-query kernels' multi-query mode;
+    f16_48rows: 48 rows, the kernel with three consumer warps.)"""
     import torch
     rng = np.random.default_rng(23)
     S, N, H, Hk = 1, 600, 16, 4
-    n_q = 2 if kind == "f16_8rows" else 4
+    n_q = {"f16_8rows": 2, "f16_48rows": 12}.get(kind, 4)
     D = 256 if kind == "f16_d256" else 128
     q = rand_f16(rng, (S, n_q, H, D))
     if kind.startswith("f16"):
