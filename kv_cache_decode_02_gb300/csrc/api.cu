@@ -11,6 +11,7 @@
 #include <mutex>
 #include <thread>
 
+#include "decode_tc.cuh"
 #include "kvattn_internal.cuh"
 
 using namespace kvattn;
@@ -119,6 +120,13 @@ cudaError_t launch_decode_units(SplitDecodeParams p, int kv_type, int head_dim, 
     p.unit_splits = unit_splits;
     const int64_t n_units = (int64_t)p.n_seq * unit_splits * p.n_head_kv * (p.n_rg > 1 ? p.n_rg : 1);
     if (n_units > (int64_t)INT32_MAX) return cudaErrorInvalidValue;  // units are numbered in 32 bits
+    if (p.mq == 5) {  // the tcgen05 multi-query kernel
+        int blocks = 0;
+        if (split_decode_tc_occupancy(&blocks) != cudaSuccess) blocks = 1;
+        const int64_t grid = std::min(n_units, (int64_t)std::max(blocks, 1) * sm_count());
+        if (grid < 1) return cudaSuccess;
+        return launch_split_decode_tc(p, (unsigned)grid, stream, pdl);
+    }
     const int64_t resident =
         (int64_t)std::max(occupancy(kv_type, head_dim, p.n_stages, p.mq == 2 ? 0 : p.mq), 1) * sm_count();
     const int64_t grid = std::min(n_units, resident);
@@ -395,11 +403,18 @@ int decode_impl(const void* q, const void* k_cache, const void* v_cache, const v
     // (four GQA-6 sequences through a plan verifying 8 tokens, 48 rows: 276 -> 202 us).  Four
     // consumer warps for 49 to 64 rows measured slower than two row groups (39.4 against
     // 37.9 us on a 16384-cell layer), which keep that range.
-    const int mq_wide = (multi && kv_type == KVATTN_KV_F16 && head_dim == 128 && mq_rows > 32 && mq_rows <= 48 &&
-                         env_int("KVATTN_MQ_WIDE", 1) != 0)
+    // f16 head_dim 128 with more than 32 rows: the tcgen05 kernel, every row of a KV head in
+    // one unit (rows in TMEM lanes, S and O accumulated in tensor memory).  Measured on the
+    // Qwen3-8B-shaped layer (16384 cells, split 256): 48 rows 33.5 -> 25.2 us, 64 rows 38.0 ->
+    // 26.7 us, the four-sequence GQA-6 plan verifying 8 tokens 202 -> 147 us; at 20 to 32 rows
+    // the mma.sync kernels stay ahead (21.3 against 22.8 us at 32).
+    const bool mq_tc = multi && kv_type == KVATTN_KV_F16 && head_dim == 128 && mq_rows > 32 &&
+                       mq_rows <= kTcMaxRows && aligned(q, 16) && env_int("KVATTN_TC", 1) != 0;
+    const int mq_wide = (!mq_tc && multi && kv_type == KVATTN_KV_F16 && head_dim == 128 && mq_rows > 32 &&
+                         mq_rows <= 48 && env_int("KVATTN_MQ_WIDE", 1) != 0)
                             ? 3
                             : 0;
-    const int rg_rows = mq_wide ? 16 * mq_wide
+    const int rg_rows = mq_tc ? kTcMaxRows : mq_wide ? 16 * mq_wide
                         : kv_type == KVATTN_KV_F16 ? (head_dim == 256 ? 16 : 32)
                                                    : (head_dim == 256 ? 8 : 16);
     const int n_rg = (multi && mq_rows > rg_rows) ? (mq_rows + rg_rows - 1) / rg_rows : 1;
@@ -512,7 +527,7 @@ int decode_impl(const void* q, const void* k_cache, const void* v_cache, const v
         // (one 8-row output tile instead of two; the quantised head_dim-256 multi-query kernels
         // are of that form already)
         const bool mq8 = multi && mq_rows <= 8 && (kv_type == KVATTN_KV_F16 || head_dim == 128);
-        p.mq = multi ? (mq_wide ? mq_wide : mq8 ? 2 : 1) : 0;
+        p.mq = multi ? (mq_tc ? 5 : mq_wide ? mq_wide : mq8 ? 2 : 1) : 0;
         p.n_rg = n_rg;
         p.rg_rows = rg_rows;
         // Quantised head_dim-128 caches with at most four query heads per KV head and an even
@@ -531,7 +546,7 @@ int decode_impl(const void* q, const void* k_cache, const void* v_cache, const v
         p.pair = pair ? 1 : 0;
         p.n_head_kv = k_hkv;
         p.group = (n_head / n_head_kv) * (pair ? 2 : 1);
-        p.n_stages = pick_stages(kv_type, k_hd, n_split * k_hkv * n_rg * n_seq, p.mq == 2 ? 0 : p.mq);
+        p.n_stages = p.mq == 5 ? 4 : pick_stages(kv_type, k_hd, n_split * k_hkv * n_rg * n_seq, p.mq == 2 ? 0 : p.mq);
         p.scale_log2 = (float)((double)scale * 1.4426950408889634074);
         apply_debug_hooks(p);
         set_kv_maps(p, kv_type, cell_plan != nullptr ? n_cells : n_cells * (int64_t)n_seq, k_hkv, k_hd);
@@ -539,8 +554,11 @@ int decode_impl(const void* q, const void* k_cache, const void* v_cache, const v
         if (e != cudaSuccess) return KVATTN_ERR_CUDA;
         if (log_on()) {
             const int64_t units = (int64_t)n_seq * n_split * k_hkv * n_rg;
+            int tc_blocks = 0;
+            if (p.mq == 5 && split_decode_tc_occupancy(&tc_blocks) != cudaSuccess) tc_blocks = 1;
             const int64_t resident =
-                (int64_t)std::max(occupancy(kv_type, k_hd, p.n_stages, p.mq == 2 ? 0 : p.mq), 1) * sm_count();
+                (int64_t)std::max(p.mq == 5 ? tc_blocks : occupancy(kv_type, k_hd, p.n_stages, p.mq == 2 ? 0 : p.mq), 1) *
+                sm_count();
             log_line("%s kv_type=%d n_seq=%d n_q=%d n_head=%d/%d head_dim=%d max_len=%lld split=%d n_split=%lld "
                      "plan=%d descriptors=%s units=%lld grid=%lld stages=%d tma=%d scale_tma=%d head_pairs=%d merge=%d",
                      multi ? "decode_multi" : (merge ? "decode" : "decode_partials"), kv_type, n_seq, n_q, n_head,

@@ -170,7 +170,7 @@ def test_window_tail_direct_validation(kvattn):
     assert f(*bad) == -1
 
 
-def test_multi_query_limits(kvattn):
+def test_multi_query_limits(kvattn, monkeypatch):
     """Checked on the host before any device work."""
     def call(**over):
         a = dict(q=A, k=B, v=C, ks=None, vs=None, kv_type=0, n_cells=1024, plan=None, plan_stride=0,
@@ -184,10 +184,15 @@ def test_multi_query_limits(kvattn):
     assert call(head_dim=64) == kvattn.KVATTN_ERR_UNSUPPORTED
     assert call(kv_type=1, ks=A, vs=A, n_q=17) == kvattn.KVATTN_ERR_UNSUPPORTED  # Q8_0: 68 rows > 64
     assert call(kv_type=3, ks=A, vs=A, n_q=17) == kvattn.KVATTN_ERR_UNSUPPORTED  # Q4_0: 68 rows > 64
-    # 100000 sequences x 2048 splits x 8 KV heads fit 32 bits, x 2 row groups (64 rows) do not
+    # 100000 sequences x 2048 splits x 8 KV heads fit 32 bits, x 4 row groups (64 rows of a
+    # Q8_0 cache, 16 a group) do not; f16 head_dim 128 takes 64 rows in one tcgen05 unit
     big = dict(n_seq=100000, max_len=65536, n_cells=65536, split=32)
-    assert call(n_q=16, **big) == kvattn.KVATTN_ERR_UNSUPPORTED
+    assert call(n_q=16, kv_type=1, ks=A, vs=A, **big) == kvattn.KVATTN_ERR_UNSUPPORTED
+    assert call(n_q=16, **big) == kvattn.KVATTN_ERR_WORKSPACE                 # one unit: only the workspace
     assert call(n_q=8, **big) == kvattn.KVATTN_ERR_WORKSPACE                  # one group: only the workspace
+    monkeypatch.setenv("KVATTN_TC", "0")                                     # the mma.sync row groups (2 x 32)
+    assert call(n_q=16, **big) == kvattn.KVATTN_ERR_UNSUPPORTED
+    monkeypatch.delenv("KVATTN_TC")
     assert call(kv_type=1) == kvattn.KVATTN_ERR_INVALID_ARG                   # Q8_0 without scales
     assert call(n_q=0) == kvattn.KVATTN_ERR_INVALID_ARG
     assert call(q=None) == kvattn.KVATTN_ERR_INVALID_ARG
