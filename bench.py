@@ -338,7 +338,7 @@ def bench_workloads(K, torch, stream, peak):
             inputs.normal_f16_torch((3000 + w.number, l), (w.n_cells, w.n_head_kv, w.head_dim), "cuda"))
            for l in range(n_buf)]
     lens = torch.tensor(w.seq_lens, dtype=torch.int32, device="cuda")
-    for n_q in (4, 8):
+    for n_q in (4, 8, 16):  # 16, 32 and 64 query rows per KV head (64: the tcgen05 kernel)
         qm = torch.randn((1, n_q, w.n_head, w.head_dim), device="cuda").half()
         wsm = torch.zeros(K.kvattn_decode_multi_workspace_bytes(1, n_q, w.n_head, w.head_dim, w.n_cells, w.split),
                           dtype=torch.uint8, device="cuda")
@@ -375,9 +375,8 @@ def bench_workloads(K, torch, stream, peak):
     valid = int((plan >= 0).sum())
     add(w.name, valid * w.n_head_kv * w.head_dim * 4, timed(fn), {"valid_cells": valid,
                                                                  "plan_entries": int(plens.sum())})
-    # the same slots verifying 8 draft tokens each: 48 query rows per KV head (two row groups);
-    # split 512 (the partials of 8 tokens x 48 heads per split make split 128 cost 394 us
-    # against 311 us at 256 or 512)
+    # the same slots verifying 8 draft tokens each: 48 query rows per KV head (the tcgen05
+    # kernel, every row of a KV head in one unit); split 512 (147 us against 157 us at 256)
     n_q, vsplit = 8, 512
     qm = inputs.normal_f16_torch((1000 + w.number, 8), (w.n_seq, n_q, w.n_head, w.head_dim), "cuda")
     wsm = torch.zeros(K.kvattn_decode_multi_workspace_bytes(w.n_seq, n_q, w.n_head, w.head_dim, plan.shape[1],
@@ -1025,7 +1024,7 @@ def window_tail_inputs(torch, inputs, n_tail=None):
 
 def profile_verify(args):
     """--kernel-reps calls of causal multi-query decode on the Qwen3-8B-shaped layer (16384
-    cells, 32/8 heads, split 256) verifying 4 or 8 draft tokens, for profilers."""
+    cells, 32/8 heads, split 256) verifying 4, 8 or 16 draft tokens, for profilers."""
     import torch
     from kv_cache_decode_02_gb300 import inputs
     from kv_cache_decode_02_gb300 import kvattn as K
@@ -1150,7 +1149,7 @@ def main():
                                                    "q4_0_n131072_d256", "window_tail_n524288",
                                                    "window_tail_n524288_direct", "window_tail_n81920",
                                                    "window_tail_n81920_direct", "qwen3_8b_layer_verify_nq4",
-                                                   "qwen3_8b_layer_verify_nq8"],
+                                                   "qwen3_8b_layer_verify_nq8", "qwen3_8b_layer_verify_nq16"],
                     help="only launch this workload's split decode (window + tail: the whole op) "
                          "--kernel-reps times (for ncu)")
     args = ap.parse_args()
