@@ -225,18 +225,20 @@ size_t kvattn_decode_multi_workspace_bytes(int n_seq, int n_q, int n_head, int h
  * counts them, token t sits at logical position L - n_q + t and attends to the logical
  * positions 0 .. L - n_q + t (plan entries or cells, -1 holes masked); a token whose window
  * is empty gets O = 0, LSE = -inf.  The G x n_q query rows of each KV head share every K/V
- * byte read from HBM (one or two 16-row MMA tiles, up to 32 rows).  n_q = 1 is exactly
- * kvattn_decode (and runs its kernels); up to 8 rows per KV head (f16, and the quantised
- * types at head_dim 128) run on the single-query kernels with per-row causal masks.
+ * byte read from HBM (one or two 16-row MMA tiles, up to 32 rows; f16 at head_dim 128 with
+ * 33 to 128 rows and q 16-byte aligned: one tcgen05 tile of all the rows).  n_q = 1 is
+ * exactly kvattn_decode (and runs its kernels); up to 8 rows per KV head (f16, and the
+ * quantised types at head_dim 128) run on the single-query kernels with per-row causal
+ * masks.
  *  q        device half [n_seq][n_q][n_head][head_dim].
  *  out, lse device float [n_seq][n_q][n_head][head_dim], [n_seq][n_q][n_head].
  *  Other arguments: as kvattn_decode.
- *  Limits (UNSUPPORTED otherwise): n_q >= 1 and (n_head / n_head_kv) * n_q <= 64 query
- *  rows per KV head (n_q <= 8 at up to 8 query heads per KV head); any kv_type; head_dim
- *  128 or 256.  Rows beyond one unit's share (f16: 32 at head_dim 128, 16 at 256; the
- *  quantised types: 16 at head_dim 128, 8 at 256) run as row groups, units of their own
- *  that read the split's K/V again, mostly from L2 (the groups of a split run side by
- *  side).
+ *  Limits (UNSUPPORTED otherwise): n_q >= 1 and (n_head / n_head_kv) * n_q <= 128 query
+ *  rows per KV head (n_q <= 16 at up to 8 query heads per KV head); any kv_type; head_dim
+ *  128 or 256.  Rows beyond one unit's share (f16: 32 at head_dim 128 when the tcgen05
+ *  tile does not serve them, 16 at 256; the quantised types: 16 at head_dim 128, 8 at 256)
+ *  run as row groups, units of their own that read the split's K/V again, mostly from L2
+ *  (the groups of a split run side by side).
  *  ws: kvattn_decode_multi_workspace_bytes(...) bytes.
  * Errors: as kvattn_decode.
  */

@@ -403,8 +403,8 @@ int decode_impl(const void* q, const void* k_cache, const void* v_cache, const v
     // (four GQA-6 sequences through a plan verifying 8 tokens, 48 rows: 276 -> 202 us).  Four
     // consumer warps for 49 to 64 rows measured slower than two row groups (39.4 against
     // 37.9 us on a 16384-cell layer), which keep that range.
-    // f16 head_dim 128 with more than 32 rows: the tcgen05 kernel, every row of a KV head in
-    // one unit (rows in TMEM lanes, S and O accumulated in tensor memory).  Measured on the
+    // f16 head_dim 128 with more than 32 rows (to 128): the tcgen05 kernel, every row of a KV
+    // head in one unit (rows in TMEM lanes, S and O accumulated in tensor memory).  Measured on the
     // Qwen3-8B-shaped layer (16384 cells, split 256): 48 rows 33.5 -> 25.2 us, 64 rows 38.0 ->
     // 26.7 us, the four-sequence GQA-6 plan verifying 8 tokens 202 -> 147 us; at 20 to 32 rows
     // the mma.sync kernels stay ahead (21.3 against 22.8 us at 32).
@@ -431,10 +431,11 @@ int decode_impl(const void* q, const void* k_cache, const void* v_cache, const v
     int st = check_shape(shape);
     if (st != KVATTN_OK) return st;
     if (multi && (int64_t)n_seq * n_q * n_head > (int64_t)INT32_MAX) return KVATTN_ERR_UNSUPPORTED;
-    // multi-query: up to 64 query rows per KV head, any cache type, head_dim 128 or 256
+    // multi-query: up to 128 query rows per KV head (16 tokens at 8 query heads per KV head),
+    // any cache type, head_dim 128 or 256
     if (multi) {
         const int rows = mq_rows;
-        const bool ok = valid_kv_type(kv_type) && rows <= 64 && (head_dim == 128 || head_dim == 256);
+        const bool ok = valid_kv_type(kv_type) && rows <= 128 && (head_dim == 128 || head_dim == 256);
         if (!ok) return KVATTN_ERR_UNSUPPORTED;
         if ((int64_t)n_seq * ((max_len + split - 1) / split) * n_head_kv * n_rg > (int64_t)INT32_MAX)
             return KVATTN_ERR_UNSUPPORTED;

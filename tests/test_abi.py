@@ -178,12 +178,14 @@ def test_multi_query_limits(kvattn, monkeypatch):
                  scale=0.0884, out=A + 8192, lse=A + 16384, ws=A + 65536, ws_bytes=1 << 30, stream=None)
         a.update(over)
         return kvattn.lib.kvattn_decode_multi(*a.values())
-    assert call(n_q=17) == kvattn.KVATTN_ERR_UNSUPPORTED           # 4 x 17 = 68 rows > 64
-    assert call(head_dim=256, n_q=17) == kvattn.KVATTN_ERR_UNSUPPORTED  # head_dim 256: 68 rows > 64
-    assert call(head_dim=256, kv_type=1, ks=A, vs=A, n_q=17) == kvattn.KVATTN_ERR_UNSUPPORTED  # 68 rows
+    assert call(n_q=33) == kvattn.KVATTN_ERR_UNSUPPORTED           # 4 x 33 = 132 rows > 128
+    assert call(head_dim=256, n_q=33) == kvattn.KVATTN_ERR_UNSUPPORTED  # head_dim 256: 132 rows > 128
+    assert call(head_dim=256, kv_type=1, ks=A, vs=A, n_q=33) == kvattn.KVATTN_ERR_UNSUPPORTED  # 132 rows
     assert call(head_dim=64) == kvattn.KVATTN_ERR_UNSUPPORTED
-    assert call(kv_type=1, ks=A, vs=A, n_q=17) == kvattn.KVATTN_ERR_UNSUPPORTED  # Q8_0: 68 rows > 64
-    assert call(kv_type=3, ks=A, vs=A, n_q=17) == kvattn.KVATTN_ERR_UNSUPPORTED  # Q4_0: 68 rows > 64
+    assert call(kv_type=1, ks=A, vs=A, n_q=33) == kvattn.KVATTN_ERR_UNSUPPORTED  # Q8_0: 132 rows > 128
+    assert call(kv_type=3, ks=A, vs=A, n_q=33) == kvattn.KVATTN_ERR_UNSUPPORTED  # Q4_0: 132 rows > 128
+    assert call(n_q=17, n_head=64) == kvattn.KVATTN_ERR_UNSUPPORTED  # 8 x 17 = 136 rows > 128
+    assert call(n_q=32, ws_bytes=1000) == kvattn.KVATTN_ERR_WORKSPACE  # 128 rows pass the limits
     # 100000 sequences x 2048 splits x 8 KV heads fit 32 bits, x 4 row groups (64 rows of a
     # Q8_0 cache, 16 a group) do not; f16 head_dim 128 takes 64 rows in one tcgen05 unit
     big = dict(n_seq=100000, max_len=65536, n_cells=65536, split=32)

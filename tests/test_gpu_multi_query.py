@@ -1,7 +1,7 @@
 """GPU parity of causal multi-query decode (kvattn_decode_multi) against the fp64 oracle:
 n_q new tokens per sequence, token t seeing logical positions 0 .. L - n_q + t, the
 G x n_q query rows of a KV head in one 16-row MMA tile (up to 16 rows: the two consumer warps
-split the cells) or two (17 to 32 rows: they split the rows); 33 to 64 rows at f16 head_dim
+split the cells) or two (17 to 32 rows: they split the rows); 33 to 128 rows at f16 head_dim
 128 run on the tcgen05 kernel (its own cases in test_gpu_multi_query_tc.py, which also runs
 the mma.sync row groups that serve them with KVATTN_TC=0); at head_dim 256 each consumer
 warp takes 8 of up to 16 rows."""
@@ -75,6 +75,7 @@ def test_multi_query_contiguous(kvattn, n_q, G, Hk, lens, split):
     (5, 4, 2, [300, 5, 2], 32),         # 20 rows: row groups of 16 and 4
     (8, 4, 2, [777, 8], 128),           # 32 rows (GQA-4 verifying 8 tokens): two row groups
     (8, 8, 1, [500, 3, 0], 64),         # 64 rows: four row groups, short and empty sequences
+    (16, 8, 1, [300, 16, 2], 64),       # 128 rows (16 tokens at GQA-8): eight row groups
 ])
 def test_multi_query_contiguous_d256(kvattn, n_q, G, Hk, lens, split):
     """head_dim 256 (Gemma-family layers): 8 query rows per consumer warp, row groups of 16
@@ -194,6 +195,7 @@ ORACLE = {"q8": oracle.decode_q8_0, "q8k_q4v": oracle.decode_q8_0_q4_0, "q4kv": 
     (5, 4, 2, [300, 5, 2], 32),         # 20 rows: row groups of 16 and 4
     (8, 4, 2, [777, 8, 3], 64),         # 32 rows (GQA-4 verifying 8 tokens): two row groups
     (8, 8, 1, [513, 0], 128),           # 64 rows: four row groups, an empty sequence
+    (16, 8, 1, [400, 16], 64),          # 128 rows: eight row groups
 ])
 def test_multi_query_quantised_contiguous(kvattn, n_q, G, Hk, lens, split, kind):
     """Quantised caches: the self-loading kernels with the whole 16-row M of the MMA, row
@@ -251,6 +253,7 @@ def test_multi_query_quantised_plan_with_holes(kvattn, kind, n_q):
     (3, 5, 2, [2049, 0], 512),          # 15 rows, an empty sequence
     (5, 2, 4, [300], 32),               # 10 rows: groups of 8 and 2
     (8, 8, 1, [500, 3], 64),            # 64 rows: eight groups
+    (16, 8, 1, [260, 7], 64),           # 128 rows: sixteen groups
 ])
 def test_multi_query_quantised_d256(kvattn, n_q, G, Hk, lens, split, kind):
     """head_dim 256 over the quantised caches: 8-row units on the single-query geometry,
@@ -315,16 +318,16 @@ def test_multi_query_quantised_one_token_equals_single_query(kvattn, kind, D):
     assert np.max(np.abs(ml.cpu().numpy()[:, 0] - sl.cpu().numpy())) <= 1e-5
 
 
-@pytest.mark.parametrize("kind", ["f16", "f16_d256", "q8", "f16_8rows", "f16_48rows"])
+@pytest.mark.parametrize("kind", ["f16", "f16_d256", "q8", "f16_8rows", "f16_48rows", "f16_128rows"])
 def test_multi_query_bounded_wait_reports_timeout_and_context_survives(kvattn, monkeypatch, kind):
     """The multi-query kernels' pipeline waits are bounded: a first tile that expects bytes
     no copy delivers (host test switch) ends in the timeout status bit, and the next call is
     clean.  (f16_8rows: 8 query rows per KV head, the single-query kernels' multi-query mode;
-    f16_48rows: 48 rows, the kernel with three consumer warps.)"""
+    f16_48rows and f16_128rows: the tcgen05 kernel with two and four row warps.)"""
     import torch
     rng = np.random.default_rng(23)
     S, N, H, Hk = 1, 600, 16, 4
-    n_q = {"f16_8rows": 2, "f16_48rows": 12}.get(kind, 4)
+    n_q = {"f16_8rows": 2, "f16_48rows": 12, "f16_128rows": 32}.get(kind, 4)
     D = 256 if kind == "f16_d256" else 128
     q = rand_f16(rng, (S, n_q, H, D))
     if kind.startswith("f16"):

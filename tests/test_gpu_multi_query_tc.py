@@ -1,5 +1,5 @@
 """GPU parity of causal multi-query decode on the fifth-generation tensor cores (f16 cache,
-head_dim 128, 33 to 64 query rows per KV head: every row of a KV head in one work unit, S,
+head_dim 128, 33 to 128 query rows per KV head: every row of a KV head in one work unit, S,
 P and O in tensor memory) against the fp64 oracle -- contiguous caches with ragged and
 empty sequences, many work units per CTA, plans whose tiles are whole runs, runs with holes
 and scattered cells over NaN-filled unused cells, the per-split descriptors such a call
@@ -38,6 +38,10 @@ CONTIGUOUS = [
     (10, 5, 3, [777, 301], 96),        # 50 rows, a ragged last tile in every sequence
     (16, 4, 1, [700, 3, 16], 32),      # 64 rows, one KV head
     (8, 8, 2, [9000, 4100], 32),       # 64 rows over 428 splits: several units per CTA
+    (12, 6, 2, [1100, 5], 128),        # 72 rows: three row warps
+    (13, 7, 1, [700, 13, 2], 32),      # 91 rows
+    (16, 8, 1, [900, 10], 64),         # 128 rows (16 tokens at GQA-8): every TMEM lane
+    (16, 8, 2, [5000, 16], 32),        # 128 rows over 314 splits
 ]
 
 
@@ -87,7 +91,7 @@ def plan_cache(kvattn, rng, kind, Hk, D, pool=24, plan_stride=None):
 
 
 @pytest.mark.parametrize("kind", ["runs", "holes", "scattered"])
-@pytest.mark.parametrize("n_q,G", [(8, 6), (16, 4), (12, 3)])
+@pytest.mark.parametrize("n_q,G", [(8, 6), (16, 4), (12, 3), (16, 8)])
 def test_tc_plan(kvattn, kind, n_q, G):
     import torch
     rng = np.random.default_rng([42, n_q, G, ["runs", "holes", "scattered"].index(kind)])
@@ -130,10 +134,10 @@ def test_tc_plan_leaves_the_split_descriptors_in_the_workspace(kvattn):
                                              plan=masked))
 
 
-@pytest.mark.parametrize("n_q,G,Hk,lens,split", [CONTIGUOUS[0], CONTIGUOUS[2], CONTIGUOUS[4]])
+@pytest.mark.parametrize("n_q,G,Hk,lens,split", [CONTIGUOUS[0], CONTIGUOUS[2], CONTIGUOUS[4], CONTIGUOUS[8]])
 def test_mma_path_for_the_same_rows(kvattn, monkeypatch, n_q, G, Hk, lens, split):
     """With the tcgen05 path off the mma.sync kernels (row groups, three consumer warps)
-    serve 33 to 64 rows; both agree with the oracle and with each other to rounding."""
+    serve 33 to 128 rows; both agree with the oracle and with each other to rounding."""
     import torch
     rng = np.random.default_rng([44, n_q, G])
     S, D = len(lens), 128
