@@ -8,7 +8,8 @@
 //    the tile's valid entries are one physical run, otherwise 16-byte cp.async copies of the
 //    valid rows straight into their swizzled places.  Before a tile's P V the first row warp
 //    zeros the V rows of the tile's other cells.
-//  * one thread of another warp issues the MMAs: S = Q K^T (M = 128 rows, N = 32 cells, K = 128
+//  * another warp issues the MMAs (the whole warp walks the schedule and waits, one elected
+//    lane issues with warp-uniform operands): S = Q K^T (M = 128 rows, N = 32 cells, K = 128
 //    dims; A = Q from tensor memory, where the rows put it once per unit, B = K from shared
 //    memory, K-major) into one of two 32-column TMEM buffers, and O += P V (A = P from the
 //    first 16 columns of that buffer, B = V in shared memory with head_dim the contiguous
@@ -41,7 +42,7 @@ namespace {
 constexpr int kTile = 32;                   // cells per stage
 constexpr int kStages = 4;
 constexpr int kWarpBuf = 8192;              // per row warp: query rows in, O rows out
-constexpr int kThreads = 6 * 32;            // warps 0-3: rows; warp 4: producer; warp 5: MMA
+constexpr int kThreads = 6 * 32;            // row warps (up to 4), a producer and an MMA warp
 constexpr int kPlane = kTile * 128;         // one 128-byte-wide plane of a tile (4 KB)
 constexpr int kStageBytes = 4 * kPlane;     // K planes 0, 1 then V planes 0, 1 (16 KB)
 constexpr int kHeader = 1024;
