@@ -340,7 +340,7 @@ def bench_workloads(K, torch, stream, peak):
     lens = torch.tensor(w.seq_lens, dtype=torch.int32, device="cuda")
     for n_q in (4, 8, 16):  # 16, 32 and 64 query rows per KV head (64: the tcgen05 kernel)
         qm = torch.randn((1, n_q, w.n_head, w.head_dim), device="cuda").half()
-        wsm = torch.zeros(K.kvattn_decode_multi_workspace_bytes(1, n_q, w.n_head, w.head_dim, w.n_cells, w.split),
+        wsm = torch.zeros(K.kvattn_decode_multi_workspace_bytes(1, n_q, w.n_head, w.head_dim, w.n_cells, 0),
                           dtype=torch.uint8, device="cuda")
         om = torch.empty((1, n_q, w.n_head, w.head_dim), dtype=torch.float32, device="cuda")
         lm = torch.empty((1, n_q, w.n_head), dtype=torch.float32, device="cuda")
@@ -350,10 +350,10 @@ def bench_workloads(K, torch, stream, peak):
             kb, vb = kvs[it[0] % n_buf]
             it[0] += 1
             K.kvattn_decode_multi(qm, kb, vb, None, None, 0, w.n_cells, None, 0, lens, 1, w.n_cells, n_q, w.n_head,
-                                  w.n_head_kv, w.head_dim, w.split, 1 / math.sqrt(w.head_dim), om, lm, wsm,
+                                  w.n_head_kv, w.head_dim, 0, 1 / math.sqrt(w.head_dim), om, lm, wsm,
                                   wsm.numel(), stream)
         add(f"qwen3_8b_layer_verify_nq{n_q}", w.n_cells * w.n_head_kv * w.head_dim * 4, timed(mq, 40),
-            {"n_q": n_q, "query_rows_per_kv_head": n_q * w.n_head // w.n_head_kv})
+            {"n_q": n_q, "query_rows_per_kv_head": n_q * w.n_head // w.n_head_kv, "split": "automatic"})
     del kvs
 
     # multi-slot GQA-6 through the compact plan (descriptors + decode + merge)

@@ -422,9 +422,18 @@ int decode_impl(const void* q, const void* k_cache, const void* v_cache, const v
         if (!valid_kv_type(kv_type)) return KVATTN_ERR_INVALID_ARG;
         if (head_dim != 128 && head_dim != 256) return KVATTN_ERR_UNSUPPORTED;
         if (n_head_kv < 1 || n_seq < 0 || max_len < 0) return KVATTN_ERR_INVALID_ARG;
-        split = n_rg > 1 ? kvattn_select_split_for(n_seq, max_len, n_head_kv * n_rg,
-                                                   auto_split_slots(kv_type, head_dim))
-                         : kvattn_select_split(kv_type, n_seq, max_len, n_head_kv, head_dim);
+        if (mq_tc) {
+            // the tcgen05 kernel's own resident CTAs: on the Qwen3-8B-shaped layer (16384
+            // cells, 8 KV heads) that is split 512, one wave of 256 units -- 48 rows 22.6 us,
+            // 64 rows 24.7 us, against 24.5 / 27.0 us at the single-query kernels' 256
+            int tc_blocks = 0;
+            if (split_decode_tc_occupancy(&tc_blocks) != cudaSuccess) tc_blocks = 1;
+            split = kvattn_select_split_for(n_seq, max_len, n_head_kv, (int64_t)std::max(tc_blocks, 1) * sm_count());
+        } else {
+            split = n_rg > 1 ? kvattn_select_split_for(n_seq, max_len, n_head_kv * n_rg,
+                                                       auto_split_slots(kv_type, head_dim))
+                             : kvattn_select_split(kv_type, n_seq, max_len, n_head_kv, head_dim);
+        }
         if (split < 0) return split;
     }
     const DecodeShape shape{n_seq, n_head, n_head_kv, head_dim, split, max_len};

@@ -3,8 +3,8 @@ head_dim 128, 33 to 128 query rows per KV head: every row of a KV head in one wo
 P and O in tensor memory) against the fp64 oracle -- contiguous caches with ragged and
 empty sequences, many work units per CTA, plans whose tiles are whole runs, runs with holes
 and scattered cells over NaN-filled unused cells, the per-split descriptors such a call
-leaves in the workspace, and the mma.sync kernels that serve the same calls when the
-tcgen05 path is switched off (KVATTN_TC=0)."""
+leaves in the workspace, the automatic split, and the mma.sync kernels that serve the same
+calls when the tcgen05 path is switched off (KVATTN_TC=0)."""
 import numpy as np
 import pytest
 
@@ -157,3 +157,24 @@ def test_mma_path_for_the_same_rows(kvattn, monkeypatch, n_q, G, Hk, lens, split
     fin = np.isfinite(l_tc.cpu().numpy())
     assert np.max(np.abs(o_tc.cpu().numpy() - o_mma.cpu().numpy())) <= 1e-3
     assert np.max(np.abs(l_tc.cpu().numpy()[fin] - l_mma.cpu().numpy()[fin]), initial=0.0) <= 1e-4
+
+
+def test_tc_split_zero_selects_one_wave_of_its_units(kvattn):
+    """split 0 on the tcgen05 path picks the split for the kernel's own two CTAs per SM (the
+    smallest power of two whose units fit one wave): the result is bit-identical to an
+    explicit call at that split, and matches the oracle."""
+    import torch
+    rng = np.random.default_rng(45)
+    S, N, Hk, G, n_q, D = 2, 6000, 4, 6, 8, 128
+    H = G * Hk
+    q = rand_f16(rng, (S, n_q, H, D))
+    k = rand_f16(rng, (S, N, Hk, D))
+    v = rand_f16(rng, (S, N, Hk, D))
+    lens = dev(np.array([N, 2500], np.int32))
+    sm = torch.cuda.get_device_properties(0).multi_processor_count
+    sp = kvattn.kvattn_select_split_for(S, N, Hk, 2 * sm)
+    o0, l0 = kvattn.decode_multi(dev(q), dev(k), dev(v), lens, split=0, n_cells=N, max_len=N)
+    o1, l1 = kvattn.decode_multi(dev(q), dev(k), dev(v), lens, split=sp, n_cells=N, max_len=N)
+    torch.cuda.synchronize()
+    assert torch.equal(o0, o1) and torch.equal(l0, l1)
+    check(o0, l0, *oracle.decode_multi(oracle.decode_f16, q, [N, 2500], k, v))
