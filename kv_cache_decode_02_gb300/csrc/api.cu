@@ -403,13 +403,28 @@ int decode_impl(const void* q, const void* k_cache, const void* v_cache, const v
     // (four GQA-6 sequences through a plan verifying 8 tokens, 48 rows: 276 -> 202 us).  Four
     // consumer warps for 49 to 64 rows measured slower than two row groups (39.4 against
     // 37.9 us on a 16384-cell layer), which keep that range.
-    // f16 head_dim 128 with more than 32 rows (to 128): the tcgen05 kernel, every row of a KV
-    // head in one unit (rows in TMEM lanes, S and O accumulated in tensor memory).  Measured on the
-    // Qwen3-8B-shaped layer (16384 cells, split 256): 48 rows 33.5 -> 25.2 us, 64 rows 38.0 ->
-    // 26.7 us, the four-sequence GQA-6 plan verifying 8 tokens 202 -> 147 us; at 20 to 32 rows
-    // the mma.sync kernels stay ahead (21.3 against 22.8 us at 32).
-    const bool mq_tc = multi && kv_type == KVATTN_KV_F16 && head_dim == 128 && mq_rows > 32 &&
+    // f16 head_dim 128 with more than 16 rows (to 128): the tcgen05 kernel, every row of a KV
+    // head in one unit (rows in TMEM lanes, S and O accumulated in tensor memory).  Measured on
+    // the Qwen3-8B-shaped layer (16384 cells): at split 256, 48 rows 33.5 -> 25.2 us, 64 rows
+    // 38.0 -> 26.7 us, the four-sequence GQA-6 plan verifying 8 tokens (split 512) 202 -> 147
+    // us.  With 17 to 32 rows it pays only when the call's units fit about one wave of its
+    // CTAs (split 512 there: 32 rows 20.1 us against 21.2 us for the mma.sync kernels at
+    // their best split, 256; at split 256 the tcgen05 kernel takes 22.0 us).
+    const bool tc_ok = multi && kv_type == KVATTN_KV_F16 && head_dim == 128 && mq_rows > 16 &&
                        mq_rows <= kTcMaxRows && aligned(q, 16) && env_int("KVATTN_TC", 1) != 0;
+    int64_t tc_slots = 1;  // its resident CTAs
+    if (tc_ok) {
+        int tc_blocks = 0;
+        if (split_decode_tc_occupancy(&tc_blocks) != cudaSuccess) tc_blocks = 1;
+        tc_slots = (int64_t)std::max(tc_blocks, 1) * sm_count();
+    }
+    // split 0 (kvattn_decode_multi picks it): one wave of the tcgen05 kernel's units
+    const int tc_split = (tc_ok && split == 0 && merge && max_len >= 0 && n_seq >= 0 && n_head_kv >= 1)
+                             ? kvattn_select_split_for(n_seq, max_len, n_head_kv, tc_slots)
+                             : split;
+    const bool mq_tc =
+        tc_ok && (mq_rows > 32 ||
+                  (tc_split > 0 && (int64_t)n_seq * ((max_len + tc_split - 1) / tc_split) * n_head_kv * 4 <= tc_slots * 5));
     const int mq_wide = (!mq_tc && multi && kv_type == KVATTN_KV_F16 && head_dim == 128 && mq_rows > 32 &&
                          mq_rows <= 48 && env_int("KVATTN_MQ_WIDE", 1) != 0)
                             ? 3
@@ -423,12 +438,10 @@ int decode_impl(const void* q, const void* k_cache, const void* v_cache, const v
         if (head_dim != 128 && head_dim != 256) return KVATTN_ERR_UNSUPPORTED;
         if (n_head_kv < 1 || n_seq < 0 || max_len < 0) return KVATTN_ERR_INVALID_ARG;
         if (mq_tc) {
-            // the tcgen05 kernel's own resident CTAs: on the Qwen3-8B-shaped layer (16384
-            // cells, 8 KV heads) that is split 512, one wave of 256 units -- 48 rows 22.6 us,
-            // 64 rows 24.7 us, against 24.5 / 27.0 us at the single-query kernels' 256
-            int tc_blocks = 0;
-            if (split_decode_tc_occupancy(&tc_blocks) != cudaSuccess) tc_blocks = 1;
-            split = kvattn_select_split_for(n_seq, max_len, n_head_kv, (int64_t)std::max(tc_blocks, 1) * sm_count());
+            // one wave of the tcgen05 kernel's units: on the Qwen3-8B-shaped layer (16384
+            // cells, 8 KV heads) split 512 -- 48 rows 22.6 us, 64 rows 24.7 us, against 24.5 /
+            // 27.0 us at the single-query kernels' 256
+            split = tc_split;
         } else {
             split = n_rg > 1 ? kvattn_select_split_for(n_seq, max_len, n_head_kv * n_rg,
                                                        auto_split_slots(kv_type, head_dim))

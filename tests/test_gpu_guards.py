@@ -241,8 +241,8 @@ MULTI = [
     # kind, D, n_q, G, lens, split  (rows per KV head = n_q * G)
     ("f16", 128, 1, 7, [900, 5], 128),        # one token, 7 rows padded to 8
     ("f16", 128, 2, 5, [700, 1, 0], 64),      # 10 rows: one 16-row tile
-    ("f16", 128, 4, 5, [1033, 4], 128),       # 20 rows: the warps split the rows
-    ("f16", 128, 6, 7, [600, 6, 2], 64),      # 42 rows: two row groups, the second ragged
+    ("f16", 128, 4, 5, [1033, 4], 128),       # 20 rows (units in one wave: the tcgen05 kernel)
+    ("f16", 128, 6, 7, [600, 6, 2], 64),      # 42 rows: the tcgen05 kernel, two row warps
     ("f16", 256, 1, 6, [500, 77], 128),
     ("f16", 256, 3, 5, [777, 0], 128),        # 15 rows: 8 per warp
     ("f16", 256, 5, 6, [400, 5], 64),         # 30 rows: row groups of 16

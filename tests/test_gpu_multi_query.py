@@ -1,10 +1,11 @@
 """GPU parity of causal multi-query decode (kvattn_decode_multi) against the fp64 oracle:
 n_q new tokens per sequence, token t seeing logical positions 0 .. L - n_q + t, the
 G x n_q query rows of a KV head in one 16-row MMA tile (up to 16 rows: the two consumer warps
-split the cells) or two (17 to 32 rows: they split the rows); 33 to 128 rows at f16 head_dim
-128 run on the tcgen05 kernel (its own cases in test_gpu_multi_query_tc.py, which also runs
-the mma.sync row groups that serve them with KVATTN_TC=0); at head_dim 256 each consumer
-warp takes 8 of up to 16 rows."""
+split the cells) or two (17 to 32 rows: they split the rows); at f16 head_dim 128, 33 to 128
+rows, and 17 to 32 rows when the call's units fit about one wave of its CTAs, run on the
+tcgen05 kernel (its own cases in test_gpu_multi_query_tc.py, which also runs the mma.sync
+layouts that serve them with KVATTN_TC=0); at head_dim 256 each consumer warp takes 8 of up
+to 16 rows."""
 import numpy as np
 import pytest
 

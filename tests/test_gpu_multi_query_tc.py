@@ -1,5 +1,5 @@
 """GPU parity of causal multi-query decode on the fifth-generation tensor cores (f16 cache,
-head_dim 128, 33 to 128 query rows per KV head: every row of a KV head in one work unit, S,
+head_dim 128, 17 to 128 query rows per KV head: every row of a KV head in one work unit, S,
 P and O in tensor memory) against the fp64 oracle -- contiguous caches with ragged and
 empty sequences, many work units per CTA, plans whose tiles are whole runs, runs with holes
 and scattered cells over NaN-filled unused cells, the per-split descriptors such a call
@@ -134,10 +134,14 @@ def test_tc_plan_leaves_the_split_descriptors_in_the_workspace(kvattn):
                                              plan=masked))
 
 
-@pytest.mark.parametrize("n_q,G,Hk,lens,split", [CONTIGUOUS[0], CONTIGUOUS[2], CONTIGUOUS[4], CONTIGUOUS[8]])
+@pytest.mark.parametrize("n_q,G,Hk,lens,split", [CONTIGUOUS[0], CONTIGUOUS[2], CONTIGUOUS[4], CONTIGUOUS[8],
+                                                 (17, 1, 2, [300, 17], 32),        # 17 rows
+                                                 (5, 5, 2, [640, 33], 64),         # 25 rows
+                                                 (8, 4, 2, [1500, 9, 5], 128)])    # 32 rows
 def test_mma_path_for_the_same_rows(kvattn, monkeypatch, n_q, G, Hk, lens, split):
-    """With the tcgen05 path off the mma.sync kernels (row groups, three consumer warps)
-    serve 33 to 128 rows; both agree with the oracle and with each other to rounding."""
+    """With the tcgen05 path off the mma.sync kernels (the two consumer warps splitting 17 to
+    32 rows, three consumer warps, row groups) serve the same calls; both agree with the
+    oracle and with each other to rounding."""
     import torch
     rng = np.random.default_rng([44, n_q, G])
     S, D = len(lens), 128

@@ -270,10 +270,15 @@ MQ_ROWS = [(2, 4), (4, 4), (8, 4), (8, 6)]
 
 @pytest.mark.parametrize("case", MQ_CASES)
 @pytest.mark.parametrize("n_q,G", MQ_ROWS)
-@pytest.mark.parametrize("kind,D", [("f16", 128), ("f16", 256), ("q8", 128), ("q8", 256), ("q8q4", 128),
-                                    ("q4", 256)])
-def test_rescale_multi_query(kvattn, kind, D, n_q, G, case):
+@pytest.mark.parametrize("kind,D", [("f16", 128), ("f16_mma", 128), ("f16", 256), ("q8", 128), ("q8", 256),
+                                    ("q8q4", 128), ("q4", 256)])
+def test_rescale_multi_query(kvattn, monkeypatch, kind, D, n_q, G, case):
+    """f16 head_dim 128 with more than 16 rows runs on the tcgen05 kernel; f16_mma is the
+    same case on the mma.sync layouts (KVATTN_TC=0)."""
     import torch
+    if kind == "f16_mma":
+        monkeypatch.setenv("KVATTN_TC", "0")
+        kind = "f16"
     rng = np.random.default_rng([33, D, n_q, G, MQ_CASES.index(case), list(KIND_ORACLE).index(kind)])
     S, N, Hk = 2, 1100, 2
     H = Hk * G
