@@ -226,7 +226,9 @@ size_t kvattn_decode_multi_workspace_bytes(int n_seq, int n_q, int n_head, int h
  * positions 0 .. L - n_q + t (plan entries or cells, -1 holes masked); a token whose window
  * is empty gets O = 0, LSE = -inf.  The G x n_q query rows of each KV head share every K/V
  * byte read from HBM (one or two 16-row MMA tiles, up to 32 rows; f16 at head_dim 128 with
- * 33 to 128 rows and q 16-byte aligned: one tcgen05 tile of all the rows).  n_q = 1 is
+ * q 16-byte aligned, 33 to 128 rows -- and 17 to 32 when the call's work units fit about
+ * one wave of its CTAs, as the automatic split arranges -- one tcgen05 tile of all the
+ * rows).  n_q = 1 is
  * exactly kvattn_decode (and runs its kernels); up to 8 rows per KV head (f16, and the
  * quantised types at head_dim 128) run on the single-query kernels with per-row causal
  * masks.
