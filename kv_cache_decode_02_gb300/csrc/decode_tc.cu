@@ -166,6 +166,22 @@ __device__ __forceinline__ TcUnit tc_unit(const SplitDecodeParams& p, uint32_t u
     return x;
 }
 
+// The V rows of a tile's cells outside `mask` (plan holes, cells past the split, rows no
+// copy brought) become zeros, so that their P = 0 never meets a non-finite value: 16 lanes
+// a row, two rows per store; then the proxy fence that orders the stores before the P V.
+__device__ __forceinline__ void zero_masked_v(unsigned char* stage, uint32_t mask, int lane) {
+    unsigned char* zv = stage + 2 * kPlane;
+    for (uint32_t m = ~mask; m != 0u;) {
+        const int c = __ffs(m) - 1;
+        const uint32_t m2 = m & (m - 1u);
+        const int c2 = m2 != 0u ? __ffs(m2) - 1 : c;
+        const int cz = lane < 16 ? c : c2;
+        *reinterpret_cast<uint4*>(zv + ((lane >> 3) & 1) * kPlane + cz * 128 + (lane & 7) * 16) = make_uint4(0u, 0u, 0u, 0u);
+        m = m2 != 0u ? m2 & (m2 - 1u) : 0u;
+    }
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
 __global__ void __launch_bounds__(kThreads, 2) split_decode_tc_f16_d128(const __grid_constant__ SplitDecodeParams p) {
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     unsigned char* smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
@@ -175,7 +191,8 @@ __global__ void __launch_bounds__(kThreads, 2) split_decode_tc_f16_d128(const __
     uint64_t* p_full = s_full + 2;                            // [2] P of a tile is in TMEM
     uint64_t* q_full = p_full + 2;                            // a unit's Q rows are staged
     uint64_t* o_bar = q_full + 1;                             // a unit's last P V is done
-    uint32_t* tile_mask = reinterpret_cast<uint32_t*>(o_bar + 1);  // [kStages] valid entries
+    uint64_t* zero_bar = o_bar + 1;                           // [kStages] masked V rows zeroed
+    uint32_t* tile_mask = reinterpret_cast<uint32_t*>(zero_bar + kStages);  // [kStages] valid entries
     uint32_t* tile_lsu = tile_mask + kStages;                      // [kStages] rows copied by the LSU
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tile_lsu + kStages);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tile_lsu + kStages + 1);
@@ -192,6 +209,11 @@ __global__ void __launch_bounds__(kThreads, 2) split_decode_tc_f16_d128(const __
     // producer and the MMA warp take warps no row needs, on other schedulers than the rows.
     const int prod_warp = row_warps <= 2 ? 2 : 4;
     const int mma_warp = row_warps <= 3 ? 3 : 5;
+    // Through a plan with up to 64 rows a spare warp zeros the V rows of a tile's masked cells
+    // (a plan hole inside a run may hold anything, and 0 x NaN is NaN on the tensor cores too)
+    // before the tile's P V; otherwise -- more rows, or a contiguous cache, whose only masked
+    // cells are past a sequence's end in its last tile -- the first row warp does.
+    const int fix_warp = (row_warps <= 2 && p.plan != nullptr) ? 4 : -1;
     const uint32_t n_units = (uint32_t)((int64_t)p.n_seq * p.unit_splits * p.n_head_kv);
 
     if (tid == 0) {
@@ -205,6 +227,7 @@ __global__ void __launch_bounds__(kThreads, 2) split_decode_tc_f16_d128(const __
         }
         mbar_init(smem_addr(q_full), 32 * row_warps);
         mbar_init(smem_addr(o_bar), 1);
+        for (int i = 0; i < kStages; ++i) mbar_init(smem_addr(&zero_bar[i]), 32);
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -295,12 +318,23 @@ __global__ void __launch_bounds__(kThreads, 2) split_decode_tc_f16_d128(const __
                 int64_t base = (int64_t)x.s * p.n_cells + tile0;
                 bool run = true;
                 if (p.plan != nullptr) {
-                    long long lo = valid ? (long long)(cell - i) : LLONG_MAX;
-                    long long hi = valid ? (long long)(cell - i) : LLONG_MIN;
+                    // one physical run: the same (cell - position) in every valid lane; a 32-bit
+                    // warp reduction unless some offset leaves that range
+                    const long long off = (long long)(cell - i);
+                    long long lo, hi;
+                    if (!__any_sync(0xffffffffu, valid && (off < INT_MIN / 2 || off > INT_MAX / 2))) {
+                        lo = __reduce_min_sync(0xffffffffu, valid ? (int)off : INT_MAX);
+                        hi = __reduce_max_sync(0xffffffffu, valid ? (int)off : INT_MIN);
+                        if (lo == INT_MAX) lo = LLONG_MAX;  // no valid lane
+                        if (hi == INT_MIN) hi = LLONG_MIN;
+                    } else {
+                        lo = valid ? off : LLONG_MAX;
+                        hi = valid ? off : LLONG_MIN;
 #pragma unroll
-                    for (int o = 16; o > 0; o >>= 1) {
-                        lo = min(lo, __shfl_xor_sync(0xffffffffu, lo, o));
-                        hi = max(hi, __shfl_xor_sync(0xffffffffu, hi, o));
+                        for (int o = 16; o > 0; o >>= 1) {
+                            lo = min(lo, __shfl_xor_sync(0xffffffffu, lo, o));
+                            hi = max(hi, __shfl_xor_sync(0xffffffffu, hi, o));
+                        }
                     }
                     run = mask != 0u && lo == hi;
                     base = lo + tile0;
@@ -409,6 +443,13 @@ __global__ void __launch_bounds__(kThreads, 2) split_decode_tc_f16_d128(const __
                     ok = false;
                     break;
                 }
+                // a tile with masked cells waits for its zeros (the zeros warp arrives for every
+                // tile, so the phase is the tile's whatever tiles were not waited for)
+                if (fix_warp >= 0 && tile_mask[T % kStages] != 0xffffffffu &&
+                    !wait_all(smem_addr(&zero_bar[T % kStages]), (T / kStages) & 1u)) {
+                    ok = false;
+                    break;
+                }
                 tc_fence_after();
                 // O += P V over the tile's 32 cells (two k-steps of 16)
                 const uint64_t vd = smem_desc(smem_addr(stages + (T % kStages) * kStageBytes) + 2 * kPlane, kPlane, 1024);
@@ -421,6 +462,24 @@ __global__ void __launch_bounds__(kThreads, 2) split_decode_tc_f16_d128(const __
                     if (t + 1 == n_tiles) mma_commit(smem_addr(o_bar));
                 }
                 __syncwarp();
+            }
+        }
+    } else if (warp == fix_warp) {
+        // ------------------------------------- zeros ------------------------------------
+        uint32_t T = 0;
+        bool ok = true;
+        for (uint32_t u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
+            const int n_tiles = tc_unit(p, u).n_tiles;
+            for (int t = 0; t < n_tiles; ++t, ++T) {
+                const int st = (int)(T % kStages);
+                if (!__all_sync(0xffffffffu, mbar_wait_bounded(smem_addr(&full_bar[st]), (T / kStages) & 1u,
+                                                                abort_flag, p.wait_limit_ns))) {
+                    ok = false;
+                    break;
+                }
+                const uint32_t mask = tile_mask[st];
+                if (mask != 0xffffffffu) zero_masked_v(stages + st * kStageBytes, mask, lane);
+                mbar_arrive(smem_addr(&zero_bar[st]));
             }
         }
     } else if (warp < row_warps) {
@@ -520,23 +579,8 @@ __global__ void __launch_bounds__(kThreads, 2) split_decode_tc_f16_d128(const __
                     break;
                 }
                 const uint32_t mask = tile_mask[T % kStages];
-                if (mask != 0xffffffffu && warp == 0) {
-                    // the V rows of cells that are not in the tile (plan holes, cells past the
-                    // split, rows no copy brought) become zeros, so that their P = 0 never meets a
-                    // non-finite value; the tile's P V is issued after this warp's arrival below
-                    unsigned char* zv = stages + (T % kStages) * kStageBytes + 2 * kPlane;
-                    for (uint32_t m = ~mask; m != 0u; m &= m - 1u) {  // 16 lanes a row, two rows at once
-                        const int c = __ffs(m) - 1;
-                        const uint32_t m2 = m & (m - 1u);
-                        const int c2 = m2 != 0u ? __ffs(m2) - 1 : c;
-                        const int cz = lane < 16 ? c : c2;
-                        *reinterpret_cast<uint4*>(zv + ((lane >> 3) & 1) * kPlane + cz * 128 + (lane & 7) * 16) =
-                            make_uint4(0u, 0u, 0u, 0u);
-                        m = m2;
-                        if (m == 0u) break;
-                    }
-                    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-                }
+                if (mask != 0xffffffffu && warp == 0 && fix_warp < 0)
+                    zero_masked_v(stages + (T % kStages) * kStageBytes, mask, lane);
                 uint32_t sv[32];
                 tmem_ld32(t_s + 32 * (T & 1u), sv);
                 tc_wait_ld();
