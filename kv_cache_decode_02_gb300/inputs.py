@@ -60,7 +60,7 @@ class Workload:
 TINY = Workload("tiny_gqa4_n512", 1, 1, 512, 8, 2, 128, 128, seq_lens=(512,))
 QWEN3_8B_LAYER = Workload("qwen3_8b_layer_n16384", 2, 1, 16384, 32, 8, 128, 256,
                           seq_lens=(16384,), layers=36)
-MULTISLOT_PLAN = Workload("multislot_gqa6_plan", 3, 4, 1152 * RECORD_CELLS, 48, 8, 128, 128,
+MULTISLOT_PLAN = Workload("multislot_gqa6_plan", 3, 4, 1152 * RECORD_CELLS, 48, 8, 128, 256,
                           seq_lens=(8192, 20480, 40960, 65536), hole_prob=0.1,
                           pool_records=1152)
 Q8_LONG_D128 = Workload("q8_0_n131072_d128", 4, 1, 131072, 32, 8, 128, 512,
