@@ -727,27 +727,41 @@ __global__ void __launch_bounds__(kThreads, 2) split_decode_tc_f16_d128(const __
     pdl_launch_dependents();
 }
 
-cudaError_t set_attr_once() {
+// Per device, once: the kernel's shared-memory attributes and how many of its CTAs fit on an
+// SM.  Shared memory decides (the runtime's occupancy query answers one CTA for this kernel
+// although two fit); two CTAs of 256 tensor-memory columns fill an SM's 512.
+struct TcSetup {
+    cudaError_t err;
+    int blocks;
+};
+TcSetup tc_setup() {
     static std::once_flag once[64];
-    static cudaError_t err[64];
+    static TcSetup done[64];
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) return e;
+    if (e != cudaSuccess) return TcSetup{e, 1};
     std::call_once(once[dev & 63], [&] {
-        cudaError_t e1 = cudaFuncSetAttribute(split_decode_tc_f16_d128, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+        TcSetup r{cudaSuccess, 1};
+        r.err = cudaFuncSetAttribute(split_decode_tc_f16_d128, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
         // the whole carve-out as shared memory: two CTAs of ~100 KB per SM
-        cudaError_t e2 = cudaFuncSetAttribute(split_decode_tc_f16_d128, cudaFuncAttributePreferredSharedMemoryCarveout,
-                                              (int)cudaSharedmemCarveoutMaxShared);
-        err[dev & 63] = e1 != cudaSuccess ? e1 : e2;
+        if (r.err == cudaSuccess)
+            r.err = cudaFuncSetAttribute(split_decode_tc_f16_d128, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                         (int)cudaSharedmemCarveoutMaxShared);
+        int per_sm = 0, reserved = 0;
+        if (r.err == cudaSuccess) r.err = cudaDeviceGetAttribute(&per_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev);
+        if (r.err == cudaSuccess) r.err = cudaDeviceGetAttribute(&reserved, cudaDevAttrReservedSharedMemoryPerBlock, dev);
+        const int fit = per_sm / (kSmem + reserved);
+        r.blocks = fit < 1 ? 1 : (fit > 2 ? 2 : fit);
+        done[dev & 63] = r;
     });
-    return err[dev & 63];
+    return done[dev & 63];
 }
 
 }  // namespace
 
 cudaError_t launch_split_decode_tc(const SplitDecodeParams& p, unsigned grid_ctas, cudaStream_t stream, bool pdl) {
-    cudaError_t e = set_attr_once();
-    if (e != cudaSuccess) return e;
+    const TcSetup t = tc_setup();
+    if (t.err != cudaSuccess) return t.err;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid_ctas, 1, 1);
     cfg.blockDim = dim3(kThreads, 1, 1);
@@ -763,17 +777,9 @@ cudaError_t launch_split_decode_tc(const SplitDecodeParams& p, unsigned grid_cta
 }
 
 cudaError_t split_decode_tc_occupancy(int* blocks) {
-    cudaError_t e = set_attr_once();
-    if (e != cudaSuccess) return e;
-    // Shared memory decides (the runtime's occupancy query answers one CTA for this kernel
-    // although two fit); two CTAs of 256 tensor-memory columns fill an SM's 512.
-    int dev = 0, per_sm = 0, reserved = 0;
-    if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
-    if ((e = cudaDeviceGetAttribute(&per_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev)) != cudaSuccess) return e;
-    if ((e = cudaDeviceGetAttribute(&reserved, cudaDevAttrReservedSharedMemoryPerBlock, dev)) != cudaSuccess) return e;
-    const int fit = per_sm / (kSmem + reserved);
-    *blocks = fit < 1 ? 1 : (fit > 2 ? 2 : fit);
-    return cudaSuccess;
+    const TcSetup t = tc_setup();
+    *blocks = t.blocks;
+    return t.err;
 }
 
 }  // namespace kvattn
