@@ -398,7 +398,8 @@ int decode_impl(const void* q, const void* k_cache, const void* v_cache, const v
     const int mq_rows = (n_head_kv >= 1 && n_head >= n_head_kv) ? (n_head / n_head_kv) * n_q : 0;
     // (f16 head_dim 128 in groups of 16 instead, each group a cell-split unit: 33.4 against
     // 29.3 us for 32 rows, 49.8 against 41.6 us for 64, on a 16384-cell 8-KV-head layer)
-    // f16 head_dim 128 with 33 to 48 rows: one unit whose three consumer warps take 16 rows
+    // f16 head_dim 128 with 33 to 48 rows, when the tcgen05 kernel below does not take them
+    // (KVATTN_TC=0, q not 16-byte aligned): one unit whose three consumer warps take 16 rows
     // each, so every tile is read once for all the rows instead of once per row group of 32
     // (four GQA-6 sequences through a plan verifying 8 tokens, 48 rows: 276 -> 202 us).  Four
     // consumer warps for 49 to 64 rows measured slower than two row groups (39.4 against
