@@ -182,3 +182,23 @@ def test_tc_split_zero_selects_one_wave_of_its_units(kvattn):
     torch.cuda.synchronize()
     assert torch.equal(o0, o1) and torch.equal(l0, l1)
     check(o0, l0, *oracle.decode_multi(oracle.decode_f16, q, [N, 2500], k, v))
+
+
+def test_q_not_16_byte_aligned_takes_the_mma_path(kvattn):
+    """The tcgen05 kernel copies query rows 16 bytes at a time; a q that is only 4-byte
+    aligned (as the entry point allows) is served by the mma.sync layouts, still exact."""
+    import torch
+    rng = np.random.default_rng(46)
+    S, N, Hk, G, n_q, D = 2, 900, 2, 6, 8, 128      # 48 rows per KV head
+    H = G * Hk
+    q = rand_f16(rng, (S, n_q, H, D))
+    k = rand_f16(rng, (S, N, Hk, D))
+    v = rand_f16(rng, (S, N, Hk, D))
+    buf = torch.empty(q.size + 2, dtype=torch.float16, device="cuda")
+    qd = buf[2:].view(S, n_q, H, D)                 # 4 bytes past a 16-byte boundary
+    qd.copy_(dev(q))
+    assert qd.data_ptr() % 16 == 4
+    out, lse = kvattn.decode_multi(qd, dev(k), dev(v), dev(np.array([N, 333], np.int32)), split=128, n_cells=N,
+                                   max_len=N)
+    torch.cuda.synchronize()
+    check(out, lse, *oracle.decode_multi(oracle.decode_f16, q, [N, 333], k, v))
