@@ -712,8 +712,9 @@ __device__ __forceinline__ void mq_tile32(uint32_t kb, uint32_t vb, uint32_t mas
 // rows per KV head, each warp attends to its 16 cells of every tile for all rows and the
 // two warps meet in the doubled end-of-unit exchange; with 17 to 32 rows, warp w takes rows
 // 16w .. 16w+15 over all 32 cells of every tile and writes them itself (no exchange); with
-// 33 to 64 rows, each group of 32 rows is a unit of its own in the same way (the groups of
-// a split are neighbouring units, so the second reads the split's K/V from L2).
+// 33 to 128 rows, each group of 32 rows is a unit of its own in the same way (the groups of
+// a split are neighbouring units, so the second reads the split's K/V from L2).  Beyond 16
+// rows the tcgen05 kernel (decode_tc.cu) takes most calls; these layouts serve the others.
 __device__ __forceinline__ void mq_consumers(const SplitDecodeParams& p, uint64_t* full_bar, uint64_t* empty_bar,
                                              const uint32_t* tile_mask, const uint32_t* tile_swz,
                                              volatile int* abort_flag, uint64_t* xchg_bar, unsigned char* xchg,
