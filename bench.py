@@ -1043,6 +1043,26 @@ def profile_verify(args):
     print(f"{args.profile_workload}: {args.kernel_reps} calls done")
 
 
+def profile_plan(args):
+    """--kernel-reps kvattn_decode calls of the multi-slot plan workload (4 GQA-6 sequences
+    through a compact plan with ~10 % holes, split 256), for profilers."""
+    import torch
+    from kv_cache_decode_02_gb300 import inputs
+    from kv_cache_decode_02_gb300 import kvattn as K
+    w = inputs.MULTISLOT_PLAN
+    lay = inputs.make_unified_layout(w)
+    plan, plens = K.build_cell_plan(lay.encoded_cells, w.n_cells)
+    k = inputs.normal_f16_torch((2000 + w.number, 0), (w.n_cells, w.n_head_kv, w.head_dim), "cuda")
+    v = inputs.normal_f16_torch((3000 + w.number, 0), (w.n_cells, w.n_head_kv, w.head_dim), "cuda")
+    q = torch.from_numpy(inputs.make_q(w)).cuda()
+    plan_d = torch.from_numpy(plan).cuda()
+    lens_d = torch.from_numpy(plens).cuda()
+    for _ in range(args.kernel_reps):
+        K.decode(q, k, v, lens_d, split=w.split, cell_plan=plan_d, n_cells=w.n_cells)
+    torch.cuda.synchronize()
+    print(f"{args.profile_workload}: {args.kernel_reps} calls done ({int((plan >= 0).sum())} valid cells)")
+
+
 def profile_interleaved(args):
     """--kernel-reps decode steps of the headline layers with the stand-in projection before
     each kvattn_decode call (launched eagerly), for an ncu launch list."""
@@ -1149,7 +1169,8 @@ def main():
                                                    "q4_0_n131072_d256", "window_tail_n524288",
                                                    "window_tail_n524288_direct", "window_tail_n81920",
                                                    "window_tail_n81920_direct", "qwen3_8b_layer_verify_nq4",
-                                                   "qwen3_8b_layer_verify_nq8", "qwen3_8b_layer_verify_nq16"],
+                                                   "qwen3_8b_layer_verify_nq8", "qwen3_8b_layer_verify_nq16",
+                                                   "multislot_gqa6_plan"],
                     help="only launch this workload's split decode (window + tail: the whole op) "
                          "--kernel-reps times (for ncu)")
     args = ap.parse_args()
@@ -1160,6 +1181,8 @@ def main():
             profile_window_tail(args)
         elif args.profile_workload.startswith("qwen3_8b_layer_verify"):
             profile_verify(args)
+        elif args.profile_workload == "multislot_gqa6_plan":
+            profile_plan(args)
         else:
             profile_workload(args)
         return
