@@ -95,6 +95,17 @@ __device__ __forceinline__ void tma_load_3d_hint(uint32_t dst, const CUtensorMap
         : "memory");
 }
 
+// TMA load of one 4-D tensor-map box (8-bit rows of 256 bytes: both 128-byte planes of the
+// box's cells in one copy).
+__device__ __forceinline__ void tma_load_4d_hint(uint32_t dst, const CUtensorMap* map, int x, int y, int z, int w,
+                                                 uint32_t bar, uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1, "
+        "{%2, %3, %4, %5}], [%6], %7;" ::"r"(dst),
+        "l"(map), "r"(x), "r"(y), "r"(z), "r"(w), "r"(bar), "l"(policy)
+        : "memory");
+}
+
 // TMA load of one 2-D tensor-map box (the scale planes of the quantised caches).
 __device__ __forceinline__ void tma_load_2d_hint(uint32_t dst, const CUtensorMap* map, int x, int y, uint32_t bar,
                                                  uint64_t policy) {
@@ -115,6 +126,16 @@ __device__ __forceinline__ uint64_t l2_evict_first_policy() {
 __device__ __forceinline__ void tma_prefetch_3d(const CUtensorMap* map, int x, int y, int z) {
     asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(map), "r"(x), "r"(y),
                  "r"(z)
+                 : "memory");
+}
+
+__device__ __forceinline__ void tma_prefetch_4d(const CUtensorMap* map, int x, int y, int z, int w) {
+    asm volatile("cp.async.bulk.prefetch.tensor.4d.L2.global.tile [%0, {%1, %2, %3, %4}];" ::"l"(map), "r"(x),
+                 "r"(y), "r"(z), "r"(w)
+                 : "memory");
+}
+__device__ __forceinline__ void tma_prefetch_2d(const CUtensorMap* map, int x, int y) {
+    asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(map), "r"(x), "r"(y)
                  : "memory");
 }
 
@@ -498,6 +519,13 @@ __device__ __forceinline__ Unit unit_at(const SplitDecodeParams& p, int64_t u) {
     return x;
 }
 
+// The query rows a unit reads are those of its (sequence, KV head, row group): units with the
+// same key share their query fragments, so a warp reloads them only when the key changes
+// (a CTA's successive units mostly keep the sequence and KV head).
+__device__ __forceinline__ int64_t q_key(const SplitDecodeParams& p, const Unit& x) {
+    return ((int64_t)x.s * p.n_head_kv + x.g) * 256 + x.rg;
+}
+
 // ---------------------------------------------------------------------------------------
 // Causal multi-query decode (f16, head_dim 128).  The G x n_q query rows of a KV head
 // (row r = token r / G, query head g*G + r % G) fill the whole M of the q.K^T MMA -- a
@@ -736,7 +764,7 @@ __device__ __forceinline__ void mq_consumers(const SplitDecodeParams& p, uint64_
     float* xl = xm + 16;                                            // [16] sum
     constexpr float kLn2 = 0.69314718055994530942f;
     uint32_t qa[8][4];
-    int64_t qa_unit = -1;
+    int64_t qa_key = -1;  // q_key of the rows whose query fragments qa holds
     uint32_t T = 0, X = 0;
     bool stop = false;
     for (int64_t u = blockIdx.x; u < n_units && !stop; u += gridDim.x) {
@@ -758,7 +786,10 @@ __device__ __forceinline__ void mq_consumers(const SplitDecodeParams& p, uint64_
             }
             continue;
         }
-        if (qa_unit != u) load_q_frags_mq(p, x.s, x.g, gq, tq, row0, qa);
+        if (qa_key != q_key(p, x)) {
+            load_q_frags_mq(p, x.s, x.g, gq, tq, row0, qa);
+            qa_key = q_key(p, x);
+        }
         float oacc[2][8][4];
 #pragma unroll
         for (int nt = 0; nt < 2; ++nt)
@@ -860,9 +891,9 @@ __device__ __forceinline__ void mq_consumers(const SplitDecodeParams& p, uint64_
         const int64_t un = u + gridDim.x;
         if (un < n_units) {
             const Unit y = unit_at(p, un);
-            if (y.n_tiles > 0) {
+            if (y.n_tiles > 0 && q_key(p, y) != qa_key) {
                 load_q_frags_mq(p, y.s, y.g, gq, tq, first_row(y), qa);
-                qa_unit = un;
+                qa_key = q_key(p, y);
             }
         }
         if (rsplit) {
@@ -994,7 +1025,7 @@ __device__ __forceinline__ void mq_consumers_rows8(const SplitDecodeParams& p, u
         }
     };
     uint32_t qa[D / 16][2];
-    int64_t qa_unit = -1;
+    int64_t qa_key = -1;  // q_key of the rows whose query fragments qa holds
     uint32_t T = 0;
     bool stop = false;
     for (int64_t u = blockIdx.x; u < n_units && !stop; u += gridDim.x) {
@@ -1015,7 +1046,10 @@ __device__ __forceinline__ void mq_consumers_rows8(const SplitDecodeParams& p, u
             }
             continue;
         }
-        if (qa_unit != u) load_q(x.s, x.g, row0, qa);
+        if (qa_key != q_key(p, x)) {
+            load_q(x.s, x.g, row0, qa);
+            qa_key = q_key(p, x);
+        }
         float oacc[D / 16][4];
         float m_run = -INFINITY, l_run = 0.f;
 #pragma unroll
@@ -1073,9 +1107,9 @@ __device__ __forceinline__ void mq_consumers_rows8(const SplitDecodeParams& p, u
         const int64_t un = u + gridDim.x;
         if (un < n_units) {
             const Unit y = unit_at(p, un);
-            if (y.n_tiles > 0) {
+            if (y.n_tiles > 0 && q_key(p, y) != qa_key) {
                 load_q(y.s, y.g, first_row(y), qa);
-                qa_unit = un;
+                qa_key = q_key(p, y);
             }
         }
         // this lane's O rows are 8w + 2tq + e; their max / sum sit in lanes 8tq + 4e
@@ -1372,7 +1406,7 @@ __device__ __forceinline__ void split_decode_body(const SplitDecodeParams& p) {
                          reinterpret_cast<unsigned char*>(xo), stages, n_stages, n_units, warp, lane);
         } else {
         uint32_t qa[D / 16][2];
-        int64_t qa_unit = -1;  // unit whose query fragments qa holds
+        int64_t qa_key = -1;  // q_key of the rows whose query fragments qa holds
         uint32_t T = 0;        // tiles consumed (ring position)
         uint32_t X = 0;        // end-of-unit exchanges done
         bool stop = false;
@@ -1405,7 +1439,10 @@ __device__ __forceinline__ void split_decode_body(const SplitDecodeParams& p) {
                 }
                 continue;
             }
-            if (qa_unit != u) load_q_frags<KVT, D>(p, x.s, x.g, gq, tq, qa, MQ8 ? x.rg : -1);
+            if (qa_key != q_key(p, x)) {
+                load_q_frags<KVT, D>(p, x.s, x.g, gq, tq, qa, MQ8 ? x.rg : -1);
+                qa_key = q_key(p, x);
+            }
             // MQ8: causal limit (logical position, exclusive) of the lane's row 8 rg + gq
             const int64_t lim_row = MQ8 ? x.len - p.n_q + 1 + (8 * x.rg + gq) / p.group : 0;
             float oacc[D / 16][4];
@@ -1485,9 +1522,9 @@ __device__ __forceinline__ void split_decode_body(const SplitDecodeParams& p) {
             const int64_t un = u + gridDim.x;
             if (un < n_units) {
                 const Unit y = unit_at(p, un);
-                if (y.n_tiles > 0) {
+                if (y.n_tiles > 0 && q_key(p, y) != qa_key) {
                     load_q_frags<KVT, D>(p, y.s, y.g, gq, tq, qa, MQ8 ? y.rg : -1);
-                    qa_unit = un;
+                    qa_key = q_key(p, y);
                 }
             }
 
@@ -2247,12 +2284,48 @@ __device__ __forceinline__ void q8_self_body(const SplitDecodeParams& p) {
     __syncthreads();
     const bool one_wave = (int64_t)gridDim.x >= n_units;
     if (one_wave) pdl_launch_dependents();  // see split_decode_body
+    // While the previous kernel drains (this CTA may be resident already, waiting for it),
+    // each warp pulls the first chunks it will load into L2.  The lengths read here may still
+    // change before the dependency wait; they only steer these hints, never the loads (boxes
+    // outside the cache are not fetched).
+    if (lane == 0 && p.use_tma != 0 && p.scl_tma != 0 && p.plan == nullptr && blockIdx.x < n_units) {
+        const Unit x = unit_at(p, blockIdx.x);
+        const int nch = unit_chunks(x);
+        for (int j = warp, k = 0; j < nch && k <= S; j += W, ++k) {
+            const int64_t base = (int64_t)x.s * p.n_cells + x.i0 + (int64_t)j * kChunkCells;
+            if (base >= INT_MAX / 2) break;
+            if constexpr (!KQ4 && Q::kPlanes > 1)
+                tma_prefetch_4d(&p.tmap_k, 0, (int)base, 0, x.g);
+            else
+                tma_prefetch_3d(&p.tmap_k, 0, x.g, (int)base);
+            if constexpr (!VQ4 && Q::kPlanes > 1)
+                tma_prefetch_4d(&p.tmap_v, 0, (int)base, 0, x.g);
+            else
+                tma_prefetch_3d(&p.tmap_v, 0, x.g, (int)base);
+            tma_prefetch_2d(&p.tmap_ks, scl_box_x<D>(x.g), (int)base);
+            tma_prefetch_2d(&p.tmap_vs, scl_box_x<D>(x.g), (int)base);
+        }
+    }
     pdl_wait();
 
     unsigned char* ring = rings + warp * S * Q::kChunkBytes;
     unsigned char* sring = scales + warp * S * Q::kSclChunk;
     uint64_t* fb = full_bar + warp * S;
     bool bad = false;
+
+    // The chunk's K and V rows by TMA into the stage at kdst: 8-bit rows of 256 bytes in one
+    // 4-D box each (both 128-byte swizzled planes), 128-byte 8-bit rows and 4-bit rows (64
+    // or 128 bytes) in one 3-D box.
+    auto load_rows = [&](uint32_t kdst, int g, int base, uint32_t bar, uint64_t pol) {
+        if constexpr (!KQ4 && Q::kPlanes > 1)
+            tma_load_4d_hint(kdst, &p.tmap_k, 0, base, 0, g, bar, pol);
+        else
+            tma_load_3d_hint(kdst, &p.tmap_k, 0, g, base, bar, pol);
+        if constexpr (!VQ4 && Q::kPlanes > 1)
+            tma_load_4d_hint(kdst + Q::kSection, &p.tmap_v, 0, base, 0, g, bar, pol);
+        else
+            tma_load_3d_hint(kdst + Q::kSection, &p.tmap_v, 0, g, base, bar, pol);
+    };
 
     // Issues the loads of chunk c.j of unit c.u into stage st.
     // Cache without a plan: the chunk's cells are consecutive rows, so the mask, the box
@@ -2273,18 +2346,7 @@ __device__ __forceinline__ void q8_self_body(const SplitDecodeParams& p) {
                 mbar_expect_tx(bar, (uint32_t)(Q::kChunkBytes + Q::kSclChunk) + extra_tx);
                 const uint64_t pol = l2_evict_first_policy();
                 const uint32_t kdst = smem_addr(stage);
-                if (KQ4) {
-                    tma_load_3d_hint(kdst, &p.tmap_k, 0, c.g, (int)base, bar, pol);
-                } else {
-#pragma unroll
-                    for (int pl = 0; pl < Q::kPlanes; ++pl) {
-                        tma_load_3d_hint(kdst + pl * Q::kPlane, &p.tmap_k, pl * 128, c.g, (int)base, bar, pol);
-                        if (!VQ4)
-                            tma_load_3d_hint(kdst + Q::kSection + pl * Q::kPlane, &p.tmap_v, pl * 128, c.g, (int)base,
-                                             bar, pol);
-                    }
-                }
-                if (VQ4) tma_load_3d_hint(kdst + Q::kSection, &p.tmap_v, 0, c.g, (int)base, bar, pol);
+                load_rows(kdst, c.g, (int)base, bar, pol);
                 const uint32_t sdst = smem_addr(sring + st * Q::kSclChunk);
                 tma_load_2d_hint(sdst, &p.tmap_ks, scl_box_x<D>(c.g), (int)base, bar, pol);
                 tma_load_2d_hint(sdst + kChunkCells * Q::kSclRow, &p.tmap_vs, scl_box_x<D>(c.g), (int)base, bar, pol);
@@ -2309,21 +2371,7 @@ __device__ __forceinline__ void q8_self_body(const SplitDecodeParams& p) {
         if (use_tma) {
             if (lane == 0) {
                 const uint32_t kdst = smem_addr(stage);
-                if (KQ4) {
-                    tma_load_3d_hint(kdst, &p.tmap_k, 0, c.g, (int)base, bar, l2_evict_first_policy());
-                } else {
-#pragma unroll
-                    for (int pl = 0; pl < Q::kPlanes; ++pl) {
-                        tma_load_3d_hint(kdst + pl * Q::kPlane, &p.tmap_k, pl * 128, c.g, (int)base, bar,
-                                         l2_evict_first_policy());
-                        if (!VQ4)
-                            tma_load_3d_hint(kdst + Q::kSection + pl * Q::kPlane, &p.tmap_v, pl * 128, c.g,
-                                             (int)base, bar, l2_evict_first_policy());
-                    }
-                }
-                // 4-bit V: one box of the chunk's D/2-byte rows (64 or 128 bytes wide)
-                if (VQ4)
-                    tma_load_3d_hint(kdst + Q::kSection, &p.tmap_v, 0, c.g, (int)base, bar, l2_evict_first_policy());
+                load_rows(kdst, c.g, (int)base, bar, l2_evict_first_policy());
                 if (scl_tma) {
                     const uint32_t sdst = smem_addr(sring + st * Q::kSclChunk);
                     tma_load_2d_hint(sdst, &p.tmap_ks, scl_box_x<D>(c.g), (int)base, bar, l2_evict_first_policy());
@@ -2411,21 +2459,7 @@ __device__ __forceinline__ void q8_self_body(const SplitDecodeParams& p) {
         if (use_tma) {
             if (lane == 0) {
                 const uint32_t kdst = smem_addr(stage);
-                if (KQ4) {
-                    tma_load_3d_hint(kdst, &p.tmap_k, 0, c.g, (int)base, bar, l2_evict_first_policy());
-                } else {
-#pragma unroll
-                    for (int pl = 0; pl < Q::kPlanes; ++pl) {
-                        tma_load_3d_hint(kdst + pl * Q::kPlane, &p.tmap_k, pl * 128, c.g, (int)base, bar,
-                                         l2_evict_first_policy());
-                        if (!VQ4)
-                            tma_load_3d_hint(kdst + Q::kSection + pl * Q::kPlane, &p.tmap_v, pl * 128, c.g,
-                                             (int)base, bar, l2_evict_first_policy());
-                    }
-                }
-                // 4-bit V: one box of the chunk's D/2-byte rows (64 or 128 bytes wide)
-                if (VQ4)
-                    tma_load_3d_hint(kdst + Q::kSection, &p.tmap_v, 0, c.g, (int)base, bar, l2_evict_first_policy());
+                load_rows(kdst, c.g, (int)base, bar, l2_evict_first_policy());
                 if (scl_tma) {
                     const uint32_t sdst = smem_addr(sring + st * Q::kSclChunk);
                     tma_load_2d_hint(sdst, &p.tmap_ks, scl_box_x<D>(c.g), (int)base, bar, l2_evict_first_policy());
@@ -2493,7 +2527,7 @@ __device__ __forceinline__ void q8_self_body(const SplitDecodeParams& p) {
         const int rows = GQ * NQ;
         const int64_t HR = (int64_t)NQ * H;  // partial rows per (sequence, split)
         uint32_t qa[D / 16][4];
-        int64_t qa_unit = -1;
+        int64_t qa_key = -1;  // q_key of the rows whose query fragments qa holds
         uint32_t C = 0, X = 0;
         bool stop = false;
         constexpr float kLn2 = 0.69314718055994530942f;
@@ -2514,7 +2548,10 @@ __device__ __forceinline__ void q8_self_body(const SplitDecodeParams& p) {
                 }
                 continue;
             }
-            if (qa_unit != u) load_q_frags_mq_q8<D, KQ4>(p, x.s, x.g, gq, tq, row0, qa);
+            if (qa_key != q_key(p, x)) {
+                load_q_frags_mq_q8<D, KQ4>(p, x.s, x.g, gq, tq, row0, qa);
+                qa_key = q_key(p, x);
+            }
             float oacc[2][D / 16][4];
 #pragma unroll
             for (int nt = 0; nt < 2; ++nt)
@@ -2581,9 +2618,9 @@ __device__ __forceinline__ void q8_self_body(const SplitDecodeParams& p) {
             const int64_t un = u + gridDim.x;
             if (un < n_units) {
                 const Unit y = unit_at(p, un);
-                if (y.n_tiles > 0) {
+                if (y.n_tiles > 0 && q_key(p, y) != qa_key) {
                     load_q_frags_mq_q8<D, KQ4>(p, y.s, y.g, gq, tq, p.rg_rows * y.rg, qa);
-                    qa_unit = un;
+                    qa_key = q_key(p, y);
                 }
             }
             if constexpr (W > 1) {
@@ -2697,7 +2734,7 @@ __device__ __forceinline__ void q8_self_body(const SplitDecodeParams& p) {
         }
     } else {
         uint32_t qa[D / 16][2];
-        int64_t qa_unit = -1;
+        int64_t qa_key = -1;  // q_key of the rows whose query fragments qa holds
         uint32_t C = 0;  // chunks consumed
         uint32_t X = 0;  // exchanges
         bool stop = false;
@@ -2752,7 +2789,10 @@ __device__ __forceinline__ void q8_self_body(const SplitDecodeParams& p) {
                 }
                 continue;
             }
-            if (qa_unit != u) load_q(x);
+            if (qa_key != q_key(p, x)) {
+                load_q(x);
+                qa_key = q_key(p, x);
+            }
             // MQ8: causal limit (logical position, exclusive) of the lane's row 8 rg + gq
             const int64_t lim_row = MQ8 ? x.len - p.n_q + 1 + (8 * x.rg + gq) / p.group : 0;
             float oacc[D / 16][4];
@@ -2821,18 +2861,22 @@ __device__ __forceinline__ void q8_self_body(const SplitDecodeParams& p) {
             const int64_t un = u + gridDim.x;
             if (un < n_units) {
                 const Unit y = unit_at(p, un);
-                if (y.n_tiles > 0) {
+                if (y.n_tiles > 0 && q_key(p, y) != qa_key) {
                     load_q(y);
-                    qa_unit = un;
+                    qa_key = q_key(p, y);
                 }
             }
             if constexpr (W > 1) {
-                if (warp > 0) {
+                // the warp that combines and writes the unit rotates with the exchange count,
+                // so that every warp takes its share of that work; the others post their
+                // (max, sum, O) to slots 0 .. W-2 in turn after it
+                const int comb = (int)(X % (uint32_t)W);
+                if (warp != comb) {
                     if (X > 0) {
                         const bool ok = mbar_wait_bounded(smem_addr(&xchg_bar[1]), (X - 1) & 1u, abort_flag, p.wait_limit_ns);
                         if (!__all_sync(0xffffffffu, ok)) break;
                     }
-                    unsigned char* slot = xchg + (warp - 1) * Q::kXchgSlot;
+                    unsigned char* slot = xchg + ((warp - comb - 1 + W) % W) * Q::kXchgSlot;
                     float4* xo = reinterpret_cast<float4*>(slot);
                     float* xm = reinterpret_cast<float*>(xo + (D / 16) * 32);
                     if (tq == 0) {
@@ -2850,7 +2894,8 @@ __device__ __forceinline__ void q8_self_body(const SplitDecodeParams& p) {
                 const bool ok = mbar_wait_bounded(smem_addr(&xchg_bar[0]), X & 1u, abort_flag, p.wait_limit_ns);
                 if (!__all_sync(0xffffffffu, ok)) break;
             }
-            // warp 0: combine the W warps' (max, sum, O) for rows 2tq, 2tq+1 and write the partial
+            // the combining warp: merge the W warps' (max, sum, O) for rows 2tq, 2tq+1 and write
+            // the partial
             float mw[W][2], lw[W][2];
 #pragma unroll
             for (int e = 0; e < 2; ++e) {

@@ -105,8 +105,10 @@ bool encode_scale_tensor_map(CUtensorMap* map, const void* base, int64_t cells, 
                              int box_cells);
 // Fill a 3-D tensor map {row elements, n_head_kv, cells} over a cell-major cache with
 // boxes of the kernel's cells x 128 bytes (a whole 64- or 128-byte row for 4-bit V rows,
-// v_side with KVATTN_KV_Q8_0_Q4_0) and the 128-byte swizzle.  Returns false if the
-// driver's encoder is unavailable or rejects the geometry (the caller then loads per cell).
+// v_side with KVATTN_KV_Q8_0_Q4_0) and the 128-byte swizzle; for 8-bit rows of 256 bytes
+// a 4-D map {128 bytes, cells, plane, n_head_kv} whose box {128, the kernel's cells, 2, 1}
+// brings both planes at once.  Returns false if the driver's encoder is unavailable or
+// rejects the geometry (the caller then loads per cell).
 bool encode_kv_tensor_map(CUtensorMap* map, const void* base, int kv_type, int64_t cells,
                           int n_head_kv, int head_dim, bool v_side);
 
