@@ -586,6 +586,15 @@ int decode_impl(const void* q, const void* k_cache, const void* v_cache, const v
         p.pair = pair ? 1 : 0;
         p.n_head_kv = k_hkv;
         p.group = (n_head / n_head_kv) * (pair ? 2 : 1);
+        // Quantised head_dim-256 kernels (and KV-head pairs) whose units overflow one wave of
+        // the two-warp CTAs but fit one wave of the one-warp ones: a unit per warp, eight CTAs
+        // per SM, no end-of-unit exchange (KVATTN_ONE_WARP=0 keeps two warps per CTA)
+        if (!multi && kv_type != KVATTN_KV_F16 && k_hd == 256 && env_int("KVATTN_ONE_WARP", 1) != 0) {
+            const int64_t units = (int64_t)n_seq * n_split * k_hkv;
+            const int64_t two = (int64_t)std::max(occupancy(kv_type, 256, 2, 0), 1) * sm_count();
+            const int64_t one = (int64_t)std::max(occupancy(kv_type, 256, 2, 4), 1) * sm_count();
+            if (units > two && units <= one) p.mq = 4;
+        }
         p.n_stages = p.mq == 5 ? 4 : pick_stages(kv_type, k_hd, n_split * k_hkv * n_rg * n_seq, p.mq == 2 ? 0 : p.mq);
         p.scale_log2 = (float)((double)scale * 1.4426950408889634074);
         apply_debug_hooks(p);
@@ -600,12 +609,13 @@ int decode_impl(const void* q, const void* k_cache, const void* v_cache, const v
                 (int64_t)std::max(p.mq == 5 ? tc_blocks : occupancy(kv_type, k_hd, p.n_stages, p.mq == 2 ? 0 : p.mq), 1) *
                 sm_count();
             log_line("%s kv_type=%d n_seq=%d n_q=%d n_head=%d/%d head_dim=%d max_len=%lld split=%d n_split=%lld "
-                     "plan=%d descriptors=%s units=%lld grid=%lld stages=%d tma=%d scale_tma=%d head_pairs=%d merge=%d",
+                     "plan=%d descriptors=%s units=%lld grid=%lld stages=%d tma=%d scale_tma=%d head_pairs=%d merge=%d "
+                     "mode=%d",
                      multi ? "decode_multi" : (merge ? "decode" : "decode_partials"), kv_type, n_seq, n_q, n_head,
                      n_head_kv, head_dim, (long long)max_len, split, (long long)n_split, cell_plan != nullptr,
                      cell_plan == nullptr ? "none" : (desc_out != nullptr ? "in-kernel" : "kernel"),
                      (long long)units, (long long)std::min(units, resident), p.n_stages, p.use_tma, p.scl_tma, p.pair,
-                     merge ? 1 : 0);
+                     merge ? 1 : 0, p.mq);
         }
     }
     if (!merge) return KVATTN_OK;

@@ -2998,6 +2998,14 @@ __device__ __forceinline__ void q8_self_body(const SplitDecodeParams& p) {
 // four CTAs (eight computing warps, no spills; measured faster than four warps x two CTAs).
 constexpr int kQ8W128 = 4, kQ8S128 = 2, kQ8B128 = 4;
 constexpr int kQ8W256 = 2, kQ8S256 = 2, kQ8B256 = 4;
+// One-warp CTAs for the head_dim-256 single-query kernels (real head_dim 256 and KV-head
+// pairs), eight per SM with the same 255 registers: a unit per warp, no end-of-unit exchange.
+// Taken when a call's units overflow one wave of the two-warp CTAs but fit one wave of these
+// (Q8_0 over 131072 cells, head_dim 128 as 1024 KV-head-pair units: 62.9 -> 59.7 us per op;
+// Q8_0 + Q4_0 60.3 -> 56.8, Q4_0 59.6 -> 56.0); with more units the two-warp kernels measured
+// better (Q8_0 head_dim 256, 2048 units: 108.9 against 114.1 us), and a third stage gained
+// nothing (60.4 us).
+constexpr int kQ8S256One = 2, kQ8B256One = 8;
 // Q8_0 multi-query (head_dim 128, up to 16 query rows): two warps of up to 255 registers,
 // four CTAs per SM -- the two output tiles and the 16-row query fragments do not fit the
 // single-query kernel's 128 registers.
@@ -3095,10 +3103,28 @@ __global__ void __launch_bounds__(kQ8W256 * 32, kQ8B256)
     q8_self_body<256, kQ8W256, kQ8S256, true, true>(p);
 }
 
+// One-warp head_dim-256 single-query kernels (mode 4).
+__global__ void __launch_bounds__(32, kQ8B256One) split_decode_q8_d256_w1(const __grid_constant__ SplitDecodeParams p) {
+    q8_self_body<256, 1, kQ8S256One>(p);
+}
+__global__ void __launch_bounds__(32, kQ8B256One)
+    split_decode_q8q4_d256_w1(const __grid_constant__ SplitDecodeParams p) {
+    q8_self_body<256, 1, kQ8S256One, true>(p);
+}
+__global__ void __launch_bounds__(32, kQ8B256One) split_decode_q4_d256_w1(const __grid_constant__ SplitDecodeParams p) {
+    q8_self_body<256, 1, kQ8S256One, true, true>(p);
+}
+
 // mode: 0 single-query, 1 multi-query, 2 f16 multi-query of up to 8 rows per unit on the
-// single-query geometry (same resources as mode 0).
+// single-query geometry (same resources as mode 0), 3 the three-consumer f16 multi-query
+// kernel, 4 the one-warp quantised head_dim-256 single-query kernels.
 const void* kernel_for(int kv_type, int head_dim, int mode = 0) {
     if (mode == 3) return reinterpret_cast<const void*>(split_decode_mq3_f16_d128);
+    if (mode == 4) {
+        if (kv_type == KVATTN_KV_Q8_0_Q4_0) return reinterpret_cast<const void*>(split_decode_q8q4_d256_w1);
+        if (kv_type == KVATTN_KV_Q4_0) return reinterpret_cast<const void*>(split_decode_q4_d256_w1);
+        return reinterpret_cast<const void*>(split_decode_q8_d256_w1);
+    }
     if (mode == 2) {
         if (kv_type == KVATTN_KV_Q8_0) return reinterpret_cast<const void*>(split_decode_mq8_q8_d128);
         if (kv_type == KVATTN_KV_Q8_0_Q4_0) return reinterpret_cast<const void*>(split_decode_mq8_q8q4_d128);
@@ -3154,6 +3180,11 @@ int split_decode_smem_bytes(int kv_type, int head_dim, int n_stages, int mode) {
     // (the head_dim-256 multi-query kernels run on the single-query geometry)
     const bool mq = mode == 1 || mode == 3;
     const bool mq128 = mq && head_dim == 128;
+    if (mode == 4) {
+        if (kv_type == KVATTN_KV_Q8_0_Q4_0) return q8_self_smem<256, 1, kQ8S256One, true>();
+        if (kv_type == KVATTN_KV_Q4_0) return q8_self_smem<256, 1, kQ8S256One, true, true>();
+        return q8_self_smem<256, 1, kQ8S256One>();
+    }
     if (kv_type == KVATTN_KV_Q8_0 && mq128) return q8_self_smem<128, kQ8WMQ, kQ8SMQ, false, false, true>();
     if (kv_type == KVATTN_KV_Q8_0_Q4_0 && mq128) return q8_self_smem<128, kQ8WMQ, kQ8SMQ, true, false, true>();
     if (kv_type == KVATTN_KV_Q4_0 && mq128) return q8_self_smem<128, kQ8WMQ, kQ8SMQ, true, true, true>();
@@ -3174,6 +3205,7 @@ int split_decode_smem_bytes(int kv_type, int head_dim, int n_stages, int mode) {
 int split_decode_block_threads(int kv_type, int head_dim, int mode) {
     const bool mq = mode == 1;
     if (mode == 3) return 4 * 32;
+    if (mode == 4) return 32;
     if (kv_type != KVATTN_KV_F16 && mq && head_dim == 128) return kQ8WMQ * 32;
     if (kv_type != KVATTN_KV_F16) return (head_dim == 128 ? kQ8W128 : kQ8W256) * 32;
     return kThreads;

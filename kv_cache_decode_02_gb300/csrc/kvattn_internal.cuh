@@ -71,7 +71,9 @@ struct SplitDecodeParams {
     int n_seq, n_head, n_head_kv, group, split;
     int n_q;                  // query tokens per sequence (multi-query decode; 1 otherwise)
     int mq;                   // 1: the multi-query kernels; 2: f16 multi-query units of up to 8
-                              // rows on the single-query kernels (single-query resources)
+                              // rows on the single-query kernels (single-query resources); 3:
+                              // the three-consumer f16 multi-query kernel; 4: the one-warp
+                              // quantised head_dim-256 single-query kernels; 5: the tcgen05 kernel
     int n_rg;                 // multi-query row groups per KV head (0 or 1: one group holding
                               // every row); the units become (sequence, split, KV head, row
                               // group), row group fastest, so the groups of one split run side
@@ -140,8 +142,9 @@ cudaError_t launch_merge(const MergeParams& p, cudaStream_t stream, bool pdl);
 cudaError_t launch_tile_copy(const void* k_src, const void* v_src, void* k_dst, void* v_dst, size_t bytes,
                              cudaStream_t stream);
 int split_decode_stage_bytes(int kv_type, int head_dim);
-// mode: 0 single-query, 1 multi-query kernels, 3 the three-consumer multi-query kernel (the
-// multi-query units of up to 8 rows, mode 2, use the single-query resources)
+// mode: 0 single-query, 1 multi-query kernels, 3 the three-consumer multi-query kernel, 4 the
+// one-warp quantised head_dim-256 single-query kernels (the multi-query units of up to 8
+// rows, mode 2, use the single-query resources)
 int split_decode_smem_bytes(int kv_type, int head_dim, int n_stages, int mode = 0);
 int split_decode_block_threads(int kv_type, int head_dim, int mode = 0);
 int split_decode_box_cells(int kv_type);

@@ -149,6 +149,10 @@ SINGLE = [
     ("q8", 128, 4, [1100, 17, 0], 128),
     ("q8q4", 128, 3, [515, 64], 64),
     ("q4", 128, 2, [2049, 3], 512),
+    # more units than one wave of two-warp CTAs: one-warp CTAs, a unit per warp (782 KV-head
+    # pair units; 628 units of head_dim 256)
+    ("q8", 128, 4, [100000], 128),
+    ("q4", 256, 6, [20000, 333], 128),
     # 125 parts a row at head_dim 128: each row's merge spread over several CTAs
     ("f16", 128, 4, [4000, 1000, 0], 32),
     ("q8", 128, 4, [4000, 77], 32),
